@@ -1,0 +1,247 @@
+"""fp64 CPU oracle for fused CSR edge attention (Graph Transformer and GATv2).
+
+TEST INFRASTRUCTURE ONLY: the library never imports this package.  The tests,
+the package smoke check and the benchmark's CPU-baseline leg are its only
+callers.  It shares no code with the CUDA path.
+
+The arithmetic lives in ``oracle.c`` (plain C, doubles, explicit edge loops,
+dense softmax per row); this module compiles it with gcc on first use and
+wraps it with ctypes.  The row partition below is host logic written from its
+definition in plain Python.
+
+Every function follows the definitions on "On Efficient Scaling of GNNs via
+IO-Aware Layers Implementations" (abstract; Yandex Research blog post,
+"Attention-based layers" paragraph) and the Graph Transformer / GATv2 score
+functions the pages cite; ``oracle.c`` states each reading in its header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_I32P = np.ctypeslib.ndpointer(dtype=np.int32, flags="C_CONTIGUOUS")
+_I64P = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_F64P = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_i64, _int, _dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (gcc, OpenMP, no FP contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        sig = {
+            "oracle_threads": ([], _int),
+            "oracle_set_threads": ([_int], None),
+            "oracle_transpose": ([_i64, _I32P, _I32P, _I32P, _I32P], _int),
+            "oracle_gt_fwd_rows": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P,
+                                    _i64, _I64P, _F64P, _F64P], _int),
+            "oracle_gt_fwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P,
+                               _F64P, _F64P], _int),
+            "oracle_gt_bwd_dq_rows": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P,
+                                       _F64P, _i64, _I64P, _F64P], _int),
+            "oracle_gt_bwd_dkdv_srcs": ([_i64, _I32P, _I32P, _I32P, _I32P, _int, _int, _F64P,
+                                         _F64P, _F64P, _F64P, _i64, _I64P, _F64P, _F64P], _int),
+            "oracle_gt_bwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P, _F64P,
+                               _F64P, _F64P, _F64P], _int),
+            "oracle_matmul": ([_i64, _int, _int, _F64P, _F64P, _F64P], _int),
+            "oracle_gatv2_fwd_rows": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P,
+                                       _dbl, _i64, _I64P, _F64P, _F64P], _int),
+            "oracle_gatv2_fwd": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P, _F64P,
+                                  _F64P, _dbl, _F64P, _F64P, _F64P, _F64P], _int),
+            "oracle_gatv2_bwd": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P, _F64P,
+                                  _F64P, _dbl, _F64P, _F64P, _F64P, _F64P, _F64P, _F64P,
+                                  _F64P], _int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _f64(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _i32(x) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _check(rc: int, name: str):
+    if rc != 0:
+        raise MemoryError(f"oracle {name} failed ({rc})")
+
+
+def threads() -> int:
+    """OpenMP threads the oracle uses."""
+    return _load().oracle_threads()
+
+
+def set_threads(n: int) -> None:
+    _load().oracle_set_threads(int(n))
+
+
+# ---------------------------------------------------------------- graph steps
+
+def transpose(indptr, indices):
+    """Transposed CSR (t_indptr[N+1], t_dst[E]): destinations of each source,
+    ascending.  Counting sort in C."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    N = len(indptr) - 1
+    t_indptr = np.zeros(N + 1, np.int32)
+    t_dst = np.zeros(max(int(indptr[-1]), 1), np.int32)
+    _check(_load().oracle_transpose(N, indptr, indices, t_indptr, t_dst), "transpose")
+    return t_indptr, t_dst[: int(indptr[-1])]
+
+
+def partition(indptr, threshold: int, chunk: int):
+    """Row partition by its definition: rows of degree > ``threshold`` are
+    split rows (ascending id); each is cut into consecutive edge chunks of
+    ``chunk`` edges (the last one shorter).  Returns int32 arrays
+    split_rows[S], chunk_ptr[S+1] (chunk range per split row), chunk_row[C],
+    chunk_beg[C], chunk_end[C]."""
+    indptr = np.asarray(indptr, dtype=np.int64)
+    split_rows, chunk_ptr, crow, cbeg, cend = [], [0], [], [], []
+    for i in range(len(indptr) - 1):
+        b, e = int(indptr[i]), int(indptr[i + 1])
+        if e - b <= threshold:
+            continue
+        split_rows.append(i)
+        x = b
+        while x < e:
+            crow.append(i)
+            cbeg.append(x)
+            cend.append(min(x + chunk, e))
+            x += chunk
+        chunk_ptr.append(len(crow))
+    as32 = lambda v: np.asarray(v, dtype=np.int32)
+    return {"split_rows": as32(split_rows), "chunk_ptr": as32(chunk_ptr),
+            "chunk_row": as32(crow), "chunk_beg": as32(cbeg), "chunk_end": as32(cend)}
+
+
+# ---------------------------------------------------------- Graph Transformer
+
+def gt_fwd(indptr, indices, Q, K, V, rows=None):
+    """out [R, H, D], lse [R, H] for the listed rows (all rows if None)."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    N, H, D = Q.shape
+    lib = _load()
+    if rows is None:
+        out = np.empty((N, H, D)); lse = np.empty((N, H))
+        _check(lib.oracle_gt_fwd(N, indptr, indices, H, D, Q, K, V, out, lse), "gt_fwd")
+        return out, lse
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), H, D)); lse = np.empty((len(rows), H))
+    _check(lib.oracle_gt_fwd_rows(N, indptr, indices, H, D, Q, K, V, len(rows), rows, out, lse),
+           "gt_fwd_rows")
+    return out, lse
+
+
+def gt_bwd(indptr, indices, Q, K, V, dO):
+    """(dQ, dK, dV), each [N, H, D], by the softmax Jacobian."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    N, H, D = Q.shape
+    dQ, dK, dV = np.empty_like(Q), np.empty_like(Q), np.empty_like(Q)
+    _check(_load().oracle_gt_bwd(N, indptr, indices, H, D, Q, K, V, dO, dQ, dK, dV), "gt_bwd")
+    return dQ, dK, dV
+
+
+def gt_bwd_dq_rows(indptr, indices, Q, K, V, dO, rows):
+    indptr, indices = _i32(indptr), _i32(indices)
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    N, H, D = Q.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    dq = np.empty((len(rows), H, D))
+    _check(_load().oracle_gt_bwd_dq_rows(N, indptr, indices, H, D, Q, K, V, dO, len(rows), rows, dq),
+           "gt_bwd_dq_rows")
+    return dq
+
+
+def gt_bwd_dkdv_srcs(indptr, indices, Q, K, V, dO, srcs, transposed=None):
+    indptr, indices = _i32(indptr), _i32(indices)
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    N, H, D = Q.shape
+    t_indptr, t_dst = transposed if transposed is not None else transpose(indptr, indices)
+    t_dst = _i32(t_dst) if len(t_dst) else np.zeros(1, np.int32)
+    srcs = np.ascontiguousarray(srcs, dtype=np.int64)
+    dk = np.empty((len(srcs), H, D)); dv = np.empty((len(srcs), H, D))
+    _check(_load().oracle_gt_bwd_dkdv_srcs(N, indptr, indices, _i32(t_indptr), t_dst, H, D,
+                                           Q, K, V, dO, len(srcs), srcs, dk, dv),
+           "gt_bwd_dkdv_srcs")
+    return dk, dv
+
+
+# ---------------------------------------------------------------------- GATv2
+
+def matmul(X, W):
+    X, W = _f64(X), _f64(W)
+    Y = np.empty((X.shape[0], W.shape[1]))
+    _load().oracle_matmul(X.shape[0], X.shape[1], W.shape[1], X, W, Y)
+    return Y
+
+
+def gatv2_fwd(indptr, indices, X, Wl, Wr, a, slope=0.2):
+    """(FL, FR, out, lse): projections [N, H, D], output [N, H, D], lse [N, H]."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    X, Wl, Wr, a = _f64(X), _f64(Wl), _f64(Wr), _f64(a)
+    N, F = X.shape
+    H, D = a.shape
+    FL = np.empty((N, H, D)); FR = np.empty((N, H, D))
+    out = np.empty((N, H, D)); lse = np.empty((N, H))
+    _check(_load().oracle_gatv2_fwd(N, F, H, D, indptr, indices, X, Wl, Wr, a, float(slope),
+                                    FL, FR, out, lse), "gatv2_fwd")
+    return FL, FR, out, lse
+
+
+def gatv2_fwd_rows(indptr, indices, FL, FR, a, rows, slope=0.2):
+    indptr, indices = _i32(indptr), _i32(indices)
+    FL, FR, a = _f64(FL), _f64(FR), _f64(a)
+    N, H, D = FL.shape
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), H, D)); lse = np.empty((len(rows), H))
+    _check(_load().oracle_gatv2_fwd_rows(N, indptr, indices, H, D, FL, FR, a, float(slope),
+                                         len(rows), rows, out, lse), "gatv2_fwd_rows")
+    return out, lse
+
+
+def gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, slope=0.2):
+    """dict with dX [N, F], dW_l, dW_r [F, H*D], da [H, D], dFL, dFR [N, H, D]."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    X, Wl, Wr, a, dO = _f64(X), _f64(Wl), _f64(Wr), _f64(a), _f64(dO)
+    N, F = X.shape
+    H, D = a.shape
+    dX = np.empty((N, F)); dWl = np.empty((F, H * D)); dWr = np.empty((F, H * D))
+    da = np.empty((H, D)); dFL = np.empty((N, H, D)); dFR = np.empty((N, H, D))
+    _check(_load().oracle_gatv2_bwd(N, F, H, D, indptr, indices, X, Wl, Wr, a, float(slope), dO,
+                                    dX, dWl, dWr, da, dFL, dFR), "gatv2_bwd")
+    return {"dX": dX, "dW_l": dWl, "dW_r": dWr, "da": da, "dFL": dFL, "dFR": dFR}

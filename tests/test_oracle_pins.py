@@ -1,0 +1,345 @@
+"""Pins for the fp64 oracle: hand-worked examples, closed forms, library
+special cases (dense masked attention, scaled_dot_product_attention, torch
+autograd), finite differences and invariants.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def rand_graph(rng, N, p, self_loops=True, dups=False):
+    """Small random destination-sorted CSR (sources ascending)."""
+    rows = []
+    for i in range(N):
+        src = [j for j in range(N) if (rng.random() < p) or (self_loops and j == i)]
+        if dups and src and rng.random() < 0.3:
+            src = sorted(src + [src[rng.integers(len(src))]])
+        rows.append(src)
+    indptr = np.zeros(N + 1, np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in rows])
+    indices = np.array([j for r in rows for j in r], np.int32)
+    return indptr, indices
+
+
+def dense_mask(indptr, indices, N):
+    m = torch.zeros(N, N, dtype=torch.bool)
+    for i in range(N):
+        for e in range(indptr[i], indptr[i + 1]):
+            m[i, indices[e]] = True
+    return m
+
+
+def dense_gt(Q, K, V, mask):
+    """Brute-force dense masked attention in torch fp64: [N,H,D] tensors."""
+    N, H, D = Q.shape
+    s = torch.einsum("ihd,jhd->hij", Q, K) / math.sqrt(D)
+    s = s.masked_fill(~mask[None], float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)                      # [H, N]
+    p = torch.exp(s - lse[..., None]).nan_to_num(0.0)      # empty rows -> 0
+    out = torch.einsum("hij,jhd->ihd", p, V)
+    return out, lse.T
+
+
+def dense_gatv2(X, Wl, Wr, a, mask, slope=0.2):
+    N = X.shape[0]
+    H, D = a.shape
+    FL = (X @ Wl).reshape(N, H, D)
+    FR = (X @ Wr).reshape(N, H, D)
+    z = FL[:, None] + FR[None, :]                          # [i, j, H, D]
+    e = (torch.nn.functional.leaky_relu(z, slope) * a).sum(-1).permute(2, 0, 1)  # [H, i, j]
+    e = e.masked_fill(~mask[None], float("-inf"))
+    lse = torch.logsumexp(e, dim=-1)
+    p = torch.exp(e - lse[..., None]).nan_to_num(0.0)
+    out = torch.einsum("hij,jhd->ihd", p, FR)
+    return out, lse.T
+
+
+# ------------------------------------------------------------ hand examples
+
+def test_gt_hand_example():
+    g = load("gt_hand.json")
+    q = np.array(g["q"]).reshape(2, 1, 1)
+    k = np.array(g["k"]).reshape(2, 1, 1)
+    v = np.array(g["v"]).reshape(2, 1, 1)
+    out, lse = oracle.gt_fwd(g["indptr"], g["indices"], q, k, v)
+    assert out[:, 0, 0] == pytest.approx(g["expected_out"], abs=1e-14)
+    assert lse[0, 0] == pytest.approx(math.log(4.0), abs=1e-14)
+    assert lse[1, 0] == pytest.approx(2.0 * math.log(3.0), abs=1e-14)
+
+
+def test_gatv2_hand_example():
+    g = load("gatv2_hand.json")
+    X = np.array(g["x"]).reshape(3, 1)
+    FL, FR, out, lse = oracle.gatv2_fwd(g["indptr"], g["indices"], X, g["W_l"], g["W_r"], g["a"],
+                                        g["slope"])
+    e1, e2 = g["expected_scores_row0"]
+    w1 = math.exp(e1) / (math.exp(e1) + math.exp(e2))
+    w2 = 1.0 - w1
+    assert out[0, 0, 0] == pytest.approx(-2.0 * w1 + 1.0 * w2, abs=1e-14)
+    assert lse[0, 0] == pytest.approx(math.log(math.exp(-0.2) + math.exp(2.0)), abs=1e-14)
+    assert np.all(out[1:] == 0.0)
+    assert np.all(np.isneginf(lse[1:]))
+
+
+def test_five_node_closed_forms():
+    """Empty row, degree-1 row, zero query (uniform weights), identical keys."""
+    rng = np.random.default_rng(11)
+    H, D = 2, 4
+    indptr = np.array([0, 3, 3, 4, 6, 8], np.int32)
+    indices = np.array([1, 2, 3, 4, 0, 3, 2, 4], np.int32)
+    Q = rng.standard_normal((5, H, D)); K = rng.standard_normal((5, H, D))
+    V = rng.standard_normal((5, H, D))
+    Q[0] = 0.0                      # row 0: uniform weights over {1,2,3}
+    K[3] = K[0]                     # row 3: identical keys for {0,3}
+    out, lse = oracle.gt_fwd(indptr, indices, Q, K, V)
+    np.testing.assert_allclose(out[0], V[[1, 2, 3]].mean(0), atol=1e-14)
+    np.testing.assert_allclose(lse[0], math.log(3.0), atol=1e-14)
+    assert np.all(out[1] == 0.0) and np.all(np.isneginf(lse[1]))
+    np.testing.assert_allclose(out[2], V[4], atol=1e-14)
+    np.testing.assert_allclose(lse[2], (Q[2] * K[4]).sum(-1) / math.sqrt(D), atol=1e-14)
+    np.testing.assert_allclose(out[3], V[[0, 3]].mean(0), atol=1e-14)
+    np.testing.assert_allclose(lse[3], (Q[3] * K[0]).sum(-1) / math.sqrt(D) + math.log(2.0),
+                               atol=1e-13)
+    m = dense_mask(indptr, indices, 5)
+    o_ref, l_ref = dense_gt(*(torch.from_numpy(x) for x in (Q, K, V)), m)
+    np.testing.assert_allclose(out[4], o_ref[4].numpy(), atol=1e-13)
+
+
+def test_gatv2_zero_attention_vector_gives_mean():
+    rng = np.random.default_rng(5)
+    N, F, H, D = 20, 6, 2, 3
+    indptr, indices = rand_graph(rng, N, 0.3)
+    X = rng.standard_normal((N, F)); Wl = rng.standard_normal((F, H * D))
+    Wr = rng.standard_normal((F, H * D)); a = np.zeros((H, D))
+    FL, FR, out, lse = oracle.gatv2_fwd(indptr, indices, X, Wl, Wr, a)
+    for i in range(N):
+        nb = indices[indptr[i]:indptr[i + 1]]
+        np.testing.assert_allclose(out[i], FR[nb].mean(0), atol=1e-13)
+        np.testing.assert_allclose(lse[i], math.log(len(nb)), atol=1e-13)
+
+
+# ------------------------------------------------------ library special cases
+
+def test_gt_complete_graph_equals_sdpa():
+    rng = np.random.default_rng(1)
+    N, H, D = 12, 3, 8
+    indptr = np.arange(0, N * N + 1, N, dtype=np.int32)
+    indices = np.tile(np.arange(N, dtype=np.int32), N)
+    Q, K, V = (rng.standard_normal((N, H, D)) for _ in range(3))
+    out, _ = oracle.gt_fwd(indptr, indices, Q, K, V)
+    t = lambda x: torch.from_numpy(x).permute(1, 0, 2)[None]  # [1, H, N, D]
+    ref = torch.nn.functional.scaled_dot_product_attention(t(Q), t(K), t(V))
+    np.testing.assert_allclose(out, ref[0].permute(1, 0, 2).numpy(), atol=1e-13)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_gt_matches_dense_masked(seed):
+    rng = np.random.default_rng(100 + seed)
+    N, H, D = 40, 2, 8
+    indptr, indices = rand_graph(rng, N, 0.15, self_loops=(seed != 2))
+    Q, K, V = (rng.standard_normal((N, H, D)) for _ in range(3))
+    out, lse = oracle.gt_fwd(indptr, indices, Q, K, V)
+    o_ref, l_ref = dense_gt(*(torch.from_numpy(x) for x in (Q, K, V)),
+                            dense_mask(indptr, indices, N))
+    np.testing.assert_allclose(out, o_ref.numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, l_ref.numpy(), atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_gatv2_matches_dense_masked(seed):
+    rng = np.random.default_rng(200 + seed)
+    N, F, H, D = 30, 5, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.2, self_loops=(seed == 0))
+    X = rng.standard_normal((N, F)); Wl = rng.standard_normal((F, H * D))
+    Wr = rng.standard_normal((F, H * D)); a = rng.standard_normal((H, D))
+    FL, FR, out, lse = oracle.gatv2_fwd(indptr, indices, X, Wl, Wr, a, 0.2)
+    t = torch.from_numpy
+    o_ref, l_ref = dense_gatv2(t(X), t(Wl), t(Wr), t(a), dense_mask(indptr, indices, N))
+    np.testing.assert_allclose(FL.reshape(N, -1), X @ Wl, atol=1e-12)
+    np.testing.assert_allclose(out, o_ref.numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, l_ref.numpy(), atol=1e-12)
+
+
+def test_gt_backward_matches_autograd():
+    rng = np.random.default_rng(7)
+    N, H, D = 36, 2, 8
+    indptr, indices = rand_graph(rng, N, 0.2)
+    indptr2, indices2 = indptr.copy(), indices.copy()
+    indptr2[:] = indptr;
+    Q, K, V, dO = (rng.standard_normal((N, H, D)) for _ in range(4))
+    # an empty row must contribute nothing
+    row = 5
+    b, e = indptr[row], indptr[row + 1]
+    indices2 = np.concatenate([indices[:b], indices[e:]]).astype(np.int32)
+    indptr2[row + 1:] -= (e - b)
+    dQ, dK, dV = oracle.gt_bwd(indptr2, indices2, Q, K, V, dO)
+    tq, tk, tv = (torch.from_numpy(x).requires_grad_() for x in (Q, K, V))
+    out, _ = dense_gt(tq, tk, tv, dense_mask(indptr2, indices2, N))
+    (out * torch.from_numpy(dO)).sum().backward()
+    np.testing.assert_allclose(dQ, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dK, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dV, tv.grad.numpy(), atol=1e-12)
+    assert np.all(dQ[row] == 0.0)
+
+
+def test_gatv2_backward_matches_autograd():
+    rng = np.random.default_rng(8)
+    N, F, H, D = 28, 6, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.25)
+    X = rng.standard_normal((N, F)); Wl = rng.standard_normal((F, H * D)) * 0.5
+    Wr = rng.standard_normal((F, H * D)) * 0.5; a = rng.standard_normal((H, D))
+    dO = rng.standard_normal((N, H, D))
+    g = oracle.gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, 0.2)
+    tX, tWl, tWr, ta = (torch.from_numpy(x).requires_grad_() for x in (X, Wl, Wr, a))
+    out, _ = dense_gatv2(tX, tWl, tWr, ta, dense_mask(indptr, indices, N))
+    (out * torch.from_numpy(dO)).sum().backward()
+    np.testing.assert_allclose(g["dX"], tX.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(g["dW_l"], tWl.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(g["dW_r"], tWr.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(g["da"], ta.grad.numpy(), atol=1e-11)
+
+
+# -------------------------------------------------------- finite differences
+
+def test_gt_backward_finite_differences():
+    rng = np.random.default_rng(9)
+    N, H, D = 15, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.3, dups=True)
+    Q, K, V, dO = (rng.standard_normal((N, H, D)) for _ in range(4))
+    grads = dict(zip("QKV", oracle.gt_bwd(indptr, indices, Q, K, V, dO)))
+    eps = 1e-6
+    for name in "QKV":
+        for _ in range(6):
+            idx = tuple(rng.integers(s) for s in Q.shape)
+            args = {"Q": Q.copy(), "K": K.copy(), "V": V.copy()}
+            args[name][idx] += eps
+            lp = (oracle.gt_fwd(indptr, indices, args["Q"], args["K"], args["V"])[0] * dO).sum()
+            args[name][idx] -= 2 * eps
+            lm = (oracle.gt_fwd(indptr, indices, args["Q"], args["K"], args["V"])[0] * dO).sum()
+            fd = (lp - lm) / (2 * eps)
+            assert fd == pytest.approx(grads[name][idx], rel=1e-6, abs=1e-8)
+
+
+def test_gatv2_backward_finite_differences():
+    rng = np.random.default_rng(10)
+    N, F, H, D = 12, 4, 2, 3
+    indptr, indices = rand_graph(rng, N, 0.35)
+    args = {"X": rng.standard_normal((N, F)), "Wl": rng.standard_normal((F, H * D)),
+            "Wr": rng.standard_normal((F, H * D)), "a": rng.standard_normal((H, D))}
+    dO = rng.standard_normal((N, H, D))
+    g = oracle.gatv2_bwd(indptr, indices, args["X"], args["Wl"], args["Wr"], args["a"], dO)
+    names = {"X": "dX", "Wl": "dW_l", "Wr": "dW_r", "a": "da"}
+    eps = 1e-6
+
+    def loss(a_):
+        return (oracle.gatv2_fwd(indptr, indices, a_["X"], a_["Wl"], a_["Wr"], a_["a"])[2] * dO).sum()
+
+    for name, gname in names.items():
+        for _ in range(5):
+            idx = tuple(rng.integers(s) for s in args[name].shape)
+            ap = {k: v.copy() for k, v in args.items()}
+            ap[name][idx] += eps
+            am = {k: v.copy() for k, v in args.items()}
+            am[name][idx] -= eps
+            fd = (loss(ap) - loss(am)) / (2 * eps)
+            assert fd == pytest.approx(g[gname][idx], rel=1e-6, abs=1e-8)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_gt_invariants():
+    rng = np.random.default_rng(12)
+    N, H, D = 50, 3, 4
+    indptr, indices = rand_graph(rng, N, 0.12, dups=True)
+    Q, K, V = (rng.standard_normal((N, H, D)) for _ in range(3))
+    out, lse = oracle.gt_fwd(indptr, indices, Q, K, V)
+    # weights sum to one: V = 1 gives out = 1
+    ones, _ = oracle.gt_fwd(indptr, indices, Q, K, np.ones_like(V))
+    np.testing.assert_allclose(ones, 1.0, atol=1e-14)
+    # convex combination: within the neighbours' range; lse bounds
+    for i in range(N):
+        nb = indices[indptr[i]:indptr[i + 1]]
+        assert np.all(out[i] <= V[nb].max(0) + 1e-12) and np.all(out[i] >= V[nb].min(0) - 1e-12)
+        s = np.einsum("hd,jhd->jh", Q[i], K[nb]) / math.sqrt(D)
+        assert np.all(lse[i] >= s.max(0) - 1e-12)
+        assert np.all(lse[i] <= s.max(0) + math.log(len(nb)) + 1e-12)
+    # permuting each row's neighbour order changes nothing
+    perm = indices.copy()
+    for i in range(N):
+        perm[indptr[i]:indptr[i + 1]] = rng.permutation(perm[indptr[i]:indptr[i + 1]])
+    out_p, lse_p = oracle.gt_fwd(indptr, perm, Q, K, V)
+    np.testing.assert_allclose(out_p, out, atol=1e-13)
+    np.testing.assert_allclose(lse_p, lse, atol=1e-13)
+    # relabelling nodes is equivariant
+    pi = rng.permutation(N)                      # new id of old node
+    inv = np.argsort(pi)
+    rows = [sorted(pi[indices[indptr[inv[n]]:indptr[inv[n] + 1]]]) for n in range(N)]
+    indptr_r = np.zeros(N + 1, np.int32)
+    indptr_r[1:] = np.cumsum([len(r) for r in rows])
+    indices_r = np.array([j for r in rows for j in r], np.int32)
+    out_r, lse_r = oracle.gt_fwd(indptr_r, indices_r, Q[inv], K[inv], V[inv])
+    np.testing.assert_allclose(out_r, out[inv], atol=1e-13)
+    np.testing.assert_allclose(lse_r, lse[inv], atol=1e-13)
+
+
+def test_sampled_entry_points_match_full():
+    rng = np.random.default_rng(13)
+    N, H, D = 45, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.15, dups=True)
+    Q, K, V, dO = (rng.standard_normal((N, H, D)) for _ in range(4))
+    out, lse = oracle.gt_fwd(indptr, indices, Q, K, V)
+    dQ, dK, dV = oracle.gt_bwd(indptr, indices, Q, K, V, dO)
+    rows = np.array([0, 7, 7, 44, 13])
+    o, l = oracle.gt_fwd(indptr, indices, Q, K, V, rows=rows)
+    np.testing.assert_array_equal(o, out[rows]); np.testing.assert_array_equal(l, lse[rows])
+    np.testing.assert_allclose(oracle.gt_bwd_dq_rows(indptr, indices, Q, K, V, dO, rows), dQ[rows],
+                               atol=1e-13)
+    dk, dv = oracle.gt_bwd_dkdv_srcs(indptr, indices, Q, K, V, dO, rows)
+    np.testing.assert_allclose(dk, dK[rows], atol=1e-13)
+    np.testing.assert_allclose(dv, dV[rows], atol=1e-13)
+
+
+# ------------------------------------------------------- graph preprocessing
+
+def test_transpose_matches_scipy_and_roundtrips():
+    sp = pytest.importorskip("scipy.sparse")
+    rng = np.random.default_rng(14)
+    N = 300
+    indptr, indices = rand_graph(rng, N, 0.02)
+    t_indptr, t_dst = oracle.transpose(indptr, indices)
+    A = sp.csr_matrix((np.ones(len(indices)), indices, indptr), shape=(N, N))
+    At = A.T.tocsr()
+    At.sort_indices()
+    np.testing.assert_array_equal(t_indptr, At.indptr)
+    np.testing.assert_array_equal(t_dst, At.indices)
+    back_ptr, back_idx = oracle.transpose(t_indptr, t_dst)
+    np.testing.assert_array_equal(back_ptr, indptr)
+    np.testing.assert_array_equal(back_idx, indices)
+
+
+def test_partition_definition():
+    rng = np.random.default_rng(15)
+    deg = rng.integers(0, 40, 200)
+    deg[[3, 50, 199]] = [300, 97, 1000]
+    indptr = np.concatenate([[0], np.cumsum(deg)]).astype(np.int32)
+    p = oracle.partition(indptr, threshold=64, chunk=32)
+    assert list(p["split_rows"]) == [i for i in range(200) if deg[i] > 64]
+    for s, i in enumerate(p["split_rows"]):
+        c0, c1 = p["chunk_ptr"][s], p["chunk_ptr"][s + 1]
+        assert c1 - c0 == math.ceil(deg[i] / 32)
+        assert p["chunk_beg"][c0] == indptr[i] and p["chunk_end"][c1 - 1] == indptr[i + 1]
+        assert np.all(p["chunk_beg"][c0 + 1:c1] == p["chunk_end"][c0:c1 - 1])
+        assert np.all(p["chunk_end"][c0:c1] - p["chunk_beg"][c0:c1] <= 32)
+        assert np.all(p["chunk_row"][c0:c1] == i)
