@@ -1,0 +1,196 @@
+/*
+ * sga.h -- C ABI of the fused CSR edge-attention library (sm_103a).
+ *
+ * What it computes (the method of "On Efficient Scaling of GNNs via IO-Aware
+ * Layers Implementations", Yandex Research blog post, "Attention-based layers"
+ * paragraph, and the arXiv abstract of the same paper): attention layers of the
+ * Graph Transformer and GATv2 kind over a graph stored as CSR sorted by
+ * destination.  For every destination row the kernels gather the neighbour
+ * rows, score them per head, run an online softmax and accumulate the weighted
+ * values; the E x H edge scores are never written to device memory.  The
+ * backward pass recomputes the weights from the per-row log-sum-exp saved by
+ * the forward pass (the FlashAttention-2 idea the blog post names).  Rows of
+ * very high degree ("super nodes", DF-GNN abstract; "degree-aware tiling" in
+ * the blog post's aggregation paragraph) are cut into chunks whose partial
+ * softmax statistics are merged in a fixed order.
+ *
+ * Conventions shared by every call
+ *  - Graph: indptr[N+1] and indices[E], int32, DEVICE memory.  Row i is the
+ *    destination; indices[indptr[i] .. indptr[i+1]) are its sources j.
+ *    Duplicate entries count as separate edges.  N < 2^31, E < 2^31.
+ *  - Node tensors are [N, H, D] row-major in the call's dtype (one node's heads
+ *    contiguous).  lse is [N, H] float32, natural log; an empty row gives
+ *    out = 0 and lse = -inf.  All tensor pointers are DEVICE pointers aligned
+ *    to 16 bytes; the caller owns every buffer it passes.
+ *  - Supported shapes: D in {32, 64, 128}; H >= 1; H*D <= 1024; GATv2 input
+ *    width F a multiple of 8 with 8 <= F <= 1024.  Anything else returns
+ *    SGA_EUNSUPPORTED.
+ *  - dtype: SGA_F32 or SGA_BF16 for every tensor of a call except lse (always
+ *    float32).  Arithmetic accumulates in float32.
+ *  - Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Every
+ *    compute call is asynchronous on that stream.  sga_plan_create and
+ *    sga_read_device_error synchronise it.
+ *  - Errors: no call throws or aborts; each returns an sga_status.  Argument
+ *    errors are detected on the host before any launch.  SGA_ECUDA means a CUDA
+ *    runtime call failed; sga_last_cuda_error() returns its code.
+ */
+#ifndef SGA_H
+#define SGA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SGA_OK = 0,
+    SGA_EINVAL = 1,         /* bad argument: null pointer, misalignment, plan mismatch, invalid CSR */
+    SGA_EUNSUPPORTED = 2,   /* shape or dtype outside the supported set */
+    SGA_ECUDA = 3,          /* a CUDA runtime call failed */
+    SGA_EWORKSPACE = 4,     /* workspace missing or smaller than sga_plan_workspace_bytes() */
+    SGA_EDEVICE_CHECK = 5   /* a device-side range check fired (see sga_read_device_error) */
+} sga_status;
+
+typedef enum { SGA_F32 = 0, SGA_BF16 = 1 } sga_dtype;
+
+/* Opaque, host-owned plan for one graph and one layer shape. */
+typedef struct sga_plan sga_plan;
+
+/* Plan options.  Zero (or a NULL pointer) selects the default of each field. */
+typedef struct {
+    int32_t split_threshold;  /* rows of degree > this are split (default 256) */
+    int32_t chunk_len;        /* edges per chunk of a split row (default 128) */
+    int32_t in_features;      /* GATv2 input width F; 0 for a Graph Transformer plan */
+    int32_t reserved;         /* must be 0 */
+} sga_plan_opts;
+
+/* Build a plan: validates the CSR on the device (indptr[0] = 0, monotone,
+ * indptr[N] = E, 0 <= indices < N), builds the transposed CSR (sources ->
+ * ascending destinations) and the degree partitions of both.
+ * indptr/indices: device pointers, read only during this call.
+ * The plan owns device memory for the transposed CSR and partitions (freed by
+ * sga_plan_destroy).  Synchronises `stream`.  Returns SGA_EINVAL for an
+ * invalid CSR, leaving *out NULL. */
+sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_t N, int64_t E,
+                           int H, int D, sga_dtype dt, const sga_plan_opts *opts,
+                           void *stream, sga_plan **out);
+
+/* Bytes of device workspace every compute call of this plan needs (may be 0). */
+size_t sga_plan_workspace_bytes(const sga_plan *plan);
+
+/* Attach caller-owned device workspace (256-byte aligned, at least
+ * sga_plan_workspace_bytes()).  Calls that use the same plan must not overlap
+ * on the device: they share this workspace. */
+sga_status sga_plan_set_workspace(sga_plan *plan, void *d_workspace, size_t bytes);
+
+void sga_plan_destroy(sga_plan *plan);
+
+/* Graph Transformer forward: s_ij = q_i . k_j / sqrt(D) per head, softmax over
+ * the row, out_i = sum_j p_ij v_j, lse_i = log sum_j exp(s_ij).
+ * Q, K, V, out: [N, H, D] in dt; lse: [N, H] float32.  The graph arguments must
+ * be the ones the plan was built from. */
+sga_status gt_attn_fwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                       const void *Q, const void *K, const void *V, int64_t N, int64_t E, int H,
+                       int D, sga_dtype dt, void *out, float *lse, void *stream);
+
+/* Graph Transformer backward.  Recomputes p_ij = exp(s_ij - lse_i) and, with
+ * Delta_i = dOut_i . out_i, dS_ij = p_ij (dOut_i . v_j - Delta_i):
+ * dQ_i = sum_j dS_ij k_j / sqrt(D),  dK_j = sum_i dS_ij q_i / sqrt(D),
+ * dV_j = sum_i p_ij dOut_i.  dK/dV walk the transposed CSR, so no atomics are
+ * used and results are bitwise reproducible.  out/lse are the forward's. */
+sga_status gt_attn_bwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                       const void *Q, const void *K, const void *V, const void *out,
+                       const float *lse, const void *dOut, int64_t N, int64_t E, int H, int D,
+                       sga_dtype dt, void *dQ, void *dK, void *dV, void *stream);
+
+/* GATv2 forward: FL = X W_l, FR = X W_r (X [N, F], W [F, H*D], FL/FR written as
+ * [N, H, D] and kept for the backward pass); e_ij = sum_d a[h,d]
+ * LeakyReLU_slope(FL[i,h,d] + FR[j,h,d]); out_i = sum_j softmax_j(e_ij) FR_j;
+ * lse as above.  a: [H, D]. */
+sga_status gatv2_fwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                     const void *X, const void *W_l, const void *W_r, const void *a, int64_t N,
+                     int64_t E, int F, int H, int D, float slope, sga_dtype dt, void *FL,
+                     void *FR, void *out, float *lse, void *stream);
+
+/* GATv2 backward by the chain rule through the softmax, LeakyReLU and both
+ * projections: dX [N, F], dW_l, dW_r [F, H*D], da [H, D] (all in dt).
+ * Reductions over nodes (dW, da) run in a fixed order: reproducible. */
+sga_status gatv2_bwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                     const void *X, const void *W_l, const void *W_r, const void *a,
+                     const void *FL, const void *FR, const void *out, const float *lse,
+                     const void *dOut, int64_t N, int64_t E, int F, int H, int D, float slope,
+                     sga_dtype dt, void *dX, void *dW_l, void *dW_r, void *da, void *stream);
+
+const char *sga_status_string(sga_status s);
+
+/* Last CUDA error code seen by a call that returned SGA_ECUDA (0 if none). */
+int sga_last_cuda_error(void);
+
+/* Device-side range checks: every gathered node id is checked against N before
+ * it is dereferenced; a failing check skips the access and sets a bit in the
+ * plan's device error word.  This call synchronises `stream`, reads the word
+ * into *code, clears it, and returns SGA_EDEVICE_CHECK if it was non-zero. */
+sga_status sga_read_device_error(const sga_plan *plan, void *stream, int32_t *code);
+
+/* ---- plan inspection (tests) -------------------------------------------- */
+
+typedef struct {
+    int64_t N, E;
+    int32_t H, D, F, dtype;
+    int32_t split_threshold, chunk_len;
+    int32_t n_split, n_chunks;        /* CSR rows split, and their chunk count */
+    int32_t t_n_split, t_n_chunks;    /* the same for the transposed CSR */
+    int64_t plan_device_bytes;        /* device memory the plan owns */
+} sga_plan_info;
+
+sga_status sga_plan_get_info(const sga_plan *plan, sga_plan_info *info);
+
+typedef enum {
+    SGA_ARR_T_INDPTR = 0,     /* [N+1] */
+    SGA_ARR_T_DST = 1,        /* [E] */
+    SGA_ARR_SPLIT_ROWS = 2,   /* [n_split] */
+    SGA_ARR_CHUNK_PTR = 3,    /* [n_split+1] */
+    SGA_ARR_CHUNK_ROW = 4,    /* [n_chunks] */
+    SGA_ARR_CHUNK_BEG = 5,    /* [n_chunks] */
+    SGA_ARR_CHUNK_END = 6,    /* [n_chunks] */
+    SGA_ARR_T_SPLIT_ROWS = 7, /* transposed-CSR counterparts of 2..6 */
+    SGA_ARR_T_CHUNK_PTR = 8,
+    SGA_ARR_T_CHUNK_ROW = 9,
+    SGA_ARR_T_CHUNK_BEG = 10,
+    SGA_ARR_T_CHUNK_END = 11
+} sga_plan_array;
+
+/* Copy one plan array into caller HOST memory of `count` int32 (must equal the
+ * array's length).  Synchronous. */
+sga_status sga_plan_copy_array(const sga_plan *plan, sga_plan_array which, int32_t *host_out,
+                               int64_t count);
+
+/* ---- instrumentation ------------------------------------------------------ */
+
+/* Kernels launched by this library since the process started (all threads). */
+int64_t sga_launch_count(void);
+
+typedef enum {
+    SGA_KERN_NONE = 0,
+    SGA_KERN_GT_FWD = 1, SGA_KERN_GT_FWD_MERGE = 2,
+    SGA_KERN_GT_BWD_DQ = 3, SGA_KERN_GT_BWD_DKDV = 4, SGA_KERN_GT_BWD_MERGE = 5,
+    SGA_KERN_GATV2_PROJ = 6, SGA_KERN_GATV2_FWD = 7, SGA_KERN_GATV2_FWD_MERGE = 8,
+    SGA_KERN_GATV2_BWD_DST = 9, SGA_KERN_GATV2_BWD_SRC = 10, SGA_KERN_GATV2_BWD_MERGE = 11,
+    SGA_KERN_GATV2_BWD_DX = 12, SGA_KERN_GATV2_BWD_DW = 13, SGA_KERN_GATV2_BWD_REDUCE = 14,
+    SGA_KERN_COUNT = 15
+} sga_kernel_id;
+
+/* Time one kernel kind with CUDA events recorded on the launching stream
+ * around each of its launches (at most 4096 launches per window).
+ * sga_profile_stop synchronises those events and returns the summed device
+ * time in milliseconds and the number of launches timed. */
+sga_status sga_profile_start(sga_kernel_id which);
+sga_status sga_profile_stop(double *total_ms, int64_t *launches);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGA_H */

@@ -1,0 +1,334 @@
+"""Fused CSR edge attention (Graph Transformer, GATv2) on sm_103a.
+
+A thin ctypes binding over the C ABI of ``libsga.so`` (declared in
+``include/sga.h``).  This module only marshals arguments: every step of the
+forward and backward passes runs in the library's CUDA kernels.  PyTorch
+provides device memory and the current stream.  There is no CPU fallback: if
+the library is missing, every call raises.
+
+Graph convention: destination-sorted CSR (row i = destination, ``indices`` =
+sources), int32, on the GPU.  Node tensors are [N, H, D], float32 or bfloat16.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsga.so")
+
+SGA_OK, SGA_EINVAL, SGA_EUNSUPPORTED, SGA_ECUDA, SGA_EWORKSPACE, SGA_EDEVICE_CHECK = range(6)
+SGA_F32, SGA_BF16 = 0, 1
+
+KERNELS = {
+    "gt_fwd": 1, "gt_fwd_merge": 2, "gt_bwd_dq": 3, "gt_bwd_dkdv": 4, "gt_bwd_merge": 5,
+    "gatv2_proj": 6, "gatv2_fwd": 7, "gatv2_fwd_merge": 8, "gatv2_bwd_dst": 9,
+    "gatv2_bwd_src": 10, "gatv2_bwd_merge": 11, "gatv2_bwd_dx": 12, "gatv2_bwd_dw": 13,
+    "gatv2_bwd_reduce": 14,
+}
+
+ARRAYS = {
+    "t_indptr": 0, "t_dst": 1, "split_rows": 2, "chunk_ptr": 3, "chunk_row": 4, "chunk_beg": 5,
+    "chunk_end": 6, "t_split_rows": 7, "t_chunk_ptr": 8, "t_chunk_row": 9, "t_chunk_beg": 10,
+    "t_chunk_end": 11,
+}
+
+
+class SgaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _lib().sga_status_string(status).decode()
+        if status == SGA_ECUDA:
+            msg += f" (cudaError {_lib().sga_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}")
+
+
+class PlanOpts(ctypes.Structure):
+    _fields_ = [("split_threshold", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
+                ("in_features", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int64), ("E", ctypes.c_int64), ("H", ctypes.c_int32),
+                ("D", ctypes.c_int32), ("F", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("split_threshold", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
+                ("n_split", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
+                ("t_n_split", ctypes.c_int32), ("t_n_chunks", ctypes.c_int32),
+                ("plan_device_bytes", ctypes.c_int64)]
+
+
+_LIB = None
+_vp, _i64, _int, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+
+_SIGNATURES = {
+    "sga_status_string": ([_int], ctypes.c_char_p),
+    "sga_last_cuda_error": ([], _int),
+    "sga_launch_count": ([], _i64),
+    "sga_plan_create": ([_vp, _vp, _i64, _i64, _int, _int, _int, ctypes.POINTER(PlanOpts), _vp,
+                         ctypes.POINTER(_vp)], _int),
+    "sga_plan_workspace_bytes": ([_vp], ctypes.c_size_t),
+    "sga_plan_set_workspace": ([_vp, _vp, ctypes.c_size_t], _int),
+    "sga_plan_destroy": ([_vp], None),
+    "sga_plan_get_info": ([_vp, ctypes.POINTER(PlanInfo)], _int),
+    "sga_plan_copy_array": ([_vp, _int, _vp, _i64], _int),
+    "sga_read_device_error": ([_vp, _vp, ctypes.POINTER(ctypes.c_int32)], _int),
+    "gt_attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp],
+                    _int),
+    "gt_attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int,
+                     _vp, _vp, _vp, _vp], _int),
+    "gatv2_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _f32, _int,
+                   _vp, _vp, _vp, _vp, _vp], _int),
+    "gatv2_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int,
+                   _int, _int, _f32, _int, _vp, _vp, _vp, _vp, _vp], _int),
+    "sga_profile_start": ([_int], _int),
+    "sga_profile_stop": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64)], _int),
+}
+
+
+def _lib():
+    """Load libsga.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: run sparse_graph_attention_csr_gb300.build "
+                              "(or __graft_entry__.build()) first; there is no CPU fallback")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _LIB = lib
+    return _LIB
+
+
+def load_library():
+    """Load the native library now; returns the ctypes handle."""
+    return _lib()
+
+
+def _check(status: int, what: str):
+    if status != SGA_OK:
+        raise SgaError(status, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SGA_F32
+    if t.dtype == torch.bfloat16:
+        return SGA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def launch_count() -> int:
+    """Kernels launched by the library in this process."""
+    return int(_lib().sga_launch_count())
+
+
+def profile_start(kernel: str):
+    _check(_lib().sga_profile_start(KERNELS[kernel]), "sga_profile_start")
+
+
+def profile_stop():
+    """(total device ms, launches) of the kernel kind being profiled."""
+    ms, n = ctypes.c_double(), ctypes.c_int64()
+    _check(_lib().sga_profile_stop(ctypes.byref(ms), ctypes.byref(n)), "sga_profile_stop")
+    return ms.value, n.value
+
+
+class Plan:
+    """A graph plan: validated CSR, transposed CSR and degree partitions on the
+    device, plus the caller-owned workspace the kernels need.
+
+    ``indptr``/``indices`` must stay alive and unchanged while the plan is used.
+    """
+
+    def __init__(self, indptr: torch.Tensor, indices: torch.Tensor, H: int, D: int,
+                 dtype=torch.bfloat16, F: int = 0, split_threshold: int = 0, chunk_len: int = 0,
+                 stream=None):
+        _need(indptr, "indptr", torch.int32)
+        _need(indices, "indices", torch.int32)
+        self.indptr, self.indices = indptr, indices
+        self.N = indptr.numel() - 1
+        self.E = indices.numel()
+        self.H, self.D, self.F = int(H), int(D), int(F)
+        self.dtype = dtype
+        self.dt = SGA_F32 if dtype == torch.float32 else SGA_BF16
+        opts = PlanOpts(int(split_threshold), int(chunk_len), int(F), 0)
+        handle = ctypes.c_void_p()
+        self._h = None
+        _check(_lib().sga_plan_create(_ptr(indptr), _ptr(indices), self.N, self.E, self.H, self.D,
+                                      self.dt, ctypes.byref(opts), _stream(stream),
+                                      ctypes.byref(handle)), "sga_plan_create")
+        self._h = handle
+        nbytes = int(_lib().sga_plan_workspace_bytes(handle))
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=indptr.device)
+        _check(_lib().sga_plan_set_workspace(handle, _ptr(self.workspace), nbytes),
+               "sga_plan_set_workspace")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and _LIB is not None:
+            _LIB.sga_plan_destroy(h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def info(self) -> dict:
+        inf = PlanInfo()
+        _check(_lib().sga_plan_get_info(self._h, ctypes.byref(inf)), "sga_plan_get_info")
+        return {name: getattr(inf, name) for name, _ in PlanInfo._fields_}
+
+    def array(self, name: str):
+        """Copy one plan array (transposed CSR or partition) to a numpy int32 array."""
+        import numpy as np
+        inf = self.info()
+        n = {"t_indptr": self.N + 1, "t_dst": self.E, "split_rows": inf["n_split"],
+             "chunk_ptr": inf["n_split"] + 1, "chunk_row": inf["n_chunks"],
+             "chunk_beg": inf["n_chunks"], "chunk_end": inf["n_chunks"],
+             "t_split_rows": inf["t_n_split"], "t_chunk_ptr": inf["t_n_split"] + 1,
+             "t_chunk_row": inf["t_n_chunks"], "t_chunk_beg": inf["t_n_chunks"],
+             "t_chunk_end": inf["t_n_chunks"]}[name]
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        _check(_lib().sga_plan_copy_array(self._h, ARRAYS[name], out.ctypes.data, n),
+               "sga_plan_copy_array")
+        return out[:n]
+
+    def device_error(self, stream=None) -> int:
+        """Read and clear the device range-check word (0 = no failed check)."""
+        code = ctypes.c_int32()
+        st = _lib().sga_read_device_error(self._h, _stream(stream), ctypes.byref(code))
+        if st not in (SGA_OK, SGA_EDEVICE_CHECK):
+            _check(st, "sga_read_device_error")
+        return int(code.value)
+
+    def _graph(self):
+        return _ptr(self.indptr), _ptr(self.indices), self.N, self.E
+
+
+# ------------------------------------------------------------ Graph Transformer
+
+def gt_attn_fwd(plan: Plan, Q, K, V, out=None, lse=None, stream=None):
+    """out [N,H,D] (dtype of Q) and lse [N,H] float32."""
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _need(t, n, plan.dtype)
+    out = torch.empty_like(Q) if out is None else out
+    lse = torch.empty(Q.shape[:2], dtype=torch.float32, device=Q.device) if lse is None else lse
+    _check(_lib().gt_attn_fwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V), plan.N,
+                              plan.E, plan.H, plan.D, plan.dt, _ptr(out), _ptr(lse),
+                              _stream(stream)), "gt_attn_fwd")
+    return out, lse
+
+
+def gt_attn_bwd(plan: Plan, Q, K, V, out, lse, dOut, dQ=None, dK=None, dV=None, stream=None):
+    """(dQ, dK, dV), each [N,H,D]."""
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("out", out), ("dOut", dOut)):
+        _need(t, n, plan.dtype)
+    _need(lse, "lse", torch.float32)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    _check(_lib().gt_attn_bwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V),
+                              _ptr(out), _ptr(lse), _ptr(dOut), plan.N, plan.E, plan.H, plan.D,
+                              plan.dt, _ptr(dQ), _ptr(dK), _ptr(dV), _stream(stream)),
+           "gt_attn_bwd")
+    return dQ, dK, dV
+
+
+# ----------------------------------------------------------------------- GATv2
+
+def gatv2_fwd(plan: Plan, X, W_l, W_r, a, slope: float = 0.2, FL=None, FR=None, out=None,
+              lse=None, stream=None):
+    """(FL, FR, out, lse): FL = X W_l and FR = X W_r as [N,H,D], out [N,H,D], lse [N,H]."""
+    for n, t in (("X", X), ("W_l", W_l), ("W_r", W_r), ("a", a)):
+        _need(t, n, plan.dtype)
+    shape = (plan.N, plan.H, plan.D)
+    FL = torch.empty(shape, dtype=X.dtype, device=X.device) if FL is None else FL
+    FR = torch.empty(shape, dtype=X.dtype, device=X.device) if FR is None else FR
+    out = torch.empty(shape, dtype=X.dtype, device=X.device) if out is None else out
+    lse = torch.empty(shape[:2], dtype=torch.float32, device=X.device) if lse is None else lse
+    _check(_lib().gatv2_fwd(plan.handle, *plan._graph()[:2], _ptr(X), _ptr(W_l), _ptr(W_r),
+                            _ptr(a), plan.N, plan.E, plan.F, plan.H, plan.D, float(slope), plan.dt,
+                            _ptr(FL), _ptr(FR), _ptr(out), _ptr(lse), _stream(stream)),
+           "gatv2_fwd")
+    return FL, FR, out, lse
+
+
+def gatv2_bwd(plan: Plan, X, W_l, W_r, a, FL, FR, out, lse, dOut, slope: float = 0.2,
+              dX=None, dW_l=None, dW_r=None, da=None, stream=None):
+    """(dX, dW_l, dW_r, da)."""
+    for n, t in (("X", X), ("W_l", W_l), ("W_r", W_r), ("a", a), ("FL", FL), ("FR", FR),
+                 ("out", out), ("dOut", dOut)):
+        _need(t, n, plan.dtype)
+    _need(lse, "lse", torch.float32)
+    dX = torch.empty_like(X) if dX is None else dX
+    dW_l = torch.empty_like(W_l) if dW_l is None else dW_l
+    dW_r = torch.empty_like(W_r) if dW_r is None else dW_r
+    da = torch.empty_like(a) if da is None else da
+    _check(_lib().gatv2_bwd(plan.handle, *plan._graph()[:2], _ptr(X), _ptr(W_l), _ptr(W_r),
+                            _ptr(a), _ptr(FL), _ptr(FR), _ptr(out), _ptr(lse), _ptr(dOut), plan.N,
+                            plan.E, plan.F, plan.H, plan.D, float(slope), plan.dt, _ptr(dX),
+                            _ptr(dW_l), _ptr(dW_r), _ptr(da), _stream(stream)), "gatv2_bwd")
+    return dX, dW_l, dW_r, da
+
+
+# -------------------------------------------------------------- autograd layers
+
+class GTAttention(torch.autograd.Function):
+    """Graph Transformer edge attention as an autograd function:
+    ``out = GTAttention.apply(Q, K, V, plan)``."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, plan):
+        Q, K, V = Q.contiguous(), K.contiguous(), V.contiguous()
+        out, lse = gt_attn_fwd(plan, Q, K, V)
+        ctx.plan = plan
+        ctx.save_for_backward(Q, K, V, out, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dOut):
+        Q, K, V, out, lse = ctx.saved_tensors
+        dQ, dK, dV = gt_attn_bwd(ctx.plan, Q, K, V, out, lse, dOut.contiguous())
+        return dQ, dK, dV, None
+
+
+class GATv2Attention(torch.autograd.Function):
+    """GATv2 layer (projections + edge attention):
+    ``out = GATv2Attention.apply(X, W_l, W_r, a, plan, slope)``."""
+
+    @staticmethod
+    def forward(ctx, X, W_l, W_r, a, plan, slope=0.2):
+        X, W_l, W_r, a = (t.contiguous() for t in (X, W_l, W_r, a))
+        FL, FR, out, lse = gatv2_fwd(plan, X, W_l, W_r, a, slope)
+        ctx.plan, ctx.slope = plan, slope
+        ctx.save_for_backward(X, W_l, W_r, a, FL, FR, out, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dOut):
+        X, W_l, W_r, a, FL, FR, out, lse = ctx.saved_tensors
+        dX, dWl, dWr, da = gatv2_bwd(ctx.plan, X, W_l, W_r, a, FL, FR, out, lse,
+                                     dOut.contiguous(), ctx.slope)
+        return dX, dWl, dWr, da, None, None

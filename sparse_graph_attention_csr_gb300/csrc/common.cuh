@@ -1,0 +1,117 @@
+// Shared device helpers for the edge-attention kernels: 16-byte row chunks,
+// bf16/fp32 conversion, warp reductions, launch bookkeeping.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/sga.h"
+
+#define SGA_FULL_MASK 0xffffffffu
+
+namespace sga {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kWarpsPerBlock = 8;
+
+// ---- element types ---------------------------------------------------------
+
+// One 16-byte chunk of a row holds EL elements of T.
+template <typename T> struct Elt;
+template <> struct Elt<float> { static constexpr int EL = 4; };
+template <> struct Elt<__nv_bfloat16> { static constexpr int EL = 8; };
+
+__device__ __forceinline__ uint4 ldg16(const void *p) {
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// Streaming gather: read-only path, do not keep in L1.
+__device__ __forceinline__ uint4 ldg16_stream(const void *p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+template <typename T> __device__ __forceinline__ void unpack(const uint4 &u, float *x);
+
+template <> __device__ __forceinline__ void unpack<float>(const uint4 &u, float *x) {
+    x[0] = __uint_as_float(u.x);
+    x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z);
+    x[3] = __uint_as_float(u.w);
+}
+
+// bf16 -> fp32 is exact: the bf16 bits are the top half of the fp32 bits.
+template <> __device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4 &u, float *x) {
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xffff0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xffff0000u);
+    x[4] = __uint_as_float(u.z << 16);
+    x[5] = __uint_as_float(u.z & 0xffff0000u);
+    x[6] = __uint_as_float(u.w << 16);
+    x[7] = __uint_as_float(u.w & 0xffff0000u);
+}
+
+template <typename T> __device__ __forceinline__ uint4 pack(const float *x);
+
+template <> __device__ __forceinline__ uint4 pack<float>(const float *x) {
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                      __float_as_uint(x[3]));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+template <> __device__ __forceinline__ uint4 pack<__nv_bfloat16>(const float *x) {
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Sum over aligned groups of W lanes (W a power of two <= 32); every lane of
+// the group receives the group total.
+template <int W> __device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) v += __shfl_xor_sync(SGA_FULL_MASK, v, o);
+    return v;
+}
+
+template <int W> __device__ __forceinline__ void group_sum2(float &a, float &b) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(SGA_FULL_MASK, a, o);
+        b += __shfl_xor_sync(SGA_FULL_MASK, b, o);
+    }
+}
+
+// exp2 that maps -inf to 0 without producing NaN for (-inf) - (-inf).
+__device__ __forceinline__ float exp2_diff(float a, float m) {
+    return (a == -INFINITY) ? 0.0f : exp2f(a - m);
+}
+
+// Device error bits (plan error word).
+constexpr int kErrIndexRange = 1;   // a gathered node id was outside [0, N)
+
+}  // namespace sga
+
+// ---- host-side launch bookkeeping (defined in api.cu) -----------------------
+namespace sga {
+void note_launch(sga_kernel_id which, cudaStream_t s, bool after);
+}

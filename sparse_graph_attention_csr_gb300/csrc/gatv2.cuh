@@ -1,0 +1,693 @@
+// GATv2 edge attention: projections, fused edge forward, and the backward
+// pass (destination pass for dFL and da, transposed source pass for dFR,
+// then the projection gradients).
+//
+// Method: the GATv2 score e_ij = sum_d a[h,d] LeakyReLU(FL[i,h,d] + FR[j,h,d])
+// with FL = X W_l and FR = X W_r ("How Attentive are Graph Attention
+// Networks?", cited by both pages) inside the fused online-softmax edge
+// kernel of "On Efficient Scaling of GNNs via IO-Aware Layers
+// Implementations" (Yandex Research blog post, "Attention-based layers"
+// paragraph).  FR_j is both the score operand and the aggregated value, so
+// the forward gathers one neighbour row per edge.  The backward recomputes
+// the weights from the saved log-sum-exp.
+//
+// The edge kernels share the Graph Transformer's lane layout (gt.cuh): one
+// warp per row or split-row chunk, 16-byte chunks per lane, heads reduced by
+// xor shuffles.
+#pragma once
+
+#include "gt.cuh"
+
+namespace sga {
+
+// --------------------------------------------------------------- edge fwd
+
+template <typename T, int D, int NC, int G>
+__global__ void __launch_bounds__(256)
+gatv2_fwd_kernel(Gatv2Args a) {
+    using S = GtShape<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
+    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemRange it;
+    if (!decode_item(item, a.rows, a.indptr, a.N, a.split_threshold, it)) return;
+    const int R = a.H * D / EL;
+    const uint4 *__restrict__ FRc = static_cast<const uint4 *>(a.FR);
+    const float slope = a.slope;
+
+    float fl[NC][EL], att[NC][EL], acc[NC][EL], m[NC], l[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c < R) {
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + (size_t)it.row * R + c), fl[k]);
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
+        } else {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) fl[k][x] = att[k][x] = 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < EL; ++x) {
+            acc[k][x] = 0.f;
+            att[k][x] *= kLog2e;   // scores directly in log2 units
+        }
+        m[k] = -INFINITY;
+        l[k] = 0.f;
+    }
+
+    for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+        const int cnt = min(32, it.end - e0);
+        const int32_t myj = load_ids(a.indices, e0, cnt, a.N, a.d_err);
+        for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+            uint4 fr[U][NC];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + g + NG * u;
+                const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
+                ok[u] = (t < cnt) && (j >= 0);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int c = gl + G * k;
+                    fr[u][k] = (ok[u] && c < R) ? ldg16_stream(FRc + (size_t)j * R + c)
+                                                : make_uint4(0, 0, 0, 0);
+                }
+            }
+            float s[U][NC];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float f[EL];
+                    unpack<T>(fr[u][k], f);
+                    float e = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        const float z = fl[k][x] + f[x];
+                        e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
+                    }
+                    e = group_sum<LH>(e);
+                    s[u][k] = ok[u] ? e : -INFINITY;
+                }
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                float mx = m[k];
+#pragma unroll
+                for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][k]);
+                if (mx == -INFINITY) continue;
+                const float alpha = exp2_diff(m[k], mx);
+                l[k] *= alpha;
+#pragma unroll
+                for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float p = exp2_diff(s[u][k], mx);
+                    l[k] += p;
+                    float f[EL];
+                    unpack<T>(fr[u][k], f);
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, f[x], acc[k][x]);
+                }
+                m[k] = mx;
+            }
+        }
+    }
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
+            const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
+            const float mx = fmaxf(m[k], mo);
+            const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
+            l[k] = l[k] * a1 + lo * a2;
+#pragma unroll
+            for (int x = 0; x < EL; ++x) {
+                const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
+                acc[k][x] = acc[k][x] * a1 + ao * a2;
+            }
+            m[k] = mx;
+        }
+    if (g != 0) return;
+    const int HD = a.H * D;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c >= R) continue;
+        const int h = c / LH;
+        if (it.partial) {
+            float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)item * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4)
+                dst[x / 4] = make_float4(acc[k][x], acc[k][x + 1], acc[k][x + 2], acc[k][x + 3]);
+            if (c % LH == 0) {
+                a.ws_ml[((size_t)item * a.H + h) * 2 + 0] = m[k];
+                a.ws_ml[((size_t)item * a.H + h) * 2 + 1] = l[k];
+            }
+        } else {
+            const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
+            float o[EL];
+#pragma unroll
+            for (int x = 0; x < EL; ++x) o[x] = acc[k][x] * inv;
+            reinterpret_cast<uint4 *>(a.out_w)[(size_t)it.row * R + c] = pack<T>(o);
+            if (c % LH == 0)
+                a.lse_w[(size_t)it.row * a.H + h] =
+                    l[k] > 0.f ? (m[k] + log2f(l[k])) * kLn2 : -INFINITY;
+        }
+    }
+}
+
+// ---------------------------------------------------- backward: dst pass
+
+// Per destination row i, for each edge (j):
+//   z = fl_i + fr_j, e = a . LReLU(z), p = exp(e - lse_i),
+//   dp = dOut_i . fr_j, de = p (dp - Delta_i),
+//   dFL_i += de a * LReLU'(z),  da += de LReLU(z).
+// Warps stride over work items; each block leaves one fp32 partial of da.
+template <typename T, int D, int NC, int G>
+__global__ void __launch_bounds__(256)
+gatv2_bwd_dst_kernel(Gatv2Args a) {
+    using S = GtShape<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    __shared__ float da_sh[1024];
+    const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
+    const int R = a.H * D / EL, HD = a.H * D;
+    const float slope = a.slope;
+    const uint4 *__restrict__ FRc = static_cast<const uint4 *>(a.FR);
+
+    for (int x = threadIdx.x; x < HD; x += blockDim.x) da_sh[x] = 0.f;
+
+    float att[NC][EL], dacc[NC][EL];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c < R) unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
+        else
+#pragma unroll
+            for (int x = 0; x < EL; ++x) att[k][x] = 0.f;
+#pragma unroll
+        for (int x = 0; x < EL; ++x) dacc[k][x] = 0.f;
+    }
+
+    const int64_t n_items = (int64_t)a.rows.n_chunks + a.N;
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
+    for (int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); item < n_items;
+         item += stride) {
+        ItemRange it;
+        if (!decode_item(item, a.rows, a.indptr, a.N, a.split_threshold, it)) continue;
+        float fl[NC][EL], go[NC][EL], dfl[NC][EL], delta[NC], lse2[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            const int c = gl + G * k;
+            float o[EL];
+            if (c < R) {
+                const size_t off = (size_t)it.row * R + c;
+                unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + off), fl[k]);
+                unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
+                unpack<T>(ldg16(static_cast<const uint4 *>(a.out) + off), o);
+                lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + c / LH) * kLog2e;
+            } else {
+#pragma unroll
+                for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = o[x] = 0.f;
+                lse2[k] = 0.f;
+            }
+            float d = 0.f;
+#pragma unroll
+            for (int x = 0; x < EL; ++x) {
+                d = fmaf(go[k][x], o[x], d);
+                dfl[k][x] = 0.f;
+            }
+            delta[k] = group_sum<LH>(d);
+        }
+        if (g == 0 && (!it.partial || it.beg == a.indptr[it.row])) {
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                const int c = gl + G * k;
+                if (c < R && c % LH == 0) a.ws_delta[(size_t)it.row * a.H + c / LH] = delta[k];
+            }
+        }
+        for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+            const int cnt = min(32, it.end - e0);
+            const int32_t myj = load_ids(a.indices, e0, cnt, a.N, a.d_err);
+            for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+                uint4 fr[U][NC];
+                bool ok[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int t = t0 + g + NG * u;
+                    const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
+                    ok[u] = (t < cnt) && (j >= 0);
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        const int c = gl + G * k;
+                        fr[u][k] = (ok[u] && c < R) ? ldg16_stream(FRc + (size_t)j * R + c)
+                                                    : make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        float f[EL];
+                        unpack<T>(fr[u][k], f);
+                        float e = 0.f, dp = 0.f;
+#pragma unroll
+                        for (int x = 0; x < EL; ++x) {
+                            const float z = fl[k][x] + f[x];
+                            e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
+                            dp = fmaf(go[k][x], f[x], dp);
+                        }
+                        group_sum2<LH>(e, dp);
+                        const float p = ok[u] ? exp2f(e * kLog2e - lse2[k]) : 0.f;
+                        const float de = p * (dp - delta[k]);
+#pragma unroll
+                        for (int x = 0; x < EL; ++x) {
+                            const float z = fl[k][x] + f[x];
+                            const bool pos = z > 0.f;
+                            dfl[k][x] = fmaf(de * att[k][x], pos ? 1.f : slope, dfl[k][x]);
+                            dacc[k][x] = fmaf(de, pos ? z : slope * z, dacc[k][x]);
+                        }
+                    }
+            }
+        }
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+            for (int k = 0; k < NC; ++k)
+#pragma unroll
+                for (int x = 0; x < EL; ++x)
+                    dfl[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dfl[k][x], off);
+        if (g == 0) {
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                const int c = gl + G * k;
+                if (c >= R) continue;
+                if (it.partial) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * HD + c * EL);
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(dfl[k][x], dfl[k][x + 1], dfl[k][x + 2], dfl[k][x + 3]);
+                } else {
+                    reinterpret_cast<uint4 *>(a.ws_dfl)[(size_t)it.row * R + c] = pack<T>(dfl[k]);
+                }
+            }
+        }
+    }
+    // da: groups -> lanes of group 0, warps -> shared memory (fixed order), one row per block
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+#pragma unroll
+            for (int x = 0; x < EL; ++x) dacc[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dacc[k][x], off);
+    __syncthreads();
+    for (int w = 0; w < kWarpsPerBlock; ++w) {
+        if ((threadIdx.x >> 5) == w && g == 0) {
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                const int c = gl + G * k;
+                if (c < R)
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) da_sh[c * EL + x] += dacc[k][x];
+            }
+        }
+        __syncthreads();
+    }
+    for (int x = threadIdx.x; x < HD; x += blockDim.x)
+        a.ws_da[(size_t)blockIdx.x * HD + x] = da_sh[x];
+}
+
+// ---------------------------------------------------- backward: src pass
+
+// Per source j over its destinations i (transposed CSR):
+//   dFR_j += p dOut_i + de a * LReLU'(z).
+template <typename T, int D, int NC, int G>
+__global__ void __launch_bounds__(256)
+gatv2_bwd_src_kernel(Gatv2Args a) {
+    using S = GtShape<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
+    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemRange it;
+    if (!decode_item(item, a.cols, a.t_indptr, a.N, a.split_threshold, it)) return;
+    const int R = a.H * D / EL;
+    const float slope = a.slope;
+    const uint4 *__restrict__ FLc = static_cast<const uint4 *>(a.FL);
+    const uint4 *__restrict__ Gc = static_cast<const uint4 *>(a.dOut);
+
+    float frj[NC][EL], att[NC][EL], dfr[NC][EL];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c < R) {
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.FR) + (size_t)it.row * R + c), frj[k]);
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
+        } else {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) frj[k][x] = att[k][x] = 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < EL; ++x) dfr[k][x] = 0.f;
+    }
+    for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+        const int cnt = min(32, it.end - e0);
+        const int32_t myi = load_ids(a.t_dst, e0, cnt, a.N, a.d_err);
+        for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+            uint4 flr[U][NC], gr[U][NC];
+            float l2[U][NC], dl[U][NC];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + g + NG * u;
+                const int32_t i = __shfl_sync(SGA_FULL_MASK, myi, t & 31);
+                ok[u] = (t < cnt) && (i >= 0);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int c = gl + G * k;
+                    if (ok[u] && c < R) {
+                        flr[u][k] = ldg16_stream(FLc + (size_t)i * R + c);
+                        gr[u][k] = ldg16_stream(Gc + (size_t)i * R + c);
+                        l2[u][k] = __ldg(a.lse + (size_t)i * a.H + c / LH);
+                        dl[u][k] = a.ws_delta[(size_t)i * a.H + c / LH];
+                    } else {
+                        flr[u][k] = make_uint4(0, 0, 0, 0);
+                        gr[u][k] = make_uint4(0, 0, 0, 0);
+                        l2[u][k] = 0.f;
+                        dl[u][k] = 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float f[EL], gf[EL];
+                    unpack<T>(flr[u][k], f);
+                    unpack<T>(gr[u][k], gf);
+                    float e = 0.f, dp = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        const float z = f[x] + frj[k][x];
+                        e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
+                        dp = fmaf(gf[x], frj[k][x], dp);
+                    }
+                    group_sum2<LH>(e, dp);
+                    const float p = ok[u] ? exp2f((e - l2[u][k]) * kLog2e) : 0.f;
+                    const float de = p * (dp - dl[u][k]);
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        const float z = f[x] + frj[k][x];
+                        dfr[k][x] = fmaf(p, gf[x], dfr[k][x]);
+                        dfr[k][x] = fmaf(de * att[k][x], z > 0.f ? 1.f : slope, dfr[k][x]);
+                    }
+                }
+        }
+    }
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+#pragma unroll
+            for (int x = 0; x < EL; ++x) dfr[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dfr[k][x], off);
+    if (g != 0) return;
+    const int HD = a.H * D;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c >= R) continue;
+        if (it.partial) {
+            float4 *dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4)
+                dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
+        } else {
+            reinterpret_cast<uint4 *>(a.ws_dfr)[(size_t)it.row * R + c] = pack<T>(dfr[k]);
+        }
+    }
+}
+
+// Finish split rows: dFL (items [0, rows.n_split)) and dFR (the rest) are the
+// chunk partial sums in chunk order.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a) {
+    constexpr int EL = Elt<T>::EL;
+    const int lane = threadIdx.x & 31;
+    int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int R = a.H * D / EL, HD = a.H * D;
+    const Partition *P = &a.rows;
+    const float *part = a.ws_row;
+    void *dst = a.ws_dfl;
+    if (s >= a.rows.n_split) {
+        s -= a.rows.n_split;
+        if (s >= a.cols.n_split) return;
+        P = &a.cols;
+        part = a.ws_col;
+        dst = a.ws_dfr;
+    }
+    const int32_t row = P->split_rows[s];
+    const int32_t c0 = P->chunk_ptr[s], c1 = P->chunk_ptr[s + 1];
+    for (int c = lane; c < R; c += 32) {
+        float acc[EL];
+#pragma unroll
+        for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+        for (int32_t ch = c0; ch < c1; ++ch) {
+            const float4 *src = reinterpret_cast<const float4 *>(part + (size_t)ch * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4) {
+                const float4 v = src[x / 4];
+                acc[x] += v.x; acc[x + 1] += v.y; acc[x + 2] += v.z; acc[x + 3] += v.w;
+            }
+        }
+        reinterpret_cast<uint4 *>(dst)[(size_t)row * R + c] = pack<T>(acc);
+    }
+}
+
+// ------------------------------------------------------------ dense GEMMs
+
+// C = sum over pairs p of op(A_p) op(B_p) with fp32 accumulation (SIMT).
+//   A: [M, K] row-major, or [K, M] row-major when TA (then op(A) = A^T).
+//   B: [K, N] row-major, or [N, K] row-major when TB.
+// Tiles 64 x 64 x 16, 256 threads, 4 x 4 outputs per thread.  Rows [k0, k1)
+// of the K range are used (split-K slabs); blockIdx.z selects the slab.
+// The result goes to C (dtype T) or, when Cpart is set, to the fp32 partial
+// Cpart[slab][M][N].
+template <typename T, bool TA, bool TB> struct GemmArgs {
+    const T *A[2];
+    const T *B[2];
+    int pairs;
+    int64_t M, N, K;
+    int64_t k_per_slab;
+    T *C;
+    float *Cpart;
+};
+
+template <typename T, bool TA, bool TB>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<T, TA, TB> g) {
+    constexpr int BM = 64, BN = 64, BK = 16;
+    __shared__ float As[BK][BM + 4];
+    __shared__ float Bs[BK][BN + 4];
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+    const int64_t k_lo = (int64_t)blockIdx.z * g.k_per_slab;
+    const int64_t k_hi = min(g.K, k_lo + g.k_per_slab);
+    float acc[4][4] = {};
+    for (int p = 0; p < g.pairs; ++p) {
+        const T *A = g.A[p], *B = g.B[p];
+        for (int64_t kb = k_lo; kb < k_hi; kb += BK) {
+            for (int idx = threadIdx.x; idx < BM * BK; idx += 256) {
+                int mm, kk;
+                if (TA) { mm = idx % BM; kk = idx / BM; } else { kk = idx % BK; mm = idx / BK; }
+                const int64_t gm = m0 + mm, gk = kb + kk;
+                float v = 0.f;
+                if (gm < g.M && gk < k_hi)
+                    v = to_f32<T>(TA ? A[gk * g.M + gm] : A[gm * g.K + gk]);
+                As[kk][mm] = v;
+            }
+            for (int idx = threadIdx.x; idx < BN * BK; idx += 256) {
+                int nn, kk;
+                if (TB) { kk = idx % BK; nn = idx / BK; } else { nn = idx % BN; kk = idx / BN; }
+                const int64_t gn = n0 + nn, gk = kb + kk;
+                float v = 0.f;
+                if (gn < g.N && gk < k_hi)
+                    v = to_f32<T>(TB ? B[gn * g.K + gk] : B[gk * g.N + gn]);
+                Bs[kk][nn] = v;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+                float av[4], bv[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) av[r] = As[kk][ty * 4 + r];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) bv[c] = Bs[kk][tx * 4 + c];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+            }
+            __syncthreads();
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int64_t gm = m0 + ty * 4 + r;
+        if (gm >= g.M) continue;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int64_t gn = n0 + tx * 4 + c;
+            if (gn >= g.N) continue;
+            if (g.Cpart) g.Cpart[((int64_t)blockIdx.z * g.M + gm) * g.N + gn] = acc[r][c];
+            else g.C[gm * g.N + gn] = from_f32<T>(acc[r][c]);
+        }
+    }
+}
+
+// dW_l, dW_r = sum of the slab partials [2][slab][F*HD] in slab order;
+// da = sum of the per-block partials in block order.
+template <typename T>
+__global__ void gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs, int64_t FHD,
+                                    T *dWl, T *dWr, const float *__restrict__ da_part, int blocks,
+                                    int HD, T *da) {
+    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < 2 * FHD) {
+        const int which = (int)(t / FHD);
+        const int64_t x = t % FHD;
+        float s = 0.f;
+        for (int k = 0; k < slabs; ++k) s += dw_part[((int64_t)which * slabs + k) * FHD + x];
+        (which ? dWr : dWl)[x] = from_f32<T>(s);
+    } else if (t < 2 * FHD + HD) {
+        const int x = (int)(t - 2 * FHD);
+        float s = 0.f;
+        for (int b = 0; b < blocks; ++b) s += da_part[(int64_t)b * HD + x];
+        da[x] = from_f32<T>(s);
+    }
+}
+
+template <typename T, bool TA, bool TB>
+cudaError_t gemm(const GemmArgs<T, TA, TB> &g, int slabs, sga_kernel_id kid, cudaStream_t s) {
+    dim3 grid((unsigned)((g.N + 63) / 64), (unsigned)((g.M + 63) / 64), (unsigned)slabs);
+    note_launch(kid, s, false);
+    gemm_simt_kernel<T, TA, TB><<<grid, 256, 0, s>>>(g);
+    note_launch(kid, s, true);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ launch
+
+template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStream_t s) {
+    constexpr int LH = D * (int)sizeof(T) / 16;
+    const int R = a.H * D / Elt<T>::EL;
+    const int HD = a.H * D;
+    // projections FL = X W_l, FR = X W_r
+    for (int w = 0; w < 2; ++w) {
+        GemmArgs<T, false, false> g{};
+        g.A[0] = static_cast<const T *>(a.X);
+        g.B[0] = static_cast<const T *>(w ? a.Wr : a.Wl);
+        g.pairs = 1;
+        g.M = a.N; g.N = HD; g.K = a.F; g.k_per_slab = a.F;
+        g.C = static_cast<T *>(w ? a.FR_w : a.FL_w);
+        g.Cpart = nullptr;
+        if (a.N > 0) {
+            cudaError_t e = gemm(g, 1, SGA_KERN_GATV2_PROJ, s);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    Gatv2Args b = a;
+    b.FL = a.FL_w;
+    b.FR = a.FR_w;
+    const int64_t items = (int64_t)a.rows.n_chunks + a.N;
+    cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
+        if (items == 0) return cudaSuccess;
+        note_launch(SGA_KERN_GATV2_FWD, s, false);
+        gatv2_fwd_kernel<T, D, NC, G><<<blocks_for_warps(items), 256, 0, s>>>(b);
+        note_launch(SGA_KERN_GATV2_FWD, s, true);
+        return cudaGetLastError();
+    });
+    if (e != cudaSuccess || a.rows.n_split == 0) return e;
+    note_launch(SGA_KERN_GATV2_FWD_MERGE, s, false);
+    gt_fwd_merge_kernel<T, D, Gatv2Args><<<blocks_for_warps(a.rows.n_split), 256, 0, s>>>(b);
+    note_launch(SGA_KERN_GATV2_FWD_MERGE, s, true);
+    return cudaGetLastError();
+}
+
+template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStream_t s) {
+    constexpr int LH = D * (int)sizeof(T) / 16;
+    const int R = a.H * D / Elt<T>::EL;
+    const int HD = a.H * D;
+    cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
+        note_launch(SGA_KERN_GATV2_BWD_DST, s, false);
+        gatv2_bwd_dst_kernel<T, D, NC, G><<<a.da_blocks, 256, 0, s>>>(a);
+        note_launch(SGA_KERN_GATV2_BWD_DST, s, true);
+        cudaError_t e2 = cudaGetLastError();
+        if (e2 != cudaSuccess) return e2;
+        const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
+        if (items_c == 0) return cudaSuccess;
+        note_launch(SGA_KERN_GATV2_BWD_SRC, s, false);
+        gatv2_bwd_src_kernel<T, D, NC, G><<<blocks_for_warps(items_c), 256, 0, s>>>(a);
+        note_launch(SGA_KERN_GATV2_BWD_SRC, s, true);
+        return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return e;
+    const int64_t merges = (int64_t)a.rows.n_split + a.cols.n_split;
+    if (merges > 0) {
+        note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
+        gatv2_bwd_merge_kernel<T, D><<<blocks_for_warps(merges), 256, 0, s>>>(a);
+        note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // dX = dFL W_l^T + dFR W_r^T
+    if (a.N > 0) {
+        GemmArgs<T, false, true> g{};
+        g.A[0] = static_cast<const T *>(a.ws_dfl);
+        g.B[0] = static_cast<const T *>(a.Wl);
+        g.A[1] = static_cast<const T *>(a.ws_dfr);
+        g.B[1] = static_cast<const T *>(a.Wr);
+        g.pairs = 2;
+        g.M = a.N; g.N = a.F; g.K = HD; g.k_per_slab = HD;
+        g.C = static_cast<T *>(a.dX);
+        if ((e = gemm(g, 1, SGA_KERN_GATV2_BWD_DX, s)) != cudaSuccess) return e;
+    }
+    // dW = X^T dF over node slabs: fp32 partials [2][slab][F][HD]
+    const int64_t per = (a.N + a.dw_slabs - 1) / a.dw_slabs;
+    const int64_t FHD = (int64_t)a.F * HD;
+    {
+        // One launch per projection; each writes slab-major partials with a stride of 2*F*HD.
+        for (int w = 0; w < 2 && a.N > 0; ++w) {
+            GemmArgs<T, true, false> g{};
+            g.A[0] = static_cast<const T *>(a.X);
+            g.B[0] = static_cast<const T *>(w ? a.ws_dfr : a.ws_dfl);
+            g.pairs = 1;
+            g.M = a.F; g.N = HD; g.K = a.N; g.k_per_slab = per;
+            g.C = nullptr;
+            g.Cpart = a.ws_dw + (size_t)w * FHD * a.dw_slabs;
+            if ((e = gemm(g, a.dw_slabs, SGA_KERN_GATV2_BWD_DW, s)) != cudaSuccess) return e;
+        }
+    }
+    const int64_t total = 2 * FHD + HD;
+    note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, false);
+    gatv2_reduce_kernel<T><<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+        a.ws_dw, a.dw_slabs, FHD, static_cast<T *>(a.dWl), static_cast<T *>(a.dWr), a.ws_da,
+        a.da_blocks, HD, static_cast<T *>(a.da));
+    note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, true);
+    return cudaGetLastError();
+}
+
+template <typename T> cudaError_t gatv2_fwd_t(const Gatv2Args &a, cudaStream_t s) {
+    switch (a.D) {
+        case 32: return gatv2_fwd_d<T, 32>(a, s);
+        case 64: return gatv2_fwd_d<T, 64>(a, s);
+        case 128: return gatv2_fwd_d<T, 128>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T> cudaError_t gatv2_bwd_t(const Gatv2Args &a, cudaStream_t s) {
+    switch (a.D) {
+        case 32: return gatv2_bwd_d<T, 32>(a, s);
+        case 64: return gatv2_bwd_d<T, 64>(a, s);
+        case 128: return gatv2_bwd_d<T, 128>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sga

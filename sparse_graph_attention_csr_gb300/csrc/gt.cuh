@@ -1,0 +1,651 @@
+// Graph Transformer edge attention: fused forward (online softmax) and the
+// recompute-from-lse backward, as templates instantiated per dtype.
+//
+// Method ("On Efficient Scaling of GNNs via IO-Aware Layers Implementations",
+// Yandex Research blog post, "Attention-based layers" paragraph): the edge
+// scores s_ij = q_i . k_j / sqrt(D) are produced and consumed on chip by an
+// online softmax and never stored; the backward pass rebuilds the weights
+// p_ij = exp(s_ij - lse_i) from the saved per-row log-sum-exp, following
+// FlashAttention-2.
+//
+// Schedule (sm_103a).  One warp owns one work item: a whole destination row,
+// or one fixed-length chunk of a split (high-degree) row.  A row of H*D
+// elements is viewed as R = H*D*sizeof(T)/16 sixteen-byte chunks; lane l of a
+// G-lane edge group holds chunks l, l+G, ...  (NC per lane), so one warp-wide
+// 16-byte load per chunk gathers a neighbour row coalesced.  When R < 32 the
+// warp splits into 32/G groups that take alternate edges and merge at the
+// end.  Each head spans LH = D*sizeof(T)/16 adjacent lanes; its dot product
+// is a log2(LH)-step xor-shuffle reduction.  U neighbours are loaded before
+// any is used, so every lane keeps U*NC*2 sixteen-byte gathers in flight.
+#pragma once
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace sga {
+
+template <typename T, int D, int NC, int G> struct GtShape {
+    static constexpr int EL = Elt<T>::EL;                     // elements per 16-byte chunk
+    static constexpr int LH = D * (int)sizeof(T) / 16;        // lanes per head
+    static constexpr int NG = 32 / G;                         // edge groups per warp
+    static constexpr int U = NC >= 8 ? 1 : 8 / NC;            // neighbours in flight
+    static_assert(LH <= G, "a head must fit in one edge group");
+};
+
+struct ItemRange {
+    int32_t row, beg, end;
+    bool partial;
+};
+
+// Work item w of a launch: chunks of split rows first, then every row (rows
+// above the split threshold are skipped; their chunks cover them).
+__device__ __forceinline__ bool decode_item(int64_t item, const Partition &P,
+                                            const int32_t *__restrict__ ptr, int64_t N,
+                                            int threshold, ItemRange &r) {
+    if (item < P.n_chunks) {
+        r.row = P.chunk_row[item];
+        r.beg = P.chunk_beg[item];
+        r.end = P.chunk_end[item];
+        r.partial = true;
+        return true;
+    }
+    const int64_t i = item - P.n_chunks;
+    if (i >= N) return false;
+    r.row = (int32_t)i;
+    r.beg = ptr[i];
+    r.end = ptr[i + 1];
+    r.partial = false;
+    return r.end - r.beg <= threshold;
+}
+
+// Fetch the 32 node ids of edges [e0, e0 + cnt) into one register per lane,
+// range-checked against N (an out-of-range id becomes -1 and flags the plan).
+__device__ __forceinline__ int32_t load_ids(const int32_t *__restrict__ ids, int32_t e0, int cnt,
+                                            int64_t N, int32_t *err) {
+    const int lane = threadIdx.x & 31;
+    int32_t j = -1;
+    if (lane < cnt) {
+        j = __ldg(ids + e0 + lane);
+        if ((uint32_t)j >= (uint32_t)N) {
+            atomicOr(err, kErrIndexRange);
+            j = -1;
+        }
+    }
+    return j;
+}
+
+// ------------------------------------------------------------------ forward
+
+template <typename T, int D, int NC, int G>
+__global__ void __launch_bounds__(256)
+gt_fwd_kernel(GtArgs a, float scale2) {
+    using S = GtShape<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
+    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemRange it;
+    if (!decode_item(item, a.rows, a.indptr, a.N, a.split_threshold, it)) return;
+    const int R = a.H * D / EL;
+    const uint4 *__restrict__ Qc = static_cast<const uint4 *>(a.Q);
+    const uint4 *__restrict__ Kc = static_cast<const uint4 *>(a.K);
+    const uint4 *__restrict__ Vc = static_cast<const uint4 *>(a.V);
+
+    float q[NC][EL], acc[NC][EL], m[NC], l[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c < R) unpack<T>(ldg16(Qc + (size_t)it.row * R + c), q[k]);
+        else
+#pragma unroll
+            for (int x = 0; x < EL; ++x) q[k][x] = 0.f;
+#pragma unroll
+        for (int x = 0; x < EL; ++x) acc[k][x] = 0.f;
+        m[k] = -INFINITY;
+        l[k] = 0.f;
+    }
+
+    for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+        const int cnt = min(32, it.end - e0);
+        const int32_t myj = load_ids(a.indices, e0, cnt, a.N, a.d_err);
+        for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+            uint4 kr[U][NC], vr[U][NC];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + g + NG * u;
+                const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
+                ok[u] = (t < cnt) && (j >= 0);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int c = gl + G * k;
+                    if (ok[u] && c < R) {
+                        kr[u][k] = ldg16_stream(Kc + (size_t)j * R + c);
+                        vr[u][k] = ldg16_stream(Vc + (size_t)j * R + c);
+                    } else {
+                        kr[u][k] = make_uint4(0, 0, 0, 0);
+                        vr[u][k] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+            float s[U][NC];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float kf[EL];
+                    unpack<T>(kr[u][k], kf);
+                    float dot = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) dot = fmaf(q[k][x], kf[x], dot);
+                    dot = group_sum<LH>(dot);
+                    s[u][k] = ok[u] ? dot * scale2 : -INFINITY;
+                }
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                float mx = m[k];
+#pragma unroll
+                for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][k]);
+                if (mx == -INFINITY) continue;
+                const float alpha = exp2_diff(m[k], mx);
+                l[k] *= alpha;
+#pragma unroll
+                for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float p = exp2_diff(s[u][k], mx);
+                    l[k] += p;
+                    float vf[EL];
+                    unpack<T>(vr[u][k], vf);
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, vf[x], acc[k][x]);
+                }
+                m[k] = mx;
+            }
+        }
+    }
+
+    // merge the edge groups of the warp (they saw disjoint edges)
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
+            const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
+            const float mx = fmaxf(m[k], mo);
+            const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
+            l[k] = l[k] * a1 + lo * a2;
+#pragma unroll
+            for (int x = 0; x < EL; ++x) {
+                const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
+                acc[k][x] = acc[k][x] * a1 + ao * a2;
+            }
+            m[k] = mx;
+        }
+    if (g != 0) return;
+
+    const int HD = a.H * D;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c >= R) continue;
+        const int h = c / LH;
+        if (it.partial) {
+            float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)item * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4)
+                dst[x / 4] = make_float4(acc[k][x], acc[k][x + 1], acc[k][x + 2], acc[k][x + 3]);
+            if (c % LH == 0) {
+                a.ws_ml[((size_t)item * a.H + h) * 2 + 0] = m[k];
+                a.ws_ml[((size_t)item * a.H + h) * 2 + 1] = l[k];
+            }
+        } else {
+            const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
+            float o[EL];
+#pragma unroll
+            for (int x = 0; x < EL; ++x) o[x] = acc[k][x] * inv;
+            reinterpret_cast<uint4 *>(a.out_w)[(size_t)it.row * R + c] = pack<T>(o);
+            if (c % LH == 0)
+                a.lse_w[(size_t)it.row * a.H + h] =
+                    l[k] > 0.f ? (m[k] + log2f(l[k])) * kLn2 : -INFINITY;
+        }
+    }
+}
+
+// Merge the chunk partials of each split row in chunk order:
+// M = max m_c, L = sum l_c 2^(m_c - M), acc = sum acc_c 2^(m_c - M).
+template <typename T, int D, typename A>
+__global__ void __launch_bounds__(256) gt_fwd_merge_kernel(A a) {
+    constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
+    const int lane = threadIdx.x & 31;
+    const int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (s >= a.rows.n_split) return;
+    const int32_t row = a.rows.split_rows[s];
+    const int32_t c0 = a.rows.chunk_ptr[s], c1 = a.rows.chunk_ptr[s + 1];
+    const int R = a.H * D / EL, HD = a.H * D;
+    for (int c = lane; c < R; c += 32) {
+        const int h = c / LH;
+        float M = -INFINITY;
+        for (int32_t ch = c0; ch < c1; ++ch) M = fmaxf(M, a.ws_ml[((size_t)ch * a.H + h) * 2]);
+        float L = 0.f, acc[EL];
+#pragma unroll
+        for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+        for (int32_t ch = c0; ch < c1; ++ch) {
+            const float w = exp2_diff(a.ws_ml[((size_t)ch * a.H + h) * 2], M);
+            L += a.ws_ml[((size_t)ch * a.H + h) * 2 + 1] * w;
+            const float4 *src = reinterpret_cast<const float4 *>(a.ws_acc + (size_t)ch * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4) {
+                const float4 v = src[x / 4];
+                acc[x] = fmaf(v.x, w, acc[x]);
+                acc[x + 1] = fmaf(v.y, w, acc[x + 1]);
+                acc[x + 2] = fmaf(v.z, w, acc[x + 2]);
+                acc[x + 3] = fmaf(v.w, w, acc[x + 3]);
+            }
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int x = 0; x < EL; ++x) acc[x] *= inv;
+        reinterpret_cast<uint4 *>(a.out_w)[(size_t)row * R + c] = pack<T>(acc);
+        if (c % LH == 0)
+            a.lse_w[(size_t)row * a.H + h] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+    }
+}
+
+// ---------------------------------------------------------- backward: dQ
+
+// Per destination row i: Delta_i = dOut_i . out_i (written for the dK/dV
+// pass), then for each edge p = 2^(s2 - lse2_i), dP = dOut_i . v_j,
+// dS = p (dP - Delta_i), dQ_i += dS k_j.  Split-row chunks write fp32
+// partial sums that the merge kernel adds in chunk order.
+template <typename T, int D, int NC, int G>
+__global__ void __launch_bounds__(256)
+gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
+    using S = GtShape<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
+    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemRange it;
+    if (!decode_item(item, a.rows, a.indptr, a.N, a.split_threshold, it)) return;
+    const int R = a.H * D / EL;
+    const uint4 *__restrict__ Kc = static_cast<const uint4 *>(a.K);
+    const uint4 *__restrict__ Vc = static_cast<const uint4 *>(a.V);
+
+    float q[NC][EL], go[NC][EL], dq[NC][EL], delta[NC], lse2[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        float o[EL];
+        if (c < R) {
+            const size_t off = (size_t)it.row * R + c;
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.Q) + off), q[k]);
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.out) + off), o);
+            lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + c / LH) * kLog2e;
+        } else {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) q[k][x] = go[k][x] = o[x] = 0.f;
+            lse2[k] = 0.f;
+        }
+        float d = 0.f;
+#pragma unroll
+        for (int x = 0; x < EL; ++x) {
+            d = fmaf(go[k][x], o[x], d);
+            dq[k][x] = 0.f;
+        }
+        delta[k] = group_sum<LH>(d);
+    }
+    if (g == 0 && (!it.partial || it.beg == a.indptr[it.row])) {
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+            const int c = gl + G * k;
+            if (c < R && c % LH == 0) a.ws_delta[(size_t)it.row * a.H + c / LH] = delta[k];
+        }
+    }
+
+    for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+        const int cnt = min(32, it.end - e0);
+        const int32_t myj = load_ids(a.indices, e0, cnt, a.N, a.d_err);
+        for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+            uint4 kr[U][NC], vr[U][NC];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + g + NG * u;
+                const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
+                ok[u] = (t < cnt) && (j >= 0);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int c = gl + G * k;
+                    if (ok[u] && c < R) {
+                        kr[u][k] = ldg16_stream(Kc + (size_t)j * R + c);
+                        vr[u][k] = ldg16_stream(Vc + (size_t)j * R + c);
+                    } else {
+                        kr[u][k] = make_uint4(0, 0, 0, 0);
+                        vr[u][k] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float kf[EL], vf[EL];
+                    unpack<T>(kr[u][k], kf);
+                    unpack<T>(vr[u][k], vf);
+                    float s = 0.f, dp = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        s = fmaf(q[k][x], kf[x], s);
+                        dp = fmaf(go[k][x], vf[x], dp);
+                    }
+                    group_sum2<LH>(s, dp);
+                    const float p = ok[u] ? exp2f(s * scale2 - lse2[k]) : 0.f;
+                    const float ds = p * (dp - delta[k]);
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) dq[k][x] = fmaf(ds, kf[x], dq[k][x]);
+                }
+        }
+    }
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+#pragma unroll
+            for (int x = 0; x < EL; ++x) dq[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dq[k][x], off);
+    if (g != 0) return;
+    const int HD = a.H * D;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c >= R) continue;
+        if (it.partial) {
+            float4 *dst = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4)
+                dst[x / 4] = make_float4(dq[k][x], dq[k][x + 1], dq[k][x + 2], dq[k][x + 3]);
+        } else {
+            float o[EL];
+#pragma unroll
+            for (int x = 0; x < EL; ++x) o[x] = dq[k][x] * scale;
+            reinterpret_cast<uint4 *>(a.dQ)[(size_t)it.row * R + c] = pack<T>(o);
+        }
+    }
+}
+
+// ------------------------------------------------------- backward: dK, dV
+
+// Per source j over its destinations i (transposed CSR):
+// p = 2^(s2 - lse2_i), dS = p (dOut_i . v_j - Delta_i),
+// dV_j += p dOut_i, dK_j += dS q_i.
+template <typename T, int D, int NC, int G>
+__global__ void __launch_bounds__(256)
+gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
+    using S = GtShape<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
+    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemRange it;
+    if (!decode_item(item, a.cols, a.t_indptr, a.N, a.split_threshold, it)) return;
+    const int R = a.H * D / EL;
+    const uint4 *__restrict__ Qc = static_cast<const uint4 *>(a.Q);
+    const uint4 *__restrict__ Gc = static_cast<const uint4 *>(a.dOut);
+
+    float kj[NC][EL], vj[NC][EL], dk[NC][EL], dv[NC][EL];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c < R) {
+            const size_t off = (size_t)it.row * R + c;
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.K) + off), kj[k]);
+            unpack<T>(ldg16(static_cast<const uint4 *>(a.V) + off), vj[k]);
+        } else {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) kj[k][x] = vj[k][x] = 0.f;
+        }
+#pragma unroll
+        for (int x = 0; x < EL; ++x) dk[k][x] = dv[k][x] = 0.f;
+    }
+
+    for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+        const int cnt = min(32, it.end - e0);
+        const int32_t myi = load_ids(a.t_dst, e0, cnt, a.N, a.d_err);
+        for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+            uint4 qr[U][NC], gr[U][NC];
+            float l2[U][NC], dl[U][NC];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int t = t0 + g + NG * u;
+                const int32_t i = __shfl_sync(SGA_FULL_MASK, myi, t & 31);
+                ok[u] = (t < cnt) && (i >= 0);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int c = gl + G * k;
+                    if (ok[u] && c < R) {
+                        qr[u][k] = ldg16_stream(Qc + (size_t)i * R + c);
+                        gr[u][k] = ldg16_stream(Gc + (size_t)i * R + c);
+                        l2[u][k] = __ldg(a.lse + (size_t)i * a.H + c / LH);
+                        dl[u][k] = a.ws_delta[(size_t)i * a.H + c / LH];
+                    } else {
+                        qr[u][k] = make_uint4(0, 0, 0, 0);
+                        gr[u][k] = make_uint4(0, 0, 0, 0);
+                        l2[u][k] = 0.f;
+                        dl[u][k] = 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float qf[EL], gf[EL];
+                    unpack<T>(qr[u][k], qf);
+                    unpack<T>(gr[u][k], gf);
+                    float s = 0.f, dp = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        s = fmaf(qf[x], kj[k][x], s);
+                        dp = fmaf(gf[x], vj[k][x], dp);
+                    }
+                    group_sum2<LH>(s, dp);
+                    const float p = ok[u] ? exp2f(s * scale2 - l2[u][k] * kLog2e) : 0.f;
+                    const float ds = p * (dp - dl[u][k]);
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        dv[k][x] = fmaf(p, gf[x], dv[k][x]);
+                        dk[k][x] = fmaf(ds, qf[x], dk[k][x]);
+                    }
+                }
+        }
+    }
+#pragma unroll
+    for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+#pragma unroll
+            for (int x = 0; x < EL; ++x) {
+                dk[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dk[k][x], off);
+                dv[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dv[k][x], off);
+            }
+    if (g != 0) return;
+    const int HD = a.H * D;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c >= R) continue;
+        if (it.partial) {
+            float4 *dk_dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * 2 * HD + c * EL);
+            float4 *dv_dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * 2 * HD + HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4) {
+                dk_dst[x / 4] = make_float4(dk[k][x], dk[k][x + 1], dk[k][x + 2], dk[k][x + 3]);
+                dv_dst[x / 4] = make_float4(dv[k][x], dv[k][x + 1], dv[k][x + 2], dv[k][x + 3]);
+            }
+        } else {
+            float o[EL];
+#pragma unroll
+            for (int x = 0; x < EL; ++x) o[x] = dk[k][x] * scale;
+            reinterpret_cast<uint4 *>(a.dK)[(size_t)it.row * R + c] = pack<T>(o);
+            reinterpret_cast<uint4 *>(a.dV)[(size_t)it.row * R + c] = pack<T>(dv[k]);
+        }
+    }
+}
+
+// Sum chunk partials in chunk order: items [0, rows.n_split) finish dQ,
+// items [rows.n_split, rows.n_split + cols.n_split) finish dK and dV.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) gt_bwd_merge_kernel(GtArgs a, float scale) {
+    constexpr int EL = Elt<T>::EL;
+    const int lane = threadIdx.x & 31;
+    int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int R = a.H * D / EL, HD = a.H * D;
+    if (s < a.rows.n_split) {
+        const int32_t row = a.rows.split_rows[s];
+        const int32_t c0 = a.rows.chunk_ptr[s], c1 = a.rows.chunk_ptr[s + 1];
+        for (int c = lane; c < R; c += 32) {
+            float acc[EL];
+#pragma unroll
+            for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+            for (int32_t ch = c0; ch < c1; ++ch) {
+                const float4 *src = reinterpret_cast<const float4 *>(a.ws_row + (size_t)ch * HD + c * EL);
+#pragma unroll
+                for (int x = 0; x < EL; x += 4) {
+                    const float4 v = src[x / 4];
+                    acc[x] += v.x; acc[x + 1] += v.y; acc[x + 2] += v.z; acc[x + 3] += v.w;
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < EL; ++x) acc[x] *= scale;
+            reinterpret_cast<uint4 *>(a.dQ)[(size_t)row * R + c] = pack<T>(acc);
+        }
+        return;
+    }
+    s -= a.rows.n_split;
+    if (s >= a.cols.n_split) return;
+    const int32_t row = a.cols.split_rows[s];
+    const int32_t c0 = a.cols.chunk_ptr[s], c1 = a.cols.chunk_ptr[s + 1];
+    for (int c = lane; c < R; c += 32) {
+        float gk[EL], gv[EL];
+#pragma unroll
+        for (int x = 0; x < EL; ++x) gk[x] = gv[x] = 0.f;
+        for (int32_t ch = c0; ch < c1; ++ch) {
+            const float4 *sk = reinterpret_cast<const float4 *>(a.ws_col + (size_t)ch * 2 * HD + c * EL);
+            const float4 *sv = reinterpret_cast<const float4 *>(a.ws_col + (size_t)ch * 2 * HD + HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4) {
+                const float4 u = sk[x / 4], v = sv[x / 4];
+                gk[x] += u.x; gk[x + 1] += u.y; gk[x + 2] += u.z; gk[x + 3] += u.w;
+                gv[x] += v.x; gv[x + 1] += v.y; gv[x + 2] += v.z; gv[x + 3] += v.w;
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < EL; ++x) gk[x] *= scale;
+        reinterpret_cast<uint4 *>(a.dK)[(size_t)row * R + c] = pack<T>(gk);
+        reinterpret_cast<uint4 *>(a.dV)[(size_t)row * R + c] = pack<T>(gv);
+    }
+}
+
+// ------------------------------------------------------------------ launch
+
+inline unsigned blocks_for_warps(int64_t warps) {
+    return (unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
+}
+
+// Calls F.template operator()<NC, G>() for the edge-group shape of a row of
+// R sixteen-byte chunks: G = 32 lanes and NC = ceil(R/32) chunks per lane,
+// or one chunk per lane in groups of G = next power of two >= R when R < 32.
+// Shapes a head of LH lanes cannot use (LH > G) or that exceed MAXNC chunks
+// per lane are never instantiated; R >= LH always holds at run time.
+template <int LH, int MAXNC, typename F> cudaError_t dispatch_shape(int R, F &&f) {
+    if (R > 64) {
+        if constexpr (MAXNC >= 8) {
+            if (R > 128) return f.template operator()<8, 32>();
+        }
+        return f.template operator()<4, 32>();
+    }
+    if (R > 32) return f.template operator()<2, 32>();
+    if constexpr (LH <= 16) {
+        if (R <= 16) {
+            if constexpr (LH <= 8) {
+                if (R <= 8) {
+                    if constexpr (LH <= 4) {
+                        if (R <= 4) return f.template operator()<1, 4>();
+                    }
+                    return f.template operator()<1, 8>();
+                }
+            }
+            return f.template operator()<1, 16>();
+        }
+    }
+    return f.template operator()<1, 32>();
+}
+
+template <typename T> constexpr int max_nc() { return sizeof(T) == 4 ? 8 : 4; }
+
+template <typename T, int D> cudaError_t gt_fwd_d(const GtArgs &a, cudaStream_t s) {
+    constexpr int LH = D * (int)sizeof(T) / 16;
+    const int R = a.H * D / Elt<T>::EL;
+    const float scale2 = kLog2e / sqrtf((float)D);
+    const int64_t items = (int64_t)a.rows.n_chunks + a.N;
+    cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
+        if (items == 0) return cudaSuccess;
+        note_launch(SGA_KERN_GT_FWD, s, false);
+        gt_fwd_kernel<T, D, NC, G><<<blocks_for_warps(items), 256, 0, s>>>(a, scale2);
+        note_launch(SGA_KERN_GT_FWD, s, true);
+        return cudaGetLastError();
+    });
+    if (e != cudaSuccess || a.rows.n_split == 0) return e;
+    note_launch(SGA_KERN_GT_FWD_MERGE, s, false);
+    gt_fwd_merge_kernel<T, D, GtArgs><<<blocks_for_warps(a.rows.n_split), 256, 0, s>>>(a);
+    note_launch(SGA_KERN_GT_FWD_MERGE, s, true);
+    return cudaGetLastError();
+}
+
+template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t s) {
+    constexpr int LH = D * (int)sizeof(T) / 16;
+    const int R = a.H * D / Elt<T>::EL;
+    const float scale = 1.0f / sqrtf((float)D);
+    const float scale2 = kLog2e * scale;
+    return dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
+        const int64_t items_r = (int64_t)a.rows.n_chunks + a.N;
+        const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
+        if (items_r > 0) {
+            note_launch(SGA_KERN_GT_BWD_DQ, s, false);
+            gt_bwd_dq_kernel<T, D, NC, G><<<blocks_for_warps(items_r), 256, 0, s>>>(a, scale2, scale);
+            note_launch(SGA_KERN_GT_BWD_DQ, s, true);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            note_launch(SGA_KERN_GT_BWD_DKDV, s, false);
+            gt_bwd_dkdv_kernel<T, D, NC, G><<<blocks_for_warps(items_c), 256, 0, s>>>(a, scale2, scale);
+            note_launch(SGA_KERN_GT_BWD_DKDV, s, true);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        const int64_t merges = (int64_t)a.rows.n_split + a.cols.n_split;
+        if (merges == 0) return cudaSuccess;
+        note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
+        gt_bwd_merge_kernel<T, D><<<blocks_for_warps(merges), 256, 0, s>>>(a, scale);
+        note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
+        return cudaGetLastError();
+    });
+}
+
+template <typename T> cudaError_t gt_fwd_t(const GtArgs &a, cudaStream_t s) {
+    switch (a.D) {
+        case 32: return gt_fwd_d<T, 32>(a, s);
+        case 64: return gt_fwd_d<T, 64>(a, s);
+        case 128: return gt_fwd_d<T, 128>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T> cudaError_t gt_bwd_t(const GtArgs &a, cudaStream_t s) {
+    switch (a.D) {
+        case 32: return gt_bwd_d<T, 32>(a, s);
+        case 64: return gt_bwd_d<T, 64>(a, s);
+        case 128: return gt_bwd_d<T, 128>(a, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sga

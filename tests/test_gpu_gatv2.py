@@ -1,0 +1,76 @@
+"""GATv2 CUDA path vs the fp64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_graph_attention_csr_gb300 as sga
+from sparse_graph_attention_csr_gb300 import synth
+
+from helpers import TORCH_DT, compare, dev
+from test_gpu_gt import csr, random_csr
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gatv2(indptr, indices, F, H, D, dtype, seed=0, split=0, chunk=0, slope=0.2):
+    rng = np.random.default_rng(seed)
+    N = len(indptr) - 1
+    lim = math.sqrt(6.0 / (F + H * D))
+
+    def rt(x):
+        t = torch.from_numpy(x.astype(np.float32)).to(TORCH_DT[dtype])
+        return t, t.to(torch.float64).numpy()
+
+    X = rt(rng.standard_normal((N, F)))
+    Wl = rt(rng.uniform(-lim, lim, (F, H * D)))
+    Wr = rt(rng.uniform(-lim, lim, (F, H * D)))
+    a = rt(rng.standard_normal((H, D)) * 0.1)
+    dO = rt(rng.standard_normal((N, H, D)))
+    return check(indptr, indices, F, H, D, dtype, X, Wl, Wr, a, dO, split, chunk, slope)
+
+
+def check(indptr, indices, F, H, D, dtype, X, Wl, Wr, a, dO, split=0, chunk=0, slope=0.2):
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, TORCH_DT[dtype], F=F, split_threshold=split, chunk_len=chunk)
+    gX, gWl, gWr, ga, gdO = (dev(t[0]) for t in (X, Wl, Wr, a, dO))
+    FL, FR, out, lse = sga.gatv2_fwd(plan, gX, gWl, gWr, ga, slope)
+    rFL, rFR, rout, rlse = oracle.gatv2_fwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], slope)
+    compare(FL, rFL, dtype, "FL")
+    compare(FR, rFR, dtype, "FR")
+    compare(out, rout, dtype, "out")
+    compare(lse, rlse, dtype, "lse")
+    dX, dWl, dWr, da = sga.gatv2_bwd(plan, gX, gWl, gWr, ga, FL, FR, out, lse, gdO, slope)
+    g = oracle.gatv2_bwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope)
+    compare(dX, g["dX"], dtype, "dX")
+    compare(dWl, g["dW_l"], dtype, "dW_l")
+    compare(dWr, g["dW_r"], dtype, "dW_r")
+    compare(da, g["da"], dtype, "da")
+    assert plan.device_error() == 0
+    return plan
+
+
+def test_small_workload_matches_oracle():
+    w = synth.small_workload(2)
+    indptr, indices = synth.make_graph(w)
+    x = synth.gatv2_inputs(w)
+    check(indptr, indices, w.F, w.H, w.D, w.dtype, x["X"], x["W_l"], x["W_r"], x["a"], x["dOut"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("F,H,D", [(128, 2, 64), (64, 1, 32), (40, 4, 32), (16, 1, 128),
+                                   (256, 8, 128)])
+def test_shapes_and_split_rows(dtype, F, H, D):
+    rng = np.random.default_rng(F + H + D)
+    indptr, indices = random_csr(rng, 400, 7, hubs=[(3, 300), (399, 90)])
+    run_gatv2(indptr, indices, F, H, D, dtype, seed=F * H, split=50, chunk=24)
+
+
+def test_edge_cases():
+    rows = [[], [3], [0, 0, 2], [], [1, 2, 3, 4], [4], [], [0, 1, 1, 1, 6]]
+    indptr, indices = csr(rows)
+    run_gatv2(indptr, indices, 8, 2, 32, "f32", split=2, chunk=1)
+    run_gatv2(indptr, indices, 8, 2, 32, "bf16")
+    run_gatv2(np.zeros(4, np.int32), np.zeros(0, np.int32), 16, 1, 32, "f32")
