@@ -74,10 +74,11 @@ def _load():
             "oracle_gatv2_fwd_rows": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P,
                                        _dbl, _i64, _I64P, _F64P, _F64P], _int),
             "oracle_gatv2_fwd": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P, _F64P,
-                                  _F64P, _dbl, _F64P, _F64P, _F64P, _F64P], _int),
+                                  _F64P, _dbl, _int, _F64P, _F64P, _F64P, _F64P], _int),
             "oracle_gatv2_bwd": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P, _F64P,
-                                  _F64P, _dbl, _F64P, _F64P, _F64P, _F64P, _F64P, _F64P,
+                                  _F64P, _dbl, _int, _F64P, _F64P, _F64P, _F64P, _F64P, _F64P,
                                   _F64P], _int),
+            "oracle_round_bf16": ([_dbl], _dbl),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -210,8 +211,18 @@ def matmul(X, W):
     return Y
 
 
-def gatv2_fwd(indptr, indices, X, Wl, Wr, a, slope=0.2):
-    """(FL, FR, out, lse): projections [N, H, D], output [N, H, D], lse [N, H]."""
+_STORE = {None: 0, "f64": 0, "f32": 1, "bf16": 2}
+
+
+def round_bf16(x: float) -> float:
+    """Nearest bfloat16 (ties to even) of a double, via float."""
+    return _load().oracle_round_bf16(float(x))
+
+
+def gatv2_fwd(indptr, indices, X, Wl, Wr, a, slope=0.2, store=None):
+    """(FL, FR, out, lse): projections [N, H, D], output [N, H, D], lse [N, H].
+    ``store`` ("f32" or "bf16") rounds the projections to the layer's storage
+    dtype before the edge stage, as the layer stores them; None keeps fp64."""
     indptr, indices = _i32(indptr), _i32(indices)
     X, Wl, Wr, a = _f64(X), _f64(Wl), _f64(Wr), _f64(a)
     N, F = X.shape
@@ -219,7 +230,7 @@ def gatv2_fwd(indptr, indices, X, Wl, Wr, a, slope=0.2):
     FL = np.empty((N, H, D)); FR = np.empty((N, H, D))
     out = np.empty((N, H, D)); lse = np.empty((N, H))
     _check(_load().oracle_gatv2_fwd(N, F, H, D, indptr, indices, X, Wl, Wr, a, float(slope),
-                                    FL, FR, out, lse), "gatv2_fwd")
+                                    _STORE[store], FL, FR, out, lse), "gatv2_fwd")
     return FL, FR, out, lse
 
 
@@ -234,14 +245,15 @@ def gatv2_fwd_rows(indptr, indices, FL, FR, a, rows, slope=0.2):
     return out, lse
 
 
-def gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, slope=0.2):
-    """dict with dX [N, F], dW_l, dW_r [F, H*D], da [H, D], dFL, dFR [N, H, D]."""
+def gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, slope=0.2, store=None):
+    """dict with dX [N, F], dW_l, dW_r [F, H*D], da [H, D], dFL, dFR [N, H, D].
+    ``store`` as in gatv2_fwd."""
     indptr, indices = _i32(indptr), _i32(indices)
     X, Wl, Wr, a, dO = _f64(X), _f64(Wl), _f64(Wr), _f64(a), _f64(dO)
     N, F = X.shape
     H, D = a.shape
     dX = np.empty((N, F)); dWl = np.empty((F, H * D)); dWr = np.empty((F, H * D))
     da = np.empty((H, D)); dFL = np.empty((N, H, D)); dFR = np.empty((N, H, D))
-    _check(_load().oracle_gatv2_bwd(N, F, H, D, indptr, indices, X, Wl, Wr, a, float(slope), dO,
-                                    dX, dWl, dWr, da, dFL, dFR), "gatv2_bwd")
+    _check(_load().oracle_gatv2_bwd(N, F, H, D, indptr, indices, X, Wl, Wr, a, float(slope),
+                                    _STORE[store], dO, dX, dWl, dWr, da, dFL, dFR), "gatv2_bwd")
     return {"dX": dX, "dW_l": dWl, "dW_r": dWr, "da": da, "dFL": dFL, "dFR": dFR}

@@ -29,7 +29,9 @@
  *    out = 0 and lse = -inf and contributes to no gradient.
  *  - GATv2: W_l multiplies the destination features, W_r the source features;
  *    the aggregated value is the source projection FR_j = x_j W_r.
- *    LeakyReLU'(0) is taken as the negative slope.
+ *    LeakyReLU'(0) is taken as the negative slope.  The projections are layer
+ *    outputs stored in the layer's dtype; the `store` argument rounds them
+ *    the same way before the edge stage uses them.
  *
  * Parallelism: OpenMP over independent rows (or sources); each output element
  * is produced by one thread in a fixed order, so results do not depend on the
@@ -375,6 +377,32 @@ int oracle_gt_bwd(int64_t N, const int32_t *indptr, const int32_t *indices, int 
 static inline double lrelu(double z, double slope) { return z > 0.0 ? z : slope * z; }
 static inline double lrelu_grad(double z, double slope) { return z > 0.0 ? 1.0 : slope; }
 
+/* Round a double to the nearest bfloat16 (ties to even), returned as a
+ * double: first to float (the projections are accumulated to a float), then
+ * the float's 32-bit pattern to its upper 16 bits with round-half-even. */
+double oracle_round_bf16(double x) {
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, sizeof(u));
+    if ((u & 0x7f800000u) != 0x7f800000u) {  /* finite */
+        u += 0x7fffu + ((u >> 16) & 1u);
+        u &= 0xffff0000u;
+    }
+    memcpy(&f, &u, sizeof(f));
+    return (double)f;
+}
+
+/* Storage rounding of the GATv2 projections: 0 keeps doubles, 1 rounds to
+ * float, 2 to bfloat16.  The layer stores FL and FR in its tensor dtype and
+ * the edge stage (forward and backward) consumes the stored values, so the
+ * LeakyReLU branch is decided on the same numbers the kernels see. */
+static void round_storage(int64_t n, double *x, int mode) {
+    if (mode == 1)
+        for (int64_t t = 0; t < n; ++t) x[t] = (double)(float)x[t];
+    else if (mode == 2)
+        for (int64_t t = 0; t < n; ++t) x[t] = oracle_round_bf16(x[t]);
+}
+
 /* Y[n, c] = sum_f X[n, f] W[f, c]   (X [N, F], W [F, C], Y [N, C]) */
 int oracle_matmul(int64_t N, int F, int C, const double *X, const double *W, double *Y) {
 #pragma omp parallel for schedule(static)
@@ -443,13 +471,16 @@ int oracle_gatv2_fwd_rows(int64_t N, const int32_t *indptr, const int32_t *indic
     return err;
 }
 
-/* Full GATv2 layer forward from X: FL = X W_l, FR = X W_r, then the edge stage. */
+/* Full GATv2 layer forward from X: FL = X W_l, FR = X W_r (stored with the
+ * rounding `store`, see round_storage), then the edge stage. */
 int oracle_gatv2_fwd(int64_t N, int F, int H, int D, const int32_t *indptr, const int32_t *indices,
                      const double *X, const double *Wl, const double *Wr, const double *a,
-                     double slope, double *FL, double *FR, double *out, double *lse) {
+                     double slope, int store, double *FL, double *FR, double *out, double *lse) {
     int HD = H * D;
     oracle_matmul(N, F, HD, X, Wl, FL);
     oracle_matmul(N, F, HD, X, Wr, FR);
+    round_storage(N * HD, FL, store);
+    round_storage(N * HD, FR, store);
     int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     if (!rows) return -1;
     for (int64_t i = 0; i < N; ++i) rows[i] = i;
@@ -483,13 +514,15 @@ static void gatv2_row_grad(int64_t i, int h, int H, int D, const int32_t *indptr
 /* Full GATv2 backward by the chain rule:
  *   out_i = sum_j p_ij FR_j,  p = softmax_j(e_ij),  e_ij = sum_d a_d LReLU(z_ijd),
  *   z_ij = FL_i + FR_j,  FL = X W_l,  FR = X W_r.
+ * The rounding of the stored projections is treated as the identity in the
+ * gradient (the projections' gradients pass straight to X, W_l, W_r).
  * Outputs dX [N, F], dWl, dWr [F, H*D], da [H, D], and the intermediate
  * dFL, dFR [N, H, D] (for inspection).  dFR_j gathers p_ij dO_i (value path)
  * plus dz_ij (score path) over the destinations of j in ascending order. */
 int oracle_gatv2_bwd(int64_t N, int F, int H, int D, const int32_t *indptr, const int32_t *indices,
                      const double *X, const double *Wl, const double *Wr, const double *a,
-                     double slope, const double *dO, double *dX, double *dWl, double *dWr,
-                     double *da, double *dFL, double *dFR) {
+                     double slope, int store, const double *dO, double *dX, double *dWl,
+                     double *dWr, double *da, double *dFL, double *dFR) {
     int HD = H * D;
     int64_t E = indptr[N];
     int64_t md = max_degree(N, indptr);
@@ -504,6 +537,8 @@ int oracle_gatv2_bwd(int64_t N, int F, int H, int D, const int32_t *indptr, cons
     if (!err) {
         oracle_matmul(N, F, HD, X, Wl, FL);
         oracle_matmul(N, F, HD, X, Wr, FR);
+        round_storage(N * HD, FL, store);
+        round_storage(N * HD, FR, store);
 #pragma omp parallel
         {
             double *s = (double *)malloc(sizeof(double) * (size_t)(md + 1));

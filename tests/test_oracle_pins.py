@@ -343,3 +343,35 @@ def test_partition_definition():
         assert np.all(p["chunk_beg"][c0 + 1:c1] == p["chunk_end"][c0:c1 - 1])
         assert np.all(p["chunk_end"][c0:c1] - p["chunk_beg"][c0:c1] <= 32)
         assert np.all(p["chunk_row"][c0:c1] == i)
+
+
+# ------------------------------------------------- storage rounding (GATv2)
+
+def test_round_bf16_matches_torch_conversion():
+    """The oracle's bfloat16 rounding (via float, ties to even) equals torch's
+    float32 -> bfloat16 conversion, including exact ties and subnormals."""
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.standard_normal(2000).astype(np.float32),
+                        (rng.standard_normal(500) * 1e-39).astype(np.float32),
+                        np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), 0.0, -0.0,
+                                  3.0e38], np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.round_bf16(float(v)) for v in x])
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_gatv2_stored_projection_rounding():
+    """store='bf16' is the edge stage run on bf16-rounded projections."""
+    rng = np.random.default_rng(22)
+    N, F, H, D = 25, 6, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.3)
+    X = rng.standard_normal((N, F)); Wl = rng.standard_normal((F, H * D))
+    Wr = rng.standard_normal((F, H * D)); a = rng.standard_normal((H, D))
+    FL, FR, out, lse = oracle.gatv2_fwd(indptr, indices, X, Wl, Wr, a, 0.2, store="bf16")
+    rl = torch.from_numpy(X @ Wl).float().to(torch.bfloat16).double().numpy().reshape(N, H, D)
+    rr = torch.from_numpy(X @ Wr).float().to(torch.bfloat16).double().numpy().reshape(N, H, D)
+    np.testing.assert_array_equal(FL, rl)
+    np.testing.assert_array_equal(FR, rr)
+    o2, l2 = oracle.gatv2_fwd_rows(indptr, indices, rl, rr, a, np.arange(N))
+    np.testing.assert_array_equal(out, o2)
+    np.testing.assert_array_equal(lse, l2)
