@@ -1,0 +1,561 @@
+#!/usr/bin/env python
+"""Benchmark of the fused CSR edge-attention layer (forward + backward).
+
+Default workload: the GATv2 layer on a Chung-Lu power-law graph (N=100k,
+~1.68M edges with self-loops, H=2, D=64, F=128, bf16).  ``--config k`` runs
+one of the other synthetic workloads (1: GT forward fp32 ER; 3: GT lognormal;
+4: GT R-MAT super nodes; 5: GT block-dense SBM).
+
+One step = forward + backward of the layer (forward only for workload 1) over
+the whole graph, inputs resident on the device, L2 flushed (a write of twice
+the L2 size) before every step and outside its timed interval.  The metric is
+edge.heads per second (E counts self-loops) in units of 1e9.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+instead (host cores, bounded row samples of the same workload).
+
+Multi-GPU: the layer is one problem per graph; ``--gpus N`` under torchrun
+runs N independent replicas (weak scaling), timed between barriers, max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_graph_attention_csr_gb300 import synth  # noqa: E402
+
+METRIC = "fused GT/GATv2 fwd+bwd edge·heads/sec (G/s)"
+UNIT = "G edge·heads/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+GT_KERNELS = ["gt_fwd", "gt_fwd_merge", "gt_bwd_dq", "gt_bwd_dkdv", "gt_bwd_merge"]
+GATV2_KERNELS = ["gatv2_proj", "gatv2_fwd", "gatv2_fwd_merge", "gatv2_bwd_dst", "gatv2_bwd_src",
+                 "gatv2_bwd_merge", "gatv2_bwd_dx", "gatv2_bwd_dw", "gatv2_bwd_reduce"]
+
+
+# --------------------------------------------------------------------------- args
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["native", "reference"], default="native")
+    p.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0,
+                   help="target CPU time of the oracle baseline sample")
+    p.add_argument("--split-threshold", type=int, default=0)
+    p.add_argument("--chunk-len", type=int, default=0)
+    p.add_argument("--json-out", default="")
+    return p.parse_args(argv)
+
+
+# ------------------------------------------------------------------ distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- byte models
+
+def algorithmic_bytes(kernel: str, N: int, E: int, H: int, D: int, F: int, s: int) -> int:
+    """Compulsory bytes of one launch: index arrays, each node's own rows once,
+    every gathered neighbour row once per edge, outputs once (fp32 lse/Delta)."""
+    HD = H * D
+    ptr, idx = 4 * (N + 1), 4 * E
+    row = N * HD * s
+    if kernel == "gt_fwd":
+        return ptr + idx + row + E * 2 * HD * s + row + 4 * N * H
+    if kernel == "gt_bwd_dq":
+        return ptr + idx + 2 * row + 4 * N * H + E * 2 * HD * s + row + 4 * N * H
+    if kernel == "gt_bwd_dkdv":
+        return ptr + idx + 2 * row + E * (2 * HD * s + 8 * H) + 2 * row
+    if kernel == "gatv2_fwd":
+        return ptr + idx + row + E * HD * s + row + 4 * N * H
+    if kernel == "gatv2_bwd_dst":
+        return ptr + idx + 2 * row + 4 * N * H + E * HD * s + row + 4 * N * H
+    if kernel == "gatv2_bwd_src":
+        return ptr + idx + row + E * (2 * HD * s + 8 * H) + row
+    if kernel == "gatv2_proj":
+        return N * F * s + F * HD * s + row
+    if kernel == "gatv2_bwd_dx":
+        return 2 * row + 2 * F * HD * s + N * F * s
+    if kernel == "gatv2_bwd_dw":
+        return N * F * s + row
+    return 0
+
+
+def kernel_flops(kernel: str, N: int, H: int, D: int, F: int) -> int:
+    HD = H * D
+    if kernel == "gatv2_proj" or kernel == "gatv2_bwd_dw":
+        return 2 * N * F * HD
+    if kernel == "gatv2_bwd_dx":
+        return 2 * 2 * N * HD * F
+    return 0
+
+
+def measured_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_graph_attention_csr_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, only if it was
+    taken on the current kernel sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    e = t.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------- workload
+
+class Workload:
+    """Host inputs (pinned), device inputs, plan and step functions."""
+
+    def __init__(self, key: int, device, split_threshold=0, chunk_len=0):
+        import sparse_graph_attention_csr_gb300 as sga
+        self.sga = sga
+        self.w = synth.WORKLOADS[key]
+        w = self.w
+        self.device = device
+        self.indptr, self.indices = synth.make_graph(w)
+        self.N, self.E = w.N, int(self.indptr[-1])
+        self.units = self.E * w.H
+        self.tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+        self.s = 4 if w.dtype == "f32" else 2
+        if w.layer == "gt":
+            x = synth.gt_inputs(w)
+            if not w.backward:
+                x["dOut"] = synth.round_to(synth.normal(w.seed, synth.STREAM_DOUT, (w.N, w.H, w.D)),
+                                           w.dtype)
+            self.in_names = ["Q", "K", "V"] + (["dOut"] if w.backward else [])
+        else:
+            x = synth.gatv2_inputs(w)
+            self.in_names = ["X", "W_l", "W_r", "a", "dOut"]
+        self.host64 = {k: v[1] for k, v in x.items()}
+        self.host = {k: x[k][0].pin_memory() if torch.cuda.is_available() else x[k][0]
+                     for k in self.in_names}
+        self.dev = {k: self.host[k].to(device) for k in self.in_names}
+        self.ip = torch.from_numpy(self.indptr).to(device)
+        self.ix = torch.from_numpy(self.indices).to(device)
+        F = w.F if w.layer == "gatv2" else 0
+        t0 = time.perf_counter()
+        self.plan = sga.Plan(self.ip, self.ix, w.H, w.D, self.tdt, F=F,
+                             split_threshold=split_threshold, chunk_len=chunk_len)
+        torch.cuda.synchronize()
+        self.plan_ms = (time.perf_counter() - t0) * 1e3
+        self.outputs = None
+
+    @property
+    def kernels(self):
+        return GT_KERNELS if self.w.layer == "gt" else GATV2_KERNELS
+
+    def step(self, d=None):
+        """One forward(+backward) pass on device tensors d; returns the outputs."""
+        sga, w = self.sga, self.w
+        d = self.dev if d is None else d
+        if w.layer == "gt":
+            out, lse = sga.gt_attn_fwd(self.plan, d["Q"], d["K"], d["V"])
+            if not w.backward:
+                return {"out": out, "lse": lse}
+            dQ, dK, dV = sga.gt_attn_bwd(self.plan, d["Q"], d["K"], d["V"], out, lse, d["dOut"])
+            return {"out": out, "lse": lse, "dQ": dQ, "dK": dK, "dV": dV}
+        FL, FR, out, lse = sga.gatv2_fwd(self.plan, d["X"], d["W_l"], d["W_r"], d["a"], 0.2)
+        dX, dWl, dWr, da = sga.gatv2_bwd(self.plan, d["X"], d["W_l"], d["W_r"], d["a"], FL, FR,
+                                         out, lse, d["dOut"], 0.2)
+        return {"out": out, "lse": lse, "dX": dX, "dW_l": dWl, "dW_r": dWr, "da": da}
+
+
+# --------------------------------------------------------------- CPU oracle leg
+
+def row_sample(indptr, indices, n_rows, rng):
+    """Random destination rows with their full edge lists, relabelled onto the
+    nodes they touch.  Returns (indptr, indices, node_ids, n_rows)."""
+    N = len(indptr) - 1
+    rows = np.sort(rng.choice(N, size=min(n_rows, N), replace=False))
+    deg = np.diff(indptr.astype(np.int64))[rows]
+    srcs = np.concatenate([indices[indptr[r]:indptr[r + 1]] for r in rows]) if len(rows) else \
+        np.zeros(0, np.int32)
+    nodes = np.unique(np.concatenate([rows, srcs]))
+    remap = {int(v): i for i, v in enumerate(nodes)}
+    new_ptr = np.zeros(len(nodes) + 1, np.int64)
+    row_pos = np.searchsorted(nodes, rows)
+    counts = np.zeros(len(nodes), np.int64)
+    counts[row_pos] = deg
+    new_ptr[1:] = np.cumsum(counts)
+    new_idx = np.empty(int(new_ptr[-1]), np.int32)
+    for r, p in zip(rows, row_pos):
+        seg = indices[indptr[r]:indptr[r + 1]]
+        new_idx[new_ptr[p]:new_ptr[p + 1]] = np.searchsorted(nodes, seg)
+    del remap
+    return new_ptr.astype(np.int32), new_idx, nodes, len(rows)
+
+
+def oracle_step(wl: synth.Workload, host64, ptr, idx, nodes):
+    """The oracle's forward(+backward) of the workload's layer on a (sub)graph."""
+    import oracle
+    if wl.layer == "gt":
+        Q, K, V = (host64[k][nodes] for k in ("Q", "K", "V"))
+        oracle.gt_fwd(ptr, idx, Q, K, V)
+        if wl.backward:
+            oracle.gt_bwd(ptr, idx, Q, K, V, host64["dOut"][nodes])
+    else:
+        X = host64["X"][nodes]
+        store = wl.dtype
+        oracle.gatv2_fwd(ptr, idx, X, host64["W_l"], host64["W_r"], host64["a"], 0.2, store=store)
+        oracle.gatv2_bwd(ptr, idx, X, host64["W_l"], host64["W_r"], host64["a"],
+                         host64["dOut"][nodes], 0.2, store=store)
+
+
+def calibrate_sample(wl, host64, indptr, indices, target_s, rng):
+    """Grow a row sample until one oracle step costs about target_s seconds."""
+    N = len(indptr) - 1
+    n = min(N, 2000)
+    while True:
+        ptr, idx, nodes, nr = row_sample(indptr, indices, n, rng)
+        t0 = time.perf_counter()
+        oracle_step(wl, host64, ptr, idx, nodes)
+        dt = time.perf_counter() - t0
+        if n >= N or dt >= 0.25 * target_s:
+            scale = target_s / max(dt, 1e-3)
+            n2 = int(min(N, max(n, n * scale)))
+            if n2 <= n * 1.2 or n >= N:
+                return ptr, idx, nodes, nr, dt
+            n = n2
+            ptr, idx, nodes, nr = row_sample(indptr, indices, n, rng)
+            t0 = time.perf_counter()
+            oracle_step(wl, host64, ptr, idx, nodes)
+            return ptr, idx, nodes, nr, time.perf_counter() - t0
+        n = min(N, n * 4)
+
+
+def cpu_baseline(wl, host64, indptr, indices, target_s):
+    import oracle
+    rng = np.random.default_rng(1234)
+    ptr, idx, nodes, nr, _ = calibrate_sample(wl, host64, indptr, indices, target_s / 2, rng)
+    t0 = time.perf_counter()
+    oracle_step(wl, host64, ptr, idx, nodes)
+    dt = time.perf_counter() - t0
+    units = int(ptr[-1]) * wl.H
+    return {"value": units / dt / 1e9, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{nr} random destination rows of {len(indptr) - 1} with their full edge "
+                      f"lists ({int(ptr[-1])} of {int(indptr[-1])} edges), fp64 forward"
+                      f"{'+backward' if wl.backward else ''}, one timed pass of {dt:.2f} s"}
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the fp64 CPU oracle on bounded row samples."""
+    if rank != 0:
+        return
+    import oracle
+    wl = synth.WORKLOADS[args.config]
+    indptr, indices = synth.make_graph(wl)
+    x = synth.gt_inputs(wl) if wl.layer == "gt" else synth.gatv2_inputs(wl)
+    host64 = {k: v[1] for k, v in x.items()}
+    if wl.layer == "gt" and not wl.backward:
+        host64["dOut"] = np.zeros((wl.N, wl.H, wl.D))
+    budget = 150.0
+    per_step = budget / max(1, args.steps + args.warmup)
+    rng = np.random.default_rng(99)
+    ptr, idx, nodes, nr, _ = calibrate_sample(wl, host64, indptr, indices, per_step, rng)
+    samples = []
+    for s in range(args.warmup + args.steps):
+        sp = row_sample(indptr, indices, nr, np.random.default_rng(1000 + s))
+        samples.append(sp)
+    for s in range(args.warmup):
+        oracle_step(wl, host64, samples[s][0], samples[s][1], samples[s][2])
+    t_total, units = 0.0, 0
+    for s in range(args.warmup, args.warmup + args.steps):
+        ptr, idx, nodes, _ = samples[s]
+        t0 = time.perf_counter()
+        oracle_step(wl, host64, ptr, idx, nodes)
+        t_total += time.perf_counter() - t0
+        units += int(ptr[-1]) * wl.H
+    value = units / t_total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "N": wl.N, "E": int(indptr[-1]), "H": wl.H, "D": wl.D,
+                   "F": wl.F, "graph": wl.graph, "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                         "sample": f"per step {nr} random destination rows with their full edge "
+                                   f"lists (about {int(samples[0][0][-1])} edges)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- native arm
+
+def run_native(args, ws, rank, local):
+    import sparse_graph_attention_csr_gb300 as sga
+    from sparse_graph_attention_csr_gb300 import build as sga_build
+    sga_build.build()
+    dev = torch.device("cuda", local)
+    wl = Workload(args.config, dev, args.split_threshold, args.chunk_len)
+    w = wl.w
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    # warm-up, then one profiled step per kernel kind to find the dominant one
+    for _ in range(args.warmup):
+        flush.zero_()
+        wl.step()
+    torch.cuda.synchronize()
+    per_kernel = {}
+    for k in wl.kernels:
+        flush.zero_()
+        sga.profile_start(k)
+        wl.step()
+        ms, n = sga.profile_stop()
+        if n:
+            per_kernel[k] = (ms, n)
+    dominant = max(per_kernel, key=lambda k: per_kernel[k][0])
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize()
+    launches0 = sga.launch_count()
+    sga.profile_start(dominant)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        wl.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(ws)
+    launches = sga.launch_count() - launches0
+    dom_ms, dom_n = sga.profile_stop()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    t_ms = max_over_ranks(sum(step_ms), ws, dev)
+    value = ws * wl.units * args.steps / (t_ms / 1e3) / 1e9
+
+    # roofline of the dominant kernel
+    peaks, peak_kind = measured_peaks()
+    F = w.F if w.layer == "gatv2" else 0
+    avg_ms = dom_ms / max(dom_n, 1)
+    flops = kernel_flops(dominant, wl.N, w.H, w.D, F)
+    if flops and dominant in ("gatv2_proj", "gatv2_bwd_dx", "gatv2_bwd_dw"):
+        ach = flops / (avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"]}
+    else:
+        nbytes = algorithmic_bytes(dominant, wl.N, wl.E, w.H, w.D, F, wl.s)
+        ach = nbytes / (avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes}
+    roof.update({"kernel": dominant, "launches": dom_n, "avg_launch_ms": avg_ms,
+                 "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json' if peak_kind == 'measured' else '6.8 TB/s, 1.9 PFLOP/s'})",
+                 "traffic": traffic_for(dominant, w.name)})
+
+    # end to end: pinned host inputs -> device, layer, outputs -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        outs = wl.step()
+        host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        d_in = {k: torch.empty_like(v) for k, v in wl.dev.items()}
+        h2d = sum(t.numel() * t.element_size() for t in wl.host.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        for _ in range(2):
+            for k in wl.in_names:
+                d_in[k].copy_(wl.host[k], non_blocking=True)
+            o = wl.step(d_in)
+            for k in host_out:
+                host_out[k].copy_(o[k], non_blocking=True)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e_ms = 0.0
+        for _ in range(args.steps):
+            flush.zero_()
+            e0.record(stream)
+            for k in wl.in_names:
+                d_in[k].copy_(wl.host[k], non_blocking=True)
+            o = wl.step(d_in)
+            for k in host_out:
+                host_out[k].copy_(o[k], non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            e_ms += e0.elapsed_time(e1)
+        e_ms = max_over_ranks(e_ms, ws, dev)
+        e2e = {"value": ws * wl.units * args.steps / (e_ms / 1e3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, wl.host64, wl.indptr, wl.indices, args.cpu_seconds)
+
+    deg = synth.degree_summary(wl.indptr)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "layer": w.layer, "graph": w.graph, "N": wl.N, "E": wl.E,
+                   "H": w.H, "D": w.D, "F": F, "max_degree": deg["max"],
+                   "pass": "fwd+bwd" if w.backward else "fwd",
+                   "l2": "flushed before every step (write of 2x L2), outside the timed interval",
+                   "parallelism": f"replicas x{ws}",
+                   "plan_build_ms": round(wl.plan_ms, 2)},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+        "kernel_ms_one_step": {k: round(v[0], 4) for k, v in per_kernel.items()},
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                json.dump(line, f, indent=1)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_native(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -51,7 +51,8 @@ void compute_layout(sga_plan *p) {
     L.delta = take((size_t)p->N * p->H * 4);
     L.fwd_ml = take((size_t)p->rows.n_chunks * p->H * 2 * 4);
     L.fwd_acc = take((size_t)p->rows.n_chunks * HD * 4);
-    L.bwd_row = take((size_t)p->rows.n_chunks * HD * 4);
+    L.bwd_row = take((size_t)p->rows.n_chunks * (p->F > 0 ? 4 : 2) * HD * 4);
+    L.bwd_rowc = take((size_t)p->rows.n_chunks * p->H * 4);
     L.bwd_col = take((size_t)p->cols.n_chunks * 2 * HD * 4);
     if (p->F > 0) {
         L.da_blocks = da_blocks_for(p->num_sms);
@@ -59,6 +60,7 @@ void compute_layout(sga_plan *p) {
         L.dfl = take((size_t)p->N * HD * ts);
         L.dfr = take((size_t)p->N * HD * ts);
         L.da_part = take((size_t)L.da_blocks * HD * 4);
+        L.da_split = take((size_t)p->rows.n_split * HD * 4);
         L.dw_part = take((size_t)2 * L.dw_slabs * p->F * HD * 4);
     }
     L.total = off;
@@ -291,6 +293,7 @@ static GtArgs gt_args(const sga_plan *p) {
         a.ws_ml = ws_at<float>(p, p->layout.fwd_ml);
         a.ws_acc = ws_at<float>(p, p->layout.fwd_acc);
         a.ws_row = ws_at<float>(p, p->layout.bwd_row);
+        a.ws_rowc = ws_at<float>(p, p->layout.bwd_rowc);
         a.ws_col = ws_at<float>(p, p->layout.bwd_col);
     }
     return a;
@@ -356,7 +359,9 @@ static Gatv2Args gatv2_args(const sga_plan *p, float slope) {
         a.ws_acc = ws_at<float>(p, p->layout.fwd_acc);
         a.ws_row = ws_at<float>(p, p->layout.bwd_row);
         a.ws_col = ws_at<float>(p, p->layout.bwd_col);
+        a.ws_rowc = ws_at<float>(p, p->layout.bwd_rowc);
         a.ws_da = ws_at<float>(p, p->layout.da_part);
+        a.ws_da_split = ws_at<float>(p, p->layout.da_split);
         a.ws_dw = ws_at<float>(p, p->layout.dw_part);
         a.ws_dfl = ws_at<void>(p, p->layout.dfl);
         a.ws_dfr = ws_at<void>(p, p->layout.dfr);

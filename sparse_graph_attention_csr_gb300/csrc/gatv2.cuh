@@ -160,10 +160,12 @@ gatv2_fwd_kernel(Gatv2Args a) {
 // ---------------------------------------------------- backward: dst pass
 
 // Per destination row i, for each edge (j):
-//   z = fl_i + fr_j, e = a . LReLU(z), p = exp(e - lse_i),
-//   dp = dOut_i . fr_j, de = p (dp - Delta_i),
-//   dFL_i += de a * LReLU'(z),  da += de LReLU(z).
-// Warps stride over work items; each block leaves one fp32 partial of da.
+//   z = fl_i + fr_j, e = a . LReLU(z), p = exp(e - lse_i), dp = dOut_i . fr_j,
+//   de = p (dp - Delta_i), dFL_i += de a * LReLU'(z), da += de LReLU(z).
+// Delta_i = sum_j p dp is accumulated in the same pass, so each de-weighted
+// sum is kept as (sum p dp x) - Delta_i (sum p x).  Warps stride over work
+// items; each block leaves one fp32 partial of da.  Split-row chunks write
+// their four partial sums and their part of Delta for the merge kernel.
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256)
 gatv2_bwd_dst_kernel(Gatv2Args a) {
@@ -195,36 +197,25 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
          item += stride) {
         ItemRange it;
         if (!decode_item(item, a.rows, a.indptr, a.N, a.split_threshold, it)) continue;
-        float fl[NC][EL], go[NC][EL], dfl[NC][EL], delta[NC], lse2[NC];
+        // fA/fB: dFL sums, gA/gB: da sums (A weighted by p dp, B by p), c: Delta part
+        float fl[NC][EL], go[NC][EL], fA[NC][EL], fB[NC][EL], gA[NC][EL], gB[NC][EL];
+        float c[NC], lse2[NC];
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
-            const int c = gl + G * k;
-            float o[EL];
-            if (c < R) {
-                const size_t off = (size_t)it.row * R + c;
+            const int ch = gl + G * k;
+            if (ch < R) {
+                const size_t off = (size_t)it.row * R + ch;
                 unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + off), fl[k]);
                 unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
-                unpack<T>(ldg16(static_cast<const uint4 *>(a.out) + off), o);
-                lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + c / LH) * kLog2e;
+                lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + ch / LH) * kLog2e;
             } else {
 #pragma unroll
-                for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = o[x] = 0.f;
+                for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = 0.f;
                 lse2[k] = 0.f;
             }
-            float d = 0.f;
 #pragma unroll
-            for (int x = 0; x < EL; ++x) {
-                d = fmaf(go[k][x], o[x], d);
-                dfl[k][x] = 0.f;
-            }
-            delta[k] = group_sum<LH>(d);
-        }
-        if (g == 0 && (!it.partial || it.beg == a.indptr[it.row])) {
-#pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                const int c = gl + G * k;
-                if (c < R && c % LH == 0) a.ws_delta[(size_t)it.row * a.H + c / LH] = delta[k];
-            }
+            for (int x = 0; x < EL; ++x) fA[k][x] = fB[k][x] = gA[k][x] = gB[k][x] = 0.f;
+            c[k] = 0.f;
         }
         for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
             const int cnt = min(32, it.end - e0);
@@ -239,9 +230,9 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                     ok[u] = (t < cnt) && (j >= 0);
 #pragma unroll
                     for (int k = 0; k < NC; ++k) {
-                        const int c = gl + G * k;
-                        fr[u][k] = (ok[u] && c < R) ? ldg16_stream(FRc + (size_t)j * R + c)
-                                                    : make_uint4(0, 0, 0, 0);
+                        const int ch = gl + G * k;
+                        fr[u][k] = (ok[u] && ch < R) ? ldg16_stream(FRc + (size_t)j * R + ch)
+                                                     : make_uint4(0, 0, 0, 0);
                     }
                 }
 #pragma unroll
@@ -259,41 +250,85 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                         }
                         group_sum2<LH>(e, dp);
                         const float p = ok[u] ? exp2f(e * kLog2e - lse2[k]) : 0.f;
-                        const float de = p * (dp - delta[k]);
+                        const float pdp = p * dp;
+                        c[k] += pdp;
 #pragma unroll
                         for (int x = 0; x < EL; ++x) {
                             const float z = fl[k][x] + f[x];
                             const bool pos = z > 0.f;
-                            dfl[k][x] = fmaf(de * att[k][x], pos ? 1.f : slope, dfl[k][x]);
-                            dacc[k][x] = fmaf(de, pos ? z : slope * z, dacc[k][x]);
+                            const float ag = pos ? att[k][x] : slope * att[k][x];
+                            const float lz = pos ? z : slope * z;
+                            fA[k][x] = fmaf(pdp, ag, fA[k][x]);
+                            fB[k][x] = fmaf(p, ag, fB[k][x]);
+                            gA[k][x] = fmaf(pdp, lz, gA[k][x]);
+                            gB[k][x] = fmaf(p, lz, gB[k][x]);
                         }
                     }
             }
         }
+        // Delta and the dFL sums over the whole warp (all edge groups)
 #pragma unroll
         for (int off = G; off < 32; off <<= 1)
 #pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
+#pragma unroll
+                for (int x = 0; x < EL; ++x) {
+                    fA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fA[k][x], off);
+                    fB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fB[k][x], off);
+                }
+            }
+        if (it.partial) {
+            // da sums of this chunk, combined over the groups, go to the merge kernel
+#pragma unroll
+            for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+                for (int k = 0; k < NC; ++k)
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        gA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gA[k][x], off);
+                        gB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gB[k][x], off);
+                    }
+            if (g == 0) {
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int ch = gl + G * k;
+                    if (ch >= R) continue;
+                    float *base = a.ws_row + (size_t)item * 4 * HD + ch * EL;
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4) {
+                        *reinterpret_cast<float4 *>(base + x) =
+                            make_float4(fA[k][x], fA[k][x + 1], fA[k][x + 2], fA[k][x + 3]);
+                        *reinterpret_cast<float4 *>(base + HD + x) =
+                            make_float4(fB[k][x], fB[k][x + 1], fB[k][x + 2], fB[k][x + 3]);
+                        *reinterpret_cast<float4 *>(base + 2 * HD + x) =
+                            make_float4(gA[k][x], gA[k][x + 1], gA[k][x + 2], gA[k][x + 3]);
+                        *reinterpret_cast<float4 *>(base + 3 * HD + x) =
+                            make_float4(gB[k][x], gB[k][x + 1], gB[k][x + 2], gB[k][x + 3]);
+                    }
+                    if (ch % LH == 0) a.ws_rowc[(size_t)item * a.H + ch / LH] = c[k];
+                }
+            }
+        } else {
+#pragma unroll
             for (int k = 0; k < NC; ++k)
 #pragma unroll
-                for (int x = 0; x < EL; ++x)
-                    dfl[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dfl[k][x], off);
-        if (g == 0) {
+                for (int x = 0; x < EL; ++x) dacc[k][x] += gA[k][x] - c[k] * gB[k][x];
+            if (g == 0) {
 #pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                const int c = gl + G * k;
-                if (c >= R) continue;
-                if (it.partial) {
-                    float4 *dst = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * HD + c * EL);
+                for (int k = 0; k < NC; ++k) {
+                    const int ch = gl + G * k;
+                    if (ch >= R) continue;
+                    float o[EL];
 #pragma unroll
-                    for (int x = 0; x < EL; x += 4)
-                        dst[x / 4] = make_float4(dfl[k][x], dfl[k][x + 1], dfl[k][x + 2], dfl[k][x + 3]);
-                } else {
-                    reinterpret_cast<uint4 *>(a.ws_dfl)[(size_t)it.row * R + c] = pack<T>(dfl[k]);
+                    for (int x = 0; x < EL; ++x) o[x] = fA[k][x] - c[k] * fB[k][x];
+                    reinterpret_cast<uint4 *>(a.ws_dfl)[(size_t)it.row * R + ch] = pack<T>(o);
+                    if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
                 }
             }
         }
     }
-    // da: groups -> lanes of group 0, warps -> shared memory (fixed order), one row per block
+    // da: groups -> lanes of group 0, warps -> shared memory in warp order
 #pragma unroll
     for (int off = G; off < 32; off <<= 1)
 #pragma unroll
@@ -426,39 +461,63 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
     }
 }
 
-// Finish split rows: dFL (items [0, rows.n_split)) and dFR (the rest) are the
-// chunk partial sums in chunk order.
+// Finish split rows in chunk order.  which == 0 (destination rows): Delta is
+// the sum of the chunk parts, dFL = sum fA - Delta sum fB, and the row's da
+// contribution sum gA - Delta sum gB goes to its own slot.  which == 1
+// (sources): dFR is the plain sum of the chunk partials.
 template <typename T, int D>
-__global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a) {
-    constexpr int EL = Elt<T>::EL;
+__global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int which) {
+    constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
     const int lane = threadIdx.x & 31;
-    int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int R = a.H * D / EL, HD = a.H * D;
-    const Partition *P = &a.rows;
-    const float *part = a.ws_row;
-    void *dst = a.ws_dfl;
-    if (s >= a.rows.n_split) {
-        s -= a.rows.n_split;
-        if (s >= a.cols.n_split) return;
-        P = &a.cols;
-        part = a.ws_col;
-        dst = a.ws_dfr;
-    }
-    const int32_t row = P->split_rows[s];
-    const int32_t c0 = P->chunk_ptr[s], c1 = P->chunk_ptr[s + 1];
+    const Partition &P = which == 0 ? a.rows : a.cols;
+    if (s >= P.n_split) return;
+    const int32_t row = P.split_rows[s];
+    const int32_t c0 = P.chunk_ptr[s], c1 = P.chunk_ptr[s + 1];
     for (int c = lane; c < R; c += 32) {
-        float acc[EL];
+        if (which == 1) {
+            float acc[EL];
 #pragma unroll
-        for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+            for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+            for (int32_t ch = c0; ch < c1; ++ch) {
+                const float4 *src = reinterpret_cast<const float4 *>(a.ws_col + (size_t)ch * HD + c * EL);
+#pragma unroll
+                for (int x = 0; x < EL; x += 4) {
+                    const float4 v = src[x / 4];
+                    acc[x] += v.x; acc[x + 1] += v.y; acc[x + 2] += v.z; acc[x + 3] += v.w;
+                }
+            }
+            reinterpret_cast<uint4 *>(a.ws_dfr)[(size_t)row * R + c] = pack<T>(acc);
+            continue;
+        }
+        const int h = c / LH;
+        float delta = 0.f;
+        for (int32_t ch = c0; ch < c1; ++ch) delta += a.ws_rowc[(size_t)ch * a.H + h];
+        float sum[4][EL];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int x = 0; x < EL; ++x) sum[q][x] = 0.f;
         for (int32_t ch = c0; ch < c1; ++ch) {
-            const float4 *src = reinterpret_cast<const float4 *>(part + (size_t)ch * HD + c * EL);
 #pragma unroll
-            for (int x = 0; x < EL; x += 4) {
-                const float4 v = src[x / 4];
-                acc[x] += v.x; acc[x + 1] += v.y; acc[x + 2] += v.z; acc[x + 3] += v.w;
+            for (int q = 0; q < 4; ++q) {
+                const float4 *src =
+                    reinterpret_cast<const float4 *>(a.ws_row + ((size_t)ch * 4 + q) * HD + c * EL);
+#pragma unroll
+                for (int x = 0; x < EL; x += 4) {
+                    const float4 v = src[x / 4];
+                    sum[q][x] += v.x; sum[q][x + 1] += v.y; sum[q][x + 2] += v.z; sum[q][x + 3] += v.w;
+                }
             }
         }
-        reinterpret_cast<uint4 *>(dst)[(size_t)row * R + c] = pack<T>(acc);
+        float o[EL];
+#pragma unroll
+        for (int x = 0; x < EL; ++x) o[x] = sum[0][x] - delta * sum[1][x];
+        reinterpret_cast<uint4 *>(a.ws_dfl)[(size_t)row * R + c] = pack<T>(o);
+#pragma unroll
+        for (int x = 0; x < EL; ++x) a.ws_da_split[(size_t)s * HD + c * EL + x] = sum[2][x] - delta * sum[3][x];
+        if (c % LH == 0) a.ws_delta[(size_t)row * a.H + h] = delta;
     }
 }
 
@@ -543,11 +602,12 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<T, TA, TB> g) {
 }
 
 // dW_l, dW_r = sum of the slab partials [2][slab][F*HD] in slab order;
-// da = sum of the per-block partials in block order.
+// da = sum of the per-block partials in block order, then of the split rows'
+// contributions in split-row order.
 template <typename T>
 __global__ void gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs, int64_t FHD,
                                     T *dWl, T *dWr, const float *__restrict__ da_part, int blocks,
-                                    int HD, T *da) {
+                                    const float *__restrict__ da_split, int n_split, int HD, T *da) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t < 2 * FHD) {
         const int which = (int)(t / FHD);
@@ -559,6 +619,7 @@ __global__ void gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs
         const int x = (int)(t - 2 * FHD);
         float s = 0.f;
         for (int b = 0; b < blocks; ++b) s += da_part[(int64_t)b * HD + x];
+        for (int b = 0; b < n_split; ++b) s += da_split[(int64_t)b * HD + x];
         da[x] = from_f32<T>(s);
     }
 }
@@ -620,21 +681,27 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
         note_launch(SGA_KERN_GATV2_BWD_DST, s, true);
         cudaError_t e2 = cudaGetLastError();
         if (e2 != cudaSuccess) return e2;
+        if (a.rows.n_split > 0) {   // Delta of split rows is needed by the source pass
+            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
+            gatv2_bwd_merge_kernel<T, D><<<blocks_for_warps(a.rows.n_split), 256, 0, s>>>(a, 0);
+            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
+            if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
+        }
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
         if (items_c == 0) return cudaSuccess;
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, false);
         gatv2_bwd_src_kernel<T, D, NC, G><<<blocks_for_warps(items_c), 256, 0, s>>>(a);
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, true);
-        return cudaGetLastError();
+        if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
+        if (a.cols.n_split > 0) {
+            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
+            gatv2_bwd_merge_kernel<T, D><<<blocks_for_warps(a.cols.n_split), 256, 0, s>>>(a, 1);
+            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
+            e2 = cudaGetLastError();
+        }
+        return e2;
     });
     if (e != cudaSuccess) return e;
-    const int64_t merges = (int64_t)a.rows.n_split + a.cols.n_split;
-    if (merges > 0) {
-        note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
-        gatv2_bwd_merge_kernel<T, D><<<blocks_for_warps(merges), 256, 0, s>>>(a);
-        note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
     // dX = dFL W_l^T + dFR W_r^T
     if (a.N > 0) {
         GemmArgs<T, false, true> g{};
@@ -667,7 +734,7 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, false);
     gatv2_reduce_kernel<T><<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
         a.ws_dw, a.dw_slabs, FHD, static_cast<T *>(a.dWl), static_cast<T *>(a.dWr), a.ws_da,
-        a.da_blocks, HD, static_cast<T *>(a.da));
+        a.da_blocks, a.ws_da_split, a.rows.n_split, HD, static_cast<T *>(a.da));
     note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, true);
     return cudaGetLastError();
 }

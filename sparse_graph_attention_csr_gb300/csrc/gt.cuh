@@ -253,10 +253,13 @@ __global__ void __launch_bounds__(256) gt_fwd_merge_kernel(A a) {
 
 // ---------------------------------------------------------- backward: dQ
 
-// Per destination row i: Delta_i = dOut_i . out_i (written for the dK/dV
-// pass), then for each edge p = 2^(s2 - lse2_i), dP = dOut_i . v_j,
-// dS = p (dP - Delta_i), dQ_i += dS k_j.  Split-row chunks write fp32
-// partial sums that the merge kernel adds in chunk order.
+// Per destination row i and edge j: p = 2^(s2 - lse2_i), dP = dOut_i . v_j.
+// With Delta_i = sum_j p dP (the exact row term; equal to dOut_i . out_i
+// before out is rounded to the storage dtype), dS = p (dP - Delta_i) and
+// dQ_i = sum_j dS k_j / sqrt(D) = (A - Delta_i B) / sqrt(D) where
+// A = sum_j p dP k_j and B = sum_j p k_j; A, B and Delta_i are accumulated in
+// the same pass over the edges.  Split-row chunks write A, B and their part
+// of Delta; the merge kernel finishes them in chunk order.
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256)
 gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
@@ -270,36 +273,23 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
     const uint4 *__restrict__ Kc = static_cast<const uint4 *>(a.K);
     const uint4 *__restrict__ Vc = static_cast<const uint4 *>(a.V);
 
-    float q[NC][EL], go[NC][EL], dq[NC][EL], delta[NC], lse2[NC];
+    float q[NC][EL], go[NC][EL], A[NC][EL], B[NC][EL], c[NC], lse2[NC];
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
-        const int c = gl + G * k;
-        float o[EL];
-        if (c < R) {
-            const size_t off = (size_t)it.row * R + c;
+        const int ch = gl + G * k;
+        if (ch < R) {
+            const size_t off = (size_t)it.row * R + ch;
             unpack<T>(ldg16(static_cast<const uint4 *>(a.Q) + off), q[k]);
             unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
-            unpack<T>(ldg16(static_cast<const uint4 *>(a.out) + off), o);
-            lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + c / LH) * kLog2e;
+            lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + ch / LH) * kLog2e;
         } else {
 #pragma unroll
-            for (int x = 0; x < EL; ++x) q[k][x] = go[k][x] = o[x] = 0.f;
+            for (int x = 0; x < EL; ++x) q[k][x] = go[k][x] = 0.f;
             lse2[k] = 0.f;
         }
-        float d = 0.f;
 #pragma unroll
-        for (int x = 0; x < EL; ++x) {
-            d = fmaf(go[k][x], o[x], d);
-            dq[k][x] = 0.f;
-        }
-        delta[k] = group_sum<LH>(d);
-    }
-    if (g == 0 && (!it.partial || it.beg == a.indptr[it.row])) {
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            const int c = gl + G * k;
-            if (c < R && c % LH == 0) a.ws_delta[(size_t)it.row * a.H + c / LH] = delta[k];
-        }
+        for (int x = 0; x < EL; ++x) A[k][x] = B[k][x] = 0.f;
+        c[k] = 0.f;
     }
 
     for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
@@ -315,10 +305,10 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                 ok[u] = (t < cnt) && (j >= 0);
 #pragma unroll
                 for (int k = 0; k < NC; ++k) {
-                    const int c = gl + G * k;
-                    if (ok[u] && c < R) {
-                        kr[u][k] = ldg16_stream(Kc + (size_t)j * R + c);
-                        vr[u][k] = ldg16_stream(Vc + (size_t)j * R + c);
+                    const int ch = gl + G * k;
+                    if (ok[u] && ch < R) {
+                        kr[u][k] = ldg16_stream(Kc + (size_t)j * R + ch);
+                        vr[u][k] = ldg16_stream(Vc + (size_t)j * R + ch);
                     } else {
                         kr[u][k] = make_uint4(0, 0, 0, 0);
                         vr[u][k] = make_uint4(0, 0, 0, 0);
@@ -340,34 +330,49 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                     }
                     group_sum2<LH>(s, dp);
                     const float p = ok[u] ? exp2f(s * scale2 - lse2[k]) : 0.f;
-                    const float ds = p * (dp - delta[k]);
+                    const float pdp = p * dp;
+                    c[k] += pdp;
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) dq[k][x] = fmaf(ds, kf[x], dq[k][x]);
+                    for (int x = 0; x < EL; ++x) {
+                        A[k][x] = fmaf(pdp, kf[x], A[k][x]);
+                        B[k][x] = fmaf(p, kf[x], B[k][x]);
+                    }
                 }
         }
     }
 #pragma unroll
     for (int off = G; off < 32; off <<= 1)
 #pragma unroll
-        for (int k = 0; k < NC; ++k)
+        for (int k = 0; k < NC; ++k) {
+            c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
 #pragma unroll
-            for (int x = 0; x < EL; ++x) dq[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dq[k][x], off);
+            for (int x = 0; x < EL; ++x) {
+                A[k][x] += __shfl_xor_sync(SGA_FULL_MASK, A[k][x], off);
+                B[k][x] += __shfl_xor_sync(SGA_FULL_MASK, B[k][x], off);
+            }
+        }
     if (g != 0) return;
     const int HD = a.H * D;
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
-        const int c = gl + G * k;
-        if (c >= R) continue;
+        const int ch = gl + G * k;
+        if (ch >= R) continue;
+        const int h = ch / LH;
         if (it.partial) {
-            float4 *dst = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * HD + c * EL);
+            float4 *dA = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * 2 * HD + ch * EL);
+            float4 *dB = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * 2 * HD + HD + ch * EL);
 #pragma unroll
-            for (int x = 0; x < EL; x += 4)
-                dst[x / 4] = make_float4(dq[k][x], dq[k][x + 1], dq[k][x + 2], dq[k][x + 3]);
+            for (int x = 0; x < EL; x += 4) {
+                dA[x / 4] = make_float4(A[k][x], A[k][x + 1], A[k][x + 2], A[k][x + 3]);
+                dB[x / 4] = make_float4(B[k][x], B[k][x + 1], B[k][x + 2], B[k][x + 3]);
+            }
+            if (ch % LH == 0) a.ws_rowc[(size_t)item * a.H + h] = c[k];
         } else {
             float o[EL];
 #pragma unroll
-            for (int x = 0; x < EL; ++x) o[x] = dq[k][x] * scale;
-            reinterpret_cast<uint4 *>(a.dQ)[(size_t)it.row * R + c] = pack<T>(o);
+            for (int x = 0; x < EL; ++x) o[x] = (A[k][x] - c[k] * B[k][x]) * scale;
+            reinterpret_cast<uint4 *>(a.dQ)[(size_t)it.row * R + ch] = pack<T>(o);
+            if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + h] = c[k];
         }
     }
 }
@@ -491,57 +496,49 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
     }
 }
 
-// Sum chunk partials in chunk order: items [0, rows.n_split) finish dQ,
-// items [rows.n_split, rows.n_split + cols.n_split) finish dK and dV.
+// Finish split rows in chunk order.  which == 0: dQ rows (Delta = sum of the
+// chunk parts, dQ = (sum A - Delta sum B) / sqrt(D), Delta stored for the
+// dK/dV pass).  which == 1: dK, dV of split sources (plain sums).
 template <typename T, int D>
-__global__ void __launch_bounds__(256) gt_bwd_merge_kernel(GtArgs a, float scale) {
-    constexpr int EL = Elt<T>::EL;
+__global__ void __launch_bounds__(256) gt_bwd_merge_kernel(GtArgs a, float scale, int which) {
+    constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
     const int lane = threadIdx.x & 31;
-    int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
     const int R = a.H * D / EL, HD = a.H * D;
-    if (s < a.rows.n_split) {
-        const int32_t row = a.rows.split_rows[s];
-        const int32_t c0 = a.rows.chunk_ptr[s], c1 = a.rows.chunk_ptr[s + 1];
-        for (int c = lane; c < R; c += 32) {
-            float acc[EL];
-#pragma unroll
-            for (int x = 0; x < EL; ++x) acc[x] = 0.f;
-            for (int32_t ch = c0; ch < c1; ++ch) {
-                const float4 *src = reinterpret_cast<const float4 *>(a.ws_row + (size_t)ch * HD + c * EL);
-#pragma unroll
-                for (int x = 0; x < EL; x += 4) {
-                    const float4 v = src[x / 4];
-                    acc[x] += v.x; acc[x + 1] += v.y; acc[x + 2] += v.z; acc[x + 3] += v.w;
-                }
-            }
-#pragma unroll
-            for (int x = 0; x < EL; ++x) acc[x] *= scale;
-            reinterpret_cast<uint4 *>(a.dQ)[(size_t)row * R + c] = pack<T>(acc);
-        }
-        return;
-    }
-    s -= a.rows.n_split;
-    if (s >= a.cols.n_split) return;
-    const int32_t row = a.cols.split_rows[s];
-    const int32_t c0 = a.cols.chunk_ptr[s], c1 = a.cols.chunk_ptr[s + 1];
+    const Partition &P = which == 0 ? a.rows : a.cols;
+    if (s >= P.n_split) return;
+    const int32_t row = P.split_rows[s];
+    const int32_t c0 = P.chunk_ptr[s], c1 = P.chunk_ptr[s + 1];
     for (int c = lane; c < R; c += 32) {
-        float gk[EL], gv[EL];
+        float x0[EL], x1[EL];
 #pragma unroll
-        for (int x = 0; x < EL; ++x) gk[x] = gv[x] = 0.f;
+        for (int x = 0; x < EL; ++x) x0[x] = x1[x] = 0.f;
+        const float *part = which == 0 ? a.ws_row : a.ws_col;
         for (int32_t ch = c0; ch < c1; ++ch) {
-            const float4 *sk = reinterpret_cast<const float4 *>(a.ws_col + (size_t)ch * 2 * HD + c * EL);
-            const float4 *sv = reinterpret_cast<const float4 *>(a.ws_col + (size_t)ch * 2 * HD + HD + c * EL);
+            const float4 *s0 = reinterpret_cast<const float4 *>(part + (size_t)ch * 2 * HD + c * EL);
+            const float4 *s1 = reinterpret_cast<const float4 *>(part + (size_t)ch * 2 * HD + HD + c * EL);
 #pragma unroll
             for (int x = 0; x < EL; x += 4) {
-                const float4 u = sk[x / 4], v = sv[x / 4];
-                gk[x] += u.x; gk[x + 1] += u.y; gk[x + 2] += u.z; gk[x + 3] += u.w;
-                gv[x] += v.x; gv[x + 1] += v.y; gv[x + 2] += v.z; gv[x + 3] += v.w;
+                const float4 u = s0[x / 4], v = s1[x / 4];
+                x0[x] += u.x; x0[x + 1] += u.y; x0[x + 2] += u.z; x0[x + 3] += u.w;
+                x1[x] += v.x; x1[x + 1] += v.y; x1[x + 2] += v.z; x1[x + 3] += v.w;
             }
         }
+        if (which == 0) {
+            const int h = c / LH;
+            float delta = 0.f;
+            for (int32_t ch = c0; ch < c1; ++ch) delta += a.ws_rowc[(size_t)ch * a.H + h];
+            float o[EL];
 #pragma unroll
-        for (int x = 0; x < EL; ++x) gk[x] *= scale;
-        reinterpret_cast<uint4 *>(a.dK)[(size_t)row * R + c] = pack<T>(gk);
-        reinterpret_cast<uint4 *>(a.dV)[(size_t)row * R + c] = pack<T>(gv);
+            for (int x = 0; x < EL; ++x) o[x] = (x0[x] - delta * x1[x]) * scale;
+            reinterpret_cast<uint4 *>(a.dQ)[(size_t)row * R + c] = pack<T>(o);
+            if (c % LH == 0) a.ws_delta[(size_t)row * a.H + h] = delta;
+        } else {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) x0[x] *= scale;
+            reinterpret_cast<uint4 *>(a.dK)[(size_t)row * R + c] = pack<T>(x0);
+            reinterpret_cast<uint4 *>(a.dV)[(size_t)row * R + c] = pack<T>(x1);
+        }
     }
 }
 
@@ -609,24 +606,29 @@ template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t 
     return dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         const int64_t items_r = (int64_t)a.rows.n_chunks + a.N;
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
-        if (items_r > 0) {
-            note_launch(SGA_KERN_GT_BWD_DQ, s, false);
-            gt_bwd_dq_kernel<T, D, NC, G><<<blocks_for_warps(items_r), 256, 0, s>>>(a, scale2, scale);
-            note_launch(SGA_KERN_GT_BWD_DQ, s, true);
-            cudaError_t e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
-            note_launch(SGA_KERN_GT_BWD_DKDV, s, false);
-            gt_bwd_dkdv_kernel<T, D, NC, G><<<blocks_for_warps(items_c), 256, 0, s>>>(a, scale2, scale);
-            note_launch(SGA_KERN_GT_BWD_DKDV, s, true);
-            e = cudaGetLastError();
-            if (e != cudaSuccess) return e;
+        if (items_r == 0) return cudaSuccess;
+        note_launch(SGA_KERN_GT_BWD_DQ, s, false);
+        gt_bwd_dq_kernel<T, D, NC, G><<<blocks_for_warps(items_r), 256, 0, s>>>(a, scale2, scale);
+        note_launch(SGA_KERN_GT_BWD_DQ, s, true);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        if (a.rows.n_split > 0) {   // Delta of split rows is needed by the dK/dV pass
+            note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
+            gt_bwd_merge_kernel<T, D><<<blocks_for_warps(a.rows.n_split), 256, 0, s>>>(a, scale, 0);
+            note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        const int64_t merges = (int64_t)a.rows.n_split + a.cols.n_split;
-        if (merges == 0) return cudaSuccess;
-        note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
-        gt_bwd_merge_kernel<T, D><<<blocks_for_warps(merges), 256, 0, s>>>(a, scale);
-        note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
-        return cudaGetLastError();
+        note_launch(SGA_KERN_GT_BWD_DKDV, s, false);
+        gt_bwd_dkdv_kernel<T, D, NC, G><<<blocks_for_warps(items_c), 256, 0, s>>>(a, scale2, scale);
+        note_launch(SGA_KERN_GT_BWD_DKDV, s, true);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (a.cols.n_split > 0) {
+            note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
+            gt_bwd_merge_kernel<T, D><<<blocks_for_warps(a.cols.n_split), 256, 0, s>>>(a, scale, 1);
+            note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
+            e = cudaGetLastError();
+        }
+        return e;
     });
 }
 

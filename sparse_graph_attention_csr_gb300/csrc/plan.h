@@ -27,7 +27,9 @@ struct WorkspaceLayout {
     size_t delta = 0;      // [N, H] f32          Delta_i = dOut_i . out_i
     size_t fwd_ml = 0;     // [n_chunks, H, 2] f32 chunk softmax stats (max, sum), log2 units
     size_t fwd_acc = 0;    // [n_chunks, H*D] f32  chunk unnormalised accumulators
-    size_t bwd_row = 0;    // [n_chunks, H*D] f32  chunk partial dQ / dFL
+    size_t bwd_row = 0;    // [n_chunks, 4, H*D] f32 chunk partial sums (dQ: A, B; dFL: A, B, da A, B)
+    size_t bwd_rowc = 0;   // [n_chunks, H] f32   chunk part of Delta
+    size_t da_split = 0;   // [n_split, H*D] f32  GATv2 da contribution of each split row
     size_t bwd_col = 0;    // [t_n_chunks, 2*H*D] f32 chunk partial dK,dV / dFR
     size_t dfl = 0;        // [N, H*D] dt  GATv2 dFL
     size_t dfr = 0;        // [N, H*D] dt  GATv2 dFR
@@ -79,7 +81,7 @@ struct GtArgs {
     int H, D;
     int split_threshold;
     Partition rows, cols;
-    float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_col;
+    float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_rowc, *ws_col;
     int32_t *d_err;
 };
 template <typename T> cudaError_t gt_fwd_t(const GtArgs &a, cudaStream_t s);
@@ -98,7 +100,7 @@ struct Gatv2Args {
     float slope;
     int split_threshold;
     Partition rows, cols;
-    float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_col, *ws_da, *ws_dw;
+    float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_rowc, *ws_col, *ws_da, *ws_da_split, *ws_dw;
     void *ws_dfl, *ws_dfr;
     int da_blocks, dw_slabs;
     int32_t *d_err;

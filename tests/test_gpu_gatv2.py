@@ -37,17 +37,22 @@ def check(indptr, indices, F, H, D, dtype, X, Wl, Wr, a, dO, split=0, chunk=0, s
     plan = sga.Plan(ip, ix, H, D, TORCH_DT[dtype], F=F, split_threshold=split, chunk_len=chunk)
     gX, gWl, gWr, ga, gdO = (dev(t[0]) for t in (X, Wl, Wr, a, dO))
     FL, FR, out, lse = sga.gatv2_fwd(plan, gX, gWl, gWr, ga, slope)
-    rFL, rFR, rout, rlse = oracle.gatv2_fwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], slope)
+    # the layer stores FL/FR in its dtype; the oracle rounds its projections the same way
+    rFL, rFR, rout, rlse = oracle.gatv2_fwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], slope,
+                                            store=dtype)
     compare(FL, rFL, dtype, "FL")
     compare(FR, rFR, dtype, "FR")
     compare(out, rout, dtype, "out")
     compare(lse, rlse, dtype, "lse")
     dX, dWl, dWr, da = sga.gatv2_bwd(plan, gX, gWl, gWr, ga, FL, FR, out, lse, gdO, slope)
-    g = oracle.gatv2_bwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope)
-    compare(dX, g["dX"], dtype, "dX")
-    compare(dWl, g["dW_l"], dtype, "dW_l")
-    compare(dWr, g["dW_r"], dtype, "dW_r")
-    compare(da, g["da"], dtype, "da")
+    g = oracle.gatv2_bwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope, store=dtype)
+    # dX, dW and da are sums over many edges or nodes: in fp32 the bound gains
+    # a relative term of 1e-5 (fp32 summation error grows with the magnitude)
+    rt = 1e-5 if dtype == "f32" else None
+    compare(dX, g["dX"], dtype, "dX", rtol=rt)
+    compare(dWl, g["dW_l"], dtype, "dW_l", rtol=rt)
+    compare(dWr, g["dW_r"], dtype, "dW_r", rtol=rt)
+    compare(da, g["da"], dtype, "da", rtol=rt)
     assert plan.device_error() == 0
     return plan
 
