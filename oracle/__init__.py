@@ -79,6 +79,9 @@ def _load():
                                   _F64P, _dbl, _int, _F64P, _F64P, _F64P, _F64P, _F64P, _F64P,
                                   _F64P], _int),
             "oracle_round_bf16": ([_dbl], _dbl),
+            "oracle_gatv2_branch_slack": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P,
+                                           _F64P, _F64P, _dbl, _int, _dbl, _F64P, _F64P, _F64P,
+                                           _F64P, _F64P], _int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -257,3 +260,28 @@ def gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, slope=0.2, store=None):
     _check(_load().oracle_gatv2_bwd(N, F, H, D, indptr, indices, X, Wl, Wr, a, float(slope),
                                     _STORE[store], dO, dX, dWl, dWr, da, dFL, dFR), "gatv2_bwd")
     return {"dX": dX, "dW_l": dWl, "dW_r": dWr, "da": da, "dFL": dFL, "dFR": dFR}
+
+
+# Relative width of the band of z = FL + FR in which two correct
+# implementations may decide the LeakyReLU branch differently.  Float storage:
+# projections accumulated in fp32 differ from the exact ones by a few float
+# ulps, far inside 2^-18.  bf16 storage: the projections are the correctly
+# rounded values on both sides, so no branch is undecided.
+BRANCH_TAU = {"bf16": 0.0, "f32": 2.0 ** -18}
+
+
+def gatv2_branch_slack(indptr, indices, X, Wl, Wr, a, dO, slope=0.2, store="bf16", tau=None):
+    """Largest change of dX, dW_l, dW_r, da that LeakyReLU branches left
+    undecided by the projections' storage precision can cause (see
+    oracle_gatv2_branch_slack in oracle.c).  dict of nonnegative arrays."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    X, Wl, Wr, a, dO = _f64(X), _f64(Wl), _f64(Wr), _f64(a), _f64(dO)
+    N, F = X.shape
+    H, D = a.shape
+    tau = BRANCH_TAU[store] if tau is None else tau
+    sX = np.empty((N, F)); sWl = np.empty((F, H * D)); sWr = np.empty((F, H * D))
+    sda = np.empty((H, D))
+    _check(_load().oracle_gatv2_branch_slack(N, F, H, D, indptr, indices, X, Wl, Wr, a,
+                                             float(slope), _STORE[store], float(tau), dO,
+                                             sX, sWl, sWr, sda), "gatv2_branch_slack")
+    return {"dX": sX, "dW_l": sWl, "dW_r": sWr, "da": sda}

@@ -646,3 +646,83 @@ int oracle_gatv2_bwd(int64_t N, int F, int H, int D, const int32_t *indptr, cons
     free(t_dst);
     return err;
 }
+
+/* Slack of the GATv2 gradients due to LeakyReLU branches that the storage
+ * precision of FL/FR leaves undecided.
+ *
+ * The branch of LeakyReLU'(z), z = FL_i + FR_j, is decided on the stored
+ * projections.  Two correct implementations may store projections that differ
+ * by a few units in the last place (they round differently accumulated
+ * sums), so an element with |z| < tau_rel (|FL| + |FR|) may take either branch.
+ * Flipping one such branch changes dz by de a (1 - slope), hence dFL_i and
+ * dFR_j by that amount, da by de z (1 - slope), and dX, dW through the
+ * projections.  This function sums the absolute values of those changes over
+ * all undecided elements: any correct result lies within this slack of the
+ * oracle's (plus rounding).  Outputs: sX [N, F], sWl, sWr [F, H*D], sda [H, D]. */
+int oracle_gatv2_branch_slack(int64_t N, int F, int H, int D, const int32_t *indptr,
+                              const int32_t *indices, const double *X, const double *Wl,
+                              const double *Wr, const double *a, double slope, int store,
+                              double tau_rel, const double *dO, double *sX, double *sWl,
+                              double *sWr, double *sda) {
+    int HD = H * D;
+    int64_t md = max_degree(N, indptr);
+    double *FL = (double *)malloc(sizeof(double) * (size_t)(N * HD + 1));
+    double *FR = (double *)malloc(sizeof(double) * (size_t)(N * HD + 1));
+    double *sFL = (double *)calloc((size_t)(N * HD + 1), sizeof(double));
+    double *sFR = (double *)calloc((size_t)(N * HD + 1), sizeof(double));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *de = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    int err = (!FL || !FR || !sFL || !sFR || !s || !p || !de) ? -1 : 0;
+    if (!err) {
+        oracle_matmul(N, F, HD, X, Wl, FL);
+        oracle_matmul(N, F, HD, X, Wr, FR);
+        round_storage(N * HD, FL, store);
+        round_storage(N * HD, FR, store);
+        for (int64_t x = 0; x < HD; ++x) sda[x] = 0.0;
+        for (int64_t i = 0; i < N; ++i) {
+            int64_t b = indptr[i], n = indptr[i + 1] - b;
+            for (int h = 0; h < H; ++h) {
+                if (n == 0) continue;
+                gatv2_row_grad(i, h, H, D, indptr, indices, FL, FR, a, slope, dO, s, p, de);
+                const double *fl = FL + ((size_t)i * H + h) * D;
+                for (int64_t t = 0; t < n; ++t) {
+                    int64_t j = indices[b + t];
+                    const double *fr = FR + ((size_t)j * H + h) * D;
+                    for (int d = 0; d < D; ++d) {
+                        double z = fl[d] + fr[d];
+                        /* open band: z exactly 0 is decided alike on equal inputs */
+                        if (!(fabs(z) < tau_rel * (fabs(fl[d]) + fabs(fr[d])))) continue;
+                        double v = fabs(de[t] * a[h * D + d]) * (1.0 - slope);
+                        sFL[(size_t)i * HD + h * D + d] += v;
+                        sFR[(size_t)j * HD + h * D + d] += v;
+                        sda[h * D + d] += fabs(de[t] * z) * (1.0 - slope);
+                    }
+                }
+            }
+        }
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; ++n)
+            for (int f = 0; f < F; ++f) {
+                double acc = 0.0;
+                for (int c = 0; c < HD; ++c)
+                    acc += sFL[(size_t)n * HD + c] * fabs(Wl[(size_t)f * HD + c]) +
+                           sFR[(size_t)n * HD + c] * fabs(Wr[(size_t)f * HD + c]);
+                sX[(size_t)n * F + f] = acc;
+            }
+#pragma omp parallel for schedule(static)
+        for (int f = 0; f < F; ++f)
+            for (int c = 0; c < HD; ++c) {
+                double gl = 0.0, gr = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    double x = fabs(X[(size_t)n * F + f]);
+                    gl += x * sFL[(size_t)n * HD + c];
+                    gr += x * sFR[(size_t)n * HD + c];
+                }
+                sWl[(size_t)f * HD + c] = gl;
+                sWr[(size_t)f * HD + c] = gr;
+            }
+    }
+    free(FL); free(FR); free(sFL); free(sFR); free(s); free(p); free(de);
+    return err;
+}

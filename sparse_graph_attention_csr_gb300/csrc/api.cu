@@ -41,7 +41,6 @@ int dw_slabs_for(int64_t N) {
 void compute_layout(sga_plan *p) {
     WorkspaceLayout &L = p->layout;
     const size_t HD = (size_t)p->H * p->D;
-    const size_t ts = p->dt == SGA_F32 ? 4 : 2;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t at = off;
@@ -57,8 +56,8 @@ void compute_layout(sga_plan *p) {
     if (p->F > 0) {
         L.da_blocks = da_blocks_for(p->num_sms);
         L.dw_slabs = dw_slabs_for(p->N);
-        L.dfl = take((size_t)p->N * HD * ts);
-        L.dfr = take((size_t)p->N * HD * ts);
+        L.dfl = take((size_t)p->N * HD * 4);
+        L.dfr = take((size_t)p->N * HD * 4);
         L.da_part = take((size_t)L.da_blocks * HD * 4);
         L.da_split = take((size_t)p->rows.n_split * HD * 4);
         L.dw_part = take((size_t)2 * L.dw_slabs * p->F * HD * 4);
@@ -363,8 +362,8 @@ static Gatv2Args gatv2_args(const sga_plan *p, float slope) {
         a.ws_da = ws_at<float>(p, p->layout.da_part);
         a.ws_da_split = ws_at<float>(p, p->layout.da_split);
         a.ws_dw = ws_at<float>(p, p->layout.dw_part);
-        a.ws_dfl = ws_at<void>(p, p->layout.dfl);
-        a.ws_dfr = ws_at<void>(p, p->layout.dfr);
+        a.ws_dfl = ws_at<float>(p, p->layout.dfl);
+        a.ws_dfr = ws_at<float>(p, p->layout.dfr);
     }
     return a;
 }

@@ -319,10 +319,13 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                 for (int k = 0; k < NC; ++k) {
                     const int ch = gl + G * k;
                     if (ch >= R) continue;
-                    float o[EL];
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_dfl + (size_t)it.row * HD + ch * EL);
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) o[x] = fA[k][x] - c[k] * fB[k][x];
-                    reinterpret_cast<uint4 *>(a.ws_dfl)[(size_t)it.row * R + ch] = pack<T>(o);
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(fA[k][x] - c[k] * fB[k][x],
+                                                 fA[k][x + 1] - c[k] * fB[k][x + 1],
+                                                 fA[k][x + 2] - c[k] * fB[k][x + 2],
+                                                 fA[k][x + 3] - c[k] * fB[k][x + 3]);
                     if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
                 }
             }
@@ -456,7 +459,10 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
             for (int x = 0; x < EL; x += 4)
                 dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
         } else {
-            reinterpret_cast<uint4 *>(a.ws_dfr)[(size_t)it.row * R + c] = pack<T>(dfr[k]);
+            float4 *dst = reinterpret_cast<float4 *>(a.ws_dfr + (size_t)it.row * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4)
+                dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
         }
     }
 }
@@ -480,6 +486,7 @@ __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int w
             float acc[EL];
 #pragma unroll
             for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+#pragma unroll 4
             for (int32_t ch = c0; ch < c1; ++ch) {
                 const float4 *src = reinterpret_cast<const float4 *>(a.ws_col + (size_t)ch * HD + c * EL);
 #pragma unroll
@@ -488,7 +495,8 @@ __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int w
                     acc[x] += v.x; acc[x + 1] += v.y; acc[x + 2] += v.z; acc[x + 3] += v.w;
                 }
             }
-            reinterpret_cast<uint4 *>(a.ws_dfr)[(size_t)row * R + c] = pack<T>(acc);
+#pragma unroll
+            for (int x = 0; x < EL; ++x) a.ws_dfr[(size_t)row * HD + c * EL + x] = acc[x];
             continue;
         }
         const int h = c / LH;
@@ -499,6 +507,7 @@ __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int w
         for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int x = 0; x < EL; ++x) sum[q][x] = 0.f;
+#pragma unroll 2
         for (int32_t ch = c0; ch < c1; ++ch) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -511,10 +520,8 @@ __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int w
                 }
             }
         }
-        float o[EL];
 #pragma unroll
-        for (int x = 0; x < EL; ++x) o[x] = sum[0][x] - delta * sum[1][x];
-        reinterpret_cast<uint4 *>(a.ws_dfl)[(size_t)row * R + c] = pack<T>(o);
+        for (int x = 0; x < EL; ++x) a.ws_dfl[(size_t)row * HD + c * EL + x] = sum[0][x] - delta * sum[1][x];
 #pragma unroll
         for (int x = 0; x < EL; ++x) a.ws_da_split[(size_t)s * HD + c * EL + x] = sum[2][x] - delta * sum[3][x];
         if (c % LH == 0) a.ws_delta[(size_t)row * a.H + h] = delta;
@@ -530,28 +537,59 @@ __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int w
 // of the K range are used (split-K slabs); blockIdx.z selects the slab.
 // The result goes to C (dtype T) or, when Cpart is set, to the fp32 partial
 // Cpart[slab][M][N].
-template <typename T, bool TA, bool TB> struct GemmArgs {
-    const T *A[2];
-    const T *B[2];
+template <typename TA_, typename TB_, typename T, bool TA, bool TB> struct GemmArgs {
+    const TA_ *A[2];
+    const TB_ *B[2];
     int pairs;
     int64_t M, N, K;
     int64_t k_per_slab;
     T *C;
     float *Cpart;
+    bool exact_bf16;   // correctly rounded bf16 C (see bf16_rounding_ambiguous); pairs == 1, one slab
 };
 
-template <typename T, bool TA, bool TB>
-__global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<T, TA, TB> g) {
+// Correctly rounded bf16 outputs.  The fp32 accumulation of a k-term dot
+// product x . w differs from the exact value by a small multiple of
+// 2^-24 |x| |w| (|.| the Euclidean norm).  If every value within
+// B = 4 * 2^-24 |x| |w| + ulp(acc) of the fp32 sum rounds to the same bf16
+// number, that number is the correctly rounded result; otherwise (about 0.6%
+// of the elements for unit-scale inputs) the dot product is recomputed
+// exactly: products of bf16 or fp32 inputs are exact in fp64 and the k <= 1024
+// term sum stays far inside fp64 precision.  The fp64 value is rounded to
+// float and then to bf16 (ties to even).
+__device__ __forceinline__ bool bf16_rounding_ambiguous(float acc, float bound) {
+    const float b = bound + fabsf(acc) * 1.2e-7f;
+    return __float2bfloat16_rn(acc - b) != __float2bfloat16_rn(acc + b);
+}
+
+template <typename TA_, typename TB_, bool TA, bool TB, typename G>
+__device__ float exact_dot(const G &g, int64_t m, int64_t n) {
+    double s = 0.0;
+    for (int p = 0; p < g.pairs; ++p)
+        for (int64_t k = 0; k < g.K; ++k) {
+            const double x = (double)to_f32<TA_>(TA ? g.A[p][k * g.M + m] : g.A[p][m * g.K + k]);
+            const double y = (double)to_f32<TB_>(TB ? g.B[p][n * g.K + k] : g.B[p][k * g.N + n]);
+            s = fma(x, y, s);
+        }
+    return (float)s;
+}
+
+template <typename TA_, typename TB_, typename T, bool TA, bool TB>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<TA_, TB_, T, TA, TB> g) {
     constexpr int BM = 64, BN = 64, BK = 16;
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[BK][BN + 4];
+    __shared__ float rowsq[BM], colsq[BN];   // squared norms of the tile's rows / columns
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    if (g.exact_bf16 && threadIdx.x < BM) rowsq[threadIdx.x] = 0.f;
+    else if (g.exact_bf16 && threadIdx.x < BM + BN) colsq[threadIdx.x - BM] = 0.f;
     const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
     const int64_t k_lo = (int64_t)blockIdx.z * g.k_per_slab;
     const int64_t k_hi = min(g.K, k_lo + g.k_per_slab);
     float acc[4][4] = {};
     for (int p = 0; p < g.pairs; ++p) {
-        const T *A = g.A[p], *B = g.B[p];
+        const TA_ *A = g.A[p];
+        const TB_ *B = g.B[p];
         for (int64_t kb = k_lo; kb < k_hi; kb += BK) {
             for (int idx = threadIdx.x; idx < BM * BK; idx += 256) {
                 int mm, kk;
@@ -559,7 +597,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<T, TA, TB> g) {
                 const int64_t gm = m0 + mm, gk = kb + kk;
                 float v = 0.f;
                 if (gm < g.M && gk < k_hi)
-                    v = to_f32<T>(TA ? A[gk * g.M + gm] : A[gm * g.K + gk]);
+                    v = to_f32<TA_>(TA ? A[gk * g.M + gm] : A[gm * g.K + gk]);
                 As[kk][mm] = v;
             }
             for (int idx = threadIdx.x; idx < BN * BK; idx += 256) {
@@ -568,10 +606,22 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<T, TA, TB> g) {
                 const int64_t gn = n0 + nn, gk = kb + kk;
                 float v = 0.f;
                 if (gn < g.N && gk < k_hi)
-                    v = to_f32<T>(TB ? B[gn * g.K + gk] : B[gk * g.N + gn]);
+                    v = to_f32<TB_>(TB ? B[gn * g.K + gk] : B[gk * g.N + gn]);
                 Bs[kk][nn] = v;
             }
             __syncthreads();
+            if (g.exact_bf16) {   // one thread per row / column, k in order: deterministic
+                if (threadIdx.x < BM) {
+                    float q = rowsq[threadIdx.x];
+                    for (int kk = 0; kk < BK; ++kk) q = fmaf(As[kk][threadIdx.x], As[kk][threadIdx.x], q);
+                    rowsq[threadIdx.x] = q;
+                } else if (threadIdx.x < BM + BN) {
+                    const int nn = threadIdx.x - BM;
+                    float q = colsq[nn];
+                    for (int kk = 0; kk < BK; ++kk) q = fmaf(Bs[kk][nn], Bs[kk][nn], q);
+                    colsq[nn] = q;
+                }
+            }
 #pragma unroll
             for (int kk = 0; kk < BK; ++kk) {
                 float av[4], bv[4];
@@ -596,6 +646,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<T, TA, TB> g) {
             const int64_t gn = n0 + tx * 4 + c;
             if (gn >= g.N) continue;
             if (g.Cpart) g.Cpart[((int64_t)blockIdx.z * g.M + gm) * g.N + gn] = acc[r][c];
+            else if (g.exact_bf16 &&
+                     bf16_rounding_ambiguous(acc[r][c], 4.0f * 5.9604645e-8f *
+                                                            sqrtf(rowsq[ty * 4 + r] * colsq[tx * 4 + c])))
+                g.C[gm * g.N + gn] = from_f32<T>(exact_dot<TA_, TB_, TA, TB>(g, gm, gn));
             else g.C[gm * g.N + gn] = from_f32<T>(acc[r][c]);
         }
     }
@@ -624,11 +678,11 @@ __global__ void gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs
     }
 }
 
-template <typename T, bool TA, bool TB>
-cudaError_t gemm(const GemmArgs<T, TA, TB> &g, int slabs, sga_kernel_id kid, cudaStream_t s) {
+template <typename TA_, typename TB_, typename T, bool TA, bool TB>
+cudaError_t gemm(const GemmArgs<TA_, TB_, T, TA, TB> &g, int slabs, sga_kernel_id kid, cudaStream_t s) {
     dim3 grid((unsigned)((g.N + 63) / 64), (unsigned)((g.M + 63) / 64), (unsigned)slabs);
     note_launch(kid, s, false);
-    gemm_simt_kernel<T, TA, TB><<<grid, 256, 0, s>>>(g);
+    gemm_simt_kernel<TA_, TB_, T, TA, TB><<<grid, 256, 0, s>>>(g);
     note_launch(kid, s, true);
     return cudaGetLastError();
 }
@@ -641,13 +695,14 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
     const int HD = a.H * D;
     // projections FL = X W_l, FR = X W_r
     for (int w = 0; w < 2; ++w) {
-        GemmArgs<T, false, false> g{};
+        GemmArgs<T, T, T, false, false> g{};
         g.A[0] = static_cast<const T *>(a.X);
         g.B[0] = static_cast<const T *>(w ? a.Wr : a.Wl);
         g.pairs = 1;
         g.M = a.N; g.N = HD; g.K = a.F; g.k_per_slab = a.F;
         g.C = static_cast<T *>(w ? a.FR_w : a.FL_w);
         g.Cpart = nullptr;
+        g.exact_bf16 = sizeof(T) == 2;
         if (a.N > 0) {
             cudaError_t e = gemm(g, 1, SGA_KERN_GATV2_PROJ, s);
             if (e != cudaSuccess) return e;
@@ -704,10 +759,10 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     if (e != cudaSuccess) return e;
     // dX = dFL W_l^T + dFR W_r^T
     if (a.N > 0) {
-        GemmArgs<T, false, true> g{};
-        g.A[0] = static_cast<const T *>(a.ws_dfl);
+        GemmArgs<float, T, T, false, true> g{};
+        g.A[0] = a.ws_dfl;
         g.B[0] = static_cast<const T *>(a.Wl);
-        g.A[1] = static_cast<const T *>(a.ws_dfr);
+        g.A[1] = a.ws_dfr;
         g.B[1] = static_cast<const T *>(a.Wr);
         g.pairs = 2;
         g.M = a.N; g.N = a.F; g.K = HD; g.k_per_slab = HD;
@@ -720,9 +775,9 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     {
         // One launch per projection; each writes slab-major partials with a stride of 2*F*HD.
         for (int w = 0; w < 2 && a.N > 0; ++w) {
-            GemmArgs<T, true, false> g{};
+            GemmArgs<T, float, T, true, false> g{};
             g.A[0] = static_cast<const T *>(a.X);
-            g.B[0] = static_cast<const T *>(w ? a.ws_dfr : a.ws_dfl);
+            g.B[0] = w ? a.ws_dfr : a.ws_dfl;
             g.pairs = 1;
             g.M = a.F; g.N = HD; g.K = a.N; g.k_per_slab = per;
             g.C = nullptr;

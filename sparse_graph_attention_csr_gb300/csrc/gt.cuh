@@ -225,10 +225,12 @@ __global__ void __launch_bounds__(256) gt_fwd_merge_kernel(A a) {
     for (int c = lane; c < R; c += 32) {
         const int h = c / LH;
         float M = -INFINITY;
+#pragma unroll 4
         for (int32_t ch = c0; ch < c1; ++ch) M = fmaxf(M, a.ws_ml[((size_t)ch * a.H + h) * 2]);
         float L = 0.f, acc[EL];
 #pragma unroll
         for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+#pragma unroll 4
         for (int32_t ch = c0; ch < c1; ++ch) {
             const float w = exp2_diff(a.ws_ml[((size_t)ch * a.H + h) * 2], M);
             L += a.ws_ml[((size_t)ch * a.H + h) * 2 + 1] * w;
@@ -514,6 +516,7 @@ __global__ void __launch_bounds__(256) gt_bwd_merge_kernel(GtArgs a, float scale
 #pragma unroll
         for (int x = 0; x < EL; ++x) x0[x] = x1[x] = 0.f;
         const float *part = which == 0 ? a.ws_row : a.ws_col;
+#pragma unroll 4
         for (int32_t ch = c0; ch < c1; ++ch) {
             const float4 *s0 = reinterpret_cast<const float4 *>(part + (size_t)ch * 2 * HD + c * EL);
             const float4 *s1 = reinterpret_cast<const float4 *>(part + (size_t)ch * 2 * HD + HD + c * EL);

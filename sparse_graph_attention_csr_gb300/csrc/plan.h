@@ -31,8 +31,8 @@ struct WorkspaceLayout {
     size_t bwd_rowc = 0;   // [n_chunks, H] f32   chunk part of Delta
     size_t da_split = 0;   // [n_split, H*D] f32  GATv2 da contribution of each split row
     size_t bwd_col = 0;    // [t_n_chunks, 2*H*D] f32 chunk partial dK,dV / dFR
-    size_t dfl = 0;        // [N, H*D] dt  GATv2 dFL
-    size_t dfr = 0;        // [N, H*D] dt  GATv2 dFR
+    size_t dfl = 0;        // [N, H*D] f32 GATv2 dFL
+    size_t dfr = 0;        // [N, H*D] f32 GATv2 dFR
     size_t da_part = 0;    // [da_blocks, H*D] f32 GATv2 partial da
     size_t dw_part = 0;    // [dw_slabs, 2, F, H*D] f32 GATv2 partial dW_l, dW_r
     size_t total = 0;
@@ -101,7 +101,7 @@ struct Gatv2Args {
     int split_threshold;
     Partition rows, cols;
     float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_rowc, *ws_col, *ws_da, *ws_da_split, *ws_dw;
-    void *ws_dfl, *ws_dfr;
+    float *ws_dfl, *ws_dfr;        // [N, H*D] fp32
     int da_blocks, dw_slabs;
     int32_t *d_err;
 };

@@ -42,17 +42,26 @@ def check(indptr, indices, F, H, D, dtype, X, Wl, Wr, a, dO, split=0, chunk=0, s
                                             store=dtype)
     compare(FL, rFL, dtype, "FL")
     compare(FR, rFR, dtype, "FR")
+    if dtype == "bf16":   # correctly rounded projections: bit-exact
+        assert np.array_equal(FL.double().cpu().numpy(), rFL)
+        assert np.array_equal(FR.double().cpu().numpy(), rFR)
     compare(out, rout, dtype, "out")
     compare(lse, rlse, dtype, "lse")
     dX, dWl, dWr, da = sga.gatv2_bwd(plan, gX, gWl, gWr, ga, FL, FR, out, lse, gdO, slope)
     g = oracle.gatv2_bwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope, store=dtype)
-    # dX, dW and da are sums over many edges or nodes: in fp32 the bound gains
-    # a relative term of 1e-5 (fp32 summation error grows with the magnitude)
-    rt = 1e-5 if dtype == "f32" else None
-    compare(dX, g["dX"], dtype, "dX", rtol=rt)
-    compare(dWl, g["dW_l"], dtype, "dW_l", rtol=rt)
-    compare(dWr, g["dW_r"], dtype, "dW_r", rtol=rt)
-    compare(da, g["da"], dtype, "da", rtol=rt)
+    # dX, dW and da are sums over many edges or nodes of terms that carry the
+    # fp32 rounding of the recomputed weights (relative ~1e-6): in fp32 the
+    # bound gains 1e-5 |ref| + 4e-6 max|ref| (about 64 float ulps of the
+    # largest entry).  bf16 keeps the stated 2e-2 + 1e-2 |ref|.
+    # LeakyReLU branches left undecided by the projections' storage precision
+    # may go either way: the oracle's slack bounds their effect.
+    rt, nm = (1e-5, 4e-6) if dtype == "f32" else (None, 0.0)
+    sl = oracle.gatv2_branch_slack(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope,
+                                   store=dtype)
+    compare(dX, g["dX"], dtype, "dX", rtol=rt, norm=nm, slack=sl["dX"])
+    compare(dWl, g["dW_l"], dtype, "dW_l", rtol=rt, norm=nm, slack=sl["dW_l"])
+    compare(dWr, g["dW_r"], dtype, "dW_r", rtol=rt, norm=nm, slack=sl["dW_r"])
+    compare(da, g["da"], dtype, "da", rtol=rt, norm=nm, slack=sl["da"])
     assert plan.device_error() == 0
     return plan
 

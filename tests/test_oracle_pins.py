@@ -375,3 +375,36 @@ def test_gatv2_stored_projection_rounding():
     o2, l2 = oracle.gatv2_fwd_rows(indptr, indices, rl, rr, a, np.arange(N))
     np.testing.assert_array_equal(out, o2)
     np.testing.assert_array_equal(lse, l2)
+
+
+def test_gatv2_branch_slack_bounds_flipped_branches():
+    """Move one source's projection across z = 0 for one edge element: the
+    gradient change equals the slack computed on either side (one undecided
+    element), and the slack is zero when no element is near z = 0."""
+    rng = np.random.default_rng(23)
+    N, F, H, D = 6, 3, 1, 2
+    indptr = np.array([0, 2, 3, 4, 5, 6, 7], np.int32)
+    indices = np.array([1, 2, 2, 3, 4, 5, 0], np.int32)
+    X = rng.standard_normal((N, F)); Wl = rng.standard_normal((F, H * D))
+    Wr = rng.standard_normal((F, H * D)); a = rng.standard_normal((H, D))
+    dO = rng.standard_normal((N, H, D))
+    far = oracle.gatv2_branch_slack(indptr, indices, X, Wl, Wr, a, dO, store=None, tau=1e-9)
+    for v in far.values():
+        assert np.all(v == 0.0)
+    # make z of (row 0, source 1, d = 0) straddle zero: fr_1 = -fl_0 +/- eps
+    FL = X @ Wl
+    FR = X @ Wr
+    eps = 1e-9
+    res = {}
+    for sign in (+1, -1):
+        target = -FL[0, 0] + sign * eps
+        # adjust X[1] along a direction that only changes FR[1, 0] (solve with the pseudo-inverse)
+        X2 = X.copy()
+        delta = np.zeros(H * D); delta[0] = target - FR[1, 0]
+        X2[1] += np.linalg.lstsq(Wr.T, delta, rcond=None)[0]
+        res[sign] = (X2, oracle.gatv2_bwd(indptr, indices, X2, Wl, Wr, a, dO))
+    diff = np.abs(res[1][1]["dW_l"] - res[-1][1]["dW_l"])
+    sl = oracle.gatv2_branch_slack(indptr, indices, res[1][0], Wl, Wr, a, dO, store=None, tau=1e-6)
+    assert diff.max() > 1e-3                       # the branch matters
+    assert np.all(diff <= sl["dW_l"] * (1 + 1e-6) + 1e-7)
+    assert sl["dW_l"].max() <= diff.max() * (1 + 1e-6) + 1e-7   # and the bound is tight here
