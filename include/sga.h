@@ -50,7 +50,8 @@ typedef enum {
     SGA_EUNSUPPORTED = 2,   /* shape or dtype outside the supported set */
     SGA_ECUDA = 3,          /* a CUDA runtime call failed */
     SGA_EWORKSPACE = 4,     /* workspace missing or smaller than sga_plan_workspace_bytes() */
-    SGA_EDEVICE_CHECK = 5   /* a device-side range check fired (see sga_read_device_error) */
+    SGA_EDEVICE_CHECK = 5,  /* a device-side range check fired (see sga_read_device_error) */
+    SGA_ELIMIT = 6          /* input needs more than gt_attn_fwd_noalloc's fixed scratch */
 } sga_status;
 
 typedef enum { SGA_F32 = 0, SGA_BF16 = 1 } sga_dtype;
@@ -133,6 +134,39 @@ int sga_last_cuda_error(void);
  * plan's device error word.  This call synchronises `stream`, reads the word
  * into *code, clears it, and returns SGA_EDEVICE_CHECK if it was non-zero. */
 sga_status sga_read_device_error(const sga_plan *plan, void *stream, int32_t *code);
+
+/* ---- forward without allocation ------------------------------------------
+ *
+ * No counterpart on the pages: this entry point exists for callers that must
+ * not allocate device memory -- an engine that reserved all of its memory up
+ * front, a plugin running inside another runtime that owns the device
+ * memory, or a latency-critical loop that cannot afford cudaMalloc's implicit
+ * device synchronisation.  It computes exactly what gt_attn_fwd computes
+ * (same kernels) but needs no plan and no workspace: the split-row partition
+ * and the chunk partials live in one file-scope static device array of
+ * 32 MiB (sga_noalloc_scratch_bytes()), which every GPU that loads this
+ * library holds until the process exits.
+ *
+ * Fixed choices and limits: rows of degree > 1024 are split into chunks of
+ * 1024 edges; at most 4096 split rows and at most
+ * 24 MiB / ((H*D + 2*H) * 4 bytes) chunks per call.  Larger inputs are
+ * rejected with SGA_ELIMIT before any edge kernel runs.  The CSR is validated
+ * on the device (SGA_EINVAL if invalid).
+ *
+ * Behaviour: the call synchronises `stream` once (to read the split count),
+ * then launches the edge kernels asynchronously on it.  The first call on a
+ * device looks up the array's device address for that device (with that
+ * device current), so make the first call before any stream capture.  Every
+ * call shares the one array and finds the previous call's data in it: calls
+ * that can overlap on the GPU (other streams, other host threads) race and
+ * must be serialised by the caller.  Allocates nothing: no cudaMalloc,
+ * cudaFree or allocating library routine. */
+sga_status gt_attn_fwd_noalloc(const int32_t *indptr, const int32_t *indices, const void *Q,
+                               const void *K, const void *V, int64_t N, int64_t E, int H, int D,
+                               sga_dtype dt, void *out, float *lse, void *stream);
+
+/* Size in bytes of the static scratch array behind gt_attn_fwd_noalloc. */
+size_t sga_noalloc_scratch_bytes(void);
 
 /* ---- plan inspection (tests) -------------------------------------------- */
 

@@ -19,7 +19,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libsga.so")
 
-SGA_OK, SGA_EINVAL, SGA_EUNSUPPORTED, SGA_ECUDA, SGA_EWORKSPACE, SGA_EDEVICE_CHECK = range(6)
+SGA_OK, SGA_EINVAL, SGA_EUNSUPPORTED, SGA_ECUDA, SGA_EWORKSPACE, SGA_EDEVICE_CHECK, SGA_ELIMIT = range(7)
 SGA_F32, SGA_BF16 = 0, 1
 
 KERNELS = {
@@ -82,6 +82,9 @@ _SIGNATURES = {
                    _vp, _vp, _vp, _vp, _vp], _int),
     "gatv2_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int,
                    _int, _int, _f32, _int, _vp, _vp, _vp, _vp, _vp], _int),
+    "gt_attn_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp],
+                            _int),
+    "sga_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "sga_profile_start": ([_int], _int),
     "sga_profile_stop": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64)], _int),
 }
@@ -254,6 +257,25 @@ def gt_attn_bwd(plan: Plan, Q, K, V, out, lse, dOut, dQ=None, dK=None, dV=None, 
                               plan.dt, _ptr(dQ), _ptr(dK), _ptr(dV), _stream(stream)),
            "gt_attn_bwd")
     return dQ, dK, dV
+
+
+def gt_attn_fwd_noalloc(indptr, indices, Q, K, V, out=None, lse=None, stream=None):
+    """Graph Transformer forward without a plan or workspace, for callers that
+    must not allocate device memory (the library uses a fixed static device
+    array instead; see include/sga.h).  Passing ``out`` and ``lse`` keeps this
+    call free of allocations on the Python side too.  Synchronises the stream
+    once.  Returns (out, lse)."""
+    _need(indptr, "indptr", torch.int32)
+    _need(indices, "indices", torch.int32)
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _need(t, n, Q.dtype)
+    N, H, D = Q.shape
+    out = torch.empty_like(Q) if out is None else out
+    lse = torch.empty((N, H), dtype=torch.float32, device=Q.device) if lse is None else lse
+    _check(_lib().gt_attn_fwd_noalloc(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), N,
+                                      indices.numel(), H, D, _dtype_code(Q), _ptr(out), _ptr(lse),
+                                      _stream(stream)), "gt_attn_fwd_noalloc")
+    return out, lse
 
 
 # ----------------------------------------------------------------------- GATv2

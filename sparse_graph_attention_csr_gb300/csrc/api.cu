@@ -145,6 +145,7 @@ const char *sga_status_string(sga_status s) {
         case SGA_ECUDA: return "CUDA runtime error";
         case SGA_EWORKSPACE: return "workspace missing or too small";
         case SGA_EDEVICE_CHECK: return "device range check failed";
+        case SGA_ELIMIT: return "input exceeds the fixed scratch of the no-allocation entry point";
     }
     return "unknown status";
 }
