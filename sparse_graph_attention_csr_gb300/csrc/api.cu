@@ -61,6 +61,10 @@ void compute_layout(sga_plan *p) {
         L.da_part = take((size_t)L.da_blocks * HD * 4);
         L.da_split = take((size_t)p->rows.n_split * HD * 4);
         L.dw_part = take((size_t)2 * L.dw_slabs * p->F * HD * 4);
+        // about 0.6% of the projection outputs need exact rounding; room for 2%
+        const int64_t cap = std::max<int64_t>(4096, (int64_t)p->N * HD * 2 / 50);
+        L.fix_cap = (int32_t)std::min<int64_t>(cap, INT32_MAX / 16);
+        L.fix = take(256 + (size_t)L.fix_cap * 8);
     }
     L.total = off;
 }
@@ -365,6 +369,9 @@ static Gatv2Args gatv2_args(const sga_plan *p, float slope) {
         a.ws_dw = ws_at<float>(p, p->layout.dw_part);
         a.ws_dfl = ws_at<float>(p, p->layout.dfl);
         a.ws_dfr = ws_at<float>(p, p->layout.dfr);
+        a.ws_fix_count = ws_at<int32_t>(p, p->layout.fix);
+        a.ws_fix_list = ws_at<int2>(p, p->layout.fix + 256);
+        a.fix_cap = p->layout.fix_cap;
     }
     return a;
 }

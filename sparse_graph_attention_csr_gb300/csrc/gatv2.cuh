@@ -16,6 +16,7 @@
 // xor shuffles.
 #pragma once
 
+#include "gemm.cuh"
 #include "gt.cuh"
 
 namespace sga {
@@ -23,137 +24,156 @@ namespace sga {
 // --------------------------------------------------------------- edge fwd
 
 template <typename T, int D, int NC, int G>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 gatv2_fwd_kernel(Gatv2Args a) {
     using S = GtShape<T, D, NC, G>;
     constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
-    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    ItemRange it;
-    if (!decode_item(item, a.rows, a.indptr, a.N, a.split_threshold, it)) return;
-    const int R = a.H * D / EL;
+    const int R = a.H * D / EL, HD = a.H * D;
     const uint4 *__restrict__ FRc = static_cast<const uint4 *>(a.FR);
     const float slope = a.slope;
+    const int64_t n_items = (int64_t)a.rows.n_chunks + a.N;
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
+    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemMeta mn, mnn;
+    meta_issue(item, a.rows, a.indptr, a.N, mn);
+    ItemRange it;
+    bool valid = meta_eval(item, mn, a.rows, a.split_threshold, it);
+    int32_t id0 = first_ids(a.indices, it, valid);
+    meta_issue(item + stride, a.rows, a.indptr, a.N, mn);
+    for (; item < n_items; item += stride) {
+        meta_issue(item + 2 * stride, a.rows, a.indptr, a.N, mnn);
+        ItemRange itn;
+        const bool validn = meta_eval(item + stride, mn, a.rows, a.split_threshold, itn);
+        const int32_t id1 = first_ids(a.indices, itn, validn);
+        if (valid) {
 
-    float fl[NC][EL], att[NC][EL], acc[NC][EL], m[NC], l[NC];
-#pragma unroll
-    for (int k = 0; k < NC; ++k) {
-        const int c = gl + G * k;
-        if (c < R) {
-            unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + (size_t)it.row * R + c), fl[k]);
-            unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
-        } else {
-#pragma unroll
-            for (int x = 0; x < EL; ++x) fl[k][x] = att[k][x] = 0.f;
-        }
-#pragma unroll
-        for (int x = 0; x < EL; ++x) {
-            acc[k][x] = 0.f;
-            att[k][x] *= kLog2e;   // scores directly in log2 units
-        }
-        m[k] = -INFINITY;
-        l[k] = 0.f;
-    }
-
-    for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-        const int cnt = min(32, it.end - e0);
-        const int32_t myj = load_ids(a.indices, e0, cnt, a.N, a.d_err);
-        for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-            uint4 fr[U][NC];
-            bool ok[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int t = t0 + g + NG * u;
-                const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
-                ok[u] = (t < cnt) && (j >= 0);
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int c = gl + G * k;
-                    fr[u][k] = (ok[u] && c < R) ? ldg16_stream(FRc + (size_t)j * R + c)
-                                                : make_uint4(0, 0, 0, 0);
-                }
-            }
-            float s[U][NC];
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    float f[EL];
-                    unpack<T>(fr[u][k], f);
-                    float e = 0.f;
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        const float z = fl[k][x] + f[x];
-                        e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
-                    }
-                    e = group_sum<LH>(e);
-                    s[u][k] = ok[u] ? e : -INFINITY;
-                }
+            float fl[NC][EL], att[NC][EL], acc[NC][EL], m[NC], l[NC];
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
-                float mx = m[k];
+                const int c = gl + G * k;
+                if (c < R) {
+                    unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + (size_t)it.row * R + c), fl[k]);
+                    unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
+                } else {
 #pragma unroll
-                for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][k]);
-                if (mx == -INFINITY) continue;
-                const float alpha = exp2_diff(m[k], mx);
-                l[k] *= alpha;
-#pragma unroll
-                for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const float p = exp2_diff(s[u][k], mx);
-                    l[k] += p;
-                    float f[EL];
-                    unpack<T>(fr[u][k], f);
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, f[x], acc[k][x]);
+                    for (int x = 0; x < EL; ++x) fl[k][x] = att[k][x] = 0.f;
                 }
-                m[k] = mx;
+#pragma unroll
+                for (int x = 0; x < EL; ++x) {
+                    acc[k][x] = 0.f;
+                    att[k][x] *= kLog2e;   // scores directly in log2 units
+                }
+                m[k] = -INFINITY;
+                l[k] = 0.f;
             }
-        }
-    }
+
+            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+                const int cnt = min(32, it.end - e0);
+                const int32_t myj = batch_ids(a.indices, e0, cnt, it, id0, a.N, a.d_err);
+                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+                    uint4 fr[U][NC];
+                    bool ok[U];
 #pragma unroll
-    for (int off = G; off < 32; off <<= 1)
+                    for (int u = 0; u < U; ++u) {
+                        const int t = t0 + g + NG * u;
+                        const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
+                        ok[u] = (t < cnt) && (j >= 0);
 #pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
-            const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
-            const float mx = fmaxf(m[k], mo);
-            const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
-            l[k] = l[k] * a1 + lo * a2;
+                        for (int k = 0; k < NC; ++k) {
+                            const int c = gl + G * k;
+                            fr[u][k] = (ok[u] && c < R) ? ldg16_stream(FRc + (size_t)j * R + c)
+                                                        : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    float s[U][NC];
 #pragma unroll
-            for (int x = 0; x < EL; ++x) {
-                const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
-                acc[k][x] = acc[k][x] * a1 + ao * a2;
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int k = 0; k < NC; ++k) {
+                            float f[EL];
+                            unpack<T>(fr[u][k], f);
+                            float e = 0.f;
+#pragma unroll
+                            for (int x = 0; x < EL; ++x) {
+                                const float z = fl[k][x] + f[x];
+                                e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
+                            }
+                            e = group_sum<LH>(e);
+                            s[u][k] = ok[u] ? e : -INFINITY;
+                        }
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        float mx = m[k];
+#pragma unroll
+                        for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][k]);
+                        if (mx == -INFINITY) continue;
+                        const float alpha = exp2_diff(m[k], mx);
+                        l[k] *= alpha;
+#pragma unroll
+                        for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
+#pragma unroll
+                        for (int u = 0; u < U; ++u) {
+                            const float p = exp2_diff(s[u][k], mx);
+                            l[k] += p;
+                            float f[EL];
+                            unpack<T>(fr[u][k], f);
+#pragma unroll
+                            for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, f[x], acc[k][x]);
+                        }
+                        m[k] = mx;
+                    }
+                }
             }
-            m[k] = mx;
-        }
-    if (g != 0) return;
-    const int HD = a.H * D;
 #pragma unroll
-    for (int k = 0; k < NC; ++k) {
-        const int c = gl + G * k;
-        if (c >= R) continue;
-        const int h = c / LH;
-        if (it.partial) {
-            float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)item * HD + c * EL);
+            for (int off = G; off < 32; off <<= 1)
 #pragma unroll
-            for (int x = 0; x < EL; x += 4)
-                dst[x / 4] = make_float4(acc[k][x], acc[k][x + 1], acc[k][x + 2], acc[k][x + 3]);
-            if (c % LH == 0) {
-                a.ws_ml[((size_t)item * a.H + h) * 2 + 0] = m[k];
-                a.ws_ml[((size_t)item * a.H + h) * 2 + 1] = l[k];
+                for (int k = 0; k < NC; ++k) {
+                    const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
+                    const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
+                    const float mx = fmaxf(m[k], mo);
+                    const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
+                    l[k] = l[k] * a1 + lo * a2;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
+                        acc[k][x] = acc[k][x] * a1 + ao * a2;
+                    }
+                    m[k] = mx;
+                }
+            if (g == 0) {
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                const int c = gl + G * k;
+                if (c >= R) continue;
+                const int h = c / LH;
+                if (it.partial) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)item * HD + c * EL);
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(acc[k][x], acc[k][x + 1], acc[k][x + 2], acc[k][x + 3]);
+                    if (c % LH == 0) {
+                        a.ws_ml[((size_t)item * a.H + h) * 2 + 0] = m[k];
+                        a.ws_ml[((size_t)item * a.H + h) * 2 + 1] = l[k];
+                    }
+                } else {
+                    const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
+                    float o[EL];
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) o[x] = acc[k][x] * inv;
+                    reinterpret_cast<uint4 *>(a.out_w)[(size_t)it.row * R + c] = pack<T>(o);
+                    if (c % LH == 0)
+                        a.lse_w[(size_t)it.row * a.H + h] =
+                            l[k] > 0.f ? (m[k] + log2f(l[k])) * kLn2 : -INFINITY;
+                }
             }
-        } else {
-            const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
-            float o[EL];
-#pragma unroll
-            for (int x = 0; x < EL; ++x) o[x] = acc[k][x] * inv;
-            reinterpret_cast<uint4 *>(a.out_w)[(size_t)it.row * R + c] = pack<T>(o);
-            if (c % LH == 0)
-                a.lse_w[(size_t)it.row * a.H + h] =
-                    l[k] > 0.f ? (m[k] + log2f(l[k])) * kLn2 : -INFINITY;
+            }
+
         }
+        it = itn;
+        valid = validn;
+        id0 = id1;
+        mn = mnn;
     }
 }
 
@@ -167,7 +187,7 @@ gatv2_fwd_kernel(Gatv2Args a) {
 // items; each block leaves one fp32 partial of da.  Split-row chunks write
 // their four partial sums and their part of Delta for the merge kernel.
 template <typename T, int D, int NC, int G>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 gatv2_bwd_dst_kernel(Gatv2Args a) {
     using S = GtShape<T, D, NC, G>;
     constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
@@ -193,143 +213,158 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
 
     const int64_t n_items = (int64_t)a.rows.n_chunks + a.N;
     const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
-    for (int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5); item < n_items;
-         item += stride) {
-        ItemRange it;
-        if (!decode_item(item, a.rows, a.indptr, a.N, a.split_threshold, it)) continue;
-        // fA/fB: dFL sums, gA/gB: da sums (A weighted by p dp, B by p), c: Delta part
-        float fl[NC][EL], go[NC][EL], fA[NC][EL], fB[NC][EL], gA[NC][EL], gB[NC][EL];
-        float c[NC], lse2[NC];
-#pragma unroll
-        for (int k = 0; k < NC; ++k) {
-            const int ch = gl + G * k;
-            if (ch < R) {
-                const size_t off = (size_t)it.row * R + ch;
-                unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + off), fl[k]);
-                unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
-                lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + ch / LH) * kLog2e;
-            } else {
-#pragma unroll
-                for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = 0.f;
-                lse2[k] = 0.f;
-            }
-#pragma unroll
-            for (int x = 0; x < EL; ++x) fA[k][x] = fB[k][x] = gA[k][x] = gB[k][x] = 0.f;
-            c[k] = 0.f;
-        }
-        for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-            const int cnt = min(32, it.end - e0);
-            const int32_t myj = load_ids(a.indices, e0, cnt, a.N, a.d_err);
-            for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-                uint4 fr[U][NC];
-                bool ok[U];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    const int t = t0 + g + NG * u;
-                    const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
-                    ok[u] = (t < cnt) && (j >= 0);
-#pragma unroll
-                    for (int k = 0; k < NC; ++k) {
-                        const int ch = gl + G * k;
-                        fr[u][k] = (ok[u] && ch < R) ? ldg16_stream(FRc + (size_t)j * R + ch)
-                                                     : make_uint4(0, 0, 0, 0);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int k = 0; k < NC; ++k) {
-                        float f[EL];
-                        unpack<T>(fr[u][k], f);
-                        float e = 0.f, dp = 0.f;
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) {
-                            const float z = fl[k][x] + f[x];
-                            e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
-                            dp = fmaf(go[k][x], f[x], dp);
-                        }
-                        group_sum2<LH>(e, dp);
-                        const float p = ok[u] ? exp2f(e * kLog2e - lse2[k]) : 0.f;
-                        const float pdp = p * dp;
-                        c[k] += pdp;
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) {
-                            const float z = fl[k][x] + f[x];
-                            const bool pos = z > 0.f;
-                            const float ag = pos ? att[k][x] : slope * att[k][x];
-                            const float lz = pos ? z : slope * z;
-                            fA[k][x] = fmaf(pdp, ag, fA[k][x]);
-                            fB[k][x] = fmaf(p, ag, fB[k][x]);
-                            gA[k][x] = fmaf(pdp, lz, gA[k][x]);
-                            gB[k][x] = fmaf(p, lz, gB[k][x]);
-                        }
-                    }
-            }
-        }
-        // Delta and the dFL sums over the whole warp (all edge groups)
-#pragma unroll
-        for (int off = G; off < 32; off <<= 1)
+    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemMeta mn, mnn;
+    meta_issue(item, a.rows, a.indptr, a.N, mn);
+    ItemRange it;
+    bool valid = meta_eval(item, mn, a.rows, a.split_threshold, it);
+    int32_t id0 = first_ids(a.indices, it, valid);
+    meta_issue(item + stride, a.rows, a.indptr, a.N, mn);
+    for (; item < n_items; item += stride) {
+        meta_issue(item + 2 * stride, a.rows, a.indptr, a.N, mnn);
+        ItemRange itn;
+        const bool validn = meta_eval(item + stride, mn, a.rows, a.split_threshold, itn);
+        const int32_t id1 = first_ids(a.indices, itn, validn);
+        if (valid) {
+            // fA/fB: dFL sums, gA/gB: da sums (A weighted by p dp, B by p), c: Delta part
+            float fl[NC][EL], go[NC][EL], fA[NC][EL], fB[NC][EL], gA[NC][EL], gB[NC][EL];
+            float c[NC], lse2[NC];
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
-                c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
+                const int ch = gl + G * k;
+                if (ch < R) {
+                    const size_t off = (size_t)it.row * R + ch;
+                    unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + off), fl[k]);
+                    unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
+                    lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + ch / LH) * kLog2e;
+                } else {
 #pragma unroll
-                for (int x = 0; x < EL; ++x) {
-                    fA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fA[k][x], off);
-                    fB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fB[k][x], off);
+                    for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = 0.f;
+                    lse2[k] = 0.f;
+                }
+#pragma unroll
+                for (int x = 0; x < EL; ++x) fA[k][x] = fB[k][x] = gA[k][x] = gB[k][x] = 0.f;
+                c[k] = 0.f;
+            }
+            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+                const int cnt = min(32, it.end - e0);
+                const int32_t myj = batch_ids(a.indices, e0, cnt, it, id0, a.N, a.d_err);
+                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+                    uint4 fr[U][NC];
+                    bool ok[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int t = t0 + g + NG * u;
+                        const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
+                        ok[u] = (t < cnt) && (j >= 0);
+#pragma unroll
+                        for (int k = 0; k < NC; ++k) {
+                            const int ch = gl + G * k;
+                            fr[u][k] = (ok[u] && ch < R) ? ldg16_stream(FRc + (size_t)j * R + ch)
+                                                         : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int k = 0; k < NC; ++k) {
+                            float f[EL];
+                            unpack<T>(fr[u][k], f);
+                            float e = 0.f, dp = 0.f;
+#pragma unroll
+                            for (int x = 0; x < EL; ++x) {
+                                const float z = fl[k][x] + f[x];
+                                e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
+                                dp = fmaf(go[k][x], f[x], dp);
+                            }
+                            group_sum2<LH>(e, dp);
+                            const float p = ok[u] ? exp2f(e * kLog2e - lse2[k]) : 0.f;
+                            const float pdp = p * dp;
+                            c[k] += pdp;
+#pragma unroll
+                            for (int x = 0; x < EL; ++x) {
+                                const float z = fl[k][x] + f[x];
+                                const bool pos = z > 0.f;
+                                const float ag = pos ? att[k][x] : slope * att[k][x];
+                                const float lz = pos ? z : slope * z;
+                                fA[k][x] = fmaf(pdp, ag, fA[k][x]);
+                                fB[k][x] = fmaf(p, ag, fB[k][x]);
+                                gA[k][x] = fmaf(pdp, lz, gA[k][x]);
+                                gB[k][x] = fmaf(p, lz, gB[k][x]);
+                            }
+                        }
                 }
             }
-        if (it.partial) {
-            // da sums of this chunk, combined over the groups, go to the merge kernel
+            // Delta and the dFL sums over the whole warp (all edge groups)
 #pragma unroll
             for (int off = G; off < 32; off <<= 1)
 #pragma unroll
-                for (int k = 0; k < NC; ++k)
+                for (int k = 0; k < NC; ++k) {
+                    c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
 #pragma unroll
                     for (int x = 0; x < EL; ++x) {
-                        gA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gA[k][x], off);
-                        gB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gB[k][x], off);
+                        fA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fA[k][x], off);
+                        fB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fB[k][x], off);
                     }
-            if (g == 0) {
+                }
+            if (it.partial) {
+                // da sums of this chunk, combined over the groups, go to the merge kernel
 #pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int ch = gl + G * k;
-                    if (ch >= R) continue;
-                    float *base = a.ws_row + (size_t)item * 4 * HD + ch * EL;
+                for (int off = G; off < 32; off <<= 1)
 #pragma unroll
-                    for (int x = 0; x < EL; x += 4) {
-                        *reinterpret_cast<float4 *>(base + x) =
-                            make_float4(fA[k][x], fA[k][x + 1], fA[k][x + 2], fA[k][x + 3]);
-                        *reinterpret_cast<float4 *>(base + HD + x) =
-                            make_float4(fB[k][x], fB[k][x + 1], fB[k][x + 2], fB[k][x + 3]);
-                        *reinterpret_cast<float4 *>(base + 2 * HD + x) =
-                            make_float4(gA[k][x], gA[k][x + 1], gA[k][x + 2], gA[k][x + 3]);
-                        *reinterpret_cast<float4 *>(base + 3 * HD + x) =
-                            make_float4(gB[k][x], gB[k][x + 1], gB[k][x + 2], gB[k][x + 3]);
+                    for (int k = 0; k < NC; ++k)
+#pragma unroll
+                        for (int x = 0; x < EL; ++x) {
+                            gA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gA[k][x], off);
+                            gB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gB[k][x], off);
+                        }
+                if (g == 0) {
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        const int ch = gl + G * k;
+                        if (ch >= R) continue;
+                        float *base = a.ws_row + (size_t)item * 4 * HD + ch * EL;
+#pragma unroll
+                        for (int x = 0; x < EL; x += 4) {
+                            *reinterpret_cast<float4 *>(base + x) =
+                                make_float4(fA[k][x], fA[k][x + 1], fA[k][x + 2], fA[k][x + 3]);
+                            *reinterpret_cast<float4 *>(base + HD + x) =
+                                make_float4(fB[k][x], fB[k][x + 1], fB[k][x + 2], fB[k][x + 3]);
+                            *reinterpret_cast<float4 *>(base + 2 * HD + x) =
+                                make_float4(gA[k][x], gA[k][x + 1], gA[k][x + 2], gA[k][x + 3]);
+                            *reinterpret_cast<float4 *>(base + 3 * HD + x) =
+                                make_float4(gB[k][x], gB[k][x + 1], gB[k][x + 2], gB[k][x + 3]);
+                        }
+                        if (ch % LH == 0) a.ws_rowc[(size_t)item * a.H + ch / LH] = c[k];
                     }
-                    if (ch % LH == 0) a.ws_rowc[(size_t)item * a.H + ch / LH] = c[k];
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < NC; ++k)
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) dacc[k][x] += gA[k][x] - c[k] * gB[k][x];
+                if (g == 0) {
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        const int ch = gl + G * k;
+                        if (ch >= R) continue;
+                        float4 *dst = reinterpret_cast<float4 *>(a.ws_dfl + (size_t)it.row * HD + ch * EL);
+#pragma unroll
+                        for (int x = 0; x < EL; x += 4)
+                            dst[x / 4] = make_float4(fA[k][x] - c[k] * fB[k][x],
+                                                     fA[k][x + 1] - c[k] * fB[k][x + 1],
+                                                     fA[k][x + 2] - c[k] * fB[k][x + 2],
+                                                     fA[k][x + 3] - c[k] * fB[k][x + 3]);
+                        if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
+                    }
                 }
             }
-        } else {
-#pragma unroll
-            for (int k = 0; k < NC; ++k)
-#pragma unroll
-                for (int x = 0; x < EL; ++x) dacc[k][x] += gA[k][x] - c[k] * gB[k][x];
-            if (g == 0) {
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int ch = gl + G * k;
-                    if (ch >= R) continue;
-                    float4 *dst = reinterpret_cast<float4 *>(a.ws_dfl + (size_t)it.row * HD + ch * EL);
-#pragma unroll
-                    for (int x = 0; x < EL; x += 4)
-                        dst[x / 4] = make_float4(fA[k][x] - c[k] * fB[k][x],
-                                                 fA[k][x + 1] - c[k] * fB[k][x + 1],
-                                                 fA[k][x + 2] - c[k] * fB[k][x + 2],
-                                                 fA[k][x + 3] - c[k] * fB[k][x + 3]);
-                    if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
-                }
-            }
+
         }
+        it = itn;
+        valid = validn;
+        id0 = id1;
+        mn = mnn;
     }
     // da: groups -> lanes of group 0, warps -> shared memory in warp order
 #pragma unroll
@@ -360,177 +395,178 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
 // Per source j over its destinations i (transposed CSR):
 //   dFR_j += p dOut_i + de a * LReLU'(z).
 template <typename T, int D, int NC, int G>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 gatv2_bwd_src_kernel(Gatv2Args a) {
     using S = GtShape<T, D, NC, G>;
     constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
-    const int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    ItemRange it;
-    if (!decode_item(item, a.cols, a.t_indptr, a.N, a.split_threshold, it)) return;
-    const int R = a.H * D / EL;
+    const int R = a.H * D / EL, HD = a.H * D;
     const float slope = a.slope;
     const uint4 *__restrict__ FLc = static_cast<const uint4 *>(a.FL);
     const uint4 *__restrict__ Gc = static_cast<const uint4 *>(a.dOut);
+    const int64_t n_items = (int64_t)a.cols.n_chunks + a.N;
+    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
+    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    ItemMeta mn, mnn;
+    meta_issue(item, a.cols, a.t_indptr, a.N, mn);
+    ItemRange it;
+    bool valid = meta_eval(item, mn, a.cols, a.split_threshold, it);
+    int32_t id0 = first_ids(a.t_dst, it, valid);
+    meta_issue(item + stride, a.cols, a.t_indptr, a.N, mn);
+    for (; item < n_items; item += stride) {
+        meta_issue(item + 2 * stride, a.cols, a.t_indptr, a.N, mnn);
+        ItemRange itn;
+        const bool validn = meta_eval(item + stride, mn, a.cols, a.split_threshold, itn);
+        const int32_t id1 = first_ids(a.t_dst, itn, validn);
+        if (valid) {
 
-    float frj[NC][EL], att[NC][EL], dfr[NC][EL];
+            float frj[NC][EL], att[NC][EL], dfr[NC][EL];
 #pragma unroll
-    for (int k = 0; k < NC; ++k) {
-        const int c = gl + G * k;
-        if (c < R) {
-            unpack<T>(ldg16(static_cast<const uint4 *>(a.FR) + (size_t)it.row * R + c), frj[k]);
-            unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
-        } else {
+            for (int k = 0; k < NC; ++k) {
+                const int c = gl + G * k;
+                if (c < R) {
+                    unpack<T>(ldg16(static_cast<const uint4 *>(a.FR) + (size_t)it.row * R + c), frj[k]);
+                    unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
+                } else {
 #pragma unroll
-            for (int x = 0; x < EL; ++x) frj[k][x] = att[k][x] = 0.f;
-        }
+                    for (int x = 0; x < EL; ++x) frj[k][x] = att[k][x] = 0.f;
+                }
 #pragma unroll
-        for (int x = 0; x < EL; ++x) dfr[k][x] = 0.f;
-    }
-    for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-        const int cnt = min(32, it.end - e0);
-        const int32_t myi = load_ids(a.t_dst, e0, cnt, a.N, a.d_err);
-        for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-            uint4 flr[U][NC], gr[U][NC];
-            float l2[U][NC], dl[U][NC];
-            bool ok[U];
+                for (int x = 0; x < EL; ++x) dfr[k][x] = 0.f;
+            }
+            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
+                const int cnt = min(32, it.end - e0);
+                const int32_t myi = batch_ids(a.t_dst, e0, cnt, it, id0, a.N, a.d_err);
+                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
+                    uint4 flr[U][NC], gr[U][NC];
+                    float l2[U][NC], dl[U][NC];
+                    bool ok[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int t = t0 + g + NG * u;
-                const int32_t i = __shfl_sync(SGA_FULL_MASK, myi, t & 31);
-                ok[u] = (t < cnt) && (i >= 0);
+                    for (int u = 0; u < U; ++u) {
+                        const int t = t0 + g + NG * u;
+                        const int32_t i = __shfl_sync(SGA_FULL_MASK, myi, t & 31);
+                        ok[u] = (t < cnt) && (i >= 0);
 #pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int c = gl + G * k;
-                    if (ok[u] && c < R) {
-                        flr[u][k] = ldg16_stream(FLc + (size_t)i * R + c);
-                        gr[u][k] = ldg16_stream(Gc + (size_t)i * R + c);
-                        l2[u][k] = __ldg(a.lse + (size_t)i * a.H + c / LH);
-                        dl[u][k] = a.ws_delta[(size_t)i * a.H + c / LH];
-                    } else {
-                        flr[u][k] = make_uint4(0, 0, 0, 0);
-                        gr[u][k] = make_uint4(0, 0, 0, 0);
-                        l2[u][k] = 0.f;
-                        dl[u][k] = 0.f;
+                        for (int k = 0; k < NC; ++k) {
+                            const int c = gl + G * k;
+                            if (ok[u] && c < R) {
+                                flr[u][k] = ldg16_stream(FLc + (size_t)i * R + c);
+                                gr[u][k] = ldg16_stream(Gc + (size_t)i * R + c);
+                                l2[u][k] = __ldg(a.lse + (size_t)i * a.H + c / LH);
+                                dl[u][k] = a.ws_delta[(size_t)i * a.H + c / LH];
+                            } else {
+                                flr[u][k] = make_uint4(0, 0, 0, 0);
+                                gr[u][k] = make_uint4(0, 0, 0, 0);
+                                l2[u][k] = 0.f;
+                                dl[u][k] = 0.f;
+                            }
+                        }
                     }
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+#pragma unroll
+                        for (int k = 0; k < NC; ++k) {
+                            float f[EL], gf[EL];
+                            unpack<T>(flr[u][k], f);
+                            unpack<T>(gr[u][k], gf);
+                            float e = 0.f, dp = 0.f;
+#pragma unroll
+                            for (int x = 0; x < EL; ++x) {
+                                const float z = f[x] + frj[k][x];
+                                e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
+                                dp = fmaf(gf[x], frj[k][x], dp);
+                            }
+                            group_sum2<LH>(e, dp);
+                            const float p = ok[u] ? exp2f((e - l2[u][k]) * kLog2e) : 0.f;
+                            const float de = p * (dp - dl[u][k]);
+#pragma unroll
+                            for (int x = 0; x < EL; ++x) {
+                                const float z = f[x] + frj[k][x];
+                                dfr[k][x] = fmaf(p, gf[x], dfr[k][x]);
+                                dfr[k][x] = fmaf(de * att[k][x], z > 0.f ? 1.f : slope, dfr[k][x]);
+                            }
+                        }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u)
+            for (int off = G; off < 32; off <<= 1)
 #pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    float f[EL], gf[EL];
-                    unpack<T>(flr[u][k], f);
-                    unpack<T>(gr[u][k], gf);
-                    float e = 0.f, dp = 0.f;
+                for (int k = 0; k < NC; ++k)
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        const float z = f[x] + frj[k][x];
-                        e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
-                        dp = fmaf(gf[x], frj[k][x], dp);
-                    }
-                    group_sum2<LH>(e, dp);
-                    const float p = ok[u] ? exp2f((e - l2[u][k]) * kLog2e) : 0.f;
-                    const float de = p * (dp - dl[u][k]);
+                    for (int x = 0; x < EL; ++x) dfr[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dfr[k][x], off);
+            if (g == 0) {
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        const float z = f[x] + frj[k][x];
-                        dfr[k][x] = fmaf(p, gf[x], dfr[k][x]);
-                        dfr[k][x] = fmaf(de * att[k][x], z > 0.f ? 1.f : slope, dfr[k][x]);
-                    }
+            for (int k = 0; k < NC; ++k) {
+                const int c = gl + G * k;
+                if (c >= R) continue;
+                if (it.partial) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * HD + c * EL);
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_dfr + (size_t)it.row * HD + c * EL);
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
                 }
+            }
+            }
+
         }
-    }
-#pragma unroll
-    for (int off = G; off < 32; off <<= 1)
-#pragma unroll
-        for (int k = 0; k < NC; ++k)
-#pragma unroll
-            for (int x = 0; x < EL; ++x) dfr[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dfr[k][x], off);
-    if (g != 0) return;
-    const int HD = a.H * D;
-#pragma unroll
-    for (int k = 0; k < NC; ++k) {
-        const int c = gl + G * k;
-        if (c >= R) continue;
-        if (it.partial) {
-            float4 *dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * HD + c * EL);
-#pragma unroll
-            for (int x = 0; x < EL; x += 4)
-                dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
-        } else {
-            float4 *dst = reinterpret_cast<float4 *>(a.ws_dfr + (size_t)it.row * HD + c * EL);
-#pragma unroll
-            for (int x = 0; x < EL; x += 4)
-                dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
-        }
+        it = itn;
+        valid = validn;
+        id0 = id1;
+        mn = mnn;
     }
 }
 
-// Finish split rows in chunk order.  which == 0 (destination rows): Delta is
-// the sum of the chunk parts, dFL = sum fA - Delta sum fB, and the row's da
-// contribution sum gA - Delta sum gB goes to its own slot.  which == 1
+// Finish split rows, one block each.  which == 0 (destination rows): Delta
+// is the sum of the chunk parts, dFL = sum fA - Delta sum fB, and the row's
+// da contribution sum gA - Delta sum gB goes to its own slot.  which == 1
 // (sources): dFR is the plain sum of the chunk partials.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int which) {
     constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
-    const int lane = threadIdx.x & 31;
-    const int64_t s = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const int R = a.H * D / EL, HD = a.H * D;
+    __shared__ float sh[kWarpsPerBlock][4][32 * EL];
+    __shared__ float shc[kWarpsPerBlock][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t s = blockIdx.x;
     const Partition &P = which == 0 ? a.rows : a.cols;
     if (s >= P.n_split) return;
     const int32_t row = P.split_rows[s];
     const int32_t c0 = P.chunk_ptr[s], c1 = P.chunk_ptr[s + 1];
-    for (int c = lane; c < R; c += 32) {
+    const int R = a.H * D / EL, HD = a.H * D;
+    for (int cb = 0; cb < R; cb += 32) {
+        const int c = cb + lane;
         if (which == 1) {
-            float acc[EL];
+            float sum[1][EL], unused;
+            block_sum_chunks<EL, 1>(a.ws_col, 1, HD, nullptr, a.H, LH, c0, c1, c, c < R,
+                                    reinterpret_cast<float (*)[1][32 * EL]>(sh), shc, sum, unused);
+            if (w == 0 && c < R)
 #pragma unroll
-            for (int x = 0; x < EL; ++x) acc[x] = 0.f;
-#pragma unroll 4
-            for (int32_t ch = c0; ch < c1; ++ch) {
-                const float4 *src = reinterpret_cast<const float4 *>(a.ws_col + (size_t)ch * HD + c * EL);
+                for (int x = 0; x < EL; ++x) a.ws_dfr[(size_t)row * HD + c * EL + x] = sum[0][x];
+        } else {
+            float sum[4][EL], delta;
+            block_sum_chunks<EL, 4>(a.ws_row, 4, HD, a.ws_rowc, a.H, LH, c0, c1, c, c < R, sh, shc,
+                                    sum, delta);
+            if (w == 0 && c < R) {
 #pragma unroll
-                for (int x = 0; x < EL; x += 4) {
-                    const float4 v = src[x / 4];
-                    acc[x] += v.x; acc[x + 1] += v.y; acc[x + 2] += v.z; acc[x + 3] += v.w;
+                for (int x = 0; x < EL; ++x) {
+                    a.ws_dfl[(size_t)row * HD + c * EL + x] = sum[0][x] - delta * sum[1][x];
+                    a.ws_da_split[(size_t)s * HD + c * EL + x] = sum[2][x] - delta * sum[3][x];
                 }
-            }
-#pragma unroll
-            for (int x = 0; x < EL; ++x) a.ws_dfr[(size_t)row * HD + c * EL + x] = acc[x];
-            continue;
-        }
-        const int h = c / LH;
-        float delta = 0.f;
-        for (int32_t ch = c0; ch < c1; ++ch) delta += a.ws_rowc[(size_t)ch * a.H + h];
-        float sum[4][EL];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int x = 0; x < EL; ++x) sum[q][x] = 0.f;
-#pragma unroll 2
-        for (int32_t ch = c0; ch < c1; ++ch) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 *src =
-                    reinterpret_cast<const float4 *>(a.ws_row + ((size_t)ch * 4 + q) * HD + c * EL);
-#pragma unroll
-                for (int x = 0; x < EL; x += 4) {
-                    const float4 v = src[x / 4];
-                    sum[q][x] += v.x; sum[q][x + 1] += v.y; sum[q][x + 2] += v.z; sum[q][x + 3] += v.w;
-                }
+                if (c % LH == 0) a.ws_delta[(size_t)row * a.H + c / LH] = delta;
             }
         }
-#pragma unroll
-        for (int x = 0; x < EL; ++x) a.ws_dfl[(size_t)row * HD + c * EL + x] = sum[0][x] - delta * sum[1][x];
-#pragma unroll
-        for (int x = 0; x < EL; ++x) a.ws_da_split[(size_t)s * HD + c * EL + x] = sum[2][x] - delta * sum[3][x];
-        if (c % LH == 0) a.ws_delta[(size_t)row * a.H + h] = delta;
+        __syncthreads();
     }
 }
 
 // ------------------------------------------------------------ dense GEMMs
 
-// C = sum over pairs p of op(A_p) op(B_p) with fp32 accumulation (SIMT).
+// C = sum over pairs p of op(A_p) op(B_p) with fp32 accumulation (SIMT),
+// used for float layers, whose fp32 tolerance the bf16 tensor cores miss.
 //   A: [M, K] row-major, or [K, M] row-major when TA (then op(A) = A^T).
 //   B: [K, N] row-major, or [N, K] row-major when TB.
 // Tiles 64 x 64 x 16, 256 threads, 4 x 4 outputs per thread.  Rows [k0, k1)
@@ -545,44 +581,14 @@ template <typename TA_, typename TB_, typename T, bool TA, bool TB> struct GemmA
     int64_t k_per_slab;
     T *C;
     float *Cpart;
-    bool exact_bf16;   // correctly rounded bf16 C (see bf16_rounding_ambiguous); pairs == 1, one slab
 };
-
-// Correctly rounded bf16 outputs.  The fp32 accumulation of a k-term dot
-// product x . w differs from the exact value by a small multiple of
-// 2^-24 |x| |w| (|.| the Euclidean norm).  If every value within
-// B = 4 * 2^-24 |x| |w| + ulp(acc) of the fp32 sum rounds to the same bf16
-// number, that number is the correctly rounded result; otherwise (about 0.6%
-// of the elements for unit-scale inputs) the dot product is recomputed
-// exactly: products of bf16 or fp32 inputs are exact in fp64 and the k <= 1024
-// term sum stays far inside fp64 precision.  The fp64 value is rounded to
-// float and then to bf16 (ties to even).
-__device__ __forceinline__ bool bf16_rounding_ambiguous(float acc, float bound) {
-    const float b = bound + fabsf(acc) * 1.2e-7f;
-    return __float2bfloat16_rn(acc - b) != __float2bfloat16_rn(acc + b);
-}
-
-template <typename TA_, typename TB_, bool TA, bool TB, typename G>
-__device__ float exact_dot(const G &g, int64_t m, int64_t n) {
-    double s = 0.0;
-    for (int p = 0; p < g.pairs; ++p)
-        for (int64_t k = 0; k < g.K; ++k) {
-            const double x = (double)to_f32<TA_>(TA ? g.A[p][k * g.M + m] : g.A[p][m * g.K + k]);
-            const double y = (double)to_f32<TB_>(TB ? g.B[p][n * g.K + k] : g.B[p][k * g.N + n]);
-            s = fma(x, y, s);
-        }
-    return (float)s;
-}
 
 template <typename TA_, typename TB_, typename T, bool TA, bool TB>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<TA_, TB_, T, TA, TB> g) {
     constexpr int BM = 64, BN = 64, BK = 16;
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[BK][BN + 4];
-    __shared__ float rowsq[BM], colsq[BN];   // squared norms of the tile's rows / columns
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
-    if (g.exact_bf16 && threadIdx.x < BM) rowsq[threadIdx.x] = 0.f;
-    else if (g.exact_bf16 && threadIdx.x < BM + BN) colsq[threadIdx.x - BM] = 0.f;
     const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
     const int64_t k_lo = (int64_t)blockIdx.z * g.k_per_slab;
     const int64_t k_hi = min(g.K, k_lo + g.k_per_slab);
@@ -610,18 +616,6 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<TA_, TB_, T, TA
                 Bs[kk][nn] = v;
             }
             __syncthreads();
-            if (g.exact_bf16) {   // one thread per row / column, k in order: deterministic
-                if (threadIdx.x < BM) {
-                    float q = rowsq[threadIdx.x];
-                    for (int kk = 0; kk < BK; ++kk) q = fmaf(As[kk][threadIdx.x], As[kk][threadIdx.x], q);
-                    rowsq[threadIdx.x] = q;
-                } else if (threadIdx.x < BM + BN) {
-                    const int nn = threadIdx.x - BM;
-                    float q = colsq[nn];
-                    for (int kk = 0; kk < BK; ++kk) q = fmaf(Bs[kk][nn], Bs[kk][nn], q);
-                    colsq[nn] = q;
-                }
-            }
 #pragma unroll
             for (int kk = 0; kk < BK; ++kk) {
                 float av[4], bv[4];
@@ -646,10 +640,6 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<TA_, TB_, T, TA
             const int64_t gn = n0 + tx * 4 + c;
             if (gn >= g.N) continue;
             if (g.Cpart) g.Cpart[((int64_t)blockIdx.z * g.M + gm) * g.N + gn] = acc[r][c];
-            else if (g.exact_bf16 &&
-                     bf16_rounding_ambiguous(acc[r][c], 4.0f * 5.9604645e-8f *
-                                                            sqrtf(rowsq[ty * 4 + r] * colsq[tx * 4 + c])))
-                g.C[gm * g.N + gn] = from_f32<T>(exact_dot<TA_, TB_, TA, TB>(g, gm, gn));
             else g.C[gm * g.N + gn] = from_f32<T>(acc[r][c]);
         }
     }
@@ -693,17 +683,48 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
     constexpr int LH = D * (int)sizeof(T) / 16;
     const int R = a.H * D / Elt<T>::EL;
     const int HD = a.H * D;
-    // projections FL = X W_l, FR = X W_r
-    for (int w = 0; w < 2; ++w) {
-        GemmArgs<T, T, T, false, false> g{};
-        g.A[0] = static_cast<const T *>(a.X);
-        g.B[0] = static_cast<const T *>(w ? a.Wr : a.Wl);
-        g.pairs = 1;
-        g.M = a.N; g.N = HD; g.K = a.F; g.k_per_slab = a.F;
-        g.C = static_cast<T *>(w ? a.FR_w : a.FL_w);
-        g.Cpart = nullptr;
-        g.exact_bf16 = sizeof(T) == 2;
+    // projections FL = X W_l, FR = X W_r (bf16: tensor cores, correctly rounded)
+    if constexpr (sizeof(T) == 2) {
         if (a.N > 0) {
+            cudaError_t e = cudaMemsetAsync(a.ws_fix_count, 0, sizeof(int32_t), s);
+            for (int w = 0; w < 2 && e == cudaSuccess; ++w) {
+                MmaGemm<T, T, T, false, true, 0> g{};
+                g.A[0] = static_cast<const T *>(a.X);
+                g.B[0] = static_cast<const T *>(w ? a.Wr : a.Wl);
+                g.pairs = 1;
+                g.M = a.N; g.N = HD; g.K = a.F; g.k_per_slab = a.F;
+                g.C = static_cast<T *>(w ? a.FR_w : a.FL_w);
+                g.fix_count = a.ws_fix_count;
+                g.fix_list = a.ws_fix_list;
+                g.fix_cap = a.fix_cap;
+                g.fix_tag = w;
+                e = mma_gemm(g, 1, SGA_KERN_GATV2_PROJ, s);
+            }
+            if (e != cudaSuccess) return e;
+            ExactRound r{};
+            r.X = static_cast<const __nv_bfloat16 *>(a.X);
+            r.W[0] = static_cast<const __nv_bfloat16 *>(a.Wl);
+            r.W[1] = static_cast<const __nv_bfloat16 *>(a.Wr);
+            r.C[0] = static_cast<__nv_bfloat16 *>(a.FL_w);
+            r.C[1] = static_cast<__nv_bfloat16 *>(a.FR_w);
+            r.M = a.N; r.N = HD; r.K = a.F;
+            r.count = a.ws_fix_count;
+            r.list = a.ws_fix_list;
+            r.cap = a.fix_cap;
+            note_launch(SGA_KERN_GATV2_PROJ, s, false);
+            exact_round_kernel<<<persistent_blocks<exact_round_kernel>(1 << 30), 256, 0, s>>>(r);
+            note_launch(SGA_KERN_GATV2_PROJ, s, true);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+    } else {
+        for (int w = 0; w < 2 && a.N > 0; ++w) {
+            GemmArgs<T, T, T, false, false> g{};
+            g.A[0] = static_cast<const T *>(a.X);
+            g.B[0] = static_cast<const T *>(w ? a.Wr : a.Wl);
+            g.pairs = 1;
+            g.M = a.N; g.N = HD; g.K = a.F; g.k_per_slab = a.F;
+            g.C = static_cast<T *>(w ? a.FR_w : a.FL_w);
+            g.Cpart = nullptr;
             cudaError_t e = gemm(g, 1, SGA_KERN_GATV2_PROJ, s);
             if (e != cudaSuccess) return e;
         }
@@ -715,13 +736,14 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
         note_launch(SGA_KERN_GATV2_FWD, s, false);
-        gatv2_fwd_kernel<T, D, NC, G><<<blocks_for_warps(items), 256, 0, s>>>(b);
+        gatv2_fwd_kernel<T, D, NC, G>
+            <<<persistent_blocks<gatv2_fwd_kernel<T, D, NC, G>>(items), 256, 0, s>>>(b);
         note_launch(SGA_KERN_GATV2_FWD, s, true);
         return cudaGetLastError();
     });
     if (e != cudaSuccess || a.rows.n_split == 0) return e;
     note_launch(SGA_KERN_GATV2_FWD_MERGE, s, false);
-    gt_fwd_merge_kernel<T, D, Gatv2Args><<<blocks_for_warps(a.rows.n_split), 256, 0, s>>>(b);
+    gt_fwd_merge_kernel<T, D, Gatv2Args><<<(unsigned)a.rows.n_split, 256, 0, s>>>(b);
     note_launch(SGA_KERN_GATV2_FWD_MERGE, s, true);
     return cudaGetLastError();
 }
@@ -738,19 +760,20 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
         if (e2 != cudaSuccess) return e2;
         if (a.rows.n_split > 0) {   // Delta of split rows is needed by the source pass
             note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
-            gatv2_bwd_merge_kernel<T, D><<<blocks_for_warps(a.rows.n_split), 256, 0, s>>>(a, 0);
+            gatv2_bwd_merge_kernel<T, D><<<(unsigned)a.rows.n_split, 256, 0, s>>>(a, 0);
             note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
             if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
         }
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
         if (items_c == 0) return cudaSuccess;
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, false);
-        gatv2_bwd_src_kernel<T, D, NC, G><<<blocks_for_warps(items_c), 256, 0, s>>>(a);
+        gatv2_bwd_src_kernel<T, D, NC, G>
+            <<<persistent_blocks<gatv2_bwd_src_kernel<T, D, NC, G>>(items_c), 256, 0, s>>>(a);
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, true);
         if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
         if (a.cols.n_split > 0) {
             note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
-            gatv2_bwd_merge_kernel<T, D><<<blocks_for_warps(a.cols.n_split), 256, 0, s>>>(a, 1);
+            gatv2_bwd_merge_kernel<T, D><<<(unsigned)a.cols.n_split, 256, 0, s>>>(a, 1);
             note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
             e2 = cudaGetLastError();
         }
@@ -758,31 +781,50 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     });
     if (e != cudaSuccess) return e;
     // dX = dFL W_l^T + dFR W_r^T
-    if (a.N > 0) {
-        GemmArgs<float, T, T, false, true> g{};
-        g.A[0] = a.ws_dfl;
-        g.B[0] = static_cast<const T *>(a.Wl);
-        g.A[1] = a.ws_dfr;
-        g.B[1] = static_cast<const T *>(a.Wr);
-        g.pairs = 2;
-        g.M = a.N; g.N = a.F; g.K = HD; g.k_per_slab = HD;
-        g.C = static_cast<T *>(a.dX);
-        if ((e = gemm(g, 1, SGA_KERN_GATV2_BWD_DX, s)) != cudaSuccess) return e;
-    }
-    // dW = X^T dF over node slabs: fp32 partials [2][slab][F][HD]
     const int64_t per = (a.N + a.dw_slabs - 1) / a.dw_slabs;
     const int64_t FHD = (int64_t)a.F * HD;
-    {
-        // One launch per projection; each writes slab-major partials with a stride of 2*F*HD.
-        for (int w = 0; w < 2 && a.N > 0; ++w) {
-            GemmArgs<T, float, T, true, false> g{};
-            g.A[0] = static_cast<const T *>(a.X);
-            g.B[0] = w ? a.ws_dfr : a.ws_dfl;
-            g.pairs = 1;
-            g.M = a.F; g.N = HD; g.K = a.N; g.k_per_slab = per;
-            g.C = nullptr;
-            g.Cpart = a.ws_dw + (size_t)w * FHD * a.dw_slabs;
-            if ((e = gemm(g, a.dw_slabs, SGA_KERN_GATV2_BWD_DW, s)) != cudaSuccess) return e;
+    if (a.N > 0) {
+        if constexpr (sizeof(T) == 2) {
+            MmaGemm<float, T, T, false, false, 1> g{};
+            g.A[0] = a.ws_dfl;
+            g.B[0] = static_cast<const T *>(a.Wl);
+            g.A[1] = a.ws_dfr;
+            g.B[1] = static_cast<const T *>(a.Wr);
+            g.pairs = 2;
+            g.M = a.N; g.N = a.F; g.K = HD; g.k_per_slab = HD;
+            g.C = static_cast<T *>(a.dX);
+            if ((e = mma_gemm(g, 1, SGA_KERN_GATV2_BWD_DX, s)) != cudaSuccess) return e;
+        } else {
+            GemmArgs<float, T, T, false, true> g{};
+            g.A[0] = a.ws_dfl;
+            g.B[0] = static_cast<const T *>(a.Wl);
+            g.A[1] = a.ws_dfr;
+            g.B[1] = static_cast<const T *>(a.Wr);
+            g.pairs = 2;
+            g.M = a.N; g.N = a.F; g.K = HD; g.k_per_slab = HD;
+            g.C = static_cast<T *>(a.dX);
+            if ((e = gemm(g, 1, SGA_KERN_GATV2_BWD_DX, s)) != cudaSuccess) return e;
+        }
+        // dW = X^T dF over node slabs: fp32 partials [2][slab][F][HD]
+        for (int w = 0; w < 2; ++w) {
+            if constexpr (sizeof(T) == 2) {
+                MmaGemm<T, float, float, true, true, 2> g{};
+                g.A[0] = static_cast<const T *>(a.X);
+                g.B[0] = w ? a.ws_dfr : a.ws_dfl;
+                g.pairs = 1;
+                g.M = a.F; g.N = HD; g.K = a.N; g.k_per_slab = per;
+                g.Cpart = a.ws_dw + (size_t)w * FHD * a.dw_slabs;
+                if ((e = mma_gemm(g, a.dw_slabs, SGA_KERN_GATV2_BWD_DW, s)) != cudaSuccess) return e;
+            } else {
+                GemmArgs<T, float, T, true, false> g{};
+                g.A[0] = static_cast<const T *>(a.X);
+                g.B[0] = w ? a.ws_dfr : a.ws_dfl;
+                g.pairs = 1;
+                g.M = a.F; g.N = HD; g.K = a.N; g.k_per_slab = per;
+                g.C = nullptr;
+                g.Cpart = a.ws_dw + (size_t)w * FHD * a.dw_slabs;
+                if ((e = gemm(g, a.dw_slabs, SGA_KERN_GATV2_BWD_DW, s)) != cudaSuccess) return e;
+            }
         }
     }
     const int64_t total = 2 * FHD + HD;

@@ -1,0 +1,401 @@
+// Dense GEMMs of the GATv2 layer on the tensor cores (bf16 mma.sync, fp32
+// accumulate): the projections FL = X W_l, FR = X W_r, the input gradient
+// dX = dFL W_l^T + dFR W_r^T and the weight gradients dW = X^T dF (split-K
+// over node slabs, fp32 partials reduced in a fixed order).
+//
+// Operands are staged through shared memory in their global layout and read
+// with ldmatrix (.trans for M- or N-major tiles).  fp32 operands (dFL, dFR)
+// are split into bf16 hi + lo parts (hi = bf16(x), lo = bf16(x - hi)), so each
+// product keeps about 16 significant bits; the two parts take two MMAs.
+//
+// Exact projections: FL/FR are stored in bf16 and decide LeakyReLU branches
+// downstream, so they are rounded correctly.  The fp32 accumulation of a
+// k-term dot product x . w differs from the exact value by a small multiple
+// of 2^-24 |x||w|.  When every value within B = 4 * 2^-24 |x||w| + ulp of
+// the fp32 result rounds to the same bf16 number, that number is correct;
+// otherwise (about 0.6% of elements for unit-scale data) the dot product is
+// recomputed with error-free transformations in fp32: bf16 x bf16 products
+// are exact in fp32 and a TwoSum cascade carries the rounding error of every
+// addition, so hi + lo equals the exact sum to far below bf16 resolution.
+// The result is rounded to float, then to bf16 (ties to even).
+#pragma once
+
+#include "common.cuh"
+
+namespace sga {
+
+namespace mm {
+
+constexpr int BM = 128, BN = 128, BK = 32, THREADS = 256;
+constexpr int PAD = 8;   // bf16 elements of row padding: conflict-free ldmatrix
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void *p) {
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 8 consecutive elements from global memory as 8 bf16 (hi) and, for fp32
+// sources, their remainders (lo).
+template <typename E> struct Stage8;
+template <> struct Stage8<__nv_bfloat16> {
+    static constexpr bool kSplit = false;
+    __device__ static void load(const __nv_bfloat16 *p, bool ok, uint4 &hi, uint4 &lo) {
+        hi = ok ? ldg16(p) : make_uint4(0, 0, 0, 0);
+        lo = make_uint4(0, 0, 0, 0);
+    }
+};
+template <> struct Stage8<float> {
+    static constexpr bool kSplit = true;
+    __device__ static void load(const float *p, bool ok, uint4 &hi, uint4 &lo) {
+        float x[8];
+        if (ok) {
+            const uint4 u0 = ldg16(p), u1 = ldg16(p + 4);
+            unpack<float>(u0, x);
+            unpack<float>(u1, x + 4);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+        float h[8], l[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            h[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+            l[i] = x[i] - h[i];
+        }
+        hi = pack<__nv_bfloat16>(h);
+        lo = pack<__nv_bfloat16>(l);
+    }
+};
+
+}  // namespace mm
+
+// C = sum_p op(A_p) op(B_p).  AM: A stored [K][M] (else [M][K]); BN_MAJOR: B
+// stored [K][N] (else [N][K]).  MODE 0: bf16 C, correctly rounded (one pair,
+// bf16 operands); MODE 1: C in TC rounded to nearest; MODE 2: fp32 partial
+// Cpart[slab][M][N] over the K rows of slab blockIdx.z.
+template <typename TA, typename TB, typename TC, bool AM, bool BN_MAJOR, int MODE>
+struct MmaGemm {
+    const TA *A[2];
+    const TB *B[2];
+    int pairs;
+    int64_t M, N, K, k_per_slab;
+    TC *C;
+    float *Cpart;
+    // MODE 0: elements whose rounding the fp32 sum leaves open are listed here
+    // (row, column | tag << 16) for exact_round_kernel; tag names the output.
+    int32_t *fix_count;
+    int2 *fix_list;
+    int32_t fix_cap, fix_tag;
+};
+
+// Exact fp32 sum of the products x_k w_k of bf16 inputs (each product is exact
+// in fp32) for k = k0, k0 + step, ...: TwoSum keeps every addition's rounding
+// error in `lo`, so hi + lo is the sum to about 2^-48 relative.
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+}
+
+template <typename TA, typename TB, typename TC, bool AM, bool BN_MAJOR, int MODE>
+__global__ void __launch_bounds__(mm::THREADS, 2)
+mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
+    using namespace mm;
+    constexpr bool SA = Stage8<TA>::kSplit, SB = Stage8<TB>::kSplit;
+    constexpr int NA = SA ? 2 : 1, NB = SB ? 2 : 1;
+    // A tile: [BM][BK+PAD] (K-major) or [BK][BM+PAD] (M-major); B likewise.
+    constexpr int A_ELEMS = AM ? BK * (BM + PAD) : BM * (BK + PAD);
+    constexpr int B_ELEMS = BN_MAJOR ? BK * (BN + PAD) : BN * (BK + PAD);
+    __shared__ __align__(16) __nv_bfloat16 As[NA][A_ELEMS];
+    __shared__ __align__(16) __nv_bfloat16 Bs[NB][B_ELEMS];
+    __shared__ float rnorm[BM], cnorm[BN];
+    constexpr int kFixSh = 512;
+    __shared__ int2 fix_sh[MODE == 0 ? kFixSh : 1];
+    __shared__ int fix_n, fix_base;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wm = warp & 3, wn = warp >> 2;          // warp tile 32 x 64
+    if (MODE == 0 && tid == 0) fix_n = 0;
+    const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
+    const int64_t k_lo = (int64_t)blockIdx.z * g.k_per_slab;
+    const int64_t k_hi = min(g.K, k_lo + g.k_per_slab);
+
+    float acc[2][8][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
+    float rsq = 0.f, csq = 0.f;   // MODE 0: squared norms (row tid/2, column tid%128)
+
+    for (int p = 0; p < g.pairs; ++p) {
+        const TA *Ap = g.A[p];
+        const TB *Bp = g.B[p];
+        for (int64_t kb = k_lo; kb < k_hi; kb += BK) {
+            // ---- stage A: 512 chunks of 8 elements
+#pragma unroll
+            for (int rep = 0; rep < 2; ++rep) {
+                const int c = tid + rep * THREADS;
+                uint4 hi, lo;
+                if (AM) {   // [K][M]: row = k, 16 chunks of 8 along m
+                    const int kr = c >> 4, mc = (c & 15) * 8;
+                    const int64_t gk = kb + kr, gm = m0 + mc;
+                    Stage8<TA>::load(Ap + gk * g.M + gm, gk < k_hi && gm < g.M, hi, lo);
+                    *reinterpret_cast<uint4 *>(&As[0][kr * (BM + PAD) + mc]) = hi;
+                    if (SA) *reinterpret_cast<uint4 *>(&As[NA - 1][kr * (BM + PAD) + mc]) = lo;
+                } else {    // [M][K]: row = m, 4 chunks of 8 along k
+                    const int mr = c >> 2, kc = (c & 3) * 8;
+                    const int64_t gm = m0 + mr, gk = kb + kc;
+                    Stage8<TA>::load(Ap + gm * g.K + gk, gm < g.M && gk < k_hi, hi, lo);
+                    *reinterpret_cast<uint4 *>(&As[0][mr * (BK + PAD) + kc]) = hi;
+                    if (SA) *reinterpret_cast<uint4 *>(&As[NA - 1][mr * (BK + PAD) + kc]) = lo;
+                }
+            }
+            // ---- stage B
+#pragma unroll
+            for (int rep = 0; rep < 2; ++rep) {
+                const int c = tid + rep * THREADS;
+                uint4 hi, lo;
+                if (BN_MAJOR) {   // [K][N]
+                    const int kr = c >> 4, nc = (c & 15) * 8;
+                    const int64_t gk = kb + kr, gn = n0 + nc;
+                    Stage8<TB>::load(Bp + gk * g.N + gn, gk < k_hi && gn < g.N, hi, lo);
+                    *reinterpret_cast<uint4 *>(&Bs[0][kr * (BN + PAD) + nc]) = hi;
+                    if (SB) *reinterpret_cast<uint4 *>(&Bs[NB - 1][kr * (BN + PAD) + nc]) = lo;
+                } else {          // [N][K]
+                    const int nr = c >> 2, kc = (c & 3) * 8;
+                    const int64_t gn = n0 + nr, gk = kb + kc;
+                    Stage8<TB>::load(Bp + gn * g.K + gk, gn < g.N && gk < k_hi, hi, lo);
+                    *reinterpret_cast<uint4 *>(&Bs[0][nr * (BK + PAD) + kc]) = hi;
+                    if (SB) *reinterpret_cast<uint4 *>(&Bs[NB - 1][nr * (BK + PAD) + kc]) = lo;
+                }
+            }
+            __syncthreads();
+            if (MODE == 0) {   // squared norms of the A rows and B columns, k in order
+                if (!AM) {
+                    const __nv_bfloat16 *row = &As[0][(tid >> 1) * (BK + PAD) + (tid & 1) * 16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const float v = __bfloat162float(row[x]);
+                        rsq = fmaf(v, v, rsq);
+                    }
+                }
+                if (BN_MAJOR) {
+                    const int col = tid & 127, k0 = (tid >> 7) * 16;
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const float v = __bfloat162float(Bs[0][(k0 + x) * (BN + PAD) + col]);
+                        csq = fmaf(v, v, csq);
+                    }
+                }
+            }
+            // ---- MMAs over the two k16 steps of the tile
+#pragma unroll
+            for (int ks = 0; ks < BK; ks += 16) {
+#pragma unroll
+                for (int ia = 0; ia < NA; ++ia)
+#pragma unroll
+                    for (int ib = 0; ib < NB; ++ib) {
+                        uint32_t af[2][4];
+#pragma unroll
+                        for (int mi = 0; mi < 2; ++mi) {
+                            const int mb = wm * 32 + mi * 16;
+                            if (AM) {
+                                const int kr = ks + (lane & 7) + ((lane >> 4) << 3);
+                                const int mc = mb + (((lane >> 3) & 1) << 3);
+                                ldsm_x4_t(af[mi], &As[ia][kr * (BM + PAD) + mc]);
+                            } else {
+                                const int mr = mb + (lane & 15);
+                                const int kc = ks + ((lane >> 4) << 3);
+                                ldsm_x4(af[mi], &As[ia][mr * (BK + PAD) + kc]);
+                            }
+                        }
+#pragma unroll
+                        for (int nj = 0; nj < 8; nj += 2) {
+                            const int nb = wn * 64 + nj * 8;
+                            uint32_t bf[4];
+                            if (BN_MAJOR) {
+                                const int kr = ks + (lane & 7) + (((lane >> 3) & 1) << 3);
+                                const int nc = nb + ((lane >> 4) << 3);
+                                ldsm_x4_t(bf, &Bs[ib][kr * (BN + PAD) + nc]);
+                            } else {
+                                const int nr = nb + (lane & 7) + ((lane >> 4) << 3);
+                                const int kc = ks + (((lane >> 3) & 1) << 3);
+                                ldsm_x4(bf, &Bs[ib][nr * (BK + PAD) + kc]);
+                            }
+#pragma unroll
+                            for (int mi = 0; mi < 2; ++mi) {
+                                mma_bf16(acc[mi][nj], af[mi], bf[0], bf[1]);
+                                mma_bf16(acc[mi][nj + 1], af[mi], bf[2], bf[3]);
+                            }
+                        }
+                    }
+            }
+            __syncthreads();
+        }
+    }
+
+    if (MODE == 0) {
+        rsq += __shfl_xor_sync(SGA_FULL_MASK, rsq, 1);
+        if ((tid & 1) == 0) rnorm[tid >> 1] = rsq;
+        if (tid >= 128) cnorm[tid & 127] = csq;
+        __syncthreads();
+        if (tid < 128) cnorm[tid] += csq;
+        __syncthreads();
+    }
+
+    // ---- epilogue: thread holds rows (lane/4, +8), columns 2*(lane%4) + {0,1}
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int lr = wm * 32 + mi * 16 + (lane >> 2) + hr * 8;
+            const int64_t gm = m0 + lr;
+            if (gm >= g.M) continue;
+#pragma unroll
+            for (int nj = 0; nj < 8; ++nj) {
+                const int lc = wn * 64 + nj * 8 + (lane & 3) * 2;
+                const int64_t gn = n0 + lc;
+                if (gn >= g.N) continue;   // N is a multiple of 8: both columns valid
+                float v0 = acc[mi][nj][hr * 2], v1 = acc[mi][nj][hr * 2 + 1];
+                if (MODE == 2) {
+                    *reinterpret_cast<float2 *>(&g.Cpart[((int64_t)blockIdx.z * g.M + gm) * g.N + gn]) =
+                        make_float2(v0, v1);
+                    continue;
+                }
+                if (MODE == 0) {
+                    const float rn = rnorm[lr];
+                    float vv[2] = {v0, v1};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float bound = 4.0f * 5.9604645e-8f * sqrtf(rn * cnorm[lc + e]) +
+                                            fabsf(vv[e]) * 1.2e-7f;
+                        if (__float2bfloat16_rn(vv[e] - bound) != __float2bfloat16_rn(vv[e] + bound)) {
+                            const int slot = atomicAdd(&fix_n, 1);
+                            if (slot < kFixSh) {
+                                fix_sh[slot] = make_int2((int)gm, (int)(gn + e) | (g.fix_tag << 16));
+                            } else {   // shared list full (not expected): exact sum in place
+                                const TA *ar = g.A[0] + gm * g.K;
+                                float sh = 0.f, sl = 0.f;
+                                for (int64_t k = 0; k < g.K; ++k) {
+                                    const float x = to_f32<TA>(ar[k]);
+                                    const float w = to_f32<TB>(BN_MAJOR ? g.B[0][k * g.N + gn + e]
+                                                                        : g.B[0][(gn + e) * g.K + k]);
+                                    float t, err;
+                                    two_sum(sh, __fmul_rn(x, w), t, err);
+                                    sh = t;
+                                    sl = __fadd_rn(sl, err);
+                                }
+                                vv[e] = __fadd_rn(sh, sl);
+                            }
+                        }
+                    }
+                    v0 = vv[0];
+                    v1 = vv[1];
+                }
+                TC *dst = g.C + gm * g.N + gn;
+                dst[0] = from_f32<TC>(v0);
+                dst[1] = from_f32<TC>(v1);
+            }
+        }
+    if (MODE == 0) {   // hand the block's open elements to exact_round_kernel
+        __syncthreads();
+        const int n = min(fix_n, kFixSh);
+        if (tid == 0) fix_base = n ? atomicAdd(g.fix_count, n) : 0;
+        __syncthreads();
+        for (int i = tid; i < n; i += THREADS) {
+            const int at = fix_base + i;
+            if (at < g.fix_cap) {
+                g.fix_list[at] = fix_sh[i];
+            } else {   // list full (not expected): exact sum in place
+                const int2 f = fix_sh[i];
+                const int64_t gm = f.x, gn = f.y & 0xffff;
+                float sh = 0.f, sl = 0.f;
+                for (int64_t k = 0; k < g.K; ++k) {
+                    const float x = to_f32<TA>(g.A[0][gm * g.K + k]);
+                    const float w = to_f32<TB>(BN_MAJOR ? g.B[0][k * g.N + gn] : g.B[0][gn * g.K + k]);
+                    float t, err;
+                    two_sum(sh, __fmul_rn(x, w), t, err);
+                    sh = t;
+                    sl = __fadd_rn(sl, err);
+                }
+                g.C[gm * g.N + gn] = from_f32<TC>(__fadd_rn(sh, sl));
+            }
+        }
+    }
+}
+
+// Recompute the listed elements exactly, one warp each: lanes split k, each
+// keeps an error-free (hi, lo) sum, and the lane sums are combined with
+// TwoSum as well.  X [M][K]; W_t [K][N] for tag t; C_t [M][N] bf16.
+struct ExactRound {
+    const __nv_bfloat16 *X;
+    const __nv_bfloat16 *W[2];
+    __nv_bfloat16 *C[2];
+    int64_t M, N, K;
+    const int32_t *count;
+    const int2 *list;
+    int32_t cap;
+};
+
+static __global__ void __launch_bounds__(256) exact_round_kernel(ExactRound r) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int n = min(*r.count, r.cap);
+    for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < n; i += nw) {
+        const int2 f = r.list[i];
+        const int64_t m = f.x, col = f.y & 0xffff;
+        const int t = f.y >> 16;
+        float hi = 0.f, lo = 0.f;
+        for (int64_t k = lane; k < r.K; k += 32) {
+            const float x = __bfloat162float(r.X[m * r.K + k]);
+            const float w = __bfloat162float(r.W[t][k * r.N + col]);
+            float s, e;
+            two_sum(hi, __fmul_rn(x, w), s, e);
+            hi = s;
+            lo = __fadd_rn(lo, e);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ho = __shfl_xor_sync(SGA_FULL_MASK, hi, o);
+            const float lo2 = __shfl_xor_sync(SGA_FULL_MASK, lo, o);
+            float s, e;
+            two_sum(hi, ho, s, e);
+            hi = s;
+            lo = __fadd_rn(__fadd_rn(lo, lo2), e);
+        }
+        if (lane == 0) r.C[t][m * r.N + col] = __float2bfloat16_rn(__fadd_rn(hi, lo));
+    }
+}
+
+template <typename TA, typename TB, typename TC, bool AM, bool BN_MAJOR, int MODE>
+cudaError_t mma_gemm(const MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> &g, int slabs,
+                     sga_kernel_id kid, cudaStream_t s) {
+    dim3 grid((unsigned)((g.N + mm::BN - 1) / mm::BN), (unsigned)((g.M + mm::BM - 1) / mm::BM),
+              (unsigned)slabs);
+    note_launch(kid, s, false);
+    mma_gemm_kernel<TA, TB, TC, AM, BN_MAJOR, MODE><<<grid, mm::THREADS, 0, s>>>(g);
+    note_launch(kid, s, true);
+    return cudaGetLastError();
+}
+
+}  // namespace sga

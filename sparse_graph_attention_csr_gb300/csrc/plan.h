@@ -35,6 +35,8 @@ struct WorkspaceLayout {
     size_t dfr = 0;        // [N, H*D] f32 GATv2 dFR
     size_t da_part = 0;    // [da_blocks, H*D] f32 GATv2 partial da
     size_t dw_part = 0;    // [dw_slabs, 2, F, H*D] f32 GATv2 partial dW_l, dW_r
+    size_t fix = 0;        // int32 count, then [fix_cap] int2 projection elements to round exactly
+    int32_t fix_cap = 0;
     size_t total = 0;
     int32_t da_blocks = 0;
     int32_t dw_slabs = 0;
@@ -102,6 +104,9 @@ struct Gatv2Args {
     Partition rows, cols;
     float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_rowc, *ws_col, *ws_da, *ws_da_split, *ws_dw;
     float *ws_dfl, *ws_dfr;        // [N, H*D] fp32
+    int32_t *ws_fix_count;
+    int2 *ws_fix_list;
+    int fix_cap;
     int da_blocks, dw_slabs;
     int32_t *d_err;
 };
