@@ -18,6 +18,7 @@
 
 #include "gemm.cuh"
 #include "gt.cuh"
+#include "tc_proj.cuh"
 
 namespace sga {
 
@@ -685,7 +686,20 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
     const int HD = a.H * D;
     // projections FL = X W_l, FR = X W_r (bf16: tensor cores, correctly rounded)
     if constexpr (sizeof(T) == 2) {
-        if (a.N > 0) {
+        if (a.N > 0 && tc_proj_supported(a.F, HD)) {   // tcgen05 path
+            TcProj tp{};
+            tp.X = static_cast<const __nv_bfloat16 *>(a.X);
+            tp.Wl = static_cast<const __nv_bfloat16 *>(a.Wl);
+            tp.Wr = static_cast<const __nv_bfloat16 *>(a.Wr);
+            tp.FL = static_cast<__nv_bfloat16 *>(a.FL_w);
+            tp.FR = static_cast<__nv_bfloat16 *>(a.FR_w);
+            tp.M = a.N;
+            tp.K = a.F;
+            tp.HD = HD;
+            tp.err = a.d_err;
+            cudaError_t e = tc_proj(tp, s);
+            if (e != cudaSuccess) return e;
+        } else if (a.N > 0) {
             cudaError_t e = cudaMemsetAsync(a.ws_fix_count, 0, sizeof(int32_t), s);
             for (int w = 0; w < 2 && e == cudaSuccess; ++w) {
                 MmaGemm<T, T, T, false, true, 0> g{};
@@ -701,20 +715,22 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
                 e = mma_gemm(g, 1, SGA_KERN_GATV2_PROJ, s);
             }
             if (e != cudaSuccess) return e;
-            ExactRound r{};
-            r.X = static_cast<const __nv_bfloat16 *>(a.X);
-            r.W[0] = static_cast<const __nv_bfloat16 *>(a.Wl);
-            r.W[1] = static_cast<const __nv_bfloat16 *>(a.Wr);
-            r.C[0] = static_cast<__nv_bfloat16 *>(a.FL_w);
-            r.C[1] = static_cast<__nv_bfloat16 *>(a.FR_w);
-            r.M = a.N; r.N = HD; r.K = a.F;
-            r.count = a.ws_fix_count;
-            r.list = a.ws_fix_list;
-            r.cap = a.fix_cap;
-            note_launch(SGA_KERN_GATV2_PROJ, s, false);
-            exact_round_kernel<<<persistent_blocks<exact_round_kernel>(1 << 30), 256, 0, s>>>(r);
-            note_launch(SGA_KERN_GATV2_PROJ, s, true);
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            if (a.F > 2 * mm::BK) {   // k range too long for in-block rounding
+                ExactRound r{};
+                r.X = static_cast<const __nv_bfloat16 *>(a.X);
+                r.W[0] = static_cast<const __nv_bfloat16 *>(a.Wl);
+                r.W[1] = static_cast<const __nv_bfloat16 *>(a.Wr);
+                r.C[0] = static_cast<__nv_bfloat16 *>(a.FL_w);
+                r.C[1] = static_cast<__nv_bfloat16 *>(a.FR_w);
+                r.M = a.N; r.N = HD; r.K = a.F;
+                r.count = a.ws_fix_count;
+                r.list = a.ws_fix_list;
+                r.cap = a.fix_cap;
+                note_launch(SGA_KERN_GATV2_PROJ, s, false);
+                exact_round_kernel<<<persistent_blocks<exact_round_kernel>(1 << 30), 256, 0, s>>>(r);
+                note_launch(SGA_KERN_GATV2_PROJ, s, true);
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
         }
     } else {
         for (int w = 0; w < 2 && a.N > 0; ++w) {

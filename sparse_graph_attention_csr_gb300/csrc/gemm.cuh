@@ -11,10 +11,13 @@
 // Exact projections: FL/FR are stored in bf16 and decide LeakyReLU branches
 // downstream, so they are rounded correctly.  The fp32 accumulation of a
 // k-term dot product x . w differs from the exact value by a small multiple
-// of 2^-24 |x||w|.  When every value within B = 4 * 2^-24 |x||w| + ulp of
-// the fp32 result rounds to the same bf16 number, that number is correct;
-// otherwise (about 0.6% of elements for unit-scale data) the dot product is
-// recomputed with error-free transformations in fp32: bf16 x bf16 products
+// of 2^-24 |x||w| (measured: at most 0.6 for sequential fp32 sums of the
+// GATv2 workload).  When every value within B = 2 * 2^-24 |x||w| + ulp of the
+// fp32 result rounds to the same bf16 number, that number is correct;
+// otherwise (about 0.35% of elements for unit-scale data) the dot product is
+// recomputed with error-free transformations in fp32 -- by one warp per
+// element from the shared-memory tiles when k <= 128, else by
+// exact_round_kernel from a workspace list: bf16 x bf16 products
 // are exact in fp32 and a TwoSum cascade carries the rounding error of every
 // addition, so hi + lo equals the exact sum to far below bf16 resolution.
 // The result is rounded to float, then to bf16 (ties to even).
@@ -26,7 +29,7 @@ namespace sga {
 
 namespace mm {
 
-constexpr int BM = 128, BN = 128, BK = 32, THREADS = 256;
+constexpr int BM = 128, BN = 128, BK = 64, THREADS = 256;
 constexpr int PAD = 8;   // bf16 elements of row padding: conflict-free ldmatrix
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void *p) {
@@ -52,38 +55,30 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 8 consecutive elements from global memory as 8 bf16 (hi) and, for fp32
-// sources, their remainders (lo).
-template <typename E> struct Stage8;
-template <> struct Stage8<__nv_bfloat16> {
-    static constexpr bool kSplit = false;
-    __device__ static void load(const __nv_bfloat16 *p, bool ok, uint4 &hi, uint4 &lo) {
-        hi = ok ? ldg16(p) : make_uint4(0, 0, 0, 0);
-        lo = make_uint4(0, 0, 0, 0);
-    }
-};
-template <> struct Stage8<float> {
-    static constexpr bool kSplit = true;
-    __device__ static void load(const float *p, bool ok, uint4 &hi, uint4 &lo) {
-        float x[8];
-        if (ok) {
-            const uint4 u0 = ldg16(p), u1 = ldg16(p + 4);
-            unpack<float>(u0, x);
-            unpack<float>(u1, x + 4);
-        } else {
+// 16-byte global -> shared copy that bypasses registers; `ok` false zero-fills.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool ok) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+                 "r"(ok ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N));
+}
+
+// bf16 hi part and remainder of 8 floats.
+__device__ __forceinline__ void split8(const uint4 &u0, const uint4 &u1, uint4 &hi, uint4 &lo) {
+    float x[8], h[8], l[8];
+    unpack<float>(u0, x);
+    unpack<float>(u1, x + 4);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = 0.f;
-        }
-        float h[8], l[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            h[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
-            l[i] = x[i] - h[i];
-        }
-        hi = pack<__nv_bfloat16>(h);
-        lo = pack<__nv_bfloat16>(l);
+    for (int i = 0; i < 8; ++i) {
+        h[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+        l[i] = x[i] - h[i];
     }
-};
+    hi = pack<__nv_bfloat16>(h);
+    lo = pack<__nv_bfloat16>(l);
+}
 
 }  // namespace mm
 
@@ -115,17 +110,27 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
 }
 
+// One operand tile of one k chunk: 1024 chunks of 8 elements, 4 per thread.
+// MAJ (the tile's rows are k) selects [BK][BX+PAD]; else [BX][BK+PAD].
+template <bool MAJ, int BX> struct TileMap {
+    __device__ static void at(int c, int &r, int &col) {   // chunk c -> (smem row, col)
+        if (MAJ) { r = c / (BX / 8); col = (c % (BX / 8)) * 8; }
+        else     { r = c / (mm::BK / 8); col = (c % (mm::BK / 8)) * 8; }
+    }
+    static constexpr int LD = MAJ ? BX + mm::PAD : mm::BK + mm::PAD;
+    static constexpr int ELEMS = MAJ ? mm::BK * (BX + mm::PAD) : BX * (mm::BK + mm::PAD);
+};
+
 template <typename TA, typename TB, typename TC, bool AM, bool BN_MAJOR, int MODE>
-__global__ void __launch_bounds__(mm::THREADS, 2)
+__global__ void __launch_bounds__(mm::THREADS, 1)
 mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
     using namespace mm;
-    constexpr bool SA = Stage8<TA>::kSplit, SB = Stage8<TB>::kSplit;
+    constexpr bool SA = sizeof(TA) == 4, SB = sizeof(TB) == 4;   // fp32 operands split hi/lo
     constexpr int NA = SA ? 2 : 1, NB = SB ? 2 : 1;
-    // A tile: [BM][BK+PAD] (K-major) or [BK][BM+PAD] (M-major); B likewise.
-    constexpr int A_ELEMS = AM ? BK * (BM + PAD) : BM * (BK + PAD);
-    constexpr int B_ELEMS = BN_MAJOR ? BK * (BN + PAD) : BN * (BK + PAD);
-    __shared__ __align__(16) __nv_bfloat16 As[NA][A_ELEMS];
-    __shared__ __align__(16) __nv_bfloat16 Bs[NB][B_ELEMS];
+    using MA = TileMap<AM, BM>;
+    using MB = TileMap<BN_MAJOR, BN>;
+    constexpr int STAGE = NA * MA::ELEMS + NB * MB::ELEMS;   // bf16 elements per stage
+    extern __shared__ __align__(16) __nv_bfloat16 smem[];
     __shared__ float rnorm[BM], cnorm[BN];
     constexpr int kFixSh = 512;
     __shared__ int2 fix_sh[MODE == 0 ? kFixSh : 1];
@@ -137,6 +142,80 @@ mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
     const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
     const int64_t k_lo = (int64_t)blockIdx.z * g.k_per_slab;
     const int64_t k_hi = min(g.K, k_lo + g.k_per_slab);
+    const int per_pair = k_hi > k_lo ? (int)((k_hi - k_lo + BK - 1) / BK) : 0;
+    const int n_chunks = per_pair * g.pairs;
+
+    // global element (row-of-tile, col-of-tile) of chunk c of the current k chunk
+    auto a_src = [&](int p, int64_t kb, int c, bool &ok) -> const TA * {
+        int r, col;
+        MA::at(c, r, col);
+        int64_t gm, gk;
+        if (AM) { gk = kb + r; gm = m0 + col; } else { gm = m0 + r; gk = kb + col; }
+        ok = gm < g.M && gk < k_hi;
+        return ok ? g.A[p] + (AM ? gk * g.M + gm : gm * g.K + gk) : g.A[p];
+    };
+    auto b_src = [&](int p, int64_t kb, int c, bool &ok) -> const TB * {
+        int r, col;
+        MB::at(c, r, col);
+        int64_t gn, gk;
+        if (BN_MAJOR) { gk = kb + r; gn = n0 + col; } else { gn = n0 + r; gk = kb + col; }
+        ok = gn < g.N && gk < k_hi;
+        return ok ? g.B[p] + (BN_MAJOR ? gk * g.N + gn : gn * g.K + gk) : g.B[p];
+    };
+    __nv_bfloat16 *stage_base[2] = {smem, smem + STAGE};
+    // fp32 operand chunks held in registers between load and store
+    uint4 ra[SA ? 8 : 1], rb[SB ? 8 : 1];
+
+    auto issue = [&](int chunk, int st) {   // start loading chunk into stage st
+        const int p = chunk / per_pair;
+        const int64_t kb = k_lo + (int64_t)(chunk % per_pair) * BK;
+        __nv_bfloat16 *As = stage_base[st], *Bs = stage_base[st] + NA * MA::ELEMS;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = tid + i * THREADS;
+            int r, col;
+            bool ok;
+            MA::at(c, r, col);
+            const TA *src = a_src(p, kb, c, ok);
+            if constexpr (SA) {
+                ra[2 * i] = ok ? ldg16(src) : make_uint4(0, 0, 0, 0);
+                ra[2 * i + 1] = ok ? ldg16(src + 4) : make_uint4(0, 0, 0, 0);
+            } else {
+                cp_async16(&As[r * MA::LD + col], src, ok);
+            }
+            MB::at(c, r, col);
+            const TB *srcb = b_src(p, kb, c, ok);
+            if constexpr (SB) {
+                rb[2 * i] = ok ? ldg16(srcb) : make_uint4(0, 0, 0, 0);
+                rb[2 * i + 1] = ok ? ldg16(srcb + 4) : make_uint4(0, 0, 0, 0);
+            } else {
+                cp_async16(&Bs[r * MB::LD + col], srcb, ok);
+            }
+        }
+        cp_async_commit();
+    };
+    auto store_regs = [&](int st) {          // fp32 chunks: split and store
+        __nv_bfloat16 *As = stage_base[st], *Bs = stage_base[st] + NA * MA::ELEMS;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = tid + i * THREADS;
+            int r, col;
+            if constexpr (SA) {
+                MA::at(c, r, col);
+                uint4 hi, lo;
+                split8(ra[2 * i], ra[2 * i + 1], hi, lo);
+                *reinterpret_cast<uint4 *>(&As[r * MA::LD + col]) = hi;
+                *reinterpret_cast<uint4 *>(&As[MA::ELEMS + r * MA::LD + col]) = lo;
+            }
+            if constexpr (SB) {
+                MB::at(c, r, col);
+                uint4 hi, lo;
+                split8(rb[2 * i], rb[2 * i + 1], hi, lo);
+                *reinterpret_cast<uint4 *>(&Bs[r * MB::LD + col]) = hi;
+                *reinterpret_cast<uint4 *>(&Bs[MB::ELEMS + r * MB::LD + col]) = lo;
+            }
+        }
+    };
 
     float acc[2][8][4];
 #pragma unroll
@@ -147,111 +226,79 @@ mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
             for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
     float rsq = 0.f, csq = 0.f;   // MODE 0: squared norms (row tid/2, column tid%128)
 
-    for (int p = 0; p < g.pairs; ++p) {
-        const TA *Ap = g.A[p];
-        const TB *Bp = g.B[p];
-        for (int64_t kb = k_lo; kb < k_hi; kb += BK) {
-            // ---- stage A: 512 chunks of 8 elements
+    if (n_chunks > 0) {
+        issue(0, 0);
+        if (SA || SB) store_regs(0);
+    }
+    for (int ch = 0; ch < n_chunks; ++ch) {
+        const int cur = ch & 1;
+        const bool more = ch + 1 < n_chunks;
+        if (more) issue(ch + 1, cur ^ 1);
+        if (more) cp_async_wait<1>(); else cp_async_wait<0>();
+        __syncthreads();
+        const __nv_bfloat16 *As = stage_base[cur], *Bs = stage_base[cur] + NA * MA::ELEMS;
+        if (MODE == 0) {   // squared norms of the A rows and B columns, k in order
+            if (!AM) {
+                const __nv_bfloat16 *row = &As[(tid >> 1) * MA::LD + (tid & 1) * 32];
 #pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-                const int c = tid + rep * THREADS;
-                uint4 hi, lo;
-                if (AM) {   // [K][M]: row = k, 16 chunks of 8 along m
-                    const int kr = c >> 4, mc = (c & 15) * 8;
-                    const int64_t gk = kb + kr, gm = m0 + mc;
-                    Stage8<TA>::load(Ap + gk * g.M + gm, gk < k_hi && gm < g.M, hi, lo);
-                    *reinterpret_cast<uint4 *>(&As[0][kr * (BM + PAD) + mc]) = hi;
-                    if (SA) *reinterpret_cast<uint4 *>(&As[NA - 1][kr * (BM + PAD) + mc]) = lo;
-                } else {    // [M][K]: row = m, 4 chunks of 8 along k
-                    const int mr = c >> 2, kc = (c & 3) * 8;
-                    const int64_t gm = m0 + mr, gk = kb + kc;
-                    Stage8<TA>::load(Ap + gm * g.K + gk, gm < g.M && gk < k_hi, hi, lo);
-                    *reinterpret_cast<uint4 *>(&As[0][mr * (BK + PAD) + kc]) = hi;
-                    if (SA) *reinterpret_cast<uint4 *>(&As[NA - 1][mr * (BK + PAD) + kc]) = lo;
+                for (int x = 0; x < 32; ++x) {
+                    const float v = __bfloat162float(row[x]);
+                    rsq = fmaf(v, v, rsq);
                 }
             }
-            // ---- stage B
+            if (BN_MAJOR) {
+                const int col = tid & 127, k0 = (tid >> 7) * 32;
 #pragma unroll
-            for (int rep = 0; rep < 2; ++rep) {
-                const int c = tid + rep * THREADS;
-                uint4 hi, lo;
-                if (BN_MAJOR) {   // [K][N]
-                    const int kr = c >> 4, nc = (c & 15) * 8;
-                    const int64_t gk = kb + kr, gn = n0 + nc;
-                    Stage8<TB>::load(Bp + gk * g.N + gn, gk < k_hi && gn < g.N, hi, lo);
-                    *reinterpret_cast<uint4 *>(&Bs[0][kr * (BN + PAD) + nc]) = hi;
-                    if (SB) *reinterpret_cast<uint4 *>(&Bs[NB - 1][kr * (BN + PAD) + nc]) = lo;
-                } else {          // [N][K]
-                    const int nr = c >> 2, kc = (c & 3) * 8;
-                    const int64_t gn = n0 + nr, gk = kb + kc;
-                    Stage8<TB>::load(Bp + gn * g.K + gk, gn < g.N && gk < k_hi, hi, lo);
-                    *reinterpret_cast<uint4 *>(&Bs[0][nr * (BK + PAD) + kc]) = hi;
-                    if (SB) *reinterpret_cast<uint4 *>(&Bs[NB - 1][nr * (BK + PAD) + kc]) = lo;
+                for (int x = 0; x < 32; ++x) {
+                    const float v = __bfloat162float(Bs[(k0 + x) * MB::LD + col]);
+                    csq = fmaf(v, v, csq);
                 }
             }
-            __syncthreads();
-            if (MODE == 0) {   // squared norms of the A rows and B columns, k in order
-                if (!AM) {
-                    const __nv_bfloat16 *row = &As[0][(tid >> 1) * (BK + PAD) + (tid & 1) * 16];
+        }
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const float v = __bfloat162float(row[x]);
-                        rsq = fmaf(v, v, rsq);
+        for (int ks = 0; ks < BK; ks += 16) {
+#pragma unroll
+            for (int ia = 0; ia < NA; ++ia)
+#pragma unroll
+                for (int ib = 0; ib < NB; ++ib) {
+                    const __nv_bfloat16 *Ai = As + ia * MA::ELEMS, *Bi = Bs + ib * MB::ELEMS;
+                    uint32_t af[2][4];
+#pragma unroll
+                    for (int mi = 0; mi < 2; ++mi) {
+                        const int mb = wm * 32 + mi * 16;
+                        if (AM) {
+                            const int kr = ks + (lane & 7) + ((lane >> 4) << 3);
+                            const int mc = mb + (((lane >> 3) & 1) << 3);
+                            ldsm_x4_t(af[mi], &Ai[kr * MA::LD + mc]);
+                        } else {
+                            const int mr = mb + (lane & 15);
+                            const int kc = ks + ((lane >> 4) << 3);
+                            ldsm_x4(af[mi], &Ai[mr * MA::LD + kc]);
+                        }
                     }
-                }
-                if (BN_MAJOR) {
-                    const int col = tid & 127, k0 = (tid >> 7) * 16;
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const float v = __bfloat162float(Bs[0][(k0 + x) * (BN + PAD) + col]);
-                        csq = fmaf(v, v, csq);
-                    }
-                }
-            }
-            // ---- MMAs over the two k16 steps of the tile
-#pragma unroll
-            for (int ks = 0; ks < BK; ks += 16) {
-#pragma unroll
-                for (int ia = 0; ia < NA; ++ia)
-#pragma unroll
-                    for (int ib = 0; ib < NB; ++ib) {
-                        uint32_t af[2][4];
+                    for (int nj = 0; nj < 8; nj += 2) {
+                        const int nb = wn * 64 + nj * 8;
+                        uint32_t bf[4];
+                        if (BN_MAJOR) {
+                            const int kr = ks + (lane & 7) + (((lane >> 3) & 1) << 3);
+                            const int nc = nb + ((lane >> 4) << 3);
+                            ldsm_x4_t(bf, &Bi[kr * MB::LD + nc]);
+                        } else {
+                            const int nr = nb + (lane & 7) + ((lane >> 4) << 3);
+                            const int kc = ks + (((lane >> 3) & 1) << 3);
+                            ldsm_x4(bf, &Bi[nr * MB::LD + kc]);
+                        }
 #pragma unroll
                         for (int mi = 0; mi < 2; ++mi) {
-                            const int mb = wm * 32 + mi * 16;
-                            if (AM) {
-                                const int kr = ks + (lane & 7) + ((lane >> 4) << 3);
-                                const int mc = mb + (((lane >> 3) & 1) << 3);
-                                ldsm_x4_t(af[mi], &As[ia][kr * (BM + PAD) + mc]);
-                            } else {
-                                const int mr = mb + (lane & 15);
-                                const int kc = ks + ((lane >> 4) << 3);
-                                ldsm_x4(af[mi], &As[ia][mr * (BK + PAD) + kc]);
-                            }
-                        }
-#pragma unroll
-                        for (int nj = 0; nj < 8; nj += 2) {
-                            const int nb = wn * 64 + nj * 8;
-                            uint32_t bf[4];
-                            if (BN_MAJOR) {
-                                const int kr = ks + (lane & 7) + (((lane >> 3) & 1) << 3);
-                                const int nc = nb + ((lane >> 4) << 3);
-                                ldsm_x4_t(bf, &Bs[ib][kr * (BN + PAD) + nc]);
-                            } else {
-                                const int nr = nb + (lane & 7) + ((lane >> 4) << 3);
-                                const int kc = ks + (((lane >> 3) & 1) << 3);
-                                ldsm_x4(bf, &Bs[ib][nr * (BK + PAD) + kc]);
-                            }
-#pragma unroll
-                            for (int mi = 0; mi < 2; ++mi) {
-                                mma_bf16(acc[mi][nj], af[mi], bf[0], bf[1]);
-                                mma_bf16(acc[mi][nj + 1], af[mi], bf[2], bf[3]);
-                            }
+                            mma_bf16(acc[mi][nj], af[mi], bf[0], bf[1]);
+                            mma_bf16(acc[mi][nj + 1], af[mi], bf[2], bf[3]);
                         }
                     }
-            }
-            __syncthreads();
+                }
         }
+        __syncthreads();
+        if (more && (SA || SB)) store_regs(cur ^ 1);
     }
 
     if (MODE == 0) {
@@ -259,7 +306,8 @@ mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
         if ((tid & 1) == 0) rnorm[tid >> 1] = rsq;
         if (tid >= 128) cnorm[tid & 127] = csq;
         __syncthreads();
-        if (tid < 128) cnorm[tid] += csq;
+        if (tid < 128) cnorm[tid] = sqrtf(cnorm[tid] + csq);
+        if (tid < 128) rnorm[tid] = sqrtf(rnorm[tid]);
         __syncthreads();
     }
 
@@ -282,63 +330,88 @@ mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
                         make_float2(v0, v1);
                     continue;
                 }
-                if (MODE == 0) {
-                    const float rn = rnorm[lr];
-                    float vv[2] = {v0, v1};
+                if (MODE == 0) {   // flag sums whose bf16 rounding is open (see header)
+                    const float rn = rnorm[lr] * (2.0f * 5.9604645e-8f);
+                    const float vv[2] = {v0, v1};
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float bound = 4.0f * 5.9604645e-8f * sqrtf(rn * cnorm[lc + e]) +
-                                            fabsf(vv[e]) * 1.2e-7f;
+                        const float bound = rn * cnorm[lc + e] + fabsf(vv[e]) * 1.2e-7f;
                         if (__float2bfloat16_rn(vv[e] - bound) != __float2bfloat16_rn(vv[e] + bound)) {
                             const int slot = atomicAdd(&fix_n, 1);
                             if (slot < kFixSh) {
-                                fix_sh[slot] = make_int2((int)gm, (int)(gn + e) | (g.fix_tag << 16));
+                                fix_sh[slot] = make_int2(lr, lc + e);
                             } else {   // shared list full (not expected): exact sum in place
-                                const TA *ar = g.A[0] + gm * g.K;
                                 float sh = 0.f, sl = 0.f;
                                 for (int64_t k = 0; k < g.K; ++k) {
-                                    const float x = to_f32<TA>(ar[k]);
-                                    const float w = to_f32<TB>(BN_MAJOR ? g.B[0][k * g.N + gn + e]
-                                                                        : g.B[0][(gn + e) * g.K + k]);
+                                    const float x = to_f32<TA>(g.A[0][gm * g.K + k]);
+                                    const float w = to_f32<TB>(g.B[0][k * g.N + gn + e]);
                                     float t, err;
                                     two_sum(sh, __fmul_rn(x, w), t, err);
                                     sh = t;
                                     sl = __fadd_rn(sl, err);
                                 }
-                                vv[e] = __fadd_rn(sh, sl);
+                                (e == 0 ? v0 : v1) = __fadd_rn(sh, sl);
                             }
                         }
                     }
-                    v0 = vv[0];
-                    v1 = vv[1];
                 }
                 TC *dst = g.C + gm * g.N + gn;
                 dst[0] = from_f32<TC>(v0);
                 dst[1] = from_f32<TC>(v1);
             }
         }
-    if (MODE == 0) {   // hand the block's open elements to exact_round_kernel
+    if (MODE == 0) {   // exact recompute of the flagged elements
+        static_assert(MODE != 0 || (!AM && BN_MAJOR), "projection layout: X [M][K], W [K][N]");
         __syncthreads();
         const int n = min(fix_n, kFixSh);
-        if (tid == 0) fix_base = n ? atomicAdd(g.fix_count, n) : 0;
-        __syncthreads();
-        for (int i = tid; i < n; i += THREADS) {
-            const int at = fix_base + i;
-            if (at < g.fix_cap) {
-                g.fix_list[at] = fix_sh[i];
-            } else {   // list full (not expected): exact sum in place
-                const int2 f = fix_sh[i];
-                const int64_t gm = f.x, gn = f.y & 0xffff;
-                float sh = 0.f, sl = 0.f;
-                for (int64_t k = 0; k < g.K; ++k) {
-                    const float x = to_f32<TA>(g.A[0][gm * g.K + k]);
-                    const float w = to_f32<TB>(BN_MAJOR ? g.B[0][k * g.N + gn] : g.B[0][gn * g.K + k]);
+        if (g.K <= 2 * BK && g.pairs == 1) {
+            // the whole k range is still in the two stages: one warp per element
+            for (int i = warp; i < n; i += THREADS / 32) {
+                const int lr = fix_sh[i].x, lc = fix_sh[i].y;
+                float hi = 0.f, lo = 0.f;
+                for (int k = lane; k < g.K; k += 32) {
+                    const __nv_bfloat16 *As = stage_base[k / BK];
+                    const __nv_bfloat16 *Bs = stage_base[k / BK] + NA * MA::ELEMS;
+                    const float x = __bfloat162float(As[lr * MA::LD + (k % BK)]);
+                    const float w = __bfloat162float(Bs[(k % BK) * MB::LD + lc]);
                     float t, err;
-                    two_sum(sh, __fmul_rn(x, w), t, err);
-                    sh = t;
-                    sl = __fadd_rn(sl, err);
+                    two_sum(hi, __fmul_rn(x, w), t, err);
+                    hi = t;
+                    lo = __fadd_rn(lo, err);
                 }
-                g.C[gm * g.N + gn] = from_f32<TC>(__fadd_rn(sh, sl));
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ho = __shfl_xor_sync(SGA_FULL_MASK, hi, o);
+                    const float lo2 = __shfl_xor_sync(SGA_FULL_MASK, lo, o);
+                    float t, err;
+                    two_sum(hi, ho, t, err);
+                    hi = t;
+                    lo = __fadd_rn(__fadd_rn(lo, lo2), err);
+                }
+                if (lane == 0) g.C[(m0 + lr) * g.N + n0 + lc] = from_f32<TC>(__fadd_rn(hi, lo));
+            }
+        } else {
+            // k range too long for shared memory (or list overflow): exact_round_kernel
+            if (tid == 0) fix_base = n ? atomicAdd(g.fix_count, n) : 0;
+            __syncthreads();
+            for (int i = tid; i < n; i += THREADS) {
+                const int2 f = fix_sh[i];
+                const int at = fix_base + i;
+                const int64_t gm = m0 + f.x, gn = n0 + f.y;
+                if (at < g.fix_cap) {
+                    g.fix_list[at] = make_int2((int)gm, (int)gn | (g.fix_tag << 16));
+                } else {   // list full (not expected): exact sum in place
+                    float sh = 0.f, sl = 0.f;
+                    for (int64_t k = 0; k < g.K; ++k) {
+                        const float x = to_f32<TA>(g.A[0][gm * g.K + k]);
+                        const float w = to_f32<TB>(g.B[0][k * g.N + gn]);
+                        float t, err;
+                        two_sum(sh, __fmul_rn(x, w), t, err);
+                        sh = t;
+                        sl = __fadd_rn(sl, err);
+                    }
+                    g.C[gm * g.N + gn] = from_f32<TC>(__fadd_rn(sh, sl));
+                }
             }
         }
     }
@@ -390,10 +463,20 @@ static __global__ void __launch_bounds__(256) exact_round_kernel(ExactRound r) {
 template <typename TA, typename TB, typename TC, bool AM, bool BN_MAJOR, int MODE>
 cudaError_t mma_gemm(const MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> &g, int slabs,
                      sga_kernel_id kid, cudaStream_t s) {
+    constexpr int NA = sizeof(TA) == 4 ? 2 : 1, NB = sizeof(TB) == 4 ? 2 : 1;
+    constexpr size_t smem = 2 * sizeof(__nv_bfloat16) *
+                            (NA * TileMap<AM, mm::BM>::ELEMS + NB * TileMap<BN_MAJOR, mm::BN>::ELEMS);
+    static bool configured = false;   // one per instantiation
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(mma_gemm_kernel<TA, TB, TC, AM, BN_MAJOR, MODE>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
     dim3 grid((unsigned)((g.N + mm::BN - 1) / mm::BN), (unsigned)((g.M + mm::BM - 1) / mm::BM),
               (unsigned)slabs);
     note_launch(kid, s, false);
-    mma_gemm_kernel<TA, TB, TC, AM, BN_MAJOR, MODE><<<grid, mm::THREADS, 0, s>>>(g);
+    mma_gemm_kernel<TA, TB, TC, AM, BN_MAJOR, MODE><<<grid, mm::THREADS, smem, s>>>(g);
     note_launch(kid, s, true);
     return cudaGetLastError();
 }
