@@ -44,7 +44,7 @@ UNIT = "G edge·heads/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
-GT_KERNELS = ["gt_fwd", "gt_fwd_merge", "gt_bwd_dq", "gt_bwd_dkdv", "gt_bwd_merge"]
+GT_KERNELS = ["gt_fwd", "gt_fwd_merge", "bsr_fwd", "gt_bwd_dq", "gt_bwd_dkdv", "gt_bwd_merge"]
 GATV2_KERNELS = ["gatv2_proj", "gatv2_fwd", "gatv2_fwd_merge", "gatv2_bwd_dst", "gatv2_bwd_src",
                  "gatv2_bwd_merge", "gatv2_bwd_dx", "gatv2_bwd_dw", "gatv2_bwd_reduce"]
 
@@ -64,6 +64,8 @@ def parse_args(argv=None):
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--split-threshold", type=int, default=0)
     p.add_argument("--chunk-len", type=int, default=0)
+    p.add_argument("--tile-min-nnz", type=int, default=0,
+                   help="> 0: block-sparse tensor-core forward (GT, bf16) with this tile threshold")
     p.add_argument("--json-out", default="")
     return p.parse_args(argv)
 
@@ -233,7 +235,7 @@ def traffic_for(kernel: str, workload: str):
 class Workload:
     """Host inputs (pinned), device inputs, plan and step functions."""
 
-    def __init__(self, key: int, device, split_threshold=0, chunk_len=0):
+    def __init__(self, key: int, device, split_threshold=0, chunk_len=0, tile_min_nnz=0):
         import sparse_graph_attention_csr_gb300 as sga
         self.sga = sga
         self.w = synth.WORKLOADS[key]
@@ -262,7 +264,8 @@ class Workload:
         F = w.F if w.layer == "gatv2" else 0
         t0 = time.perf_counter()
         self.plan = sga.Plan(self.ip, self.ix, w.H, w.D, self.tdt, F=F,
-                             split_threshold=split_threshold, chunk_len=chunk_len)
+                             split_threshold=split_threshold, chunk_len=chunk_len,
+                             tile_min_nnz=tile_min_nnz)
         torch.cuda.synchronize()
         self.plan_ms = (time.perf_counter() - t0) * 1e3
         self.outputs = None
@@ -415,7 +418,7 @@ def run_native(args, ws, rank, local):
     from sparse_graph_attention_csr_gb300 import build as sga_build
     sga_build.build()
     dev = torch.device("cuda", local)
-    wl = Workload(args.config, dev, args.split_threshold, args.chunk_len)
+    wl = Workload(args.config, dev, args.split_threshold, args.chunk_len, args.tile_min_nnz)
     w = wl.w
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size

@@ -64,12 +64,23 @@ typedef struct {
     int32_t split_threshold;  /* rows of degree > this are split (default 256) */
     int32_t chunk_len;        /* edges per chunk of a split row (default 128) */
     int32_t in_features;      /* GATv2 input width F; 0 for a Graph Transformer plan */
-    int32_t reserved;         /* must be 0 */
+    int32_t tile_min_nnz;     /* > 0: block-sparse tensor-core forward, see below; 0: off */
 } sga_plan_opts;
 
 /* Build a plan: validates the CSR on the device (indptr[0] = 0, monotone,
  * indptr[N] = E, 0 <= indices < N), builds the transposed CSR (sources ->
  * ascending destinations) and the degree partitions of both.
+ * Block-sparse plans (opts->tile_min_nnz > 0; bf16, D in {64, 128}, N <= 2^18):
+ * the "block-sparse graph representation that enables the use of tensor
+ * cores" of the IO-aware layers blog post ("Attention-based layers"
+ * paragraph).  Destinations are grouped in panels of 128 rows and sources in
+ * column tiles of 16; every (panel, tile) pair with at least tile_min_nnz edges
+ * is kept with one 16-bit source mask per panel row, all other edges form a
+ * residual CSR.  gt_attn_fwd then computes the kept tiles on the tcgen05
+ * tensor cores and the residual edges with the CSR kernels, merged by
+ * log-sum-exp; gt_attn_bwd is unchanged (it needs only out and lse).  A
+ * mask holds an edge once, so an edge repeated inside a kept tile is refused
+ * (SGA_EINVAL); other shapes and dtypes return SGA_EUNSUPPORTED.
  * indptr/indices: device pointers, read only during this call.
  * The plan owns device memory for the transposed CSR and partitions (freed by
  * sga_plan_destroy).  Synchronises `stream`.  Returns SGA_EINVAL for an
@@ -177,6 +188,9 @@ typedef struct {
     int32_t n_split, n_chunks;        /* CSR rows split, and their chunk count */
     int32_t t_n_split, t_n_chunks;    /* the same for the transposed CSR */
     int64_t plan_device_bytes;        /* device memory the plan owns */
+    int32_t n_tiles;                  /* block-sparse plans: kept tiles */
+    int32_t n_panels;                 /*   panels of 128 rows */
+    int64_t E_residual;               /*   edges left in the residual CSR */
 } sga_plan_info;
 
 sga_status sga_plan_get_info(const sga_plan *plan, sga_plan_info *info);
@@ -193,7 +207,12 @@ typedef enum {
     SGA_ARR_T_CHUNK_PTR = 8,
     SGA_ARR_T_CHUNK_ROW = 9,
     SGA_ARR_T_CHUNK_BEG = 10,
-    SGA_ARR_T_CHUNK_END = 11
+    SGA_ARR_T_CHUNK_END = 11,
+    SGA_ARR_TILE_PTR = 12,    /* [n_panels+1] block-sparse plans */
+    SGA_ARR_TILE_COL = 13,    /* [n_tiles] */
+    SGA_ARR_TILE_BITS = 14,   /* [n_tiles*64]: the [n_tiles][128] uint16 masks, as int32 words */
+    SGA_ARR_R_INDPTR = 15,    /* [N+1] residual CSR */
+    SGA_ARR_R_INDICES = 16    /* [E_residual] */
 } sga_plan_array;
 
 /* Copy one plan array into caller HOST memory of `count` int32 (must equal the
@@ -213,7 +232,8 @@ typedef enum {
     SGA_KERN_GATV2_PROJ = 6, SGA_KERN_GATV2_FWD = 7, SGA_KERN_GATV2_FWD_MERGE = 8,
     SGA_KERN_GATV2_BWD_DST = 9, SGA_KERN_GATV2_BWD_SRC = 10, SGA_KERN_GATV2_BWD_MERGE = 11,
     SGA_KERN_GATV2_BWD_DX = 12, SGA_KERN_GATV2_BWD_DW = 13, SGA_KERN_GATV2_BWD_REDUCE = 14,
-    SGA_KERN_COUNT = 15
+    SGA_KERN_BSR_FWD = 15,
+    SGA_KERN_COUNT = 16
 } sga_kernel_id;
 
 /* Time one kernel kind with CUDA events recorded on the launching stream

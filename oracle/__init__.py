@@ -285,3 +285,40 @@ def gatv2_branch_slack(indptr, indices, X, Wl, Wr, a, dO, slope=0.2, store="bf16
                                              float(slope), _STORE[store], float(tau), dO,
                                              sX, sWl, sWr, sda), "gatv2_branch_slack")
     return {"dX": sX, "dW_l": sWl, "dW_r": sWr, "da": sda}
+
+
+# ------------------------------------------------------------ block-sparse tiles
+
+def tile_extract(indptr, indices, N, min_nnz, panel=128, width=16):
+    """Block-sparse split of a CSR by its definition: rows in panels of
+    ``panel`` destinations, sources in column tiles of ``width``; a
+    (panel, tile) pair with at least ``min_nnz`` edges is kept, with one
+    ``width``-bit mask per panel row (bit b: source width*tile + b present);
+    every other edge stays in a residual CSR (same row order and source order).
+
+    Returns dict: tile_ptr [P+1], tile_col [T], tile_bits [T, panel] (uint16),
+    r_indptr [N+1], r_indices [E_r]."""
+    indptr = np.asarray(indptr, dtype=np.int64)
+    indices = np.asarray(indices, dtype=np.int64)
+    P = (N + panel - 1) // panel
+    rows = np.repeat(np.arange(N), np.diff(indptr))
+    pan, col = rows // panel, indices // width
+    key = pan * ((N + width - 1) // width) + col
+    uniq, counts = np.unique(key, return_counts=True)
+    kept_keys = uniq[counts >= min_nnz]
+    kept = np.isin(key, kept_keys)
+    tile_ptr = np.zeros(P + 1, np.int64)
+    kp = kept_keys // ((N + width - 1) // width)
+    np.add.at(tile_ptr, kp + 1, 1)
+    tile_ptr = np.cumsum(tile_ptr)
+    tile_col = (kept_keys % ((N + width - 1) // width)).astype(np.int32)
+    tile_bits = np.zeros((len(kept_keys), panel), np.uint16)
+    tix = np.searchsorted(kept_keys, key[kept])
+    np.bitwise_or.at(tile_bits, (tix, rows[kept] % panel),
+                     (1 << (indices[kept] % width)).astype(np.uint16))
+    r_counts = np.bincount(rows[~kept], minlength=N)
+    r_indptr = np.zeros(N + 1, np.int64)
+    r_indptr[1:] = np.cumsum(r_counts)
+    return {"tile_ptr": tile_ptr.astype(np.int32), "tile_col": tile_col,
+            "tile_bits": tile_bits, "r_indptr": r_indptr.astype(np.int32),
+            "r_indices": indices[~kept].astype(np.int32)}

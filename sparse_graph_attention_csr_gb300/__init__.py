@@ -26,13 +26,14 @@ KERNELS = {
     "gt_fwd": 1, "gt_fwd_merge": 2, "gt_bwd_dq": 3, "gt_bwd_dkdv": 4, "gt_bwd_merge": 5,
     "gatv2_proj": 6, "gatv2_fwd": 7, "gatv2_fwd_merge": 8, "gatv2_bwd_dst": 9,
     "gatv2_bwd_src": 10, "gatv2_bwd_merge": 11, "gatv2_bwd_dx": 12, "gatv2_bwd_dw": 13,
-    "gatv2_bwd_reduce": 14,
+    "gatv2_bwd_reduce": 14, "bsr_fwd": 15,
 }
 
 ARRAYS = {
     "t_indptr": 0, "t_dst": 1, "split_rows": 2, "chunk_ptr": 3, "chunk_row": 4, "chunk_beg": 5,
     "chunk_end": 6, "t_split_rows": 7, "t_chunk_ptr": 8, "t_chunk_row": 9, "t_chunk_beg": 10,
-    "t_chunk_end": 11,
+    "t_chunk_end": 11, "tile_ptr": 12, "tile_col": 13, "tile_bits": 14, "r_indptr": 15,
+    "r_indices": 16,
 }
 
 
@@ -47,7 +48,7 @@ class SgaError(RuntimeError):
 
 class PlanOpts(ctypes.Structure):
     _fields_ = [("split_threshold", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
-                ("in_features", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("in_features", ctypes.c_int32), ("tile_min_nnz", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -56,7 +57,8 @@ class PlanInfo(ctypes.Structure):
                 ("split_threshold", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
                 ("n_split", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
                 ("t_n_split", ctypes.c_int32), ("t_n_chunks", ctypes.c_int32),
-                ("plan_device_bytes", ctypes.c_int64)]
+                ("plan_device_bytes", ctypes.c_int64), ("n_tiles", ctypes.c_int32),
+                ("n_panels", ctypes.c_int32), ("E_residual", ctypes.c_int64)]
 
 
 _LIB = None
@@ -167,7 +169,7 @@ class Plan:
 
     def __init__(self, indptr: torch.Tensor, indices: torch.Tensor, H: int, D: int,
                  dtype=torch.bfloat16, F: int = 0, split_threshold: int = 0, chunk_len: int = 0,
-                 stream=None):
+                 tile_min_nnz: int = 0, stream=None):
         _need(indptr, "indptr", torch.int32)
         _need(indices, "indices", torch.int32)
         self.indptr, self.indices = indptr, indices
@@ -176,7 +178,7 @@ class Plan:
         self.H, self.D, self.F = int(H), int(D), int(F)
         self.dtype = dtype
         self.dt = SGA_F32 if dtype == torch.float32 else SGA_BF16
-        opts = PlanOpts(int(split_threshold), int(chunk_len), int(F), 0)
+        opts = PlanOpts(int(split_threshold), int(chunk_len), int(F), int(tile_min_nnz))
         handle = ctypes.c_void_p()
         self._h = None
         _check(_lib().sga_plan_create(_ptr(indptr), _ptr(indices), self.N, self.E, self.H, self.D,
@@ -212,7 +214,11 @@ class Plan:
              "chunk_beg": inf["n_chunks"], "chunk_end": inf["n_chunks"],
              "t_split_rows": inf["t_n_split"], "t_chunk_ptr": inf["t_n_split"] + 1,
              "t_chunk_row": inf["t_n_chunks"], "t_chunk_beg": inf["t_n_chunks"],
-             "t_chunk_end": inf["t_n_chunks"]}[name]
+             "t_chunk_end": inf["t_n_chunks"],
+             "tile_ptr": inf["n_panels"] + 1 if inf["n_panels"] else 0,
+             "tile_col": inf["n_tiles"], "tile_bits": inf["n_tiles"] * 64,
+             "r_indptr": self.N + 1 if inf["n_panels"] else 0,
+             "r_indices": inf["E_residual"]}[name]
         out = np.zeros(max(n, 1), dtype=np.int32)
         _check(_lib().sga_plan_copy_array(self._h, ARRAYS[name], out.ctypes.data, n),
                "sga_plan_copy_array")

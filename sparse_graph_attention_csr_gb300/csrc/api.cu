@@ -170,8 +170,10 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     if (!supported_shape(H, D)) return SGA_EUNSUPPORTED;
     sga_plan_opts o{};
     if (opts) o = *opts;
-    if (o.split_threshold < 0 || o.chunk_len < 0 || o.in_features < 0 || o.reserved != 0)
+    if (o.split_threshold < 0 || o.chunk_len < 0 || o.in_features < 0 || o.tile_min_nnz < 0)
         return SGA_EINVAL;
+    if (o.tile_min_nnz > 0 && (!bsr_fwd_supported(dt, D) || N > (1 << 18) || o.tile_min_nnz > 128 * 16))
+        return SGA_EUNSUPPORTED;
     if (o.in_features != 0 && (o.in_features % 8 != 0 || o.in_features > 1024))
         return SGA_EUNSUPPORTED;
     sga_plan *p = new (std::nothrow) sga_plan();
@@ -199,6 +201,35 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
         return st;
     }
     compute_layout(p);
+    if (o.tile_min_nnz > 0) {
+        p->tiles.min_nnz = o.tile_min_nnz;
+        st = bsr_build(p, static_cast<cudaStream_t>(stream));
+        sga_plan *rp = st == SGA_OK ? new (std::nothrow) sga_plan() : nullptr;
+        if (st == SGA_OK && !rp) st = SGA_EINVAL;
+        if (st == SGA_OK) {   // plan over the residual CSR
+            rp->N = N;
+            rp->E = p->tiles.E_res;
+            rp->H = H;
+            rp->D = D;
+            rp->dt = dt;
+            rp->split_threshold = p->split_threshold;
+            rp->chunk_len = p->chunk_len;
+            rp->indptr = p->tiles.r_indptr;
+            rp->indices = p->tiles.r_indices;
+            rp->num_sms = p->num_sms;
+            p->residual = rp;
+            st = plan_build(rp, static_cast<cudaStream_t>(stream));
+            if (st == SGA_OK) {
+                compute_layout(rp);
+                p->residual_ws = p->layout.total;
+                p->layout.total += round256(rp->layout.total);
+            }
+        }
+        if (st != SGA_OK) {
+            sga_plan_destroy(p);
+            return st;
+        }
+    }
     *out = p;
     return SGA_OK;
 }
@@ -213,11 +244,20 @@ sga_status sga_plan_set_workspace(sga_plan *plan, void *d_workspace, size_t byte
     }
     plan->ws = d_workspace;
     plan->ws_bytes = bytes;
+    if (plan->residual) {
+        plan->residual->ws = static_cast<char *>(d_workspace) + plan->residual_ws;
+        plan->residual->ws_bytes = plan->residual->layout.total;
+    }
     return SGA_OK;
 }
 
 void sga_plan_destroy(sga_plan *plan) {
     if (!plan) return;
+    if (plan->residual) {
+        plan_free(plan->residual);
+        delete plan->residual;
+        plan->residual = nullptr;
+    }
     plan_free(plan);
     delete plan;
 }
@@ -236,7 +276,10 @@ sga_status sga_plan_get_info(const sga_plan *p, sga_plan_info *info) {
     info->n_chunks = p->rows.n_chunks;
     info->t_n_split = p->cols.n_split;
     info->t_n_chunks = p->cols.n_chunks;
-    info->plan_device_bytes = p->device_bytes;
+    info->plan_device_bytes = p->device_bytes + (p->residual ? p->residual->device_bytes : 0);
+    info->n_tiles = p->tiles.n_tiles;
+    info->n_panels = p->tiles.n_panels;
+    info->E_residual = p->tiles.E_res;
     return SGA_OK;
 }
 
@@ -259,6 +302,14 @@ sga_status sga_plan_copy_array(const sga_plan *p, sga_plan_array which, int32_t 
         case SGA_ARR_T_CHUNK_ROW: src = C.chunk_row; n = C.n_chunks; break;
         case SGA_ARR_T_CHUNK_BEG: src = C.chunk_beg; n = C.n_chunks; break;
         case SGA_ARR_T_CHUNK_END: src = C.chunk_end; n = C.n_chunks; break;
+        case SGA_ARR_TILE_PTR: src = p->tiles.tile_ptr; n = p->tiles.min_nnz ? p->tiles.n_panels + 1 : 0; break;
+        case SGA_ARR_TILE_COL: src = p->tiles.tile_col; n = p->tiles.n_tiles; break;
+        case SGA_ARR_TILE_BITS:
+            src = reinterpret_cast<const int32_t *>(p->tiles.tile_bits);
+            n = (int64_t)p->tiles.n_tiles * 64;
+            break;
+        case SGA_ARR_R_INDPTR: src = p->tiles.r_indptr; n = p->tiles.min_nnz ? p->N + 1 : 0; break;
+        case SGA_ARR_R_INDICES: src = p->tiles.r_indices; n = p->tiles.E_res; break;
         default: return SGA_EINVAL;
     }
     if (count != n) return SGA_EINVAL;
@@ -309,13 +360,39 @@ sga_status gt_attn_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *
     sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, p ? p->F : 0);
     if (st != SGA_OK) return st;
     if (!tensors_ok(N, {Q, K, V, out, lse})) return SGA_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->residual) {   // block-sparse plan: residual edges on the CSR path, tiles on tcgen05
+        GtArgs r = gt_args(p->residual);
+        r.Q = Q;
+        r.K = K;
+        r.V = V;
+        r.out_w = out;
+        r.lse_w = lse;
+        r.d_err = p->d_err;
+        cudaError_t e = gt_fwd_t<__nv_bfloat16>(r, s);
+        if (e != cudaSuccess) return cuda_status(e);
+        BsrArgs b{};
+        b.Q = Q;
+        b.K = K;
+        b.V = V;
+        b.out = out;
+        b.lse = lse;
+        b.tile_ptr = p->tiles.tile_ptr;
+        b.tile_col = p->tiles.tile_col;
+        b.tile_bits = p->tiles.tile_bits;
+        b.N = N;
+        b.H = H;
+        b.D = D;
+        b.n_panels = p->tiles.n_panels;
+        b.d_err = p->d_err;
+        return cuda_status(launch_bsr_fwd(b, s));
+    }
     GtArgs a = gt_args(p);
     a.Q = Q;
     a.K = K;
     a.V = V;
     a.out_w = out;
     a.lse_w = lse;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     return cuda_status(dt == SGA_F32 ? gt_fwd_t<float>(a, s) : gt_fwd_t<__nv_bfloat16>(a, s));
 }
 

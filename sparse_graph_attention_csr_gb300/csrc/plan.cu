@@ -113,6 +113,8 @@ scan_apply_kernel(const int32_t *in, int32_t *out, int64_t n, const int32_t *__r
     }
 }
 
+}  // namespace
+
 int64_t scan_tmp_elems(int64_t n) {
     int64_t t = 0;
     while (n > kScanTile) {
@@ -138,6 +140,8 @@ cudaError_t exclusive_scan(const int32_t *in, int32_t *out, int64_t n, int32_t *
     scan_apply_kernel<<<(unsigned)nb, kScanThreads, 0, s>>>(in, out, n, offs);
     return cudaGetLastError();
 }
+
+namespace {
 
 // ------------------------------------------------------------- radix sort
 

@@ -42,6 +42,20 @@ struct WorkspaceLayout {
     int32_t dw_slabs = 0;
 };
 
+// Block-sparse split of the CSR (tensor-core forward): 128-row panels x
+// 16-source column tiles with at least min_nnz edges are kept, each with one
+// 16-bit source mask per panel row; all other edges form a residual CSR.
+struct TileSet {
+    int32_t min_nnz = 0;            // 0: no block-sparse representation
+    int32_t n_panels = 0, n_tiles = 0;
+    int64_t E_res = 0;
+    int32_t *tile_ptr = nullptr;    // [n_panels + 1]
+    int32_t *tile_col = nullptr;    // [n_tiles] column tile (sources 16c .. 16c+15)
+    uint16_t *tile_bits = nullptr;  // [n_tiles][128] source masks per panel row
+    int32_t *r_indptr = nullptr;    // [N + 1] residual CSR
+    int32_t *r_indices = nullptr;   // [E_res]
+};
+
 }  // namespace sga
 
 struct sga_plan {
@@ -54,6 +68,9 @@ struct sga_plan {
     int32_t *t_indptr = nullptr;       // [N + 1]
     int32_t *t_dst = nullptr;          // [E]
     sga::Partition rows, cols;         // partitions of the CSR and the transposed CSR
+    sga::TileSet tiles;                // block-sparse split (tiles.min_nnz > 0)
+    sga_plan *residual = nullptr;      // plan over the residual CSR (block-sparse plans)
+    size_t residual_ws = 0;            // offset of the residual plan's workspace
     int32_t *d_err = nullptr;          // device error word
     void *ws = nullptr;
     size_t ws_bytes = 0;
@@ -65,11 +82,17 @@ struct sga_plan {
 
 namespace sga {
 
-// ---- plan builders (plan.cu) ----
+// ---- plan builders (plan.cu, bsr.cu) ----
 sga_status plan_build(sga_plan *p, cudaStream_t s);
+sga_status bsr_build(sga_plan *p, cudaStream_t s);   // fills p->tiles (plan-owned memory)
 void plan_free(sga_plan *p);
 void set_cuda_error(cudaError_t e);
 int get_cuda_error();
+
+// Device exclusive prefix sum of n int32 (out may alias in); tmp holds
+// scan_tmp_elems(n) int32.
+int64_t scan_tmp_elems(int64_t n);
+cudaError_t exclusive_scan(const int32_t *in, int32_t *out, int64_t n, int32_t *tmp, cudaStream_t s);
 
 // ---- Graph Transformer (gt.cu) ----
 struct GtArgs {
@@ -111,6 +134,21 @@ struct Gatv2Args {
     int32_t *d_err;
 };
 template <typename T> cudaError_t gatv2_fwd_t(const Gatv2Args &a, cudaStream_t s);
+
+// ---- block-sparse tensor-core forward (bsr_fwd.cu) ----
+struct BsrArgs {
+    const void *Q, *K, *V;      // [N, H, D] bf16
+    void *out;                  // in: residual forward, out: merged
+    float *lse;                 // likewise
+    const int32_t *tile_ptr, *tile_col;
+    const uint16_t *tile_bits;
+    int64_t N;
+    int H, D;
+    int n_panels;
+    int32_t *d_err;
+};
+bool bsr_fwd_supported(sga_dtype dt, int D);
+cudaError_t launch_bsr_fwd(const BsrArgs &a, cudaStream_t s);
 template <typename T> cudaError_t gatv2_bwd_t(const Gatv2Args &a, cudaStream_t s);
 
 }  // namespace sga

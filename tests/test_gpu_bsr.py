@@ -1,0 +1,162 @@
+"""Block-sparse tensor-core forward (kept 128 x 16 tiles on tcgen05, residual
+edges on the CSR kernels, merged by log-sum-exp) vs the fp64 oracle, and the
+tile extraction vs its definition, bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_graph_attention_csr_gb300 as sga
+from sparse_graph_attention_csr_gb300 import synth
+
+from helpers import compare, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def sbm_graph(seed, N, block=256, p_in=0.15, inter=4):
+    rng = np.random.default_rng(seed)
+    return synth.graph_sbm(rng, N, block, p_in, inter) if N % block == 0 else \
+        synth.graph_sbm(rng, (N // block) * block, block, p_in, inter)
+
+
+def ragged_graph(seed, N):
+    """Dense diagonal blocks plus random edges, N not a multiple of 128 or 16."""
+    rng = np.random.default_rng(seed)
+    dst, src = [], []
+    for b0 in range(0, N, 96):
+        b1 = min(N, b0 + 96)
+        m = rng.random((b1 - b0, b1 - b0)) < 0.3
+        d, s = np.nonzero(m)
+        dst.append(d + b0)
+        src.append(s + b0)
+    n = 3 * N
+    dst.append(rng.integers(0, N, n))
+    src.append(rng.integers(0, N, n))
+    return synth.csr_from_edges(N, np.concatenate(dst), np.concatenate(src))
+
+
+def inputs(seed, N, H, D, std):
+    g = torch.Generator().manual_seed(seed)
+    t = [(torch.randn(N, H, D, generator=g) * std).to(torch.bfloat16) for _ in range(4)]
+    return [(x, x.double().numpy()) for x in t]
+
+
+def check_tiles(plan, indptr, indices, N, tau):
+    ref = oracle.tile_extract(indptr, indices, N, tau)
+    np.testing.assert_array_equal(plan.array("tile_ptr"), ref["tile_ptr"])
+    np.testing.assert_array_equal(plan.array("tile_col"), ref["tile_col"])
+    bits = plan.array("tile_bits").view(np.uint16).reshape(-1, 128)
+    np.testing.assert_array_equal(bits, ref["tile_bits"])
+    np.testing.assert_array_equal(plan.array("r_indptr"), ref["r_indptr"])
+    np.testing.assert_array_equal(plan.array("r_indices"), ref["r_indices"])
+    return ref
+
+
+@pytest.mark.parametrize("case", ["sbm_d128", "sbm_d64", "ragged_d128"])
+def test_block_sparse_forward_and_backward(case):
+    if case.startswith("sbm"):
+        N, H, D = 4096, 4, (128 if case.endswith("128") else 64)
+        indptr, indices = sbm_graph(7, N)
+        tau = 16
+    else:
+        N, H, D = 1000, 2, 128
+        indptr, indices = ragged_graph(8, N)
+        tau = 24
+    (q, qf), (k, kf), (v, vf), (do, dof) = inputs(3, N, H, D, D ** -0.5)
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, tile_min_nnz=tau)
+    inf = plan.info()
+    assert inf["n_tiles"] > 0 and inf["E_residual"] > 0
+    ref_t = check_tiles(plan, indptr, indices, N, tau)
+    # most of the SBM's edges fall in kept tiles
+    if case.startswith("sbm"):
+        assert inf["E_residual"] < 0.25 * len(indices)
+    Q, K, V, dO = (dev(x) for x in (q, k, v, do))
+    out, lse = sga.gt_attn_fwd(plan, Q, K, V)
+    ro, rl = oracle.gt_fwd(indptr, indices, qf, kf, vf)
+    compare(out, ro, "bf16", "out")
+    compare(lse, rl, "bf16", "lse")
+    # same layer on the CSR path (plan without tiles)
+    plan_csr = sga.Plan(ip, ix, H, D, torch.bfloat16)
+    out_c, lse_c = sga.gt_attn_fwd(plan_csr, Q, K, V)
+    compare(out, out_c.double().cpu().numpy(), "bf16", "out vs CSR path")
+    dQ, dK, dV = sga.gt_attn_bwd(plan, Q, K, V, out, lse, dO)
+    rq, rk, rv = oracle.gt_bwd(indptr, indices, qf, kf, vf, dof)
+    compare(dQ, rq, "bf16", "dQ")
+    compare(dK, rk, "bf16", "dK")
+    compare(dV, rv, "bf16", "dV")
+    assert plan.device_error() == 0
+
+
+def test_block_sparse_is_deterministic_and_handles_empty_panels():
+    N, H, D = 2000, 1, 64
+    indptr, indices = ragged_graph(9, N)
+    # a threshold no tile reaches: everything stays on the CSR path
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, tile_min_nnz=2048)
+    assert plan.info()["n_tiles"] == 0
+    (q, qf), (k, kf), (v, vf), _ = inputs(5, N, H, D, 0.125)
+    Q, K, V = dev(q), dev(k), dev(v)
+    out, lse = sga.gt_attn_fwd(plan, Q, K, V)
+    ro, rl = oracle.gt_fwd(indptr, indices, qf, kf, vf)
+    compare(out, ro, "bf16", "out")
+    plan2 = sga.Plan(ip, ix, H, D, torch.bfloat16, tile_min_nnz=20)
+    a = sga.gt_attn_fwd(plan2, Q, K, V)
+    b = sga.gt_attn_fwd(plan2, Q, K, V)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    compare(a[0], ro, "bf16", "out")
+
+
+def test_block_sparse_rejects_repeated_edges_in_kept_tiles():
+    # row 0 lists source 3 twice; its tile (panel 0, sources 0..15) is kept
+    N = 64
+    rows = [list(range(16)) + [3]] + [list(range(16))] * (N - 1)
+    indptr = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
+    indices = np.concatenate(rows).astype(np.int32)
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    with pytest.raises(sga.SgaError) as ei:
+        sga.Plan(ip, ix, 1, 64, torch.bfloat16, tile_min_nnz=8)
+    assert ei.value.status == sga.SGA_EINVAL
+    # the same graph on the CSR path counts the repeat as its own edge
+    sga.Plan(ip, ix, 1, 64, torch.bfloat16)
+    # a repeat in a tile that is not kept stays in the residual CSR
+    indices2 = indices.copy()
+    indices2[16] = 40   # row 0: source 40 (tile 2, one edge) instead of the repeat
+    rows2 = indices2.tolist()
+    indices3 = np.array(rows2[:16] + [40, 40] + rows2[17:], np.int32)
+    indptr3 = indptr.copy()
+    indptr3[1:] += 1
+    ip3, ix3 = dev(torch.from_numpy(indptr3)), dev(torch.from_numpy(indices3))
+    plan = sga.Plan(ip3, ix3, 1, 64, torch.bfloat16, tile_min_nnz=8)
+    assert plan.info()["E_residual"] == 2
+
+
+def test_block_sparse_rejects_unsupported_shapes():
+    indptr = np.array([0, 1, 2], np.int32)
+    indices = np.array([0, 1], np.int32)
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    for dtype, D in ((torch.float32, 64), (torch.bfloat16, 32)):
+        with pytest.raises(sga.SgaError) as ei:
+            sga.Plan(ip, ix, 1, D, dtype, tile_min_nnz=4)
+        assert ei.value.status == sga.SGA_EUNSUPPORTED
+
+
+@pytest.mark.slow
+def test_workload5_block_sparse_sampled():
+    w = synth.WORKLOADS[5]
+    indptr, indices = synth.make_graph(w)
+    x = synth.gt_inputs(w)
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, w.H, w.D, torch.bfloat16, tile_min_nnz=16)
+    check_tiles(plan, indptr, indices, w.N, 16)
+    Q, K, V = (dev(x[n][0]) for n in ("Q", "K", "V"))
+    out, lse = sga.gt_attn_fwd(plan, Q, K, V)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(55)
+    rows = np.unique(np.concatenate([rng.integers(0, w.N, 2000), [0, 127, 128, w.N - 1]]))
+    ro, rl = oracle.gt_fwd(indptr, indices, x["Q"][1], x["K"][1], x["V"][1], rows=rows)
+    r = torch.from_numpy(rows).cuda()
+    compare(out[r], ro, "bf16", "out")
+    compare(lse[r], rl, "bf16", "lse")
+    assert plan.device_error() == 0

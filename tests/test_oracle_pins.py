@@ -408,3 +408,43 @@ def test_gatv2_branch_slack_bounds_flipped_branches():
     assert diff.max() > 1e-3                       # the branch matters
     assert np.all(diff <= sl["dW_l"] * (1 + 1e-6) + 1e-7)
     assert sl["dW_l"].max() <= diff.max() * (1 + 1e-6) + 1e-7   # and the bound is tight here
+
+
+# ------------------------------------------------------------ block-sparse tiles
+
+def test_tile_extract_by_brute_force():
+    """Tiles, bitmaps and residual against an explicit per-edge loop; the kept
+    and residual edges partition the graph."""
+    rng = np.random.default_rng(31)
+    N = 300
+    indptr, indices = rand_graph(rng, N, 0.04)
+    # a dense block so that some tiles pass the threshold
+    rows = [list(indices[indptr[i]:indptr[i + 1]]) for i in range(N)]
+    for i in range(128, 200):
+        rows[i] = sorted(set(rows[i]) | set(range(32, 64)))
+    indptr = np.zeros(N + 1, np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in rows])
+    indices = np.array([j for r in rows for j in r], np.int32)
+    t = oracle.tile_extract(indptr, indices, N, min_nnz=20)
+    counts = {}
+    for i in range(N):
+        for e in range(indptr[i], indptr[i + 1]):
+            k = (i // 128, indices[e] // 16)
+            counts[k] = counts.get(k, 0) + 1
+    kept = sorted(k for k, c in counts.items() if c >= 20)
+    assert len(kept) > 0
+    got = [(p, c) for p in range(len(t["tile_ptr"]) - 1)
+           for c in t["tile_col"][t["tile_ptr"][p]:t["tile_ptr"][p + 1]]]
+    assert got == kept
+    res_rows = [[] for _ in range(N)]
+    for i in range(N):
+        for e in range(indptr[i], indptr[i + 1]):
+            j = indices[e]
+            k = (i // 128, j // 16)
+            if k in counts and counts[k] >= 20:
+                ti = kept.index(k)
+                assert t["tile_bits"][ti, i % 128] >> (j % 16) & 1
+            else:
+                res_rows[i].append(j)
+    assert [list(t["r_indices"][t["r_indptr"][i]:t["r_indptr"][i + 1]]) for i in range(N)] == res_rows
+    assert sum(bin(int(b)).count("1") for b in t["tile_bits"].ravel()) + len(t["r_indices"]) == len(indices)
