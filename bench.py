@@ -44,7 +44,8 @@ UNIT = "G edge·heads/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
-GT_KERNELS = ["gt_fwd", "gt_fwd_merge", "bsr_fwd", "gt_bwd_dq", "gt_bwd_dkdv", "gt_bwd_merge"]
+GT_KERNELS = ["gt_fwd", "gt_fwd_merge", "bsr_fwd", "bsr_bwd_delta", "gt_bwd_dq", "gt_bwd_dkdv",
+              "gt_bwd_merge", "bsr_bwd_dq", "bsr_bwd_dkdv"]
 GATV2_KERNELS = ["gatv2_proj", "gatv2_fwd", "gatv2_fwd_merge", "gatv2_bwd_dst", "gatv2_bwd_src",
                  "gatv2_bwd_merge", "gatv2_bwd_dx", "gatv2_bwd_dw", "gatv2_bwd_reduce"]
 
@@ -188,6 +189,25 @@ def algorithmic_bytes(kernel: str, N: int, E: int, H: int, D: int, F: int, s: in
     return 0
 
 
+def bsr_bytes(kernel: str, N: int, H: int, D: int, s: int, n_tiles: int, n_entries: int) -> int:
+    """Compulsory bytes of one block-sparse launch: each panel's own rows once,
+    the 16 source rows of every kept tile once per head, 256 bytes of masks
+    per tile, row statistics once; the dK/dV pass reads the 128 destination
+    rows of every (row panel, column panel) entry."""
+    HD = H * D
+    row = N * HD * s
+    tiles = n_tiles * (16 * 2 * HD * s + 256 + 4)
+    if kernel == "bsr_fwd":          # Q; K, V per tile; out, lse read and written
+        return row + tiles + 2 * row + 8 * N * H
+    if kernel == "bsr_bwd_delta":    # Q, dOut, lse; K, V per tile; Delta_t written
+        return 2 * row + 4 * N * H + tiles + 4 * N * H
+    if kernel == "bsr_bwd_dq":       # as above + Delta read, dQ read and written
+        return 2 * row + 8 * N * H + tiles + 2 * row
+    if kernel == "bsr_bwd_dkdv":     # K, V; per entry Q, dOut, lse, Delta of 128 rows, 8 masks
+        return 2 * row + n_entries * (128 * (2 * HD * s + 8 * H) + 8 * 256 + 36) + 4 * row
+    return 0
+
+
 def kernel_flops(kernel: str, N: int, H: int, D: int, F: int) -> int:
     HD = H * D
     if kernel == "gatv2_proj" or kernel == "gatv2_bwd_dw":
@@ -268,6 +288,8 @@ class Workload:
                              tile_min_nnz=tile_min_nnz)
         torch.cuda.synchronize()
         self.plan_ms = (time.perf_counter() - t0) * 1e3
+        self.tile_min_nnz = tile_min_nnz
+        self.E_residual = self.plan.info()["E_residual"] if tile_min_nnz else self.E
         self.outputs = None
 
     @property
@@ -474,13 +496,34 @@ def run_native(args, ws, rank, local):
         roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": ach / peaks["bf16_tflops"]}
     else:
-        nbytes = algorithmic_bytes(dominant, wl.N, wl.E, w.H, w.D, F, wl.s)
+        # on a block-sparse plan the CSR kernels see only the residual edges
+        e_k = wl.E_residual if wl.tile_min_nnz else wl.E
+        if dominant.startswith("bsr_"):
+            inf = wl.plan.info()
+            nbytes = bsr_bytes(dominant, wl.N, w.H, w.D, wl.s, inf["n_tiles"], inf["n_entries"])
+        else:
+            nbytes = algorithmic_bytes(dominant, wl.N, e_k, w.H, w.D, F, wl.s)
         ach = nbytes / (avg_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes}
     roof.update({"kernel": dominant, "launches": dom_n, "avg_launch_ms": avg_ms,
                  "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json' if peak_kind == 'measured' else '6.8 TB/s, 1.9 PFLOP/s'})",
                  "traffic": traffic_for(dominant, w.name)})
+
+    # block-sparse forward: tensor-core rate of the tile kernel (MMA work
+    # issued, masked slots included) over one step
+    bsr = None
+    if wl.tile_min_nnz:
+        inf = wl.plan.info()
+        ms_b, n_b = per_kernel.get("bsr_fwd", (0.0, 0))
+        mma = 2 * 2 * inf["n_tiles"] * w.H * 128 * 16 * w.D
+        bsr = {"tile_min_nnz": wl.tile_min_nnz, "n_tiles": inf["n_tiles"], "n_entries": inf["n_entries"],
+               "E_in_tiles": wl.E - inf["E_residual"], "E_residual": inf["E_residual"],
+               "tile_fill": (wl.E - inf["E_residual"]) / max(1, inf["n_tiles"] * 128 * 16),
+               "bsr_fwd_ms": ms_b, "mma_flop": mma}
+        if ms_b > 0:
+            t = mma / (ms_b / 1e3) / 1e12
+            bsr.update({"mma_tflops": t, "frac_of_bf16_peak": t / peaks["bf16_tflops"]})
 
     # end to end: pinned host inputs -> device, layer, outputs -> pinned host
     e2e = None
@@ -531,8 +574,10 @@ def run_native(args, ws, rank, local):
                    "pass": "fwd+bwd" if w.backward else "fwd",
                    "l2": "flushed before every step (write of 2x L2), outside the timed interval",
                    "parallelism": f"replicas x{ws}",
-                   "plan_build_ms": round(wl.plan_ms, 2)},
+                   "plan_build_ms": round(wl.plan_ms, 2),
+                   "tile_min_nnz": wl.tile_min_nnz},
         "roofline": roof,
+        "block_sparse": bsr,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

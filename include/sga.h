@@ -78,7 +78,10 @@ typedef struct {
  * is kept with one 16-bit source mask per panel row, all other edges form a
  * residual CSR.  gt_attn_fwd then computes the kept tiles on the tcgen05
  * tensor cores and the residual edges with the CSR kernels, merged by
- * log-sum-exp; gt_attn_bwd is unchanged (it needs only out and lse).  A
+ * log-sum-exp.  gt_attn_bwd computes the tile part of the row term Delta on
+ * the tensor cores, runs the residual CSR backward with it, then adds the
+ * tiles' dQ (row panels) and dK/dV (column panels of 128 sources) from
+ * tensor-core products (FlashAttention-2 style).  A
  * mask holds an edge once, so an edge repeated inside a kept tile is refused
  * (SGA_EINVAL); other shapes and dtypes return SGA_EUNSUPPORTED.
  * indptr/indices: device pointers, read only during this call.
@@ -191,6 +194,8 @@ typedef struct {
     int32_t n_tiles;                  /* block-sparse plans: kept tiles */
     int32_t n_panels;                 /*   panels of 128 rows */
     int64_t E_residual;               /*   edges left in the residual CSR */
+    int32_t n_entries;                /*   (row panel, 128-source column panel) pairs with a kept tile */
+    int32_t reserved;
 } sga_plan_info;
 
 sga_status sga_plan_get_info(const sga_plan *plan, sga_plan_info *info);
@@ -232,8 +237,9 @@ typedef enum {
     SGA_KERN_GATV2_PROJ = 6, SGA_KERN_GATV2_FWD = 7, SGA_KERN_GATV2_FWD_MERGE = 8,
     SGA_KERN_GATV2_BWD_DST = 9, SGA_KERN_GATV2_BWD_SRC = 10, SGA_KERN_GATV2_BWD_MERGE = 11,
     SGA_KERN_GATV2_BWD_DX = 12, SGA_KERN_GATV2_BWD_DW = 13, SGA_KERN_GATV2_BWD_REDUCE = 14,
-    SGA_KERN_BSR_FWD = 15,
-    SGA_KERN_COUNT = 16
+    SGA_KERN_BSR_FWD = 15, SGA_KERN_BSR_BWD_DELTA = 16, SGA_KERN_BSR_BWD_DQ = 17,
+    SGA_KERN_BSR_BWD_DKDV = 18,
+    SGA_KERN_COUNT = 19
 } sga_kernel_id;
 
 /* Time one kernel kind with CUDA events recorded on the launching stream

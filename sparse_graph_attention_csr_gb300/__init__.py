@@ -26,7 +26,8 @@ KERNELS = {
     "gt_fwd": 1, "gt_fwd_merge": 2, "gt_bwd_dq": 3, "gt_bwd_dkdv": 4, "gt_bwd_merge": 5,
     "gatv2_proj": 6, "gatv2_fwd": 7, "gatv2_fwd_merge": 8, "gatv2_bwd_dst": 9,
     "gatv2_bwd_src": 10, "gatv2_bwd_merge": 11, "gatv2_bwd_dx": 12, "gatv2_bwd_dw": 13,
-    "gatv2_bwd_reduce": 14, "bsr_fwd": 15,
+    "gatv2_bwd_reduce": 14, "bsr_fwd": 15, "bsr_bwd_delta": 16, "bsr_bwd_dq": 17,
+    "bsr_bwd_dkdv": 18,
 }
 
 ARRAYS = {
@@ -58,7 +59,8 @@ class PlanInfo(ctypes.Structure):
                 ("n_split", ctypes.c_int32), ("n_chunks", ctypes.c_int32),
                 ("t_n_split", ctypes.c_int32), ("t_n_chunks", ctypes.c_int32),
                 ("plan_device_bytes", ctypes.c_int64), ("n_tiles", ctypes.c_int32),
-                ("n_panels", ctypes.c_int32), ("E_residual", ctypes.c_int64)]
+                ("n_panels", ctypes.c_int32), ("E_residual", ctypes.c_int64),
+                ("n_entries", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _LIB = None

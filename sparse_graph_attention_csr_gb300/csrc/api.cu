@@ -280,6 +280,7 @@ sga_status sga_plan_get_info(const sga_plan *p, sga_plan_info *info) {
     info->n_tiles = p->tiles.n_tiles;
     info->n_panels = p->tiles.n_panels;
     info->E_residual = p->tiles.E_res;
+    info->n_entries = p->tiles.n_entries;
     return SGA_OK;
 }
 
@@ -403,7 +404,7 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
     sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, p ? p->F : 0);
     if (st != SGA_OK) return st;
     if (!tensors_ok(N, {Q, K, V, out, lse, dOut, dQ, dK, dV})) return SGA_EINVAL;
-    GtArgs a = gt_args(p);
+    GtArgs a = gt_args(p->residual ? p->residual : p);
     a.Q = Q;
     a.K = K;
     a.V = V;
@@ -414,6 +415,39 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
     a.dK = dK;
     a.dV = dV;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (p->residual) {   // block-sparse plan: tiles on tcgen05 around the residual CSR passes
+        BsrBwdArgs b{};
+        b.Q = Q;
+        b.K = K;
+        b.V = V;
+        b.dOut = dOut;
+        b.lse = lse;
+        b.delta_t = ws_at<float>(p, p->layout.delta);
+        b.dQ = dQ;
+        b.dK = dK;
+        b.dV = dV;
+        b.tile_ptr = p->tiles.tile_ptr;
+        b.tile_col = p->tiles.tile_col;
+        b.tile_bits = p->tiles.tile_bits;
+        b.ct_ptr = p->tiles.ct_ptr;
+        b.ct_panel = p->tiles.ct_panel;
+        b.ct_tile = p->tiles.ct_tile;
+        b.N = N;
+        b.H = H;
+        b.D = D;
+        b.n_panels = p->tiles.n_panels;
+        b.n_cpanels = p->tiles.n_cpanels;
+        b.d_err = p->d_err;
+        cudaError_t e = cudaMemsetAsync(b.delta_t, 0, sizeof(float) * (size_t)N * H, s);
+        if (e == cudaSuccess) e = launch_bsr_bwd_delta(b, s);
+        a.delta_in = b.delta_t;   // the residual rows' Delta gains the tile part
+        a.d_err = p->d_err;
+        if (e == cudaSuccess) e = gt_bwd_t<__nv_bfloat16>(a, s);
+        b.delta = a.ws_delta;     // full Delta of every row
+        if (e == cudaSuccess) e = launch_bsr_bwd_dq(b, s);
+        if (e == cudaSuccess) e = launch_bsr_bwd_dkdv(b, s);
+        return cuda_status(e);
+    }
     return cuda_status(dt == SGA_F32 ? gt_bwd_t<float>(a, s) : gt_bwd_t<__nv_bfloat16>(a, s));
 }
 

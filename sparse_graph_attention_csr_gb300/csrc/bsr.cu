@@ -11,6 +11,7 @@
 // pairs); kept tiles are listed in column order.  Everything is determined by
 // the graph and min_nnz: the arrays are bit-exact.
 #include <algorithm>
+#include <vector>
 
 #include "common.cuh"
 #include "plan.h"
@@ -213,8 +214,54 @@ sga_status bsr_build(sga_plan *p, cudaStream_t s) {
     if ((e = cudaMemcpyAsync(&repeated, dup, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fail(e);
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(e);
     for (void *x : tmp) cudaFree(x);
+    tmp.clear();
     // a tile mask holds an edge once: repeated edges inside kept tiles cannot be represented
-    return repeated ? SGA_EINVAL : SGA_OK;
+    if (repeated) return SGA_EINVAL;
+
+    // column view (host, O(tiles)): entries (row panel, column panel of 8 tile
+    // columns) in column-panel order, row panels ascending within each
+    std::vector<int32_t> h_ptr(T.n_panels + 1), h_col(T.n_tiles);
+    if ((e = cudaMemcpy(h_ptr.data(), T.tile_ptr, sizeof(int32_t) * (T.n_panels + 1), cudaMemcpyDeviceToHost)) !=
+        cudaSuccess)
+        return fail(e);
+    if (T.n_tiles > 0 &&
+        (e = cudaMemcpy(h_col.data(), T.tile_col, sizeof(int32_t) * T.n_tiles, cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return fail(e);
+    T.n_cpanels = T.n_panels;   // 128 sources per column panel, N sources
+    std::vector<int32_t> c_ptr(T.n_cpanels + 1, 0);
+    for (int32_t pn = 0; pn < T.n_panels; ++pn)
+        for (int32_t t = h_ptr[pn]; t < h_ptr[pn + 1]; ++t)
+            if (t == h_ptr[pn] || h_col[t] / 8 != h_col[t - 1] / 8) ++c_ptr[h_col[t] / 8 + 1];
+    for (int32_t c = 0; c < T.n_cpanels; ++c) c_ptr[c + 1] += c_ptr[c];
+    T.n_entries = c_ptr[T.n_cpanels];
+    std::vector<int32_t> c_panel(T.n_entries), c_tile((size_t)T.n_entries * 8, -1), fillp(c_ptr);
+    for (int32_t pn = 0; pn < T.n_panels; ++pn) {
+        int32_t cur = -1;
+        for (int32_t t = h_ptr[pn]; t < h_ptr[pn + 1]; ++t) {
+            const int32_t cp = h_col[t] / 8;
+            if (t == h_ptr[pn] || cp != h_col[t - 1] / 8) {
+                cur = fillp[cp]++;
+                c_panel[cur] = pn;
+            }
+            c_tile[(size_t)cur * 8 + h_col[t] % 8] = t;
+        }
+    }
+    if ((e = alloc((void **)&T.ct_ptr, sizeof(int32_t) * (T.n_cpanels + 1), true)) != cudaSuccess) return fail(e);
+    if ((e = alloc((void **)&T.ct_panel, sizeof(int32_t) * T.n_entries, true)) != cudaSuccess) return fail(e);
+    if ((e = alloc((void **)&T.ct_tile, sizeof(int32_t) * 8 * (size_t)T.n_entries, true)) != cudaSuccess)
+        return fail(e);
+    if ((e = cudaMemcpy(T.ct_ptr, c_ptr.data(), sizeof(int32_t) * (T.n_cpanels + 1), cudaMemcpyHostToDevice)) !=
+        cudaSuccess)
+        return fail(e);
+    if (T.n_entries > 0) {
+        if ((e = cudaMemcpy(T.ct_panel, c_panel.data(), sizeof(int32_t) * T.n_entries, cudaMemcpyHostToDevice)) !=
+            cudaSuccess)
+            return fail(e);
+        if ((e = cudaMemcpy(T.ct_tile, c_tile.data(), sizeof(int32_t) * 8 * (size_t)T.n_entries,
+                            cudaMemcpyHostToDevice)) != cudaSuccess)
+            return fail(e);
+    }
+    return SGA_OK;
 }
 
 }  // namespace sga

@@ -28,27 +28,6 @@ constexpr int kBsThreads = 128;
 constexpr int kGroup = 64;           // sources per group (four 16-wide tiles)
 constexpr float kLazy = 8.0f;        // log2 growth that triggers a rescale
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
-                 ::"r"(addr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-          "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
-          "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
-          "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
-          "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 struct BsLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
     uint32_t q, k[2], vn[2], vt, p, total;
     int vn_ld;      // bf16 elements per natural V row (D + 8: conflict-free ldmatrix)
@@ -143,9 +122,9 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
             const int mi = lane >> 3, rr = lane & 7;
             const uint32_t src = sbase + L.vn[b] + (uint32_t)((jb * 8 + rr) * L.vn_ld + (db0 + mi) * 8) * 2;
             uint32_t v[4];
-            ldsm_x4_trans(v, src);
+            tc::ldsm_x4_trans(v, src);
             const uint32_t dst = sbase + L.vt + tc::sw128_offset((db0 + mi) * 8 + rr, jb * 8, D);
-            stsm_x4(dst, v);
+            tc::stsm_x4(dst, v);
         }
         tc::fence_proxy_async();
         __syncthreads();
@@ -196,7 +175,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
                 tc::tmem_ld32(tO + tlane + cb, u);
 #pragma unroll
                 for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
-                tmem_st32(tO + tlane + cb, u);
+                tc::tmem_st32(tO + tlane + cb, u);
             }
         }
         if (grow) {

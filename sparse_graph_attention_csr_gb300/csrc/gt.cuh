@@ -535,11 +535,12 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                         }
                         if (ch % LH == 0) a.ws_rowc[(size_t)item * a.H + h] = c[k];
                     } else {
+                        const float dl = c[k] + (a.delta_in ? a.delta_in[(size_t)it.row * a.H + h] : 0.f);
                         float o[EL];
 #pragma unroll
-                        for (int x = 0; x < EL; ++x) o[x] = (A[k][x] - c[k] * B[k][x]) * scale;
+                        for (int x = 0; x < EL; ++x) o[x] = (A[k][x] - dl * B[k][x]) * scale;
                         reinterpret_cast<uint4 *>(a.dQ)[(size_t)it.row * R + ch] = pack<T>(o);
-                        if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + h] = c[k];
+                        if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + h] = dl;
                     }
                 }
             }
@@ -710,6 +711,7 @@ __global__ void __launch_bounds__(256) gt_bwd_merge_kernel(GtArgs a, float scale
                                 shc, sum, delta);
         if (w == 0 && c < R) {
             if (which == 0) {
+                if (a.delta_in) delta += a.delta_in[(size_t)row * a.H + c / LH];
                 float o[EL];
 #pragma unroll
                 for (int x = 0; x < EL; ++x) o[x] = (sum[0][x] - delta * sum[1][x]) * scale;

@@ -54,6 +54,13 @@ struct TileSet {
     uint16_t *tile_bits = nullptr;  // [n_tiles][128] source masks per panel row
     int32_t *r_indptr = nullptr;    // [N + 1] residual CSR
     int32_t *r_indices = nullptr;   // [E_res]
+    // column view for the dK/dV pass: column panels of 128 sources (8 tile
+    // columns); one entry per (row panel, column panel) pair holding a kept
+    // tile, entries of a column panel in ascending row-panel order
+    int32_t n_cpanels = 0, n_entries = 0;
+    int32_t *ct_ptr = nullptr;      // [n_cpanels + 1]
+    int32_t *ct_panel = nullptr;    // [n_entries] row panel
+    int32_t *ct_tile = nullptr;     // [n_entries][8] tile index per tile column, -1: none
 };
 
 }  // namespace sga
@@ -107,6 +114,9 @@ struct GtArgs {
     int split_threshold;
     Partition rows, cols;
     float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_rowc, *ws_col;
+    // optional [N, H] term added to each row's Delta: the share of edges that
+    // another pass (the block-sparse tiles) handles; nullptr: none
+    const float *delta_in;
     int32_t *d_err;
 };
 template <typename T> cudaError_t gt_fwd_t(const GtArgs &a, cudaStream_t s);
@@ -149,6 +159,25 @@ struct BsrArgs {
 };
 bool bsr_fwd_supported(sga_dtype dt, int D);
 cudaError_t launch_bsr_fwd(const BsrArgs &a, cudaStream_t s);
+
+struct BsrBwdArgs {
+    const void *Q, *K, *V, *dOut;   // [N, H, D] bf16
+    const float *lse;               // [N, H]
+    float *delta_t;                 // [N, H] tile part of Delta (written by the Delta pass)
+    const float *delta;             // [N, H] full Delta (read by the dQ and dK/dV passes)
+    void *dQ, *dK, *dV;             // in: residual gradients, out: with the tile part added
+    const int32_t *tile_ptr, *tile_col;
+    const uint16_t *tile_bits;
+    const int32_t *ct_ptr, *ct_panel, *ct_tile;
+    int64_t N;
+    int H, D;
+    int n_panels, n_cpanels;
+    int32_t *d_err;
+};
+// Delta pass (delta_t), dQ pass, dK/dV pass (bsr_bwd.cu).
+cudaError_t launch_bsr_bwd_delta(const BsrBwdArgs &a, cudaStream_t s);
+cudaError_t launch_bsr_bwd_dq(const BsrBwdArgs &a, cudaStream_t s);
+cudaError_t launch_bsr_bwd_dkdv(const BsrBwdArgs &a, cudaStream_t s);
 template <typename T> cudaError_t gatv2_bwd_t(const Gatv2Args &a, cudaStream_t s);
 
 }  // namespace sga
