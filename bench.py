@@ -67,6 +67,9 @@ def parse_args(argv=None):
     p.add_argument("--chunk-len", type=int, default=0)
     p.add_argument("--tile-min-nnz", type=int, default=0,
                    help="> 0: block-sparse tensor-core forward (GT, bf16) with this tile threshold")
+    p.add_argument("--nodes", type=int, default=0,
+                   help="profiling case: the workload's recipe at this many nodes "
+                        "(SBM, ER and Chung-Lu graphs; draws scale with N)")
     p.add_argument("--json-out", default="")
     return p.parse_args(argv)
 
@@ -255,10 +258,14 @@ def traffic_for(kernel: str, workload: str):
 class Workload:
     """Host inputs (pinned), device inputs, plan and step functions."""
 
-    def __init__(self, key: int, device, split_threshold=0, chunk_len=0, tile_min_nnz=0):
+    def __init__(self, key: int, device, split_threshold=0, chunk_len=0, tile_min_nnz=0, nodes=0):
         import sparse_graph_attention_csr_gb300 as sga
         self.sga = sga
         self.w = synth.WORKLOADS[key]
+        if nodes:
+            w0 = self.w
+            params = {k: int(v * nodes / w0.N) for k, v in w0.params.items() if k == "draws"}
+            self.w = w0.scaled(N=nodes, name=f"{w0.name}_at_n{nodes}", params=params)
         w = self.w
         self.device = device
         self.indptr, self.indices = synth.make_graph(w)
@@ -440,7 +447,7 @@ def run_native(args, ws, rank, local):
     from sparse_graph_attention_csr_gb300 import build as sga_build
     sga_build.build()
     dev = torch.device("cuda", local)
-    wl = Workload(args.config, dev, args.split_threshold, args.chunk_len, args.tile_min_nnz)
+    wl = Workload(args.config, dev, args.split_threshold, args.chunk_len, args.tile_min_nnz, args.nodes)
     w = wl.w
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size

@@ -20,7 +20,9 @@
 #pragma once
 
 #include "common.cuh"
+#include "items.cuh"
 #include "plan.h"
+#include "stream.cuh"
 
 namespace sga {
 
@@ -32,258 +34,147 @@ template <typename T, int D, int NC, int G> struct GtShape {
     static_assert(LH <= G, "a head must fit in one edge group");
 };
 
-struct ItemRange {
-    int32_t row, beg, end;
-    bool partial;
-};
-
-// Work item w of a launch: chunks of split rows first, then every row (rows
-// above the split threshold are skipped; their chunks cover them).
-__device__ __forceinline__ bool decode_item(int64_t item, const Partition &P,
-                                            const int32_t *__restrict__ ptr, int64_t N,
-                                            int threshold, ItemRange &r) {
-    if (item < P.n_chunks) {
-        r.row = P.chunk_row[item];
-        r.beg = P.chunk_beg[item];
-        r.end = P.chunk_end[item];
-        r.partial = true;
-        return true;
-    }
-    const int64_t i = item - P.n_chunks;
-    if (i >= N) return false;
-    r.row = (int32_t)i;
-    r.beg = ptr[i];
-    r.end = ptr[i + 1];
-    r.partial = false;
-    return r.end - r.beg <= threshold;
-}
-
-// Fetch the 32 node ids of edges [e0, e0 + cnt) into one register per lane,
-// range-checked against N (an out-of-range id becomes -1 and flags the plan).
-__device__ __forceinline__ int32_t load_ids(const int32_t *__restrict__ ids, int32_t e0, int cnt,
-                                            int64_t N, int32_t *err) {
-    const int lane = threadIdx.x & 31;
-    int32_t j = -1;
-    if (lane < cnt) {
-        j = __ldg(ids + e0 + lane);
-        if ((uint32_t)j >= (uint32_t)N) {
-            atomicOr(err, kErrIndexRange);
-            j = -1;
-        }
-    }
-    return j;
-}
-
-// Persistent warps walk the items w, w + S, w + 2S, ... (S = warps in the
-// grid) through a three-stage pipeline: while item k runs, the metadata of
-// item k + 2S (chunk descriptor or indptr pair) and the first 32 node ids of
-// item k + S are already in flight, so a short row costs one gather latency
-// instead of three dependent ones.
-struct ItemMeta {
-    int32_t row, beg, end;   // raw loads; row < 0 past the last item
-};
-
-__device__ __forceinline__ void meta_issue(int64_t item, const Partition &P,
-                                           const int32_t *__restrict__ ptr, int64_t N,
-                                           ItemMeta &m) {
-    if (item < P.n_chunks) {
-        m.row = __ldg(P.chunk_row + item);
-        m.beg = __ldg(P.chunk_beg + item);
-        m.end = __ldg(P.chunk_end + item);
-    } else if (item - P.n_chunks < N) {
-        const int64_t i = item - P.n_chunks;
-        m.row = (int32_t)i;
-        m.beg = __ldg(ptr + i);
-        m.end = __ldg(ptr + i + 1);
-    } else {
-        m.row = -1;
-        m.beg = m.end = 0;
-    }
-}
-
-// True when the item is to be processed here (not past the end, and not a row
-// above the split threshold, whose chunks are separate items).
-__device__ __forceinline__ bool meta_eval(int64_t item, const ItemMeta &m, const Partition &P,
-                                          int threshold, ItemRange &r) {
-    r.row = m.row;
-    r.beg = m.beg;
-    r.end = m.end;
-    r.partial = item < P.n_chunks;
-    return m.row >= 0 && (r.partial || m.end - m.beg <= threshold);
-}
-
-// First batch of node ids of an item (lanes past the item's edges read nothing).
-__device__ __forceinline__ int32_t first_ids(const int32_t *__restrict__ ids, const ItemRange &r,
-                                             bool valid) {
-    const int lane = threadIdx.x & 31;
-    return (valid && lane < r.end - r.beg) ? __ldg(ids + r.beg + lane) : 0;
-}
-
-// Node ids of edges [e0, e0 + cnt), range-checked like load_ids: the
-// prefetched batch for the item's first 32 edges, a fresh load after that.
-__device__ __forceinline__ int32_t batch_ids(const int32_t *__restrict__ ids, int32_t e0, int cnt,
-                                             const ItemRange &r, int32_t id0, int64_t N,
-                                             int32_t *err) {
-    if (e0 != r.beg) return load_ids(ids, e0, cnt, N, err);
-    const int lane = threadIdx.x & 31;
-    if (lane >= cnt) return -1;
-    if ((uint32_t)id0 >= (uint32_t)N) {
-        atomicOr(err, kErrIndexRange);
-        return -1;
-    }
-    return id0;
-}
-
 // ------------------------------------------------------------------ forward
+
+// Stream shape of a kernel with NROW gathered row arrays: U neighbours per
+// group and step (1 when a lane holds two or more chunks of a row), and a ring
+// of about 10 KB per warp (2 to 8 steps).
+template <int NC, int NROW, int NSC = 0, int NOWN = 1, int NOSC = 0> struct RingDims {
+    static constexpr int U = NC >= 2 ? 1 : 2;
+    static constexpr int STEP_BYTES = U * NC * 32 * (NROW * 16 + NSC * 4);
+    static constexpr int OWN_BYTES = NC * 32 * (NOWN * 16 + NOSC * 4);
+    static constexpr int QD = 3 * OWN_BYTES > 4096 ? 2 : 3;
+    static constexpr int FIT = (13312 - QD * OWN_BYTES) / STEP_BYTES;
+    static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
+};
+template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC>
+using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC>::U, NROW, NSC, NOWN, NOSC,
+                          RingDims<NC, NROW, NSC, NOWN, NOSC>::DEPTH, RingDims<NC, NROW, NSC, NOWN, NOSC>::QD>;
+
+// gathered K, V; own Q
+template <typename T, int D, int NC, int G> using GtFwdStream = RingCfg<NC, G, 2, 0, 1, 0>;
+// gathered K, V; own Q, dOut, lse
+template <typename T, int D, int NC, int G> using GtDqStream = RingCfg<NC, G, 2, 0, 2, 1>;
+// gathered Q, dOut, lse, Delta (over the transposed CSR); own K, V
+template <typename T, int D, int NC, int G> using GtDkdvStream = RingCfg<NC, G, 2, 2, 2, 0>;
 
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gt_fwd_kernel(GtArgs a, float scale2) {
     using S = GtShape<T, D, NC, G>;
-    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    using C = GtFwdStream<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, U = C::U;
+    extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
     const int R = a.H * D / EL, HD = a.H * D;
-    const uint4 *__restrict__ Qc = static_cast<const uint4 *>(a.Q);
-    const uint4 *__restrict__ Kc = static_cast<const uint4 *>(a.K);
-    const uint4 *__restrict__ Vc = static_cast<const uint4 *>(a.V);
-    const int64_t n_items = (int64_t)a.rows.n_chunks + a.N;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
-    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-
-    ItemMeta mn, mnn;
-    meta_issue(item, a.rows, a.indptr, a.N, mn);
-    ItemRange it;
-    bool valid = meta_eval(item, mn, a.rows, a.split_threshold, it);
-    int32_t id0 = first_ids(a.indices, it, valid);
-    meta_issue(item + stride, a.rows, a.indptr, a.N, mn);
-    for (; item < n_items; item += stride) {
-        meta_issue(item + 2 * stride, a.rows, a.indptr, a.N, mnn);
-        ItemRange itn;
-        const bool validn = meta_eval(item + stride, mn, a.rows, a.split_threshold, itn);
-        const int32_t id1 = first_ids(a.indices, itn, validn);
-        if (valid) {
-            float q[NC][EL], acc[NC][EL], m[NC], l[NC];
+    StreamArrays arr{};
+    arr.rows[0] = static_cast<const uint4 *>(a.K);
+    arr.rows[1] = static_cast<const uint4 *>(a.V);
+    arr.own[0] = static_cast<const uint4 *>(a.Q);
+    EdgeStream<C> st;
+    st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
+            a.split_threshold, a.d_err);
+    StreamItem it;
+    while (st.next_item(it)) {
+        float q[NC][EL], acc[NC][EL], m[NC], l[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) q[k][x] = acc[k][x] = 0.f;
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+        }
+        for (int step = 0; step < it.nsteps; ++step) {
+            st.wait_step();
+            if (step == 0)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) unpack<T>(st.own_row(0, k), q[k]);
+            float sc[U][NC];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                ok[u] = st.valid(u);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float kf[EL];
+                    unpack<T>(st.row(u, 0, k), kf);
+                    float dot = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) dot = fmaf(q[k][x], kf[x], dot);
+                    dot = group_sum<LH>(dot);
+                    sc[u][k] = ok[u] ? dot * scale2 : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                float mx = m[k];
+#pragma unroll
+                for (int u = 0; u < U; ++u) mx = fmaxf(mx, sc[u][k]);
+                if (mx == -INFINITY) continue;
+                const float alpha = exp2_diff(m[k], mx);
+                l[k] *= alpha;
+#pragma unroll
+                for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float p = exp2_diff(sc[u][k], mx);
+                    l[k] += p;
+                    float vf[EL];
+                    unpack<T>(st.row(u, 1, k), vf);
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, vf[x], acc[k][x]);
+                }
+                m[k] = mx;
+            }
+            st.release_step();
+        }
+        // merge the edge groups of the warp (they saw disjoint edges)
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
+                const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
+                const float mx = fmaxf(m[k], mo);
+                const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
+                l[k] = l[k] * a1 + lo * a2;
+#pragma unroll
+                for (int x = 0; x < EL; ++x) {
+                    const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
+                    acc[k][x] = acc[k][x] * a1 + ao * a2;
+                }
+                m[k] = mx;
+            }
+        if (g == 0) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 const int c = gl + G * k;
-                if (c < R) unpack<T>(ldg16(Qc + (size_t)it.row * R + c), q[k]);
-                else
+                if (c >= R) continue;
+                const int h = c / LH;
+                if (it.partial) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)it.item * HD + c * EL);
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) q[k][x] = 0.f;
-#pragma unroll
-                for (int x = 0; x < EL; ++x) acc[k][x] = 0.f;
-                m[k] = -INFINITY;
-                l[k] = 0.f;
-            }
-            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-                const int cnt = min(32, it.end - e0);
-                const int32_t myj = batch_ids(a.indices, e0, cnt, it, id0, a.N, a.d_err);
-                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-                    uint4 kr[U][NC], vr[U][NC];
-                    bool ok[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int t = t0 + g + NG * u;
-                        const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
-                        ok[u] = (t < cnt) && (j >= 0);
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            const int c = gl + G * k;
-                            if (ok[u] && c < R) {
-                                kr[u][k] = ldg16_stream(Kc + (size_t)j * R + c);
-                                vr[u][k] = ldg16_stream(Vc + (size_t)j * R + c);
-                            } else {
-                                kr[u][k] = make_uint4(0, 0, 0, 0);
-                                vr[u][k] = make_uint4(0, 0, 0, 0);
-                            }
-                        }
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(acc[k][x], acc[k][x + 1], acc[k][x + 2], acc[k][x + 3]);
+                    if (c % LH == 0) {
+                        a.ws_ml[((size_t)it.item * a.H + h) * 2 + 0] = m[k];
+                        a.ws_ml[((size_t)it.item * a.H + h) * 2 + 1] = l[k];
                     }
-                    float sc[U][NC];
+                } else {
+                    const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
+                    float o[EL];
 #pragma unroll
-                    for (int u = 0; u < U; ++u)
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            float kf[EL];
-                            unpack<T>(kr[u][k], kf);
-                            float dot = 0.f;
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) dot = fmaf(q[k][x], kf[x], dot);
-                            dot = group_sum<LH>(dot);
-                            sc[u][k] = ok[u] ? dot * scale2 : -INFINITY;
-                        }
-#pragma unroll
-                    for (int k = 0; k < NC; ++k) {
-                        float mx = m[k];
-#pragma unroll
-                        for (int u = 0; u < U; ++u) mx = fmaxf(mx, sc[u][k]);
-                        if (mx == -INFINITY) continue;
-                        const float alpha = exp2_diff(m[k], mx);
-                        l[k] *= alpha;
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
-#pragma unroll
-                        for (int u = 0; u < U; ++u) {
-                            const float p = exp2_diff(sc[u][k], mx);
-                            l[k] += p;
-                            float vf[EL];
-                            unpack<T>(vr[u][k], vf);
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, vf[x], acc[k][x]);
-                        }
-                        m[k] = mx;
-                    }
-                }
-            }
-            // merge the edge groups of the warp (they saw disjoint edges)
-#pragma unroll
-            for (int off = G; off < 32; off <<= 1)
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
-                    const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
-                    const float mx = fmaxf(m[k], mo);
-                    const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
-                    l[k] = l[k] * a1 + lo * a2;
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
-                        acc[k][x] = acc[k][x] * a1 + ao * a2;
-                    }
-                    m[k] = mx;
-                }
-            if (g == 0) {
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int c = gl + G * k;
-                    if (c >= R) continue;
-                    const int h = c / LH;
-                    if (it.partial) {
-                        float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)item * HD + c * EL);
-#pragma unroll
-                        for (int x = 0; x < EL; x += 4)
-                            dst[x / 4] = make_float4(acc[k][x], acc[k][x + 1], acc[k][x + 2], acc[k][x + 3]);
-                        if (c % LH == 0) {
-                            a.ws_ml[((size_t)item * a.H + h) * 2 + 0] = m[k];
-                            a.ws_ml[((size_t)item * a.H + h) * 2 + 1] = l[k];
-                        }
-                    } else {
-                        const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
-                        float o[EL];
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) o[x] = acc[k][x] * inv;
-                        reinterpret_cast<uint4 *>(a.out_w)[(size_t)it.row * R + c] = pack<T>(o);
-                        if (c % LH == 0)
-                            a.lse_w[(size_t)it.row * a.H + h] =
-                                l[k] > 0.f ? (m[k] + log2f(l[k])) * kLn2 : -INFINITY;
-                    }
+                    for (int x = 0; x < EL; ++x) o[x] = acc[k][x] * inv;
+                    reinterpret_cast<uint4 *>(a.out_w)[(size_t)it.row * R + c] = pack<T>(o);
+                    if (c % LH == 0)
+                        a.lse_w[(size_t)it.row * a.H + h] =
+                            l[k] > 0.f ? (m[k] + log2f(l[k])) * kLn2 : -INFINITY;
                 }
             }
         }
-        it = itn;
-        valid = validn;
-        id0 = id1;
-        mn = mnn;
+        st.finish_item();
     }
+    st.drain();
 }
 
 // Merge the chunk partials of each split row: one block per split row, warp
@@ -421,135 +312,105 @@ template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
     using S = GtShape<T, D, NC, G>;
-    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    using C = GtDqStream<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, U = C::U;
+    extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
     const int R = a.H * D / EL, HD = a.H * D;
-    const uint4 *__restrict__ Kc = static_cast<const uint4 *>(a.K);
-    const uint4 *__restrict__ Vc = static_cast<const uint4 *>(a.V);
-    const int64_t n_items = (int64_t)a.rows.n_chunks + a.N;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
-    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-
-    ItemMeta mn, mnn;
-    meta_issue(item, a.rows, a.indptr, a.N, mn);
-    ItemRange it;
-    bool valid = meta_eval(item, mn, a.rows, a.split_threshold, it);
-    int32_t id0 = first_ids(a.indices, it, valid);
-    meta_issue(item + stride, a.rows, a.indptr, a.N, mn);
-    for (; item < n_items; item += stride) {
-        meta_issue(item + 2 * stride, a.rows, a.indptr, a.N, mnn);
-        ItemRange itn;
-        const bool validn = meta_eval(item + stride, mn, a.rows, a.split_threshold, itn);
-        const int32_t id1 = first_ids(a.indices, itn, validn);
-        if (valid) {
-            float q[NC][EL], go[NC][EL], A[NC][EL], B[NC][EL], c[NC], lse2[NC];
+    StreamArrays arr{};
+    arr.rows[0] = static_cast<const uint4 *>(a.K);
+    arr.rows[1] = static_cast<const uint4 *>(a.V);
+    arr.own[0] = static_cast<const uint4 *>(a.Q);
+    arr.own[1] = static_cast<const uint4 *>(a.dOut);
+    arr.osc[0] = a.lse;
+    EdgeStream<C> st;
+    st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
+            a.split_threshold, a.d_err);
+    StreamItem it;
+    while (st.next_item(it)) {
+        float q[NC][EL], go[NC][EL], A[NC][EL], B[NC][EL], c[NC], lse2[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) q[k][x] = go[k][x] = A[k][x] = B[k][x] = 0.f;
+            c[k] = 0.f;
+            lse2[k] = 0.f;
+        }
+        for (int step = 0; step < it.nsteps; ++step) {
+            st.wait_step();
+            if (step == 0)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    unpack<T>(st.own_row(0, k), q[k]);
+                    unpack<T>(st.own_row(1, k), go[k]);
+                    lse2[k] = st.own_scalar(0, k) * kLog2e;
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool ok = st.valid(u);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float kf[EL], vf[EL];
+                    unpack<T>(st.row(u, 0, k), kf);
+                    unpack<T>(st.row(u, 1, k), vf);
+                    float sdot = 0.f, dp = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        sdot = fmaf(q[k][x], kf[x], sdot);
+                        dp = fmaf(go[k][x], vf[x], dp);
+                    }
+                    group_sum2<LH>(sdot, dp);
+                    const float p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
+                    const float pdp = p * dp;
+                    c[k] += pdp;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        A[k][x] = fmaf(pdp, kf[x], A[k][x]);
+                        B[k][x] = fmaf(p, kf[x], B[k][x]);
+                    }
+                }
+            }
+            st.release_step();
+        }
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
+#pragma unroll
+                for (int x = 0; x < EL; ++x) {
+                    A[k][x] += __shfl_xor_sync(SGA_FULL_MASK, A[k][x], off);
+                    B[k][x] += __shfl_xor_sync(SGA_FULL_MASK, B[k][x], off);
+                }
+            }
+        if (g == 0) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 const int ch = gl + G * k;
-                if (ch < R) {
-                    const size_t off = (size_t)it.row * R + ch;
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.Q) + off), q[k]);
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
-                    lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + ch / LH) * kLog2e;
+                if (ch >= R) continue;
+                const int h = ch / LH;
+                if (it.partial) {
+                    float4 *dA = reinterpret_cast<float4 *>(a.ws_row + (size_t)it.item * 2 * HD + ch * EL);
+                    float4 *dB = reinterpret_cast<float4 *>(a.ws_row + (size_t)it.item * 2 * HD + HD + ch * EL);
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4) {
+                        dA[x / 4] = make_float4(A[k][x], A[k][x + 1], A[k][x + 2], A[k][x + 3]);
+                        dB[x / 4] = make_float4(B[k][x], B[k][x + 1], B[k][x + 2], B[k][x + 3]);
+                    }
+                    if (ch % LH == 0) a.ws_rowc[(size_t)it.item * a.H + h] = c[k];
                 } else {
+                    const float dl = c[k] + (a.delta_in ? a.delta_in[(size_t)it.row * a.H + h] : 0.f);
+                    float o[EL];
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) q[k][x] = go[k][x] = 0.f;
-                    lse2[k] = 0.f;
-                }
-#pragma unroll
-                for (int x = 0; x < EL; ++x) A[k][x] = B[k][x] = 0.f;
-                c[k] = 0.f;
-            }
-            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-                const int cnt = min(32, it.end - e0);
-                const int32_t myj = batch_ids(a.indices, e0, cnt, it, id0, a.N, a.d_err);
-                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-                    uint4 kr[U][NC], vr[U][NC];
-                    bool ok[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int t = t0 + g + NG * u;
-                        const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
-                        ok[u] = (t < cnt) && (j >= 0);
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            const int ch = gl + G * k;
-                            if (ok[u] && ch < R) {
-                                kr[u][k] = ldg16_stream(Kc + (size_t)j * R + ch);
-                                vr[u][k] = ldg16_stream(Vc + (size_t)j * R + ch);
-                            } else {
-                                kr[u][k] = make_uint4(0, 0, 0, 0);
-                                vr[u][k] = make_uint4(0, 0, 0, 0);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < U; ++u)
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            float kf[EL], vf[EL];
-                            unpack<T>(kr[u][k], kf);
-                            unpack<T>(vr[u][k], vf);
-                            float sdot = 0.f, dp = 0.f;
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                sdot = fmaf(q[k][x], kf[x], sdot);
-                                dp = fmaf(go[k][x], vf[x], dp);
-                            }
-                            group_sum2<LH>(sdot, dp);
-                            const float p = ok[u] ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
-                            const float pdp = p * dp;
-                            c[k] += pdp;
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                A[k][x] = fmaf(pdp, kf[x], A[k][x]);
-                                B[k][x] = fmaf(p, kf[x], B[k][x]);
-                            }
-                        }
-                }
-            }
-#pragma unroll
-            for (int off = G; off < 32; off <<= 1)
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        A[k][x] += __shfl_xor_sync(SGA_FULL_MASK, A[k][x], off);
-                        B[k][x] += __shfl_xor_sync(SGA_FULL_MASK, B[k][x], off);
-                    }
-                }
-            if (g == 0) {
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int ch = gl + G * k;
-                    if (ch >= R) continue;
-                    const int h = ch / LH;
-                    if (it.partial) {
-                        float4 *dA = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * 2 * HD + ch * EL);
-                        float4 *dB = reinterpret_cast<float4 *>(a.ws_row + (size_t)item * 2 * HD + HD + ch * EL);
-#pragma unroll
-                        for (int x = 0; x < EL; x += 4) {
-                            dA[x / 4] = make_float4(A[k][x], A[k][x + 1], A[k][x + 2], A[k][x + 3]);
-                            dB[x / 4] = make_float4(B[k][x], B[k][x + 1], B[k][x + 2], B[k][x + 3]);
-                        }
-                        if (ch % LH == 0) a.ws_rowc[(size_t)item * a.H + h] = c[k];
-                    } else {
-                        const float dl = c[k] + (a.delta_in ? a.delta_in[(size_t)it.row * a.H + h] : 0.f);
-                        float o[EL];
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) o[x] = (A[k][x] - dl * B[k][x]) * scale;
-                        reinterpret_cast<uint4 *>(a.dQ)[(size_t)it.row * R + ch] = pack<T>(o);
-                        if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + h] = dl;
-                    }
+                    for (int x = 0; x < EL; ++x) o[x] = (A[k][x] - dl * B[k][x]) * scale;
+                    reinterpret_cast<uint4 *>(a.dQ)[(size_t)it.row * R + ch] = pack<T>(o);
+                    if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + h] = dl;
                 }
             }
         }
-        it = itn;
-        valid = validn;
-        id0 = id1;
-        mn = mnn;
+        st.finish_item();
     }
+    st.drain();
 }
 
 // ------------------------------------------------------- backward: dK, dV
@@ -561,131 +422,96 @@ template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
     using S = GtShape<T, D, NC, G>;
-    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    using C = GtDkdvStream<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, U = C::U;
+    extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
     const int R = a.H * D / EL, HD = a.H * D;
-    const uint4 *__restrict__ Qc = static_cast<const uint4 *>(a.Q);
-    const uint4 *__restrict__ Gc = static_cast<const uint4 *>(a.dOut);
-    const int64_t n_items = (int64_t)a.cols.n_chunks + a.N;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
-    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-
-    ItemMeta mn, mnn;
-    meta_issue(item, a.cols, a.t_indptr, a.N, mn);
-    ItemRange it;
-    bool valid = meta_eval(item, mn, a.cols, a.split_threshold, it);
-    int32_t id0 = first_ids(a.t_dst, it, valid);
-    meta_issue(item + stride, a.cols, a.t_indptr, a.N, mn);
-    for (; item < n_items; item += stride) {
-        meta_issue(item + 2 * stride, a.cols, a.t_indptr, a.N, mnn);
-        ItemRange itn;
-        const bool validn = meta_eval(item + stride, mn, a.cols, a.split_threshold, itn);
-        const int32_t id1 = first_ids(a.t_dst, itn, validn);
-        if (valid) {
-            float kj[NC][EL], vj[NC][EL], dk[NC][EL], dv[NC][EL];
+    StreamArrays arr{};
+    arr.rows[0] = static_cast<const uint4 *>(a.Q);
+    arr.rows[1] = static_cast<const uint4 *>(a.dOut);
+    arr.sc[0] = a.lse;
+    arr.sc[1] = a.ws_delta;
+    arr.own[0] = static_cast<const uint4 *>(a.K);
+    arr.own[1] = static_cast<const uint4 *>(a.V);
+    EdgeStream<C> st;
+    st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.cols, a.t_indptr, a.t_dst, a.N, a.H, R, LH,
+            a.split_threshold, a.d_err);
+    StreamItem it;
+    while (st.next_item(it)) {
+        float kj[NC][EL], vj[NC][EL], dk[NC][EL], dv[NC][EL];
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+#pragma unroll
+            for (int x = 0; x < EL; ++x) kj[k][x] = vj[k][x] = dk[k][x] = dv[k][x] = 0.f;
+        for (int step = 0; step < it.nsteps; ++step) {
+            st.wait_step();
+            if (step == 0)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    unpack<T>(st.own_row(0, k), kj[k]);
+                    unpack<T>(st.own_row(1, k), vj[k]);
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool ok = st.valid(u);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float qf[EL], gf[EL];
+                    unpack<T>(st.row(u, 0, k), qf);
+                    unpack<T>(st.row(u, 1, k), gf);
+                    float sdot = 0.f, dp = 0.f;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        sdot = fmaf(qf[x], kj[k][x], sdot);
+                        dp = fmaf(gf[x], vj[k][x], dp);
+                    }
+                    group_sum2<LH>(sdot, dp);
+                    const float p = ok ? exp2f(sdot * scale2 - st.scalar(u, 0, k) * kLog2e) : 0.f;
+                    const float ds = p * (dp - st.scalar(u, 1, k));
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) {
+                        dv[k][x] = fmaf(p, gf[x], dv[k][x]);
+                        dk[k][x] = fmaf(ds, qf[x], dk[k][x]);
+                    }
+                }
+            }
+            st.release_step();
+        }
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+            for (int k = 0; k < NC; ++k)
+#pragma unroll
+                for (int x = 0; x < EL; ++x) {
+                    dk[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dk[k][x], off);
+                    dv[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dv[k][x], off);
+                }
+        if (g == 0) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 const int c = gl + G * k;
-                if (c < R) {
-                    const size_t off = (size_t)it.row * R + c;
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.K) + off), kj[k]);
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.V) + off), vj[k]);
+                if (c >= R) continue;
+                if (it.partial) {
+                    float4 *dk_dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)it.item * 2 * HD + c * EL);
+                    float4 *dv_dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)it.item * 2 * HD + HD + c * EL);
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4) {
+                        dk_dst[x / 4] = make_float4(dk[k][x], dk[k][x + 1], dk[k][x + 2], dk[k][x + 3]);
+                        dv_dst[x / 4] = make_float4(dv[k][x], dv[k][x + 1], dv[k][x + 2], dv[k][x + 3]);
+                    }
                 } else {
+                    float o[EL];
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) kj[k][x] = vj[k][x] = 0.f;
-                }
-#pragma unroll
-                for (int x = 0; x < EL; ++x) dk[k][x] = dv[k][x] = 0.f;
-            }
-            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-                const int cnt = min(32, it.end - e0);
-                const int32_t myi = batch_ids(a.t_dst, e0, cnt, it, id0, a.N, a.d_err);
-                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-                    uint4 qr[U][NC], gr[U][NC];
-                    float l2[U][NC], dl[U][NC];
-                    bool ok[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int t = t0 + g + NG * u;
-                        const int32_t i = __shfl_sync(SGA_FULL_MASK, myi, t & 31);
-                        ok[u] = (t < cnt) && (i >= 0);
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            const int c = gl + G * k;
-                            if (ok[u] && c < R) {
-                                qr[u][k] = ldg16_stream(Qc + (size_t)i * R + c);
-                                gr[u][k] = ldg16_stream(Gc + (size_t)i * R + c);
-                                l2[u][k] = __ldg(a.lse + (size_t)i * a.H + c / LH);
-                                dl[u][k] = a.ws_delta[(size_t)i * a.H + c / LH];
-                            } else {
-                                qr[u][k] = make_uint4(0, 0, 0, 0);
-                                gr[u][k] = make_uint4(0, 0, 0, 0);
-                                l2[u][k] = 0.f;
-                                dl[u][k] = 0.f;
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < U; ++u)
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            float qf[EL], gf[EL];
-                            unpack<T>(qr[u][k], qf);
-                            unpack<T>(gr[u][k], gf);
-                            float sdot = 0.f, dp = 0.f;
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                sdot = fmaf(qf[x], kj[k][x], sdot);
-                                dp = fmaf(gf[x], vj[k][x], dp);
-                            }
-                            group_sum2<LH>(sdot, dp);
-                            const float p = ok[u] ? exp2f(sdot * scale2 - l2[u][k] * kLog2e) : 0.f;
-                            const float ds = p * (dp - dl[u][k]);
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                dv[k][x] = fmaf(p, gf[x], dv[k][x]);
-                                dk[k][x] = fmaf(ds, qf[x], dk[k][x]);
-                            }
-                        }
-                }
-            }
-#pragma unroll
-            for (int off = G; off < 32; off <<= 1)
-#pragma unroll
-                for (int k = 0; k < NC; ++k)
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        dk[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dk[k][x], off);
-                        dv[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dv[k][x], off);
-                    }
-            if (g == 0) {
-#pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    const int c = gl + G * k;
-                    if (c >= R) continue;
-                    if (it.partial) {
-                        float4 *dk_dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * 2 * HD + c * EL);
-                        float4 *dv_dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * 2 * HD + HD + c * EL);
-#pragma unroll
-                        for (int x = 0; x < EL; x += 4) {
-                            dk_dst[x / 4] = make_float4(dk[k][x], dk[k][x + 1], dk[k][x + 2], dk[k][x + 3]);
-                            dv_dst[x / 4] = make_float4(dv[k][x], dv[k][x + 1], dv[k][x + 2], dv[k][x + 3]);
-                        }
-                    } else {
-                        float o[EL];
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) o[x] = dk[k][x] * scale;
-                        reinterpret_cast<uint4 *>(a.dK)[(size_t)it.row * R + c] = pack<T>(o);
-                        reinterpret_cast<uint4 *>(a.dV)[(size_t)it.row * R + c] = pack<T>(dv[k]);
-                    }
+                    for (int x = 0; x < EL; ++x) o[x] = dk[k][x] * scale;
+                    reinterpret_cast<uint4 *>(a.dK)[(size_t)it.row * R + c] = pack<T>(o);
+                    reinterpret_cast<uint4 *>(a.dV)[(size_t)it.row * R + c] = pack<T>(dv[k]);
                 }
             }
         }
-        it = itn;
-        valid = validn;
-        id0 = id1;
-        mn = mnn;
+        st.finish_item();
     }
+    st.drain();
 }
 
 // Finish split rows, one block each.  which == 0: dQ rows (Delta = sum of
@@ -736,19 +562,38 @@ inline unsigned blocks_for_warps(int64_t warps) {
 
 // Grid of a persistent edge kernel: every block resident at once (occupancy
 // times the SM count), or fewer when there are fewer items than warps.
-template <auto Kernel> unsigned persistent_blocks(int64_t items) {
+template <auto Kernel> unsigned persistent_blocks(int64_t items, size_t smem = 0, int warps = kWarpsPerBlock) {
     static int per_sm = -1;   // one cache per kernel instantiation
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (per_sm < 0) {
+        if (smem > 48 * 1024)
+            cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         int nb = 1;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, Kernel, 256, 0) != cudaSuccess) nb = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, Kernel, warps * 32, smem) != cudaSuccess) nb = 1;
         per_sm = nb > 0 ? nb : 1;
     }
     const int64_t full = (int64_t)per_sm * (sms > 0 ? sms : 1);
-    const int64_t need = (items + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t need = (items + warps - 1) / warps;
     return (unsigned)(need < full ? (need > 0 ? need : 1) : full);
+}
+
+// Warps per block of a streamed kernel: eight, fewer when eight rings would
+// not fit the 227 KB of shared memory a block may use.
+template <typename C> constexpr int stream_warps() {
+    constexpr int fit = (227 * 1024) / C::BYTES;
+    return fit >= kWarpsPerBlock ? kWarpsPerBlock : (fit > 0 ? fit : 1);
+}
+
+// Launch a persistent streamed kernel over `items` work items.
+template <typename C, auto Kernel, typename... Args>
+cudaError_t launch_streamed(int64_t items, cudaStream_t s, Args... args) {
+    constexpr int warps = stream_warps<C>();
+    static_assert((size_t)C::BYTES * warps <= 227 * 1024, "one warp's ring must fit a block");
+    constexpr size_t smem = (size_t)C::BYTES * warps;
+    Kernel<<<persistent_blocks<Kernel>(items, smem, warps), warps * 32, smem, s>>>(args...);
+    return cudaGetLastError();
 }
 
 // Calls F.template operator()<NC, G>() for the edge-group shape of a row of
@@ -790,10 +635,9 @@ template <typename T, int D> cudaError_t gt_fwd_d(const GtArgs &a, cudaStream_t 
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
         note_launch(SGA_KERN_GT_FWD, s, false);
-        gt_fwd_kernel<T, D, NC, G>
-            <<<persistent_blocks<gt_fwd_kernel<T, D, NC, G>>(items), 256, 0, s>>>(a, scale2);
+        const cudaError_t e = launch_streamed<GtFwdStream<T, D, NC, G>, gt_fwd_kernel<T, D, NC, G>>(items, s, a, scale2);
         note_launch(SGA_KERN_GT_FWD, s, true);
-        return cudaGetLastError();
+        return e;
     });
     if (e != cudaSuccess || a.rows.n_split == 0) return e;
     note_launch(SGA_KERN_GT_FWD_MERGE, s, false);
@@ -812,10 +656,9 @@ template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t 
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
         if (items_r == 0) return cudaSuccess;
         note_launch(SGA_KERN_GT_BWD_DQ, s, false);
-        gt_bwd_dq_kernel<T, D, NC, G>
-            <<<persistent_blocks<gt_bwd_dq_kernel<T, D, NC, G>>(items_r), 256, 0, s>>>(a, scale2, scale);
+        cudaError_t e = launch_streamed<GtDqStream<T, D, NC, G>, gt_bwd_dq_kernel<T, D, NC, G>>(items_r, s, a,
+                                                                                            scale2, scale);
         note_launch(SGA_KERN_GT_BWD_DQ, s, true);
-        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         if (a.rows.n_split > 0) {   // Delta of split rows is needed by the dK/dV pass
             note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
@@ -824,10 +667,9 @@ template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t 
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         note_launch(SGA_KERN_GT_BWD_DKDV, s, false);
-        gt_bwd_dkdv_kernel<T, D, NC, G>
-            <<<persistent_blocks<gt_bwd_dkdv_kernel<T, D, NC, G>>(items_c), 256, 0, s>>>(a, scale2, scale);
+        e = launch_streamed<GtDkdvStream<T, D, NC, G>, gt_bwd_dkdv_kernel<T, D, NC, G>>(items_c, s, a, scale2, scale);
         note_launch(SGA_KERN_GT_BWD_DKDV, s, true);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess) return e;
         if (a.cols.n_split > 0) {
             note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
             gt_bwd_merge_kernel<T, D><<<(unsigned)a.cols.n_split, 256, 0, s>>>(a, scale, 1);

@@ -1,0 +1,329 @@
+// Edge stream: the gather side of the persistent edge kernels, decoupled from
+// their arithmetic by a per-warp ring in shared memory.
+//
+// A warp walks its work items (w, w + S, w + 2S, ...; S = warps in the grid).
+// An item is a whole row or one chunk of a split row; its edges are consumed
+// in steps of STEP = NG * U edges (U per edge group of G lanes, NG groups per
+// warp).  For every step the warp's "producer" copies, with cp.async, the
+// gathered rows of the step's neighbours (NROW arrays of R sixteen-byte
+// chunks per node; lane l of a group copies chunks l, l + G, ...) and their
+// per-head scalars (NSC arrays of [N, H] fp32) into a ring of DEPTH step
+// slots; the "consumer" (the same warp, later) computes on slot t while the
+// copies of steps t+1 .. t+DEPTH-1 are in flight.  An item's own rows (NOWN
+// arrays) and own scalars (NOSC) are copied when the item is queued, so the
+// next items' first loads overlap the tail of the current one.  Items wait in
+// a small queue (QD entries) in shared memory.
+//
+// Every lane reads back only the chunks it copied itself, so the ring needs no
+// block-level synchronisation; lane 0 writes the per-step validity masks and
+// queue entries, which the other lanes read after a __syncwarp.  Each step
+// records the commit group that carried it; the consumer waits for exactly
+// that group, so steps may lag groups (the producer commits an empty group
+// when it has nothing to issue) without breaking the pipeline.
+#pragma once
+
+#include "common.cuh"
+#include "items.cuh"
+#include "plan.h"
+
+namespace sga {
+
+__device__ __forceinline__ void cp16_async(uint32_t dst, const void *src, bool ok) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0));
+}
+__device__ __forceinline__ void cp4_async(uint32_t dst, const void *src, bool ok) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0));
+}
+__device__ __forceinline__ void cp_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Wait until at most n of this thread's most recent groups are pending.
+__device__ __forceinline__ void cp_wait_newer(int n) {
+    switch (n < 0 ? 0 : n) {
+        case 0: cp_wait_group<0>(); break;
+        case 1: cp_wait_group<1>(); break;
+        case 2: cp_wait_group<2>(); break;
+        case 3: cp_wait_group<3>(); break;
+        case 4: cp_wait_group<4>(); break;
+        case 5: cp_wait_group<5>(); break;
+        case 6: cp_wait_group<6>(); break;
+        default: cp_wait_group<7>(); break;
+    }
+}
+
+template <int NC_, int G_, int U_, int NROW_, int NSC_, int NOWN_, int NOSC_, int DEPTH_, int QD_>
+struct StreamCfg {
+    static constexpr int NC = NC_, G = G_, U = U_, NROW = NROW_, NSC = NSC_, NOWN = NOWN_,
+                         NOSC = NOSC_, DEPTH = DEPTH_, QD = QD_;
+    static constexpr int NG = 32 / G, STEP = NG * U;
+    static_assert(DEPTH >= 2 && DEPTH <= 8, "ring depth");
+    static_assert(QD >= 2, "queue depth");
+    static_assert(32 % STEP == 0, "a step must not straddle a batch of 32 ids");
+    // per-warp shared memory layout (bytes)
+    static constexpr int ROW_SLOT = U * NROW * NC * 32 * 16;
+    static constexpr int SC_SLOT = U * NSC * NC * 32 * 4;
+    static constexpr int OWN_SLOT = NOWN * NC * 32 * 16;
+    static constexpr int OSC_SLOT = NOSC * NC * 32 * 4;
+    static constexpr int OFF_ROW = 0;
+    static constexpr int OFF_OWN = OFF_ROW + DEPTH * ROW_SLOT;
+    static constexpr int OFF_SC = OFF_OWN + QD * OWN_SLOT;
+    static constexpr int OFF_OSC = OFF_SC + DEPTH * SC_SLOT;
+    static constexpr int OFF_MASK = OFF_OSC + QD * OSC_SLOT;      // [DEPTH][U] uint32
+    static constexpr int OFF_GRP = OFF_MASK + DEPTH * U * 4;       // [DEPTH] int32
+    static constexpr int OFF_Q = (OFF_GRP + DEPTH * 4 + 15) / 16 * 16;   // [QD] int4
+    static constexpr int BYTES = OFF_Q + QD * 16;
+    // 16-byte regions (cp.async 16, uint4 / int4 accesses) start on 16 bytes,
+    // 4-byte regions on 4 bytes; BYTES keeps every warp's base 16-aligned
+    static_assert(OFF_ROW % 16 == 0 && OFF_OWN % 16 == 0 && ROW_SLOT % 16 == 0 && OWN_SLOT % 16 == 0,
+                  "row slots must be 16-byte aligned");
+    static_assert(OFF_SC % 4 == 0 && OFF_OSC % 4 == 0 && OFF_MASK % 4 == 0 && OFF_GRP % 4 == 0,
+                  "scalar slots must be 4-byte aligned");
+    static_assert(OFF_Q % 16 == 0 && BYTES % 16 == 0, "queue entries and warp bases must be 16-byte aligned");
+};
+
+// One queued item, as the consumer sees it.
+struct StreamItem {
+    int32_t row;      // destination (or source) node
+    int32_t nsteps;   // steps of STEP edges; 0 for an empty row
+    int32_t item;     // work item index (chunk index when partial)
+    int32_t partial;  // 1: a chunk of a split row
+};
+
+struct StreamArrays {
+    const uint4 *rows[4];   // gathered node rows, [N][R] sixteen-byte chunks
+    const float *sc[2];     // gathered per-head scalars, [N][H]
+    const uint4 *own[2];    // the item's own rows
+    const float *osc[2];    // the item's own scalars
+};
+
+template <typename C> struct EdgeStream {
+    // fixed
+    unsigned char *sm;       // this warp's shared memory
+    uint32_t sa;             // its shared-space address
+    StreamArrays arr;
+    Partition P;
+    const int32_t *ptr, *ids;
+    int64_t N;
+    int H, R, LH, threshold;
+    int32_t *err;
+    int64_t stride, n_items;
+    int lane, g, gl;
+    // producer
+    int64_t nx_item;         // next item to consider
+    ItemMeta m1, m2;         // descriptors of nx_item and nx_item + stride
+    int32_t ids1;            // first id batch of nx_item (when valid)
+    bool v1;                 // nx_item is a valid item (its ids1 were issued)
+    ItemRange r1;
+    int32_t p_beg, p_deg, p_step, p_nsteps, p_ids, p_ids_nx;
+    int32_t p_issued, gc, q_tail;
+    bool p_done;
+    // consumer
+    int32_t c_step, q_head;
+
+    __device__ __forceinline__ void init(unsigned char *warp_smem, const StreamArrays &a, const Partition &part,
+                                         const int32_t *ptr_, const int32_t *ids_, int64_t N_, int H_, int R_,
+                                         int LH_, int threshold_, int32_t *err_) {
+        sm = warp_smem;
+        sa = (uint32_t)__cvta_generic_to_shared(warp_smem);
+        arr = a;
+        P = part;
+        ptr = ptr_;
+        ids = ids_;
+        N = N_;
+        H = H_;
+        R = R_;
+        LH = LH_;
+        threshold = threshold_;
+        err = err_;
+        lane = threadIdx.x & 31;
+        g = lane / C::G;
+        gl = lane % C::G;
+        stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+        n_items = (int64_t)P.n_chunks + N;
+        nx_item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        meta_issue(nx_item, P, ptr, N, m1);
+        meta_issue(nx_item + stride, P, ptr, N, m2);
+        v1 = meta_eval(nx_item, m1, P, threshold, r1);
+        ids1 = first_ids(ids, r1, v1);
+        p_beg = p_deg = p_step = p_nsteps = 0;
+        p_ids = p_ids_nx = -1;
+        p_issued = gc = q_tail = 0;
+        p_done = false;
+        c_step = q_head = 0;
+        for (int i = 0; i < C::DEPTH - 1; ++i) produce();
+    }
+
+    // ---- producer ----------------------------------------------------------
+
+    // Queue the next item to be processed here; false when there is none.
+    __device__ __forceinline__ bool advance_item() {
+        for (;;) {
+            if (nx_item >= n_items || m1.row < 0) {
+                p_done = true;
+                return false;
+            }
+            const bool valid = v1;
+            const ItemRange r = r1;
+            const int64_t cur = nx_item;
+            int32_t first = ids1;
+            // rotate the descriptor pipeline
+            nx_item += stride;
+            m1 = m2;
+            meta_issue(nx_item + stride, P, ptr, N, m2);
+            v1 = meta_eval(nx_item, m1, P, threshold, r1);
+            ids1 = first_ids(ids, r1, v1);
+            if (!valid) continue;   // a row above the split threshold: its chunks cover it
+            const int32_t deg = r.end - r.beg;
+            if (lane < deg && lane < 32) {
+                if ((uint32_t)first >= (uint32_t)N) {
+                    atomicOr(err, kErrIndexRange);
+                    first = -1;
+                }
+            } else {
+                first = -1;
+            }
+            p_beg = r.beg;
+            p_deg = deg;
+            p_step = 0;
+            p_nsteps = (deg + C::STEP - 1) / C::STEP;
+            p_ids = first;
+            p_ids_nx = deg > 32 ? load_ids(ids, r.beg + 32, min(32, deg - 32), N, err) : -1;
+            const int qs = q_tail % C::QD;
+            if (lane == 0) {
+                int4 e;
+                e.x = r.row;
+                e.y = p_nsteps;
+                e.z = (int32_t)cur;
+                e.w = r.partial ? 1 : 0;
+                *reinterpret_cast<int4 *>(sm + C::OFF_Q + qs * 16) = e;
+            }
+            // the item's own rows and scalars
+            if (p_nsteps > 0) {
+#pragma unroll
+                for (int o = 0; o < C::NOWN; ++o)
+#pragma unroll
+                    for (int k = 0; k < C::NC; ++k) {
+                        const int c = gl + C::G * k;
+                        const bool ok = c < R;
+                        cp16_async(sa + C::OFF_OWN + qs * C::OWN_SLOT + ((o * C::NC + k) * 32 + lane) * 16,
+                                   ok ? arr.own[o] + (size_t)r.row * R + c : arr.own[o], ok);
+                    }
+#pragma unroll
+                for (int o = 0; o < C::NOSC; ++o)
+#pragma unroll
+                    for (int k = 0; k < C::NC; ++k) {
+                        const int c = gl + C::G * k;
+                        const bool ok = c < R;
+                        cp4_async(sa + C::OFF_OSC + qs * C::OSC_SLOT + ((o * C::NC + k) * 32 + lane) * 4,
+                                  ok ? arr.osc[o] + (size_t)r.row * H + c / LH : arr.osc[o], ok);
+                    }
+            }
+            ++q_tail;
+            return true;
+        }
+    }
+
+    __device__ __forceinline__ void issue_step() {
+        const int slot = p_issued % C::DEPTH;
+        const int32_t e0 = p_step * C::STEP;   // item-local first edge of the step
+        if (p_step > 0 && (e0 & 31) == 0) {    // next batch of 32 ids
+            p_ids = p_ids_nx;
+            p_ids_nx = e0 + 32 < p_deg ? load_ids(ids, p_beg + e0 + 32, min(32, p_deg - e0 - 32), N, err) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < C::U; ++u) {
+            const int32_t e = e0 + g + C::NG * u;
+            const int32_t j = __shfl_sync(SGA_FULL_MASK, p_ids, e & 31);
+            const bool ok = e < p_deg && j >= 0;
+#pragma unroll
+            for (int r = 0; r < C::NROW; ++r)
+#pragma unroll
+                for (int k = 0; k < C::NC; ++k) {
+                    const int c = gl + C::G * k;
+                    const bool okc = ok && c < R;
+                    cp16_async(sa + C::OFF_ROW + slot * C::ROW_SLOT + (((u * C::NROW + r) * C::NC + k) * 32 + lane) * 16,
+                               okc ? arr.rows[r] + (size_t)j * R + c : arr.rows[r], okc);
+                }
+#pragma unroll
+            for (int s = 0; s < C::NSC; ++s)
+#pragma unroll
+                for (int k = 0; k < C::NC; ++k) {
+                    const int c = gl + C::G * k;
+                    const bool okc = ok && c < R;
+                    cp4_async(sa + C::OFF_SC + slot * C::SC_SLOT + (((u * C::NSC + s) * C::NC + k) * 32 + lane) * 4,
+                              okc ? arr.sc[s] + (size_t)j * H + c / LH : arr.sc[s], okc);
+                }
+            const unsigned m = __ballot_sync(SGA_FULL_MASK, ok);
+            if (lane == 0) reinterpret_cast<uint32_t *>(sm + C::OFF_MASK)[slot * C::U + u] = m;
+        }
+        if (lane == 0) reinterpret_cast<int32_t *>(sm + C::OFF_GRP)[slot] = gc;
+        ++p_step;
+        ++p_issued;
+    }
+
+    // Issue at most one step (queueing items as needed), then commit a group.
+    __device__ __forceinline__ void produce() {
+        if (!p_done) {
+            bool ready = p_step < p_nsteps;
+            while (!ready && q_tail - q_head < C::QD && advance_item()) ready = p_step < p_nsteps;
+            if (ready && p_issued - c_step < C::DEPTH) issue_step();
+        }
+        cp_commit_group();
+        ++gc;
+    }
+
+    // ---- consumer ----------------------------------------------------------
+
+    // The next item in order; false when the warp has no more.  (The producer
+    // runs DEPTH - 1 >= 1 steps ahead, so every item up to and including the
+    // one holding the next step is already queued.)
+    __device__ __forceinline__ bool next_item(StreamItem &it) {
+        __syncwarp();
+        while (q_head == q_tail && !p_done) produce();
+        __syncwarp();
+        if (q_head == q_tail) return false;
+        const int4 e = *reinterpret_cast<const int4 *>(sm + C::OFF_Q + (q_head % C::QD) * 16);
+        it.row = e.x;
+        it.nsteps = e.y;
+        it.item = e.z;
+        it.partial = e.w;
+        return true;
+    }
+    __device__ __forceinline__ void finish_item() { ++q_head; }
+
+    // Make the data of the next step (and the current item's own rows) visible.
+    __device__ __forceinline__ void wait_step() {
+        __syncwarp();
+        produce();
+        const int grp = reinterpret_cast<const int32_t *>(sm + C::OFF_GRP)[c_step % C::DEPTH];
+        cp_wait_newer(gc - 1 - grp);
+        __syncwarp();
+    }
+    __device__ __forceinline__ void release_step() { ++c_step; }
+
+    __device__ __forceinline__ bool valid(int u) const {
+        const uint32_t m = reinterpret_cast<const uint32_t *>(sm + C::OFF_MASK)[(c_step % C::DEPTH) * C::U + u];
+        return (m >> lane) & 1u;
+    }
+    __device__ __forceinline__ uint4 row(int u, int r, int k) const {
+        return *reinterpret_cast<const uint4 *>(
+            sm + C::OFF_ROW + (c_step % C::DEPTH) * C::ROW_SLOT + (((u * C::NROW + r) * C::NC + k) * 32 + lane) * 16);
+    }
+    __device__ __forceinline__ float scalar(int u, int s, int k) const {
+        return *reinterpret_cast<const float *>(
+            sm + C::OFF_SC + (c_step % C::DEPTH) * C::SC_SLOT + (((u * C::NSC + s) * C::NC + k) * 32 + lane) * 4);
+    }
+    __device__ __forceinline__ uint4 own_row(int o, int k) const {
+        return *reinterpret_cast<const uint4 *>(
+            sm + C::OFF_OWN + (q_head % C::QD) * C::OWN_SLOT + ((o * C::NC + k) * 32 + lane) * 16);
+    }
+    __device__ __forceinline__ float own_scalar(int o, int k) const {
+        return *reinterpret_cast<const float *>(
+            sm + C::OFF_OSC + (q_head % C::QD) * C::OSC_SLOT + ((o * C::NC + k) * 32 + lane) * 4);
+    }
+
+    __device__ __forceinline__ void drain() { cp_wait_group<0>(); }
+};
+
+}  // namespace sga
