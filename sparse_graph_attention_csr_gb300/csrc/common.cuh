@@ -102,6 +102,37 @@ template <int W> __device__ __forceinline__ void group_sum2(float &a, float &b) 
 }
 
 // exp2 that maps -inf to 0 without producing NaN for (-inf) - (-inf).
+// Two fp32 fused multiply-adds in one instruction (each lane rounded as fmaf).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+// sum_x a[x] b[x] over an even count, as two interleaved fma chains
+template <int EL> __device__ __forceinline__ float dot2(const float *a, const float *b) {
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int x = 0; x < EL; x += 2) s = ffma2(make_float2(a[x], a[x + 1]), make_float2(b[x], b[x + 1]), s);
+    return s.x + s.y;
+}
+// acc[x] += p x[x]
+template <int EL> __device__ __forceinline__ void axpy2(float *acc, float p, const float *x) {
+#pragma unroll
+    for (int i = 0; i < EL; i += 2) {
+        const float2 r = ffma2(make_float2(p, p), make_float2(x[i], x[i + 1]), make_float2(acc[i], acc[i + 1]));
+        acc[i] = r.x;
+        acc[i + 1] = r.y;
+    }
+}
+
+// Log2 growth of a row maximum that triggers a rescale of the accumulator
+// in the lazily rescaled online softmax.
+constexpr float kLazyLog2 = 8.0f;
+
 __device__ __forceinline__ float exp2_diff(float a, float m) {
     return (a == -INFINITY) ? 0.0f : exp2f(a - m);
 }

@@ -98,33 +98,33 @@ gt_fwd_kernel(GtArgs a, float scale2) {
                 for (int k = 0; k < NC; ++k) {
                     float kf[EL];
                     unpack<T>(st.row(u, 0, k), kf);
-                    float dot = 0.f;
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) dot = fmaf(q[k][x], kf[x], dot);
-                    dot = group_sum<LH>(dot);
+                    const float dot = group_sum<LH>(dot2<EL>(q[k], kf));
                     sc[u][k] = ok[u] ? dot * scale2 : -INFINITY;
                 }
             }
+            // online softmax with a lazily moved maximum: the accumulator is
+            // rescaled only when a score exceeds the running maximum by more
+            // than 2^kLazyLog2, so weights stay below 2^kLazyLog2
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
-                float mx = m[k];
+                float mx = sc[0][k];
 #pragma unroll
-                for (int u = 0; u < U; ++u) mx = fmaxf(mx, sc[u][k]);
-                if (mx == -INFINITY) continue;
-                const float alpha = exp2_diff(m[k], mx);
-                l[k] *= alpha;
+                for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[u][k]);
+                if (mx > m[k] + kLazyLog2) {
+                    const float alpha = exp2_diff(m[k], mx);
+                    l[k] *= alpha;
 #pragma unroll
-                for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
+                    for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
+                    m[k] = mx;
+                }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const float p = exp2_diff(sc[u][k], mx);
+                    const float p = exp2_diff(sc[u][k], m[k]);
                     l[k] += p;
                     float vf[EL];
                     unpack<T>(st.row(u, 1, k), vf);
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, vf[x], acc[k][x]);
+                    axpy2<EL>(acc[k], p, vf);
                 }
-                m[k] = mx;
             }
             st.release_step();
         }
@@ -343,7 +343,7 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                 for (int k = 0; k < NC; ++k) {
                     unpack<T>(st.own_row(0, k), q[k]);
                     unpack<T>(st.own_row(1, k), go[k]);
-                    lse2[k] = st.own_scalar(0, k) * kLog2e;
+                    lse2[k] = st.own_scalar(0, (gl + G * k) / LH) * kLog2e;
                 }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -353,21 +353,13 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                     float kf[EL], vf[EL];
                     unpack<T>(st.row(u, 0, k), kf);
                     unpack<T>(st.row(u, 1, k), vf);
-                    float sdot = 0.f, dp = 0.f;
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        sdot = fmaf(q[k][x], kf[x], sdot);
-                        dp = fmaf(go[k][x], vf[x], dp);
-                    }
+                    float sdot = dot2<EL>(q[k], kf), dp = dot2<EL>(go[k], vf);
                     group_sum2<LH>(sdot, dp);
                     const float p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
                     const float pdp = p * dp;
                     c[k] += pdp;
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        A[k][x] = fmaf(pdp, kf[x], A[k][x]);
-                        B[k][x] = fmaf(p, kf[x], B[k][x]);
-                    }
+                    axpy2<EL>(A[k], pdp, kf);
+                    axpy2<EL>(B[k], p, kf);
                 }
             }
             st.release_step();
@@ -460,20 +452,13 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
                     float qf[EL], gf[EL];
                     unpack<T>(st.row(u, 0, k), qf);
                     unpack<T>(st.row(u, 1, k), gf);
-                    float sdot = 0.f, dp = 0.f;
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        sdot = fmaf(qf[x], kj[k][x], sdot);
-                        dp = fmaf(gf[x], vj[k][x], dp);
-                    }
+                    float sdot = dot2<EL>(qf, kj[k]), dp = dot2<EL>(gf, vj[k]);
                     group_sum2<LH>(sdot, dp);
-                    const float p = ok ? exp2f(sdot * scale2 - st.scalar(u, 0, k) * kLog2e) : 0.f;
-                    const float ds = p * (dp - st.scalar(u, 1, k));
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        dv[k][x] = fmaf(p, gf[x], dv[k][x]);
-                        dk[k][x] = fmaf(ds, qf[x], dk[k][x]);
-                    }
+                    const int h = (gl + G * k) / LH;
+                    const float p = ok ? exp2f(sdot * scale2 - st.scalar(u, 0, h) * kLog2e) : 0.f;
+                    const float ds = p * (dp - st.scalar(u, 1, h));
+                    axpy2<EL>(dv[k], p, gf);
+                    axpy2<EL>(dk[k], ds, qf);
                 }
             }
             st.release_step();

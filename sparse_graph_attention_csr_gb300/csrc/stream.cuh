@@ -7,16 +7,18 @@
 // warp).  For every step the warp's "producer" copies, with cp.async, the
 // gathered rows of the step's neighbours (NROW arrays of R sixteen-byte
 // chunks per node; lane l of a group copies chunks l, l + G, ...) and their
-// per-head scalars (NSC arrays of [N, H] fp32) into a ring of DEPTH step
+// per-head scalars (NSC arrays of [N, H] fp32; lane h < H of a group copies
+// head h) into a ring of DEPTH step
 // slots; the "consumer" (the same warp, later) computes on slot t while the
 // copies of steps t+1 .. t+DEPTH-1 are in flight.  An item's own rows (NOWN
 // arrays) and own scalars (NOSC) are copied when the item is queued, so the
 // next items' first loads overlap the tail of the current one.  Items wait in
 // a small queue (QD entries) in shared memory.
 //
-// Every lane reads back only the chunks it copied itself, so the ring needs no
-// block-level synchronisation; lane 0 writes the per-step validity masks and
-// queue entries, which the other lanes read after a __syncwarp.  Each step
+// The ring is private to its warp: lanes read the chunks they copied
+// themselves and the per-head scalars of their own head; lane 0 writes the
+// per-step validity masks and queue entries.  All of it is read after the
+// wait and a __syncwarp.  Each step
 // records the commit group that carried it; the consumer waits for exactly
 // that group, so steps may lag groups (the producer commits an empty group
 // when it has nothing to issue) without breaking the pipeline.
@@ -62,9 +64,9 @@ struct StreamCfg {
     static_assert(32 % STEP == 0, "a step must not straddle a batch of 32 ids");
     // per-warp shared memory layout (bytes)
     static constexpr int ROW_SLOT = U * NROW * NC * 32 * 16;
-    static constexpr int SC_SLOT = U * NSC * NC * 32 * 4;
+    static constexpr int SC_SLOT = U * NSC * 32 * 4;     // [U][NSC][group g * G + head]
     static constexpr int OWN_SLOT = NOWN * NC * 32 * 16;
-    static constexpr int OSC_SLOT = NOSC * NC * 32 * 4;
+    static constexpr int OSC_SLOT = NOSC * 32 * 4;       // [NOSC][head]
     static constexpr int OFF_ROW = 0;
     static constexpr int OFF_OWN = OFF_ROW + DEPTH * ROW_SLOT;
     static constexpr int OFF_SC = OFF_OWN + QD * OWN_SLOT;
@@ -116,10 +118,10 @@ template <typename C> struct EdgeStream {
     bool v1;                 // nx_item is a valid item (its ids1 were issued)
     ItemRange r1;
     int32_t p_beg, p_deg, p_step, p_nsteps, p_ids, p_ids_nx;
-    int32_t p_issued, gc, q_tail;
+    int32_t p_issued, gc, q_tail, p_slot, q_tslot;
     bool p_done;
     // consumer
-    int32_t c_step, q_head;
+    int32_t c_step, q_head, c_slot, q_hslot;
 
     __device__ __forceinline__ void init(unsigned char *warp_smem, const StreamArrays &a, const Partition &part,
                                          const int32_t *ptr_, const int32_t *ids_, int64_t N_, int H_, int R_,
@@ -148,9 +150,9 @@ template <typename C> struct EdgeStream {
         ids1 = first_ids(ids, r1, v1);
         p_beg = p_deg = p_step = p_nsteps = 0;
         p_ids = p_ids_nx = -1;
-        p_issued = gc = q_tail = 0;
+        p_issued = gc = q_tail = p_slot = q_tslot = 0;
         p_done = false;
-        c_step = q_head = 0;
+        c_step = q_head = c_slot = q_hslot = 0;
         for (int i = 0; i < C::DEPTH - 1; ++i) produce();
     }
 
@@ -189,7 +191,7 @@ template <typename C> struct EdgeStream {
             p_nsteps = (deg + C::STEP - 1) / C::STEP;
             p_ids = first;
             p_ids_nx = deg > 32 ? load_ids(ids, r.beg + 32, min(32, deg - 32), N, err) : -1;
-            const int qs = q_tail % C::QD;
+            const int qs = q_tslot;
             if (lane == 0) {
                 int4 e;
                 e.x = r.row;
@@ -209,23 +211,20 @@ template <typename C> struct EdgeStream {
                         cp16_async(sa + C::OFF_OWN + qs * C::OWN_SLOT + ((o * C::NC + k) * 32 + lane) * 16,
                                    ok ? arr.own[o] + (size_t)r.row * R + c : arr.own[o], ok);
                     }
+                if (lane < H)
 #pragma unroll
-                for (int o = 0; o < C::NOSC; ++o)
-#pragma unroll
-                    for (int k = 0; k < C::NC; ++k) {
-                        const int c = gl + C::G * k;
-                        const bool ok = c < R;
-                        cp4_async(sa + C::OFF_OSC + qs * C::OSC_SLOT + ((o * C::NC + k) * 32 + lane) * 4,
-                                  ok ? arr.osc[o] + (size_t)r.row * H + c / LH : arr.osc[o], ok);
-                    }
+                    for (int o = 0; o < C::NOSC; ++o)
+                        cp4_async(sa + C::OFF_OSC + qs * C::OSC_SLOT + (o * 32 + lane) * 4,
+                                  arr.osc[o] + (size_t)r.row * H + lane, true);
             }
             ++q_tail;
+            q_tslot = q_tslot + 1 == C::QD ? 0 : q_tslot + 1;
             return true;
         }
     }
 
     __device__ __forceinline__ void issue_step() {
-        const int slot = p_issued % C::DEPTH;
+        const int slot = p_slot;
         const int32_t e0 = p_step * C::STEP;   // item-local first edge of the step
         if (p_step > 0 && (e0 & 31) == 0) {    // next batch of 32 ids
             p_ids = p_ids_nx;
@@ -245,21 +244,18 @@ template <typename C> struct EdgeStream {
                     cp16_async(sa + C::OFF_ROW + slot * C::ROW_SLOT + (((u * C::NROW + r) * C::NC + k) * 32 + lane) * 16,
                                okc ? arr.rows[r] + (size_t)j * R + c : arr.rows[r], okc);
                 }
+            if (gl < H)
 #pragma unroll
-            for (int s = 0; s < C::NSC; ++s)
-#pragma unroll
-                for (int k = 0; k < C::NC; ++k) {
-                    const int c = gl + C::G * k;
-                    const bool okc = ok && c < R;
-                    cp4_async(sa + C::OFF_SC + slot * C::SC_SLOT + (((u * C::NSC + s) * C::NC + k) * 32 + lane) * 4,
-                              okc ? arr.sc[s] + (size_t)j * H + c / LH : arr.sc[s], okc);
-                }
+                for (int s = 0; s < C::NSC; ++s)
+                    cp4_async(sa + C::OFF_SC + slot * C::SC_SLOT + ((u * C::NSC + s) * 32 + lane) * 4,
+                              ok ? arr.sc[s] + (size_t)j * H + gl : arr.sc[s], ok);
             const unsigned m = __ballot_sync(SGA_FULL_MASK, ok);
             if (lane == 0) reinterpret_cast<uint32_t *>(sm + C::OFF_MASK)[slot * C::U + u] = m;
         }
         if (lane == 0) reinterpret_cast<int32_t *>(sm + C::OFF_GRP)[slot] = gc;
         ++p_step;
         ++p_issued;
+        p_slot = p_slot + 1 == C::DEPTH ? 0 : p_slot + 1;
     }
 
     // Issue at most one step (queueing items as needed), then commit a group.
@@ -283,44 +279,53 @@ template <typename C> struct EdgeStream {
         while (q_head == q_tail && !p_done) produce();
         __syncwarp();
         if (q_head == q_tail) return false;
-        const int4 e = *reinterpret_cast<const int4 *>(sm + C::OFF_Q + (q_head % C::QD) * 16);
+        const int4 e = *reinterpret_cast<const int4 *>(sm + C::OFF_Q + q_hslot * 16);
         it.row = e.x;
         it.nsteps = e.y;
         it.item = e.z;
         it.partial = e.w;
         return true;
     }
-    __device__ __forceinline__ void finish_item() { ++q_head; }
+    __device__ __forceinline__ void finish_item() {
+        ++q_head;
+        q_hslot = q_hslot + 1 == C::QD ? 0 : q_hslot + 1;
+    }
 
     // Make the data of the next step (and the current item's own rows) visible.
     __device__ __forceinline__ void wait_step() {
         __syncwarp();
         produce();
-        const int grp = reinterpret_cast<const int32_t *>(sm + C::OFF_GRP)[c_step % C::DEPTH];
-        cp_wait_newer(gc - 1 - grp);
+        const int newer = gc - 1 - reinterpret_cast<const int32_t *>(sm + C::OFF_GRP)[c_slot];
+        if (newer >= C::DEPTH - 1) cp_wait_group<C::DEPTH - 1>();   // the steady state
+        else cp_wait_newer(newer);
         __syncwarp();
     }
-    __device__ __forceinline__ void release_step() { ++c_step; }
+    __device__ __forceinline__ void release_step() {
+        ++c_step;
+        c_slot = c_slot + 1 == C::DEPTH ? 0 : c_slot + 1;
+    }
 
     __device__ __forceinline__ bool valid(int u) const {
-        const uint32_t m = reinterpret_cast<const uint32_t *>(sm + C::OFF_MASK)[(c_step % C::DEPTH) * C::U + u];
+        const uint32_t m = reinterpret_cast<const uint32_t *>(sm + C::OFF_MASK)[c_slot * C::U + u];
         return (m >> lane) & 1u;
     }
     __device__ __forceinline__ uint4 row(int u, int r, int k) const {
         return *reinterpret_cast<const uint4 *>(
-            sm + C::OFF_ROW + (c_step % C::DEPTH) * C::ROW_SLOT + (((u * C::NROW + r) * C::NC + k) * 32 + lane) * 16);
+            sm + C::OFF_ROW + c_slot * C::ROW_SLOT + (((u * C::NROW + r) * C::NC + k) * 32 + lane) * 16);
     }
-    __device__ __forceinline__ float scalar(int u, int s, int k) const {
-        return *reinterpret_cast<const float *>(
-            sm + C::OFF_SC + (c_step % C::DEPTH) * C::SC_SLOT + (((u * C::NSC + s) * C::NC + k) * 32 + lane) * 4);
+    // scalar s of this lane's neighbour u, head h
+    __device__ __forceinline__ float scalar(int u, int s, int h) const {
+        // (lanes past the row's last head read a slot entry they never use)
+        return *reinterpret_cast<const float *>(sm + C::OFF_SC + c_slot * C::SC_SLOT +
+                                                ((u * C::NSC + s) * 32 + ((g * C::G + h) & 31)) * 4);
     }
     __device__ __forceinline__ uint4 own_row(int o, int k) const {
         return *reinterpret_cast<const uint4 *>(
-            sm + C::OFF_OWN + (q_head % C::QD) * C::OWN_SLOT + ((o * C::NC + k) * 32 + lane) * 16);
+            sm + C::OFF_OWN + q_hslot * C::OWN_SLOT + ((o * C::NC + k) * 32 + lane) * 16);
     }
-    __device__ __forceinline__ float own_scalar(int o, int k) const {
-        return *reinterpret_cast<const float *>(
-            sm + C::OFF_OSC + (q_head % C::QD) * C::OSC_SLOT + ((o * C::NC + k) * 32 + lane) * 4);
+    // own scalar o of the current item, head h
+    __device__ __forceinline__ float own_scalar(int o, int h) const {
+        return *reinterpret_cast<const float *>(sm + C::OFF_OSC + q_hslot * C::OSC_SLOT + (o * 32 + (h & 31)) * 4);
     }
 
     __device__ __forceinline__ void drain() { cp_wait_group<0>(); }
