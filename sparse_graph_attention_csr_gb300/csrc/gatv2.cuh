@@ -24,138 +24,134 @@ namespace sga {
 
 // --------------------------------------------------------------- edge fwd
 
+// gathered FR; own FL
+template <typename T, int D, int NC, int G> using Gatv2FwdStream = RingCfg<NC, G, 1, 0, 1, 0>;
+// gathered FR; own FL, dOut, lse
+template <typename T, int D, int NC, int G> using Gatv2DstStream = RingCfg<NC, G, 1, 0, 2, 1>;
+// gathered FL, dOut, lse, Delta (transposed CSR); own FR
+template <typename T, int D, int NC, int G> using Gatv2SrcStream = RingCfg<NC, G, 2, 2, 1, 0>;
+
+// LeakyReLU of fl + fr over one chunk, and its slope factor
+template <int EL>
+__device__ __forceinline__ void lrelu_chunk(const float *fl, const float *fr, float slope, float *lz, float *d) {
+#pragma unroll
+    for (int x = 0; x < EL; ++x) {
+        const float z = fl[x] + fr[x];
+        const bool pos = z > 0.f;
+        lz[x] = pos ? z : slope * z;
+        if (d) d[x] = pos ? 1.f : slope;
+    }
+}
+
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gatv2_fwd_kernel(Gatv2Args a) {
     using S = GtShape<T, D, NC, G>;
-    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    using C = Gatv2FwdStream<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, U = C::U;
+    extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
     const int R = a.H * D / EL, HD = a.H * D;
-    const uint4 *__restrict__ FRc = static_cast<const uint4 *>(a.FR);
     const float slope = a.slope;
-    const int64_t n_items = (int64_t)a.rows.n_chunks + a.N;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
-    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    ItemMeta mn, mnn;
-    meta_issue(item, a.rows, a.indptr, a.N, mn);
-    ItemRange it;
-    bool valid = meta_eval(item, mn, a.rows, a.split_threshold, it);
-    int32_t id0 = first_ids(a.indices, it, valid);
-    meta_issue(item + stride, a.rows, a.indptr, a.N, mn);
-    for (; item < n_items; item += stride) {
-        meta_issue(item + 2 * stride, a.rows, a.indptr, a.N, mnn);
-        ItemRange itn;
-        const bool validn = meta_eval(item + stride, mn, a.rows, a.split_threshold, itn);
-        const int32_t id1 = first_ids(a.indices, itn, validn);
-        if (valid) {
-
-            float fl[NC][EL], att[NC][EL], acc[NC][EL], m[NC], l[NC];
+    float att[NC][EL];   // a, in log2 units: scores come out in log2 units
 #pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                const int c = gl + G * k;
-                if (c < R) {
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + (size_t)it.row * R + c), fl[k]);
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
-                } else {
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c < R) unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
+        else
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) fl[k][x] = att[k][x] = 0.f;
-                }
+            for (int x = 0; x < EL; ++x) att[k][x] = 0.f;
 #pragma unroll
-                for (int x = 0; x < EL; ++x) {
-                    acc[k][x] = 0.f;
-                    att[k][x] *= kLog2e;   // scores directly in log2 units
-                }
-                m[k] = -INFINITY;
-                l[k] = 0.f;
-            }
-
-            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-                const int cnt = min(32, it.end - e0);
-                const int32_t myj = batch_ids(a.indices, e0, cnt, it, id0, a.N, a.d_err);
-                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-                    uint4 fr[U][NC];
-                    bool ok[U];
+        for (int x = 0; x < EL; ++x) att[k][x] *= kLog2e;
+    }
+    StreamArrays arr{};
+    arr.rows[0] = static_cast<const uint4 *>(a.FR);
+    arr.own[0] = static_cast<const uint4 *>(a.FL);
+    EdgeStream<C> st;
+    st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
+            a.split_threshold, a.d_err);
+    StreamItem it;
+    while (st.next_item(it)) {
+        float fl[NC][EL], acc[NC][EL], m[NC], l[NC];
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int t = t0 + g + NG * u;
-                        const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
-                        ok[u] = (t < cnt) && (j >= 0);
+        for (int k = 0; k < NC; ++k) {
 #pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            const int c = gl + G * k;
-                            fr[u][k] = (ok[u] && c < R) ? ldg16_stream(FRc + (size_t)j * R + c)
-                                                        : make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                    float s[U][NC];
+            for (int x = 0; x < EL; ++x) fl[k][x] = acc[k][x] = 0.f;
+            m[k] = -INFINITY;
+            l[k] = 0.f;
+        }
+        for (int step = 0; step < it.nsteps; ++step) {
+            st.wait_step();
+            if (step == 0)
 #pragma unroll
-                    for (int u = 0; u < U; ++u)
+                for (int k = 0; k < NC; ++k) unpack<T>(st.own_row(0, k), fl[k]);
+            float sc[U][NC];
 #pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            float f[EL];
-                            unpack<T>(fr[u][k], f);
-                            float e = 0.f;
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                const float z = fl[k][x] + f[x];
-                                e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
-                            }
-                            e = group_sum<LH>(e);
-                            s[u][k] = ok[u] ? e : -INFINITY;
-                        }
-#pragma unroll
-                    for (int k = 0; k < NC; ++k) {
-                        float mx = m[k];
-#pragma unroll
-                        for (int u = 0; u < U; ++u) mx = fmaxf(mx, s[u][k]);
-                        if (mx == -INFINITY) continue;
-                        const float alpha = exp2_diff(m[k], mx);
-                        l[k] *= alpha;
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
-#pragma unroll
-                        for (int u = 0; u < U; ++u) {
-                            const float p = exp2_diff(s[u][k], mx);
-                            l[k] += p;
-                            float f[EL];
-                            unpack<T>(fr[u][k], f);
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, f[x], acc[k][x]);
-                        }
-                        m[k] = mx;
-                    }
-                }
-            }
-#pragma unroll
-            for (int off = G; off < 32; off <<= 1)
+            for (int u = 0; u < U; ++u) {
+                const bool ok = st.valid(u);
 #pragma unroll
                 for (int k = 0; k < NC; ++k) {
-                    const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
-                    const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
-                    const float mx = fmaxf(m[k], mo);
-                    const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
-                    l[k] = l[k] * a1 + lo * a2;
+                    float f[EL], lz[EL];
+                    unpack<T>(st.row(u, 0, k), f);
+                    lrelu_chunk<EL>(fl[k], f, slope, lz, nullptr);
+                    const float e = group_sum<LH>(dot2<EL>(att[k], lz));
+                    sc[u][k] = ok ? e : -INFINITY;
+                }
+            }
+            // lazily rescaled online softmax (see the Graph Transformer forward)
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
-                        acc[k][x] = acc[k][x] * a1 + ao * a2;
-                    }
+            for (int k = 0; k < NC; ++k) {
+                float mx = sc[0][k];
+#pragma unroll
+                for (int u = 1; u < U; ++u) mx = fmaxf(mx, sc[u][k]);
+                if (mx > m[k] + kLazyLog2) {
+                    const float alpha = exp2_diff(m[k], mx);
+                    l[k] *= alpha;
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) acc[k][x] *= alpha;
                     m[k] = mx;
                 }
-            if (g == 0) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float p = exp2_diff(sc[u][k], m[k]);
+                    l[k] += p;
+                    float f[EL];
+                    unpack<T>(st.row(u, 0, k), f);
+                    axpy2<EL>(acc[k], p, f);
+                }
+            }
+            st.release_step();
+        }
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1)
+#pragma unroll
+            for (int k = 0; k < NC; ++k) {
+                const float mo = __shfl_xor_sync(SGA_FULL_MASK, m[k], off);
+                const float lo = __shfl_xor_sync(SGA_FULL_MASK, l[k], off);
+                const float mx = fmaxf(m[k], mo);
+                const float a1 = exp2_diff(m[k], mx), a2 = exp2_diff(mo, mx);
+                l[k] = l[k] * a1 + lo * a2;
+#pragma unroll
+                for (int x = 0; x < EL; ++x) {
+                    const float ao = __shfl_xor_sync(SGA_FULL_MASK, acc[k][x], off);
+                    acc[k][x] = acc[k][x] * a1 + ao * a2;
+                }
+                m[k] = mx;
+            }
+        if (g == 0) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 const int c = gl + G * k;
                 if (c >= R) continue;
                 const int h = c / LH;
                 if (it.partial) {
-                    float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)item * HD + c * EL);
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_acc + (size_t)it.item * HD + c * EL);
 #pragma unroll
                     for (int x = 0; x < EL; x += 4)
                         dst[x / 4] = make_float4(acc[k][x], acc[k][x + 1], acc[k][x + 2], acc[k][x + 3]);
                     if (c % LH == 0) {
-                        a.ws_ml[((size_t)item * a.H + h) * 2 + 0] = m[k];
-                        a.ws_ml[((size_t)item * a.H + h) * 2 + 1] = l[k];
+                        a.ws_ml[((size_t)it.item * a.H + h) * 2 + 0] = m[k];
+                        a.ws_ml[((size_t)it.item * a.H + h) * 2 + 1] = l[k];
                     }
                 } else {
                     const float inv = l[k] > 0.f ? 1.f / l[k] : 0.f;
@@ -168,14 +164,10 @@ gatv2_fwd_kernel(Gatv2Args a) {
                             l[k] > 0.f ? (m[k] + log2f(l[k])) * kLn2 : -INFINITY;
                 }
             }
-            }
-
         }
-        it = itn;
-        valid = validn;
-        id0 = id1;
-        mn = mnn;
+        st.finish_item();
     }
+    st.drain();
 }
 
 // ---------------------------------------------------- backward: dst pass
@@ -191,12 +183,13 @@ template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gatv2_bwd_dst_kernel(Gatv2Args a) {
     using S = GtShape<T, D, NC, G>;
-    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    using C = Gatv2DstStream<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, U = C::U;
     __shared__ float da_sh[1024];
+    extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
     const int R = a.H * D / EL, HD = a.H * D;
     const float slope = a.slope;
-    const uint4 *__restrict__ FRc = static_cast<const uint4 *>(a.FR);
 
     for (int x = threadIdx.x; x < HD; x += blockDim.x) da_sh[x] = 0.f;
 
@@ -211,162 +204,126 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
 #pragma unroll
         for (int x = 0; x < EL; ++x) dacc[k][x] = 0.f;
     }
-
-    const int64_t n_items = (int64_t)a.rows.n_chunks + a.N;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
-    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    ItemMeta mn, mnn;
-    meta_issue(item, a.rows, a.indptr, a.N, mn);
-    ItemRange it;
-    bool valid = meta_eval(item, mn, a.rows, a.split_threshold, it);
-    int32_t id0 = first_ids(a.indices, it, valid);
-    meta_issue(item + stride, a.rows, a.indptr, a.N, mn);
-    for (; item < n_items; item += stride) {
-        meta_issue(item + 2 * stride, a.rows, a.indptr, a.N, mnn);
-        ItemRange itn;
-        const bool validn = meta_eval(item + stride, mn, a.rows, a.split_threshold, itn);
-        const int32_t id1 = first_ids(a.indices, itn, validn);
-        if (valid) {
-            // fA/fB: dFL sums, gA/gB: da sums (A weighted by p dp, B by p), c: Delta part
-            float fl[NC][EL], go[NC][EL], fA[NC][EL], fB[NC][EL], gA[NC][EL], gB[NC][EL];
-            float c[NC], lse2[NC];
+    StreamArrays arr{};
+    arr.rows[0] = static_cast<const uint4 *>(a.FR);
+    arr.own[0] = static_cast<const uint4 *>(a.FL);
+    arr.own[1] = static_cast<const uint4 *>(a.dOut);
+    arr.osc[0] = a.lse;
+    EdgeStream<C> st;
+    st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
+            a.split_threshold, a.d_err);
+    StreamItem it;
+    while (st.next_item(it)) {
+        // fA/fB: dFL sums, gA/gB: da sums (A weighted by p dp, B by p), c: Delta part
+        float fl[NC][EL], go[NC][EL], fA[NC][EL], fB[NC][EL], gA[NC][EL], gB[NC][EL];
+        float c[NC], lse2[NC];
+#pragma unroll
+        for (int k = 0; k < NC; ++k) {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = fA[k][x] = fB[k][x] = gA[k][x] = gB[k][x] = 0.f;
+            c[k] = 0.f;
+            lse2[k] = 0.f;
+        }
+        for (int step = 0; step < it.nsteps; ++step) {
+            st.wait_step();
+            if (step == 0)
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    unpack<T>(st.own_row(0, k), fl[k]);
+                    unpack<T>(st.own_row(1, k), go[k]);
+                    lse2[k] = st.own_scalar(0, (gl + G * k) / LH) * kLog2e;
+                }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const bool ok = st.valid(u);
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    float f[EL], lz[EL], dz[EL];
+                    unpack<T>(st.row(u, 0, k), f);
+                    lrelu_chunk<EL>(fl[k], f, slope, lz, dz);
+                    float e = dot2<EL>(att[k], lz), dp = dot2<EL>(go[k], f);
+                    group_sum2<LH>(e, dp);
+                    const float p = ok ? exp2f(e * kLog2e - lse2[k]) : 0.f;
+                    const float pdp = p * dp;
+                    c[k] += pdp;
+                    float ag[EL];
+#pragma unroll
+                    for (int x = 0; x < EL; ++x) ag[x] = att[k][x] * dz[x];
+                    axpy2<EL>(fA[k], pdp, ag);
+                    axpy2<EL>(fB[k], p, ag);
+                    axpy2<EL>(gA[k], pdp, lz);
+                    axpy2<EL>(gB[k], p, lz);
+                }
+            }
+            st.release_step();
+        }
+        // Delta and the dFL sums over the whole warp (all edge groups)
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1)
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
-                const int ch = gl + G * k;
-                if (ch < R) {
-                    const size_t off = (size_t)it.row * R + ch;
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.FL) + off), fl[k]);
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.dOut) + off), go[k]);
-                    lse2[k] = __ldg(a.lse + (size_t)it.row * a.H + ch / LH) * kLog2e;
-                } else {
+                c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = 0.f;
-                    lse2[k] = 0.f;
-                }
-#pragma unroll
-                for (int x = 0; x < EL; ++x) fA[k][x] = fB[k][x] = gA[k][x] = gB[k][x] = 0.f;
-                c[k] = 0.f;
-            }
-            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-                const int cnt = min(32, it.end - e0);
-                const int32_t myj = batch_ids(a.indices, e0, cnt, it, id0, a.N, a.d_err);
-                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-                    uint4 fr[U][NC];
-                    bool ok[U];
-#pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int t = t0 + g + NG * u;
-                        const int32_t j = __shfl_sync(SGA_FULL_MASK, myj, t & 31);
-                        ok[u] = (t < cnt) && (j >= 0);
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            const int ch = gl + G * k;
-                            fr[u][k] = (ok[u] && ch < R) ? ldg16_stream(FRc + (size_t)j * R + ch)
-                                                         : make_uint4(0, 0, 0, 0);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < U; ++u)
-#pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            float f[EL];
-                            unpack<T>(fr[u][k], f);
-                            float e = 0.f, dp = 0.f;
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                const float z = fl[k][x] + f[x];
-                                e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
-                                dp = fmaf(go[k][x], f[x], dp);
-                            }
-                            group_sum2<LH>(e, dp);
-                            const float p = ok[u] ? exp2f(e * kLog2e - lse2[k]) : 0.f;
-                            const float pdp = p * dp;
-                            c[k] += pdp;
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                const float z = fl[k][x] + f[x];
-                                const bool pos = z > 0.f;
-                                const float ag = pos ? att[k][x] : slope * att[k][x];
-                                const float lz = pos ? z : slope * z;
-                                fA[k][x] = fmaf(pdp, ag, fA[k][x]);
-                                fB[k][x] = fmaf(p, ag, fB[k][x]);
-                                gA[k][x] = fmaf(pdp, lz, gA[k][x]);
-                                gB[k][x] = fmaf(p, lz, gB[k][x]);
-                            }
-                        }
+                for (int x = 0; x < EL; ++x) {
+                    fA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fA[k][x], off);
+                    fB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fB[k][x], off);
                 }
             }
-            // Delta and the dFL sums over the whole warp (all edge groups)
+        if (it.partial) {
+            // da sums of this chunk, combined over the groups, go to the merge kernel
 #pragma unroll
             for (int off = G; off < 32; off <<= 1)
 #pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) {
-                        fA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fA[k][x], off);
-                        fB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fB[k][x], off);
-                    }
-                }
-            if (it.partial) {
-                // da sums of this chunk, combined over the groups, go to the merge kernel
-#pragma unroll
-                for (int off = G; off < 32; off <<= 1)
-#pragma unroll
-                    for (int k = 0; k < NC; ++k)
-#pragma unroll
-                        for (int x = 0; x < EL; ++x) {
-                            gA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gA[k][x], off);
-                            gB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gB[k][x], off);
-                        }
-                if (g == 0) {
-#pragma unroll
-                    for (int k = 0; k < NC; ++k) {
-                        const int ch = gl + G * k;
-                        if (ch >= R) continue;
-                        float *base = a.ws_row + (size_t)item * 4 * HD + ch * EL;
-#pragma unroll
-                        for (int x = 0; x < EL; x += 4) {
-                            *reinterpret_cast<float4 *>(base + x) =
-                                make_float4(fA[k][x], fA[k][x + 1], fA[k][x + 2], fA[k][x + 3]);
-                            *reinterpret_cast<float4 *>(base + HD + x) =
-                                make_float4(fB[k][x], fB[k][x + 1], fB[k][x + 2], fB[k][x + 3]);
-                            *reinterpret_cast<float4 *>(base + 2 * HD + x) =
-                                make_float4(gA[k][x], gA[k][x + 1], gA[k][x + 2], gA[k][x + 3]);
-                            *reinterpret_cast<float4 *>(base + 3 * HD + x) =
-                                make_float4(gB[k][x], gB[k][x + 1], gB[k][x + 2], gB[k][x + 3]);
-                        }
-                        if (ch % LH == 0) a.ws_rowc[(size_t)item * a.H + ch / LH] = c[k];
-                    }
-                }
-            } else {
-#pragma unroll
                 for (int k = 0; k < NC; ++k)
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) dacc[k][x] += gA[k][x] - c[k] * gB[k][x];
-                if (g == 0) {
-#pragma unroll
-                    for (int k = 0; k < NC; ++k) {
-                        const int ch = gl + G * k;
-                        if (ch >= R) continue;
-                        float4 *dst = reinterpret_cast<float4 *>(a.ws_dfl + (size_t)it.row * HD + ch * EL);
-#pragma unroll
-                        for (int x = 0; x < EL; x += 4)
-                            dst[x / 4] = make_float4(fA[k][x] - c[k] * fB[k][x],
-                                                     fA[k][x + 1] - c[k] * fB[k][x + 1],
-                                                     fA[k][x + 2] - c[k] * fB[k][x + 2],
-                                                     fA[k][x + 3] - c[k] * fB[k][x + 3]);
-                        if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
+                    for (int x = 0; x < EL; ++x) {
+                        gA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gA[k][x], off);
+                        gB[k][x] += __shfl_xor_sync(SGA_FULL_MASK, gB[k][x], off);
                     }
+            if (g == 0) {
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int ch = gl + G * k;
+                    if (ch >= R) continue;
+                    float *base = a.ws_row + (size_t)it.item * 4 * HD + ch * EL;
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4) {
+                        *reinterpret_cast<float4 *>(base + x) =
+                            make_float4(fA[k][x], fA[k][x + 1], fA[k][x + 2], fA[k][x + 3]);
+                        *reinterpret_cast<float4 *>(base + HD + x) =
+                            make_float4(fB[k][x], fB[k][x + 1], fB[k][x + 2], fB[k][x + 3]);
+                        *reinterpret_cast<float4 *>(base + 2 * HD + x) =
+                            make_float4(gA[k][x], gA[k][x + 1], gA[k][x + 2], gA[k][x + 3]);
+                        *reinterpret_cast<float4 *>(base + 3 * HD + x) =
+                            make_float4(gB[k][x], gB[k][x + 1], gB[k][x + 2], gB[k][x + 3]);
+                    }
+                    if (ch % LH == 0) a.ws_rowc[(size_t)it.item * a.H + ch / LH] = c[k];
                 }
             }
-
+        } else {
+#pragma unroll
+            for (int k = 0; k < NC; ++k)
+#pragma unroll
+                for (int x = 0; x < EL; ++x) dacc[k][x] += gA[k][x] - c[k] * gB[k][x];
+            if (g == 0) {
+#pragma unroll
+                for (int k = 0; k < NC; ++k) {
+                    const int ch = gl + G * k;
+                    if (ch >= R) continue;
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_dfl + (size_t)it.row * HD + ch * EL);
+#pragma unroll
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(fA[k][x] - c[k] * fB[k][x],
+                                                 fA[k][x + 1] - c[k] * fB[k][x + 1],
+                                                 fA[k][x + 2] - c[k] * fB[k][x + 2],
+                                                 fA[k][x + 3] - c[k] * fB[k][x + 3]);
+                    if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
+                }
+            }
         }
-        it = itn;
-        valid = validn;
-        id0 = id1;
-        mn = mnn;
+        st.finish_item();
     }
+    st.drain();
     // da: groups -> lanes of group 0, warps -> shared memory in warp order
 #pragma unroll
     for (int off = G; off < 32; off <<= 1)
@@ -375,7 +332,7 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
 #pragma unroll
             for (int x = 0; x < EL; ++x) dacc[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dacc[k][x], off);
     __syncthreads();
-    for (int w = 0; w < kWarpsPerBlock; ++w) {
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
         if ((threadIdx.x >> 5) == w && g == 0) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
@@ -399,127 +356,86 @@ template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gatv2_bwd_src_kernel(Gatv2Args a) {
     using S = GtShape<T, D, NC, G>;
-    constexpr int EL = S::EL, LH = S::LH, NG = S::NG, U = S::U;
+    using C = Gatv2SrcStream<T, D, NC, G>;
+    constexpr int EL = S::EL, LH = S::LH, U = C::U;
+    extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
     const int R = a.H * D / EL, HD = a.H * D;
     const float slope = a.slope;
-    const uint4 *__restrict__ FLc = static_cast<const uint4 *>(a.FL);
-    const uint4 *__restrict__ Gc = static_cast<const uint4 *>(a.dOut);
-    const int64_t n_items = (int64_t)a.cols.n_chunks + a.N;
-    const int64_t stride = (int64_t)gridDim.x * kWarpsPerBlock;
-    int64_t item = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    ItemMeta mn, mnn;
-    meta_issue(item, a.cols, a.t_indptr, a.N, mn);
-    ItemRange it;
-    bool valid = meta_eval(item, mn, a.cols, a.split_threshold, it);
-    int32_t id0 = first_ids(a.t_dst, it, valid);
-    meta_issue(item + stride, a.cols, a.t_indptr, a.N, mn);
-    for (; item < n_items; item += stride) {
-        meta_issue(item + 2 * stride, a.cols, a.t_indptr, a.N, mnn);
-        ItemRange itn;
-        const bool validn = meta_eval(item + stride, mn, a.cols, a.split_threshold, itn);
-        const int32_t id1 = first_ids(a.t_dst, itn, validn);
-        if (valid) {
-
-            float frj[NC][EL], att[NC][EL], dfr[NC][EL];
+    float att[NC][EL];
 #pragma unroll
-            for (int k = 0; k < NC; ++k) {
-                const int c = gl + G * k;
-                if (c < R) {
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.FR) + (size_t)it.row * R + c), frj[k]);
-                    unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
-                } else {
+    for (int k = 0; k < NC; ++k) {
+        const int c = gl + G * k;
+        if (c < R) unpack<T>(ldg16(static_cast<const uint4 *>(a.a) + c), att[k]);
+        else
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) frj[k][x] = att[k][x] = 0.f;
-                }
+            for (int x = 0; x < EL; ++x) att[k][x] = 0.f;
+    }
+    StreamArrays arr{};
+    arr.rows[0] = static_cast<const uint4 *>(a.FL);
+    arr.rows[1] = static_cast<const uint4 *>(a.dOut);
+    arr.sc[0] = a.lse;
+    arr.sc[1] = a.ws_delta;
+    arr.own[0] = static_cast<const uint4 *>(a.FR);
+    EdgeStream<C> st;
+    st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.cols, a.t_indptr, a.t_dst, a.N, a.H, R, LH,
+            a.split_threshold, a.d_err);
+    StreamItem it;
+    while (st.next_item(it)) {
+        float frj[NC][EL], dfr[NC][EL];
 #pragma unroll
-                for (int x = 0; x < EL; ++x) dfr[k][x] = 0.f;
-            }
-            for (int32_t e0 = it.beg; e0 < it.end; e0 += 32) {
-                const int cnt = min(32, it.end - e0);
-                const int32_t myi = batch_ids(a.t_dst, e0, cnt, it, id0, a.N, a.d_err);
-                for (int t0 = 0; t0 < cnt; t0 += NG * U) {
-                    uint4 flr[U][NC], gr[U][NC];
-                    float l2[U][NC], dl[U][NC];
-                    bool ok[U];
+        for (int k = 0; k < NC; ++k)
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int t = t0 + g + NG * u;
-                        const int32_t i = __shfl_sync(SGA_FULL_MASK, myi, t & 31);
-                        ok[u] = (t < cnt) && (i >= 0);
+            for (int x = 0; x < EL; ++x) frj[k][x] = dfr[k][x] = 0.f;
+        for (int step = 0; step < it.nsteps; ++step) {
+            st.wait_step();
+            if (step == 0)
 #pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            const int c = gl + G * k;
-                            if (ok[u] && c < R) {
-                                flr[u][k] = ldg16_stream(FLc + (size_t)i * R + c);
-                                gr[u][k] = ldg16_stream(Gc + (size_t)i * R + c);
-                                l2[u][k] = __ldg(a.lse + (size_t)i * a.H + c / LH);
-                                dl[u][k] = a.ws_delta[(size_t)i * a.H + c / LH];
-                            } else {
-                                flr[u][k] = make_uint4(0, 0, 0, 0);
-                                gr[u][k] = make_uint4(0, 0, 0, 0);
-                                l2[u][k] = 0.f;
-                                dl[u][k] = 0.f;
-                            }
-                        }
-                    }
+                for (int k = 0; k < NC; ++k) unpack<T>(st.own_row(0, k), frj[k]);
 #pragma unroll
-                    for (int u = 0; u < U; ++u)
+            for (int u = 0; u < U; ++u) {
+                const bool ok = st.valid(u);
 #pragma unroll
-                        for (int k = 0; k < NC; ++k) {
-                            float f[EL], gf[EL];
-                            unpack<T>(flr[u][k], f);
-                            unpack<T>(gr[u][k], gf);
-                            float e = 0.f, dp = 0.f;
+                for (int k = 0; k < NC; ++k) {
+                    float f[EL], gf[EL], lz[EL], dz[EL];
+                    unpack<T>(st.row(u, 0, k), f);
+                    unpack<T>(st.row(u, 1, k), gf);
+                    lrelu_chunk<EL>(f, frj[k], slope, lz, dz);
+                    float e = dot2<EL>(att[k], lz), dp = dot2<EL>(gf, frj[k]);
+                    group_sum2<LH>(e, dp);
+                    const int h = (gl + G * k) / LH;
+                    const float p = ok ? exp2f((e - st.scalar(u, 0, h)) * kLog2e) : 0.f;
+                    const float de = p * (dp - st.scalar(u, 1, h));
+                    float w[EL];
 #pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                const float z = f[x] + frj[k][x];
-                                e = fmaf(att[k][x], z > 0.f ? z : slope * z, e);
-                                dp = fmaf(gf[x], frj[k][x], dp);
-                            }
-                            group_sum2<LH>(e, dp);
-                            const float p = ok[u] ? exp2f((e - l2[u][k]) * kLog2e) : 0.f;
-                            const float de = p * (dp - dl[u][k]);
-#pragma unroll
-                            for (int x = 0; x < EL; ++x) {
-                                const float z = f[x] + frj[k][x];
-                                dfr[k][x] = fmaf(p, gf[x], dfr[k][x]);
-                                dfr[k][x] = fmaf(de * att[k][x], z > 0.f ? 1.f : slope, dfr[k][x]);
-                            }
-                        }
+                    for (int x = 0; x < EL; ++x) w[x] = att[k][x] * dz[x];
+                    axpy2<EL>(dfr[k], p, gf);
+                    axpy2<EL>(dfr[k], de, w);
                 }
             }
+            st.release_step();
+        }
 #pragma unroll
-            for (int off = G; off < 32; off <<= 1)
+        for (int off = G; off < 32; off <<= 1)
 #pragma unroll
-                for (int k = 0; k < NC; ++k)
+            for (int k = 0; k < NC; ++k)
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) dfr[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dfr[k][x], off);
-            if (g == 0) {
+                for (int x = 0; x < EL; ++x) dfr[k][x] += __shfl_xor_sync(SGA_FULL_MASK, dfr[k][x], off);
+        if (g == 0) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 const int c = gl + G * k;
                 if (c >= R) continue;
-                if (it.partial) {
-                    float4 *dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)item * HD + c * EL);
+                float *base = it.partial ? a.ws_col + (size_t)it.item * HD : a.ws_dfr + (size_t)it.row * HD;
+                float4 *dst = reinterpret_cast<float4 *>(base + c * EL);
 #pragma unroll
-                    for (int x = 0; x < EL; x += 4)
-                        dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
-                } else {
-                    float4 *dst = reinterpret_cast<float4 *>(a.ws_dfr + (size_t)it.row * HD + c * EL);
-#pragma unroll
-                    for (int x = 0; x < EL; x += 4)
-                        dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
-                }
+                for (int x = 0; x < EL; x += 4)
+                    dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
             }
-            }
-
         }
-        it = itn;
-        valid = validn;
-        id0 = id1;
-        mn = mnn;
+        st.finish_item();
     }
+    st.drain();
 }
 
 // Finish split rows, one block each.  which == 0 (destination rows): Delta
@@ -752,10 +668,10 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
         note_launch(SGA_KERN_GATV2_FWD, s, false);
-        gatv2_fwd_kernel<T, D, NC, G>
-            <<<persistent_blocks<gatv2_fwd_kernel<T, D, NC, G>>(items), 256, 0, s>>>(b);
+        const cudaError_t e2 =
+            launch_streamed<Gatv2FwdStream<T, D, NC, G>, gatv2_fwd_kernel<T, D, NC, G>>(items, s, b);
         note_launch(SGA_KERN_GATV2_FWD, s, true);
-        return cudaGetLastError();
+        return e2;
     });
     if (e != cudaSuccess || a.rows.n_split == 0) return e;
     note_launch(SGA_KERN_GATV2_FWD_MERGE, s, false);
@@ -770,9 +686,10 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     const int HD = a.H * D;
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         note_launch(SGA_KERN_GATV2_BWD_DST, s, false);
-        gatv2_bwd_dst_kernel<T, D, NC, G><<<a.da_blocks, 256, 0, s>>>(a);
+        // one da partial per block: exactly da_blocks blocks
+        cudaError_t e2 = launch_streamed_grid<Gatv2DstStream<T, D, NC, G>, gatv2_bwd_dst_kernel<T, D, NC, G>,
+                                              4096>(a.da_blocks, s, a);
         note_launch(SGA_KERN_GATV2_BWD_DST, s, true);
-        cudaError_t e2 = cudaGetLastError();
         if (e2 != cudaSuccess) return e2;
         if (a.rows.n_split > 0) {   // Delta of split rows is needed by the source pass
             note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
@@ -783,10 +700,9 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
         if (items_c == 0) return cudaSuccess;
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, false);
-        gatv2_bwd_src_kernel<T, D, NC, G>
-            <<<persistent_blocks<gatv2_bwd_src_kernel<T, D, NC, G>>(items_c), 256, 0, s>>>(a);
+        e2 = launch_streamed<Gatv2SrcStream<T, D, NC, G>, gatv2_bwd_src_kernel<T, D, NC, G>>(items_c, s, a);
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, true);
-        if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
+        if (e2 != cudaSuccess) return e2;
         if (a.cols.n_split > 0) {
             note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
             gatv2_bwd_merge_kernel<T, D><<<(unsigned)a.cols.n_split, 256, 0, s>>>(a, 1);

@@ -564,10 +564,11 @@ template <auto Kernel> unsigned persistent_blocks(int64_t items, size_t smem = 0
     return (unsigned)(need < full ? (need > 0 ? need : 1) : full);
 }
 
-// Warps per block of a streamed kernel: eight, fewer when eight rings would
-// not fit the 227 KB of shared memory a block may use.
-template <typename C> constexpr int stream_warps() {
-    constexpr int fit = (227 * 1024) / C::BYTES;
+// Warps per block of a streamed kernel: eight, fewer when eight rings (and
+// the kernel's STATIC bytes of static shared memory) would not fit the 227 KB
+// a block may use.
+template <typename C, int STATIC = 0> constexpr int stream_warps() {
+    constexpr int fit = (227 * 1024 - STATIC) / C::BYTES;
     return fit >= kWarpsPerBlock ? kWarpsPerBlock : (fit > 0 ? fit : 1);
 }
 
@@ -578,6 +579,24 @@ cudaError_t launch_streamed(int64_t items, cudaStream_t s, Args... args) {
     static_assert((size_t)C::BYTES * warps <= 227 * 1024, "one warp's ring must fit a block");
     constexpr size_t smem = (size_t)C::BYTES * warps;
     Kernel<<<persistent_blocks<Kernel>(items, smem, warps), warps * 32, smem, s>>>(args...);
+    return cudaGetLastError();
+}
+
+// The same with a fixed grid (kernels that leave one partial per block).
+template <typename C, auto Kernel, int STATIC, typename... Args>
+cudaError_t launch_streamed_grid(unsigned grid, cudaStream_t s, Args... args) {
+    constexpr int warps = stream_warps<C, STATIC>();
+    static_assert((size_t)C::BYTES * warps + STATIC <= 227 * 1024, "one warp's ring must fit a block");
+    constexpr size_t smem = (size_t)C::BYTES * warps;
+    static bool configured = false;
+    if (!configured) {
+        if (smem > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        configured = true;
+    }
+    Kernel<<<grid, warps * 32, smem, s>>>(args...);
     return cudaGetLastError();
 }
 
