@@ -31,15 +31,25 @@ template <typename T, int D, int NC, int G> using Gatv2DstStream = RingCfg<NC, G
 // gathered FL, dOut, lse, Delta (transposed CSR); own FR
 template <typename T, int D, int NC, int G> using Gatv2SrcStream = RingCfg<NC, G, 2, 2, 1, 0>;
 
-// LeakyReLU of fl + fr over one chunk, and its slope factor
+// LeakyReLU of z = fl + fr over one chunk and its slope factor d (1 or
+// slope): lz = z d.
 template <int EL>
 __device__ __forceinline__ void lrelu_chunk(const float *fl, const float *fr, float slope, float *lz, float *d) {
 #pragma unroll
     for (int x = 0; x < EL; ++x) {
         const float z = fl[x] + fr[x];
-        const bool pos = z > 0.f;
-        lz[x] = pos ? z : slope * z;
-        if (d) d[x] = pos ? 1.f : slope;
+        d[x] = z > 0.f ? 1.f : slope;
+        lz[x] = z * d[x];
+    }
+}
+// LeakyReLU alone, as h z + k |z| with h = (1 + slope) / 2, k = (1 - slope) / 2
+// (fma-pipe arithmetic only; within an ulp of the select form).
+template <int EL>
+__device__ __forceinline__ void lrelu_fma(const float *fl, const float *fr, float h, float k, float *lz) {
+#pragma unroll
+    for (int x = 0; x < EL; ++x) {
+        const float z = fl[x] + fr[x];
+        lz[x] = fmaf(k, fabsf(z), h * z);
     }
 }
 
@@ -52,7 +62,7 @@ gatv2_fwd_kernel(Gatv2Args a) {
     extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
     const int R = a.H * D / EL, HD = a.H * D;
-    const float slope = a.slope;
+    const float lr_h = 0.5f * (1.f + a.slope), lr_k = 0.5f * (1.f - a.slope);
     float att[NC][EL];   // a, in log2 units: scores come out in log2 units
 #pragma unroll
     for (int k = 0; k < NC; ++k) {
@@ -93,7 +103,7 @@ gatv2_fwd_kernel(Gatv2Args a) {
                 for (int k = 0; k < NC; ++k) {
                     float f[EL], lz[EL];
                     unpack<T>(st.row(u, 0, k), f);
-                    lrelu_chunk<EL>(fl[k], f, slope, lz, nullptr);
+                    lrelu_fma<EL>(fl[k], f, lr_h, lr_k, lz);
                     const float e = group_sum<LH>(dot2<EL>(att[k], lz));
                     sc[u][k] = ok ? e : -INFINITY;
                 }
@@ -562,26 +572,42 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs<TA_, TB_, T, TA
     }
 }
 
-// dW_l, dW_r = sum of the slab partials [2][slab][F*HD] in slab order;
-// da = sum of the per-block partials in block order, then of the split rows'
-// contributions in split-row order.
+// dW_l, dW_r = sum of the slab partials [2][slab][F*HD]; da = sum of the
+// per-block partials followed by the split rows' contributions.  A block of
+// 32 outputs x 8 lanes of partials: lane group r adds partials r, r + 8, ...
+// in increasing order, then group 0 adds the eight sums in order, so the
+// result is independent of scheduling.
+constexpr int kRedOut = 32, kRedGroups = 8;
 template <typename T>
-__global__ void gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs, int64_t FHD,
-                                    T *dWl, T *dWr, const float *__restrict__ da_part, int blocks,
-                                    const float *__restrict__ da_split, int n_split, int HD, T *da) {
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(kRedOut * kRedGroups)
+gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs, int64_t FHD, T *dWl, T *dWr,
+                    const float *__restrict__ da_part, int blocks, const float *__restrict__ da_split,
+                    int n_split, int HD, T *da) {
+    __shared__ float sh[kRedGroups][kRedOut];
+    const int o = threadIdx.x % kRedOut, r = threadIdx.x / kRedOut;
+    const int64_t t = (int64_t)blockIdx.x * kRedOut + o;
+    float sum = 0.f;
     if (t < 2 * FHD) {
         const int which = (int)(t / FHD);
         const int64_t x = t % FHD;
-        float s = 0.f;
-        for (int k = 0; k < slabs; ++k) s += dw_part[((int64_t)which * slabs + k) * FHD + x];
-        (which ? dWr : dWl)[x] = from_f32<T>(s);
+        for (int k = r; k < slabs; k += kRedGroups) sum += dw_part[((int64_t)which * slabs + k) * FHD + x];
     } else if (t < 2 * FHD + HD) {
         const int x = (int)(t - 2 * FHD);
-        float s = 0.f;
-        for (int b = 0; b < blocks; ++b) s += da_part[(int64_t)b * HD + x];
-        for (int b = 0; b < n_split; ++b) s += da_split[(int64_t)b * HD + x];
-        da[x] = from_f32<T>(s);
+        for (int k = r; k < blocks + n_split; k += kRedGroups)
+            sum += k < blocks ? da_part[(int64_t)k * HD + x] : da_split[(int64_t)(k - blocks) * HD + x];
+    }
+    sh[r][o] = sum;
+    __syncthreads();
+    if (r == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int q = 0; q < kRedGroups; ++q) tot += sh[q][o];
+        if (t < 2 * FHD) {
+            const int which = (int)(t / FHD);
+            (which ? dWr : dWl)[t % FHD] = from_f32<T>(tot);
+        } else if (t < 2 * FHD + HD) {
+            da[t - 2 * FHD] = from_f32<T>(tot);
+        }
     }
 }
 
@@ -761,7 +787,7 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     }
     const int64_t total = 2 * FHD + HD;
     note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, false);
-    gatv2_reduce_kernel<T><<<(unsigned)((total + 255) / 256), 256, 0, s>>>(
+    gatv2_reduce_kernel<T><<<(unsigned)((total + kRedOut - 1) / kRedOut), kRedOut * kRedGroups, 0, s>>>(
         a.ws_dw, a.dw_slabs, FHD, static_cast<T *>(a.dWl), static_cast<T *>(a.dWr), a.ws_da,
         a.da_blocks, a.ws_da_split, a.rows.n_split, HD, static_cast<T *>(a.da));
     note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, true);

@@ -39,8 +39,9 @@ template <typename T, int D, int NC, int G> struct GtShape {
 // Stream shape of a kernel with NROW gathered row arrays: U neighbours per
 // group and step (1 when a lane holds two or more chunks of a row), and a ring
 // of about 10 KB per warp (2 to 8 steps).
-template <int NC, int NROW, int NSC = 0, int NOWN = 1, int NOSC = 0> struct RingDims {
-    static constexpr int U = NC >= 2 ? 1 : 2;
+template <int NC, int NROW, int NSC = 0, int NOWN = 1, int NOSC = 0, int G = 32> struct RingDims {
+    // edges per group and step: more when a row is short (several groups per warp)
+    static constexpr int U = NC >= 2 ? 1 : (G < 32 ? 4 : 2);
     static constexpr int STEP_BYTES = U * NC * 32 * (NROW * 16 + NSC * 4);
     static constexpr int OWN_BYTES = NC * 32 * (NOWN * 16 + NOSC * 4);
     static constexpr int QD = 3 * OWN_BYTES > 4096 ? 2 : 3;
@@ -48,8 +49,8 @@ template <int NC, int NROW, int NSC = 0, int NOWN = 1, int NOSC = 0> struct Ring
     static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
 };
 template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC>
-using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC>::U, NROW, NSC, NOWN, NOSC,
-                          RingDims<NC, NROW, NSC, NOWN, NOSC>::DEPTH, RingDims<NC, NROW, NSC, NOWN, NOSC>::QD>;
+using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G>::U, NROW, NSC, NOWN, NOSC,
+                          RingDims<NC, NROW, NSC, NOWN, NOSC, G>::DEPTH, RingDims<NC, NROW, NSC, NOWN, NOSC, G>::QD>;
 
 // gathered K, V; own Q
 template <typename T, int D, int NC, int G> using GtFwdStream = RingCfg<NC, G, 2, 0, 1, 0>;
