@@ -33,9 +33,11 @@ inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
 
 int da_blocks_for(int num_sms) { return std::max(1, num_sms * 2); }
-int dw_slabs_for(int64_t N) {
-    int64_t s = (N + 1023) / 1024;
-    return (int)std::min<int64_t>(std::max<int64_t>(s, 1), 256);
+// Split-K slabs of the weight-gradient GEMMs: at least 256 node rows each,
+// at most two per SM.
+int dw_slabs_for(int64_t N, int num_sms) {
+    const int64_t s = (N + 255) / 256;
+    return (int)std::min<int64_t>(std::max<int64_t>(s, 1), std::max(2 * num_sms, 1));
 }
 
 void compute_layout(sga_plan *p) {
@@ -55,7 +57,7 @@ void compute_layout(sga_plan *p) {
     L.bwd_col = take((size_t)p->cols.n_chunks * 2 * HD * 4);
     if (p->F > 0) {
         L.da_blocks = da_blocks_for(p->num_sms);
-        L.dw_slabs = dw_slabs_for(p->N);
+        L.dw_slabs = dw_slabs_for(p->N, p->num_sms);
         L.dfl = take((size_t)p->N * HD * 4);
         L.dfr = take((size_t)p->N * HD * 4);
         L.da_part = take((size_t)L.da_blocks * HD * 4);

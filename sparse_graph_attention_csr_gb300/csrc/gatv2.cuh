@@ -586,15 +586,36 @@ gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs, int64_t FHD, T
     __shared__ float sh[kRedGroups][kRedOut];
     const int o = threadIdx.x % kRedOut, r = threadIdx.x / kRedOut;
     const int64_t t = (int64_t)blockIdx.x * kRedOut + o;
+    // partials r, r + 8, r + 16, ... are fetched eight at a time (independent
+    // loads in flight) and added in increasing order
+    constexpr int kBatch = 8;
     float sum = 0.f;
     if (t < 2 * FHD) {
         const int which = (int)(t / FHD);
-        const int64_t x = t % FHD;
-        for (int k = r; k < slabs; k += kRedGroups) sum += dw_part[((int64_t)which * slabs + k) * FHD + x];
+        const float *base = dw_part + (int64_t)which * slabs * FHD + t % FHD;
+        for (int k0 = r; k0 < slabs; k0 += kRedGroups * kBatch) {
+            float v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int k = k0 + j * kRedGroups;
+                v[j] = k < slabs ? base[(int64_t)k * FHD] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) sum += v[j];
+        }
     } else if (t < 2 * FHD + HD) {
-        const int x = (int)(t - 2 * FHD);
-        for (int k = r; k < blocks + n_split; k += kRedGroups)
-            sum += k < blocks ? da_part[(int64_t)k * HD + x] : da_split[(int64_t)(k - blocks) * HD + x];
+        const int x = (int)(t - 2 * FHD), n = blocks + n_split;
+        for (int k0 = r; k0 < n; k0 += kRedGroups * kBatch) {
+            float v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int k = k0 + j * kRedGroups;
+                v[j] = k < blocks ? da_part[(int64_t)k * HD + x]
+                                  : (k < n ? da_split[(int64_t)(k - blocks) * HD + x] : 0.f);
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) sum += v[j];
+        }
     }
     sh[r][o] = sum;
     __syncthreads();

@@ -122,7 +122,7 @@ template <bool MAJ, int BX> struct TileMap {
 };
 
 template <typename TA, typename TB, typename TC, bool AM, bool BN_MAJOR, int MODE>
-__global__ void __launch_bounds__(mm::THREADS, 1)
+__global__ void __launch_bounds__(mm::THREADS, MODE == 0 ? 1 : 2)
 mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
     using namespace mm;
     constexpr bool SA = sizeof(TA) == 4, SB = sizeof(TB) == 4;   // fp32 operands split hi/lo
