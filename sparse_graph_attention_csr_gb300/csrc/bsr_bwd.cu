@@ -109,16 +109,21 @@ __device__ __forceinline__ void add_row_from_tmem(uint32_t taddr, __nv_bfloat16 
 
 // ------------------------------------------------------------ row passes
 
+// The Delta pass keeps one K/V buffer (the next group loads once the S and dP
+// products have consumed it), so that two of its CTAs share an SM; the dQ
+// pass, above half an SM's shared memory either way, keeps two.
+__host__ __device__ constexpr int row_buffers(int mode) { return mode == 0 ? 1 : 2; }
+
 struct RowLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
     uint32_t q, g, k[2], v[2], kt, ds, total;
     __host__ __device__ RowLayout(int D, int mode) {
-        const uint32_t DA = (uint32_t)D / 64;
+        const uint32_t DA = (uint32_t)D / 64, NB = (uint32_t)row_buffers(mode);
         q = 0;
         g = q + DA * 128 * 128;
         k[0] = g + DA * 128 * 128;
-        k[1] = k[0] + DA * kGroup * 128;
+        k[1] = k[0] + (NB - 1) * DA * kGroup * 128;
         v[0] = k[1] + DA * kGroup * 128;
-        v[1] = v[0] + DA * kGroup * 128;
+        v[1] = v[0] + (NB - 1) * DA * kGroup * 128;
         kt = v[1] + DA * kGroup * 128;
         ds = kt + (mode == 1 ? (uint32_t)D * 128 : 0);
         total = ds + (mode == 1 ? 128 * 128 : 0);
@@ -170,9 +175,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
     float dsum = 0.f;
     bool failed = false;
     int n_o = 0;   // dQ products issued (uniform over the CTA)
+    constexpr int NB = row_buffers(MODE);
     for (int g = 0; g < ng; ++g) {
-        const int b = g & 1;
-        if (g + 1 < ng) {
+        const int b = NB == 2 ? (g & 1) : 0;
+        if (NB == 2 && g + 1 < ng) {
             load_tile_rows<D>(sbase + L.k[b ^ 1], K, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
             load_tile_rows<D>(sbase + L.v[b ^ 1], V, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
             tc::cp_commit();
@@ -196,6 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
         if (!tc::mbar_wait(&mbar_s, g & 1, tc::kWaitLimit)) failed = true;
         if (__syncthreads_or(failed)) break;
         tc::fence_after_sync();
+        if (NB == 1 && g + 1 < ng) {   // K and V consumed: the next group loads during the softmax
+            load_tile_rows<D>(sbase + L.k[0], K, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
+            load_tile_rows<D>(sbase + L.v[0], V, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
+            tc::cp_commit();
+        }
 
         uint32_t bits[4];
 #pragma unroll

@@ -28,20 +28,21 @@ constexpr int kBsThreads = 128;
 constexpr int kGroup = 64;           // sources per group (four 16-wide tiles)
 constexpr float kLazy = 8.0f;        // log2 growth that triggers a rescale
 
+// One K/V buffer: the next group's rows load while the current group's
+// softmax and P V product run (the S product has consumed K, the transpose V),
+// which keeps a CTA under 100 KB so that two CTAs share an SM.
 struct BsLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t q, k[2], vn[2], vt, p, total;
+    uint32_t q, k, vn, vt, p, total;
     int vn_ld;      // bf16 elements per natural V row (D + 8: conflict-free ldmatrix)
     __host__ __device__ BsLayout(int D) {
         const int DA = (D + 63) / 64;
         vn_ld = D + 8;
         q = 0;
-        k[0] = q + (uint32_t)DA * 128 * 128;
-        k[1] = k[0] + (uint32_t)DA * kGroup * 128;
-        vt = k[1] + (uint32_t)DA * kGroup * 128;
+        k = q + (uint32_t)DA * 128 * 128;
+        vt = k + (uint32_t)DA * kGroup * 128;
         p = vt + (uint32_t)D * 128;
-        vn[0] = p + 128 * 128;
-        vn[1] = vn[0] + (uint32_t)kGroup * vn_ld * 2;
-        total = vn[1] + (uint32_t)kGroup * vn_ld * 2;
+        vn = p + 128 * 128;
+        total = vn + (uint32_t)kGroup * vn_ld * 2;
     }
 };
 
@@ -80,19 +81,19 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
         tc::cp16(sbase + L.q + tc::sw128_offset(rr, c * 8, 128),
                  ok ? Q + ((r0 + rr) * H + h) * D + c * 8 : Q, ok);
     }
-    auto load_group = [&](int g, int b) {
+    auto load_group = [&](int g) {
         for (int idx = tid; idx < kGroup * DC; idx += kBsThreads) {
             const int jr = idx / DC, c = idx % DC;
             const int32_t ti = t0 + 4 * g + jr / 16;
             const int64_t j = ti < t1 ? (int64_t)a.tile_col[ti] * 16 + (jr % 16) : -1;
             const bool ok = j >= 0 && j < a.N;
             const size_t off = ok ? ((size_t)j * H + h) * D + c * 8 : 0;
-            tc::cp16(sbase + L.k[b] + tc::sw128_offset(jr, c * 8, kGroup), K + off, ok);
-            tc::cp16(sbase + L.vn[b] + (uint32_t)(jr * L.vn_ld + c * 8) * 2, V + off, ok);
+            tc::cp16(sbase + L.k + tc::sw128_offset(jr, c * 8, kGroup), K + off, ok);
+            tc::cp16(sbase + L.vn + (uint32_t)(jr * L.vn_ld + c * 8) * 2, V + off, ok);
         }
         tc::cp_commit();
     };
-    load_group(0, 0);   // Q travels in the same first group
+    load_group(0);   // Q travels in the same first group
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tO = tmem_base, tS = tmem_base + D;
@@ -104,13 +105,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
     bool failed = false;
     int n_o = 0;   // P V products issued (uniform over the CTA)
     for (int g = 0; g < ng; ++g) {
-        const int b = g & 1;
-        if (g + 1 < ng) {
-            load_group(g + 1, b ^ 1);
-            tc::cp_wait<1>();
-        } else {
-            tc::cp_wait<0>();
-        }
+        tc::cp_wait<0>();   // this group's K and V rows
         // the previous P V product must be done before P, V^T and O are touched
         if (g > 0 && !tc::mbar_wait(&mbar_o, (g - 1) & 1, tc::kWaitLimit)) failed = true;
         if (__syncthreads_or(failed)) break;
@@ -120,7 +115,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
         for (int blk = warp; blk < (kGroup / 8) * (D / 8) / 4; blk += kBsThreads / 32) {
             const int jb = (blk * 4) / (D / 8), db0 = (blk * 4) % (D / 8);
             const int mi = lane >> 3, rr = lane & 7;
-            const uint32_t src = sbase + L.vn[b] + (uint32_t)((jb * 8 + rr) * L.vn_ld + (db0 + mi) * 8) * 2;
+            const uint32_t src = sbase + L.vn + (uint32_t)((jb * 8 + rr) * L.vn_ld + (db0 + mi) * 8) * 2;
             uint32_t v[4];
             tc::ldsm_x4_trans(v, src);
             const uint32_t dst = sbase + L.vt + tc::sw128_offset((db0 + mi) * 8 + rr, jb * 8, D);
@@ -133,7 +128,7 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t ao = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
                 const uint32_t bo = (uint32_t)((kk >> 2) * kGroup * 128 + (kk & 3) * 32);
-                tc::mma_bf16_ss(tS, tc::desc_sw128(sbase + L.q + ao), tc::desc_sw128(sbase + L.k[b] + bo),
+                tc::mma_bf16_ss(tS, tc::desc_sw128(sbase + L.q + ao), tc::desc_sw128(sbase + L.k + bo),
                                 idesc_s, kk > 0);
             }
             tc::mma_commit(&mbar_s);
@@ -141,6 +136,8 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
         if (!tc::mbar_wait(&mbar_s, g & 1, tc::kWaitLimit)) failed = true;
         if (__syncthreads_or(failed)) break;
         tc::fence_after_sync();
+        // K and V are consumed: the next group's rows load during the softmax
+        if (g + 1 < ng) load_group(g + 1);
 
         // masked, scaled scores of row r; lazy online softmax
         float s[kGroup];
