@@ -22,6 +22,30 @@
 
 namespace sga {
 
+// The projection gradients dFL, dFR are kept per node row in the workspace:
+// fp32 [N][HD] for fp32 layers; for bf16 layers a bf16 pair per value,
+// row = [hi(0..HD) | lo(0..HD)] with hi = bf16(x), lo = bf16(x - hi) (about 16
+// significant bits, the split the tensor-core GEMMs consume), the same 4
+// bytes per value.
+template <typename T, int EL>
+__device__ __forceinline__ void store_dF(float *ws, int64_t row, int HD, int c, const float *v) {
+    if constexpr (sizeof(T) == 4) {
+        float4 *dst = reinterpret_cast<float4 *>(ws + (size_t)row * HD + c * EL);
+#pragma unroll
+        for (int x = 0; x < EL; x += 4) dst[x / 4] = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+    } else {
+        float h[EL], l[EL];
+#pragma unroll
+        for (int x = 0; x < EL; ++x) {
+            h[x] = __bfloat162float(__float2bfloat16_rn(v[x]));
+            l[x] = v[x] - h[x];
+        }
+        __nv_bfloat16 *base = reinterpret_cast<__nv_bfloat16 *>(ws) + (size_t)row * 2 * HD + c * EL;
+        *reinterpret_cast<uint4 *>(base) = pack<__nv_bfloat16>(h);
+        *reinterpret_cast<uint4 *>(base + HD) = pack<__nv_bfloat16>(l);
+    }
+}
+
 // --------------------------------------------------------------- edge fwd
 
 // gathered FR; own FL
@@ -320,13 +344,10 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                 for (int k = 0; k < NC; ++k) {
                     const int ch = gl + G * k;
                     if (ch >= R) continue;
-                    float4 *dst = reinterpret_cast<float4 *>(a.ws_dfl + (size_t)it.row * HD + ch * EL);
+                    float v[EL];
 #pragma unroll
-                    for (int x = 0; x < EL; x += 4)
-                        dst[x / 4] = make_float4(fA[k][x] - c[k] * fB[k][x],
-                                                 fA[k][x + 1] - c[k] * fB[k][x + 1],
-                                                 fA[k][x + 2] - c[k] * fB[k][x + 2],
-                                                 fA[k][x + 3] - c[k] * fB[k][x + 3]);
+                    for (int x = 0; x < EL; ++x) v[x] = fA[k][x] - c[k] * fB[k][x];
+                    store_dF<T, EL>(a.ws_dfl, it.row, HD, ch, v);
                     if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
                 }
             }
@@ -436,11 +457,14 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
             for (int k = 0; k < NC; ++k) {
                 const int c = gl + G * k;
                 if (c >= R) continue;
-                float *base = it.partial ? a.ws_col + (size_t)it.item * HD : a.ws_dfr + (size_t)it.row * HD;
-                float4 *dst = reinterpret_cast<float4 *>(base + c * EL);
+                if (it.partial) {
+                    float4 *dst = reinterpret_cast<float4 *>(a.ws_col + (size_t)it.item * HD + c * EL);
 #pragma unroll
-                for (int x = 0; x < EL; x += 4)
-                    dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
+                    for (int x = 0; x < EL; x += 4)
+                        dst[x / 4] = make_float4(dfr[k][x], dfr[k][x + 1], dfr[k][x + 2], dfr[k][x + 3]);
+                } else {
+                    store_dF<T, EL>(a.ws_dfr, it.row, HD, c, dfr[k]);
+                }
             }
         }
         st.finish_item();
@@ -470,19 +494,19 @@ __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int w
             float sum[1][EL], unused;
             block_sum_chunks<EL, 1>(a.ws_col, 1, HD, nullptr, a.H, LH, c0, c1, c, c < R,
                                     reinterpret_cast<float (*)[1][32 * EL]>(sh), shc, sum, unused);
-            if (w == 0 && c < R)
-#pragma unroll
-                for (int x = 0; x < EL; ++x) a.ws_dfr[(size_t)row * HD + c * EL + x] = sum[0][x];
+            if (w == 0 && c < R) store_dF<T, EL>(a.ws_dfr, row, HD, c, sum[0]);
         } else {
             float sum[4][EL], delta;
             block_sum_chunks<EL, 4>(a.ws_row, 4, HD, a.ws_rowc, a.H, LH, c0, c1, c, c < R, sh, shc,
                                     sum, delta);
             if (w == 0 && c < R) {
+                float v[EL];
 #pragma unroll
                 for (int x = 0; x < EL; ++x) {
-                    a.ws_dfl[(size_t)row * HD + c * EL + x] = sum[0][x] - delta * sum[1][x];
+                    v[x] = sum[0][x] - delta * sum[1][x];
                     a.ws_da_split[(size_t)s * HD + c * EL + x] = sum[2][x] - delta * sum[3][x];
                 }
+                store_dF<T, EL>(a.ws_dfl, row, HD, c, v);
                 if (c % LH == 0) a.ws_delta[(size_t)row * a.H + c / LH] = delta;
             }
         }
@@ -764,12 +788,17 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     const int64_t FHD = (int64_t)a.F * HD;
     if (a.N > 0) {
         if constexpr (sizeof(T) == 2) {
-            MmaGemm<float, T, T, false, false, 1> g{};
-            g.A[0] = a.ws_dfl;
-            g.B[0] = static_cast<const T *>(a.Wl);
-            g.A[1] = a.ws_dfr;
-            g.B[1] = static_cast<const T *>(a.Wr);
-            g.pairs = 2;
+            // four bf16 pairs: dFL hi, dFL lo, dFR hi, dFR lo against W_l, W_l, W_r, W_r
+            MmaGemm<T, T, T, false, false, 1> g{};
+            const T *dfl = reinterpret_cast<const T *>(a.ws_dfl), *dfr = reinterpret_cast<const T *>(a.ws_dfr);
+            g.A[0] = dfl;
+            g.A[1] = dfl + HD;
+            g.A[2] = dfr;
+            g.A[3] = dfr + HD;
+            g.B[0] = g.B[1] = static_cast<const T *>(a.Wl);
+            g.B[2] = g.B[3] = static_cast<const T *>(a.Wr);
+            g.pairs = 4;
+            g.lda = 2 * HD;
             g.M = a.N; g.N = a.F; g.K = HD; g.k_per_slab = HD;
             g.C = static_cast<T *>(a.dX);
             if ((e = mma_gemm(g, 1, SGA_KERN_GATV2_BWD_DX, s)) != cudaSuccess) return e;
@@ -787,10 +816,13 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
         // dW = X^T dF over node slabs: fp32 partials [2][slab][F][HD]
         for (int w = 0; w < 2; ++w) {
             if constexpr (sizeof(T) == 2) {
-                MmaGemm<T, float, float, true, true, 2> g{};
-                g.A[0] = static_cast<const T *>(a.X);
-                g.B[0] = w ? a.ws_dfr : a.ws_dfl;
-                g.pairs = 1;
+                MmaGemm<T, T, float, true, true, 2> g{};   // X^T (dF hi) + X^T (dF lo)
+                const T *df = reinterpret_cast<const T *>(w ? a.ws_dfr : a.ws_dfl);
+                g.A[0] = g.A[1] = static_cast<const T *>(a.X);
+                g.B[0] = df;
+                g.B[1] = df + HD;
+                g.pairs = 2;
+                g.ldb = 2 * HD;
                 g.M = a.F; g.N = HD; g.K = a.N; g.k_per_slab = per;
                 g.Cpart = a.ws_dw + (size_t)w * FHD * a.dw_slabs;
                 if ((e = mma_gemm(g, a.dw_slabs, SGA_KERN_GATV2_BWD_DW, s)) != cudaSuccess) return e;

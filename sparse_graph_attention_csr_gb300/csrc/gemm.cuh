@@ -88,10 +88,11 @@ __device__ __forceinline__ void split8(const uint4 &u0, const uint4 &u1, uint4 &
 // Cpart[slab][M][N] over the K rows of slab blockIdx.z.
 template <typename TA, typename TB, typename TC, bool AM, bool BN_MAJOR, int MODE>
 struct MmaGemm {
-    const TA *A[2];
-    const TB *B[2];
-    int pairs;
+    const TA *A[4];
+    const TB *B[4];
+    int pairs;                // 1 .. 4
     int64_t M, N, K, k_per_slab;
+    int64_t lda, ldb;         // leading dimensions (elements); 0: packed (M or K, N or K)
     TC *C;
     float *Cpart;
     // MODE 0: elements whose rounding the fp32 sum leaves open are listed here
@@ -145,6 +146,7 @@ mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
     const int per_pair = k_hi > k_lo ? (int)((k_hi - k_lo + BK - 1) / BK) : 0;
     const int n_chunks = per_pair * g.pairs;
 
+    const int64_t lda = g.lda ? g.lda : (AM ? g.M : g.K), ldb = g.ldb ? g.ldb : (BN_MAJOR ? g.N : g.K);
     // global element (row-of-tile, col-of-tile) of chunk c of the current k chunk
     auto a_src = [&](int p, int64_t kb, int c, bool &ok) -> const TA * {
         int r, col;
@@ -152,7 +154,7 @@ mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
         int64_t gm, gk;
         if (AM) { gk = kb + r; gm = m0 + col; } else { gm = m0 + r; gk = kb + col; }
         ok = gm < g.M && gk < k_hi;
-        return ok ? g.A[p] + (AM ? gk * g.M + gm : gm * g.K + gk) : g.A[p];
+        return ok ? g.A[p] + (AM ? gk * lda + gm : gm * lda + gk) : g.A[p];
     };
     auto b_src = [&](int p, int64_t kb, int c, bool &ok) -> const TB * {
         int r, col;
@@ -160,7 +162,7 @@ mma_gemm_kernel(MmaGemm<TA, TB, TC, AM, BN_MAJOR, MODE> g) {
         int64_t gn, gk;
         if (BN_MAJOR) { gk = kb + r; gn = n0 + col; } else { gn = n0 + r; gk = kb + col; }
         ok = gn < g.N && gk < k_hi;
-        return ok ? g.B[p] + (BN_MAJOR ? gk * g.N + gn : gn * g.K + gk) : g.B[p];
+        return ok ? g.B[p] + (BN_MAJOR ? gk * ldb + gn : gn * ldb + gk) : g.B[p];
     };
     __nv_bfloat16 *stage_base[2] = {smem, smem + STAGE};
     // fp32 operand chunks held in registers between load and store
