@@ -18,6 +18,7 @@
 
 #include "gemm.cuh"
 #include "gt.cuh"
+#include "tc_dx.cuh"
 #include "tc_proj.cuh"
 
 namespace sga {
@@ -788,6 +789,22 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     const int64_t FHD = (int64_t)a.F * HD;
     if (a.N > 0) {
         if constexpr (sizeof(T) == 2) {
+          if (tc_dx_supported(a.F, HD, a.N)) {   // tcgen05 + TMA
+            TcDx t{};
+            t.dfl = reinterpret_cast<const __nv_bfloat16 *>(a.ws_dfl);
+            t.dfr = reinterpret_cast<const __nv_bfloat16 *>(a.ws_dfr);
+            t.Wl = static_cast<const __nv_bfloat16 *>(a.Wl);
+            t.Wr = static_cast<const __nv_bfloat16 *>(a.Wr);
+            t.dX = static_cast<__nv_bfloat16 *>(a.dX);
+            t.M = a.N;
+            t.F = a.F;
+            t.HD = HD;
+            t.err = a.d_err;
+            note_launch(SGA_KERN_GATV2_BWD_DX, s, false);
+            e = tc_dx(t, s);
+            note_launch(SGA_KERN_GATV2_BWD_DX, s, true);
+            if (e != cudaSuccess) return e;
+          } else {
             // four bf16 pairs: dFL hi, dFL lo, dFR hi, dFR lo against W_l, W_l, W_r, W_r
             MmaGemm<T, T, T, false, false, 1> g{};
             const T *dfl = reinterpret_cast<const T *>(a.ws_dfl), *dfr = reinterpret_cast<const T *>(a.ws_dfr);
@@ -802,6 +819,7 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
             g.M = a.N; g.N = a.F; g.K = HD; g.k_per_slab = HD;
             g.C = static_cast<T *>(a.dX);
             if ((e = mma_gemm(g, 1, SGA_KERN_GATV2_BWD_DX, s)) != cudaSuccess) return e;
+          }
         } else {
             GemmArgs<float, T, T, false, true> g{};
             g.A[0] = a.ws_dfl;

@@ -1,0 +1,34 @@
+// GATv2 input gradient dX = dFL W_l^T + dFR W_r^T on the tcgen05 tensor cores,
+// operands streamed by the Tensor Memory Accelerator.
+//
+// dFL and dFR are the workspace's bf16 (hi, lo) rows [M][2 HD] (hi then lo,
+// about 16 significant bits of the fp32 gradients); W_l, W_r are [F][HD] bf16.
+// With K running over [dFL hi | dFL lo | dFR hi | dFR lo] (4 HD) and the
+// weights repeated [W_l | W_l | W_r | W_r], dX is one K-major product
+// (M x F x 4 HD) per 128-row tile, accumulated in fp32 in TMEM and rounded to
+// bf16 once.
+#pragma once
+
+#include "common.cuh"
+
+namespace sga {
+
+struct TcDx {
+    const __nv_bfloat16 *dfl, *dfr;   // [M][2 HD]: hi row then lo row
+    const __nv_bfloat16 *Wl, *Wr;     // [F][HD]
+    __nv_bfloat16 *dX;                // [M][F]
+    int64_t M;
+    int F, HD;
+    int32_t *err;                     // device error word (timed-out waits)
+};
+
+// HD in {64, 128}; F a multiple of 32 in [32, 256] (one MMA's N; the epilogue
+// moves 32 accumulator columns at a time); M < 2^31.
+inline bool tc_dx_supported(int F, int HD, int64_t M) {
+    return (HD == 64 || HD == 128) && F % 32 == 0 && F >= 32 && F <= 256 && M < (int64_t(1) << 31);
+}
+
+// Launch on stream s (tc_dx.cu).
+cudaError_t tc_dx(const TcDx &p, cudaStream_t s);
+
+}  // namespace sga
