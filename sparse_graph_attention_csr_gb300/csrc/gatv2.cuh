@@ -786,6 +786,7 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     if (e != cudaSuccess) return e;
     // dX = dFL W_l^T + dFR W_r^T
     const int64_t per = (a.N + a.dw_slabs - 1) / a.dw_slabs;
+    int dw_slabs_used = 0;   // slabs the tensor-core dW wrote (0: the GEMM below wrote dw_slabs)
     const int64_t FHD = (int64_t)a.F * HD;
     if (a.N > 0) {
         if constexpr (sizeof(T) == 2) {
@@ -832,7 +833,31 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
             if ((e = gemm(g, 1, SGA_KERN_GATV2_BWD_DX, s)) != cudaSuccess) return e;
         }
         // dW = X^T dF over node slabs: fp32 partials [2][slab][F][HD]
-        for (int w = 0; w < 2; ++w) {
+        if constexpr (sizeof(T) == 2) {
+            if (tc_dw_supported(a.F, HD, a.N)) {   // tcgen05 + TMA, both matrices in one pass
+                int dev = 0, sms = 1;
+                cudaGetDevice(&dev);
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                TcDw t{};
+                t.X = static_cast<const __nv_bfloat16 *>(a.X);
+                t.dfl = reinterpret_cast<const __nv_bfloat16 *>(a.ws_dfl);
+                t.dfr = reinterpret_cast<const __nv_bfloat16 *>(a.ws_dfr);
+                t.part = a.ws_dw;
+                t.M = a.N;
+                t.F = a.F;
+                t.HD = HD;
+                t.slab_rows = dw_slab_rows(a.N, sms);
+                t.slabs = (int)((a.N + t.slab_rows - 1) / t.slab_rows);
+                t.err = a.d_err;
+                if (t.slabs > a.dw_slabs) return cudaErrorInvalidValue;   // the workspace holds dw_slabs
+                note_launch(SGA_KERN_GATV2_BWD_DW, s, false);
+                e = tc_dw(t, s);
+                note_launch(SGA_KERN_GATV2_BWD_DW, s, true);
+                if (e != cudaSuccess) return e;
+                dw_slabs_used = t.slabs;
+            }
+        }
+        for (int w = 0; w < 2 && dw_slabs_used == 0; ++w) {
             if constexpr (sizeof(T) == 2) {
                 MmaGemm<T, T, float, true, true, 2> g{};   // X^T (dF hi) + X^T (dF lo)
                 const T *df = reinterpret_cast<const T *>(w ? a.ws_dfr : a.ws_dfl);
@@ -859,7 +884,8 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     const int64_t total = 2 * FHD + HD;
     note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, false);
     gatv2_reduce_kernel<T><<<(unsigned)((total + kRedOut - 1) / kRedOut), kRedOut * kRedGroups, 0, s>>>(
-        a.ws_dw, a.dw_slabs, FHD, static_cast<T *>(a.dWl), static_cast<T *>(a.dWr), a.ws_da,
+        a.ws_dw, dw_slabs_used ? dw_slabs_used : a.dw_slabs, FHD, static_cast<T *>(a.dWl), static_cast<T *>(a.dWr),
+        a.ws_da,
         a.da_blocks, a.ws_da_split, a.rows.n_split, HD, static_cast<T *>(a.da));
     note_launch(SGA_KERN_GATV2_BWD_REDUCE, s, true);
     return cudaGetLastError();

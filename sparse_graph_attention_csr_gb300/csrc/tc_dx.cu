@@ -182,10 +182,151 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dx_kernel(const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------- dW
+
+constexpr int kDwThreads = 128;
+constexpr uint32_t kBox = 64 * 128;   // TMA box: 64 node rows x 64 bf16 (128 bytes)
+
+struct DwParams {
+    CUtensorMap tx;      // X as [M][F], box 64 x 64
+    CUtensorMap tf[2];   // dFL, dFR as [M][2 HD], box 64 x 64
+    float *part;
+    int64_t M;
+    int F, HD, slab_rows, slabs;
+    int32_t *err;
+};
+
+// Shared-memory descriptor of an MN-major operand made of 64-element MN
+// blocks (one TMA box each, `lbo` bytes apart) of 128-byte rows, one row per
+// k, 128-byte swizzle; 8-row K groups are 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3fff);
+    d |= (uint64_t)((lbo >> 4) & 0x3fff) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Per stage: X boxes (F / 64), then dF boxes ordered (w, hi/lo, h block).
+__host__ __device__ inline uint32_t dw_stage_bytes(int F, int HD) {
+    return (uint32_t)(F / 64 + 4 * (HD / 64)) * kBox;
+}
+// two stages, plus a pad that keeps every descriptor read inside the allocation
+__host__ __device__ inline size_t dw_smem(int F, int HD) { return 1024 + 2 * (size_t)dw_stage_bytes(F, HD) + 16384; }
+
+__global__ void __launch_bounds__(kDwThreads, 1) tc_dw_kernel(const __grid_constant__ DwParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t full[2], empty[2], done;
+    __shared__ uint32_t tmem_base;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int F = p.F, HD = p.HD, FB = F / 64, AS = HD / 64;
+    const uint32_t stage = dw_stage_bytes(F, HD), sbase = tc::smem_u32(smem);
+    const int64_t r0 = (int64_t)blockIdx.x * p.slab_rows;
+    const int64_t rows = min((int64_t)p.slab_rows, p.M - r0);
+    const int nchunks = rows > 0 ? (int)((rows + 63) / 64) : 0;
+    const uint32_t tcols = 2 * HD <= 128 ? 128 : 256;   // dW_l then dW_r accumulators, HD columns each
+
+    if (warp == 0) tc::tmem_alloc(&tmem_base, tcols);
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&full[b], 1);
+            tc::mbar_init(&empty[b], 1);
+        }
+        tc::mbar_init(&done, 1);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tbase = tmem_base;
+    bool failed = false;
+
+    if (warp == 0 && lane == 0) {   // ---------------- TMA producer
+        int c = 0;
+        for (; c < nchunks; ++c) {
+            const int s = c & 1, n = c >> 1;
+            if (n >= 1 && !tc::mbar_wait(&empty[s], (n - 1) & 1, tc::kWaitLimit)) {
+                failed = true;
+                break;
+            }
+            const int y = (int)(r0 + 64 * c);
+            const uint32_t st = sbase + (uint32_t)s * stage;
+            mbar_expect_tx(&full[s], stage);
+            for (int fb = 0; fb < FB; ++fb) tma_load_2d(st + fb * kBox, &p.tx, fb * 64, y, &full[s]);
+            for (int w = 0; w < 2; ++w)
+                for (int part = 0; part < 2; ++part)
+                    for (int a = 0; a < AS; ++a)
+                        tma_load_2d(st + (uint32_t)(FB + (w * 2 + part) * AS + a) * kBox, &p.tf[w], part * HD + a * 64,
+                                    y, &full[s]);
+        }
+        if (failed) atomicOr(p.err, tc::kErrMmaTimeout);
+        for (int i = c - 1; i >= 0 && i >= c - 2; --i)   // issued loads land before the CTA ends
+            tc::mbar_wait(&full[i & 1], (i >> 1) & 1, tc::kWaitLimit);
+    } else if (warp == 1 && lane == 0) {   // ---------------- MMA issuer
+        // M = F (A = X^T, MN-major), N = HD (B = dF^T, MN-major), K = 64 nodes per chunk
+        const uint32_t idesc = tc::idesc_bf16(128, HD) | (1u << 15) | (1u << 16);
+        for (int c = 0; c < nchunks; ++c) {
+            const int s = c & 1, n = c >> 1;
+            if (!tc::mbar_wait(&full[s], n & 1, tc::kWaitLimit)) {
+                failed = true;
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t st = sbase + (uint32_t)s * stage;
+            for (int w = 0; w < 2; ++w)
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t b0 = st + (uint32_t)(FB + (w * 2 + part) * AS) * kBox;
+                    for (int kk = 0; kk < 4; ++kk)   // 16 nodes = two 8-row K groups per step
+                        tc::mma_bf16_ss(tbase + (uint32_t)(w * HD), desc_mn_sw128(st + kk * 2048, kBox),
+                                        desc_mn_sw128(b0 + kk * 2048, kBox), idesc,
+                                        (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                }
+            tc::mma_commit(&empty[s]);
+        }
+        if (failed) atomicOr(p.err, tc::kErrMmaTimeout);
+        tc::mma_commit(&done);
+    }
+    // ---------------- epilogue (all four warps): TMEM lane f = row f of dW
+    const bool ok = nchunks == 0 || tc::mbar_wait(&done, 0, tc::kWaitLimit);
+    __syncwarp();   // warps 0 and 1 reconverge before the warp-collective TMEM loads
+    tc::fence_after_sync();
+    const int f = warp * 32 + lane;
+    for (int w = 0; w < 2; ++w)
+        for (int cb = 0; cb < HD; cb += 32) {
+            uint32_t v[32];
+            tc::tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + (uint32_t)(w * HD + cb), v);   // warp-collective
+            if (f < F && ok) {
+                float4 *dst = reinterpret_cast<float4 *>(
+                    p.part + (((size_t)w * p.slabs + blockIdx.x) * F + f) * HD + cb);
+                if (nchunks == 0) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                }
+            }
+        }
+    if (!ok && tid == 0) atomicOr(p.err, tc::kErrMmaTimeout);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_dealloc(tbase, tcols);
+    }
+}
+
 }  // namespace
 
-cudaError_t tc_dx(const TcDx &p, cudaStream_t s) {
-    if (p.M == 0) return cudaSuccess;
+namespace {
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+cudaError_t tmap_encoder(PFN_cuTensorMapEncodeTiled_v12000 &out) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     if (!encode) {
         void *fn = nullptr;
@@ -195,6 +336,31 @@ cudaError_t tc_dx(const TcDx &p, cudaStream_t s) {
         if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
         encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    out = encode;
+    return cudaSuccess;
+}
+
+// Row-major [rows][cols] bf16 matrix, boxes of box_cols x box_rows, 128-byte swizzle.
+cudaError_t bf16_map(CUtensorMap *m, const __nv_bfloat16 *base, int64_t rows, int64_t cols, int64_t row_elems,
+                     uint32_t box_cols, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    cudaError_t e = tmap_encoder(encode);
+    if (e != cudaSuccess) return e;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * sizeof(__nv_bfloat16)};
+    const cuuint32_t box[2] = {box_cols, box_rows}, estr[2] = {1, 1};
+    const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t tc_dx(const TcDx &p, cudaStream_t s) {
+    if (p.M == 0) return cudaSuccess;
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    if (cudaError_t e = tmap_encoder(encode); e != cudaSuccess) return e;
     DxParams dp{};
     const __nv_bfloat16 *src[2] = {p.dfl, p.dfr};
     for (int i = 0; i < 2; ++i) {
@@ -226,6 +392,31 @@ cudaError_t tc_dx(const TcDx &p, cudaStream_t s) {
     const int64_t tiles = (p.M + 127) / 128;
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
     tc_dx_kernel<<<grid, kThreads, smem, s>>>(dp);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_dw(const TcDw &p, cudaStream_t s) {
+    if (p.slabs == 0) return cudaSuccess;
+    DwParams dp{};
+    cudaError_t e = bf16_map(&dp.tx, p.X, p.M, p.F, p.F, 64, 64);
+    if (e == cudaSuccess) e = bf16_map(&dp.tf[0], p.dfl, p.M, 2 * p.HD, 2 * p.HD, 64, 64);
+    if (e == cudaSuccess) e = bf16_map(&dp.tf[1], p.dfr, p.M, 2 * p.HD, 2 * p.HD, 64, 64);
+    if (e != cudaSuccess) return e;
+    dp.part = p.part;
+    dp.M = p.M;
+    dp.F = p.F;
+    dp.HD = p.HD;
+    dp.slab_rows = p.slab_rows;
+    dp.slabs = p.slabs;
+    dp.err = p.err;
+    const size_t smem = dw_smem(p.F, p.HD);
+    static bool configured = false;
+    if (!configured) {
+        e = cudaFuncSetAttribute(tc_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    tc_dw_kernel<<<(unsigned)p.slabs, kDwThreads, smem, s>>>(dp);
     return cudaGetLastError();
 }
 

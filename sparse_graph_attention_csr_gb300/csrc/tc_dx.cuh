@@ -31,4 +31,34 @@ inline bool tc_dx_supported(int F, int HD, int64_t M) {
 // Launch on stream s (tc_dx.cu).
 cudaError_t tc_dx(const TcDx &p, cudaStream_t s);
 
+// Weight gradients dW_l = X^T dFL, dW_r = X^T dFR over node slabs: each CTA
+// takes slab_rows consecutive nodes (a multiple of 64) and writes fp32
+// partials part[w][slab][F][HD] (w = 0: dW_l, 1: dW_r), reduced afterwards in
+// slab order.  Both operands are node-major in memory; they are loaded by TMA
+// as 64 x 64 boxes and consumed as MN-major tcgen05 operands.
+struct TcDw {
+    const __nv_bfloat16 *X;            // [M][F]
+    const __nv_bfloat16 *dfl, *dfr;    // [M][2 HD]: hi row then lo row
+    float *part;                       // [2][slabs][F][HD]
+    int64_t M;
+    int F, HD;
+    int slab_rows, slabs;
+    int32_t *err;
+};
+
+// F == 128 (one MMA's M), HD in {64, 128}.
+inline bool tc_dw_supported(int F, int HD, int64_t M) {
+    return F == 128 && (HD == 64 || HD == 128) && M < (int64_t(1) << 31);
+}
+
+// Nodes per weight-gradient slab: a multiple of 64, at least 256, at most two
+// slabs per SM; slabs = ceil(M / rows).
+inline int dw_slab_rows(int64_t M, int num_sms) {
+    const int64_t per = (M + 2 * (int64_t)num_sms - 1) / (2 * (int64_t)num_sms);
+    const int64_t r = per < 256 ? 256 : per;
+    return (int)((r + 63) / 64 * 64);
+}
+
+cudaError_t tc_dw(const TcDw &p, cudaStream_t s);
+
 }  // namespace sga

@@ -75,7 +75,7 @@ def test_small_workload_matches_oracle():
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("F,H,D", [(128, 2, 64), (64, 1, 32), (40, 4, 32), (16, 1, 128),
-                                   (256, 8, 128), (48, 3, 32), (256, 1, 64), (32, 1, 128)])
+                                   (256, 8, 128), (48, 3, 32), (256, 1, 64), (32, 1, 128), (128, 1, 64)])
 def test_shapes_and_split_rows(dtype, F, H, D):
     rng = np.random.default_rng(F + H + D)
     indptr, indices = random_csr(rng, 400, 7, hubs=[(3, 300), (399, 90)])
