@@ -340,9 +340,10 @@ cudaError_t tmap_encoder(PFN_cuTensorMapEncodeTiled_v12000 &out) {
     return cudaSuccess;
 }
 
-// Row-major [rows][cols] bf16 matrix, boxes of box_cols x box_rows, 128-byte swizzle.
-cudaError_t bf16_map(CUtensorMap *m, const __nv_bfloat16 *base, int64_t rows, int64_t cols, int64_t row_elems,
-                     uint32_t box_cols, uint32_t box_rows) {
+}  // namespace
+
+cudaError_t bf16_tensor_map(CUtensorMap *m, const __nv_bfloat16 *base, int64_t rows, int64_t cols,
+                            int64_t row_elems, uint32_t box_cols, uint32_t box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     cudaError_t e = tmap_encoder(encode);
     if (e != cudaSuccess) return e;
@@ -354,8 +355,6 @@ cudaError_t bf16_map(CUtensorMap *m, const __nv_bfloat16 *base, int64_t rows, in
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
-
-}  // namespace
 
 cudaError_t tc_dx(const TcDx &p, cudaStream_t s) {
     if (p.M == 0) return cudaSuccess;
@@ -398,9 +397,9 @@ cudaError_t tc_dx(const TcDx &p, cudaStream_t s) {
 cudaError_t tc_dw(const TcDw &p, cudaStream_t s) {
     if (p.slabs == 0) return cudaSuccess;
     DwParams dp{};
-    cudaError_t e = bf16_map(&dp.tx, p.X, p.M, p.F, p.F, 64, 64);
-    if (e == cudaSuccess) e = bf16_map(&dp.tf[0], p.dfl, p.M, 2 * p.HD, 2 * p.HD, 64, 64);
-    if (e == cudaSuccess) e = bf16_map(&dp.tf[1], p.dfr, p.M, 2 * p.HD, 2 * p.HD, 64, 64);
+    cudaError_t e = bf16_tensor_map(&dp.tx, p.X, p.M, p.F, p.F, 64, 64);
+    if (e == cudaSuccess) e = bf16_tensor_map(&dp.tf[0], p.dfl, p.M, 2 * p.HD, 2 * p.HD, 64, 64);
+    if (e == cudaSuccess) e = bf16_tensor_map(&dp.tf[1], p.dfr, p.M, 2 * p.HD, 2 * p.HD, 64, 64);
     if (e != cudaSuccess) return e;
     dp.part = p.part;
     dp.M = p.M;

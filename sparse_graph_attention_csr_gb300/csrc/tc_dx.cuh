@@ -9,6 +9,8 @@
 // bf16 once.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace sga {
@@ -60,5 +62,11 @@ inline int dw_slab_rows(int64_t M, int num_sms) {
 }
 
 cudaError_t tc_dw(const TcDw &p, cudaStream_t s);
+
+// TMA descriptor of a row-major [rows][cols] bf16 matrix with rows of
+// row_elems elements, boxes of box_cols x box_rows, 128-byte swizzle (the
+// K-major tile layout of tc.cuh), out-of-range elements read as zero.
+cudaError_t bf16_tensor_map(CUtensorMap *m, const __nv_bfloat16 *base, int64_t rows, int64_t cols,
+                            int64_t row_elems, uint32_t box_cols, uint32_t box_rows);
 
 }  // namespace sga

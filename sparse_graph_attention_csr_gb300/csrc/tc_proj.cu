@@ -1,252 +1,318 @@
-// tcgen05 kernel of the GATv2 projections (declared in tc_proj.cuh).
+// tcgen05 + TMA kernel of the GATv2 projections (declared in tc_proj.cuh).
+//
+// Persistent CTAs over 128-row tiles of X, warp-specialised:
+//   warp 0, one lane: TMA loads of a tile's X rows (K/64 atoms of 128 rows x
+//     64 bf16, 128-byte swizzle) into one of nslot slots ("sfull");
+//   warp 1, one lane: the tile's MMAs (128 x 2HD x 16) into one of two TMEM
+//     accumulators ("tfull");
+//   warps 2-17: the epilogue.  Warp w reads TMEM lanes 32 (w mod 4) .. (tile
+//     rows) and every fourth 32-column chunk, checks whether each fp32 value's
+//     bf16 rounding is settled (bound 2 * 2^-24 |x||w| + ulp), stores FL/FR,
+//     frees the accumulator ("tempty"), then recomputes the flagged elements
+//     exactly from the slot's X rows and the staged weights (half-warp per
+//     element, TwoSum) and frees the slot ("sempty").
+// The weights [W_l | W_r] are transposed into the K-major operand once per
+// CTA.  Every mbarrier wait is bounded; the epilogue warps take their
+// timeout decision together (barrier reduction), so none is left at a named
+// barrier.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gemm.cuh"
 #include "tc.cuh"
+#include "tc_dx.cuh"
 #include "tc_proj.cuh"
 
 namespace sga {
+namespace {
 
-// Warps: 4 lane quarters (TMEM lanes 32q .. 32q+31 = tile rows) times
-// NT / 64 column groups of 64 accumulator columns each.
-constexpr int kTpMaxThreads = 512;
+constexpr int kEpiWarps = 16, kEpiThreads = 32 * kEpiWarps, kThreads = 64 + kEpiThreads;
+constexpr int kColGroups = kEpiWarps / 4;   // epilogue warps per TMEM lane quarter
 constexpr int kTpFix = 1024;
+constexpr uint32_t kAtom = 128 * 128;   // 128 rows x 64 bf16
 
-// A tiles in flight: three when they fit (the next tile's MMA and the load of
-// the one after run during an epilogue), else two.
-__host__ __device__ inline int tc_proj_abufs(int K, int HD) {
-    const int KA = (K + 63) / 64;
-    return 1024 + (size_t)KA * 2 * HD * 128 + 3 * (size_t)KA * 128 * 128 <= 227 * 1024 ? 3 : 2;
+struct ProjParams {
+    CUtensorMap tx;   // X as [M][K] bf16, box 64 x 128
+    const __nv_bfloat16 *Wl, *Wr;
+    __nv_bfloat16 *FL, *FR;
+    int64_t M;
+    int K, HD, nslot;
+    int32_t *err;
+};
+
+__host__ __device__ inline size_t proj_b_bytes(int K, int HD) { return (size_t)((K + 63) / 64) * 2 * HD * 128; }
+// X slots in flight: three when they fit, else two
+__host__ __device__ inline int proj_slots(int K, int HD) {
+    const size_t slot = (size_t)((K + 63) / 64) * kAtom;
+    return 1024 + proj_b_bytes(K, HD) + 3 * slot <= 227 * 1024 ? 3 : 2;
 }
-__host__ __device__ inline size_t tc_proj_smem(int K, int HD) {
-    const int KA = (K + 63) / 64;
-    return 1024 + (size_t)KA * 2 * HD * 128 + tc_proj_abufs(K, HD) * (size_t)KA * 128 * 128;
+__host__ __device__ inline size_t proj_smem(int K, int HD) {
+    return 1024 + proj_b_bytes(K, HD) + (size_t)proj_slots(K, HD) * ((K + 63) / 64) * kAtom;
 }
 
-__device__ __forceinline__ float bf16_at(const unsigned char *tile, int row, int k, int R) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + tc::sw128_offset(row, k, R)));
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(mbar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(mbar)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_u32(mbar))
+        : "memory");
+}
+// Named barrier 1 over the epilogue warps.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kEpiThreads) : "memory"); }
+// The same barrier, returning whether any epilogue thread passed `flag`.
+__device__ __forceinline__ bool epi_any(bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r) : "r"((uint32_t)flag), "n"(kEpiThreads) : "memory");
+    return r != 0;
 }
 
-// Squared Euclidean norm of row `row` of a swizzled K-major tile (16-byte reads).
-__device__ __forceinline__ float row_sq(const unsigned char *tile, int row, int K, int R) {
+__device__ __forceinline__ float bf16_at(uint32_t tile, int row, int k, int R) {
+    __nv_bfloat16 v;
+    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(*reinterpret_cast<unsigned short *>(&v))
+                 : "r"(tile + tc::sw128_offset(row, k, R)));
+    return __bfloat162float(v);
+}
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+    uint4 u;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "r"(addr));
+    return u;
+}
+// Squared Euclidean norm of row `row` of a swizzled K-major tile of R rows.
+__device__ __forceinline__ float row_sq(uint32_t tile, int row, int K, int R) {
     float q = 0.f;
     for (int c = 0; c < K / 8; ++c) {
-        const uint4 u = *reinterpret_cast<const uint4 *>(tile + tc::sw128_offset(row, c * 8, R));
         float x[8];
-        unpack<__nv_bfloat16>(u, x);
+        unpack<__nv_bfloat16>(lds16(tile + tc::sw128_offset(row, c * 8, R)), x);
 #pragma unroll
         for (int i = 0; i < 8; ++i) q = fmaf(x[i], x[i], q);
     }
     return q;
 }
 
-__global__ void __launch_bounds__(kTpMaxThreads, 1) tc_proj_kernel(TcProj p) {
+__global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_constant__ ProjParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ float cnorm[256], rnorm[128];
-    __shared__ uint64_t mbar[2];   // MMA completion per TMEM accumulator
+    __shared__ float cnorm[256];
+    __shared__ uint64_t sfull[3], sempty[3], tfull[2], tempty[2], done;
     __shared__ uint32_t tmem_base;
     __shared__ int2 fixl[kTpFix];
     __shared__ int fix_n;
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
-    const int K = p.K, HD = p.HD, NT = 2 * HD, KA = (K + 63) / 64, KC = K / 8;
-    const int quarter = warp & 3, cgroup = warp >> 2;   // rows 32*quarter.., columns 64*cgroup..
-    const int NBUF = tc_proj_abufs(K, HD);
-    unsigned char *Bs = smem;
-    unsigned char *As[3];
-    for (int b = 0; b < 3; ++b) As[b] = Bs + (size_t)KA * NT * 128 + (size_t)(b < NBUF ? b : 0) * KA * 16384;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = p.K, HD = p.HD, NT = 2 * HD, KA = (K + 63) / 64, KC = K / 8, NS = p.nslot;
+    const uint32_t sB = tc::smem_u32(smem), sX = sB + (uint32_t)proj_b_bytes(K, HD), slot_bytes = KA * kAtom;
     const int64_t n_tiles = (p.M + 127) / 128;
-    const uint32_t idesc = tc::idesc_bf16(128, NT);
-    const uint32_t tcols = NT > 128 ? 512 : 256;   // two accumulators of NT columns
+    const uint32_t tcols = NT > 128 ? 512 : (NT > 64 ? 256 : 128);   // two accumulators of NT columns
 
     if (warp == 0) tc::tmem_alloc(&tmem_base, tcols);
     if (tid == 0) {
-        tc::mbar_init(&mbar[0], 1);
-        tc::mbar_init(&mbar[1], 1);
+        for (int s = 0; s < 3; ++s) {
+            tc::mbar_init(&sfull[s], 1);
+            tc::mbar_init(&sempty[s], kEpiThreads);
+        }
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&tfull[b], 1);
+            tc::mbar_init(&tempty[b], kEpiThreads);
+        }
+        tc::mbar_init(&done, 1);
         fix_n = 0;
     }
-    // B = [W_l | W_r]^T, K-major swizzled: row n = output column (loads of
-    // several iterations in flight before their stores)
+    // B = [W_l | W_r]^T, K-major swizzled: row n = output column
 #pragma unroll 4
-    for (int idx = tid; idx < K * (NT / 8); idx += nthr) {
+    for (int idx = tid; idx < K * (NT / 8); idx += kThreads) {
         const int k = idx / (NT / 8), n0 = (idx % (NT / 8)) * 8;
         const __nv_bfloat16 *W = n0 < HD ? p.Wl : p.Wr;
         const uint4 u = ldg16(W + (size_t)k * HD + (n0 % HD));
         const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&u);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            *reinterpret_cast<__nv_bfloat16 *>(Bs + tc::sw128_offset(n0 + i, k, NT)) = e[i];
+            *reinterpret_cast<__nv_bfloat16 *>(smem + tc::sw128_offset(n0 + i, k, NT)) = e[i];
     }
-    auto load_a = [&](int64_t tile, int st) {
-        const int64_t m0 = tile * 128;
-        const uint32_t base = tc::smem_u32(As[st]);
-        for (int idx = tid; idx < 128 * KC; idx += nthr) {
-            const int r = idx / KC, c = idx % KC;
-            const bool ok = m0 + r < p.M;
-            tc::cp16(base + tc::sw128_offset(r, c * 8, 128), ok ? p.X + (m0 + r) * K + c * 8 : p.X, ok);
-        }
-        tc::cp_commit();
-    };
-    const int64_t stride = gridDim.x;
-    const int64_t tile0 = blockIdx.x;
-    // tiles of this CTA: tile0, tile0 + stride, ...; A of tile j sits in buffer j % NBUF
-    if (tile0 < n_tiles) load_a(tile0, 0);
-    if (tile0 + stride < n_tiles) load_a(tile0 + stride, 1 % NBUF);
-    else tc::cp_commit();
     __syncthreads();
-    for (int n = tid; n < NT; n += nthr) cnorm[n] = sqrtf(row_sq(Bs, n, K, NT));   // column norms of W
+    for (int n = tid; n < NT; n += kThreads) cnorm[n] = sqrtf(row_sq(sB, n, K, NT));   // column norms of W
+    tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tbase = tmem_base;
-    // D[acc] = A[buf] B^T, one elected thread
-    auto issue_mma = [&](int buf, int acc) {
-        tc::fence_after_sync();
-        const uint32_t a0 = tc::smem_u32(As[buf]), b0 = tc::smem_u32(Bs), d = tbase + (uint32_t)(acc * NT);
-        for (int kk = 0; kk < K / 16; ++kk) {
-            const uint32_t ao = (uint32_t)((kk >> 2) * 16384 + (kk & 3) * 32);
-            const uint32_t bo = (uint32_t)((kk >> 2) * NT * 128 + (kk & 3) * 32);
-            tc::mma_bf16_ss(d, tc::desc_sw128(a0 + ao), tc::desc_sw128(b0 + bo), idesc, kk > 0);
-        }
-        tc::mma_commit(&mbar[acc]);
-    };
-    if (tile0 < n_tiles) {   // the first tile's product
-        tc::cp_wait<1>();
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) issue_mma(0, 0);
-    }
 
-    bool failed = false;
-    int64_t tile = tile0;
-    for (int it = 0; tile < n_tiles; tile += stride, ++it) {
-        const int st = it % NBUF, acc = it & 1;
-        const bool has_next = tile + stride < n_tiles;
-        // with three buffers, the tile after next loads now (its buffer held tile it - 1)
-        if (NBUF == 3) {
-            if (tile + 2 * stride < n_tiles) load_a(tile + 2 * stride, (it + 2) % 3);
-            else tc::cp_commit();
+    if (warp == 0 && lane == 0) {   // ---------------- TMA producer
+        int it = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+            const int s = it % NS, n = it / NS;
+            if (n >= 1 && !tc::mbar_wait(&sempty[s], (n - 1) & 1, tc::kWaitLimit)) {
+                ok = false;
+                break;
+            }
+            mbar_expect_tx(&sfull[s], slot_bytes);
+            for (int a = 0; a < KA; ++a)
+                tma_load_2d(sX + (uint32_t)s * slot_bytes + a * kAtom, &p.tx, a * 64, (int)(t * 128), &sfull[s]);
         }
-        if (has_next) {   // the next tile's product runs during this epilogue
-            if (NBUF == 3) tc::cp_wait<1>();
-            else tc::cp_wait<0>();
-            tc::fence_proxy_async();
-            __syncthreads();
-            if (tid == 0) issue_mma((it + 1) % NBUF, acc ^ 1);
+        if (!ok) atomicOr(p.err, tc::kErrMmaTimeout);
+        for (int i = it - 1; i >= 0 && i >= it - NS; --i)   // issued loads land before the CTA ends
+            tc::mbar_wait(&sfull[i % NS], (i / NS) & 1, tc::kWaitLimit);
+    } else if (warp == 1 && lane == 0) {   // ---------------- MMA issuer
+        const uint32_t idesc = tc::idesc_bf16(128, NT);
+        int it = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+            const int s = it % NS, n = it / NS, acc = it & 1, u = it >> 1;
+            if ((u >= 1 && !tc::mbar_wait(&tempty[acc], (u - 1) & 1, tc::kWaitLimit)) ||
+                !tc::mbar_wait(&sfull[s], n & 1, tc::kWaitLimit)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t a0 = sX + (uint32_t)s * slot_bytes, d = tbase + (uint32_t)(acc * NT);
+            for (int kk = 0; kk < K / 16; ++kk) {
+                const uint32_t ao = (uint32_t)((kk >> 2) * kAtom + (kk & 3) * 32);
+                const uint32_t bo = (uint32_t)((kk >> 2) * NT * 128 + (kk & 3) * 32);
+                tc::mma_bf16_ss(d, tc::desc_sw128(a0 + ao), tc::desc_sw128(sB + bo), idesc, kk > 0);
+            }
+            tc::mma_commit(&tfull[acc]);
         }
-        bool ok = tc::mbar_wait(&mbar[acc], (it >> 1) & 1, tc::kWaitLimit);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) atomicOr(p.err, tc::kErrMmaTimeout);
-            failed = true;
-            tc::mbar_wait(&mbar[acc], (it >> 1) & 1, tc::kWaitLimit);
-            if (has_next) tc::mbar_wait(&mbar[acc ^ 1], ((it + 1) >> 1) & 1, tc::kWaitLimit);
-            break;
-        }
-        tc::fence_after_sync();
-        const uint32_t tacc = tbase + (uint32_t)(acc * NT);
-
-        // epilogue: thread owns row r of the tile and 64 columns of it
-        const int r = quarter * 32 + lane;
-        const int64_t m = tile * 128 + r;
-        if (cgroup == 0) rnorm[r] = sqrtf(row_sq(As[st], r, K, 128)) * (2.0f * 5.9604645e-8f);
-        __syncthreads();
-        const float rn = rnorm[r];
+        if (!ok) atomicOr(p.err, tc::kErrMmaTimeout);
+        tc::mma_commit(&done);   // completes when every product issued above has
+        tc::mbar_wait(&done, 0, tc::kWaitLimit);
+    } else if (warp >= 2) {   // ---------------- epilogue
+        const int ew = warp - 2, et = tid - 64, quarter = warp & 3, cgroup = ew >> 2;
+        const int r = quarter * 32 + lane;   // tile row = TMEM lane
+        int it = 0;
+        for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+            const int s = it % NS, acc = it & 1;
+            const bool ok = tc::mbar_wait(&tfull[acc], (it >> 1) & 1, tc::kWaitLimit) &&
+                            tc::mbar_wait(&sfull[s], (it / NS) & 1, tc::kWaitLimit);   // the X rows, for the norms
+            if (epi_any(!ok)) {
+                if (et == 0) atomicOr(p.err, tc::kErrMmaTimeout);
+                break;
+            }
+            tc::fence_after_sync();
+            const uint32_t xs = sX + (uint32_t)s * slot_bytes;
+            const int64_t m = t * 128 + r;
+            const float rn = sqrtf(row_sq(xs, r, K, 128)) * (2.0f * 5.9604645e-8f);
 #pragma unroll 1
-        for (int cc = cgroup * 2; cc < cgroup * 2 + 2; ++cc) {
-            uint32_t v[32];
-            tc::tmem_ld32(tacc + ((uint32_t)(quarter * 32) << 16) + cc * 32, v);
-            float o[32];
-            uint32_t overflow = 0;   // flagged elements the list had no room for
+            for (int cc = cgroup; cc < NT / 32; cc += kColGroups) {
+                uint32_t v[32];
+                tc::tmem_ld32(tbase + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * NT + cc * 32), v);
+                float o[32];
+                uint32_t flags = 0, overflow = 0;   // unsettled elements; those the list had no room for
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float f = __uint_as_float(v[i]);
-                const int col = cc * 32 + i;
-                const float bound = fmaf(rn, cnorm[col], fabsf(f) * 1.2e-7f);
-                o[i] = f;
-                if (__float2bfloat16_rn(f - bound) != __float2bfloat16_rn(f + bound)) {
+                for (int i = 0; i < 32; ++i) {
+                    const float f = __uint_as_float(v[i]);
+                    const float bound = fmaf(rn, cnorm[cc * 32 + i], fabsf(f) * 1.2e-7f);
+                    o[i] = f;
+                    flags |= (uint32_t)(__float2bfloat16_rn(f - bound) != __float2bfloat16_rn(f + bound)) << i;
+                }
+                for (uint32_t fl = flags; fl; fl &= fl - 1) {
+                    const int i = __ffs(fl) - 1;
                     const int slot = atomicAdd(&fix_n, 1);
-                    if (slot < kTpFix) fixl[slot] = make_int2(r, col);
+                    if (slot < kTpFix) fixl[slot] = make_int2(r, cc * 32 + i);
                     else overflow |= 1u << i;
                 }
+                // (not expected: about 0.5% of a tile's elements are flagged) exact sums by this thread
+                for (uint32_t ov = overflow; ov; ov &= ov - 1) {
+                    const int i = __ffs(ov) - 1, col = cc * 32 + i;
+                    float hi = 0.f, lo = 0.f;
+                    for (int k = 0; k < K; ++k) {
+                        float tt, e;
+                        two_sum(hi, __fmul_rn(bf16_at(xs, r, k, 128), bf16_at(sB, col, k, NT)), tt, e);
+                        hi = tt;
+                        lo = __fadd_rn(lo, e);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        if (q == i) o[q] = __fadd_rn(hi, lo);
+                }
+                if (m < p.M) {
+                    const int c0 = cc * 32;
+                    __nv_bfloat16 *dst = c0 < HD ? p.FL + m * HD + c0 : p.FR + m * HD + (c0 - HD);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) reinterpret_cast<uint4 *>(dst)[q] = pack<__nv_bfloat16>(o + 8 * q);
+                }
             }
-            // (not expected: about 0.5% of a tile's elements are flagged) exact sums by this thread
-            for (uint32_t ov = overflow; ov; ov &= ov - 1) {
-                const int i = __ffs(ov) - 1, col = cc * 32 + i;
+            tc::fence_before_sync();
+            mbar_arrive(&tempty[acc]);   // the accumulator may take the tile after next
+            epi_sync();                  // every flagged element is listed (and its plain value stored)
+            // exact recompute: a half-warp per element, lane j takes 16-byte
+            // chunks j, j + 16, ... of the X row and of the W column
+            const int nf = min(fix_n, kTpFix), hl = lane & 15;
+            for (int i0 = ew * 2; i0 < nf; i0 += 2 * kEpiWarps) {
+                const int i = i0 + (lane >> 4);
+                const bool act = i < nf;
+                const int fr = act ? fixl[i].x : 0, fc = act ? fixl[i].y : 0;
                 float hi = 0.f, lo = 0.f;
-                for (int k = 0; k < K; ++k) {
-                    float t, e;
-                    two_sum(hi, __fmul_rn(bf16_at(As[st], r, k, 128), bf16_at(Bs, col, k, NT)), t, e);
-                    hi = t;
-                    lo = __fadd_rn(lo, e);
+                for (int c = hl; c < KC; c += 16) {
+                    float xa[8], xb[8];
+                    unpack<__nv_bfloat16>(lds16(xs + tc::sw128_offset(fr, c * 8, 128)), xa);
+                    unpack<__nv_bfloat16>(lds16(sB + tc::sw128_offset(fc, c * 8, NT)), xb);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float tt, e;
+                        two_sum(hi, __fmul_rn(xa[q], xb[q]), tt, e);
+                        hi = tt;
+                        lo = __fadd_rn(lo, e);
+                    }
                 }
 #pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    if (q == i) o[q] = __fadd_rn(hi, lo);
-            }
-            if (m < p.M) {
-                const int c0 = cc * 32;
-                __nv_bfloat16 *dst = c0 < HD ? p.FL + m * HD + c0 : p.FR + m * HD + (c0 - HD);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    reinterpret_cast<uint4 *>(dst)[q] = pack<__nv_bfloat16>(o + 8 * q);
-            }
-        }
-        tc::fence_before_sync();
-        __syncthreads();
-        // exact recompute of the flagged elements: a half-warp per element,
-        // lane j takes the 16-byte chunks j, j + 16, ... of the row of A and
-        // of the column of W (eight exact products each), TwoSum throughout
-        const int nf = min(fix_n, kTpFix);
-        const int hl = lane & 15;
-        for (int i0 = warp * 2; i0 < nf; i0 += nthr / 16) {
-            const int i = i0 + (lane >> 4);
-            const bool act = i < nf;
-            const int fr = act ? fixl[i].x : 0, fc = act ? fixl[i].y : 0;
-            float hi = 0.f, lo = 0.f;
-            for (int c = hl; c < KC; c += 16) {
-                float xa[8], xb[8];
-                unpack<__nv_bfloat16>(*reinterpret_cast<const uint4 *>(As[st] + tc::sw128_offset(fr, c * 8, 128)), xa);
-                unpack<__nv_bfloat16>(*reinterpret_cast<const uint4 *>(Bs + tc::sw128_offset(fc, c * 8, NT)), xb);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    float t, e;
-                    two_sum(hi, __fmul_rn(xa[q], xb[q]), t, e);
-                    hi = t;
-                    lo = __fadd_rn(lo, e);
+                for (int o2 = 8; o2 > 0; o2 >>= 1) {
+                    const float ho = __shfl_xor_sync(SGA_FULL_MASK, hi, o2);
+                    const float lo2 = __shfl_xor_sync(SGA_FULL_MASK, lo, o2);
+                    float tt, e;
+                    two_sum(hi, ho, tt, e);
+                    hi = tt;
+                    lo = __fadd_rn(__fadd_rn(lo, lo2), e);
+                }
+                const int64_t fm = t * 128 + fr;
+                if (act && hl == 0 && fm < p.M) {
+                    __nv_bfloat16 *dst = fc < HD ? p.FL + fm * HD + fc : p.FR + fm * HD + (fc - HD);
+                    *dst = __float2bfloat16_rn(__fadd_rn(hi, lo));
                 }
             }
-#pragma unroll
-            for (int o2 = 8; o2 > 0; o2 >>= 1) {
-                const float ho = __shfl_xor_sync(SGA_FULL_MASK, hi, o2);
-                const float lo2 = __shfl_xor_sync(SGA_FULL_MASK, lo, o2);
-                float t, e;
-                two_sum(hi, ho, t, e);
-                hi = t;
-                lo = __fadd_rn(__fadd_rn(lo, lo2), e);
-            }
-            const int64_t fm = tile * 128 + fr;
-            if (act && hl == 0 && fm < p.M) {
-                __nv_bfloat16 *dst = fc < HD ? p.FL + fm * HD + fc : p.FR + fm * HD + (fc - HD);
-                *dst = __float2bfloat16_rn(__fadd_rn(hi, lo));
-            }
+            epi_sync();   // the list is consumed
+            if (et == 0) fix_n = 0;
+            epi_sync();   // the reset is seen before the next tile's flags
+            mbar_arrive(&sempty[s]);   // the slot's X rows are no longer read
         }
-        __syncthreads();
-        if (tid == 0) fix_n = 0;
-        // with two buffers, the tile after next loads into this tile's buffer now
-        if (NBUF == 2 && tile + 2 * stride < n_tiles) load_a(tile + 2 * stride, st);
     }
-    tc::cp_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tbase, tcols);
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_dealloc(tbase, tcols);
+    }
 }
 
+}  // namespace
+
 cudaError_t tc_proj(const TcProj &p, cudaStream_t s) {
-    const size_t smem = tc_proj_smem(p.K, p.HD);
+    if (p.M == 0) return cudaSuccess;
+    ProjParams pp{};
+    cudaError_t e = bf16_tensor_map(&pp.tx, p.X, p.M, p.K, p.K, 64, 128);
+    if (e != cudaSuccess) return e;
+    pp.Wl = p.Wl;
+    pp.Wr = p.Wr;
+    pp.FL = p.FL;
+    pp.FR = p.FR;
+    pp.M = p.M;
+    pp.K = p.K;
+    pp.HD = p.HD;
+    pp.nslot = proj_slots(p.K, p.HD);
+    pp.err = p.err;
+    const size_t smem = proj_smem(p.K, p.HD);
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tc_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem > 200 * 1024 ? (int)smem : 200 * 1024);
+        e = cudaFuncSetAttribute(tc_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
@@ -256,8 +322,7 @@ cudaError_t tc_proj(const TcProj &p, cudaStream_t s) {
     const int64_t tiles = (p.M + 127) / 128;
     const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
     note_launch(SGA_KERN_GATV2_PROJ, s, false);
-    const int threads = 128 * (2 * p.HD / 64);   // 4 lane quarters x column groups of 64
-    tc_proj_kernel<<<grid, threads, smem, s>>>(p);
+    tc_proj_kernel<<<grid, kThreads, smem, s>>>(pp);
     note_launch(SGA_KERN_GATV2_PROJ, s, true);
     return cudaGetLastError();
 }
