@@ -11,11 +11,14 @@
 //   Delta pass (per row panel, groups of four kept tiles = 64 sources):
 //     S = Q K^T, dP = dOut V^T, Delta_t = row sums of p dP over tile edges;
 //   dQ pass (same loop, Delta known): dS in bf16 to shared memory,
-//     dQ += dS K (K^T made with ldmatrix.trans / stmatrix);
+//     dQ += dS K;
 //   dK/dV pass (per column panel of 128 sources, over the row panels that
 //     keep one of its tiles, 64 rows at a time):
 //     S^T = K Q^T, dP^T = V dOut^T, P^T and dS^T to shared memory,
 //     dV += P^T dOut, dK += dS^T Q.
+// Node rows are staged once, 128-byte swizzled with 64-wide column atoms: the
+// K-major operand over D of the S and dP products, and as they stand the
+// MN-major operand over D of the dQ, dV and dK products (no transposes).
 // The residual CSR passes run in between (their Delta includes Delta_t), so
 // each pass here adds its tile part to gradients already stored.  No atomics:
 // every output row is owned by one CTA, and the results are deterministic.
@@ -57,18 +60,12 @@ __device__ __forceinline__ void load_tile_rows(uint32_t dst, const __nv_bfloat16
     }
 }
 
-// X (64 rows x D, swizzled K-major) -> X^T (D rows x 64, swizzled K-major),
-// 8x8 blocks by ldmatrix.trans / stmatrix, spread over the CTA's warps.
-template <int D>
-__device__ __forceinline__ void transpose64(uint32_t src, uint32_t dst) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mi = lane >> 3, rr = lane & 7;
-    for (int blk = warp; blk < 8 * (D / 8) / 4; blk += kThreads / 32) {
-        const int jb = (blk * 4) / (D / 8), db0 = (blk * 4) % (D / 8);
-        uint32_t v[4];
-        tc::ldsm_x4_trans(v, src + tc::sw128_offset(jb * 8 + rr, (db0 + mi) * 8, 64));
-        tc::stsm_x4(dst + tc::sw128_offset((db0 + mi) * 8 + rr, jb * 8, D), v);
-    }
+// Four k-steps over 64 node rows (K = 64): A K-major (one 64-wide atom of the
+// A tile), B the 64 node rows x N columns as an MN-major operand.
+__device__ __forceinline__ void mma_rows64(uint32_t tmem, uint32_t a, uint32_t b_rows, uint32_t idesc, bool first) {
+    for (int kk = 0; kk < 4; ++kk)
+        tc::mma_bf16_ss(tmem, tc::desc_sw128(a + kk * 32), tc::desc_sw128_mn(b_rows + kk * 2048, 64 * 128), idesc,
+                        (!first || kk > 0) ? 1u : 0u);
 }
 
 // D/16 k-steps of a 128 x N product with both operands K-major over D
@@ -80,13 +77,6 @@ __device__ __forceinline__ void mma_over_d(uint32_t tmem, uint32_t a, uint32_t b
         const uint32_t bo = (uint32_t)((kk >> 2) * RB * 128 + (kk & 3) * 32);
         tc::mma_bf16_ss(tmem, tc::desc_sw128(a + ao), tc::desc_sw128(b + bo), idesc, kk > 0);
     }
-}
-
-// Four k-steps over one 64-wide atom (K = 64), accumulating unless `first`.
-__device__ __forceinline__ void mma_over_64(uint32_t tmem, uint32_t a, uint32_t b, uint32_t idesc, bool first) {
-    for (int kk = 0; kk < 4; ++kk)
-        tc::mma_bf16_ss(tmem, tc::desc_sw128(a + kk * 32), tc::desc_sw128(b + kk * 32), idesc,
-                        (!first || kk > 0) ? 1u : 0u);
 }
 
 // Add an fp32 row (from TMEM, times `scale`) to a bf16 row of D values.
@@ -115,7 +105,7 @@ __device__ __forceinline__ void add_row_from_tmem(uint32_t taddr, __nv_bfloat16 
 __host__ __device__ constexpr int row_buffers(int mode) { return mode == 0 ? 1 : 2; }
 
 struct RowLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t q, g, k[2], v[2], kt, ds, total;
+    uint32_t q, g, k[2], v[2], ds, total;
     __host__ __device__ RowLayout(int D, int mode) {
         const uint32_t DA = (uint32_t)D / 64, NB = (uint32_t)row_buffers(mode);
         q = 0;
@@ -124,8 +114,7 @@ struct RowLayout {   // byte offsets in dynamic shared memory (1024-aligned base
         k[1] = k[0] + (NB - 1) * DA * kGroup * 128;
         v[0] = k[1] + DA * kGroup * 128;
         v[1] = v[0] + (NB - 1) * DA * kGroup * 128;
-        kt = v[1] + DA * kGroup * 128;
-        ds = kt + (mode == 1 ? (uint32_t)D * 128 : 0);
+        ds = v[1] + DA * kGroup * 128;
         total = ds + (mode == 1 ? 128 * 128 : 0);
     }
 };
@@ -169,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
     tc::fence_after_sync();
     const uint32_t tS = tmem_base, tP = tmem_base + 64, tQ = tmem_base + 128;
     const uint32_t tlane = (uint32_t)(warp * 32) << 16;
-    const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_q = tc::idesc_bf16(128, D);
+    const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_q = tc::idesc_bf16(128, D) | tc::kMajorMnB;
     const float scale2 = kLog2e * rsqrtf((float)D);
 
     float dsum = 0.f;
@@ -178,6 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
     constexpr int NB = row_buffers(MODE);
     for (int g = 0; g < ng; ++g) {
         const int b = NB == 2 ? (g & 1) : 0;
+        // the previous dS K product reads dS and the other K buffer: it must be done first
+        if (MODE == 1 && g > 0 && !tc::mbar_wait(&mbar_o, (g - 1) & 1, tc::kWaitLimit)) failed = true;
+        if (__syncthreads_or(failed)) break;
         if (NB == 2 && g + 1 < ng) {
             load_tile_rows<D>(sbase + L.k[b ^ 1], K, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
             load_tile_rows<D>(sbase + L.v[b ^ 1], V, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
@@ -186,11 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
         } else {
             tc::cp_wait<0>();
         }
-        // the previous dS K product reads K^T and dS: it must be done first
-        if (MODE == 1 && g > 0 && !tc::mbar_wait(&mbar_o, (g - 1) & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
         tc::fence_after_sync();
-        if (MODE == 1) transpose64<D>(sbase + L.k[b], sbase + L.kt);
         tc::fence_proxy_async();
         __syncthreads();
         if (tid == 0) {   // S = Q K^T, dP = dOut V^T
@@ -242,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
             __syncthreads();
             if (tid == 0) {   // dQ += dS K
                 tc::fence_after_sync();
-                mma_over_64(tQ, sbase + L.ds, sbase + L.kt, idesc_q, g == 0);
+                mma_rows64(tQ, sbase + L.ds, sbase + L.k[b], idesc_q, g == 0);
                 tc::mma_commit(&mbar_o);
             }
             ++n_o;
@@ -269,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
 // ----------------------------------------------------------- column pass
 
 struct ColLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t kc, vc, qh[2], gh[2], qt, gt, p, ds, bits[2], lse[2], dl[2], total;
+    uint32_t kc, vc, qh[2], gh[2], p, ds, bits[2], lse[2], dl[2], total;
     __host__ __device__ ColLayout(int D) {
         const uint32_t DA = (uint32_t)D / 64;
         kc = 0;
@@ -278,9 +266,7 @@ struct ColLayout {   // byte offsets in dynamic shared memory (1024-aligned base
         qh[1] = qh[0] + DA * 64 * 128;
         gh[0] = qh[1] + DA * 64 * 128;
         gh[1] = gh[0] + DA * 64 * 128;
-        qt = gh[1] + DA * 64 * 128;
-        gt = qt + (uint32_t)D * 128;
-        p = gt + (uint32_t)D * 128;
+        p = gh[1] + DA * 64 * 128;
         ds = p + 128 * 128;
         bits[0] = ds + 128 * 128;     // 8 tiles x 64 rows x 16 bits
         bits[1] = bits[0] + 1024;
@@ -349,25 +335,23 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(BsrBwdArgs a) 
     tc::fence_after_sync();
     const uint32_t tS = tmem_base, tP = tmem_base + 64, tV = tmem_base + 128, tK = tmem_base + 128 + D;
     const uint32_t tlane = (uint32_t)(warp * 32) << 16;
-    const uint32_t idesc_s = tc::idesc_bf16(128, 64), idesc_d = tc::idesc_bf16(128, D);
+    const uint32_t idesc_s = tc::idesc_bf16(128, 64), idesc_d = tc::idesc_bf16(128, D) | tc::kMajorMnB;
     const float scale2 = kLog2e * rsqrtf((float)D);
 
     bool failed = false;
     int n_o = 0;
     for (int u = 0; u < nu; ++u) {
         const int b = u & 1;
+        // the previous dV / dK products read P^T, dS^T and the other unit's dOut and Q rows
+        if (u > 0 && !tc::mbar_wait(&mbar_o, (u - 1) & 1, tc::kWaitLimit)) failed = true;
+        if (__syncthreads_or(failed)) break;
         if (u + 1 < nu) {
             load_unit(u + 1, b ^ 1);
             tc::cp_wait<1>();
         } else {
             tc::cp_wait<0>();
         }
-        // the previous dV / dK products read dOut^T, Q^T, P^T and dS^T
-        if (u > 0 && !tc::mbar_wait(&mbar_o, (u - 1) & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
         tc::fence_after_sync();
-        transpose64<D>(sbase + L.qh[b], sbase + L.qt);
-        transpose64<D>(sbase + L.gh[b], sbase + L.gt);
         tc::fence_proxy_async();
         __syncthreads();
         if (tid == 0) {   // S^T = K Q^T, dP^T = V dOut^T
@@ -410,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(BsrBwdArgs a) 
         __syncthreads();
         if (tid == 0) {   // dV += P^T dOut, dK += dS^T Q
             tc::fence_after_sync();
-            mma_over_64(tV, sbase + L.p, sbase + L.gt, idesc_d, u == 0);
-            mma_over_64(tK, sbase + L.ds, sbase + L.qt, idesc_d, u == 0);
+            mma_rows64(tV, sbase + L.p, sbase + L.gh[b], idesc_d, u == 0);
+            mma_rows64(tK, sbase + L.ds, sbase + L.qh[b], idesc_d, u == 0);
             tc::mma_commit(&mbar_o);
         }
         ++n_o;

@@ -10,9 +10,10 @@
 // softmax with a lazily moved maximum (the accumulator is rescaled only when
 // a row's maximum grows by more than 2^8, so P stays below 2^8); P goes to
 // shared memory in bf16 and O += P V_group (128 x D, K = 64) accumulates in
-// TMEM.  V rows are transposed into the K-major operand with ldmatrix.trans /
-// stmatrix.  The group's K and V rows are loaded with cp.async while the
-// previous group computes.
+// TMEM.  V rows stay in their node-major 128-byte-swizzled layout, which is
+// the MN-major B operand of that product (no transpose).  The next group's K
+// rows load once S has consumed K, its V rows once the previous P V product
+// has consumed the other V buffer; both overlap the softmax.
 //
 // The residual edges (outside kept tiles) were processed beforehand by the
 // CSR forward, whose out/lse sit in the output buffers; each row's tile result
@@ -28,21 +29,18 @@ constexpr int kBsThreads = 128;
 constexpr int kGroup = 64;           // sources per group (four 16-wide tiles)
 constexpr float kLazy = 8.0f;        // log2 growth that triggers a rescale
 
-// One K/V buffer: the next group's rows load while the current group's
-// softmax and P V product run (the S product has consumed K, the transpose V),
-// which keeps a CTA under 100 KB so that two CTAs share an SM.
+// One K buffer (reloaded once S has consumed it) and two V buffers (the P V
+// product reads V directly): under 100 KB, so two CTAs share an SM.
 struct BsLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t q, k, vn, vt, p, total;
-    int vn_ld;      // bf16 elements per natural V row (D + 8: conflict-free ldmatrix)
+    uint32_t q, k, v[2], p, total;
     __host__ __device__ BsLayout(int D) {
-        const int DA = (D + 63) / 64;
-        vn_ld = D + 8;
+        const uint32_t DA = (uint32_t)(D + 63) / 64;
         q = 0;
-        k = q + (uint32_t)DA * 128 * 128;
-        vt = k + (uint32_t)DA * kGroup * 128;
-        p = vt + (uint32_t)D * 128;
-        vn = p + 128 * 128;
-        total = vn + (uint32_t)kGroup * vn_ld * 2;
+        k = q + DA * 128 * 128;
+        v[0] = k + DA * kGroup * 128;
+        v[1] = v[0] + DA * kGroup * 128;
+        p = v[1] + DA * kGroup * 128;
+        total = p + 128 * 128;
     }
 };
 
@@ -81,46 +79,38 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
         tc::cp16(sbase + L.q + tc::sw128_offset(rr, c * 8, 128),
                  ok ? Q + ((r0 + rr) * H + h) * D + c * 8 : Q, ok);
     }
-    auto load_group = [&](int g) {
+    // rows of group g's kept tiles (zero past N or past the panel's tiles) of
+    // one head of X into the swizzled tile at dst
+    auto load_rows = [&](int g, const __nv_bfloat16 *X, uint32_t dst) {
         for (int idx = tid; idx < kGroup * DC; idx += kBsThreads) {
             const int jr = idx / DC, c = idx % DC;
             const int32_t ti = t0 + 4 * g + jr / 16;
             const int64_t j = ti < t1 ? (int64_t)a.tile_col[ti] * 16 + (jr % 16) : -1;
             const bool ok = j >= 0 && j < a.N;
-            const size_t off = ok ? ((size_t)j * H + h) * D + c * 8 : 0;
-            tc::cp16(sbase + L.k + tc::sw128_offset(jr, c * 8, kGroup), K + off, ok);
-            tc::cp16(sbase + L.vn + (uint32_t)(jr * L.vn_ld + c * 8) * 2, V + off, ok);
+            tc::cp16(dst + tc::sw128_offset(jr, c * 8, kGroup), ok ? X + ((size_t)j * H + h) * D + c * 8 : X, ok);
         }
         tc::cp_commit();
     };
-    load_group(0);   // Q travels in the same first group
+    load_rows(0, K, sbase + L.k);   // Q travels in the same first group
+    load_rows(0, V, sbase + L.v[0]);
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tO = tmem_base, tS = tmem_base + D;
     const uint32_t tlane = (uint32_t)(warp * 32) << 16;
-    const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_o = tc::idesc_bf16(128, D);
+    const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_o = tc::idesc_bf16(128, D) | tc::kMajorMnB;
     const float scale2 = kLog2e * rsqrtf((float)D);
 
     float m = -INFINITY, l = 0.f;
     bool failed = false;
     int n_o = 0;   // P V products issued (uniform over the CTA)
     for (int g = 0; g < ng; ++g) {
+        const int b = g & 1;
         tc::cp_wait<0>();   // this group's K and V rows
-        // the previous P V product must be done before P, V^T and O are touched
+        // the previous P V product must be done before P, O and the other V buffer are touched
         if (g > 0 && !tc::mbar_wait(&mbar_o, (g - 1) & 1, tc::kWaitLimit)) failed = true;
         if (__syncthreads_or(failed)) break;
         tc::fence_after_sync();
-        // V^T (D rows x 64 sources, K-major, swizzled) from the natural V rows:
-        // 8x8 blocks, ldmatrix.trans then stmatrix; block (jb, db) -> rows d, columns j
-        for (int blk = warp; blk < (kGroup / 8) * (D / 8) / 4; blk += kBsThreads / 32) {
-            const int jb = (blk * 4) / (D / 8), db0 = (blk * 4) % (D / 8);
-            const int mi = lane >> 3, rr = lane & 7;
-            const uint32_t src = sbase + L.vn + (uint32_t)((jb * 8 + rr) * L.vn_ld + (db0 + mi) * 8) * 2;
-            uint32_t v[4];
-            tc::ldsm_x4_trans(v, src);
-            const uint32_t dst = sbase + L.vt + tc::sw128_offset((db0 + mi) * 8 + rr, jb * 8, D);
-            tc::stsm_x4(dst, v);
-        }
+        if (g + 1 < ng) load_rows(g + 1, V, sbase + L.v[b ^ 1]);   // lands during this group
         tc::fence_proxy_async();
         __syncthreads();
         if (tid == 0) {   // S = Q K^T
@@ -136,8 +126,8 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
         if (!tc::mbar_wait(&mbar_s, g & 1, tc::kWaitLimit)) failed = true;
         if (__syncthreads_or(failed)) break;
         tc::fence_after_sync();
-        // K and V are consumed: the next group's rows load during the softmax
-        if (g + 1 < ng) load_group(g + 1);
+        // K is consumed: the next group's K rows load during the softmax
+        if (g + 1 < ng) load_rows(g + 1, K, sbase + L.k);
 
         // masked, scaled scores of row r; lazy online softmax
         float s[kGroup];
@@ -195,9 +185,11 @@ __global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
         __syncthreads();
         if (tid == 0) {   // O += P V
             tc::fence_after_sync();
+            // B = V rows as an MN-major operand: D-wide column atoms of 64 rows, 16 rows per k-step
             for (int kk = 0; kk < kGroup / 16; ++kk)
                 tc::mma_bf16_ss(tO, tc::desc_sw128(sbase + L.p + kk * 32),
-                                tc::desc_sw128(sbase + L.vt + kk * 32), idesc_o, (g > 0 || kk > 0));
+                                tc::desc_sw128_mn(sbase + L.v[b] + kk * 2048, kGroup * 128), idesc_o,
+                                (g > 0 || kk > 0));
             tc::mma_commit(&mbar_o);
         }
         ++n_o;

@@ -37,6 +37,22 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr) {
     return d;
 }
 
+// Descriptor of an MN-major operand with 128-byte swizzle: 64-element MN
+// blocks of 128-byte rows, one row per k (a node-major tile of 64-wide column
+// atoms, as the K-major loads above lay it out), blocks `lbo` bytes apart,
+// 8-row K groups 1024 bytes apart.  One 16-deep k-step spans two K groups
+// (2048 bytes).  Used with the transpose bit of the instruction descriptor.
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t smem_addr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr >> 4) & 0x3fff);
+    d |= (uint64_t)((lbo >> 4) & 0x3fff) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+constexpr uint32_t kMajorMnA = 1u << 15, kMajorMnB = 1u << 16;   // instruction descriptor transpose bits
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
@@ -116,19 +132,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
           "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
           "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// ---- 8x8 b16 matrix moves (shared memory) ---------------------------------
-
-// Four 8x8 matrices, transposed on the way in: lanes 8m .. 8m+7 give the row
-// addresses (16 bytes each) of matrix m.
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};"
-                 ::"r"(addr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
 }
 
 // ---- mbarrier --------------------------------------------------------------

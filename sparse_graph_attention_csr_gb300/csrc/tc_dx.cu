@@ -196,19 +196,6 @@ struct DwParams {
     int32_t *err;
 };
 
-// Shared-memory descriptor of an MN-major operand made of 64-element MN
-// blocks (one TMA box each, `lbo` bytes apart) of 128-byte rows, one row per
-// k, 128-byte swizzle; 8-row K groups are 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t addr, uint32_t lbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr >> 4) & 0x3fff);
-    d |= (uint64_t)((lbo >> 4) & 0x3fff) << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
 // Per stage: X boxes (F / 64), then dF boxes ordered (w, hi/lo, h block).
 __host__ __device__ inline uint32_t dw_stage_bytes(int F, int HD) {
     return (uint32_t)(F / 64 + 4 * (HD / 64)) * kBox;
@@ -267,7 +254,7 @@ __global__ void __launch_bounds__(kDwThreads, 1) tc_dw_kernel(const __grid_const
             tc::mbar_wait(&full[i & 1], (i >> 1) & 1, tc::kWaitLimit);
     } else if (warp == 1 && lane == 0) {   // ---------------- MMA issuer
         // M = F (A = X^T, MN-major), N = HD (B = dF^T, MN-major), K = 64 nodes per chunk
-        const uint32_t idesc = tc::idesc_bf16(128, HD) | (1u << 15) | (1u << 16);
+        const uint32_t idesc = tc::idesc_bf16(128, HD) | tc::kMajorMnA | tc::kMajorMnB;
         for (int c = 0; c < nchunks; ++c) {
             const int s = c & 1, n = c >> 1;
             if (!tc::mbar_wait(&full[s], n & 1, tc::kWaitLimit)) {
@@ -280,8 +267,8 @@ __global__ void __launch_bounds__(kDwThreads, 1) tc_dw_kernel(const __grid_const
                 for (int part = 0; part < 2; ++part) {
                     const uint32_t b0 = st + (uint32_t)(FB + (w * 2 + part) * AS) * kBox;
                     for (int kk = 0; kk < 4; ++kk)   // 16 nodes = two 8-row K groups per step
-                        tc::mma_bf16_ss(tbase + (uint32_t)(w * HD), desc_mn_sw128(st + kk * 2048, kBox),
-                                        desc_mn_sw128(b0 + kk * 2048, kBox), idesc,
+                        tc::mma_bf16_ss(tbase + (uint32_t)(w * HD), tc::desc_sw128_mn(st + kk * 2048, kBox),
+                                        tc::desc_sw128_mn(b0 + kk * 2048, kBox), idesc,
                                         (c > 0 || part > 0 || kk > 0) ? 1u : 0u);
                 }
             tc::mma_commit(&empty[s]);
