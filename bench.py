@@ -303,20 +303,63 @@ class Workload:
     def kernels(self):
         return GT_KERNELS if self.w.layer == "gt" else GATV2_KERNELS
 
-    def step(self, d=None):
-        """One forward(+backward) pass on device tensors d; returns the outputs."""
+    def forward(self, d):
+        """The layer's forward on device tensors d: (outputs, saved tensors)."""
         sga, w = self.sga, self.w
-        d = self.dev if d is None else d
         if w.layer == "gt":
             out, lse = sga.gt_attn_fwd(self.plan, d["Q"], d["K"], d["V"])
-            if not w.backward:
-                return {"out": out, "lse": lse}
-            dQ, dK, dV = sga.gt_attn_bwd(self.plan, d["Q"], d["K"], d["V"], out, lse, d["dOut"])
-            return {"out": out, "lse": lse, "dQ": dQ, "dK": dK, "dV": dV}
+            return {"out": out, "lse": lse}, (out, lse)
         FL, FR, out, lse = sga.gatv2_fwd(self.plan, d["X"], d["W_l"], d["W_r"], d["a"], 0.2)
+        return {"out": out, "lse": lse}, (FL, FR, out, lse)
+
+    def backward(self, d, saved):
+        """The layer's backward: its gradients."""
+        sga, w = self.sga, self.w
+        if w.layer == "gt":
+            out, lse = saved
+            dQ, dK, dV = sga.gt_attn_bwd(self.plan, d["Q"], d["K"], d["V"], out, lse, d["dOut"])
+            return {"dQ": dQ, "dK": dK, "dV": dV}
+        FL, FR, out, lse = saved
         dX, dWl, dWr, da = sga.gatv2_bwd(self.plan, d["X"], d["W_l"], d["W_r"], d["a"], FL, FR,
                                          out, lse, d["dOut"], 0.2)
-        return {"out": out, "lse": lse, "dX": dX, "dW_l": dWl, "dW_r": dWr, "da": da}
+        return {"dX": dX, "dW_l": dWl, "dW_r": dWr, "da": da}
+
+    def step(self, d=None):
+        """One forward(+backward) pass on device tensors d; returns the outputs."""
+        d = self.dev if d is None else d
+        outs, saved = self.forward(d)
+        if self.w.backward:
+            outs.update(self.backward(d, saved))
+        return outs
+
+    def step_e2e(self, d_in, host_out, copy_stream):
+        """One step from pinned host inputs to pinned host outputs, as a user
+        overlaps it: the forward's inputs go up on the compute stream, the
+        upstream gradient on a copy stream during the forward, the forward's
+        outputs come down on the copy stream during the backward, the
+        gradients on the compute stream after it."""
+        main = torch.cuda.current_stream()
+        bwd_only = [k for k in self.in_names if k == "dOut"]
+        copy_stream.wait_stream(main)   # the previous step's reads of the input buffers are done
+        for k in self.in_names:
+            if k not in bwd_only:
+                d_in[k].copy_(self.host[k], non_blocking=True)
+        with torch.cuda.stream(copy_stream):
+            for k in bwd_only:
+                d_in[k].copy_(self.host[k], non_blocking=True)
+        ev_in = copy_stream.record_event()
+        outs, saved = self.forward(d_in)
+        ev_fwd = main.record_event()
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_fwd)
+            for k, v in outs.items():
+                host_out[k].copy_(v, non_blocking=True)
+        ev_out = copy_stream.record_event()
+        if self.w.backward:
+            main.wait_event(ev_in)
+            for k, v in self.backward(d_in, saved).items():
+                host_out[k].copy_(v, non_blocking=True)
+        main.wait_event(ev_out)
 
 
 # --------------------------------------------------------------- CPU oracle leg
@@ -540,12 +583,9 @@ def run_native(args, ws, rank, local):
         d_in = {k: torch.empty_like(v) for k, v in wl.dev.items()}
         h2d = sum(t.numel() * t.element_size() for t in wl.host.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+        copy_stream = torch.cuda.Stream(dev)
         for _ in range(2):
-            for k in wl.in_names:
-                d_in[k].copy_(wl.host[k], non_blocking=True)
-            o = wl.step(d_in)
-            for k in host_out:
-                host_out[k].copy_(o[k], non_blocking=True)
+            wl.step_e2e(d_in, host_out, copy_stream)
         torch.cuda.synchronize()
         barrier(ws)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -554,11 +594,7 @@ def run_native(args, ws, rank, local):
         for _ in range(args.steps):
             flush.zero_()
             e0.record(stream)
-            for k in wl.in_names:
-                d_in[k].copy_(wl.host[k], non_blocking=True)
-            o = wl.step(d_in)
-            for k in host_out:
-                host_out[k].copy_(o[k], non_blocking=True)
+            wl.step_e2e(d_in, host_out, copy_stream)
             e1.record(stream)
             e1.synchronize()
             e_ms += e0.elapsed_time(e1)
