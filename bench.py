@@ -433,10 +433,25 @@ def cpu_baseline(wl, host64, indptr, indices, target_s):
     oracle_step(wl, host64, ptr, idx, nodes)
     dt = time.perf_counter() - t0
     units = int(ptr[-1]) * wl.H
-    return {"value": units / dt / 1e9, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{nr} random destination rows of {len(indptr) - 1} with their full edge "
-                      f"lists ({int(ptr[-1])} of {int(indptr[-1])} edges), fp64 forward"
-                      f"{'+backward' if wl.backward else ''}, one timed pass of {dt:.2f} s"}
+    res = {"value": units / dt / 1e9, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+           "sample": f"{nr} random destination rows of {len(indptr) - 1} with their full edge "
+                     f"lists ({int(ptr[-1])} of {int(indptr[-1])} edges), fp64 forward"
+                     f"{'+backward' if wl.backward else ''}, one timed pass of {dt:.2f} s"}
+    if wl.key in (1, 2):   # the two smallest workloads also on one core
+        all_threads = oracle.threads()
+        oracle.set_threads(1)
+        try:
+            ptr1, idx1, nodes1, nr1, _ = calibrate_sample(wl, host64, indptr, indices, target_s / 4,
+                                                          np.random.default_rng(4321))
+            t0 = time.perf_counter()
+            oracle_step(wl, host64, ptr1, idx1, nodes1)
+            dt1 = time.perf_counter() - t0
+        finally:
+            oracle.set_threads(all_threads)
+        res["single_core"] = {"value": int(ptr1[-1]) * wl.H / dt1 / 1e9, "unit": UNIT, "cores": 1,
+                              "sample": f"{nr1} random destination rows ({int(ptr1[-1])} edges), "
+                                        f"one timed pass of {dt1:.2f} s"}
+    return res
 
 
 def run_reference(args, ws, rank):
@@ -533,6 +548,14 @@ def run_native(args, ws, rank, local):
     dom_ms, dom_n = sga.profile_stop()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
+    # the same steps back to back without the L2 flush (labelled warm-L2; not the metric)
+    ew0, ew1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ew0.record(stream)
+    for i in range(args.steps):
+        wl.step()
+    ew1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = ew0.elapsed_time(ew1) / args.steps
     t_ms = max_over_ranks(sum(step_ms), ws, dev)
     value = ws * wl.units * args.steps / (t_ms / 1e3) / 1e9
 
@@ -626,6 +649,7 @@ def run_native(args, ws, rank, local):
         "gpu_launches": launches,
         "clocks": clk,
         "step_ms_p10_p50_p90": [float(np.percentile(step_ms, q)) for q in (10, 50, 90)],
+        "warm_l2_ms_per_step": warm_ms,
         "kernel_ms_one_step": {k: round(v[0], 4) for k, v in per_kernel.items()},
         "wall_s": round(wall, 3),
     }

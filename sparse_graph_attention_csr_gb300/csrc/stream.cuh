@@ -71,15 +71,16 @@ struct StreamCfg {
     static constexpr int OFF_OWN = OFF_ROW + DEPTH * ROW_SLOT;
     static constexpr int OFF_SC = OFF_OWN + QD * OWN_SLOT;
     static constexpr int OFF_OSC = OFF_SC + DEPTH * SC_SLOT;
-    static constexpr int OFF_MASK = OFF_OSC + QD * OSC_SLOT;      // [DEPTH][U] uint32
-    static constexpr int OFF_GRP = OFF_MASK + DEPTH * U * 4;       // [DEPTH] int32
+    static_assert(U <= 4, "a step's validity masks fill one 16-byte record");
+    static constexpr int OFF_MASK = (OFF_OSC + QD * OSC_SLOT + 15) / 16 * 16;   // [DEPTH] uint4: masks of u = 0..3
+    static constexpr int OFF_GRP = OFF_MASK + DEPTH * 16;          // [DEPTH] int32
     static constexpr int OFF_Q = (OFF_GRP + DEPTH * 4 + 15) / 16 * 16;   // [QD] int4
     static constexpr int BYTES = OFF_Q + QD * 16;
     // 16-byte regions (cp.async 16, uint4 / int4 accesses) start on 16 bytes,
     // 4-byte regions on 4 bytes; BYTES keeps every warp's base 16-aligned
     static_assert(OFF_ROW % 16 == 0 && OFF_OWN % 16 == 0 && ROW_SLOT % 16 == 0 && OWN_SLOT % 16 == 0,
                   "row slots must be 16-byte aligned");
-    static_assert(OFF_SC % 4 == 0 && OFF_OSC % 4 == 0 && OFF_MASK % 4 == 0 && OFF_GRP % 4 == 0,
+    static_assert(OFF_SC % 4 == 0 && OFF_OSC % 4 == 0 && OFF_MASK % 16 == 0 && OFF_GRP % 4 == 0,
                   "scalar slots must be 4-byte aligned");
     static_assert(OFF_Q % 16 == 0 && BYTES % 16 == 0, "queue entries and warp bases must be 16-byte aligned");
 };
@@ -122,6 +123,7 @@ template <typename C> struct EdgeStream {
     bool p_done;
     // consumer
     int32_t c_step, q_head, c_slot, q_hslot;
+    uint4 c_mask;            // validity masks of the current step (lane bit per neighbour u)
 
     __device__ __forceinline__ void init(unsigned char *warp_smem, const StreamArrays &a, const Partition &part,
                                          const int32_t *ptr_, const int32_t *ids_, int64_t N_, int H_, int R_,
@@ -226,6 +228,7 @@ template <typename C> struct EdgeStream {
     __device__ __forceinline__ void issue_step() {
         const int slot = p_slot;
         const int32_t e0 = p_step * C::STEP;   // item-local first edge of the step
+        uint32_t masks[4] = {0u, 0u, 0u, 0u};
         if (p_step > 0 && (e0 & 31) == 0) {    // next batch of 32 ids
             p_ids = p_ids_nx;
             p_ids_nx = e0 + 32 < p_deg ? load_ids(ids, p_beg + e0 + 32, min(32, p_deg - e0 - 32), N, err) : -1;
@@ -249,10 +252,12 @@ template <typename C> struct EdgeStream {
                 for (int s = 0; s < C::NSC; ++s)
                     cp4_async(sa + C::OFF_SC + slot * C::SC_SLOT + ((u * C::NSC + s) * 32 + lane) * 4,
                               ok ? arr.sc[s] + (size_t)j * H + gl : arr.sc[s], ok);
-            const unsigned m = __ballot_sync(SGA_FULL_MASK, ok);
-            if (lane == 0) reinterpret_cast<uint32_t *>(sm + C::OFF_MASK)[slot * C::U + u] = m;
+            masks[u] = __ballot_sync(SGA_FULL_MASK, ok);
         }
-        if (lane == 0) reinterpret_cast<int32_t *>(sm + C::OFF_GRP)[slot] = gc;
+        if (lane == 0) {
+            *reinterpret_cast<uint4 *>(sm + C::OFF_MASK + slot * 16) = make_uint4(masks[0], masks[1], masks[2], masks[3]);
+            reinterpret_cast<int32_t *>(sm + C::OFF_GRP)[slot] = gc;
+        }
         ++p_step;
         ++p_issued;
         p_slot = p_slot + 1 == C::DEPTH ? 0 : p_slot + 1;
@@ -299,6 +304,7 @@ template <typename C> struct EdgeStream {
         if (newer >= C::DEPTH - 1) cp_wait_group<C::DEPTH - 1>();   // the steady state
         else cp_wait_newer(newer);
         __syncwarp();
+        c_mask = *reinterpret_cast<const uint4 *>(sm + C::OFF_MASK + c_slot * 16);
     }
     __device__ __forceinline__ void release_step() {
         ++c_step;
@@ -306,7 +312,7 @@ template <typename C> struct EdgeStream {
     }
 
     __device__ __forceinline__ bool valid(int u) const {
-        const uint32_t m = reinterpret_cast<const uint32_t *>(sm + C::OFF_MASK)[c_slot * C::U + u];
+        const uint32_t m = u == 0 ? c_mask.x : (u == 1 ? c_mask.y : (u == 2 ? c_mask.z : c_mask.w));
         return (m >> lane) & 1u;
     }
     __device__ __forceinline__ uint4 row(int u, int r, int k) const {
