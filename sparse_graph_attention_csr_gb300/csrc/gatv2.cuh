@@ -61,10 +61,13 @@ template <typename T, int D, int NC, int G> using Gatv2SrcStream = RingCfg<NC, G
 template <int EL>
 __device__ __forceinline__ void lrelu_chunk(const float *fl, const float *fr, float slope, float *lz, float *d) {
 #pragma unroll
-    for (int x = 0; x < EL; ++x) {
-        const float z = fl[x] + fr[x];
-        d[x] = z > 0.f ? 1.f : slope;
-        lz[x] = z * d[x];
+    for (int x = 0; x < EL; x += 2) {
+        const float2 z = fadd2(make_float2(fl[x], fl[x + 1]), make_float2(fr[x], fr[x + 1]));
+        d[x] = z.x > 0.f ? 1.f : slope;
+        d[x + 1] = z.y > 0.f ? 1.f : slope;
+        const float2 l = fmul2(z, make_float2(d[x], d[x + 1]));
+        lz[x] = l.x;
+        lz[x + 1] = l.y;
     }
 }
 // LeakyReLU alone, as h z + k |z| with h = (1 + slope) / 2, k = (1 - slope) / 2
@@ -249,7 +252,8 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
             a.split_threshold, a.d_err);
     StreamItem it;
     while (st.next_item(it)) {
-        // fA/fB: dFL sums, gA/gB: da sums (A weighted by p dp, B by p), c: Delta part
+        // fA/fB: dFL sums (of LReLU'(z), times a after the row), gA/gB: da sums
+        // (A weighted by p dp, B by p), c: Delta part
         float fl[NC][EL], go[NC][EL], fA[NC][EL], fB[NC][EL], gA[NC][EL], gB[NC][EL];
         float c[NC], lse2[NC];
 #pragma unroll
@@ -281,17 +285,27 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                     const float p = ok ? exp2f(e * kLog2e - lse2[k]) : 0.f;
                     const float pdp = p * dp;
                     c[k] += pdp;
-                    float ag[EL];
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) ag[x] = att[k][x] * dz[x];
-                    axpy2<EL>(fA[k], pdp, ag);
-                    axpy2<EL>(fB[k], p, ag);
+                    axpy2<EL>(fA[k], pdp, dz);
+                    axpy2<EL>(fB[k], p, dz);
                     axpy2<EL>(gA[k], pdp, lz);
                     axpy2<EL>(gB[k], p, lz);
                 }
             }
             st.release_step();
         }
+        // a is constant over the row: the dFL sums take it once
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+#pragma unroll
+            for (int x = 0; x < EL; x += 2) {
+                const float2 ax = make_float2(att[k][x], att[k][x + 1]);
+                const float2 ra = fmul2(ax, make_float2(fA[k][x], fA[k][x + 1]));
+                const float2 rb = fmul2(ax, make_float2(fB[k][x], fB[k][x + 1]));
+                fA[k][x] = ra.x;
+                fA[k][x + 1] = ra.y;
+                fB[k][x] = rb.x;
+                fB[k][x + 1] = rb.y;
+            }
         // Delta and the dFL sums over the whole warp (all edge groups)
 #pragma unroll
         for (int off = G; off < 32; off <<= 1)
@@ -414,11 +428,15 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
             a.split_threshold, a.d_err);
     StreamItem it;
     while (st.next_item(it)) {
-        float frj[NC][EL], dfr[NC][EL];
+        // dfr: sum of p dOut_i; dfw: sum of de LReLU'(z), times a after the
+        // column (up to two chunks per lane; wider rows lack the registers and
+        // weight each edge's term by a directly)
+        constexpr bool kFactorA = NC <= 2;
+        float frj[NC][EL], dfr[NC][EL], dfw[NC][EL];
 #pragma unroll
         for (int k = 0; k < NC; ++k)
 #pragma unroll
-            for (int x = 0; x < EL; ++x) frj[k][x] = dfr[k][x] = 0.f;
+            for (int x = 0; x < EL; ++x) frj[k][x] = dfr[k][x] = dfw[k][x] = 0.f;
         for (int step = 0; step < it.nsteps; ++step) {
             st.wait_step();
             if (step == 0)
@@ -438,15 +456,28 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
                     const int h = (gl + G * k) / LH;
                     const float p = ok ? exp2f((e - st.scalar(u, 0, h)) * kLog2e) : 0.f;
                     const float de = p * (dp - st.scalar(u, 1, h));
-                    float w[EL];
-#pragma unroll
-                    for (int x = 0; x < EL; ++x) w[x] = att[k][x] * dz[x];
                     axpy2<EL>(dfr[k], p, gf);
-                    axpy2<EL>(dfr[k], de, w);
+                    if constexpr (kFactorA) {
+                        axpy2<EL>(dfw[k], de, dz);
+                    } else {
+                        float w[EL];
+#pragma unroll
+                        for (int x = 0; x < EL; ++x) w[x] = att[k][x] * dz[x];
+                        axpy2<EL>(dfr[k], de, w);
+                    }
                 }
             }
             st.release_step();
         }
+#pragma unroll
+        for (int k = 0; k < NC; ++k)
+#pragma unroll
+            for (int x = 0; x < EL && kFactorA; x += 2) {
+                const float2 r = ffma2(make_float2(att[k][x], att[k][x + 1]), make_float2(dfw[k][x], dfw[k][x + 1]),
+                                       make_float2(dfr[k][x], dfr[k][x + 1]));
+                dfr[k][x] = r.x;
+                dfr[k][x + 1] = r.y;
+            }
 #pragma unroll
         for (int off = G; off < 32; off <<= 1)
 #pragma unroll
