@@ -642,9 +642,9 @@ gatv2_reduce_kernel(const float *__restrict__ dw_part, int slabs, int64_t FHD, T
     __shared__ float sh[kRedGroups][kRedOut];
     const int o = threadIdx.x % kRedOut, r = threadIdx.x / kRedOut;
     const int64_t t = (int64_t)blockIdx.x * kRedOut + o;
-    // partials r, r + 8, r + 16, ... are fetched eight at a time (independent
-    // loads in flight) and added in increasing order
-    constexpr int kBatch = 8;
+    // partials r, r + 8, r + 16, ... are fetched sixteen at a time
+    // (independent loads in flight) and added in increasing order
+    constexpr int kBatch = 16;
     float sum = 0.f;
     if (t < 2 * FHD) {
         const int which = (int)(t / FHD);

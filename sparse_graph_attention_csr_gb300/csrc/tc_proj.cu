@@ -40,11 +40,14 @@ struct ProjParams {
     int32_t *err;
 };
 
+// static shared memory of the kernel, with room to spare (norms, barriers, fix list)
+constexpr size_t kStaticSmem = 16 * 1024;
+
 __host__ __device__ inline size_t proj_b_bytes(int K, int HD) { return (size_t)((K + 63) / 64) * 2 * HD * 128; }
-// X slots in flight: three when they fit, else two
+// X slots in flight: three when they fit beside the static arrays, else two
 __host__ __device__ inline int proj_slots(int K, int HD) {
     const size_t slot = (size_t)((K + 63) / 64) * kAtom;
-    return 1024 + proj_b_bytes(K, HD) + 3 * slot <= 227 * 1024 ? 3 : 2;
+    return 1024 + proj_b_bytes(K, HD) + 3 * slot + kStaticSmem <= 227 * 1024 ? 3 : 2;
 }
 __host__ __device__ inline size_t proj_smem(int K, int HD) {
     return 1024 + proj_b_bytes(K, HD) + (size_t)proj_slots(K, HD) * ((K + 63) / 64) * kAtom;
@@ -102,7 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_const
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ float cnorm[256];
+    __shared__ __align__(16) float cnorm[256];
+    __shared__ float rsq[kColGroups][128];   // quarters of each tile row's squared norm
     __shared__ uint64_t sfull[3], sempty[3], tfull[2], tempty[2], done;
     __shared__ uint32_t tmem_base;
     __shared__ int2 fixl[kTpFix];
@@ -200,19 +204,46 @@ __global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_const
             tc::fence_after_sync();
             const uint32_t xs = sX + (uint32_t)s * slot_bytes;
             const int64_t m = t * 128 + r;
-            const float rn = sqrtf(row_sq(xs, r, K, 128)) * (2.0f * 5.9604645e-8f);
+            {   // the lane quarter's four column groups split the row norm's K range
+                const int c0 = cgroup * (KC / kColGroups), c1 = c0 + KC / kColGroups;
+                float q0 = 0.f, q1 = 0.f;
+                for (int c = c0; c < c1; ++c) {
+                    float x[8];
+                    unpack<__nv_bfloat16>(lds16(xs + tc::sw128_offset(r, c * 8, 128)), x);
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        q0 = fmaf(x[i], x[i], q0);
+                        q1 = fmaf(x[i + 1], x[i + 1], q1);
+                    }
+                }
+                rsq[cgroup][r] = q0 + q1;
+            }
+            epi_sync();   // (the next tile's writes come after this tile's later barriers)
+            const float rn = sqrtf(((rsq[0][r] + rsq[1][r]) + rsq[2][r]) + rsq[3][r]) * (2.0f * 5.9604645e-8f);
 #pragma unroll 1
             for (int cc = cgroup; cc < NT / 32; cc += kColGroups) {
                 uint32_t v[32];
                 tc::tmem_ld32(tbase + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * NT + cc * 32), v);
-                float o[32];
+                float o[32], cn[32];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 c4 = reinterpret_cast<const float4 *>(cnorm + cc * 32)[q];
+                    cn[4 * q] = c4.x;
+                    cn[4 * q + 1] = c4.y;
+                    cn[4 * q + 2] = c4.z;
+                    cn[4 * q + 3] = c4.w;
+                }
                 uint32_t flags = 0, overflow = 0;   // unsettled elements; those the list had no room for
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const float f = __uint_as_float(v[i]);
-                    const float bound = fmaf(rn, cnorm[cc * 32 + i], fabsf(f) * 1.2e-7f);
+                    const float bound = fmaf(rn, cn[i], fabsf(f) * 1.2e-7f);
                     o[i] = f;
-                    flags |= (uint32_t)(__float2bfloat16_rn(f - bound) != __float2bfloat16_rn(f + bound)) << i;
+                    // both ends of [f - bound, f + bound] rounded at once; unsettled
+                    // when their bf16 bit patterns differ
+                    const __nv_bfloat162 ends = __floats2bfloat162_rn(f - bound, f + bound);
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(&ends);
+                    flags |= (uint32_t)(((w ^ (w >> 16)) & 0xffffu) != 0u) << i;
                 }
                 for (uint32_t fl = flags; fl; fl &= fl - 1) {
                     const int i = __ffs(fl) - 1;
