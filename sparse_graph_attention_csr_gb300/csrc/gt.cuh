@@ -37,27 +37,33 @@ template <typename T, int D, int NC, int G> struct GtShape {
 // ------------------------------------------------------------------ forward
 
 // Stream shape of a kernel with NROW gathered row arrays: U neighbours per
-// group and step (1 when a lane holds two or more chunks of a row), and a ring
-// of about 10 KB per warp (2 to 8 steps).
-template <int NC, int NROW, int NSC = 0, int NOWN = 1, int NOSC = 0, int G = 32> struct RingDims {
-    // edges per group and step: more when a row is short (several groups per warp)
-    static constexpr int U = NC >= 2 ? 1 : (G < 32 ? 4 : 2);
+// group and step, and a ring of about 10 KB per warp (2 to 8 steps).  Rows of
+// one chunk per lane take 4 neighbours a step when groups are narrower than a
+// warp, else U1; rows of two chunks per lane take U2; wider rows take 1.  More
+// neighbours a step spread the per-step bookkeeping (queue, masks, waits) over
+// more edges but leave fewer steps in flight and hold more registers, so each
+// kernel takes the largest counts that keep its registers.
+template <int NC, int NROW, int NSC = 0, int NOWN = 1, int NOSC = 0, int G = 32, int U2 = 1, int U1 = 2>
+struct RingDims {
+    static constexpr int U = NC >= 2 ? (NC == 2 ? U2 : 1) : (G < 32 ? 4 : U1);
     static constexpr int STEP_BYTES = U * NC * 32 * (NROW * 16 + NSC * 4);
     static constexpr int OWN_BYTES = NC * 32 * (NOWN * 16 + NOSC * 4);
     static constexpr int QD = 3 * OWN_BYTES > 4096 ? 2 : 3;
     static constexpr int FIT = (13312 - QD * OWN_BYTES) / STEP_BYTES;
+    static_assert(U <= 2 || FIT >= 2, "two steps of several neighbours must fit the ring");
     static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
 };
-template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC>
-using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G>::U, NROW, NSC, NOWN, NOSC,
-                          RingDims<NC, NROW, NSC, NOWN, NOSC, G>::DEPTH, RingDims<NC, NROW, NSC, NOWN, NOSC, G>::QD>;
+template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC, int U2 = 1, int U1 = 2>
+using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::U, NROW, NSC, NOWN, NOSC,
+                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
+                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD>;
 
 // gathered K, V; own Q
-template <typename T, int D, int NC, int G> using GtFwdStream = RingCfg<NC, G, 2, 0, 1, 0>;
+template <typename T, int D, int NC, int G> using GtFwdStream = RingCfg<NC, G, 2, 0, 1, 0, 2, 4>;
 // gathered K, V; own Q, dOut, lse
-template <typename T, int D, int NC, int G> using GtDqStream = RingCfg<NC, G, 2, 0, 2, 1>;
+template <typename T, int D, int NC, int G> using GtDqStream = RingCfg<NC, G, 2, 0, 2, 1, 1, 4>;
 // gathered Q, dOut, lse, Delta (over the transposed CSR); own K, V
-template <typename T, int D, int NC, int G> using GtDkdvStream = RingCfg<NC, G, 2, 2, 2, 0>;
+template <typename T, int D, int NC, int G> using GtDkdvStream = RingCfg<NC, G, 2, 2, 2, 0, 1, 4>;
 
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
