@@ -61,7 +61,7 @@ using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>:
 // gathered K, V; own Q
 template <typename T, int D, int NC, int G> using GtFwdStream = RingCfg<NC, G, 2, 0, 1, 0, 2, 4>;
 // gathered K, V; own Q, dOut, lse
-template <typename T, int D, int NC, int G> using GtDqStream = RingCfg<NC, G, 2, 0, 2, 1, 1, 4>;
+template <typename T, int D, int NC, int G> using GtDqStream = RingCfg<NC, G, 2, 0, 2, 1, 2, 4>;
 // gathered Q, dOut, lse, Delta (over the transposed CSR); own K, V
 template <typename T, int D, int NC, int G> using GtDkdvStream = RingCfg<NC, G, 2, 2, 2, 0, 1, 4>;
 
@@ -352,7 +352,9 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                     unpack<T>(st.own_row(1, k), go[k]);
                     lse2[k] = st.own_scalar(0, (gl + G * k) / LH) * kLog2e;
                 }
-#pragma unroll
+            // two-chunk rows take their two neighbours one after the other
+            // (unrolled, the pair needs more registers than a thread has)
+#pragma unroll(NC >= 2 ? 1 : U)
             for (int u = 0; u < U; ++u) {
                 const bool ok = st.valid(u);
 #pragma unroll
