@@ -34,6 +34,26 @@ template <typename T, int D, int NC, int G> struct GtShape {
     static_assert(LH <= G, "a head must fit in one edge group");
 };
 
+// Head sums of two value pairs per lane, (s0, t0) of its first chunk and
+// (s1, t1) of its second, when both chunks' heads span the same LH lanes
+// (two chunks per lane, LH >= 2): the lanes whose bit LH/2 is clear finish the
+// first chunk's sums and the others the second's, so one exchange halves the
+// work before the usual butterfly.  Returns whether this lane finished the
+// second chunk; (s, t) are its head sums.
+template <int LH>
+__device__ __forceinline__ bool head_sums_split(float s0, float t0, float s1, float t1, float &s, float &t) {
+    static_assert(LH >= 2, "a head spans at least two lanes");
+    const bool hi = (threadIdx.x & (LH / 2)) != 0;
+    s = (hi ? s1 : s0) + __shfl_xor_sync(SGA_FULL_MASK, hi ? s0 : s1, LH / 2);
+    t = (hi ? t1 : t0) + __shfl_xor_sync(SGA_FULL_MASK, hi ? t0 : t1, LH / 2);
+#pragma unroll
+    for (int o = LH / 4; o > 0; o >>= 1) {
+        s += __shfl_xor_sync(SGA_FULL_MASK, s, o);
+        t += __shfl_xor_sync(SGA_FULL_MASK, t, o);
+    }
+    return hi;
+}
+
 // ------------------------------------------------------------------ forward
 
 // Stream shape of a kernel with NROW gathered row arrays: U neighbours per
@@ -357,18 +377,45 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
 #pragma unroll(NC >= 2 ? 1 : U)
             for (int u = 0; u < U; ++u) {
                 const bool ok = st.valid(u);
+                if constexpr (NC == 2) {
+                    // the two chunks' head sums split across lane pairs: one
+                    // weight per lane, exchanged afterwards
+                    float kf[2][EL], sd[2], dv[2];
 #pragma unroll
-                for (int k = 0; k < NC; ++k) {
-                    float kf[EL], vf[EL];
-                    unpack<T>(st.row(u, 0, k), kf);
-                    unpack<T>(st.row(u, 1, k), vf);
-                    float sdot = dot2<EL>(q[k], kf), dp = dot2<EL>(go[k], vf);
-                    group_sum2<LH>(sdot, dp);
-                    const float p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
+                    for (int k = 0; k < 2; ++k) {
+                        float vf[EL];
+                        unpack<T>(st.row(u, 0, k), kf[k]);
+                        unpack<T>(st.row(u, 1, k), vf);
+                        sd[k] = dot2<EL>(q[k], kf[k]);
+                        dv[k] = dot2<EL>(go[k], vf);
+                    }
+                    float sdot, dp;
+                    const bool hi = head_sums_split<LH>(sd[0], dv[0], sd[1], dv[1], sdot, dp);
+                    const float p = ok ? exp2f(sdot * scale2 - (hi ? lse2[1] : lse2[0])) : 0.f;
                     const float pdp = p * dp;
-                    c[k] += pdp;
-                    axpy2<EL>(A[k], pdp, kf);
-                    axpy2<EL>(B[k], p, kf);
+                    const float po = __shfl_xor_sync(SGA_FULL_MASK, p, LH / 2);
+                    const float pdpo = __shfl_xor_sync(SGA_FULL_MASK, pdp, LH / 2);
+                    const float p0 = hi ? po : p, p1 = hi ? p : po, d0 = hi ? pdpo : pdp, d1 = hi ? pdp : pdpo;
+                    c[0] += d0;
+                    c[1] += d1;
+                    axpy2<EL>(A[0], d0, kf[0]);
+                    axpy2<EL>(B[0], p0, kf[0]);
+                    axpy2<EL>(A[1], d1, kf[1]);
+                    axpy2<EL>(B[1], p1, kf[1]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < NC; ++k) {
+                        float kf[EL], vf[EL];
+                        unpack<T>(st.row(u, 0, k), kf);
+                        unpack<T>(st.row(u, 1, k), vf);
+                        float sdot = dot2<EL>(q[k], kf), dp = dot2<EL>(go[k], vf);
+                        group_sum2<LH>(sdot, dp);
+                        const float p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
+                        const float pdp = p * dp;
+                        c[k] += pdp;
+                        axpy2<EL>(A[k], pdp, kf);
+                        axpy2<EL>(B[k], p, kf);
+                    }
                 }
             }
             st.release_step();
