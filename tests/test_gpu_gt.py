@@ -96,7 +96,7 @@ def test_small_workloads_match_oracle(key):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("H,D", [(1, 32), (2, 32), (1, 64), (2, 64), (4, 32), (3, 64), (1, 128),
-                                 (4, 128), (8, 128), (5, 32)])
+                                 (4, 128), (8, 128), (5, 32), (3, 128), (6, 64)])
 def test_every_lane_layout(dtype, H, D):
     """Edge groups of 4..32 lanes and 1..8 chunks per lane; forced splitting."""
     rng = np.random.default_rng(H * 1000 + D)
