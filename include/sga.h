@@ -167,20 +167,33 @@ sga_status sga_read_device_error(const sga_plan *plan, void *stream, int32_t *co
  * rejected with SGA_ELIMIT before any edge kernel runs.  The CSR is validated
  * on the device (SGA_EINVAL if invalid).
  *
- * Behaviour: the call synchronises `stream` once (to read the split count),
- * then launches the edge kernels asynchronously on it.  The first call on a
+ * Behaviour: the call synchronises `stream` once (it copies the split count
+ * back to the host to size the launches), then launches the edge kernels
+ * asynchronously on it.  Because of that synchronisation it cannot be called
+ * while `stream` is being captured into a CUDA graph.  The first call on a
  * device looks up the array's device address for that device (with that
- * device current), so make the first call before any stream capture.  Every
- * call shares the one array and finds the previous call's data in it: calls
- * that can overlap on the GPU (other streams, other host threads) race and
- * must be serialised by the caller.  Allocates nothing: no cudaMalloc,
- * cudaFree or allocating library routine. */
+ * device current).  Every call shares the one array and finds the previous
+ * call's data in it: calls that can overlap on the GPU (other streams, other
+ * host threads) race and must be serialised by the caller.  Allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Range checks: the CSR is validated before the edge kernels run, so their
+ * own per-gather range check can fire only if indices change between the
+ * validation and the gathers.  Such a failure skips the access and sets a bit
+ * in a word of the static array, which sga_noalloc_read_device_error reads. */
 sga_status gt_attn_fwd_noalloc(const int32_t *indptr, const int32_t *indices, const void *Q,
                                const void *K, const void *V, int64_t N, int64_t E, int H, int D,
                                sga_dtype dt, void *out, float *lse, void *stream);
 
 /* Size in bytes of the static scratch array behind gt_attn_fwd_noalloc. */
 size_t sga_noalloc_scratch_bytes(void);
+
+/* Read and clear the device range-check word of gt_attn_fwd_noalloc on the
+ * current device (0: no failed check since the last read).  Synchronises
+ * `stream`; returns SGA_EDEVICE_CHECK if the word was non-zero.  It shares the
+ * static array with gt_attn_fwd_noalloc, so it must not overlap such a call
+ * on another stream. */
+sga_status sga_noalloc_read_device_error(void *stream, int32_t *code);
 
 /* ---- plan inspection (tests) -------------------------------------------- */
 

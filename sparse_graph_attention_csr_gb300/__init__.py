@@ -89,6 +89,7 @@ _SIGNATURES = {
     "gt_attn_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp],
                             _int),
     "sga_noalloc_scratch_bytes": ([], ctypes.c_size_t),
+    "sga_noalloc_read_device_error": ([_vp, ctypes.POINTER(ctypes.c_int32)], _int),
     "sga_profile_start": ([_int], _int),
     "sga_profile_stop": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64)], _int),
 }
@@ -272,18 +273,53 @@ def gt_attn_fwd_noalloc(indptr, indices, Q, K, V, out=None, lse=None, stream=Non
     must not allocate device memory (the library uses a fixed static device
     array instead; see include/sga.h).  Passing ``out`` and ``lse`` keeps this
     call free of allocations on the Python side too.  Synchronises the stream
-    once.  Returns (out, lse)."""
+    once, so it cannot run inside a CUDA graph capture.  Returns (out, lse).
+
+    Shapes are checked here before the library sees any pointer: N is taken
+    from ``indptr`` (N + 1 entries), Q, K, V (and ``out``) must be [N, H, D] of
+    one dtype, ``lse`` [N, H] float32, all on one device."""
     _need(indptr, "indptr", torch.int32)
     _need(indices, "indices", torch.int32)
+    if indptr.dim() != 1 or indices.dim() != 1 or indptr.numel() < 1:
+        raise ValueError("indptr and indices must be 1-D, indptr with N + 1 entries")
+    N = indptr.numel() - 1
+    if Q.dim() != 3 or Q.shape[0] != N:
+        raise ValueError(f"Q must be [N, H, D] with N = indptr.numel() - 1 = {N}, got {tuple(Q.shape)}")
     for n, t in (("Q", Q), ("K", K), ("V", V)):
         _need(t, n, Q.dtype)
-    N, H, D = Q.shape
-    out = torch.empty_like(Q) if out is None else out
-    lse = torch.empty((N, H), dtype=torch.float32, device=Q.device) if lse is None else lse
+        if t.shape != Q.shape:
+            raise ValueError(f"{n} must have Q's shape {tuple(Q.shape)}, got {tuple(t.shape)}")
+    _, H, D = Q.shape
+    if out is None:
+        out = torch.empty_like(Q)
+    else:
+        _need(out, "out", Q.dtype)
+        if out.shape != Q.shape:
+            raise ValueError(f"out must have Q's shape {tuple(Q.shape)}, got {tuple(out.shape)}")
+    if lse is None:
+        lse = torch.empty((N, H), dtype=torch.float32, device=Q.device)
+    else:
+        _need(lse, "lse", torch.float32)
+        if tuple(lse.shape) != (N, H):
+            raise ValueError(f"lse must be [{N}, {H}], got {tuple(lse.shape)}")
+    for n, t in (("indptr", indptr), ("indices", indices), ("K", K), ("V", V), ("out", out),
+                 ("lse", lse)):
+        if t.device != Q.device:
+            raise ValueError(f"{n} is on {t.device}, Q on {Q.device}")
     _check(_lib().gt_attn_fwd_noalloc(_ptr(indptr), _ptr(indices), _ptr(Q), _ptr(K), _ptr(V), N,
                                       indices.numel(), H, D, _dtype_code(Q), _ptr(out), _ptr(lse),
                                       _stream(stream)), "gt_attn_fwd_noalloc")
     return out, lse
+
+
+def noalloc_device_error(stream=None) -> int:
+    """Read and clear gt_attn_fwd_noalloc's device range-check word on the
+    current device (0 = no failed check).  Synchronises the stream."""
+    code = ctypes.c_int32()
+    st = _lib().sga_noalloc_read_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (SGA_OK, SGA_EDEVICE_CHECK):
+        _check(st, "sga_noalloc_read_device_error")
+    return int(code.value)
 
 
 # ----------------------------------------------------------------------- GATv2

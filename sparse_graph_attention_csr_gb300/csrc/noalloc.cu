@@ -3,6 +3,8 @@
 // that gt_attn_fwd keeps in its plan and workspace live here in one
 // file-scope static device array instead; the caller passes only the graph,
 // Q/K/V and the outputs.  The edge kernels are the same as gt_attn_fwd's.
+#include <stddef.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -23,7 +25,8 @@ struct NaHeader {
     int32_t n_split;    // split rows found (may exceed kNaMaxSplit: then rejected)
     int32_t n_chunks;   // chunks those rows need
     int32_t csr_err;    // CSR validation bits
-    int32_t range_err;  // device range-check word of the edge kernels
+    int32_t range_err;  // device range-check word of the edge kernels; kept across
+                        // calls until sga_noalloc_read_device_error reads and clears it
 };
 constexpr size_t kOffHeader = 0;
 constexpr size_t kOffSplitRows = 256;
@@ -176,8 +179,10 @@ extern "C" sga_status gt_attn_fwd_noalloc(const int32_t *indptr, const int32_t *
         return SGA_ECUDA;
     }
     unsigned char *scratch = static_cast<unsigned char *>(base);
-    // every call starts from a cleared header: the array keeps the last call's contents
-    ce = cudaMemsetAsync(scratch + kOffHeader, 0, sizeof(NaHeader), s);
+    // every call starts from cleared split counts and CSR bits (the array keeps
+    // the last call's contents); the range-check word is left for the caller to
+    // read with sga_noalloc_read_device_error
+    ce = cudaMemsetAsync(scratch + kOffHeader, 0, offsetof(NaHeader, range_err), s);
     if (ce == cudaSuccess && (N > 0 || E > 0)) {
         int64_t work = N > E ? N : E;
         unsigned blocks = (unsigned)((work + 255) / 256);
@@ -233,4 +238,22 @@ extern "C" sga_status gt_attn_fwd_noalloc(const int32_t *indptr, const int32_t *
         return SGA_ECUDA;
     }
     return SGA_OK;
+}
+
+extern "C" sga_status sga_noalloc_read_device_error(void *stream, int32_t *code) {
+    if (!code) return SGA_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void *base = nullptr;
+    cudaError_t ce = scratch_address(&base);
+    int32_t *word = &reinterpret_cast<NaHeader *>(static_cast<unsigned char *>(base) + kOffHeader)->range_err;
+    int32_t v = 0;
+    if (ce == cudaSuccess) ce = cudaMemcpyAsync(&v, word, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(word, 0, sizeof(int32_t), s);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+    if (ce != cudaSuccess) {
+        set_cuda_error(ce);
+        return SGA_ECUDA;
+    }
+    *code = v;
+    return v ? SGA_EDEVICE_CHECK : SGA_OK;
 }

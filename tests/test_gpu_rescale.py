@@ -1,0 +1,266 @@
+"""Parity cases that reach the online softmax's rescale of a non-empty
+accumulator, and the merge of split-row chunks whose maxima are far apart.
+
+The kernels move each row's running maximum lazily: the accumulator and its
+sum are rescaled only when a later score exceeds the running maximum by more
+than 2^8 (8 ln 2 ~ 5.55 in natural units).  Scores of N(0,1)-sized inputs
+rarely do that, so these inputs are built as a staircase: every source node j
+carries a level t_j (levels 7 apart), q_i and k_j point along one direction
+per head so that s_ij ~ c_i t_j, and each destination row lists its sources
+in ascending t, so scores climb by ~7 per level along the edge list (rows
+with c_i < 0 descend instead).  Split rows with forced small chunks then have
+chunk maxima several levels apart.  Each case asserts, on the inputs, that
+the rises happen, then compares the CUDA path with the fp64 oracle element by
+element (fp32: |err| <= 1e-5; bf16: 2e-2 + 1e-2 |ref|).  The method's
+passage: online softmax in on-chip memory (Yandex Research blog post on
+"On Efficient Scaling of GNNs via IO-Aware Layers Implementations",
+"Attention-based layers" paragraph)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_graph_attention_csr_gb300 as sga
+from sparse_graph_attention_csr_gb300 import synth
+
+from helpers import TORCH_DT, compare, dev
+
+pytestmark = pytest.mark.gpu
+
+RISE = 8.0 * math.log(2.0)   # natural-log growth that triggers a rescale
+
+
+def rounded(x, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(TORCH_DT[dtype])
+    return t, t.to(torch.float64).numpy()
+
+
+def staircase_graph(rng, N, mean_deg, t, hubs=()):
+    """Rows with Poisson(mean_deg) random sources plus a self-loop, each row's
+    sources ordered by ascending level t (a valid CSR: the order of a row's
+    entries is free)."""
+    rows = []
+    for i in range(N):
+        r = set(rng.integers(0, N, rng.poisson(mean_deg)).tolist()) | {i}
+        rows.append(r)
+    for h, d in hubs:
+        rows[h] = set(rng.integers(0, N, d).tolist()) | {h}
+    rows = [sorted(r, key=lambda j: (t[j], j)) for r in rows]
+    indptr = np.zeros(N + 1, np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in rows])
+    return indptr, np.array([j for r in rows for j in r], np.int32)
+
+
+def staircase_qk(rng, N, H, D, levels, neg_frac, noise=0.15):
+    """Per-node levels t_j, row signs/scales c_i, and Q, K with
+    q_i . k_j / sqrt(D) = c_i (t_j + 0.3 h) + small cross terms."""
+    t = np.asarray(levels)[rng.integers(0, len(levels), N)] + noise * rng.standard_normal(N)
+    c = rng.uniform(0.9, 1.1, N)
+    c[rng.random(N) < neg_frac] *= -1.0
+    u = rng.standard_normal((H, D))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    s4 = D ** 0.25
+    Q = c[:, None, None] * u[None] * s4 + 0.02 * rng.standard_normal((N, H, D))
+    th = t[:, None] + 0.3 * np.arange(H)[None, :]
+    K = th[:, :, None] * u[None] * s4 + 0.02 * rng.standard_normal((N, H, D))
+    return t, Q, K
+
+
+def rescale_rows(indptr, indices, Q, K):
+    """Rows (head 0) in which some edge's score exceeds the maximum of all
+    earlier edges of the row by more than 8 ln 2."""
+    D = Q.shape[2]
+    n = 0
+    for i in range(len(indptr) - 1):
+        b, e = indptr[i], indptr[i + 1]
+        if e - b < 2:
+            continue
+        s = K[indices[b:e], 0, :] @ Q[i, 0, :] / math.sqrt(D)
+        run = np.maximum.accumulate(s)
+        if np.any(s[1:] > run[:-1] + RISE):
+            n += 1
+    return n
+
+
+def run_gt_case(indptr, indices, Qf, Kf, V, dO, H, D, dtype, split=0, chunk=0, backward=True):
+    Q, qf = rounded(Qf, dtype)
+    K, kf = rounded(Kf, dtype)
+    Vt, vf = rounded(V, dtype)
+    dOt, dof = rounded(dO, dtype)
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, TORCH_DT[dtype], split_threshold=split, chunk_len=chunk)
+    gQ, gK, gV, gdO = dev(Q), dev(K), dev(Vt), dev(dOt)
+    out, lse = sga.gt_attn_fwd(plan, gQ, gK, gV)
+    ro, rl = oracle.gt_fwd(indptr, indices, qf, kf, vf)
+    compare(out, ro, dtype, "out")
+    compare(lse, rl, dtype, "lse")
+    if backward:
+        dQ, dK, dV = sga.gt_attn_bwd(plan, gQ, gK, gV, out, lse, gdO)
+        rq, rk, rv = oracle.gt_bwd(indptr, indices, qf, kf, vf, dof)
+        compare(dQ, rq, dtype, "dQ")
+        compare(dK, rk, dtype, "dK")
+        compare(dV, rv, dtype, "dV")
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0
+    return qf, kf
+
+
+# fp32 keeps |s| below ~4: the recomputed weights of the backward carry an
+# fp32 rounding that grows with |s| (and with |lse|), and the 1e-5 bound leaves
+# room for no more; bf16 spans four levels
+LEVELS = {"f32": (-3.5, 3.5), "bf16": (-10.5, -3.5, 3.5, 10.5)}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("H,D", [(4, 32), (1, 32), (2, 64), (1, 128), (4, 128), (8, 128), (3, 64)])
+def test_gt_rising_scores_every_lane_layout(dtype, H, D):
+    """Rows of 4..32-lane groups and 1..8 chunks per lane, scores climbing by
+    ~7 per level along each row; split rows (threshold 40, chunks of 16) whose
+    chunk maxima are levels apart; 15% of rows descending."""
+    rng = np.random.default_rng(100 * H + D + (7 if dtype == "bf16" else 0))
+    N = 600
+    t, Qf, Kf = staircase_qk(rng, N, H, D, LEVELS[dtype], neg_frac=0.15)
+    # mean degree 30: most rows take more than one warp step (up to 32 edges)
+    indptr, indices = staircase_graph(rng, N, 30, t, hubs=[(5, 400), (321, 150), (599, 90)])
+    V = rng.standard_normal((N, H, D))
+    dO = rng.standard_normal((N, H, D))
+    qf, kf = run_gt_case(indptr, indices, Qf, Kf, V, dO, H, D, dtype, split=40, chunk=16)
+    assert rescale_rows(indptr, indices, qf, kf) > 0.4 * N
+    # unsplit as well (the hub rows then run as whole rows of many steps)
+    run_gt_case(indptr, indices, Qf, Kf, V, dO, H, D, dtype, backward=False)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_gt_split_chunks_with_far_apart_maxima(dtype):
+    """A handful of hub rows of ~1000 edges cut into chunks of 16: along each
+    row the chunk maxima climb through every level, so the merge weights
+    chunks by 2^(m_c - m) with m_c up to ~20 natural units below m; one hub
+    descends, so its first chunk holds the maximum."""
+    rng = np.random.default_rng(41 if dtype == "f32" else 42)
+    N, H, D = 1200, 2, 64
+    t, Qf, Kf = staircase_qk(rng, N, H, D, LEVELS[dtype], neg_frac=0.0)
+    hubs = [(h, 1000) for h in (0, 17, 600, 1199)]
+    Qf[17] *= -1.0
+    indptr, indices = staircase_graph(rng, N, 3, t, hubs=hubs)
+    V = rng.standard_normal((N, H, D))
+    dO = rng.standard_normal((N, H, D))
+    qf, kf = run_gt_case(indptr, indices, Qf, Kf, V, dO, H, D, dtype, split=64, chunk=16)
+    # chunk maxima of a climbing hub are far apart
+    b, e = indptr[0], indptr[1]
+    s = kf[indices[b:e], 0, :] @ qf[0, 0, :] / math.sqrt(D)
+    cmax = [s[x:x + 16].max() for x in range(0, e - b, 16)]
+    assert max(cmax) - min(cmax) > RISE
+
+
+def test_gt_workload_recipe_with_scaled_scores():
+    """The lognormal workload's recipe (bf16, H=4, D=128, hub row) with Q and
+    K scaled so scores have standard deviation ~4: rises past 2^8 happen on
+    ordinary random rows too, without any ordering."""
+    w = synth.small_workload(3)
+    indptr, indices = synth.make_graph(w)
+    x = synth.gt_inputs(w)
+    # Q, K ~ N(0, 1/D): scaling both by sqrt(4 D) gives q.k/sqrt(D) ~ N(0, 16)
+    s = math.sqrt(4.0 * w.D)
+    Qf = x["Q"][1] * s
+    Kf = x["K"][1] * s
+    qf, kf = run_gt_case(indptr, indices, Qf, Kf, x["V"][1], x["dOut"][1], w.H, w.D, "bf16",
+                         split=48, chunk=16)
+    assert rescale_rows(indptr, indices, qf, kf) > 0.1 * w.N
+
+
+@pytest.mark.parametrize("dtype,ascale", [("f32", 4.0), ("bf16", 12.0)])
+def test_gatv2_rising_scores(dtype, ascale):
+    """GATv2 with a large attention vector (scores spread over tens of units)
+    and each row's sources ordered by ascending score; hub rows split into
+    chunks of 24.  Forward element by element; backward with the tolerances
+    of the GATv2 parity tests."""
+    rng = np.random.default_rng(77 if dtype == "f32" else 78)
+    N, F, H, D = 500, 64, 2, 64
+    lim = math.sqrt(6.0 / (F + H * D))
+    X, xf = rounded(rng.standard_normal((N, F)), dtype)
+    Wl, wlf = rounded(rng.uniform(-lim, lim, (F, H * D)), dtype)
+    Wr, wrf = rounded(rng.uniform(-lim, lim, (F, H * D)), dtype)
+    a, af = rounded(rng.standard_normal((H, D)) * ascale / math.sqrt(D), dtype)
+    dO, dof = rounded(rng.standard_normal((N, H, D)), dtype)
+    # random graph, then each row ordered by its head-0 score on the stored projections
+    base_ptr, base_idx = staircase_graph(rng, N, 12, np.zeros(N), hubs=[(3, 350), (444, 120)])
+    FL, FR, _, _ = oracle.gatv2_fwd(base_ptr, base_idx, xf, wlf, wrf, af, 0.2, store=dtype)
+    indices = base_idx.copy()
+    n_rise = 0
+    for i in range(N):
+        b, e = base_ptr[i], base_ptr[i + 1]
+        z = FL[i, 0][None, :] + FR[base_idx[b:e], 0, :]
+        sc = (np.where(z > 0, z, 0.2 * z) * af[0][None, :]).sum(-1)
+        order = np.argsort(sc, kind="stable")
+        indices[b:e] = base_idx[b:e][order]
+        ss = sc[order]
+        if e - b >= 2 and np.any(ss[1:] > np.maximum.accumulate(ss)[:-1] + RISE):
+            n_rise += 1
+    assert n_rise > 0.3 * N
+    ip, ix = dev(torch.from_numpy(base_ptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, TORCH_DT[dtype], F=F, split_threshold=50, chunk_len=24)
+    gX, gWl, gWr, ga, gdO = (dev(v) for v in (X, Wl, Wr, a, dO))
+    gFL, gFR, out, lse = sga.gatv2_fwd(plan, gX, gWl, gWr, ga, 0.2)
+    rFL, rFR, ro, rl = oracle.gatv2_fwd(base_ptr, indices, xf, wlf, wrf, af, 0.2, store=dtype)
+    compare(out, ro, dtype, "out")
+    compare(lse, rl, dtype, "lse")
+    dX, dWl, dWr, da = sga.gatv2_bwd(plan, gX, gWl, gWr, ga, gFL, gFR, out, lse, gdO, 0.2)
+    g = oracle.gatv2_bwd(base_ptr, indices, xf, wlf, wrf, af, dof, 0.2, store=dtype)
+    sl = oracle.gatv2_branch_slack(base_ptr, indices, xf, wlf, wrf, af, dof, 0.2, store=dtype)
+    rt, nm = (1e-5, 4e-6) if dtype == "f32" else (None, 0.0)
+    compare(dX, g["dX"], dtype, "dX", rtol=rt, norm=nm, slack=sl["dX"])
+    compare(dWl, g["dW_l"], dtype, "dW_l", rtol=rt, norm=nm, slack=sl["dW_l"])
+    compare(dWr, g["dW_r"], dtype, "dW_r", rtol=rt, norm=nm, slack=sl["dW_r"])
+    compare(da, g["da"], dtype, "da", rtol=rt, norm=nm, slack=sl["da"])
+    assert plan.device_error() == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_block_sparse_tiles_with_rising_levels(D):
+    """Block-sparse plan on an SBM whose sources climb by one level (7
+    natural units) every 64 columns (four 16-column tiles, the group the tile
+    kernel takes at once): later tile groups exceed the running maximum by
+    more than 2^8; one row panel in eight descends.  Residual (inter-
+    community) edges merge with the tiles by log-sum-exp."""
+    rng = np.random.default_rng(D)
+    N, H = 4096, 2
+    indptr, indices = synth.graph_sbm(np.random.default_rng(9), N, 256, 0.15, 4)
+    level = ((np.arange(N) % 256) // 64).astype(np.float64)
+    t = (level - 1.5) * 7.0 + 0.15 * rng.standard_normal(N)
+    u = rng.standard_normal((H, D))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    s4 = D ** 0.25
+    c = np.ones(N)
+    c[(np.arange(N) // 128) % 8 == 3] = -1.0
+    Qf = c[:, None, None] * u[None] * s4 + 0.02 * rng.standard_normal((N, H, D))
+    Kf = t[:, None, None] * u[None] * s4 + 0.02 * rng.standard_normal((N, H, D))
+    V = rng.standard_normal((N, H, D))
+    dO = rng.standard_normal((N, H, D))
+    Q, qf = rounded(Qf, "bf16")
+    K, kf = rounded(Kf, "bf16")
+    Vt, vf = rounded(V, "bf16")
+    dOt, dof = rounded(dO, "bf16")
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, tile_min_nnz=16)
+    inf = plan.info()
+    assert inf["n_tiles"] > 0 and inf["E_residual"] < 0.25 * len(indices)
+    # within a row's kept tiles (ascending columns) scores climb past 2^8
+    i = 5
+    srcs = indices[indptr[i]:indptr[i + 1]]
+    own = srcs[srcs // 256 == i // 256]
+    s = kf[own, 0, :] @ qf[i, 0, :] / math.sqrt(D)
+    assert s.max() - s[(own % 256) < 64].max() > 2 * RISE
+    gQ, gK, gV, gdO = dev(Q), dev(K), dev(Vt), dev(dOt)
+    out, lse = sga.gt_attn_fwd(plan, gQ, gK, gV)
+    ro, rl = oracle.gt_fwd(indptr, indices, qf, kf, vf)
+    compare(out, ro, "bf16", "out")
+    compare(lse, rl, "bf16", "lse")
+    dQ, dK, dV = sga.gt_attn_bwd(plan, gQ, gK, gV, out, lse, gdO)
+    rq, rk, rv = oracle.gt_bwd(indptr, indices, qf, kf, vf, dof)
+    compare(dQ, rq, "bf16", "dQ")
+    compare(dK, rk, "bf16", "dK")
+    compare(dV, rv, "bf16", "dV")
+    torch.cuda.synchronize()
+    assert plan.device_error() == 0

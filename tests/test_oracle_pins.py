@@ -211,6 +211,47 @@ def test_gatv2_backward_matches_autograd():
     np.testing.assert_allclose(g["da"], ta.grad.numpy(), atol=1e-11)
 
 
+def straight_through(Y, store):
+    """Y rounded to the storage dtype in value, the identity in gradient."""
+    r = Y.detach().float()
+    r = r.to(torch.bfloat16).double() if store == "bf16" else r.double()
+    return Y + (r - Y).detach()
+
+
+@pytest.mark.parametrize("store", ["bf16", "f32"])
+def test_gatv2_backward_with_stored_projections_matches_straight_through_autograd(store):
+    """store='bf16'/'f32' in the backward: the edge stage runs on the rounded
+    projections (branches decided on them) and the rounding passes gradients
+    unchanged.  torch autograd of the dense form with a straight-through
+    rounding step must agree; the projections are made large enough that the
+    rounding moves the gradients far beyond the tolerance (a backward that
+    ignored the storage mode fails)."""
+    rng = np.random.default_rng(24 if store == "bf16" else 25)
+    N, F, H, D = 27, 6, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.3)
+    X = rng.standard_normal((N, F)) * 3.0
+    Wl = rng.standard_normal((F, H * D)); Wr = rng.standard_normal((F, H * D))
+    a = rng.standard_normal((H, D)); dO = rng.standard_normal((N, H, D))
+    g = oracle.gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, 0.2, store=store)
+    g64 = oracle.gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, 0.2)
+    tX, tWl, tWr, ta = (torch.from_numpy(x).requires_grad_() for x in (X, Wl, Wr, a))
+    FL = straight_through(tX @ tWl, store).reshape(N, H, D)
+    FR = straight_through(tX @ tWr, store).reshape(N, H, D)
+    mask = dense_mask(indptr, indices, N)
+    z = FL[:, None] + FR[None, :]
+    e = (torch.nn.functional.leaky_relu(z, 0.2) * ta).sum(-1).permute(2, 0, 1)
+    e = e.masked_fill(~mask[None], float("-inf"))
+    p = torch.exp(e - torch.logsumexp(e, dim=-1)[..., None]).nan_to_num(0.0)
+    out = torch.einsum("hij,jhd->ihd", p, FR)
+    (out * torch.from_numpy(dO)).sum().backward()
+    for name, t in (("dX", tX), ("dW_l", tWl), ("dW_r", tWr), ("da", ta)):
+        ref = t.grad.numpy()
+        np.testing.assert_allclose(g[name], ref, atol=1e-10 * max(1.0, np.abs(ref).max()))
+        # the rounding matters: fp64 projections give gradients outside the check
+        # (relative ~1e-2 for bf16, ~1e-7 for fp32, both far above 1e-10)
+        assert np.abs(g64[name] - ref).max() > (1e-4 if store == "bf16" else 1e-8) * np.abs(ref).max()
+
+
 # -------------------------------------------------------- finite differences
 
 def test_gt_backward_finite_differences():
