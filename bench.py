@@ -5,7 +5,7 @@ Default workload: the Graph Transformer layer on the largest graph, an R-MAT
 graph with super nodes (N=2^20, 32.4M edges with self-loops, H=4, D=64, bf16,
 forward + backward).  ``--config k`` runs one of the other synthetic
 workloads (1: GT forward fp32 ER; 2: GATv2 Chung-Lu; 3: GT lognormal;
-5: GT block-dense SBM).
+5: GT block-dense SBM; 6: min aggregation, lognormal graph, 512 features).
 
 One step = forward + backward of the layer (forward only for workload 1) over
 the whole graph, inputs resident on the device, L2 flushed (a write of twice
@@ -47,6 +47,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 GT_KERNELS = ["gt_fwd", "gt_fwd_merge", "bsr_fwd", "bsr_bwd_delta", "gt_bwd_dq", "gt_bwd_dkdv",
               "gt_bwd_merge", "bsr_bwd_dq", "bsr_bwd_dkdv"]
+AGG_KERNELS = ["agg_fwd", "agg_fwd_merge", "agg_bwd", "agg_bwd_cast"]
 GATV2_KERNELS = ["gatv2_proj", "gatv2_fwd", "gatv2_fwd_merge", "gatv2_bwd_dst", "gatv2_bwd_src",
                  "gatv2_bwd_merge", "gatv2_bwd_dx", "gatv2_bwd_dw", "gatv2_bwd_reduce"]
 
@@ -59,13 +60,16 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["native", "reference"], default="native")
-    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--config", type=int, default=4, choices=[1, 2, 3, 4, 5, 6])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="target CPU time of the oracle baseline sample")
     p.add_argument("--split-threshold", type=int, default=0)
     p.add_argument("--chunk-len", type=int, default=0)
+    p.add_argument("--schedule", type=int, default=0, choices=[0, 1, 2],
+                   help="Graph Transformer forward thread mapping: 0 edge stream, "
+                        "1 feature-parallel, 2 edge-parallel scores + feature-parallel aggregation")
     p.add_argument("--tile-min-nnz", type=int, default=0,
                    help="> 0: block-sparse tensor-core forward (GT, bf16) with this tile threshold")
     p.add_argument("--nodes", type=int, default=0,
@@ -184,6 +188,10 @@ def algorithmic_bytes(kernel: str, N: int, E: int, H: int, D: int, F: int, s: in
         return ptr + idx + 2 * row + 4 * N * H + E * HD * s + row + 4 * N * H
     if kernel == "gatv2_bwd_src":
         return ptr + idx + row + E * (2 * HD * s + 8 * H) + row
+    if kernel == "agg_fwd":          # gathered rows; out and the winning source written
+        return ptr + idx + E * HD * s + row + 4 * N * HD
+    if kernel == "agg_bwd":          # arg and dOut read, dX written
+        return 4 * N * HD + row + row
     if kernel == "gatv2_proj":
         return N * F * s + F * HD * s + row
     if kernel == "gatv2_bwd_dx":
@@ -259,7 +267,8 @@ def traffic_for(kernel: str, workload: str):
 class Workload:
     """Host inputs (pinned), device inputs, plan and step functions."""
 
-    def __init__(self, key: int, device, split_threshold=0, chunk_len=0, tile_min_nnz=0, nodes=0):
+    def __init__(self, key: int, device, split_threshold=0, chunk_len=0, tile_min_nnz=0, nodes=0,
+                 schedule=0):
         import sparse_graph_attention_csr_gb300 as sga
         self.sga = sga
         self.w = synth.WORKLOADS[key]
@@ -280,6 +289,9 @@ class Workload:
                 x["dOut"] = synth.round_to(synth.normal(w.seed, synth.STREAM_DOUT, (w.N, w.H, w.D)),
                                            w.dtype)
             self.in_names = ["Q", "K", "V"] + (["dOut"] if w.backward else [])
+        elif w.layer.startswith("agg"):
+            x = synth.agg_inputs(w)
+            self.in_names = ["X", "dOut"]
         else:
             x = synth.gatv2_inputs(w)
             self.in_names = ["X", "W_l", "W_r", "a", "dOut"]
@@ -293,7 +305,10 @@ class Workload:
         t0 = time.perf_counter()
         self.plan = sga.Plan(self.ip, self.ix, w.H, w.D, self.tdt, F=F,
                              split_threshold=split_threshold, chunk_len=chunk_len,
-                             tile_min_nnz=tile_min_nnz)
+                             tile_min_nnz=tile_min_nnz,
+                             layer=sga.SGA_LAYER_MINMAX if w.layer.startswith("agg")
+                             else sga.SGA_LAYER_ATTENTION, schedule=schedule)
+        self.schedule = schedule
         torch.cuda.synchronize()
         self.plan_ms = (time.perf_counter() - t0) * 1e3
         self.tile_min_nnz = tile_min_nnz
@@ -302,6 +317,8 @@ class Workload:
 
     @property
     def kernels(self):
+        if self.w.layer.startswith("agg"):
+            return AGG_KERNELS
         return GT_KERNELS if self.w.layer == "gt" else GATV2_KERNELS
 
     def forward(self, d):
@@ -310,6 +327,9 @@ class Workload:
         if w.layer == "gt":
             out, lse = sga.gt_attn_fwd(self.plan, d["Q"], d["K"], d["V"])
             return {"out": out, "lse": lse}, (out, lse)
+        if w.layer.startswith("agg"):
+            out, arg = sga.agg_minmax_fwd(self.plan, d["X"], w.layer[4:])
+            return {"out": out, "arg": arg}, arg
         FL, FR, out, lse = sga.gatv2_fwd(self.plan, d["X"], d["W_l"], d["W_r"], d["a"], 0.2)
         return {"out": out, "lse": lse}, (FL, FR, out, lse)
 
@@ -320,6 +340,8 @@ class Workload:
             out, lse = saved
             dQ, dK, dV = sga.gt_attn_bwd(self.plan, d["Q"], d["K"], d["V"], out, lse, d["dOut"])
             return {"dQ": dQ, "dK": dK, "dV": dV}
+        if w.layer.startswith("agg"):
+            return {"dX": sga.agg_minmax_bwd(self.plan, saved, d["dOut"])}
         FL, FR, out, lse = saved
         dX, dWl, dWr, da = sga.gatv2_bwd(self.plan, d["X"], d["W_l"], d["W_r"], d["a"], FL, FR,
                                          out, lse, d["dOut"], 0.2)
@@ -391,6 +413,11 @@ def row_sample(indptr, indices, n_rows, rng):
 def oracle_step(wl: synth.Workload, host64, ptr, idx, nodes):
     """The oracle's forward(+backward) of the workload's layer on a (sub)graph."""
     import oracle
+    if wl.layer.startswith("agg"):
+        _, arg = oracle.agg_fwd(ptr, idx, host64["X"][nodes], wl.layer[4:])
+        if wl.backward:
+            oracle.agg_bwd(arg, host64["dOut"][nodes])
+        return
     if wl.layer == "gt":
         Q, K, V = (host64[k][nodes] for k in ("Q", "K", "V"))
         oracle.gt_fwd(ptr, idx, Q, K, V)
@@ -462,7 +489,8 @@ def run_reference(args, ws, rank):
     import oracle
     wl = synth.WORKLOADS[args.config]
     indptr, indices = synth.make_graph(wl)
-    x = synth.gt_inputs(wl) if wl.layer == "gt" else synth.gatv2_inputs(wl)
+    x = (synth.gt_inputs(wl) if wl.layer == "gt" else
+         synth.agg_inputs(wl) if wl.layer.startswith("agg") else synth.gatv2_inputs(wl))
     host64 = {k: v[1] for k, v in x.items()}
     if wl.layer == "gt" and not wl.backward:
         host64["dOut"] = np.zeros((wl.N, wl.H, wl.D))
@@ -506,7 +534,8 @@ def run_native(args, ws, rank, local):
     from sparse_graph_attention_csr_gb300 import build as sga_build
     sga_build.build()
     dev = torch.device("cuda", local)
-    wl = Workload(args.config, dev, args.split_threshold, args.chunk_len, args.tile_min_nnz, args.nodes)
+    wl = Workload(args.config, dev, args.split_threshold, args.chunk_len, args.tile_min_nnz, args.nodes,
+                  args.schedule)
     w = wl.w
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -667,7 +696,8 @@ def run_native(args, ws, rank, local):
                    "l2": "flushed before every step (write of 2x L2), outside the timed interval",
                    "parallelism": f"replicas x{ws}",
                    "plan_build_ms": round(wl.plan_ms, 2),
-                   "tile_min_nnz": wl.tile_min_nnz},
+                   "tile_min_nnz": wl.tile_min_nnz,
+                   "schedule": ["stream", "feature", "bilevel"][wl.schedule]},
         "roofline": roof,
         "memory": memory,
         "block_sparse": bsr,

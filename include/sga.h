@@ -59,13 +59,34 @@ typedef enum { SGA_F32 = 0, SGA_BF16 = 1 } sga_dtype;
 /* Opaque, host-owned plan for one graph and one layer shape. */
 typedef struct sga_plan sga_plan;
 
+/* Layer a plan serves (its workspace layout). */
+typedef enum {
+    SGA_LAYER_ATTENTION = 0,  /* Graph Transformer (in_features = 0) or GATv2 (in_features > 0) */
+    SGA_LAYER_MINMAX = 1      /* min / max neighbourhood aggregation (agg_minmax_fwd/bwd) */
+} sga_layer;
+
 /* Plan options.  Zero (or a NULL pointer) selects the default of each field. */
 typedef struct {
     int32_t split_threshold;  /* rows of degree > this are split (default 256) */
     int32_t chunk_len;        /* edges per chunk of a split row (default 128) */
     int32_t in_features;      /* GATv2 input width F; 0 for a Graph Transformer plan */
     int32_t tile_min_nnz;     /* > 0: block-sparse tensor-core forward, see below; 0: off */
+    int32_t layer;            /* sga_layer (default SGA_LAYER_ATTENTION) */
+    int32_t schedule;         /* sga_schedule of the Graph Transformer CSR forward (default 0) */
 } sga_plan_opts;
+
+/* Thread mapping of the Graph Transformer forward over the CSR (the backward
+ * and the GATv2 passes always use the edge stream).  The pages contrast
+ * neighbour-parallel with feature-parallel kernels (IO-aware layers arXiv
+ * abstract) and schedule the score and aggregation stages with different
+ * mappings (DF-GNN abstract, "bi-level thread scheduling").  Results agree
+ * with the default up to fp32 rounding order. */
+typedef enum {
+    SGA_SCHED_STREAM = 0,   /* warps over rows, groups of lanes over a row's features, several
+                               neighbours per step staged through a shared-memory ring */
+    SGA_SCHED_FEATURE = 1,  /* warp per row, lanes over features, one neighbour at a time, direct loads */
+    SGA_SCHED_BILEVEL = 2   /* scores edge-parallel (a lane per edge), aggregation feature-parallel */
+} sga_schedule;
 
 /* Build a plan: validates the CSR on the device (indptr[0] = 0, monotone,
  * indptr[N] = E, 0 <= indices < N), builds the transposed CSR (sources ->
@@ -137,6 +158,72 @@ sga_status gatv2_bwd(const sga_plan *plan, const int32_t *indptr, const int32_t 
                      const void *FL, const void *FR, const void *out, const float *lse,
                      const void *dOut, int64_t N, int64_t E, int F, int H, int D, float slope,
                      sga_dtype dt, void *dX, void *dW_l, void *dW_r, void *da, void *stream);
+
+/* ---- min / max aggregation ------------------------------------------------
+ *
+ * The degree-aware reduction layer of "On Efficient Scaling of GNNs via
+ * IO-Aware Layers Implementations" (arXiv abstract: degree-aware reduction
+ * kernels; Yandex Research blog post, "Aggregation layers" paragraph):
+ * out_i[f] = max (or min) over the sources j of row i of X_j[f], for every
+ * element f of the node rows ([N, H, D] tensors read as [N, H*D]).  Needs a
+ * plan built with opts->layer = SGA_LAYER_MINMAX (same N, E, H, D, dt).
+ * arg[N, H*D] (int32, caller-owned, 16-byte aligned) receives the source node
+ * that holds each extreme: the first edge of the row in CSR order among equal
+ * values.  An empty row gives out = 0 and arg = -1.  Values must not be NaN.
+ * Rows above the split threshold are cut into chunks whose partial extremes
+ * are merged in chunk order; out and arg are exact (bit-identical to the
+ * definition). */
+typedef enum { SGA_AGG_MAX = 0, SGA_AGG_MIN = 1 } sga_agg_op;
+
+sga_status agg_minmax_fwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                          const void *X, int64_t N, int64_t E, int H, int D, sga_dtype dt,
+                          sga_agg_op op, void *out, int32_t *arg, void *stream);
+
+/* Backward of the min / max aggregation: dX_j[f] = sum of dOut_i[f] over the
+ * rows i whose element f was won by j (arg from the forward).  One fp32
+ * atomic add per (i, f) into an fp32 accumulator (dX itself for fp32 layers,
+ * the plan's workspace for bf16 layers, then rounded to bf16), so elements
+ * that receive several contributions are sums in a run-dependent order. */
+sga_status agg_minmax_bwd(const sga_plan *plan, const int32_t *arg, const void *dOut, int64_t N,
+                          int H, int D, sga_dtype dt, void *dX, void *stream);
+
+/* ---- graph reordering ------------------------------------------------------
+ *
+ * "On Efficient Scaling of GNNs via IO-Aware Layers Implementations" (arXiv
+ * abstract) studies graph reordering, which benefits neighbour-parallel
+ * (gather-dominated) kernels: relabelled so that rows processed together
+ * share neighbours, a graph's gathers hit the cache more often.  The pages
+ * name no ordering; two are provided.  A user relabels once (graph and node
+ * tensors) and runs the layers on the relabelled graph; the outputs are the
+ * relabelled outputs (sga_permute_rows with inverse = 1 maps them back). */
+typedef enum {
+    SGA_ORDER_DEGREE = 0,  /* descending in-degree (times a node is gathered), ties by id */
+    SGA_ORDER_RCM = 1      /* reverse Cuthill-McKee on the symmetrised graph: breadth-first
+                              levels from each component's start node (least degree, least
+                              id; components in that order), a level ordered by the position
+                              of each node's earliest-placed neighbour in the level before,
+                              then degree, then id; the whole order reversed.  Degree =
+                              row degree + transposed degree (CSR entries) */
+} sga_order;
+
+/* perm[N] (device, int32) receives the new id of every node.  Exact and
+ * deterministic (bit-identical to the sequential definition).  Allocates its
+ * temporary device memory, frees it before returning, synchronises `stream`. */
+sga_status sga_reorder(const int32_t *indptr, const int32_t *indices, int64_t N, int64_t E,
+                       sga_order method, int32_t *perm, void *stream);
+
+/* The relabelled graph: new row perm[v] holds the sources of old row v as
+ * perm[j], in their original order.  new_indptr[N+1], new_indices[E]: device,
+ * caller-owned.  Synchronises `stream`. */
+sga_status sga_relabel_csr(const int32_t *indptr, const int32_t *indices, int64_t N, int64_t E,
+                           const int32_t *perm, int32_t *new_indptr, int32_t *new_indices,
+                           void *stream);
+
+/* Permute the rows of a node tensor (row_bytes a multiple of 16, buffers
+ * 16-byte aligned and distinct): dst[perm[v]] = src[v], or with inverse = 1
+ * dst[v] = src[perm[v]].  Asynchronous on `stream`. */
+sga_status sga_permute_rows(const void *src, int64_t N, int64_t row_bytes, const int32_t *perm,
+                            int inverse, void *dst, void *stream);
 
 const char *sga_status_string(sga_status s);
 
@@ -252,7 +339,9 @@ typedef enum {
     SGA_KERN_GATV2_BWD_DX = 12, SGA_KERN_GATV2_BWD_DW = 13, SGA_KERN_GATV2_BWD_REDUCE = 14,
     SGA_KERN_BSR_FWD = 15, SGA_KERN_BSR_BWD_DELTA = 16, SGA_KERN_BSR_BWD_DQ = 17,
     SGA_KERN_BSR_BWD_DKDV = 18,
-    SGA_KERN_COUNT = 19
+    SGA_KERN_AGG_FWD = 19, SGA_KERN_AGG_FWD_MERGE = 20, SGA_KERN_AGG_BWD = 21,
+    SGA_KERN_AGG_BWD_CAST = 22,
+    SGA_KERN_COUNT = 23
 } sga_kernel_id;
 
 /* Time one kernel kind with CUDA events recorded on the launching stream

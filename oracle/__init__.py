@@ -79,6 +79,9 @@ def _load():
                                   _F64P, _dbl, _int, _F64P, _F64P, _F64P, _F64P, _F64P, _F64P,
                                   _F64P], _int),
             "oracle_round_bf16": ([_dbl], _dbl),
+            "oracle_agg_fwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _I32P], _int),
+            "oracle_agg_bwd": ([_i64, _int, _I32P, _F64P, _F64P], _int),
+            "oracle_rcm": ([_i64, _I32P, _I32P, _I32P], _int),
             "oracle_gatv2_branch_slack": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P,
                                            _F64P, _F64P, _dbl, _int, _dbl, _F64P, _F64P, _F64P,
                                            _F64P, _F64P], _int),
@@ -285,6 +288,75 @@ def gatv2_branch_slack(indptr, indices, X, Wl, Wr, a, dO, slope=0.2, store="bf16
                                              float(slope), _STORE[store], float(tau), dO,
                                              sX, sWl, sWr, sda), "gatv2_branch_slack")
     return {"dX": sX, "dW_l": sWl, "dW_r": sWr, "da": sda}
+
+
+# ------------------------------------------------------- min / max aggregation
+
+def agg_fwd(indptr, indices, X, op="max"):
+    """(out, arg) of the min / max aggregation over [N, ...] node rows (any
+    trailing shape, flattened per node): out = the extreme of the sources'
+    values per element, arg = the source of its first occurrence in CSR
+    order (-1 and out = 0 for an empty row)."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    X = _f64(X)
+    N = X.shape[0]
+    F = int(np.prod(X.shape[1:])) if X.ndim > 1 else 1
+    out = np.empty(X.shape)
+    arg = np.empty(X.shape, np.int32)
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    _check(_load().oracle_agg_fwd(N, indptr, ix, F, 1 if op == "max" else 0, X, out, arg),
+           "agg_fwd")
+    return out, arg
+
+
+def agg_bwd(arg, dO):
+    """dX: dO routed to the winning sources (sum over the rows that chose them)."""
+    arg = _i32(arg)
+    dO = _f64(dO)
+    N = dO.shape[0]
+    F = int(np.prod(dO.shape[1:])) if dO.ndim > 1 else 1
+    dX = np.empty(dO.shape)
+    _check(_load().oracle_agg_bwd(N, F, arg, dO, dX), "agg_bwd")
+    return dX
+
+
+# ------------------------------------------------------------ graph reordering
+
+def order_degree(indptr, indices):
+    """perm[v] = new id: nodes by descending in-degree (times gathered), ties
+    by ascending id."""
+    N = len(indptr) - 1
+    indeg = np.bincount(np.asarray(indices, dtype=np.int64), minlength=N)
+    order = np.lexsort((np.arange(N), -indeg))
+    perm = np.empty(N, np.int32)
+    perm[order] = np.arange(N, dtype=np.int32)
+    return perm
+
+
+def order_rcm(indptr, indices):
+    """perm[v] = new id under reverse Cuthill-McKee (queue-based, in C; see
+    oracle_rcm in oracle.c for the tie rules)."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    N = len(indptr) - 1
+    perm = np.empty(max(N, 1), np.int32)
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    _check(_load().oracle_rcm(N, indptr, ix, perm), "rcm")
+    return perm[:N]
+
+
+def relabel_csr(indptr, indices, perm):
+    """The graph under perm: new row perm[v] = old row v with sources mapped
+    through perm, in their original order."""
+    indptr = np.asarray(indptr, dtype=np.int64)
+    N = len(indptr) - 1
+    inv = np.empty(N, np.int64)
+    inv[np.asarray(perm, dtype=np.int64)] = np.arange(N)
+    deg = np.diff(indptr)[inv]
+    new_ptr = np.zeros(N + 1, np.int64)
+    new_ptr[1:] = np.cumsum(deg)
+    rows = [np.asarray(perm)[indices[indptr[inv[u]]:indptr[inv[u] + 1]]] for u in range(N)]
+    new_idx = np.concatenate(rows) if rows else np.zeros(0)
+    return new_ptr.astype(np.int32), new_idx.astype(np.int32)
 
 
 # ------------------------------------------------------------ block-sparse tiles

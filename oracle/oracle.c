@@ -726,3 +726,111 @@ int oracle_gatv2_branch_slack(int64_t N, int F, int H, int D, const int32_t *ind
     free(FL); free(FR); free(sFL); free(sFR); free(s); free(p); free(de);
     return err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Min / max neighbourhood aggregation                                       */
+/* ------------------------------------------------------------------------ */
+
+/* The degree-aware reduction layer of "On Efficient Scaling of GNNs via
+ * IO-Aware Layers Implementations" (arXiv abstract; Yandex Research blog post,
+ * "Aggregation layers" paragraph), written from its definition: for every
+ * destination row i and element f of the node rows (X [N, F]), walk the row's
+ * edges in CSR order; the first edge is taken, a later edge replaces it only
+ * when its value is strictly greater (is_max) or strictly smaller (min).
+ * out[i, f] is the extreme value, arg[i, f] the source of its first
+ * occurrence; an empty row gives out = 0 and arg = -1. */
+int oracle_agg_fwd(int64_t N, const int32_t *indptr, const int32_t *indices, int F, int is_max,
+                   const double *X, double *out, int32_t *arg) {
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t i = 0; i < N; ++i) {
+        for (int f = 0; f < F; ++f) {
+            double best = 0.0;
+            int32_t who = -1;
+            for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e) {
+                int32_t j = indices[e];
+                double v = X[(size_t)j * F + f];
+                if (who < 0 || (is_max ? v > best : v < best)) {
+                    best = v;
+                    who = j;
+                }
+            }
+            out[(size_t)i * F + f] = who < 0 ? 0.0 : best;
+            arg[(size_t)i * F + f] = who;
+        }
+    }
+    return 0;
+}
+
+/* Backward of the aggregation: dX[j, f] = sum of dO[i, f] over the rows i
+ * with arg[i, f] = j, rows taken in ascending order. */
+int oracle_agg_bwd(int64_t N, int F, const int32_t *arg, const double *dO, double *dX) {
+    for (int64_t x = 0; x < N * F; ++x) dX[x] = 0.0;
+    for (int64_t i = 0; i < N; ++i)
+        for (int f = 0; f < F; ++f) {
+            int32_t j = arg[(size_t)i * F + f];
+            if (j >= 0) dX[(size_t)j * F + f] += dO[(size_t)i * F + f];
+        }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Graph reordering                                                          */
+/* ------------------------------------------------------------------------ */
+
+static const int32_t *g_sort_deg;   /* key of the comparator below (single-threaded use) */
+
+static int cmp_deg_id(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    if (g_sort_deg[x] != g_sort_deg[y]) return g_sort_deg[x] < g_sort_deg[y] ? -1 : 1;
+    return x < y ? -1 : (x > y ? 1 : 0);
+}
+
+/* Reverse Cuthill-McKee, the queue-based algorithm as it is usually stated:
+ * degree(v) = row degree + transposed degree (CSR entries, self-loops and
+ * duplicates included); the next start is the unvisited node of least
+ * degree (least id on ties); a dequeued node appends its unvisited
+ * neighbours over both edge directions (each once), in order of ascending
+ * degree, then id; the final order is reversed: perm[v] = new id of v.  The
+ * graph reordering the IO-aware layers abstract studies names no ordering;
+ * this is the classic bandwidth-reducing one. */
+int oracle_rcm(int64_t N, const int32_t *indptr, const int32_t *indices, int32_t *perm) {
+    int64_t E = indptr[N];
+    int32_t *deg = (int32_t *)calloc((size_t)(N + 1), sizeof(int32_t));
+    int32_t *t_indptr = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N + 1));
+    int32_t *t_dst = (int32_t *)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    int32_t *sorted = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N + 1));
+    int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)(N + 1));
+    char *visited = (char *)calloc((size_t)(N + 1), 1);
+    int err = (!deg || !t_indptr || !t_dst || !sorted || !order || !visited) ? -1 : 0;
+    if (!err) {
+        oracle_transpose(N, indptr, indices, t_indptr, t_dst);
+        for (int64_t v = 0; v < N; ++v)
+            deg[v] = (indptr[v + 1] - indptr[v]) + (t_indptr[v + 1] - t_indptr[v]);
+        for (int64_t v = 0; v < N; ++v) sorted[v] = (int32_t)v;
+        g_sort_deg = deg;
+        qsort(sorted, (size_t)N, sizeof(int32_t), cmp_deg_id);
+        int64_t head = 0, tail = 0, next_start = 0;
+        while (tail < N) {
+            while (visited[sorted[next_start]]) ++next_start;
+            int32_t s = sorted[next_start];
+            visited[s] = 1;
+            order[tail++] = s;
+            while (head < tail) {
+                int32_t u = order[head++];
+                int64_t first = tail;
+                for (int64_t e = indptr[u]; e < indptr[u + 1]; ++e) {
+                    int32_t w = indices[e];
+                    if (!visited[w]) { visited[w] = 1; order[tail++] = w; }
+                }
+                for (int64_t e = t_indptr[u]; e < t_indptr[u + 1]; ++e) {
+                    int32_t w = t_dst[e];
+                    if (!visited[w]) { visited[w] = 1; order[tail++] = w; }
+                }
+                qsort(order + first, (size_t)(tail - first), sizeof(int32_t), cmp_deg_id);
+            }
+        }
+        for (int64_t p = 0; p < N; ++p) perm[order[p]] = (int32_t)(N - 1 - p);
+    }
+    free(deg); free(t_indptr); free(t_dst); free(sorted); free(order); free(visited);
+    return err;
+}

@@ -27,8 +27,12 @@ KERNELS = {
     "gatv2_proj": 6, "gatv2_fwd": 7, "gatv2_fwd_merge": 8, "gatv2_bwd_dst": 9,
     "gatv2_bwd_src": 10, "gatv2_bwd_merge": 11, "gatv2_bwd_dx": 12, "gatv2_bwd_dw": 13,
     "gatv2_bwd_reduce": 14, "bsr_fwd": 15, "bsr_bwd_delta": 16, "bsr_bwd_dq": 17,
-    "bsr_bwd_dkdv": 18,
+    "bsr_bwd_dkdv": 18, "agg_fwd": 19, "agg_fwd_merge": 20, "agg_bwd": 21, "agg_bwd_cast": 22,
 }
+
+SGA_LAYER_ATTENTION, SGA_LAYER_MINMAX = 0, 1
+SGA_AGG_MAX, SGA_AGG_MIN = 0, 1
+SGA_SCHED_STREAM, SGA_SCHED_FEATURE, SGA_SCHED_BILEVEL = 0, 1, 2
 
 ARRAYS = {
     "t_indptr": 0, "t_dst": 1, "split_rows": 2, "chunk_ptr": 3, "chunk_row": 4, "chunk_beg": 5,
@@ -49,7 +53,8 @@ class SgaError(RuntimeError):
 
 class PlanOpts(ctypes.Structure):
     _fields_ = [("split_threshold", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
-                ("in_features", ctypes.c_int32), ("tile_min_nnz", ctypes.c_int32)]
+                ("in_features", ctypes.c_int32), ("tile_min_nnz", ctypes.c_int32),
+                ("layer", ctypes.c_int32), ("schedule", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -90,6 +95,9 @@ _SIGNATURES = {
                             _int),
     "sga_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "sga_noalloc_read_device_error": ([_vp, ctypes.POINTER(ctypes.c_int32)], _int),
+    "agg_minmax_fwd": ([_vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _vp, _vp, _vp],
+                       _int),
+    "agg_minmax_bwd": ([_vp, _vp, _vp, _i64, _int, _int, _int, _vp, _vp], _int),
     "sga_profile_start": ([_int], _int),
     "sga_profile_stop": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64)], _int),
 }
@@ -172,7 +180,8 @@ class Plan:
 
     def __init__(self, indptr: torch.Tensor, indices: torch.Tensor, H: int, D: int,
                  dtype=torch.bfloat16, F: int = 0, split_threshold: int = 0, chunk_len: int = 0,
-                 tile_min_nnz: int = 0, stream=None):
+                 tile_min_nnz: int = 0, layer: int = SGA_LAYER_ATTENTION,
+                 schedule: int = SGA_SCHED_STREAM, stream=None):
         _need(indptr, "indptr", torch.int32)
         _need(indices, "indices", torch.int32)
         self.indptr, self.indices = indptr, indices
@@ -181,7 +190,9 @@ class Plan:
         self.H, self.D, self.F = int(H), int(D), int(F)
         self.dtype = dtype
         self.dt = SGA_F32 if dtype == torch.float32 else SGA_BF16
-        opts = PlanOpts(int(split_threshold), int(chunk_len), int(F), int(tile_min_nnz))
+        self.layer = int(layer)
+        opts = PlanOpts(int(split_threshold), int(chunk_len), int(F), int(tile_min_nnz),
+                        self.layer, int(schedule))
         handle = ctypes.c_void_p()
         self._h = None
         _check(_lib().sga_plan_create(_ptr(indptr), _ptr(indices), self.N, self.E, self.H, self.D,
@@ -359,6 +370,32 @@ def gatv2_bwd(plan: Plan, X, W_l, W_r, a, FL, FR, out, lse, dOut, slope: float =
     return dX, dW_l, dW_r, da
 
 
+# ------------------------------------------------------- min / max aggregation
+
+def agg_minmax_fwd(plan: Plan, X, op: str = "max", out=None, arg=None, stream=None):
+    """(out, arg): out [N,H,D] = elementwise max (or min) of the sources' rows,
+    arg [N,H,D] int32 = the winning source (first edge on ties, -1 for an
+    empty row).  ``plan`` must be built with layer=SGA_LAYER_MINMAX."""
+    _need(X, "X", plan.dtype)
+    out = torch.empty_like(X) if out is None else out
+    arg = torch.empty(X.shape, dtype=torch.int32, device=X.device) if arg is None else arg
+    code = {"max": SGA_AGG_MAX, "min": SGA_AGG_MIN}[op]
+    _check(_lib().agg_minmax_fwd(plan.handle, *plan._graph()[:2], _ptr(X), plan.N, plan.E, plan.H,
+                                 plan.D, plan.dt, code, _ptr(out), _ptr(arg), _stream(stream)),
+           "agg_minmax_fwd")
+    return out, arg
+
+
+def agg_minmax_bwd(plan: Plan, arg, dOut, dX=None, stream=None):
+    """dX [N,H,D]: dOut routed to the winning sources of the forward."""
+    _need(arg, "arg", torch.int32)
+    _need(dOut, "dOut", plan.dtype)
+    dX = torch.empty_like(dOut) if dX is None else dX
+    _check(_lib().agg_minmax_bwd(plan.handle, _ptr(arg), _ptr(dOut), plan.N, plan.H, plan.D,
+                                 plan.dt, _ptr(dX), _stream(stream)), "agg_minmax_bwd")
+    return dX
+
+
 # -------------------------------------------------------------- autograd layers
 
 class GTAttention(torch.autograd.Function):
@@ -378,6 +415,23 @@ class GTAttention(torch.autograd.Function):
         Q, K, V, out, lse = ctx.saved_tensors
         dQ, dK, dV = gt_attn_bwd(ctx.plan, Q, K, V, out, lse, dOut.contiguous())
         return dQ, dK, dV, None
+
+
+class MinMaxAggregation(torch.autograd.Function):
+    """Min / max neighbourhood aggregation:
+    ``out = MinMaxAggregation.apply(X, plan, "max")``."""
+
+    @staticmethod
+    def forward(ctx, X, plan, op="max"):
+        out, arg = agg_minmax_fwd(plan, X.contiguous(), op)
+        ctx.plan = plan
+        ctx.save_for_backward(arg)
+        return out
+
+    @staticmethod
+    def backward(ctx, dOut):
+        (arg,) = ctx.saved_tensors
+        return agg_minmax_bwd(ctx.plan, arg, dOut.contiguous()), None, None
 
 
 class GATv2Attention(torch.autograd.Function):

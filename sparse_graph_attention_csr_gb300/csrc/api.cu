@@ -49,11 +49,20 @@ void compute_layout(sga_plan *p) {
         off += round256(bytes);
         return at;
     };
+    if (p->layer == SGA_LAYER_MINMAX) {
+        L.agg_val = take((size_t)p->rows.n_chunks * HD * 4);
+        L.agg_pos = take((size_t)p->rows.n_chunks * HD * 4);
+        if (p->dt == SGA_BF16) L.agg_acc = take((size_t)p->N * HD * 4);
+        L.total = off;
+        return;
+    }
     L.delta = take((size_t)p->N * p->H * 4);
+    L.lse_n = take((size_t)p->N * p->H * 4);
     L.fwd_ml = take((size_t)p->rows.n_chunks * p->H * 2 * 4);
     L.fwd_acc = take((size_t)p->rows.n_chunks * HD * 4);
     L.bwd_row = take((size_t)p->rows.n_chunks * (p->F > 0 ? 4 : 2) * HD * 4);
-    L.bwd_rowc = take((size_t)p->rows.n_chunks * p->H * 4);
+    L.bwd_rowc = take((size_t)p->rows.n_chunks * p->H * 2 * 4);
+    if (p->tiles.min_nnz > 0) L.zt = take((size_t)p->N * p->H * 4);
     L.bwd_col = take((size_t)p->cols.n_chunks * 2 * HD * 4);
     if (p->F > 0) {
         L.da_blocks = da_blocks_for(p->num_sms);
@@ -174,6 +183,9 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     if (opts) o = *opts;
     if (o.split_threshold < 0 || o.chunk_len < 0 || o.in_features < 0 || o.tile_min_nnz < 0)
         return SGA_EINVAL;
+    if (o.layer != SGA_LAYER_ATTENTION && o.layer != SGA_LAYER_MINMAX) return SGA_EINVAL;
+    if (o.layer == SGA_LAYER_MINMAX && (o.in_features != 0 || o.tile_min_nnz != 0)) return SGA_EINVAL;
+    if (o.schedule < SGA_SCHED_STREAM || o.schedule > SGA_SCHED_BILEVEL) return SGA_EINVAL;
     if (o.tile_min_nnz > 0 && (!bsr_fwd_supported(dt, D) || N > (1 << 18) || o.tile_min_nnz > 128 * 16))
         return SGA_EUNSUPPORTED;
     if (o.in_features != 0 && (o.in_features % 8 != 0 || o.in_features > 1024))
@@ -185,6 +197,8 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     p->H = H;
     p->D = D;
     p->F = o.in_features;
+    p->layer = o.layer;
+    p->schedule = o.schedule;
     p->dt = dt;
     p->split_threshold = o.split_threshold > 0 ? o.split_threshold : 256;
     p->chunk_len = o.chunk_len > 0 ? o.chunk_len : 128;
@@ -202,9 +216,9 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
         delete p;
         return st;
     }
+    p->tiles.min_nnz = o.tile_min_nnz;   // before the layout: block-sparse plans take more workspace
     compute_layout(p);
     if (o.tile_min_nnz > 0) {
-        p->tiles.min_nnz = o.tile_min_nnz;
         st = bsr_build(p, static_cast<cudaStream_t>(stream));
         sga_plan *rp = st == SGA_OK ? new (std::nothrow) sga_plan() : nullptr;
         if (st == SGA_OK && !rp) st = SGA_EINVAL;
@@ -353,6 +367,7 @@ static GtArgs gt_args(const sga_plan *p) {
         a.ws_row = ws_at<float>(p, p->layout.bwd_row);
         a.ws_rowc = ws_at<float>(p, p->layout.bwd_rowc);
         a.ws_col = ws_at<float>(p, p->layout.bwd_col);
+        a.ws_lse = ws_at<float>(p, p->layout.lse_n);
     }
     return a;
 }
@@ -360,6 +375,7 @@ static GtArgs gt_args(const sga_plan *p) {
 sga_status gt_attn_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *indices,
                        const void *Q, const void *K, const void *V, int64_t N, int64_t E, int H,
                        int D, sga_dtype dt, void *out, float *lse, void *stream) {
+    if (p && p->layer != SGA_LAYER_ATTENTION) return SGA_EINVAL;
     sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, p ? p->F : 0);
     if (st != SGA_OK) return st;
     if (!tensors_ok(N, {Q, K, V, out, lse})) return SGA_EINVAL;
@@ -396,6 +412,9 @@ sga_status gt_attn_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *
     a.V = V;
     a.out_w = out;
     a.lse_w = lse;
+    if (p->schedule != SGA_SCHED_STREAM)
+        return cuda_status(dt == SGA_F32 ? gt_fwd_sched_t<float>(a, p->schedule, s)
+                                         : gt_fwd_sched_t<__nv_bfloat16>(a, p->schedule, s));
     return cuda_status(dt == SGA_F32 ? gt_fwd_t<float>(a, s) : gt_fwd_t<__nv_bfloat16>(a, s));
 }
 
@@ -403,6 +422,7 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
                        const void *Q, const void *K, const void *V, const void *out,
                        const float *lse, const void *dOut, int64_t N, int64_t E, int H, int D,
                        sga_dtype dt, void *dQ, void *dK, void *dV, void *stream) {
+    if (p && p->layer != SGA_LAYER_ATTENTION) return SGA_EINVAL;
     sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, p ? p->F : 0);
     if (st != SGA_OK) return st;
     if (!tensors_ok(N, {Q, K, V, out, lse, dOut, dQ, dK, dV})) return SGA_EINVAL;
@@ -425,6 +445,7 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
         b.dOut = dOut;
         b.lse = lse;
         b.delta_t = ws_at<float>(p, p->layout.delta);
+        b.z_t = ws_at<float>(p, p->layout.zt);
         b.dQ = dQ;
         b.dK = dK;
         b.dV = dV;
@@ -441,11 +462,14 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
         b.n_cpanels = p->tiles.n_cpanels;
         b.d_err = p->d_err;
         cudaError_t e = cudaMemsetAsync(b.delta_t, 0, sizeof(float) * (size_t)N * H, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(b.z_t, 0, sizeof(float) * (size_t)N * H, s);
         if (e == cudaSuccess) e = launch_bsr_bwd_delta(b, s);
-        a.delta_in = b.delta_t;   // the residual rows' Delta gains the tile part
+        a.delta_in = b.delta_t;   // the residual rows' C and Z gain the tile parts
+        a.z_in = b.z_t;
         a.d_err = p->d_err;
         if (e == cudaSuccess) e = gt_bwd_t<__nv_bfloat16>(a, s);
-        b.delta = a.ws_delta;     // full Delta of every row
+        b.delta = a.ws_delta;     // full (normalised) Delta of every row
+        b.lse_n = a.ws_lse;       // and lse + ln Z
         if (e == cudaSuccess) e = launch_bsr_bwd_dq(b, s);
         if (e == cudaSuccess) e = launch_bsr_bwd_dkdv(b, s);
         return cuda_status(e);
@@ -477,6 +501,7 @@ static Gatv2Args gatv2_args(const sga_plan *p, float slope) {
         a.ws_row = ws_at<float>(p, p->layout.bwd_row);
         a.ws_col = ws_at<float>(p, p->layout.bwd_col);
         a.ws_rowc = ws_at<float>(p, p->layout.bwd_rowc);
+        a.ws_lse = ws_at<float>(p, p->layout.lse_n);
         a.ws_da = ws_at<float>(p, p->layout.da_part);
         a.ws_da_split = ws_at<float>(p, p->layout.da_split);
         a.ws_dw = ws_at<float>(p, p->layout.dw_part);
@@ -537,6 +562,55 @@ sga_status gatv2_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *in
     a.da = da;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return cuda_status(dt == SGA_F32 ? gatv2_bwd_t<float>(a, s) : gatv2_bwd_t<__nv_bfloat16>(a, s));
+}
+
+static AggArgs agg_args(const sga_plan *p) {
+    AggArgs a{};
+    a.indptr = p->indptr;
+    a.indices = p->indices;
+    a.N = p->N;
+    a.HD = p->H * p->D;
+    a.split_threshold = p->split_threshold;
+    a.num_sms = p->num_sms;
+    a.rows = p->rows;
+    a.d_err = p->d_err;
+    if (p->ws) {
+        a.ws_val = ws_at<float>(p, p->layout.agg_val);
+        a.ws_pos = ws_at<int32_t>(p, p->layout.agg_pos);
+        a.ws_acc = ws_at<float>(p, p->layout.agg_acc);
+    }
+    return a;
+}
+
+sga_status agg_minmax_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *indices,
+                          const void *X, int64_t N, int64_t E, int H, int D, sga_dtype dt,
+                          sga_agg_op op, void *out, int32_t *arg, void *stream) {
+    if (p && p->layer != SGA_LAYER_MINMAX) return SGA_EINVAL;
+    if (op != SGA_AGG_MAX && op != SGA_AGG_MIN) return SGA_EINVAL;
+    sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, 0);
+    if (st != SGA_OK) return st;
+    if (!tensors_ok(N, {X, out, arg})) return SGA_EINVAL;
+    AggArgs a = agg_args(p);
+    a.X = X;
+    a.out = out;
+    a.arg = arg;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool mx = op == SGA_AGG_MAX;
+    return cuda_status(dt == SGA_F32 ? agg_fwd_t<float>(a, mx, s) : agg_fwd_t<__nv_bfloat16>(a, mx, s));
+}
+
+sga_status agg_minmax_bwd(const sga_plan *p, const int32_t *arg, const void *dOut, int64_t N,
+                          int H, int D, sga_dtype dt, void *dX, void *stream) {
+    if (!p || p->layer != SGA_LAYER_MINMAX) return SGA_EINVAL;
+    if (N != p->N || H != p->H || D != p->D || dt != p->dt) return SGA_EINVAL;
+    if (p->layout.total > 0 && (!p->ws || p->ws_bytes < p->layout.total)) return SGA_EWORKSPACE;
+    if (!tensors_ok(N, {arg, dOut, dX})) return SGA_EINVAL;
+    AggArgs a = agg_args(p);
+    a.arg = const_cast<int32_t *>(arg);
+    a.dOut = dOut;
+    a.dX = dX;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(dt == SGA_F32 ? agg_bwd_t<float>(a, s) : agg_bwd_t<__nv_bfloat16>(a, s));
 }
 
 sga_status sga_profile_start(sga_kernel_id which) {

@@ -4,22 +4,31 @@
 // variant.  For a kept tile edge (i, j), with s = q_i . k_j / sqrt(D):
 //   p = exp(s - lse_i),  dP = dOut_i . v_j,  dS = p (dP - Delta_i),
 //   dQ_i += dS k_j / sqrt(D),  dK_j += dS q_i / sqrt(D),  dV_j += p dOut_i,
-// with Delta_i = sum over all edges of row i of p dP.
+// with Delta_i = sum over all edges of row i of p dP.  The weights are
+// normalised to sum to one per row (the residual CSR pass divides by
+// Z = sum p over all of the row's edges and stores lse + ln Z, which the dQ and
+// dK/dV passes here use): the Delta pass returns the tile parts of
+// sum p dP and of Z.
 //
 // Three passes, each one CTA of 4 warps per (panel, head); all products on
 // the tensor cores with fp32 accumulators in TMEM:
 //   Delta pass (per row panel, groups of four kept tiles = 64 sources):
-//     S = Q K^T, dP = dOut V^T, Delta_t = row sums of p dP over tile edges;
-//   dQ pass (same loop, Delta known): dS in bf16 to shared memory,
-//     dQ += dS K;
+//     S = Q K^T, dP = dOut V^T, the row sums of p dP and of p over tile edges;
+//   dQ pass (same loop, Delta known): dS to shared memory as a pair of bf16
+//     tiles (hi = bf16(dS), lo = bf16(dS - hi): about 16 significant bits),
+//     dQ += dS_hi K + dS_lo K;
 //   dK/dV pass (per column panel of 128 sources, over the row panels that
 //     keep one of its tiles, 64 rows at a time):
-//     S^T = K Q^T, dP^T = V dOut^T, P^T and dS^T to shared memory,
-//     dV += P^T dOut, dK += dS^T Q.
+//     S^T = K Q^T, dP^T = V dOut^T, P^T and the dS^T pair to shared memory,
+//     dV += P^T dOut, dK += dS^T_hi Q + dS^T_lo Q.
+// dS is split because it cancels: a row's dS sum to zero, so a single bf16
+// rounding of every term (2^-9 relative) leaves dQ and dK errors of 2^-9 times
+// the sum of |dS k| terms, which is far larger than the result where scores
+// or dP are large.  P (non-negative) and the node rows stay single bf16.
 // Node rows are staged once, 128-byte swizzled with 64-wide column atoms: the
 // K-major operand over D of the S and dP products, and as they stand the
 // MN-major operand over D of the dQ, dV and dK products (no transposes).
-// The residual CSR passes run in between (their Delta includes Delta_t), so
+// The residual CSR passes run in between (their Delta includes the tile part), so
 // each pass here adds its tile part to gradients already stored.  No atomics:
 // every output row is owned by one CTA, and the results are deterministic.
 #include "common.cuh"
@@ -79,6 +88,17 @@ __device__ __forceinline__ void mma_over_d(uint32_t tmem, uint32_t a, uint32_t b
     }
 }
 
+// Eight fp32 values as a bf16 pair: hi = the nearest bf16, lo = the nearest
+// bf16 of the remainder (x - hi is exact in fp32).
+__device__ __forceinline__ void split_bf16x8(const float *x, uint4 &hi, uint4 &lo) {
+    float h[8], r[8];
+    hi = pack<__nv_bfloat16>(x);
+    unpack<__nv_bfloat16>(hi, h);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] = x[i] - h[i];
+    lo = pack<__nv_bfloat16>(r);
+}
+
 // Add an fp32 row (from TMEM, times `scale`) to a bf16 row of D values.
 template <int D>
 __device__ __forceinline__ void add_row_from_tmem(uint32_t taddr, __nv_bfloat16 *dst, float scale, bool has) {
@@ -105,7 +125,7 @@ __device__ __forceinline__ void add_row_from_tmem(uint32_t taddr, __nv_bfloat16 
 __host__ __device__ constexpr int row_buffers(int mode) { return mode == 0 ? 1 : 2; }
 
 struct RowLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t q, g, k[2], v[2], ds, total;
+    uint32_t q, g, k[2], v[2], ds, ds_lo, total;
     __host__ __device__ RowLayout(int D, int mode) {
         const uint32_t DA = (uint32_t)D / 64, NB = (uint32_t)row_buffers(mode);
         q = 0;
@@ -115,11 +135,12 @@ struct RowLayout {   // byte offsets in dynamic shared memory (1024-aligned base
         v[0] = k[1] + DA * kGroup * 128;
         v[1] = v[0] + (NB - 1) * DA * kGroup * 128;
         ds = v[1] + DA * kGroup * 128;
-        total = ds + (mode == 1 ? 128 * 128 : 0);
+        ds_lo = ds + (mode == 1 ? 128 * 128 : 0);
+        total = ds_lo + (mode == 1 ? 128 * 128 : 0);
     }
 };
 
-// MODE 0: Delta pass (writes delta_t).  MODE 1: dQ pass (adds to dQ).
+// MODE 0: Delta pass (writes delta_t, z_t).  MODE 1: dQ pass (adds to dQ).
 template <int D, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) {
     extern __shared__ unsigned char smem_raw[];
@@ -152,7 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
     load_tile_rows<D>(sbase + L.k[0], K, a.tile_col, t0, t1, a.N, H, h);
     load_tile_rows<D>(sbase + L.v[0], V, a.tile_col, t0, t1, a.N, H, h);
     tc::cp_commit();
-    const float lse2 = in ? a.lse[row * H + h] * kLog2e : 0.f;
+    // the Delta pass uses the forward's lse and sums C and Z of its tile edges;
+    // the dQ pass uses the normalised lse + ln Z and Delta = C / Z of the row
+    const float lse2 = in ? (MODE == 0 ? a.lse : a.lse_n)[row * H + h] * kLog2e : 0.f;
     const float dl = (MODE == 1 && in) ? a.delta[row * H + h] : 0.f;
     __syncthreads();
     tc::fence_after_sync();
@@ -161,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
     const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_q = tc::idesc_bf16(128, D) | tc::kMajorMnB;
     const float scale2 = kLog2e * rsqrtf((float)D);
 
-    float dsum = 0.f;
+    float dsum = 0.f, zsum = 0.f;
     bool failed = false;
     int n_o = 0;   // dQ products issued (uniform over the CTA)
     constexpr int NB = row_buffers(MODE);
@@ -214,23 +237,31 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
                 const bool on = (bits[c >> 4] >> (c & 15)) & 1u;
                 const float p = on ? exp2f(__uint_as_float(us[i]) * scale2 - lse2) : 0.f;
                 const float dp = __uint_as_float(up[i]);
-                if (MODE == 0) dsum = fmaf(p, dp, dsum);
+                if (MODE == 0) {
+                    dsum = fmaf(p, dp, dsum);
+                    zsum += p;
+                }
                 ds[i] = p * (dp - dl);
             }
             if (MODE == 1) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(smem + L.ds + tc::sw128_offset(tid, half * 32 + c * 8, 128)) =
-                        pack<__nv_bfloat16>(ds + 8 * c);
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t o = tc::sw128_offset(tid, half * 32 + c * 8, 128);
+                    uint4 hi, lo;
+                    split_bf16x8(ds + 8 * c, hi, lo);
+                    *reinterpret_cast<uint4 *>(smem + L.ds + o) = hi;
+                    *reinterpret_cast<uint4 *>(smem + L.ds_lo + o) = lo;
+                }
             }
         }
         tc::fence_before_sync();
         if (MODE == 1) {
             tc::fence_proxy_async();
             __syncthreads();
-            if (tid == 0) {   // dQ += dS K
+            if (tid == 0) {   // dQ += dS_hi K + dS_lo K
                 tc::fence_after_sync();
                 mma_rows64(tQ, sbase + L.ds, sbase + L.k[b], idesc_q, g == 0);
+                mma_rows64(tQ, sbase + L.ds_lo, sbase + L.k[b], idesc_q, false);
                 tc::mma_commit(&mbar_o);
             }
             ++n_o;
@@ -243,7 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
         if (tid == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
         if (MODE == 1 && n_o > 0) tc::mbar_wait(&mbar_o, (n_o - 1) & 1, tc::kWaitLimit);
     } else if (MODE == 0) {
-        if (in) a.delta_t[row * H + h] = dsum;
+        if (in) {
+            a.delta_t[row * H + h] = dsum;
+            a.z_t[row * H + h] = zsum;
+        }
     } else {
         tc::fence_after_sync();
         __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dQ) + (row * H + h) * D;
@@ -257,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) 
 // ----------------------------------------------------------- column pass
 
 struct ColLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t kc, vc, qh[2], gh[2], p, ds, bits[2], lse[2], dl[2], total;
+    uint32_t kc, vc, qh[2], gh[2], p, ds, ds_lo, bits[2], lse[2], dl[2], total;
     __host__ __device__ ColLayout(int D) {
         const uint32_t DA = (uint32_t)D / 64;
         kc = 0;
@@ -268,7 +302,8 @@ struct ColLayout {   // byte offsets in dynamic shared memory (1024-aligned base
         gh[1] = gh[0] + DA * 64 * 128;
         p = gh[1] + DA * 64 * 128;
         ds = p + 128 * 128;
-        bits[0] = ds + 128 * 128;     // 8 tiles x 64 rows x 16 bits
+        ds_lo = ds + 128 * 128;
+        bits[0] = ds_lo + 128 * 128;  // 8 tiles x 64 rows x 16 bits
         bits[1] = bits[0] + 1024;
         lse[0] = bits[1] + 1024;      // 64 fp32
         lse[1] = lse[0] + 256;
@@ -323,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(BsrBwdArgs a) 
             const int i = tid - 64;
             const bool ok = row0 + i < a.N;
             const size_t off = ok ? (size_t)(row0 + i) * H + h : 0;
-            tc::cp4(sbase + L.lse[b] + i * 4, a.lse + off, ok);
+            tc::cp4(sbase + L.lse[b] + i * 4, a.lse_n + off, ok);
             tc::cp4(sbase + L.dl[b] + i * 4, a.delta + off, ok);
         }
         tc::cp_commit();
@@ -385,17 +420,21 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(BsrBwdArgs a) 
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint32_t o = tc::sw128_offset(tid, half * 32 + c * 8, 128);
+                uint4 hi, lo;
+                split_bf16x8(ds + 8 * c, hi, lo);
                 *reinterpret_cast<uint4 *>(smem + L.p + o) = pack<__nv_bfloat16>(pv + 8 * c);
-                *reinterpret_cast<uint4 *>(smem + L.ds + o) = pack<__nv_bfloat16>(ds + 8 * c);
+                *reinterpret_cast<uint4 *>(smem + L.ds + o) = hi;
+                *reinterpret_cast<uint4 *>(smem + L.ds_lo + o) = lo;
             }
         }
         tc::fence_before_sync();
         tc::fence_proxy_async();
         __syncthreads();
-        if (tid == 0) {   // dV += P^T dOut, dK += dS^T Q
+        if (tid == 0) {   // dV += P^T dOut, dK += dS^T_hi Q + dS^T_lo Q
             tc::fence_after_sync();
             mma_rows64(tV, sbase + L.p, sbase + L.gh[b], idesc_d, u == 0);
             mma_rows64(tK, sbase + L.ds, sbase + L.qh[b], idesc_d, u == 0);
+            mma_rows64(tK, sbase + L.ds_lo, sbase + L.qh[b], idesc_d, false);
             tc::mma_commit(&mbar_o);
         }
         ++n_o;

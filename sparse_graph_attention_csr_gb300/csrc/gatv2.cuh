@@ -213,10 +213,13 @@ gatv2_fwd_kernel(Gatv2Args a) {
 // Per destination row i, for each edge (j):
 //   z = fl_i + fr_j, e = a . LReLU(z), p = exp(e - lse_i), dp = dOut_i . fr_j,
 //   de = p (dp - Delta_i), dFL_i += de a * LReLU'(z), da += de LReLU(z).
-// Delta_i = sum_j p dp is accumulated in the same pass, so each de-weighted
-// sum is kept as (sum p dp x) - Delta_i (sum p x).  Warps stride over work
-// items; each block leaves one fp32 partial of da.  Split-row chunks write
-// their four partial sums and their part of Delta for the merge kernel.
+// C_i = sum_j p dp and Z_i = sum_j p are accumulated in the same pass, so
+// each de-weighted sum is kept as (sum p dp x) - Delta_i (sum p x), with the
+// weights normalised by Z at the end of the row (RowNorm, gt.cuh: Delta =
+// C / Z, sums / Z, lse + ln Z stored for the source pass).  Warps stride over
+// work items; each block leaves one fp32 partial of da.  Split-row chunks
+// write their four partial sums and their parts of C and Z for the merge
+// kernel.
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gatv2_bwd_dst_kernel(Gatv2Args a) {
@@ -255,12 +258,12 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
         // fA/fB: dFL sums (of LReLU'(z), times a after the row), gA/gB: da sums
         // (A weighted by p dp, B by p), c: Delta part
         float fl[NC][EL], go[NC][EL], fA[NC][EL], fB[NC][EL], gA[NC][EL], gB[NC][EL];
-        float c[NC], lse2[NC];
+        float c[NC], z[NC], lse2[NC];
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
 #pragma unroll
             for (int x = 0; x < EL; ++x) fl[k][x] = go[k][x] = fA[k][x] = fB[k][x] = gA[k][x] = gB[k][x] = 0.f;
-            c[k] = 0.f;
+            c[k] = z[k] = 0.f;
             lse2[k] = 0.f;
         }
         for (int step = 0; step < it.nsteps; ++step) {
@@ -285,6 +288,7 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                     const float p = ok ? exp2f(e * kLog2e - lse2[k]) : 0.f;
                     const float pdp = p * dp;
                     c[k] += pdp;
+                    z[k] += p;
                     axpy2<EL>(fA[k], pdp, dz);
                     axpy2<EL>(fB[k], p, dz);
                     axpy2<EL>(gA[k], pdp, lz);
@@ -312,6 +316,7 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
+                z[k] += __shfl_xor_sync(SGA_FULL_MASK, z[k], off);
 #pragma unroll
                 for (int x = 0; x < EL; ++x) {
                     fA[k][x] += __shfl_xor_sync(SGA_FULL_MASK, fA[k][x], off);
@@ -346,24 +351,35 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                         *reinterpret_cast<float4 *>(base + 3 * HD + x) =
                             make_float4(gB[k][x], gB[k][x + 1], gB[k][x + 2], gB[k][x + 3]);
                     }
-                    if (ch % LH == 0) a.ws_rowc[(size_t)it.item * a.H + ch / LH] = c[k];
+                    if (ch % LH == 0) {
+                        a.ws_rowc[((size_t)it.item * a.H + ch / LH) * 2] = c[k];
+                        a.ws_rowc[((size_t)it.item * a.H + ch / LH) * 2 + 1] = z[k];
+                    }
                 }
             }
         } else {
+            // normalised weights p / Z (RowNorm): Delta = C / Z, sums / Z
 #pragma unroll
-            for (int k = 0; k < NC; ++k)
+            for (int k = 0; k < NC; ++k) {
+                const RowNorm nrm(c[k], z[k]);
 #pragma unroll
-                for (int x = 0; x < EL; ++x) dacc[k][x] += gA[k][x] - c[k] * gB[k][x];
+                for (int x = 0; x < EL; ++x) dacc[k][x] += (gA[k][x] - nrm.delta * gB[k][x]) * nrm.inv_z;
+            }
             if (g == 0) {
 #pragma unroll
                 for (int k = 0; k < NC; ++k) {
                     const int ch = gl + G * k;
                     if (ch >= R) continue;
+                    const RowNorm nrm(c[k], z[k]);
                     float v[EL];
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) v[x] = fA[k][x] - c[k] * fB[k][x];
+                    for (int x = 0; x < EL; ++x) v[x] = (fA[k][x] - nrm.delta * fB[k][x]) * nrm.inv_z;
                     store_dF<T, EL>(a.ws_dfl, it.row, HD, ch, v);
-                    if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + ch / LH] = c[k];
+                    if (ch % LH == 0) {
+                        const size_t rh = (size_t)it.row * a.H + ch / LH;
+                        a.ws_delta[rh] = nrm.delta;
+                        a.ws_lse[rh] = a.lse[rh] + nrm.lse_shift;
+                    }
                 }
             }
         }
@@ -420,7 +436,7 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
     StreamArrays arr{};
     arr.rows[0] = static_cast<const uint4 *>(a.FL);
     arr.rows[1] = static_cast<const uint4 *>(a.dOut);
-    arr.sc[0] = a.lse;
+    arr.sc[0] = a.ws_lse;     // lse + ln Z of each destination (normalised weights)
     arr.sc[1] = a.ws_delta;
     arr.own[0] = static_cast<const uint4 *>(a.FR);
     EdgeStream<C> st;
@@ -504,15 +520,17 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
     st.drain();
 }
 
-// Finish split rows, one block each.  which == 0 (destination rows): Delta
-// is the sum of the chunk parts, dFL = sum fA - Delta sum fB, and the row's
-// da contribution sum gA - Delta sum gB goes to its own slot.  which == 1
-// (sources): dFR is the plain sum of the chunk partials.
+// Finish split rows, one block each.  which == 0 (destination rows): C and
+// Z are the sums of the chunk parts, normalised as in the destination pass
+// (Delta = C / Z): dFL = (sum fA - Delta sum fB) / Z, and the row's da
+// contribution (sum gA - Delta sum gB) / Z goes to its own slot; Delta and
+// lse + ln Z are stored for the source pass.  which == 1 (sources): dFR is
+// the plain sum of the chunk partials.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int which) {
     constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
     __shared__ float sh[kWarpsPerBlock][4][32 * EL];
-    __shared__ float shc[kWarpsPerBlock][32];
+    __shared__ float shc[kWarpsPerBlock][2][32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t s = blockIdx.x;
     const Partition &P = which == 0 ? a.rows : a.cols;
@@ -523,23 +541,28 @@ __global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int w
     for (int cb = 0; cb < R; cb += 32) {
         const int c = cb + lane;
         if (which == 1) {
-            float sum[1][EL], unused;
-            block_sum_chunks<EL, 1>(a.ws_col, 1, HD, nullptr, a.H, LH, c0, c1, c, c < R,
-                                    reinterpret_cast<float (*)[1][32 * EL]>(sh), shc, sum, unused);
+            float sum[1][EL], unused[2];
+            block_sum_chunks<EL, 1, 2>(a.ws_col, 1, HD, nullptr, a.H, LH, c0, c1, c, c < R,
+                                       reinterpret_cast<float (*)[1][32 * EL]>(sh), shc, sum, unused);
             if (w == 0 && c < R) store_dF<T, EL>(a.ws_dfr, row, HD, c, sum[0]);
         } else {
-            float sum[4][EL], delta;
-            block_sum_chunks<EL, 4>(a.ws_row, 4, HD, a.ws_rowc, a.H, LH, c0, c1, c, c < R, sh, shc,
-                                    sum, delta);
+            float sum[4][EL], cz[2];
+            block_sum_chunks<EL, 4, 2>(a.ws_row, 4, HD, a.ws_rowc, a.H, LH, c0, c1, c, c < R, sh,
+                                       shc, sum, cz);
             if (w == 0 && c < R) {
+                const RowNorm nrm(cz[0], cz[1]);
                 float v[EL];
 #pragma unroll
                 for (int x = 0; x < EL; ++x) {
-                    v[x] = sum[0][x] - delta * sum[1][x];
-                    a.ws_da_split[(size_t)s * HD + c * EL + x] = sum[2][x] - delta * sum[3][x];
+                    v[x] = (sum[0][x] - nrm.delta * sum[1][x]) * nrm.inv_z;
+                    a.ws_da_split[(size_t)s * HD + c * EL + x] = (sum[2][x] - nrm.delta * sum[3][x]) * nrm.inv_z;
                 }
                 store_dF<T, EL>(a.ws_dfl, row, HD, c, v);
-                if (c % LH == 0) a.ws_delta[(size_t)row * a.H + c / LH] = delta;
+                if (c % LH == 0) {
+                    const size_t rh = (size_t)row * a.H + c / LH;
+                    a.ws_delta[rh] = nrm.delta;
+                    a.ws_lse[rh] = a.lse[rh] + nrm.lse_shift;
+                }
             }
         }
         __syncthreads();

@@ -274,21 +274,24 @@ __global__ void __launch_bounds__(256) gt_fwd_merge_kernel(A a) {
 
 // Sum of chunk partials for one split row, block-cooperatively: warp w adds
 // chunks w, w+8, ... of `NCOMP` HD-wide components (component q of chunk ch at
-// part[(ch * stride_c + q) * HD]) and, if `parts_c`, the per-head scalars;
-// the 8 warp sums are then added in warp order into sum[q][x] / csum for
+// part[(ch * stride_c + q) * HD]) and, if `parts_c`, NSC per-head scalars
+// (scalar t of chunk ch, head h at parts_c[(ch * H + h) * NSC + t]); the 8
+// warp sums are then added in warp order into sum[q][x] / csum[t] for
 // lane-chunk c of the current batch (valid in warp 0).
-template <int EL, int NCOMP>
+template <int EL, int NCOMP, int NSC = 1>
 __device__ __forceinline__ void block_sum_chunks(const float *__restrict__ part, int stride_c, int HD,
                                                  const float *__restrict__ parts_c, int H, int LH,
                                                  int32_t c0, int32_t c1, int c, bool active,
-                                                 float (*sh)[NCOMP][32 * EL], float (*shc)[32],
-                                                 float (&sum)[NCOMP][EL], float &csum) {
+                                                 float (*sh)[NCOMP][32 * EL], float (*shc)[NSC][32],
+                                                 float (&sum)[NCOMP][EL], float (&csum)[NSC]) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    float x[NCOMP][EL], xc = 0.f;
+    float x[NCOMP][EL], xc[NSC];
 #pragma unroll
     for (int q = 0; q < NCOMP; ++q)
 #pragma unroll
         for (int e = 0; e < EL; ++e) x[q][e] = 0.f;
+#pragma unroll
+    for (int t = 0; t < NSC; ++t) xc[t] = 0.f;
     if (active) {
         for (int32_t ch = c0 + w; ch < c1; ch += kWarpsPerBlock) {
 #pragma unroll
@@ -301,30 +304,52 @@ __device__ __forceinline__ void block_sum_chunks(const float *__restrict__ part,
                     x[q][e] += v.x; x[q][e + 1] += v.y; x[q][e + 2] += v.z; x[q][e + 3] += v.w;
                 }
             }
-            if (parts_c) xc += parts_c[(size_t)ch * H + c / LH];
+            if (parts_c)
+#pragma unroll
+                for (int t = 0; t < NSC; ++t) xc[t] += parts_c[((size_t)ch * H + c / LH) * NSC + t];
         }
     }
 #pragma unroll
     for (int q = 0; q < NCOMP; ++q)
 #pragma unroll
         for (int e = 0; e < EL; ++e) sh[w][q][lane * EL + e] = x[q][e];
-    shc[w][lane] = xc;
+#pragma unroll
+    for (int t = 0; t < NSC; ++t) shc[w][t][lane] = xc[t];
     __syncthreads();
     if (w == 0) {
 #pragma unroll
         for (int q = 0; q < NCOMP; ++q)
 #pragma unroll
             for (int e = 0; e < EL; ++e) sum[q][e] = 0.f;
-        csum = 0.f;
+#pragma unroll
+        for (int t = 0; t < NSC; ++t) csum[t] = 0.f;
         for (int v = 0; v < kWarpsPerBlock; ++v) {
 #pragma unroll
             for (int q = 0; q < NCOMP; ++q)
 #pragma unroll
                 for (int e = 0; e < EL; ++e) sum[q][e] += sh[v][q][lane * EL + e];
-            csum += shc[v][lane];
+#pragma unroll
+            for (int t = 0; t < NSC; ++t) csum[t] += shc[v][t][lane];
         }
     }
 }
+
+// Row normalisation of the backward pass.  The weights are recomputed as
+// p = 2^(s2 - lse2) from the forward's fp32 lse, whose rounding scales a
+// whole row's weights by one factor (1 + eps), so they sum to Z = 1 + eps
+// rather than 1; left alone, that error reaches the gradients through
+// Delta times sum_j p x_j, which does not cancel.  The passes therefore also
+// sum Z = sum_j p and use the normalised weights p / Z: Delta = C / Z (C =
+// sum p dP), the row sums divided by Z, and lse + ln Z stored for the
+// transposed pass, whose recomputed weights are then normalised as well.
+struct RowNorm {
+    float inv_z, delta, lse_shift;   // 1/Z, C/Z, ln Z
+    __device__ __forceinline__ RowNorm(float c, float z) {
+        inv_z = z > 0.f ? 1.f / z : 0.f;
+        delta = c * inv_z;
+        lse_shift = z > 0.f ? logf(z) : 0.f;
+    }
+};
 
 // ---------------------------------------------------------- backward: dQ
 
@@ -332,9 +357,10 @@ __device__ __forceinline__ void block_sum_chunks(const float *__restrict__ part,
 // With Delta_i = sum_j p dP (the exact row term; equal to dOut_i . out_i
 // before out is rounded to the storage dtype), dS = p (dP - Delta_i) and
 // dQ_i = sum_j dS k_j / sqrt(D) = (A - Delta_i B) / sqrt(D) where
-// A = sum_j p dP k_j and B = sum_j p k_j; A, B and Delta_i are accumulated in
-// the same pass over the edges.  Split-row chunks write A, B and their part
-// of Delta; the merge kernel finishes them in chunk order.
+// A = sum_j p dP k_j and B = sum_j p k_j; A, B, C = sum_j p dP and Z =
+// sum_j p are accumulated in the same pass over the edges and the weights
+// normalised by Z at the end (RowNorm).  Split-row chunks write A, B and
+// their parts of C and Z; the merge kernel finishes them in chunk order.
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
@@ -355,12 +381,12 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
             a.split_threshold, a.d_err);
     StreamItem it;
     while (st.next_item(it)) {
-        float q[NC][EL], go[NC][EL], A[NC][EL], B[NC][EL], c[NC], lse2[NC];
+        float q[NC][EL], go[NC][EL], A[NC][EL], B[NC][EL], c[NC], z[NC], lse2[NC];
 #pragma unroll
         for (int k = 0; k < NC; ++k) {
 #pragma unroll
             for (int x = 0; x < EL; ++x) q[k][x] = go[k][x] = A[k][x] = B[k][x] = 0.f;
-            c[k] = 0.f;
+            c[k] = z[k] = 0.f;
             lse2[k] = 0.f;
         }
         for (int step = 0; step < it.nsteps; ++step) {
@@ -398,6 +424,8 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                     const float p0 = hi ? po : p, p1 = hi ? p : po, d0 = hi ? pdpo : pdp, d1 = hi ? pdp : pdpo;
                     c[0] += d0;
                     c[1] += d1;
+                    z[0] += p0;
+                    z[1] += p1;
                     axpy2<EL>(A[0], d0, kf[0]);
                     axpy2<EL>(B[0], p0, kf[0]);
                     axpy2<EL>(A[1], d1, kf[1]);
@@ -413,6 +441,7 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                         const float p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
                         const float pdp = p * dp;
                         c[k] += pdp;
+                        z[k] += p;
                         axpy2<EL>(A[k], pdp, kf);
                         axpy2<EL>(B[k], p, kf);
                     }
@@ -425,6 +454,7 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
 #pragma unroll
             for (int k = 0; k < NC; ++k) {
                 c[k] += __shfl_xor_sync(SGA_FULL_MASK, c[k], off);
+                z[k] += __shfl_xor_sync(SGA_FULL_MASK, z[k], off);
 #pragma unroll
                 for (int x = 0; x < EL; ++x) {
                     A[k][x] += __shfl_xor_sync(SGA_FULL_MASK, A[k][x], off);
@@ -445,14 +475,23 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                         dA[x / 4] = make_float4(A[k][x], A[k][x + 1], A[k][x + 2], A[k][x + 3]);
                         dB[x / 4] = make_float4(B[k][x], B[k][x + 1], B[k][x + 2], B[k][x + 3]);
                     }
-                    if (ch % LH == 0) a.ws_rowc[(size_t)it.item * a.H + h] = c[k];
+                    if (ch % LH == 0) {
+                        a.ws_rowc[((size_t)it.item * a.H + h) * 2] = c[k];
+                        a.ws_rowc[((size_t)it.item * a.H + h) * 2 + 1] = z[k];
+                    }
                 } else {
-                    const float dl = c[k] + (a.delta_in ? a.delta_in[(size_t)it.row * a.H + h] : 0.f);
+                    const size_t rh = (size_t)it.row * a.H + h;
+                    const RowNorm nrm(c[k] + (a.delta_in ? a.delta_in[rh] : 0.f),
+                                      z[k] + (a.z_in ? a.z_in[rh] : 0.f));
+                    const float sc = scale * nrm.inv_z;
                     float o[EL];
 #pragma unroll
-                    for (int x = 0; x < EL; ++x) o[x] = (A[k][x] - dl * B[k][x]) * scale;
+                    for (int x = 0; x < EL; ++x) o[x] = (A[k][x] - nrm.delta * B[k][x]) * sc;
                     reinterpret_cast<uint4 *>(a.dQ)[(size_t)it.row * R + ch] = pack<T>(o);
-                    if (ch % LH == 0) a.ws_delta[(size_t)it.row * a.H + h] = dl;
+                    if (ch % LH == 0) {
+                        a.ws_delta[rh] = nrm.delta;
+                        a.ws_lse[rh] = a.lse[rh] + nrm.lse_shift;
+                    }
                 }
             }
         }
@@ -465,7 +504,8 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
 
 // Per source j over its destinations i (transposed CSR):
 // p = 2^(s2 - lse2_i), dS = p (dOut_i . v_j - Delta_i),
-// dV_j += p dOut_i, dK_j += dS q_i.
+// dV_j += p dOut_i, dK_j += dS q_i, with the dQ pass's normalised lse_i
+// (lse_i + ln Z_i) and Delta_i.
 template <typename T, int D, int NC, int G>
 __global__ void __launch_bounds__(256, 2)
 gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
@@ -478,7 +518,7 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
     StreamArrays arr{};
     arr.rows[0] = static_cast<const uint4 *>(a.Q);
     arr.rows[1] = static_cast<const uint4 *>(a.dOut);
-    arr.sc[0] = a.lse;
+    arr.sc[0] = a.ws_lse;     // lse + ln Z of each destination (normalised weights)
     arr.sc[1] = a.ws_delta;
     arr.own[0] = static_cast<const uint4 *>(a.K);
     arr.own[1] = static_cast<const uint4 *>(a.V);
@@ -555,14 +595,14 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
     st.drain();
 }
 
-// Finish split rows, one block each.  which == 0: dQ rows (Delta = sum of
-// the chunk parts, dQ = (sum A - Delta sum B) / sqrt(D), Delta stored for the
-// dK/dV pass).  which == 1: dK, dV of split sources (plain sums).
+// Finish split rows, one block each.  which == 0: dQ rows (C and Z = sums of
+// the chunk parts, normalised as in the dQ pass, Delta and lse + ln Z stored
+// for the dK/dV pass).  which == 1: dK, dV of split sources (plain sums).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) gt_bwd_merge_kernel(GtArgs a, float scale, int which) {
     constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
     __shared__ float sh[kWarpsPerBlock][2][32 * EL];
-    __shared__ float shc[kWarpsPerBlock][32];
+    __shared__ float shc[kWarpsPerBlock][2][32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int64_t s = blockIdx.x;
     const Partition &P = which == 0 ? a.rows : a.cols;
@@ -572,18 +612,24 @@ __global__ void __launch_bounds__(256) gt_bwd_merge_kernel(GtArgs a, float scale
     const int R = a.H * D / EL, HD = a.H * D;
     for (int cb = 0; cb < R; cb += 32) {
         const int c = cb + lane;
-        float sum[2][EL], delta;
-        block_sum_chunks<EL, 2>(which == 0 ? a.ws_row : a.ws_col, 2, HD,
-                                which == 0 ? a.ws_rowc : nullptr, a.H, LH, c0, c1, c, c < R, sh,
-                                shc, sum, delta);
+        float sum[2][EL], cz[2];
+        block_sum_chunks<EL, 2, 2>(which == 0 ? a.ws_row : a.ws_col, 2, HD,
+                                   which == 0 ? a.ws_rowc : nullptr, a.H, LH, c0, c1, c, c < R, sh,
+                                   shc, sum, cz);
         if (w == 0 && c < R) {
             if (which == 0) {
-                if (a.delta_in) delta += a.delta_in[(size_t)row * a.H + c / LH];
+                const size_t rh = (size_t)row * a.H + c / LH;
+                const RowNorm nrm(cz[0] + (a.delta_in ? a.delta_in[rh] : 0.f),
+                                  cz[1] + (a.z_in ? a.z_in[rh] : 0.f));
+                const float sc = scale * nrm.inv_z;
                 float o[EL];
 #pragma unroll
-                for (int x = 0; x < EL; ++x) o[x] = (sum[0][x] - delta * sum[1][x]) * scale;
+                for (int x = 0; x < EL; ++x) o[x] = (sum[0][x] - nrm.delta * sum[1][x]) * sc;
                 reinterpret_cast<uint4 *>(a.dQ)[(size_t)row * R + c] = pack<T>(o);
-                if (c % LH == 0) a.ws_delta[(size_t)row * a.H + c / LH] = delta;
+                if (c % LH == 0) {
+                    a.ws_delta[rh] = nrm.delta;
+                    a.ws_lse[rh] = a.lse[rh] + nrm.lse_shift;
+                }
             } else {
 #pragma unroll
                 for (int x = 0; x < EL; ++x) sum[0][x] *= scale;

@@ -411,4 +411,35 @@ void plan_free(sga_plan *p) {
     p->owned.clear();
 }
 
+
+int64_t radix_hist_elems(int64_t n) {
+    const int64_t n_tiles = (n + kRadixTile - 1) / kRadixTile;
+    return (int64_t)kRadixBins * std::max<int64_t>(n_tiles, 1);
+}
+
+// Stable LSD radix sort of n (key, value) pairs by the low `bits` bits of the
+// non-negative keys, 8 bits per pass.  (*ka, *va) hold the input, (*kb, *vb)
+// scratch of n each; hist holds radix_hist_elems(n) and scan_tmp
+// scan_tmp_elems(radix_hist_elems(n)) int32.  The sorted pairs end in
+// (*ka, *va): the buffer pointers are swapped as the passes alternate.
+cudaError_t radix_sort_pairs(int32_t **ka, int32_t **va, int32_t **kb, int32_t **vb, int64_t n,
+                             int bits, int32_t *hist, int32_t *scan_tmp, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int64_t n_tiles = (n + kRadixTile - 1) / kRadixTile;
+    const int64_t hist_n = (int64_t)kRadixBins * n_tiles;
+    const unsigned blocks = (unsigned)((n_tiles + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    for (int shift = 0; shift < bits; shift += kRadixBits) {
+        radix_hist_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(*ka, n, shift, n_tiles, hist);
+        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess) e = exclusive_scan(hist, hist, hist_n, scan_tmp, s);
+        if (e != cudaSuccess) return e;
+        radix_scatter_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(*ka, *va, n, shift, n_tiles, hist,
+                                                                  *kb, *vb);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        std::swap(*ka, *kb);
+        std::swap(*va, *vb);
+    }
+    return cudaSuccess;
+}
+
 }  // namespace sga

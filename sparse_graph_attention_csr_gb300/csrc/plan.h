@@ -24,11 +24,13 @@ struct Partition {
 
 // Byte offsets of the regions of the caller's workspace.
 struct WorkspaceLayout {
-    size_t delta = 0;      // [N, H] f32          Delta_i = dOut_i . out_i
+    size_t delta = 0;      // [N, H] f32          Delta_i = dOut_i . out_i (normalised weights)
+    size_t lse_n = 0;      // [N, H] f32          lse_i + ln Z_i (backward row normalisation)
+    size_t zt = 0;         // [N, H] f32          block-sparse plans: tile part of Z_i
     size_t fwd_ml = 0;     // [n_chunks, H, 2] f32 chunk softmax stats (max, sum), log2 units
     size_t fwd_acc = 0;    // [n_chunks, H*D] f32  chunk unnormalised accumulators
     size_t bwd_row = 0;    // [n_chunks, 4, H*D] f32 chunk partial sums (dQ: A, B; dFL: A, B, da A, B)
-    size_t bwd_rowc = 0;   // [n_chunks, H] f32   chunk part of Delta
+    size_t bwd_rowc = 0;   // [n_chunks, H, 2] f32 chunk parts of C = sum p dP and Z = sum p
     size_t da_split = 0;   // [n_split, H*D] f32  GATv2 da contribution of each split row
     size_t bwd_col = 0;    // [t_n_chunks, 2*H*D] f32 chunk partial dK,dV / dFR
     size_t dfl = 0;        // [N, H*D] f32 GATv2 dFL
@@ -36,6 +38,9 @@ struct WorkspaceLayout {
     size_t da_part = 0;    // [da_blocks, H*D] f32 GATv2 partial da
     size_t dw_part = 0;    // [dw_slabs, 2, F, H*D] f32 GATv2 partial dW_l, dW_r
     size_t fix = 0;        // int32 count, then [fix_cap] int2 projection elements to round exactly
+    size_t agg_val = 0;    // [n_chunks, H*D] f32  min/max aggregation: chunk extremes
+    size_t agg_pos = 0;    // [n_chunks, H*D] i32  their edge positions
+    size_t agg_acc = 0;    // [N, H*D] f32         backward accumulator (bf16 layers)
     int32_t fix_cap = 0;
     size_t total = 0;
     int32_t da_blocks = 0;
@@ -68,6 +73,8 @@ struct TileSet {
 struct sga_plan {
     int64_t N = 0, E = 0;
     int H = 0, D = 0, F = 0;
+    int layer = SGA_LAYER_ATTENTION;   // what the plan's workspace serves
+    int schedule = SGA_SCHED_STREAM;   // thread mapping of the GT CSR forward
     sga_dtype dt = SGA_F32;
     int split_threshold = 256, chunk_len = 128;
     const int32_t *indptr = nullptr;   // graph the plan was built from
@@ -101,6 +108,12 @@ int get_cuda_error();
 int64_t scan_tmp_elems(int64_t n);
 cudaError_t exclusive_scan(const int32_t *in, int32_t *out, int64_t n, int32_t *tmp, cudaStream_t s);
 
+// Stable LSD radix sort of (key, value) int32 pairs by the low `bits` bits of
+// the non-negative keys (plan.cu); the sorted pairs end in (*ka, *va).
+int64_t radix_hist_elems(int64_t n);
+cudaError_t radix_sort_pairs(int32_t **ka, int32_t **va, int32_t **kb, int32_t **vb, int64_t n,
+                             int bits, int32_t *hist, int32_t *scan_tmp, cudaStream_t s);
+
 // ---- Graph Transformer (gt.cu) ----
 struct GtArgs {
     const int32_t *indptr, *indices;
@@ -114,13 +127,17 @@ struct GtArgs {
     int split_threshold;
     Partition rows, cols;
     float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_rowc, *ws_col;
-    // optional [N, H] term added to each row's Delta: the share of edges that
-    // another pass (the block-sparse tiles) handles; nullptr: none
-    const float *delta_in;
+    float *ws_lse;                 // [N, H] lse + ln Z written by the dQ pass
+    // optional [N, H] terms added to each row's C = sum p dP and Z = sum p:
+    // the share of edges that another pass (the block-sparse tiles)
+    // handles; nullptr: none
+    const float *delta_in, *z_in;
     int32_t *d_err;
 };
 template <typename T> cudaError_t gt_fwd_t(const GtArgs &a, cudaStream_t s);
 template <typename T> cudaError_t gt_bwd_t(const GtArgs &a, cudaStream_t s);
+// GT forward with an alternative thread mapping (gt_sched.cu)
+template <typename T> cudaError_t gt_fwd_sched_t(const GtArgs &a, int schedule, cudaStream_t s);
 
 // ---- GATv2 (gatv2.cu) ----
 struct Gatv2Args {
@@ -136,6 +153,7 @@ struct Gatv2Args {
     int split_threshold;
     Partition rows, cols;
     float *ws_ml, *ws_acc, *ws_delta, *ws_row, *ws_rowc, *ws_col, *ws_da, *ws_da_split, *ws_dw;
+    float *ws_lse;                 // [N, H] lse + ln Z written by the destination pass
     float *ws_dfl, *ws_dfr;        // [N, H*D] fp32
     int32_t *ws_fix_count;
     int2 *ws_fix_list;
@@ -162,9 +180,11 @@ cudaError_t launch_bsr_fwd(const BsrArgs &a, cudaStream_t s);
 
 struct BsrBwdArgs {
     const void *Q, *K, *V, *dOut;   // [N, H, D] bf16
-    const float *lse;               // [N, H]
-    float *delta_t;                 // [N, H] tile part of Delta (written by the Delta pass)
+    const float *lse;               // [N, H] the forward's lse (Delta pass)
+    float *delta_t;                 // [N, H] tile part of C = sum p dP (written by the Delta pass)
+    float *z_t;                     // [N, H] tile part of Z = sum p (written by the Delta pass)
     const float *delta;             // [N, H] full Delta (read by the dQ and dK/dV passes)
+    const float *lse_n;             // [N, H] lse + ln Z (read by the dQ and dK/dV passes)
     void *dQ, *dK, *dV;             // in: residual gradients, out: with the tile part added
     const int32_t *tile_ptr, *tile_col;
     const uint16_t *tile_bits;
@@ -179,5 +199,23 @@ cudaError_t launch_bsr_bwd_delta(const BsrBwdArgs &a, cudaStream_t s);
 cudaError_t launch_bsr_bwd_dq(const BsrBwdArgs &a, cudaStream_t s);
 cudaError_t launch_bsr_bwd_dkdv(const BsrBwdArgs &a, cudaStream_t s);
 template <typename T> cudaError_t gatv2_bwd_t(const Gatv2Args &a, cudaStream_t s);
+
+// ---- min / max aggregation (agg.cu) ----
+struct AggArgs {
+    const int32_t *indptr, *indices;
+    const void *X, *dOut;   // [N, HD] in the layer dtype
+    void *out, *dX;         // likewise
+    int32_t *arg;           // [N, HD] winning source node (-1: empty row)
+    int64_t N;
+    int HD;
+    int split_threshold;
+    int num_sms;
+    Partition rows;
+    float *ws_val, *ws_acc;
+    int32_t *ws_pos;
+    int32_t *d_err;
+};
+template <typename T> cudaError_t agg_fwd_t(const AggArgs &a, bool is_max, cudaStream_t s);
+template <typename T> cudaError_t agg_bwd_t(const AggArgs &a, cudaStream_t s);
 
 }  // namespace sga

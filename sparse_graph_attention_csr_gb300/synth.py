@@ -22,6 +22,9 @@ structure:
 4. R-MAT (0.57, 0.19, 0.19, 0.05), scale 20, 2^25 draws (GT, bf16, H=4, D=64).
 5. Stochastic block model, 1024 contiguous communities of 256, p_in=0.15,
    4N inter-community draws (GT, bf16, H=4, D=128).
+6. Min / max aggregation over workload 3's graph (N=170k, lognormal
+   Chung-Lu with a hub), node rows of 512 bf16 features (read as H=4 x D=128),
+   the width of the pages' min-aggregation figure.
 """
 from __future__ import annotations
 
@@ -39,7 +42,7 @@ class Workload:
     """One synthetic workload: graph recipe, layer kind and tensor shapes."""
     key: int
     name: str
-    layer: str              # "gt" or "gatv2"
+    layer: str              # "gt", "gatv2", "agg_min" or "agg_max"
     graph: str              # "er" | "chung_lu" | "lognormal_cl" | "rmat" | "sbm"
     N: int
     H: int
@@ -71,6 +74,9 @@ WORKLOADS = {
     5: Workload(5, "gt_sbm_n262k_h4_d128_bf16", "gt", "sbm", 262_144, 4, 128, "bf16", True, 5,
                 {"block": 256, "p_in": 0.15, "inter_per_node": 4},
                 qkv_std=1.0 / math.sqrt(128)),
+    6: Workload(6, "agg_min_lognormal_n170k_f512_bf16", "agg_min", "lognormal_cl", 170_000, 4, 128,
+                "bf16", True, 6, {"draws": 1_200_000, "median": 7.0, "sigma": 1.15,
+                                  "hub_weight": 10_000.0}),
 }
 
 
@@ -89,6 +95,8 @@ def small_workload(key: int) -> Workload:
         return w.scaled(N=1 << 14, params={"scale": 14, "draws": 1 << 19})
     if key == 5:
         return w.scaled(N=4096)
+    if key == 6:
+        return w.scaled(N=9000, params={"draws": 63_000, "hub_weight": 2500.0})
     raise KeyError(key)
 
 
@@ -293,6 +301,17 @@ def gatv2_inputs(w: Workload, N: int | None = None):
     }
     if w.backward:
         out["dOut"] = round_to(normal(w.seed, STREAM_DOUT, (N, w.H, w.D)), w.dtype)
+    return out
+
+
+def agg_inputs(w: Workload, N: int | None = None):
+    """X [N, H, D] ~ N(0, 1) rounded to the workload dtype (the min / max
+    aggregation's node rows) and dOut [N, H, D] ~ N(0, 1)."""
+    N = w.N if N is None else N
+    shape = (N, w.H, w.D)
+    out = {"X": round_to(normal(w.seed, STREAM_A, shape), w.dtype)}
+    if w.backward:
+        out["dOut"] = round_to(normal(w.seed, STREAM_DOUT, shape), w.dtype)
     return out
 
 

@@ -170,19 +170,28 @@ def test_gt_workload_recipe_with_scaled_scores():
     assert rescale_rows(indptr, indices, qf, kf) > 0.1 * w.N
 
 
-@pytest.mark.parametrize("dtype,ascale", [("f32", 4.0), ("bf16", 12.0)])
-def test_gatv2_rising_scores(dtype, ascale):
-    """GATv2 with a large attention vector (scores spread over tens of units)
-    and each row's sources ordered by ascending score; hub rows split into
-    chunks of 24.  Forward element by element; backward with the tolerances
-    of the GATv2 parity tests."""
+@pytest.mark.parametrize("dtype,levels", [("f32", (0.0, 4.0)), ("bf16", (0.0, 4.0, 8.0, 12.0))])
+def test_gatv2_rising_scores(dtype, levels):
+    """GATv2 staircase: feature 0 of X carries a per-node level t_j, W_r maps
+    it onto every column (row 0 of W_r is 1, of W_l 0) and a > 0, so the
+    score e_ij grows by ~7 per level; each row lists its sources by ascending
+    score; hub rows are split into chunks of 24.  Forward element by element;
+    backward with the tolerances of the GATv2 parity tests."""
     rng = np.random.default_rng(77 if dtype == "f32" else 78)
     N, F, H, D = 500, 64, 2, 64
     lim = math.sqrt(6.0 / (F + H * D))
-    X, xf = rounded(rng.standard_normal((N, F)), dtype)
-    Wl, wlf = rounded(rng.uniform(-lim, lim, (F, H * D)), dtype)
-    Wr, wrf = rounded(rng.uniform(-lim, lim, (F, H * D)), dtype)
-    a, af = rounded(rng.standard_normal((H, D)) * ascale / math.sqrt(D), dtype)
+    x = rng.standard_normal((N, F))
+    x[:, 0] = np.asarray(levels)[rng.integers(0, len(levels), N)]
+    wl = rng.uniform(-lim, lim, (F, H * D))
+    wl[0, :] = 0.0
+    wr = rng.uniform(-lim, lim, (F, H * D))
+    wr[0, :] = 1.0
+    # sum_d a_d ~ 7/4: a level step of 4 moves the score by ~7
+    av = np.abs(rng.standard_normal((H, D))) * (7.0 / 4.0) / (D * 0.8)
+    X, xf = rounded(x, dtype)
+    Wl, wlf = rounded(wl, dtype)
+    Wr, wrf = rounded(wr, dtype)
+    a, af = rounded(av, dtype)
     dO, dof = rounded(rng.standard_normal((N, H, D)), dtype)
     # random graph, then each row ordered by its head-0 score on the stored projections
     base_ptr, base_idx = staircase_graph(rng, N, 12, np.zeros(N), hubs=[(3, 350), (444, 120)])

@@ -489,3 +489,189 @@ def test_tile_extract_by_brute_force():
                 res_rows[i].append(j)
     assert [list(t["r_indices"][t["r_indptr"][i]:t["r_indptr"][i + 1]]) for i in range(N)] == res_rows
     assert sum(bin(int(b)).count("1") for b in t["tile_bits"].ravel()) + len(t["r_indices"]) == len(indices)
+
+
+# ------------------------------------------------------- min / max aggregation
+
+def test_agg_hand_example():
+    g = load("agg_hand.json")
+    ip, ix = np.array(g["indptr"], np.int32), np.array(g["indices"], np.int32)
+    X = np.array(g["X"], float)
+    for op in ("max", "min"):
+        out, arg = oracle.agg_fwd(ip, ix, X, op)
+        np.testing.assert_array_equal(out, np.array(g[op + "_out"], float))
+        np.testing.assert_array_equal(arg, np.array(g[op + "_arg"]))
+    _, arg = oracle.agg_fwd(ip, ix, X, "max")
+    np.testing.assert_array_equal(oracle.agg_bwd(arg, np.array(g["dO"], float)),
+                                  np.array(g["max_dX"], float))
+
+
+@pytest.mark.parametrize("op", ["max", "min"])
+def test_agg_matches_dense_masked_reduction(op):
+    """Duplicate-free graphs with ascending sources: a dense masked max/min,
+    and numpy's argmax/argmin (first occurrence, i.e. the smallest source,
+    which is the first edge of an ascending row), with values drawn from a
+    small set so that ties are frequent."""
+    rng = np.random.default_rng(51 if op == "max" else 52)
+    N, F = 40, 6
+    indptr, indices = rand_graph(rng, N, 0.2, self_loops=False)
+    # empty row 5
+    deg = np.diff(indptr)
+    indices = np.delete(indices, np.arange(indptr[5], indptr[6]))
+    deg[5] = 0
+    indptr = np.concatenate([[0], np.cumsum(deg)]).astype(np.int32)
+    X = rng.integers(-3, 4, (N, F)).astype(float)
+    out, arg = oracle.agg_fwd(indptr, indices, X, op)
+    mask = dense_mask(indptr, indices, N).numpy()
+    fill = -np.inf if op == "max" else np.inf
+    dense = np.where(mask[:, :, None], X[None, :, :], fill)   # [i, j, f]
+    red = dense.max(1) if op == "max" else dense.min(1)
+    who = dense.argmax(1) if op == "max" else dense.argmin(1)
+    empty = ~mask.any(1)
+    np.testing.assert_array_equal(out[~empty], red[~empty])
+    np.testing.assert_array_equal(arg[~empty], who[~empty])
+    assert np.all(out[empty] == 0.0) and np.all(arg[empty] == -1)
+    assert empty.any() and (~empty).any()
+
+
+@pytest.mark.parametrize("op", ["max", "min"])
+def test_agg_matches_torch_scatter_reduce_and_autograd(op):
+    """torch.scatter_reduce (amax / amin over the edges) gives the values;
+    with tie-free inputs its autograd gives the gradient of the backward."""
+    rng = np.random.default_rng(53 if op == "max" else 54)
+    N, F = 60, 5
+    indptr, indices = rand_graph(rng, N, 0.1, dups=True)
+    X = rng.standard_normal((N, F))
+    dO = rng.standard_normal((N, F))
+    out, arg = oracle.agg_fwd(indptr, indices, X, op)
+    dX = oracle.agg_bwd(arg, dO)
+    rows = torch.from_numpy(np.repeat(np.arange(N), np.diff(indptr)).astype(np.int64))
+    tX = torch.from_numpy(X).requires_grad_()
+    src = tX[torch.from_numpy(indices.astype(np.int64))]
+    red = torch.zeros(N, F, dtype=torch.float64).scatter_reduce(
+        0, rows[:, None].expand(-1, F), src, reduce="amax" if op == "max" else "amin",
+        include_self=False)
+    np.testing.assert_array_equal(out, red.detach().numpy())
+    (red * torch.from_numpy(dO)).sum().backward()
+    # a duplicated edge repeats a value: torch splits the gradient among the
+    # copies, the definition sends it once to that source; both sum to the same
+    np.testing.assert_allclose(dX, tX.grad.numpy(), atol=1e-12)
+
+
+def test_agg_invariants():
+    """Reordering a row's edges keeps every value; the winner changes only
+    among equal values; relabelling nodes is equivariant."""
+    rng = np.random.default_rng(55)
+    N, F = 50, 4
+    indptr, indices = rand_graph(rng, N, 0.15)
+    X = rng.integers(-2, 3, (N, F)).astype(float)
+    out, arg = oracle.agg_fwd(indptr, indices, X, "max")
+    ix2 = indices.copy()
+    for i in range(N):
+        b, e = indptr[i], indptr[i + 1]
+        ix2[b:e] = rng.permutation(ix2[b:e])
+    out2, arg2 = oracle.agg_fwd(indptr, ix2, X, "max")
+    np.testing.assert_array_equal(out, out2)
+    has = arg >= 0
+    np.testing.assert_array_equal(X[arg[has], np.nonzero(has)[1]], X[arg2[has], np.nonzero(has)[1]])
+    perm = rng.permutation(N)             # node v becomes perm[v]
+    inv = np.argsort(perm)
+    rows = [perm[indices[indptr[inv[u]]:indptr[inv[u] + 1]]] for u in range(N)]
+    ip3 = np.zeros(N + 1, np.int32)
+    ip3[1:] = np.cumsum([len(r) for r in rows])
+    ix3 = np.concatenate(rows).astype(np.int32)
+    X3 = np.empty_like(X)
+    X3[perm] = X
+    out3, arg3 = oracle.agg_fwd(ip3, ix3, X3, "max")
+    np.testing.assert_array_equal(out3[perm], out)
+    np.testing.assert_array_equal(np.where(arg >= 0, perm[np.maximum(arg, 0)], -1), arg3[perm])
+
+
+# ------------------------------------------------------------ graph reordering
+
+def test_reorder_hand_example():
+    g = load("reorder_hand.json")
+    ip, ix = np.array(g["indptr"], np.int32), np.array(g["indices"], np.int32)
+    np.testing.assert_array_equal(oracle.order_rcm(ip, ix), g["rcm_perm"])
+    np.testing.assert_array_equal(oracle.order_degree(ip, ix), g["degree_perm"])
+
+
+def sym_graph(rng, N, p):
+    """Symmetric, duplicate-free, without self-loops (sources ascending)."""
+    a = rng.random((N, N)) < p
+    a = np.triu(a, 1)
+    a = a | a.T
+    indptr = np.zeros(N + 1, np.int32)
+    indptr[1:] = np.cumsum(a.sum(1))
+    return indptr, np.nonzero(a)[1].astype(np.int32)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3, 4])
+def test_rcm_matches_scipy_on_symmetric_graphs(seed):
+    """On a symmetric graph without self-loops or duplicates, the degree used
+    here is twice the matrix row count, so the ordering rules coincide with
+    scipy.sparse.csgraph.reverse_cuthill_mckee's (least-degree start,
+    children by ascending degree, ties by id).  scipy breaks ties between
+    equal-degree start nodes of different components in an unspecified
+    order, so the graphs here are connected."""
+    sp = pytest.importorskip("scipy.sparse")
+    from scipy.sparse.csgraph import connected_components, reverse_cuthill_mckee
+    rng = np.random.default_rng(seed)
+    N = 60
+    indptr, indices = sym_graph(rng, N, 0.12)
+    m = sp.csr_matrix((np.ones(len(indices)), indices, indptr), shape=(N, N))
+    assert connected_components(m, directed=False)[0] == 1
+    order = reverse_cuthill_mckee(m, symmetric_mode=True)
+    perm = oracle.order_rcm(indptr, indices)
+    # scipy returns the order (position -> node); ours is node -> position
+    np.testing.assert_array_equal(np.argsort(perm), order)
+
+
+def test_rcm_recovers_a_shuffled_path_and_grid_bandwidth():
+    rng = np.random.default_rng(5)
+    N = 50
+    lab = rng.permutation(N)
+    rows = [[] for _ in range(N)]
+    for t in range(N - 1):                        # path lab[0] - lab[1] - ... - lab[N-1]
+        rows[lab[t + 1]].append(lab[t])
+    indptr = np.zeros(N + 1, np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in rows])
+    indices = np.array([j for r in rows for j in r], np.int32)
+    perm = oracle.order_rcm(indptr, indices)
+    new_pos = perm[lab]                           # positions along the path
+    assert np.all(np.abs(np.diff(new_pos)) == 1)  # bandwidth 1
+    # a 12 x 12 grid under random labels: bandwidth falls to the grid's width order
+    W = 12
+    lab = rng.permutation(W * W)
+    rows = [[] for _ in range(W * W)]
+    for r in range(W):
+        for c in range(W):
+            if c + 1 < W:
+                rows[lab[r * W + c]].append(lab[r * W + c + 1])
+            if r + 1 < W:
+                rows[lab[r * W + c]].append(lab[(r + 1) * W + c])
+    indptr = np.zeros(W * W + 1, np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in rows])
+    indices = np.array([j for r in rows for j in r], np.int32)
+    perm = oracle.order_rcm(indptr, indices)
+    dst = np.repeat(np.arange(W * W), np.diff(indptr))
+    bw_before = np.abs(dst - indices).max()
+    bw_after = np.abs(perm[dst] - perm[indices]).max()
+    assert bw_after <= W + 1 < bw_before
+
+
+def test_relabelled_graph_is_equivariant():
+    """A relabelled graph with relabelled features gives the relabelled
+    attention output (checked through the oracle's Graph Transformer)."""
+    rng = np.random.default_rng(6)
+    N, H, D = 40, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.15, dups=True)
+    for perm in (oracle.order_rcm(indptr, indices), oracle.order_degree(indptr, indices)):
+        assert sorted(perm.tolist()) == list(range(N))
+        ip2, ix2 = oracle.relabel_csr(indptr, indices, perm)
+        Q, K, V = (rng.standard_normal((N, H, D)) for _ in range(3))
+        P = lambda x: x[np.argsort(perm)]         # row perm[v] of the result = row v
+        o1, l1 = oracle.gt_fwd(indptr, indices, Q, K, V)
+        o2, l2 = oracle.gt_fwd(ip2, ix2, P(Q), P(K), P(V))
+        np.testing.assert_allclose(o2, P(o1), atol=1e-12)
+        np.testing.assert_allclose(l2, P(l1), atol=1e-12)
