@@ -73,6 +73,8 @@ typedef struct {
     int32_t tile_min_nnz;     /* > 0: block-sparse tensor-core forward, see below; 0: off */
     int32_t layer;            /* sga_layer (default SGA_LAYER_ATTENTION) */
     int32_t schedule;         /* sga_schedule of the Graph Transformer CSR forward (default 0) */
+    int32_t edge_bias;        /* 1: the plan also serves gt_attn_bias_fwd/bwd (keeps the CSR edge
+                                 of every transposed entry: 4 more bytes per edge) */
 } sga_plan_opts;
 
 /* Thread mapping of the Graph Transformer forward over the CSR (the backward
@@ -140,6 +142,26 @@ sga_status gt_attn_bwd(const sga_plan *plan, const int32_t *indptr, const int32_
                        const void *Q, const void *K, const void *V, const void *out,
                        const float *lse, const void *dOut, int64_t N, int64_t E, int H, int D,
                        sga_dtype dt, void *dQ, void *dK, void *dV, void *stream);
+
+/* Graph Transformer with an additive per-edge, per-head score bias (the
+ * edge-feature term of "Masked Label Prediction: Unified Message Passing
+ * Model", the Graph Transformer the IO-aware layers pages cite, in its
+ * simplest form; DF-GNN's abstract names the AT-GNN family, GAT and Graph
+ * Transformer): s_ij = q_i . k_j / sqrt(D) + bias[e, h] for the CSR entry e
+ * of edge (i <- j).  bias: [E, H] float32 (both dtypes), device, 4-byte
+ * aligned.  Needs a plan built with opts->edge_bias = 1 (CSR path, edge
+ * stream schedule; block-sparse plans are refused).  The backward adds
+ * dbias[E, H] float32 = dL/dbias = dS of every edge (written through the
+ * plan's transposed-edge map by the dK/dV pass). */
+sga_status gt_attn_bias_fwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                            const void *Q, const void *K, const void *V, const float *bias,
+                            int64_t N, int64_t E, int H, int D, sga_dtype dt, void *out, float *lse,
+                            void *stream);
+sga_status gt_attn_bias_bwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                            const void *Q, const void *K, const void *V, const float *bias,
+                            const void *out, const float *lse, const void *dOut, int64_t N,
+                            int64_t E, int H, int D, sga_dtype dt, void *dQ, void *dK, void *dV,
+                            float *dbias, void *stream);
 
 /* GATv2 forward: FL = X W_l, FR = X W_r (X [N, F], W [F, H*D], FL/FR written as
  * [N, H, D] and kept for the backward pass); e_ij = sum_d a[h,d]

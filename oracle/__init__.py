@@ -82,6 +82,12 @@ def _load():
             "oracle_agg_fwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _I32P], _int),
             "oracle_agg_bwd": ([_i64, _int, _I32P, _F64P, _F64P], _int),
             "oracle_rcm": ([_i64, _I32P, _I32P, _I32P], _int),
+            "oracle_gt_bias_fwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P, _F64P,
+                                    _F64P, _F64P], _int),
+            "oracle_gt_bias_bwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P, _F64P,
+                                    _F64P, _F64P, _F64P, _F64P, _F64P], _int),
+            "oracle_gatv2_bwd_bound": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P, _F64P,
+                                        _F64P, _dbl, _F64P, _F64P, _F64P, _F64P, _F64P], _int),
             "oracle_gatv2_branch_slack": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P,
                                            _F64P, _F64P, _dbl, _int, _dbl, _F64P, _F64P, _F64P,
                                            _F64P, _F64P], _int),
@@ -181,6 +187,34 @@ def gt_bwd(indptr, indices, Q, K, V, dO):
     dQ, dK, dV = np.empty_like(Q), np.empty_like(Q), np.empty_like(Q)
     _check(_load().oracle_gt_bwd(N, indptr, indices, H, D, Q, K, V, dO, dQ, dK, dV), "gt_bwd")
     return dQ, dK, dV
+
+
+def gt_bias_fwd(indptr, indices, Q, K, V, B):
+    """GT forward with an additive score bias B [E, H] (CSR edge order):
+    s_ij = q_i . k_j / sqrt(D) + B[e, h].  (out [N, H, D], lse [N, H])."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    Q, K, V, B = _f64(Q), _f64(K), _f64(V), _f64(B)
+    N, H, D = Q.shape
+    out = np.empty((N, H, D)); lse = np.empty((N, H))
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    Bp = B if B.size else np.zeros(1)
+    _check(_load().oracle_gt_bias_fwd(N, indptr, ix, H, D, Q, K, V, Bp, out, lse), "gt_bias_fwd")
+    return out, lse
+
+
+def gt_bias_bwd(indptr, indices, Q, K, V, B, dO):
+    """(dQ, dK, dV, dB) of the biased GT layer; dB = dS per edge and head."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    Q, K, V, B, dO = _f64(Q), _f64(K), _f64(V), _f64(B), _f64(dO)
+    N, H, D = Q.shape
+    E = len(indices)
+    dQ, dK, dV = np.empty_like(Q), np.empty_like(Q), np.empty_like(Q)
+    dB = np.empty((max(E, 1), H))
+    ix = indices if E else np.zeros(1, np.int32)
+    Bp = B if B.size else np.zeros(1)
+    _check(_load().oracle_gt_bias_bwd(N, indptr, ix, H, D, Q, K, V, Bp, dO, dQ, dK, dV, dB),
+           "gt_bias_bwd")
+    return dQ, dK, dV, dB[:E]
 
 
 def gt_bwd_dq_rows(indptr, indices, Q, K, V, dO, rows):
@@ -357,6 +391,24 @@ def relabel_csr(indptr, indices, perm):
     rows = [np.asarray(perm)[indices[indptr[inv[u]]:indptr[inv[u] + 1]]] for u in range(N)]
     new_idx = np.concatenate(rows) if rows else np.zeros(0)
     return new_ptr.astype(np.int32), new_idx.astype(np.int32)
+
+
+# ------------------------------------------- rounding bound of the fp32 GATv2 backward
+
+def gatv2_bwd_bound(indptr, indices, X, Wl, Wr, a, dO, slope=0.2):
+    """Elementwise first-order bound on |fp32 result - exact| of dX, dW_l,
+    dW_r, da for a float GATv2 layer (see oracle_gatv2_bwd_bound in
+    oracle.c for the arithmetic it covers).  dict of nonnegative arrays."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    X, Wl, Wr, a, dO = _f64(X), _f64(Wl), _f64(Wr), _f64(a), _f64(dO)
+    N, F = X.shape
+    H, D = a.shape
+    bX = np.empty((N, F)); bWl = np.empty((F, H * D)); bWr = np.empty((F, H * D))
+    bda = np.empty((H, D))
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    _check(_load().oracle_gatv2_bwd_bound(N, F, H, D, indptr, ix, X, Wl, Wr, a, float(slope), dO,
+                                          bX, bWl, bWr, bda), "gatv2_bwd_bound")
+    return {"dX": bX, "dW_l": bWl, "dW_r": bWr, "da": bda}
 
 
 # ------------------------------------------------------------ block-sparse tiles

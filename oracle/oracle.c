@@ -87,10 +87,12 @@ int oracle_transpose(int64_t N, const int32_t *indptr, const int32_t *indices,
 /* Graph Transformer                                                         */
 /* ------------------------------------------------------------------------ */
 
-/* Scores of one row for head h: s[e - b] = (q_i . k_j) / sqrt(D). */
+/* Scores of one row for head h: s[e - b] = (q_i . k_j) / sqrt(D), plus the
+ * edge's bias B[e, h] when B is given (the Graph Transformer with an additive
+ * per-edge, per-head score term; B is [E, H] in CSR edge order). */
 static void gt_row_scores(int64_t i, int h, int H, int D, const int32_t *indptr,
                           const int32_t *indices, const double *Q, const double *K,
-                          double *s) {
+                          const double *B, double *s) {
     int64_t b = indptr[i], en = indptr[i + 1];
     const double *q = Q + ((size_t)i * H + h) * D;
     double inv = 1.0 / sqrt((double)D);
@@ -98,7 +100,7 @@ static void gt_row_scores(int64_t i, int h, int H, int D, const int32_t *indptr,
         const double *k = K + ((size_t)indices[e] * H + h) * D;
         double dot = 0.0;
         for (int d = 0; d < D; ++d) dot += q[d] * k[d];
-        s[e - b] = dot * inv;
+        s[e - b] = dot * inv + (B ? B[(size_t)e * H + h] : 0.0);
     }
 }
 
@@ -123,10 +125,11 @@ static int64_t max_degree(int64_t N, const int32_t *indptr) {
     return mx;
 }
 
-/* GT forward for the listed rows.  out_rows[r] is [H, D], lse_rows[r] is [H]. */
-int oracle_gt_fwd_rows(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
-                       const double *Q, const double *K, const double *V,
-                       int64_t nrows, const int64_t *rows, double *out_rows, double *lse_rows) {
+/* GT forward for the listed rows.  out_rows[r] is [H, D], lse_rows[r] is [H];
+ * B: optional [E, H] score bias (NULL: none). */
+static int gt_fwd_rows_impl(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                            const double *Q, const double *K, const double *V, const double *B,
+                            int64_t nrows, const int64_t *rows, double *out_rows, double *lse_rows) {
     int64_t md = max_degree(N, indptr);
     int err = 0;
 #pragma omp parallel
@@ -142,7 +145,7 @@ int oracle_gt_fwd_rows(int64_t N, const int32_t *indptr, const int32_t *indices,
                 int64_t i = rows[r];
                 int64_t b = indptr[i], n = indptr[i + 1] - b;
                 for (int h = 0; h < H; ++h) {
-                    gt_row_scores(i, h, H, D, indptr, indices, Q, K, s);
+                    gt_row_scores(i, h, H, D, indptr, indices, Q, K, B, s);
                     lse_rows[r * H + h] = softmax(n, s, p);
                     double *o = out_rows + ((size_t)r * H + h) * D;
                     for (int d = 0; d < D; ++d) o[d] = 0.0;
@@ -159,23 +162,37 @@ int oracle_gt_fwd_rows(int64_t N, const int32_t *indptr, const int32_t *indices,
     return err;
 }
 
-int oracle_gt_fwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
-                  const double *Q, const double *K, const double *V, double *out, double *lse) {
+int oracle_gt_fwd_rows(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                       const double *Q, const double *K, const double *V,
+                       int64_t nrows, const int64_t *rows, double *out_rows, double *lse_rows) {
+    return gt_fwd_rows_impl(N, indptr, indices, H, D, Q, K, V, NULL, nrows, rows, out_rows, lse_rows);
+}
+
+/* GT forward of every row; B: optional [E, H] score bias (NULL: none). */
+int oracle_gt_bias_fwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                       const double *Q, const double *K, const double *V, const double *B,
+                       double *out, double *lse) {
     int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
     if (!rows) return -1;
     for (int64_t i = 0; i < N; ++i) rows[i] = i;
-    int rc = oracle_gt_fwd_rows(N, indptr, indices, H, D, Q, K, V, N, rows, out, lse);
+    int rc = gt_fwd_rows_impl(N, indptr, indices, H, D, Q, K, V, B, N, rows, out, lse);
     free(rows);
     return rc;
+}
+
+int oracle_gt_fwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                  const double *Q, const double *K, const double *V, double *out, double *lse) {
+    return oracle_gt_bias_fwd(N, indptr, indices, H, D, Q, K, V, NULL, out, lse);
 }
 
 /* Softmax Jacobian of one row, head h.  Fills p[t] (weights), ds[t]
  * (dL/ds = p (dP - sum_t' p dP)) with dP[t] = dO_i . v_j. */
 static void gt_row_grad(int64_t i, int h, int H, int D, const int32_t *indptr,
                         const int32_t *indices, const double *Q, const double *K,
-                        const double *V, const double *dO, double *s, double *p, double *ds) {
+                        const double *V, const double *B, const double *dO, double *s, double *p,
+                        double *ds) {
     int64_t b = indptr[i], n = indptr[i + 1] - b;
-    gt_row_scores(i, h, H, D, indptr, indices, Q, K, s);
+    gt_row_scores(i, h, H, D, indptr, indices, Q, K, B, s);
     softmax(n, s, p);
     const double *g = dO + ((size_t)i * H + h) * D;
     double sum_pdp = 0.0;
@@ -213,7 +230,7 @@ int oracle_gt_bwd_dq_rows(int64_t N, const int32_t *indptr, const int32_t *indic
                     double *o = dq_rows + ((size_t)r * H + h) * D;
                     for (int d = 0; d < D; ++d) o[d] = 0.0;
                     if (n == 0) continue;
-                    gt_row_grad(i, h, H, D, indptr, indices, Q, K, V, dO, s, p, ds);
+                    gt_row_grad(i, h, H, D, indptr, indices, Q, K, V, NULL, dO, s, p, ds);
                     for (int64_t t = 0; t < n; ++t) {
                         const double *k = K + ((size_t)indices[b + t] * H + h) * D;
                         for (int d = 0; d < D; ++d) o[d] += ds[t] * k[d] * inv;
@@ -258,7 +275,7 @@ int oracle_gt_bwd_dkdv_srcs(int64_t N, const int32_t *indptr, const int32_t *ind
                     int64_t i = t_dst[te];
                     int64_t b = indptr[i], n = indptr[i + 1] - b;
                     for (int h = 0; h < H; ++h) {
-                        gt_row_grad(i, h, H, D, indptr, indices, Q, K, V, dO, s, p, ds);
+                        gt_row_grad(i, h, H, D, indptr, indices, Q, K, V, NULL, dO, s, p, ds);
                         const double *q = Q + ((size_t)i * H + h) * D;
                         const double *g = dO + ((size_t)i * H + h) * D;
                         /* every occurrence of j in row i (duplicates are separate edges) */
@@ -285,9 +302,22 @@ int oracle_gt_bwd_dkdv_srcs(int64_t N, const int32_t *indptr, const int32_t *ind
 /* Full GT backward: per row, the softmax Jacobian gives p_e and dS_e for every
  * edge; dQ_i is summed per row; dK_j and dV_j are summed per source over its
  * edges in ascending edge order (the oracle's own edge grouping). */
+int oracle_gt_bias_bwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                       const double *Q, const double *K, const double *V, const double *B,
+                       const double *dO, double *dQ, double *dK, double *dV, double *dB);
+
 int oracle_gt_bwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
                   const double *Q, const double *K, const double *V, const double *dO,
                   double *dQ, double *dK, double *dV) {
+    return oracle_gt_bias_bwd(N, indptr, indices, H, D, Q, K, V, NULL, dO, dQ, dK, dV, NULL);
+}
+
+/* As oracle_gt_bwd with the optional [E, H] score bias B; dB (if given,
+ * [E, H]) receives dL/dB = dS of every edge (the bias enters the score with
+ * unit weight). */
+int oracle_gt_bias_bwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                       const double *Q, const double *K, const double *V, const double *B,
+                       const double *dO, double *dQ, double *dK, double *dV, double *dB) {
     int64_t E = indptr[N];
     int64_t md = max_degree(N, indptr);
     double inv = 1.0 / sqrt((double)D);
@@ -316,7 +346,7 @@ int oracle_gt_bwd(int64_t N, const int32_t *indptr, const int32_t *indices, int 
                         double *o = dQ + ((size_t)i * H + h) * D;
                         for (int d = 0; d < D; ++d) o[d] = 0.0;
                         if (n == 0) continue;
-                        gt_row_grad(i, h, H, D, indptr, indices, Q, K, V, dO, s, p, ds);
+                        gt_row_grad(i, h, H, D, indptr, indices, Q, K, V, B, dO, s, p, ds);
                         for (int64_t t = 0; t < n; ++t) {
                             P[(b + t) * H + h] = p[t];
                             DS[(b + t) * H + h] = ds[t];
@@ -362,6 +392,8 @@ int oracle_gt_bwd(int64_t N, const int32_t *indptr, const int32_t *indices, int 
             }
         }
     }
+    if (!err && dB)
+        for (int64_t x = 0; x < E * H; ++x) dB[x] = DS[x];
     free(P);
     free(DS);
     free(eptr);
@@ -832,5 +864,270 @@ int oracle_rcm(int64_t N, const int32_t *indptr, const int32_t *indices, int32_t
         for (int64_t p = 0; p < N; ++p) perm[order[p]] = (int32_t)(N - 1 - p);
     }
     free(deg); free(t_indptr); free(t_dst); free(sorted); free(order); free(visited);
+    return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Rounding bound of the fp32 GATv2 backward                                 */
+/* ------------------------------------------------------------------------ */
+
+/* Rounding factor of a sum of n fp32 terms: |computed - exact| <= gam(n)
+ * times the sum of the terms' magnitudes.  The deterministic factor is
+ * n u / (1 - n u) (u = 2^-24), reached only when every rounding error has
+ * the same sign; rounding errors of independent operations behave as
+ * independent zero-mean variables, and the probabilistic analysis of Higham
+ * and Mary ("A New Approach to Probabilistic Rounding Error Analysis", SIAM
+ * J. Sci. Comput. 41, 2019) bounds the sum by lambda sqrt(n) u with
+ * probability at least 1 - 2 exp(-lambda^2 / 2) per sum.  lambda = 6 (failure
+ * probability below 3e-8 per sum); the smaller of the two factors is used. */
+static double gam(double n) {
+    const double u = 1.0 / 16777216.0, lambda = 6.0;
+    double det = n * u / (1.0 - n * u), prob = lambda * sqrt(n > 1.0 ? n : 1.0) * u;
+    return det < prob ? det : prob;
+}
+
+/* First-order bound on |fp32 result - exact result| of every GATv2 gradient
+ * (dX, dW_l, dW_r, da), for float storage of the projections (store = 1),
+ * derived for the arithmetic the layer performs in fp32:
+ *   - projections by fp32 dot products of F terms (|dFL| <= gamma_F sum |x w|
+ *     plus their storage rounding);
+ *   - per edge: z = FL_i + FR_j, e = sum_d a_d LReLU(z_d) (D terms), the
+ *     weight recomputed from the forward's lse as 2^(e log2 e - lse log2 e)
+ *     (relative error <= |de| + u (2|e| + 2|lse|) + 4u, the last for the
+ *     exponential) and normalised by the row sum Z (deg terms), and
+ *     dp = dOut_i . FR_j (D terms);
+ *   - row sums kept as sum p dp x - Delta sum p x (the destination pass),
+ *     whose rounding is gamma_(deg+2) times the sums of |p dp x| and
+ *     |Delta p x|, not of |de x|;
+ *   - the source pass's direct sums of p dOut_i + de a LReLU'(z) over each
+ *     source's destinations; da summed over all rows (gamma_N); dX over 2 H D
+ *     products and dW over N nodes.
+ * Every sum of n terms is bounded by gam(n) times the sum of the magnitudes
+ * of its terms (any summation order; gam is the probabilistic factor above);
+ * errors carried in are propagated to first order and add up worst-case.  LeakyReLU branches decided differently by the two sides are not
+ * covered here (oracle_gatv2_branch_slack bounds them).  Outputs: bX [N, F],
+ * bWl, bWr [F, H*D], bda [H, D]. */
+int oracle_gatv2_bwd_bound(int64_t N, int F, int H, int D, const int32_t *indptr,
+                           const int32_t *indices, const double *X, const double *Wl,
+                           const double *Wr, const double *a, double slope, const double *dO,
+                           double *bX, double *bWl, double *bWr, double *bda) {
+    const double u = 1.0 / 16777216.0;
+    int HD = H * D;
+    int64_t E = indptr[N];
+    int64_t md = max_degree(N, indptr);
+    double *FL = (double *)malloc(sizeof(double) * (size_t)(N * HD + 1));
+    double *FR = (double *)malloc(sizeof(double) * (size_t)(N * HD + 1));
+    double *bFL = (double *)malloc(sizeof(double) * (size_t)(N * HD + 1));
+    double *bFR = (double *)malloc(sizeof(double) * (size_t)(N * HD + 1));
+    double *dFL = (double *)calloc((size_t)(N * HD + 1), sizeof(double));   /* |exact dFL| */
+    double *dFR = (double *)calloc((size_t)(N * HD + 1), sizeof(double));   /* |exact dFR| */
+    double *eFL = (double *)calloc((size_t)(N * HD + 1), sizeof(double));   /* bound on dFL */
+    double *eFR = (double *)calloc((size_t)(N * HD + 1), sizeof(double));   /* bound on dFR */
+    double *mFR = (double *)calloc((size_t)(N * HD + 1), sizeof(double));   /* sum of |terms| of dFR */
+    double *lse = (double *)malloc(sizeof(double) * (size_t)(N * H + 1));
+    double *delta = (double *)malloc(sizeof(double) * (size_t)(N * H + 1));
+    double *bdelta = (double *)malloc(sizeof(double) * (size_t)(N * H + 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *rho = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *bdp = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *rowda = (double *)calloc((size_t)HD + 1, sizeof(double));      /* sum over rows of |row da| */
+    int err = (!FL || !FR || !bFL || !bFR || !dFL || !dFR || !eFL || !eFR || !mFR || !lse ||
+               !delta || !bdelta || !s || !p || !rho || !dp || !bdp || !rowda) ? -1 : 0;
+    if (!err) {
+        oracle_matmul(N, F, HD, X, Wl, FL);
+        oracle_matmul(N, F, HD, X, Wr, FR);
+        for (int64_t n = 0; n < N; ++n)
+            for (int c = 0; c < HD; ++c) {
+                double ml = 0.0, mr = 0.0;
+                for (int f = 0; f < F; ++f) {
+                    ml += fabs(X[(size_t)n * F + f] * Wl[(size_t)f * HD + c]);
+                    mr += fabs(X[(size_t)n * F + f] * Wr[(size_t)f * HD + c]);
+                }
+                /* fp32 accumulation of F products, plus the storage rounding of both sides */
+                bFL[(size_t)n * HD + c] = gam(F) * ml + 2.0 * u * fabs(FL[(size_t)n * HD + c]);
+                bFR[(size_t)n * HD + c] = gam(F) * mr + 2.0 * u * fabs(FR[(size_t)n * HD + c]);
+            }
+        round_storage(N * HD, FL, 1);
+        round_storage(N * HD, FR, 1);
+        for (int x = 0; x < HD; ++x) bda[x] = 0.0;
+        /* destination rows: dFL, Delta, da */
+        for (int64_t i = 0; i < N; ++i) {
+            int64_t b = indptr[i], n = indptr[i + 1] - b;
+            for (int h = 0; h < H; ++h) {
+                if (n == 0) { lse[i * H + h] = 0.0; delta[i * H + h] = 0.0; bdelta[i * H + h] = 0.0; continue; }
+                const double *fl = FL + ((size_t)i * H + h) * D;
+                const double *bfl = bFL + ((size_t)i * H + h) * D;
+                const double *ah = a + (size_t)h * D;
+                const double *g = dO + ((size_t)i * H + h) * D;
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < n; ++t) {
+                    const double *fr = FR + ((size_t)indices[b + t] * H + h) * D;
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d) acc += ah[d] * lrelu(fl[d] + fr[d], slope);
+                    s[t] = acc;
+                    if (acc > mx) mx = acc;
+                }
+                double Z = 0.0;
+                for (int64_t t = 0; t < n; ++t) Z += exp(s[t] - mx);
+                double L = mx + log(Z);
+                lse[i * H + h] = L;
+                double rmax = 0.0, C = 0.0, mC = 0.0, bC = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    int64_t j = indices[b + t];
+                    const double *fr = FR + ((size_t)j * H + h) * D;
+                    const double *bfr = bFR + ((size_t)j * H + h) * D;
+                    double be = 0.0, me = 0.0, dpv = 0.0, mdp = 0.0, bd = 0.0;
+                    for (int d = 0; d < D; ++d) {
+                        double z = fl[d] + fr[d], lz = lrelu(z, slope);
+                        double bz = bfl[d] + bfr[d] + u * fabs(z);
+                        be += fabs(ah[d]) * (bz + u * fabs(lz));
+                        me += fabs(ah[d] * lz);
+                        dpv += g[d] * fr[d];
+                        mdp += fabs(g[d] * fr[d]);
+                        bd += fabs(g[d]) * bfr[d];
+                    }
+                    be += gam(D) * me;
+                    p[t] = exp(s[t] - L);
+                    rho[t] = be + u * (2.0 * fabs(s[t]) + 2.0 * fabs(L)) + 4.0 * u;
+                    if (rho[t] > rmax) rmax = rho[t];
+                    dp[t] = dpv;
+                    bdp[t] = bd + gam(D) * mdp;
+                    C += p[t] * dpv;
+                    mC += p[t] * fabs(dpv);
+                }
+                /* normalisation by Z: every weight also carries Z's relative error */
+                for (int64_t t = 0; t < n; ++t) rho[t] += rmax + gam((double)n) + u;
+                for (int64_t t = 0; t < n; ++t) bC += rho[t] * p[t] * fabs(dp[t]) + p[t] * bdp[t];
+                bC += gam((double)n) * mC;
+                delta[i * H + h] = C;
+                bdelta[i * H + h] = bC;
+                /* dFL and da of this row from the decomposed sums */
+                for (int d = 0; d < D; ++d) {
+                    double eA = 0.0, magA = 0.0, magB = 0.0, ex = 0.0, gda = 0.0, ega = 0.0, mga = 0.0, mgb = 0.0;
+                    for (int64_t t = 0; t < n; ++t) {
+                        int64_t j = indices[b + t];
+                        double fr = FR[((size_t)j * H + h) * D + d];
+                        double z = fl[d] + fr, lp = lrelu_grad(z, slope), lz = lrelu(z, slope);
+                        double bz = bfl[d] + bFR[((size_t)j * H + h) * D + d] + u * fabs(z);
+                        double de = p[t] * (dp[t] - C);
+                        double bde = rho[t] * p[t] * fabs(dp[t] - C) + p[t] * (bdp[t] + bC) +
+                                     2.0 * u * p[t] * fabs(dp[t] - C);
+                        ex += de * lp;
+                        eA += bde * lp;
+                        magA += p[t] * fabs(dp[t]) * lp;
+                        magB += p[t] * lp;
+                        gda += de * lz;
+                        ega += bde * fabs(lz) + fabs(de) * bz;
+                        mga += p[t] * fabs(dp[t] * lz);
+                        mgb += p[t] * fabs(lz);
+                    }
+                    double gm = gam((double)n + 2.0);
+                    double vFL = ah[d] * ex;
+                    dFL[(size_t)i * HD + h * D + d] = fabs(vFL);
+                    eFL[(size_t)i * HD + h * D + d] =
+                        fabs(ah[d]) * (eA + gm * (magA + fabs(C) * magB)) + 2.0 * u * fabs(vFL);
+                    rowda[h * D + d] += fabs(gda);
+                    bda[h * D + d] += ega + gm * (mga + fabs(C) * mgb) + u * fabs(gda);
+                }
+            }
+        }
+        /* source columns: dFR = sum over destinations of p dOut_i + de a LReLU'(z) */
+        for (int64_t i = 0; i < N; ++i) {
+            int64_t b = indptr[i], n = indptr[i + 1] - b;
+            for (int h = 0; h < H; ++h) {
+                if (n == 0) continue;
+                const double *fl = FL + ((size_t)i * H + h) * D;
+                const double *bfl = bFL + ((size_t)i * H + h) * D;
+                const double *ah = a + (size_t)h * D;
+                const double *g = dO + ((size_t)i * H + h) * D;
+                double L = lse[i * H + h], C = delta[i * H + h], bC = bdelta[i * H + h];
+                double rmax = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    int64_t j = indices[b + t];
+                    const double *fr = FR + ((size_t)j * H + h) * D;
+                    const double *bfr = bFR + ((size_t)j * H + h) * D;
+                    double e = 0.0, be = 0.0, me = 0.0;
+                    for (int d = 0; d < D; ++d) {
+                        double z = fl[d] + fr[d], lz = lrelu(z, slope);
+                        e += ah[d] * lz;
+                        be += fabs(ah[d]) * (bfl[d] + bfr[d] + u * fabs(z) + u * fabs(lz));
+                        me += fabs(ah[d] * lz);
+                    }
+                    rho[t] = be + gam(D) * me + u * (2.0 * fabs(e) + 2.0 * fabs(L)) + 4.0 * u;
+                    if (rho[t] > rmax) rmax = rho[t];
+                    p[t] = exp(e - L);
+                }
+                for (int64_t t = 0; t < n; ++t) {
+                    int64_t j = indices[b + t];
+                    const double *fr = FR + ((size_t)j * H + h) * D;
+                    const double *bfr = bFR + ((size_t)j * H + h) * D;
+                    double dpv = 0.0, mdp = 0.0, bd = 0.0;
+                    for (int d = 0; d < D; ++d) {
+                        dpv += g[d] * fr[d];
+                        mdp += fabs(g[d] * fr[d]);
+                        bd += fabs(g[d]) * bfr[d];
+                    }
+                    double r = rho[t] + rmax + gam((double)n) + 2.0 * u;   /* lse + ln Z stored in fp32 */
+                    double de = p[t] * (dpv - C);
+                    double bde = r * p[t] * fabs(dpv - C) + p[t] * (bd + gam(D) * mdp + bC) +
+                                 2.0 * u * p[t] * fabs(dpv - C);
+                    for (int d = 0; d < D; ++d) {
+                        double z = fl[d] + fr[d], lp = lrelu_grad(z, slope);
+                        size_t o = (size_t)j * HD + h * D + d;
+                        double term = p[t] * g[d] + de * ah[d] * lp;
+                        dFR[o] += term;
+                        mFR[o] += fabs(p[t] * g[d]) + fabs(de * ah[d] * lp);
+                        eFR[o] += r * p[t] * fabs(g[d]) + fabs(ah[d]) * lp * bde +
+                                  2.0 * u * (fabs(p[t] * g[d]) + fabs(de * ah[d]));
+                    }
+                }
+            }
+        }
+        /* dFR sums over each source's destinations (t_deg terms, at most N) */
+        int32_t *tdeg = (int32_t *)calloc((size_t)(N + 1), sizeof(int32_t));
+        if (!tdeg) err = -1;
+        else {
+            for (int64_t e = 0; e < E; ++e) tdeg[indices[e]]++;
+            for (int64_t j = 0; j < N; ++j)
+                for (int c = 0; c < HD; ++c) {
+                    size_t o = (size_t)j * HD + c;
+                    eFR[o] += gam((double)tdeg[j]) * mFR[o] + u * fabs(dFR[o]);
+                    dFR[o] = fabs(dFR[o]);
+                }
+            free(tdeg);
+        }
+        for (int x = 0; x < HD; ++x) bda[x] += gam((double)N) * rowda[x];
+        /* dX = dFL W_l^T + dFR W_r^T (2 H D products), dW = X^T dF (N products) */
+        for (int64_t n = 0; n < N; ++n)
+            for (int f = 0; f < F; ++f) {
+                double be = 0.0, mg = 0.0;
+                for (int c = 0; c < HD; ++c) {
+                    size_t o = (size_t)n * HD + c;
+                    double wl = fabs(Wl[(size_t)f * HD + c]), wr = fabs(Wr[(size_t)f * HD + c]);
+                    be += eFL[o] * wl + eFR[o] * wr;
+                    mg += dFL[o] * wl + dFR[o] * wr;
+                }
+                bX[(size_t)n * F + f] = be + gam(2.0 * HD) * mg + u * mg;
+            }
+        for (int f = 0; f < F; ++f)
+            for (int c = 0; c < HD; ++c) {
+                double bl = 0.0, br = 0.0, ml = 0.0, mr = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    double x = fabs(X[(size_t)n * F + f]);
+                    size_t o = (size_t)n * HD + c;
+                    bl += x * eFL[o];
+                    br += x * eFR[o];
+                    ml += x * dFL[o];
+                    mr += x * dFR[o];
+                }
+                bWl[(size_t)f * HD + c] = bl + gam((double)N) * ml + u * ml;
+                bWr[(size_t)f * HD + c] = br + gam((double)N) * mr + u * mr;
+            }
+    }
+    free(FL); free(FR); free(bFL); free(bFR); free(dFL); free(dFR); free(eFL); free(eFR); free(mFR);
+    free(lse); free(delta); free(bdelta); free(s); free(p); free(rho); free(dp); free(bdp);
+    free(rowda);
     return err;
 }

@@ -33,6 +33,7 @@ KERNELS = {
 SGA_LAYER_ATTENTION, SGA_LAYER_MINMAX = 0, 1
 SGA_AGG_MAX, SGA_AGG_MIN = 0, 1
 SGA_SCHED_STREAM, SGA_SCHED_FEATURE, SGA_SCHED_BILEVEL = 0, 1, 2
+SGA_ORDER_DEGREE, SGA_ORDER_RCM = 0, 1
 
 ARRAYS = {
     "t_indptr": 0, "t_dst": 1, "split_rows": 2, "chunk_ptr": 3, "chunk_row": 4, "chunk_beg": 5,
@@ -54,7 +55,8 @@ class SgaError(RuntimeError):
 class PlanOpts(ctypes.Structure):
     _fields_ = [("split_threshold", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
                 ("in_features", ctypes.c_int32), ("tile_min_nnz", ctypes.c_int32),
-                ("layer", ctypes.c_int32), ("schedule", ctypes.c_int32)]
+                ("layer", ctypes.c_int32), ("schedule", ctypes.c_int32),
+                ("edge_bias", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -91,6 +93,10 @@ _SIGNATURES = {
                    _vp, _vp, _vp, _vp, _vp], _int),
     "gatv2_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int,
                    _int, _int, _f32, _int, _vp, _vp, _vp, _vp, _vp], _int),
+    "gt_attn_bias_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp,
+                          _vp, _vp], _int),
+    "gt_attn_bias_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int,
+                          _int, _vp, _vp, _vp, _vp, _vp], _int),
     "gt_attn_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp],
                             _int),
     "sga_noalloc_scratch_bytes": ([], ctypes.c_size_t),
@@ -98,6 +104,9 @@ _SIGNATURES = {
     "agg_minmax_fwd": ([_vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _vp, _vp, _vp],
                        _int),
     "agg_minmax_bwd": ([_vp, _vp, _vp, _i64, _int, _int, _int, _vp, _vp], _int),
+    "sga_reorder": ([_vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
+    "sga_relabel_csr": ([_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp], _int),
+    "sga_permute_rows": ([_vp, _i64, _i64, _vp, _int, _vp, _vp], _int),
     "sga_profile_start": ([_int], _int),
     "sga_profile_stop": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_i64)], _int),
 }
@@ -181,7 +190,7 @@ class Plan:
     def __init__(self, indptr: torch.Tensor, indices: torch.Tensor, H: int, D: int,
                  dtype=torch.bfloat16, F: int = 0, split_threshold: int = 0, chunk_len: int = 0,
                  tile_min_nnz: int = 0, layer: int = SGA_LAYER_ATTENTION,
-                 schedule: int = SGA_SCHED_STREAM, stream=None):
+                 schedule: int = SGA_SCHED_STREAM, edge_bias: bool = False, stream=None):
         _need(indptr, "indptr", torch.int32)
         _need(indices, "indices", torch.int32)
         self.indptr, self.indices = indptr, indices
@@ -192,7 +201,7 @@ class Plan:
         self.dt = SGA_F32 if dtype == torch.float32 else SGA_BF16
         self.layer = int(layer)
         opts = PlanOpts(int(split_threshold), int(chunk_len), int(F), int(tile_min_nnz),
-                        self.layer, int(schedule))
+                        self.layer, int(schedule), 1 if edge_bias else 0)
         handle = ctypes.c_void_p()
         self._h = None
         _check(_lib().sga_plan_create(_ptr(indptr), _ptr(indices), self.N, self.E, self.H, self.D,
@@ -277,6 +286,40 @@ def gt_attn_bwd(plan: Plan, Q, K, V, out, lse, dOut, dQ=None, dK=None, dV=None, 
                               plan.dt, _ptr(dQ), _ptr(dK), _ptr(dV), _stream(stream)),
            "gt_attn_bwd")
     return dQ, dK, dV
+
+
+def gt_attn_bias_fwd(plan: Plan, Q, K, V, bias, out=None, lse=None, stream=None):
+    """Graph Transformer with a per-edge, per-head score bias [E, H] float32
+    (CSR edge order): (out, lse).  The plan needs edge_bias=True."""
+    for n, t in (("Q", Q), ("K", K), ("V", V)):
+        _need(t, n, plan.dtype)
+    _need(bias, "bias", torch.float32)
+    if tuple(bias.shape) != (plan.E, plan.H):
+        raise ValueError(f"bias must be [{plan.E}, {plan.H}], got {tuple(bias.shape)}")
+    out = torch.empty_like(Q) if out is None else out
+    lse = torch.empty(Q.shape[:2], dtype=torch.float32, device=Q.device) if lse is None else lse
+    _check(_lib().gt_attn_bias_fwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V),
+                                   _ptr(bias), plan.N, plan.E, plan.H, plan.D, plan.dt, _ptr(out),
+                                   _ptr(lse), _stream(stream)), "gt_attn_bias_fwd")
+    return out, lse
+
+
+def gt_attn_bias_bwd(plan: Plan, Q, K, V, bias, out, lse, dOut, dQ=None, dK=None, dV=None,
+                     dbias=None, stream=None):
+    """(dQ, dK, dV, dbias) of the biased layer; dbias [E, H] float32."""
+    for n, t in (("Q", Q), ("K", K), ("V", V), ("out", out), ("dOut", dOut)):
+        _need(t, n, plan.dtype)
+    _need(lse, "lse", torch.float32)
+    _need(bias, "bias", torch.float32)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    dbias = torch.empty_like(bias) if dbias is None else dbias
+    _check(_lib().gt_attn_bias_bwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V),
+                                   _ptr(bias), _ptr(out), _ptr(lse), _ptr(dOut), plan.N, plan.E,
+                                   plan.H, plan.D, plan.dt, _ptr(dQ), _ptr(dK), _ptr(dV),
+                                   _ptr(dbias), _stream(stream)), "gt_attn_bias_bwd")
+    return dQ, dK, dV, dbias
 
 
 def gt_attn_fwd_noalloc(indptr, indices, Q, K, V, out=None, lse=None, stream=None):
@@ -368,6 +411,46 @@ def gatv2_bwd(plan: Plan, X, W_l, W_r, a, FL, FR, out, lse, dOut, slope: float =
                             plan.E, plan.F, plan.H, plan.D, float(slope), plan.dt, _ptr(dX),
                             _ptr(dW_l), _ptr(dW_r), _ptr(da), _stream(stream)), "gatv2_bwd")
     return dX, dW_l, dW_r, da
+
+
+# ------------------------------------------------------------ graph reordering
+
+def reorder(indptr, indices, method: str = "rcm", stream=None):
+    """perm [N] int32 on the device: the new id of every node under the
+    ordering ("rcm": reverse Cuthill-McKee, "degree": descending in-degree)."""
+    _need(indptr, "indptr", torch.int32)
+    _need(indices, "indices", torch.int32)
+    N = indptr.numel() - 1
+    perm = torch.empty(max(N, 1), dtype=torch.int32, device=indptr.device)
+    code = {"degree": SGA_ORDER_DEGREE, "rcm": SGA_ORDER_RCM}[method]
+    _check(_lib().sga_reorder(_ptr(indptr), _ptr(indices), N, indices.numel(), code, _ptr(perm),
+                              _stream(stream)), "sga_reorder")
+    return perm[:N]
+
+
+def relabel_csr(indptr, indices, perm, stream=None):
+    """(new_indptr, new_indices): row perm[v] = old row v, sources mapped."""
+    for n, t in (("indptr", indptr), ("indices", indices), ("perm", perm)):
+        _need(t, n, torch.int32)
+    N = indptr.numel() - 1
+    new_ptr = torch.empty_like(indptr)
+    new_idx = torch.empty_like(indices)
+    _check(_lib().sga_relabel_csr(_ptr(indptr), _ptr(indices), N, indices.numel(), _ptr(perm),
+                                  _ptr(new_ptr), _ptr(new_idx), _stream(stream)), "sga_relabel_csr")
+    return new_ptr, new_idx
+
+
+def permute_rows(x, perm, inverse: bool = False, out=None, stream=None):
+    """Rows of a node tensor under perm: out[perm[v]] = x[v] (inverse:
+    out[v] = x[perm[v]])."""
+    _need(x, "x")
+    _need(perm, "perm", torch.int32)
+    out = torch.empty_like(x) if out is None else out
+    N = x.shape[0]
+    row_bytes = x.numel() // max(N, 1) * x.element_size()
+    _check(_lib().sga_permute_rows(_ptr(x), N, row_bytes, _ptr(perm), 1 if inverse else 0,
+                                   _ptr(out), _stream(stream)), "sga_permute_rows")
+    return out
 
 
 # ------------------------------------------------------- min / max aggregation

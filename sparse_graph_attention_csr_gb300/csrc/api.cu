@@ -63,6 +63,7 @@ void compute_layout(sga_plan *p) {
     L.bwd_row = take((size_t)p->rows.n_chunks * (p->F > 0 ? 4 : 2) * HD * 4);
     L.bwd_rowc = take((size_t)p->rows.n_chunks * p->H * 2 * 4);
     if (p->tiles.min_nnz > 0) L.zt = take((size_t)p->N * p->H * 4);
+    if (p->edge_bias) L.bias_t = take((size_t)p->E * p->H * 4);
     L.bwd_col = take((size_t)p->cols.n_chunks * 2 * HD * 4);
     if (p->F > 0) {
         L.da_blocks = da_blocks_for(p->num_sms);
@@ -186,6 +187,9 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     if (o.layer != SGA_LAYER_ATTENTION && o.layer != SGA_LAYER_MINMAX) return SGA_EINVAL;
     if (o.layer == SGA_LAYER_MINMAX && (o.in_features != 0 || o.tile_min_nnz != 0)) return SGA_EINVAL;
     if (o.schedule < SGA_SCHED_STREAM || o.schedule > SGA_SCHED_BILEVEL) return SGA_EINVAL;
+    if (o.edge_bias != 0 && o.edge_bias != 1) return SGA_EINVAL;
+    if (o.edge_bias && (o.layer != SGA_LAYER_ATTENTION || o.in_features != 0 || o.tile_min_nnz != 0))
+        return SGA_EUNSUPPORTED;
     if (o.tile_min_nnz > 0 && (!bsr_fwd_supported(dt, D) || N > (1 << 18) || o.tile_min_nnz > 128 * 16))
         return SGA_EUNSUPPORTED;
     if (o.in_features != 0 && (o.in_features % 8 != 0 || o.in_features > 1024))
@@ -199,6 +203,7 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     p->F = o.in_features;
     p->layer = o.layer;
     p->schedule = o.schedule;
+    p->edge_bias = o.edge_bias;
     p->dt = dt;
     p->split_threshold = o.split_threshold > 0 ? o.split_threshold : 256;
     p->chunk_len = o.chunk_len > 0 ? o.chunk_len : 128;
@@ -368,7 +373,10 @@ static GtArgs gt_args(const sga_plan *p) {
         a.ws_rowc = ws_at<float>(p, p->layout.bwd_rowc);
         a.ws_col = ws_at<float>(p, p->layout.bwd_col);
         a.ws_lse = ws_at<float>(p, p->layout.lse_n);
+        if (p->edge_bias) a.bias_t = ws_at<float>(p, p->layout.bias_t);
     }
+    a.E = p->E;
+    a.t_eid = p->t_eid;
     return a;
 }
 
@@ -474,6 +482,54 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
         if (e == cudaSuccess) e = launch_bsr_bwd_dkdv(b, s);
         return cuda_status(e);
     }
+    return cuda_status(dt == SGA_F32 ? gt_bwd_t<float>(a, s) : gt_bwd_t<__nv_bfloat16>(a, s));
+}
+
+sga_status gt_attn_bias_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *indices,
+                            const void *Q, const void *K, const void *V, const float *bias,
+                            int64_t N, int64_t E, int H, int D, sga_dtype dt, void *out, float *lse,
+                            void *stream) {
+    if (p && (p->layer != SGA_LAYER_ATTENTION || !p->edge_bias)) return SGA_EINVAL;
+    sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, 0);
+    if (st != SGA_OK) return st;
+    if (p->schedule != SGA_SCHED_STREAM || p->residual) return SGA_EUNSUPPORTED;
+    if (!tensors_ok(N, {Q, K, V, out, lse})) return SGA_EINVAL;
+    if (E > 0 && (!bias || !aligned(bias, 4))) return SGA_EINVAL;
+    GtArgs a = gt_args(p);
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.out_w = out;
+    a.lse_w = lse;
+    a.bias = E > 0 ? bias : nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(dt == SGA_F32 ? gt_fwd_t<float>(a, s) : gt_fwd_t<__nv_bfloat16>(a, s));
+}
+
+sga_status gt_attn_bias_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *indices,
+                            const void *Q, const void *K, const void *V, const float *bias,
+                            const void *out, const float *lse, const void *dOut, int64_t N,
+                            int64_t E, int H, int D, sga_dtype dt, void *dQ, void *dK, void *dV,
+                            float *dbias, void *stream) {
+    if (p && (p->layer != SGA_LAYER_ATTENTION || !p->edge_bias)) return SGA_EINVAL;
+    sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, 0);
+    if (st != SGA_OK) return st;
+    if (p->residual) return SGA_EUNSUPPORTED;
+    if (!tensors_ok(N, {Q, K, V, out, lse, dOut, dQ, dK, dV})) return SGA_EINVAL;
+    if (E > 0 && (!bias || !dbias || !aligned(bias, 4) || !aligned(dbias, 4))) return SGA_EINVAL;
+    GtArgs a = gt_args(p);
+    a.Q = Q;
+    a.K = K;
+    a.V = V;
+    a.out = out;
+    a.lse = lse;
+    a.dOut = dOut;
+    a.dQ = dQ;
+    a.dK = dK;
+    a.dV = dV;
+    a.bias = E > 0 ? bias : nullptr;
+    a.dbias = dbias;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     return cuda_status(dt == SGA_F32 ? gt_bwd_t<float>(a, s) : gt_bwd_t<__nv_bfloat16>(a, s));
 }
 

@@ -19,6 +19,8 @@
 // any is used, so every lane keeps U*NC*2 sixteen-byte gathers in flight.
 #pragma once
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "items.cuh"
 #include "plan.h"
@@ -65,10 +67,14 @@ __device__ __forceinline__ bool head_sums_split(float s0, float t0, float s1, fl
 // kernel takes the largest counts that keep its registers.
 template <int NC, int NROW, int NSC = 0, int NOWN = 1, int NOSC = 0, int G = 32, int U2 = 1, int U1 = 2>
 struct RingDims {
-    static constexpr int U = NC >= 2 ? (NC == 2 ? U2 : 1) : (G < 32 ? 4 : U1);
-    static constexpr int STEP_BYTES = U * NC * 32 * (NROW * 16 + NSC * 4);
+    static constexpr int U0 = NC >= 2 ? (NC == 2 ? U2 : 1) : (G < 32 ? 4 : U1);
     static constexpr int OWN_BYTES = NC * 32 * (NOWN * 16 + NOSC * 4);
     static constexpr int QD = 3 * OWN_BYTES > 4096 ? 2 : 3;
+    // a step of U0 neighbours that leaves room for fewer than two steps
+    // (several gathered scalars per neighbour) takes two neighbours instead
+    static constexpr int U = (U0 > 2 && (13312 - QD * OWN_BYTES) / (U0 * NC * 32 * (NROW * 16 + NSC * 4)) < 2)
+                                 ? 2 : U0;
+    static constexpr int STEP_BYTES = U * NC * 32 * (NROW * 16 + NSC * 4);
     static constexpr int FIT = (13312 - QD * OWN_BYTES) / STEP_BYTES;
     static_assert(U <= 2 || FIT >= 2, "two steps of several neighbours must fit the ring");
     static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
@@ -78,18 +84,24 @@ using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>:
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD>;
 
-// gathered K, V; own Q
-template <typename T, int D, int NC, int G> using GtFwdStream = RingCfg<NC, G, 2, 0, 1, 0, 2, 4>;
-// gathered K, V; own Q, dOut, lse
-template <typename T, int D, int NC, int G> using GtDqStream = RingCfg<NC, G, 2, 0, 2, 1, 2, 4>;
-// gathered Q, dOut, lse, Delta (over the transposed CSR); own K, V
-template <typename T, int D, int NC, int G> using GtDkdvStream = RingCfg<NC, G, 2, 2, 2, 0, 1, 4>;
+// gathered K, V (and the edge's score bias); own Q
+template <typename T, int D, int NC, int G, bool BIAS = false>
+using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4>;
+// gathered K, V (and the edge's score bias); own Q, dOut, lse
+template <typename T, int D, int NC, int G, bool BIAS = false>
+using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4>;
+// gathered Q, dOut, lse, Delta (over the transposed CSR; and the edge's score
+// bias in transposed order); own K, V
+template <typename T, int D, int NC, int G, bool BIAS = false>
+using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4>;
 
-template <typename T, int D, int NC, int G>
+// With BIAS, each edge's score gains a per-head term b[e, h] (fp32, [E, H] in
+// CSR edge order): s_ij = q_i . k_j / sqrt(D) + b_eh.
+template <typename T, int D, int NC, int G, bool BIAS>
 __global__ void __launch_bounds__(256, 2)
 gt_fwd_kernel(GtArgs a, float scale2) {
     using S = GtShape<T, D, NC, G>;
-    using C = GtFwdStream<T, D, NC, G>;
+    using C = GtFwdStream<T, D, NC, G, BIAS>;
     constexpr int EL = S::EL, LH = S::LH, U = C::U;
     extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
@@ -98,6 +110,10 @@ gt_fwd_kernel(GtArgs a, float scale2) {
     arr.rows[0] = static_cast<const uint4 *>(a.K);
     arr.rows[1] = static_cast<const uint4 *>(a.V);
     arr.own[0] = static_cast<const uint4 *>(a.Q);
+    if (BIAS) {
+        arr.sc[0] = a.bias;
+        arr.sc_edge = 1u;
+    }
     EdgeStream<C> st;
     st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
             a.split_threshold, a.d_err);
@@ -125,8 +141,9 @@ gt_fwd_kernel(GtArgs a, float scale2) {
                 for (int k = 0; k < NC; ++k) {
                     float kf[EL];
                     unpack<T>(st.row(u, 0, k), kf);
-                    const float dot = group_sum<LH>(dot2<EL>(q[k], kf));
-                    sc[u][k] = ok[u] ? dot * scale2 : -INFINITY;
+                    float dot = group_sum<LH>(dot2<EL>(q[k], kf)) * scale2;
+                    if (BIAS) dot += st.scalar(u, 0, (gl + G * k) / LH) * kLog2e;
+                    sc[u][k] = ok[u] ? dot : -INFINITY;
                 }
             }
             // online softmax with a lazily moved maximum: the accumulator is
@@ -361,11 +378,11 @@ struct RowNorm {
 // sum_j p are accumulated in the same pass over the edges and the weights
 // normalised by Z at the end (RowNorm).  Split-row chunks write A, B and
 // their parts of C and Z; the merge kernel finishes them in chunk order.
-template <typename T, int D, int NC, int G>
+template <typename T, int D, int NC, int G, bool BIAS>
 __global__ void __launch_bounds__(256, 2)
 gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
     using S = GtShape<T, D, NC, G>;
-    using C = GtDqStream<T, D, NC, G>;
+    using C = GtDqStream<T, D, NC, G, BIAS>;
     constexpr int EL = S::EL, LH = S::LH, U = C::U;
     extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
@@ -376,6 +393,10 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
     arr.own[0] = static_cast<const uint4 *>(a.Q);
     arr.own[1] = static_cast<const uint4 *>(a.dOut);
     arr.osc[0] = a.lse;
+    if (BIAS) {
+        arr.sc[0] = a.bias;
+        arr.sc_edge = 1u;
+    }
     EdgeStream<C> st;
     st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
             a.split_threshold, a.d_err);
@@ -417,7 +438,9 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                     }
                     float sdot, dp;
                     const bool hi = head_sums_split<LH>(sd[0], dv[0], sd[1], dv[1], sdot, dp);
-                    const float p = ok ? exp2f(sdot * scale2 - (hi ? lse2[1] : lse2[0])) : 0.f;
+                    float arg = sdot * scale2 - (hi ? lse2[1] : lse2[0]);
+                    if (BIAS) arg += st.scalar(u, 0, (gl + G * (hi ? 1 : 0)) / LH) * kLog2e;
+                    const float p = ok ? exp2f(arg) : 0.f;
                     const float pdp = p * dp;
                     const float po = __shfl_xor_sync(SGA_FULL_MASK, p, LH / 2);
                     const float pdpo = __shfl_xor_sync(SGA_FULL_MASK, pdp, LH / 2);
@@ -438,7 +461,9 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                         unpack<T>(st.row(u, 1, k), vf);
                         float sdot = dot2<EL>(q[k], kf), dp = dot2<EL>(go[k], vf);
                         group_sum2<LH>(sdot, dp);
-                        const float p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
+                        float arg = sdot * scale2 - lse2[k];
+                        if (BIAS) arg += st.scalar(u, 0, (gl + G * k) / LH) * kLog2e;
+                        const float p = ok ? exp2f(arg) : 0.f;
                         const float pdp = p * dp;
                         c[k] += pdp;
                         z[k] += p;
@@ -506,11 +531,12 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
 // p = 2^(s2 - lse2_i), dS = p (dOut_i . v_j - Delta_i),
 // dV_j += p dOut_i, dK_j += dS q_i, with the dQ pass's normalised lse_i
 // (lse_i + ln Z_i) and Delta_i.
-template <typename T, int D, int NC, int G>
+template <typename T, int D, int NC, int G, bool BIAS>
 __global__ void __launch_bounds__(256, 2)
 gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
     using S = GtShape<T, D, NC, G>;
-    using C = GtDkdvStream<T, D, NC, G>;
+    using C = GtDkdvStream<T, D, NC, G, BIAS>;
+    constexpr int NG = C::NG, STEP = C::STEP;
     constexpr int EL = S::EL, LH = S::LH, U = C::U;
     extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
@@ -522,12 +548,19 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
     arr.sc[1] = a.ws_delta;
     arr.own[0] = static_cast<const uint4 *>(a.K);
     arr.own[1] = static_cast<const uint4 *>(a.V);
+    if (BIAS) {
+        arr.sc[2] = a.bias_t;   // the bias in transposed-CSR order
+        arr.sc_edge = 4u;
+    }
     EdgeStream<C> st;
     st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.cols, a.t_indptr, a.t_dst, a.N, a.H, R, LH,
             a.split_threshold, a.d_err);
     StreamItem it;
     while (st.next_item(it)) {
         float kj[NC][EL], vj[NC][EL], dk[NC][EL], dv[NC][EL];
+        // transposed position of the item's first edge (bias gradient output)
+        int32_t tbeg = 0;
+        if (BIAS) tbeg = it.partial ? __ldg(a.cols.chunk_beg + it.item) : __ldg(a.t_indptr + it.row);
 #pragma unroll
         for (int k = 0; k < NC; ++k)
 #pragma unroll
@@ -551,10 +584,17 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
                     float sdot = dot2<EL>(qf, kj[k]), dp = dot2<EL>(gf, vj[k]);
                     group_sum2<LH>(sdot, dp);
                     const int h = (gl + G * k) / LH;
-                    const float p = ok ? exp2f(sdot * scale2 - st.scalar(u, 0, h) * kLog2e) : 0.f;
+                    float arg = sdot * scale2 - st.scalar(u, 0, h) * kLog2e;
+                    if (BIAS) arg += st.scalar(u, 2, h) * kLog2e;
+                    const float p = ok ? exp2f(arg) : 0.f;
                     const float ds = p * (dp - st.scalar(u, 1, h));
                     axpy2<EL>(dv[k], p, gf);
                     axpy2<EL>(dk[k], ds, qf);
+                    if (BIAS && ok && (gl + G * k) % LH == 0 && gl + G * k < R) {
+                        // dL/db = dS, at the edge's position in CSR order
+                        const int32_t te = tbeg + step * STEP + g + NG * u;
+                        a.dbias[(size_t)__ldg(a.t_eid + te) * a.H + h] = ds;
+                    }
                 }
             }
             st.release_step();
@@ -733,7 +773,7 @@ template <int LH, int MAXNC, typename F> cudaError_t dispatch_shape(int R, F &&f
 
 template <typename T> constexpr int max_nc() { return sizeof(T) == 4 ? 8 : 4; }
 
-template <typename T, int D> cudaError_t gt_fwd_d(const GtArgs &a, cudaStream_t s) {
+template <typename T, int D, bool BIAS> cudaError_t gt_fwd_db(const GtArgs &a, cudaStream_t s) {
     constexpr int LH = D * (int)sizeof(T) / 16;
     const int R = a.H * D / Elt<T>::EL;
     const float scale2 = kLog2e / sqrtf((float)D);
@@ -741,7 +781,8 @@ template <typename T, int D> cudaError_t gt_fwd_d(const GtArgs &a, cudaStream_t 
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
         note_launch(SGA_KERN_GT_FWD, s, false);
-        const cudaError_t e = launch_streamed<GtFwdStream<T, D, NC, G>, gt_fwd_kernel<T, D, NC, G>>(items, s, a, scale2);
+        const cudaError_t e = launch_streamed<GtFwdStream<T, D, NC, G, BIAS>, gt_fwd_kernel<T, D, NC, G, BIAS>>(
+            items, s, a, scale2);
         note_launch(SGA_KERN_GT_FWD, s, true);
         return e;
     });
@@ -752,7 +793,22 @@ template <typename T, int D> cudaError_t gt_fwd_d(const GtArgs &a, cudaStream_t 
     return cudaGetLastError();
 }
 
-template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t s) {
+template <typename T, int D> cudaError_t gt_fwd_d(const GtArgs &a, cudaStream_t s) {
+    return a.bias ? gt_fwd_db<T, D, true>(a, s) : gt_fwd_db<T, D, false>(a, s);
+}
+
+// bias_t[te, h] = bias[t_eid[te], h]: the score bias in transposed-CSR order
+static __global__ void bias_transpose_kernel(const float *__restrict__ bias, const int32_t *__restrict__ t_eid,
+                                      int64_t E, int H, float *__restrict__ bias_t) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t n = E * H;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += stride) {
+        const int64_t te = x / H;
+        bias_t[x] = bias[(size_t)__ldg(t_eid + te) * H + (x - te * H)];
+    }
+}
+
+template <typename T, int D, bool BIAS> cudaError_t gt_bwd_db(const GtArgs &a, cudaStream_t s) {
     constexpr int LH = D * (int)sizeof(T) / 16;
     const int R = a.H * D / Elt<T>::EL;
     const float scale = 1.0f / sqrtf((float)D);
@@ -761,9 +817,18 @@ template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t 
         const int64_t items_r = (int64_t)a.rows.n_chunks + a.N;
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
         if (items_r == 0) return cudaSuccess;
+        if (BIAS) {
+            const int64_t n = a.E * a.H;
+            if (n > 0) {
+                const unsigned g = (unsigned)std::min<int64_t>((n + 255) / 256, 8192);
+                bias_transpose_kernel<<<g, 256, 0, s>>>(a.bias, a.t_eid, a.E, a.H, a.bias_t);
+                const cudaError_t e0 = cudaGetLastError();
+                if (e0 != cudaSuccess) return e0;
+            }
+        }
         note_launch(SGA_KERN_GT_BWD_DQ, s, false);
-        cudaError_t e = launch_streamed<GtDqStream<T, D, NC, G>, gt_bwd_dq_kernel<T, D, NC, G>>(items_r, s, a,
-                                                                                            scale2, scale);
+        cudaError_t e = launch_streamed<GtDqStream<T, D, NC, G, BIAS>, gt_bwd_dq_kernel<T, D, NC, G, BIAS>>(
+            items_r, s, a, scale2, scale);
         note_launch(SGA_KERN_GT_BWD_DQ, s, true);
         if (e != cudaSuccess) return e;
         if (a.rows.n_split > 0) {   // Delta of split rows is needed by the dK/dV pass
@@ -773,7 +838,8 @@ template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t 
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         note_launch(SGA_KERN_GT_BWD_DKDV, s, false);
-        e = launch_streamed<GtDkdvStream<T, D, NC, G>, gt_bwd_dkdv_kernel<T, D, NC, G>>(items_c, s, a, scale2, scale);
+        e = launch_streamed<GtDkdvStream<T, D, NC, G, BIAS>, gt_bwd_dkdv_kernel<T, D, NC, G, BIAS>>(
+            items_c, s, a, scale2, scale);
         note_launch(SGA_KERN_GT_BWD_DKDV, s, true);
         if (e != cudaSuccess) return e;
         if (a.cols.n_split > 0) {
@@ -784,6 +850,10 @@ template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t 
         }
         return e;
     });
+}
+
+template <typename T, int D> cudaError_t gt_bwd_d(const GtArgs &a, cudaStream_t s) {
+    return a.bias ? gt_bwd_db<T, D, true>(a, s) : gt_bwd_db<T, D, false>(a, s);
 }
 
 template <typename T> cudaError_t gt_fwd_t(const GtArgs &a, cudaStream_t s) {

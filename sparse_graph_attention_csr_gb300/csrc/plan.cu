@@ -210,6 +210,19 @@ __global__ void radix_scatter_kernel(const int32_t *__restrict__ keys,
     }
 }
 
+__global__ void iota_edges_kernel(int32_t *__restrict__ x, int64_t n) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += stride) x[e] = (int32_t)e;
+}
+
+// t_dst[te] = row of CSR edge t_eid[te]
+__global__ void gather_rows_kernel(const int32_t *__restrict__ rows, const int32_t *__restrict__ t_eid,
+                                   int64_t n, int32_t *__restrict__ t_dst) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t te = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; te < n; te += stride)
+        t_dst[te] = rows[t_eid[te]];
+}
+
 __global__ void count_sources_kernel(const int32_t *__restrict__ indices, int64_t E,
                                      int32_t *__restrict__ counts) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -327,6 +340,7 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
     p->d_err = own.get<int32_t>(1);
     p->t_indptr = own.get<int32_t>(N + 1);
     p->t_dst = own.get<int32_t>(E);
+    if (p->edge_bias) p->t_eid = own.get<int32_t>(E);
     if (own.err != cudaSuccess) {
         set_cuda_error(own.err);
         own.release();
@@ -368,7 +382,12 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
     SGA_TRY(tmp.err);
     if (E > 0) {
         SGA_TRY(cudaMemcpyAsync(ka, p->indices, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
-        edge_rows_kernel<<<grid_for(N * 32, 256, INT32_MAX), 256, 0, s>>>(p->indptr, N, va);
+        // values: the destination of every edge, or (edge-bias plans) the
+        // edge itself, whose destination is looked up after the sort
+        if (p->edge_bias)
+            iota_edges_kernel<<<grid_for(E, 256, 8192), 256, 0, s>>>(va, E);
+        else
+            edge_rows_kernel<<<grid_for(N * 32, 256, INT32_MAX), 256, 0, s>>>(p->indptr, N, va);
         SGA_TRY(cudaGetLastError());
         int bits = 1;
         while (bits < 31 && ((int64_t)1 << bits) < N) ++bits;
@@ -383,7 +402,14 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
             std::swap(ka, kb);
             std::swap(va, vb);
         }
-        SGA_TRY(cudaMemcpyAsync(p->t_dst, va, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
+        if (p->edge_bias) {
+            SGA_TRY(cudaMemcpyAsync(p->t_eid, va, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
+            edge_rows_kernel<<<grid_for(N * 32, 256, INT32_MAX), 256, 0, s>>>(p->indptr, N, kb);
+            gather_rows_kernel<<<grid_for(E, 256, 8192), 256, 0, s>>>(kb, va, E, p->t_dst);
+            SGA_TRY(cudaGetLastError());
+        } else {
+            SGA_TRY(cudaMemcpyAsync(p->t_dst, va, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
+        }
     }
     SGA_TRY(cudaMemsetAsync(p->t_indptr, 0, sizeof(int32_t) * (N + 1), s));
     if (E > 0) {

@@ -27,6 +27,7 @@ struct WorkspaceLayout {
     size_t delta = 0;      // [N, H] f32          Delta_i = dOut_i . out_i (normalised weights)
     size_t lse_n = 0;      // [N, H] f32          lse_i + ln Z_i (backward row normalisation)
     size_t zt = 0;         // [N, H] f32          block-sparse plans: tile part of Z_i
+    size_t bias_t = 0;     // [E, H] f32          edge-bias plans: the bias in transposed order
     size_t fwd_ml = 0;     // [n_chunks, H, 2] f32 chunk softmax stats (max, sum), log2 units
     size_t fwd_acc = 0;    // [n_chunks, H*D] f32  chunk unnormalised accumulators
     size_t bwd_row = 0;    // [n_chunks, 4, H*D] f32 chunk partial sums (dQ: A, B; dFL: A, B, da A, B)
@@ -81,6 +82,8 @@ struct sga_plan {
     const int32_t *indices = nullptr;
     int32_t *t_indptr = nullptr;       // [N + 1]
     int32_t *t_dst = nullptr;          // [E]
+    int32_t *t_eid = nullptr;          // [E] CSR edge of each transposed entry (edge-bias plans)
+    int edge_bias = 0;                 // plan serves gt_attn_bias_fwd/bwd
     sga::Partition rows, cols;         // partitions of the CSR and the transposed CSR
     sga::TileSet tiles;                // block-sparse split (tiles.min_nnz > 0)
     sga_plan *residual = nullptr;      // plan over the residual CSR (block-sparse plans)
@@ -132,6 +135,13 @@ struct GtArgs {
     // the share of edges that another pass (the block-sparse tiles)
     // handles; nullptr: none
     const float *delta_in, *z_in;
+    // optional score bias [E, H] fp32 (CSR order; nullptr: none), its copy in
+    // transposed order (workspace), the transposed position -> CSR edge map,
+    // and the bias gradient dL/db [E, H] fp32
+    const float *bias;
+    float *bias_t, *dbias;
+    const int32_t *t_eid;
+    int64_t E;
     int32_t *d_err;
 };
 template <typename T> cudaError_t gt_fwd_t(const GtArgs &a, cudaStream_t s);

@@ -7,8 +7,8 @@
 // warp).  For every step the warp's "producer" copies, with cp.async, the
 // gathered rows of the step's neighbours (NROW arrays of R sixteen-byte
 // chunks per node; lane l of a group copies chunks l, l + G, ...) and their
-// per-head scalars (NSC arrays of [N, H] fp32; lane h < H of a group copies
-// head h) into a ring of DEPTH step
+// per-head scalars (NSC arrays of [N, H] fp32, or [E, H] indexed by the edge's
+// CSR position; lane h < H of a group copies head h) into a ring of DEPTH step
 // slots; the "consumer" (the same warp, later) computes on slot t while the
 // copies of steps t+1 .. t+DEPTH-1 are in flight.  An item's own rows (NOWN
 // arrays) and own scalars (NOSC) are copied when the item is queued, so the
@@ -56,6 +56,7 @@ __device__ __forceinline__ void cp_wait_newer(int n) {
 
 template <int NC_, int G_, int U_, int NROW_, int NSC_, int NOWN_, int NOSC_, int DEPTH_, int QD_>
 struct StreamCfg {
+    static_assert(NSC_ <= 3, "at most three gathered scalar arrays");
     static constexpr int NC = NC_, G = G_, U = U_, NROW = NROW_, NSC = NSC_, NOWN = NOWN_,
                          NOSC = NOSC_, DEPTH = DEPTH_, QD = QD_;
     static constexpr int NG = 32 / G, STEP = NG * U;
@@ -95,9 +96,10 @@ struct StreamItem {
 
 struct StreamArrays {
     const uint4 *rows[4];   // gathered node rows, [N][R] sixteen-byte chunks
-    const float *sc[2];     // gathered per-head scalars, [N][H]
+    const float *sc[3];     // gathered per-head scalars, [N][H] (or [E][H], see sc_edge)
     const uint4 *own[2];    // the item's own rows
     const float *osc[2];    // the item's own scalars
+    uint32_t sc_edge;       // bit s set: sc[s] is indexed by the edge's CSR position, not its node
 };
 
 template <typename C> struct EdgeStream {
@@ -249,9 +251,11 @@ template <typename C> struct EdgeStream {
                 }
             if (gl < H)
 #pragma unroll
-                for (int s = 0; s < C::NSC; ++s)
+                for (int s = 0; s < C::NSC; ++s) {
+                    const size_t at = ((arr.sc_edge >> s) & 1u) ? (size_t)(p_beg + e) : (size_t)j;
                     cp4_async(sa + C::OFF_SC + slot * C::SC_SLOT + ((u * C::NSC + s) * 32 + lane) * 4,
-                              ok ? arr.sc[s] + (size_t)j * H + gl : arr.sc[s], ok);
+                              ok ? arr.sc[s] + at * H + gl : arr.sc[s], ok);
+                }
             masks[u] = __ballot_sync(SGA_FULL_MASK, ok);
         }
         if (lane == 0) {

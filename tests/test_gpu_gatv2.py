@@ -49,21 +49,28 @@ def check(indptr, indices, F, H, D, dtype, X, Wl, Wr, a, dO, split=0, chunk=0, s
     compare(lse, rlse, dtype, "lse")
     dX, dWl, dWr, da = sga.gatv2_bwd(plan, gX, gWl, gWr, ga, FL, FR, out, lse, gdO, slope)
     g = oracle.gatv2_bwd(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope, store=dtype)
-    # dX, dW and da are sums over many edges or nodes of terms that carry the
-    # fp32 rounding of the recomputed weights (relative ~1e-6): in fp32 the
-    # bound gains 1e-5 |ref| + 4e-6 max|ref| (about 64 float ulps of the
-    # largest entry).  bf16 keeps the stated 2e-2 + 1e-2 |ref|.
-    # LeakyReLU branches left undecided by the projections' storage precision
-    # may go either way: the oracle's slack bounds their effect.
-    rt, nm = (1e-5, 4e-6) if dtype == "f32" else (None, 0.0)
-    sl = oracle.gatv2_branch_slack(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope,
-                                   store=dtype)
-    compare(dX, g["dX"], dtype, "dX", rtol=rt, norm=nm, slack=sl["dX"])
-    compare(dWl, g["dW_l"], dtype, "dW_l", rtol=rt, norm=nm, slack=sl["dW_l"])
-    compare(dWr, g["dW_r"], dtype, "dW_r", rtol=rt, norm=nm, slack=sl["dW_r"])
-    compare(da, g["da"], dtype, "da", rtol=rt, norm=nm, slack=sl["da"])
+    check_grads(indptr, indices, X, Wl, Wr, a, dO, slope, dtype, g, dX, dWl, dWr, da)
     assert plan.device_error() == 0
     return plan
+
+
+def check_grads(indptr, indices, X, Wl, Wr, a, dO, slope, dtype, g, dX, dWl, dWr, da):
+    """bf16: the stated 2e-2 + 1e-2 |ref|.  fp32 (not one of the workloads):
+    dX, dW and da are sums over many edges or nodes whose terms cancel, so no
+    fixed fp32 tolerance holds per element; the check is 1e-5 plus the
+    oracle's first-order rounding bound of the fp32 backward (derived from
+    the arithmetic, loose).  LeakyReLU branches left undecided by the
+    projections' storage precision may go either way: the oracle's slack
+    bounds their effect."""
+    sl = oracle.gatv2_branch_slack(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope,
+                                   store=dtype)
+    if dtype == "f32":
+        b = oracle.gatv2_bwd_bound(indptr, indices, X[1], Wl[1], Wr[1], a[1], dO[1], slope)
+        sl = {k: sl[k] + b[k] for k in sl}
+    compare(dX, g["dX"], dtype, "dX", slack=sl["dX"])
+    compare(dWl, g["dW_l"], dtype, "dW_l", slack=sl["dW_l"])
+    compare(dWr, g["dW_r"], dtype, "dW_r", slack=sl["dW_r"])
+    compare(da, g["da"], dtype, "da", slack=sl["da"])
 
 
 def test_small_workload_matches_oracle():

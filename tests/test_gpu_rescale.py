@@ -26,6 +26,7 @@ import sparse_graph_attention_csr_gb300 as sga
 from sparse_graph_attention_csr_gb300 import synth
 
 from helpers import TORCH_DT, compare, dev
+from test_gpu_gatv2 import check_grads
 
 pytestmark = pytest.mark.gpu
 
@@ -217,12 +218,8 @@ def test_gatv2_rising_scores(dtype, levels):
     compare(lse, rl, dtype, "lse")
     dX, dWl, dWr, da = sga.gatv2_bwd(plan, gX, gWl, gWr, ga, gFL, gFR, out, lse, gdO, 0.2)
     g = oracle.gatv2_bwd(base_ptr, indices, xf, wlf, wrf, af, dof, 0.2, store=dtype)
-    sl = oracle.gatv2_branch_slack(base_ptr, indices, xf, wlf, wrf, af, dof, 0.2, store=dtype)
-    rt, nm = (1e-5, 4e-6) if dtype == "f32" else (None, 0.0)
-    compare(dX, g["dX"], dtype, "dX", rtol=rt, norm=nm, slack=sl["dX"])
-    compare(dWl, g["dW_l"], dtype, "dW_l", rtol=rt, norm=nm, slack=sl["dW_l"])
-    compare(dWr, g["dW_r"], dtype, "dW_r", rtol=rt, norm=nm, slack=sl["dW_r"])
-    compare(da, g["da"], dtype, "da", rtol=rt, norm=nm, slack=sl["da"])
+    check_grads(base_ptr, indices, (X, xf), (Wl, wlf), (Wr, wrf), (a, af), (dO, dof), 0.2, dtype,
+                g, dX, dWl, dWr, da)
     assert plan.device_error() == 0
 
 

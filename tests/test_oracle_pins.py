@@ -675,3 +675,131 @@ def test_relabelled_graph_is_equivariant():
         o2, l2 = oracle.gt_fwd(ip2, ix2, P(Q), P(K), P(V))
         np.testing.assert_allclose(o2, P(o1), atol=1e-12)
         np.testing.assert_allclose(l2, P(l1), atol=1e-12)
+
+
+# ------------------------------------- rounding bound of the fp32 GATv2 backward
+
+def fp32_dense_gatv2_grads(indptr, indices, X, Wl, Wr, a, dO, slope=0.2):
+    """An independent fp32 evaluation: torch autograd of the dense form,
+    every tensor float32 (projections, scores, softmax, gradients)."""
+    N = X.shape[0]
+    H, D = a.shape
+    tX, tWl, tWr, ta = (torch.from_numpy(x).float().requires_grad_() for x in (X, Wl, Wr, a))
+    FL = (tX @ tWl).reshape(N, H, D)
+    FR = (tX @ tWr).reshape(N, H, D)
+    z = FL[:, None] + FR[None, :]
+    e = (torch.nn.functional.leaky_relu(z, slope) * ta).sum(-1).permute(2, 0, 1)
+    e = e.masked_fill(~dense_mask(indptr, indices, N)[None], float("-inf"))
+    p = torch.exp(e - torch.logsumexp(e, -1)[..., None]).nan_to_num(0.0)
+    out = torch.einsum("hij,jhd->ihd", p, FR)
+    (out * torch.from_numpy(dO).float()).sum().backward()
+    return {"dX": tX.grad, "dW_l": tWl.grad, "dW_r": tWr.grad, "da": ta.grad}
+
+
+@pytest.mark.parametrize("seed,ascale", [(1, 1.0), (2, 4.0), (3, 8.0)])
+def test_gatv2_fp32_bound_covers_an_fp32_evaluation_and_is_not_vacuous(seed, ascale):
+    """The first-order rounding bound of the fp32 backward holds for an
+    independent fp32 evaluation (with the LeakyReLU branch slack of float
+    storage) and stays below 5% of the largest gradient.  It adds carried
+    errors worst-case, so it is loose (about 10^3 times the errors an fp32
+    evaluation shows): at the workloads' attention-vector scale (0.1 per
+    element) it still separates a one-edge mistake, at larger scales it no
+    longer does -- fp32 GATv2 gradient checks are consistency checks."""
+    rng = np.random.default_rng(seed)
+    N, F, H, D = 80, 16, 2, 16
+    indptr, indices = rand_graph(rng, N, 0.15)
+    lim = math.sqrt(6 / (F + H * D))
+    f32 = lambda x: x.astype(np.float32).astype(np.float64)
+    X = f32(rng.standard_normal((N, F)))
+    Wl, Wr = f32(rng.uniform(-lim, lim, (F, H * D))), f32(rng.uniform(-lim, lim, (F, H * D)))
+    a = f32(rng.standard_normal((H, D)) * ascale / math.sqrt(D))
+    dO = f32(rng.standard_normal((N, H, D)))
+    g = oracle.gatv2_bwd(indptr, indices, X, Wl, Wr, a, dO, 0.2, store="f32")
+    b = oracle.gatv2_bwd_bound(indptr, indices, X, Wl, Wr, a, dO, 0.2)
+    sl = oracle.gatv2_branch_slack(indptr, indices, X, Wl, Wr, a, dO, 0.2, store="f32")
+    t = fp32_dense_gatv2_grads(indptr, indices, X, Wl, Wr, a, dO)
+    # one edge dropped (row 0 loses its last source): a plausible indexing mistake
+    ip2 = indptr.copy()
+    ip2[1:] -= 1
+    ix2 = np.delete(indices, indptr[1] - 1)
+    g2 = oracle.gatv2_bwd(ip2, ix2, X, Wl, Wr, a, dO, 0.2, store="f32")
+    for k in ("dX", "dW_l", "dW_r", "da"):
+        err = np.abs(t[k].double().numpy() - g[k])
+        assert np.all(err <= b[k] + sl[k]), k
+        assert b[k].max() < 0.05 * np.abs(g[k]).max(), k
+        if ascale == 1.0:
+            assert np.any(np.abs(g2[k] - g[k]) > 10 * (b[k] + sl[k])), k
+
+
+# ------------------------------------------------- Graph Transformer with edge bias
+
+def edge_rows(indptr):
+    return np.repeat(np.arange(len(indptr) - 1), np.diff(indptr))
+
+
+def test_gt_bias_complete_graph_equals_sdpa_with_float_mask():
+    """The additive score bias is scaled_dot_product_attention's float
+    attn_mask on a complete graph (every row lists every node once)."""
+    rng = np.random.default_rng(61)
+    N, H, D = 9, 3, 8
+    indptr = (np.arange(N + 1) * N).astype(np.int32)
+    indices = np.tile(np.arange(N), N).astype(np.int32)
+    Q, K, V = (rng.standard_normal((N, H, D)) for _ in range(3))
+    B = rng.standard_normal((N * N, H)) * 2.0
+    out, lse = oracle.gt_bias_fwd(indptr, indices, Q, K, V, B)
+    mask = torch.from_numpy(B.reshape(N, N, H).transpose(2, 0, 1).copy())   # [H, i, j]
+    t = lambda x: torch.from_numpy(x).permute(1, 0, 2)                      # [H, N, D]
+    ref = torch.nn.functional.scaled_dot_product_attention(t(Q), t(K), t(V), attn_mask=mask)
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), atol=1e-12)
+
+
+def test_gt_bias_backward_matches_autograd():
+    rng = np.random.default_rng(62)
+    N, H, D = 22, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.25)
+    E = len(indices)
+    Q, K, V, dO = (rng.standard_normal((N, H, D)) for _ in range(4))
+    B = rng.standard_normal((E, H)) * 3.0
+    dQ, dK, dV, dB = oracle.gt_bias_bwd(indptr, indices, Q, K, V, B, dO)
+    tq, tk, tv = (torch.from_numpy(x).requires_grad_() for x in (Q, K, V))
+    tb = torch.from_numpy(B).requires_grad_()
+    rows = torch.from_numpy(edge_rows(indptr))
+    cols = torch.from_numpy(indices.astype(np.int64))
+    s = torch.einsum("ihd,jhd->hij", tq, tk) / math.sqrt(D)
+    bias = torch.zeros(H, N, N, dtype=torch.float64).index_put((torch.arange(H)[:, None].expand(H, E),
+                                                                 rows[None].expand(H, E),
+                                                                 cols[None].expand(H, E)), tb.T)
+    mask = dense_mask(indptr, indices, N)
+    s = (s + bias).masked_fill(~mask[None], float("-inf"))
+    p = torch.exp(s - torch.logsumexp(s, -1)[..., None]).nan_to_num(0.0)
+    out = torch.einsum("hij,jhd->ihd", p, tv)
+    (out * torch.from_numpy(dO)).sum().backward()
+    np.testing.assert_allclose(dQ, tq.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dK, tk.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dV, tv.grad.numpy(), atol=1e-11)
+    np.testing.assert_allclose(dB, tb.grad.numpy(), atol=1e-11)
+
+
+def test_gt_bias_special_cases():
+    """Zero bias is the plain layer; a bias constant over a row (per head)
+    leaves the output unchanged and shifts lse by that constant; the bias
+    gradient of each row and head sums to zero (softmax Jacobian)."""
+    rng = np.random.default_rng(63)
+    N, H, D = 30, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.2, dups=True)
+    E = len(indices)
+    Q, K, V, dO = (rng.standard_normal((N, H, D)) for _ in range(4))
+    o0, l0 = oracle.gt_fwd(indptr, indices, Q, K, V)
+    ob, lb = oracle.gt_bias_fwd(indptr, indices, Q, K, V, np.zeros((E, H)))
+    np.testing.assert_array_equal(ob, o0)
+    np.testing.assert_array_equal(lb, l0)
+    c = rng.standard_normal((N, H))
+    oc, lc = oracle.gt_bias_fwd(indptr, indices, Q, K, V, c[edge_rows(indptr)])
+    np.testing.assert_allclose(oc, o0, atol=1e-12)
+    fin = np.isfinite(l0)
+    np.testing.assert_allclose(lc[fin], (l0 + c)[fin], atol=1e-12)
+    B = rng.standard_normal((E, H))
+    dB = oracle.gt_bias_bwd(indptr, indices, Q, K, V, B, dO)[3]
+    sums = np.zeros((N, H))
+    np.add.at(sums, edge_rows(indptr), dB)
+    np.testing.assert_allclose(sums, 0.0, atol=1e-12)
