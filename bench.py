@@ -73,6 +73,9 @@ def parse_args(argv=None):
     p.add_argument("--reorder", choices=["none", "rcm", "degree"], default="none",
                    help="relabel the graph and node inputs once (outside the timed region) "
                         "with this ordering before planning")
+    p.add_argument("--row-order", type=int, default=0, choices=[0, 1, 2],
+                   help="walking order of the edge kernels: 0 default (= 1), 1 descending degree, "
+                        "2 ascending id")
     p.add_argument("--tile-min-nnz", type=int, default=0,
                    help="> 0: block-sparse tensor-core forward (GT, bf16) with this tile threshold")
     p.add_argument("--nodes", type=int, default=0,
@@ -271,7 +274,7 @@ class Workload:
     """Host inputs (pinned), device inputs, plan and step functions."""
 
     def __init__(self, key: int, device, split_threshold=0, chunk_len=0, tile_min_nnz=0, nodes=0,
-                 schedule=0, reorder="none"):
+                 schedule=0, reorder="none", row_order=0):
         import sparse_graph_attention_csr_gb300 as sga
         self.sga = sga
         self.w = synth.WORKLOADS[key]
@@ -332,7 +335,8 @@ class Workload:
                              split_threshold=split_threshold, chunk_len=chunk_len,
                              tile_min_nnz=tile_min_nnz,
                              layer=sga.SGA_LAYER_MINMAX if w.layer.startswith("agg")
-                             else sga.SGA_LAYER_ATTENTION, schedule=schedule)
+                             else sga.SGA_LAYER_ATTENTION, schedule=schedule, row_order=row_order)
+        self.row_order = row_order
         self.schedule = schedule
         torch.cuda.synchronize()
         self.plan_ms = (time.perf_counter() - t0) * 1e3
@@ -560,7 +564,7 @@ def run_native(args, ws, rank, local):
     sga_build.build()
     dev = torch.device("cuda", local)
     wl = Workload(args.config, dev, args.split_threshold, args.chunk_len, args.tile_min_nnz, args.nodes,
-                  args.schedule, args.reorder)
+                  args.schedule, args.reorder, args.row_order)
     w = wl.w
     stream = torch.cuda.current_stream(dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -723,7 +727,8 @@ def run_native(args, ws, rank, local):
                    "plan_build_ms": round(wl.plan_ms, 2),
                    "tile_min_nnz": wl.tile_min_nnz,
                    "schedule": ["stream", "feature", "bilevel"][wl.schedule],
-                   "reorder": wl.reorder, "reorder_ms": round(wl.reorder_ms, 2)},
+                   "reorder": wl.reorder, "reorder_ms": round(wl.reorder_ms, 2),
+                   "row_order": "ascending id" if wl.row_order == 2 else "descending degree"},
         "roofline": roof,
         "memory": memory,
         "block_sparse": bsr,

@@ -62,7 +62,8 @@ typedef struct sga_plan sga_plan;
 /* Layer a plan serves (its workspace layout). */
 typedef enum {
     SGA_LAYER_ATTENTION = 0,  /* Graph Transformer (in_features = 0) or GATv2 (in_features > 0) */
-    SGA_LAYER_MINMAX = 1      /* min / max neighbourhood aggregation (agg_minmax_fwd/bwd) */
+    SGA_LAYER_MINMAX = 1,     /* min / max neighbourhood aggregation (agg_minmax_fwd/bwd) */
+    SGA_LAYER_GAT = 2         /* GAT edge attention (gat_attn_fwd/bwd) */
 } sga_layer;
 
 /* Plan options.  Zero (or a NULL pointer) selects the default of each field. */
@@ -75,6 +76,10 @@ typedef struct {
     int32_t schedule;         /* sga_schedule of the Graph Transformer CSR forward (default 0) */
     int32_t edge_bias;        /* 1: the plan also serves gt_attn_bias_fwd/bwd (keeps the CSR edge
                                  of every transposed entry: 4 more bytes per edge) */
+    int32_t row_order;        /* order in which the edge kernels walk rows (and transposed rows):
+                                 1 (default): by descending degree, ties by id (long rows first
+                                 balances the persistent warps); 2: by ascending id.  Results are
+                                 bit-identical either way */
 } sga_plan_opts;
 
 /* Thread mapping of the Graph Transformer forward over the CSR (the backward
@@ -162,6 +167,28 @@ sga_status gt_attn_bias_bwd(const sga_plan *plan, const int32_t *indptr, const i
                             const void *out, const float *lse, const void *dOut, int64_t N,
                             int64_t E, int H, int D, sga_dtype dt, void *dQ, void *dK, void *dV,
                             float *dbias, void *stream);
+
+/* GAT edge attention (the original graph attention score; GAT and the Graph
+ * Transformer are the attention GNNs DF-GNN's abstract names): with the
+ * projected features Fv [N, H, D] (in dt) and the two per-node halves of the
+ * score el, er [N, H] (float32; el_i = a_l . Fv_i, er_j = a_r . Fv_j, dense
+ * per-node dots the caller computes),
+ *   e_ij = LeakyReLU_slope(el_i + er_j), p = softmax over the row,
+ *   out_i = sum_j p_ij Fv_j, lse as above.
+ * The backward returns the edge stage's gradients: dFv [N, H, D] (in dt; the
+ * value path, sum over j's destinations of p dOut_i), del, der [N, H]
+ * float32; the layer's dFL = dFv + a_l del + a_r der and the projection's
+ * gradients are dense follow-ups.  Needs a plan built with
+ * opts->layer = SGA_LAYER_GAT. */
+sga_status gat_attn_fwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                        const void *Fv, const float *el, const float *er, int64_t N, int64_t E,
+                        int H, int D, float slope, sga_dtype dt, void *out, float *lse,
+                        void *stream);
+sga_status gat_attn_bwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
+                        const void *Fv, const float *el, const float *er, const void *out,
+                        const float *lse, const void *dOut, int64_t N, int64_t E, int H, int D,
+                        float slope, sga_dtype dt, void *dFv, float *del, float *der,
+                        void *stream);
 
 /* GATv2 forward: FL = X W_l, FR = X W_r (X [N, F], W [F, H*D], FL/FR written as
  * [N, H, D] and kept for the backward pass); e_ij = sum_d a[h,d]
@@ -339,7 +366,10 @@ typedef enum {
     SGA_ARR_TILE_COL = 13,    /* [n_tiles] */
     SGA_ARR_TILE_BITS = 14,   /* [n_tiles*64]: the [n_tiles][128] uint16 masks, as int32 words */
     SGA_ARR_R_INDPTR = 15,    /* [N+1] residual CSR */
-    SGA_ARR_R_INDICES = 16    /* [E_residual] */
+    SGA_ARR_R_INDICES = 16,   /* [E_residual] */
+    SGA_ARR_ROW_ORDER = 17,   /* [N] walking order of the rows (row_order plans) */
+    SGA_ARR_T_ROW_ORDER = 18, /* [N] walking order of the transposed rows */
+    SGA_ARR_T_EID = 19        /* [E] CSR edge of each transposed entry (edge-bias plans) */
 } sga_plan_array;
 
 /* Copy one plan array into caller HOST memory of `count` int32 (must equal the
@@ -363,7 +393,8 @@ typedef enum {
     SGA_KERN_BSR_BWD_DKDV = 18,
     SGA_KERN_AGG_FWD = 19, SGA_KERN_AGG_FWD_MERGE = 20, SGA_KERN_AGG_BWD = 21,
     SGA_KERN_AGG_BWD_CAST = 22,
-    SGA_KERN_COUNT = 23
+    SGA_KERN_GAT_FWD = 23, SGA_KERN_GAT_BWD_DST = 24, SGA_KERN_GAT_BWD_SRC = 25,
+    SGA_KERN_COUNT = 26
 } sga_kernel_id;
 
 /* Time one kernel kind with CUDA events recorded on the launching stream

@@ -82,6 +82,14 @@ def _load():
             "oracle_agg_fwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _I32P], _int),
             "oracle_agg_bwd": ([_i64, _int, _I32P, _F64P, _F64P], _int),
             "oracle_rcm": ([_i64, _I32P, _I32P, _I32P], _int),
+            "oracle_gat_edge_fwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P, _dbl, _F64P,
+                                     _F64P], _int),
+            "oracle_gat_edge_bwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P, _dbl, _F64P,
+                                     _F64P, _F64P, _F64P], _int),
+            "oracle_gat_fwd": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P, _F64P, _dbl, _int,
+                                _F64P, _F64P, _F64P], _int),
+            "oracle_gat_bwd": ([_i64, _int, _int, _int, _I32P, _I32P, _F64P, _F64P, _F64P, _dbl, _int,
+                                _F64P, _F64P, _F64P, _F64P, _F64P], _int),
             "oracle_gt_bias_fwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P, _F64P,
                                     _F64P, _F64P], _int),
             "oracle_gt_bias_bwd": ([_i64, _I32P, _I32P, _int, _int, _F64P, _F64P, _F64P, _F64P,
@@ -322,6 +330,63 @@ def gatv2_branch_slack(indptr, indices, X, Wl, Wr, a, dO, slope=0.2, store="bf16
                                              float(slope), _STORE[store], float(tau), dO,
                                              sX, sWl, sWr, sda), "gatv2_branch_slack")
     return {"dX": sX, "dW_l": sWl, "dW_r": sWr, "da": sda}
+
+
+# --------------------------------------------------- GAT (original attention score)
+
+def gat_fwd(indptr, indices, X, W, a, slope=0.2, store=None):
+    """(FL, out, lse) of the GAT layer: FL = X W [N, H, D] (rounded to
+    ``store`` as the layer stores it), e_ij = LeakyReLU(a[h,0] . FL_i +
+    a[h,1] . FL_j), softmax over the row, out_i = sum_j p_ij FL_j.
+    a: [H, 2, D]."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    X, W, a = _f64(X), _f64(W), _f64(a)
+    N, F = X.shape
+    H, _, D = a.shape
+    FL = np.empty((N, H, D)); out = np.empty((N, H, D)); lse = np.empty((N, H))
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    _check(_load().oracle_gat_fwd(N, F, H, D, indptr, ix, X, W, a, float(slope), _STORE[store],
+                                  FL, out, lse), "gat_fwd")
+    return FL, out, lse
+
+
+def gat_bwd(indptr, indices, X, W, a, dO, slope=0.2, store=None):
+    """dict with dX [N, F], dW [F, H*D], da [H, 2, D], dFL [N, H, D]."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    X, W, a, dO = _f64(X), _f64(W), _f64(a), _f64(dO)
+    N, F = X.shape
+    H, _, D = a.shape
+    dX = np.empty((N, F)); dW = np.empty((F, H * D)); da = np.empty((H, 2, D))
+    dFL = np.empty((N, H, D))
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    _check(_load().oracle_gat_bwd(N, F, H, D, indptr, ix, X, W, a, float(slope), _STORE[store], dO,
+                                  dX, dW, da, dFL), "gat_bwd")
+    return {"dX": dX, "dW": dW, "da": da, "dFL": dFL}
+
+
+def gat_edge_fwd(indptr, indices, Fv, el, er, slope=0.2):
+    """GAT edge stage: (out [N, H, D], lse [N, H]) from the projected
+    features Fv [N, H, D] and the score halves el, er [N, H]."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    Fv, el, er = _f64(Fv), _f64(el), _f64(er)
+    N, H, D = Fv.shape
+    out = np.empty((N, H, D)); lse = np.empty((N, H))
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    _check(_load().oracle_gat_edge_fwd(N, indptr, ix, H, D, Fv, el, er, float(slope), out, lse),
+           "gat_edge_fwd")
+    return out, lse
+
+
+def gat_edge_bwd(indptr, indices, Fv, el, er, dO, slope=0.2):
+    """(dFv, del, der) of the GAT edge stage (dFv: the value path only)."""
+    indptr, indices = _i32(indptr), _i32(indices)
+    Fv, el, er, dO = _f64(Fv), _f64(el), _f64(er), _f64(dO)
+    N, H, D = Fv.shape
+    dFv = np.empty((N, H, D)); de_l = np.empty((N, H)); de_r = np.empty((N, H))
+    ix = indices if len(indices) else np.zeros(1, np.int32)
+    _check(_load().oracle_gat_edge_bwd(N, indptr, ix, H, D, Fv, el, er, float(slope), dO, dFv, de_l,
+                                       de_r), "gat_edge_bwd")
+    return dFv, de_l, de_r
 
 
 # ------------------------------------------------------- min / max aggregation

@@ -1131,3 +1131,242 @@ int oracle_gatv2_bwd_bound(int64_t N, int F, int H, int D, const int32_t *indptr
     free(rowda);
     return err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* GAT (the original graph attention score)                                  */
+/* ------------------------------------------------------------------------ */
+
+/* The GAT layer of the AT-GNN family named by "DF-GNN: Dynamic Fusion
+ * Framework for Attention Graph Neural Networks on GPUs" (abstract), in its
+ * usual per-head form: FL = X W ([N, F] x [F, H*D], stored with the rounding
+ * `store`), el_i = a[h,0,:] . FL_i, er_j = a[h,1,:] . FL_j (a is [H, 2, D]:
+ * the destination and source halves of the attention vector),
+ * e_ij = LeakyReLU(el_i + er_j), p = softmax over the row, out_i =
+ * sum_j p_ij FL_j, lse as for the other layers. */
+static void gat_row(int64_t i, int h, int H, int D, const int32_t *indptr, const int32_t *indices,
+                    const double *FL, const double *a, double slope, double *s) {
+    const double *al = a + ((size_t)h * 2 + 0) * D, *ar = a + ((size_t)h * 2 + 1) * D;
+    const double *fi = FL + ((size_t)i * H + h) * D;
+    double el = 0.0;
+    for (int d = 0; d < D; ++d) el += al[d] * fi[d];
+    for (int64_t e = indptr[i]; e < indptr[i + 1]; ++e) {
+        const double *fj = FL + ((size_t)indices[e] * H + h) * D;
+        double er = 0.0;
+        for (int d = 0; d < D; ++d) er += ar[d] * fj[d];
+        s[e - indptr[i]] = lrelu(el + er, slope);
+    }
+}
+
+int oracle_gat_fwd(int64_t N, int F, int H, int D, const int32_t *indptr, const int32_t *indices,
+                   const double *X, const double *W, const double *a, double slope, int store,
+                   double *FL, double *out, double *lse) {
+    int HD = H * D;
+    int64_t md = max_degree(N, indptr);
+    oracle_matmul(N, F, HD, X, W, FL);
+    round_storage(N * HD, FL, store);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+        double *p = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+        if (!s || !p) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for schedule(dynamic, 64)
+            for (int64_t i = 0; i < N; ++i) {
+                int64_t b = indptr[i], n = indptr[i + 1] - b;
+                for (int h = 0; h < H; ++h) {
+                    gat_row(i, h, H, D, indptr, indices, FL, a, slope, s);
+                    lse[i * H + h] = softmax(n, s, p);
+                    double *o = out + ((size_t)i * H + h) * D;
+                    for (int d = 0; d < D; ++d) o[d] = 0.0;
+                    for (int64_t t = 0; t < n; ++t) {
+                        const double *fj = FL + ((size_t)indices[b + t] * H + h) * D;
+                        for (int d = 0; d < D; ++d) o[d] += p[t] * fj[d];
+                    }
+                }
+            }
+        }
+        free(s);
+        free(p);
+    }
+    return err;
+}
+
+/* GAT backward by the chain rule (the storage rounding of FL passes
+ * gradients unchanged, as for GATv2):
+ *   dp = dO_i . FL_j, Delta_i = sum p dp, de = p (dp - Delta_i),
+ *   dz = de LeakyReLU'(el_i + er_j),
+ *   del_i = sum_j dz (over the row), der_j = sum_i dz (over j's destinations),
+ *   dFL_n = sum over edges with source n of p dO_i  +  a_l del_n  +  a_r der_n,
+ *   da[h,0,:] = sum_n del_n FL_n,  da[h,1,:] = sum_n der_n FL_n,
+ *   dX = dFL W^T,  dW = X^T dFL.
+ * Edges are visited in CSR order; per-node sums are accumulated in that
+ * order (serial).  Outputs dX [N, F], dW [F, H*D], da [H, 2, D], dFL. */
+int oracle_gat_bwd(int64_t N, int F, int H, int D, const int32_t *indptr, const int32_t *indices,
+                   const double *X, const double *W, const double *a, double slope, int store,
+                   const double *dO, double *dX, double *dW, double *da, double *dFL) {
+    int HD = H * D;
+    int64_t md = max_degree(N, indptr);
+    double *FL = (double *)malloc(sizeof(double) * (size_t)(N * HD + 1));
+    double *del = (double *)calloc((size_t)(N * H + 1), sizeof(double));
+    double *der = (double *)calloc((size_t)(N * H + 1), sizeof(double));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    int err = (!FL || !del || !der || !s || !p || !dp) ? -1 : 0;
+    if (!err) {
+        oracle_matmul(N, F, HD, X, W, FL);
+        round_storage(N * HD, FL, store);
+        for (int64_t x = 0; x < N * HD; ++x) dFL[x] = 0.0;
+        for (int64_t i = 0; i < N; ++i) {
+            int64_t b = indptr[i], n = indptr[i + 1] - b;
+            for (int h = 0; h < H; ++h) {
+                if (n == 0) continue;
+                gat_row(i, h, H, D, indptr, indices, FL, a, slope, s);
+                softmax(n, s, p);
+                const double *g = dO + ((size_t)i * H + h) * D;
+                double delta = 0.0;
+                for (int64_t t = 0; t < n; ++t) {
+                    const double *fj = FL + ((size_t)indices[b + t] * H + h) * D;
+                    double v = 0.0;
+                    for (int d = 0; d < D; ++d) v += g[d] * fj[d];
+                    dp[t] = v;
+                    delta += p[t] * v;
+                }
+                /* recover the pre-activation el + er of each edge for LeakyReLU' */
+                const double *al = a + ((size_t)h * 2 + 0) * D, *ar = a + ((size_t)h * 2 + 1) * D;
+                const double *fi = FL + ((size_t)i * H + h) * D;
+                double el = 0.0;
+                for (int d = 0; d < D; ++d) el += al[d] * fi[d];
+                for (int64_t t = 0; t < n; ++t) {
+                    int64_t j = indices[b + t];
+                    const double *fj = FL + ((size_t)j * H + h) * D;
+                    double er = 0.0;
+                    for (int d = 0; d < D; ++d) er += ar[d] * fj[d];
+                    double de = p[t] * (dp[t] - delta);
+                    double dz = de * lrelu_grad(el + er, slope);
+                    del[i * H + h] += dz;
+                    der[j * H + h] += dz;
+                    double *dj = dFL + ((size_t)j * H + h) * D;
+                    for (int d = 0; d < D; ++d) dj[d] += p[t] * g[d];
+                }
+            }
+        }
+        for (int64_t n = 0; n < N; ++n)
+            for (int h = 0; h < H; ++h) {
+                const double *al = a + ((size_t)h * 2 + 0) * D, *ar = a + ((size_t)h * 2 + 1) * D;
+                double *dn = dFL + ((size_t)n * H + h) * D;
+                for (int d = 0; d < D; ++d) dn[d] += al[d] * del[n * H + h] + ar[d] * der[n * H + h];
+            }
+        for (int64_t x = 0; x < 2 * HD; ++x) da[x] = 0.0;
+        for (int64_t n = 0; n < N; ++n)
+            for (int h = 0; h < H; ++h)
+                for (int d = 0; d < D; ++d) {
+                    double f = FL[((size_t)n * H + h) * D + d];
+                    da[((size_t)h * 2 + 0) * D + d] += del[n * H + h] * f;
+                    da[((size_t)h * 2 + 1) * D + d] += der[n * H + h] * f;
+                }
+#pragma omp parallel for schedule(static)
+        for (int64_t n = 0; n < N; ++n)
+            for (int f = 0; f < F; ++f) {
+                double acc = 0.0;
+                for (int c = 0; c < HD; ++c) acc += dFL[(size_t)n * HD + c] * W[(size_t)f * HD + c];
+                dX[(size_t)n * F + f] = acc;
+            }
+#pragma omp parallel for schedule(static)
+        for (int f = 0; f < F; ++f) {
+            double *gw = dW + (size_t)f * HD;
+            for (int c = 0; c < HD; ++c) gw[c] = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double x = X[(size_t)n * F + f];
+                for (int c = 0; c < HD; ++c) gw[c] += x * dFL[(size_t)n * HD + c];
+            }
+        }
+    }
+    free(FL); free(del); free(der); free(s); free(p); free(dp);
+    return err;
+}
+
+/* GAT edge stage on given inputs: Fv [N, H, D] (the projected features),
+ * el, er [N, H]: e_ij = LeakyReLU(el_i + er_j), p = softmax over the row,
+ * out_i = sum_j p_ij Fv_j, lse.  Backward: dFv (the value path only:
+ * dFv_j = sum over j's destinations of p dO_i), del_i = sum_j dz_ij,
+ * der_j = sum_i dz_ij with dz = p (dO_i . Fv_j - Delta_i) LeakyReLU'(el_i + er_j);
+ * the layer-level gradients follow by the chain rule through el = a_l . FL,
+ * er = a_r . FL and FL = X W (oracle_gat_bwd). */
+int oracle_gat_edge_fwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                        const double *Fv, const double *el, const double *er, double slope,
+                        double *out, double *lse) {
+    int64_t md = max_degree(N, indptr);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+        double *p = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+        if (!s || !p) {
+#pragma omp atomic write
+            err = -1;
+        } else {
+#pragma omp for schedule(dynamic, 64)
+            for (int64_t i = 0; i < N; ++i) {
+                int64_t b = indptr[i], n = indptr[i + 1] - b;
+                for (int h = 0; h < H; ++h) {
+                    for (int64_t t = 0; t < n; ++t)
+                        s[t] = lrelu(el[i * H + h] + er[(int64_t)indices[b + t] * H + h], slope);
+                    lse[i * H + h] = softmax(n, s, p);
+                    double *o = out + ((size_t)i * H + h) * D;
+                    for (int d = 0; d < D; ++d) o[d] = 0.0;
+                    for (int64_t t = 0; t < n; ++t) {
+                        const double *v = Fv + ((size_t)indices[b + t] * H + h) * D;
+                        for (int d = 0; d < D; ++d) o[d] += p[t] * v[d];
+                    }
+                }
+            }
+        }
+        free(s);
+        free(p);
+    }
+    return err;
+}
+
+int oracle_gat_edge_bwd(int64_t N, const int32_t *indptr, const int32_t *indices, int H, int D,
+                        const double *Fv, const double *el, const double *er, double slope,
+                        const double *dO, double *dFv, double *del, double *der) {
+    int64_t md = max_degree(N, indptr);
+    double *s = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *p = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    double *dp = (double *)malloc(sizeof(double) * (size_t)(md + 1));
+    if (!s || !p || !dp) { free(s); free(p); free(dp); return -1; }
+    for (int64_t x = 0; x < N * H * D; ++x) dFv[x] = 0.0;
+    for (int64_t x = 0; x < N * H; ++x) { del[x] = 0.0; der[x] = 0.0; }
+    for (int64_t i = 0; i < N; ++i) {
+        int64_t b = indptr[i], n = indptr[i + 1] - b;
+        for (int h = 0; h < H; ++h) {
+            if (n == 0) continue;
+            for (int64_t t = 0; t < n; ++t)
+                s[t] = lrelu(el[i * H + h] + er[(int64_t)indices[b + t] * H + h], slope);
+            softmax(n, s, p);
+            const double *g = dO + ((size_t)i * H + h) * D;
+            double delta = 0.0;
+            for (int64_t t = 0; t < n; ++t) {
+                const double *v = Fv + ((size_t)indices[b + t] * H + h) * D;
+                double x = 0.0;
+                for (int d = 0; d < D; ++d) x += g[d] * v[d];
+                dp[t] = x;
+                delta += p[t] * x;
+            }
+            for (int64_t t = 0; t < n; ++t) {
+                int64_t j = indices[b + t];
+                double dz = p[t] * (dp[t] - delta) * lrelu_grad(el[i * H + h] + er[j * H + h], slope);
+                del[i * H + h] += dz;
+                der[j * H + h] += dz;
+                double *dj = dFv + ((size_t)j * H + h) * D;
+                for (int d = 0; d < D; ++d) dj[d] += p[t] * g[d];
+            }
+        }
+    }
+    free(s); free(p); free(dp);
+    return 0;
+}

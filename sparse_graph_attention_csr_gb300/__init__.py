@@ -28,9 +28,10 @@ KERNELS = {
     "gatv2_bwd_src": 10, "gatv2_bwd_merge": 11, "gatv2_bwd_dx": 12, "gatv2_bwd_dw": 13,
     "gatv2_bwd_reduce": 14, "bsr_fwd": 15, "bsr_bwd_delta": 16, "bsr_bwd_dq": 17,
     "bsr_bwd_dkdv": 18, "agg_fwd": 19, "agg_fwd_merge": 20, "agg_bwd": 21, "agg_bwd_cast": 22,
+    "gat_fwd": 23, "gat_bwd_dst": 24, "gat_bwd_src": 25,
 }
 
-SGA_LAYER_ATTENTION, SGA_LAYER_MINMAX = 0, 1
+SGA_LAYER_ATTENTION, SGA_LAYER_MINMAX, SGA_LAYER_GAT = 0, 1, 2
 SGA_AGG_MAX, SGA_AGG_MIN = 0, 1
 SGA_SCHED_STREAM, SGA_SCHED_FEATURE, SGA_SCHED_BILEVEL = 0, 1, 2
 SGA_ORDER_DEGREE, SGA_ORDER_RCM = 0, 1
@@ -39,7 +40,7 @@ ARRAYS = {
     "t_indptr": 0, "t_dst": 1, "split_rows": 2, "chunk_ptr": 3, "chunk_row": 4, "chunk_beg": 5,
     "chunk_end": 6, "t_split_rows": 7, "t_chunk_ptr": 8, "t_chunk_row": 9, "t_chunk_beg": 10,
     "t_chunk_end": 11, "tile_ptr": 12, "tile_col": 13, "tile_bits": 14, "r_indptr": 15,
-    "r_indices": 16,
+    "r_indices": 16, "row_order": 17, "t_row_order": 18, "t_eid": 19,
 }
 
 
@@ -56,7 +57,7 @@ class PlanOpts(ctypes.Structure):
     _fields_ = [("split_threshold", ctypes.c_int32), ("chunk_len", ctypes.c_int32),
                 ("in_features", ctypes.c_int32), ("tile_min_nnz", ctypes.c_int32),
                 ("layer", ctypes.c_int32), ("schedule", ctypes.c_int32),
-                ("edge_bias", ctypes.c_int32)]
+                ("edge_bias", ctypes.c_int32), ("row_order", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -97,6 +98,10 @@ _SIGNATURES = {
                           _vp, _vp], _int),
     "gt_attn_bias_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int,
                           _int, _vp, _vp, _vp, _vp, _vp], _int),
+    "gat_attn_fwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _f32, _int, _vp, _vp,
+                      _vp], _int),
+    "gat_attn_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _f32,
+                      _int, _vp, _vp, _vp, _vp], _int),
     "gt_attn_fwd_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _vp, _vp, _vp],
                             _int),
     "sga_noalloc_scratch_bytes": ([], ctypes.c_size_t),
@@ -190,7 +195,8 @@ class Plan:
     def __init__(self, indptr: torch.Tensor, indices: torch.Tensor, H: int, D: int,
                  dtype=torch.bfloat16, F: int = 0, split_threshold: int = 0, chunk_len: int = 0,
                  tile_min_nnz: int = 0, layer: int = SGA_LAYER_ATTENTION,
-                 schedule: int = SGA_SCHED_STREAM, edge_bias: bool = False, stream=None):
+                 schedule: int = SGA_SCHED_STREAM, edge_bias: bool = False,
+                 row_order: int = 0, stream=None):
         _need(indptr, "indptr", torch.int32)
         _need(indices, "indices", torch.int32)
         self.indptr, self.indices = indptr, indices
@@ -200,8 +206,10 @@ class Plan:
         self.dtype = dtype
         self.dt = SGA_F32 if dtype == torch.float32 else SGA_BF16
         self.layer = int(layer)
+        # walking order of the edge kernels: 0 (default) / 1 descending degree, 2 ascending id
+        self.row_order, self.edge_bias = int(row_order), bool(edge_bias)
         opts = PlanOpts(int(split_threshold), int(chunk_len), int(F), int(tile_min_nnz),
-                        self.layer, int(schedule), 1 if edge_bias else 0)
+                        self.layer, int(schedule), 1 if edge_bias else 0, int(row_order))
         handle = ctypes.c_void_p()
         self._h = None
         _check(_lib().sga_plan_create(_ptr(indptr), _ptr(indices), self.N, self.E, self.H, self.D,
@@ -241,7 +249,10 @@ class Plan:
              "tile_ptr": inf["n_panels"] + 1 if inf["n_panels"] else 0,
              "tile_col": inf["n_tiles"], "tile_bits": inf["n_tiles"] * 64,
              "r_indptr": self.N + 1 if inf["n_panels"] else 0,
-             "r_indices": inf["E_residual"]}[name]
+             "r_indices": inf["E_residual"],
+             "row_order": self.N if self.row_order != 2 else 0,
+             "t_row_order": self.N if self.row_order != 2 else 0,
+             "t_eid": self.E if self.edge_bias else 0}[name]
         out = np.zeros(max(n, 1), dtype=np.int32)
         _check(_lib().sga_plan_copy_array(self._h, ARRAYS[name], out.ctypes.data, n),
                "sga_plan_copy_array")
@@ -453,6 +464,40 @@ def permute_rows(x, perm, inverse: bool = False, out=None, stream=None):
     return out
 
 
+# ------------------------------------------------------------------------- GAT
+
+def gat_attn_fwd(plan: Plan, Fv, el, er, slope: float = 0.2, out=None, lse=None, stream=None):
+    """GAT edge attention: (out [N,H,D], lse [N,H]) from the projected features
+    Fv [N,H,D] and the score halves el, er [N,H] float32.  The plan must be
+    built with layer=SGA_LAYER_GAT."""
+    _need(Fv, "Fv", plan.dtype)
+    _need(el, "el", torch.float32)
+    _need(er, "er", torch.float32)
+    out = torch.empty_like(Fv) if out is None else out
+    lse = torch.empty(Fv.shape[:2], dtype=torch.float32, device=Fv.device) if lse is None else lse
+    _check(_lib().gat_attn_fwd(plan.handle, *plan._graph()[:2], _ptr(Fv), _ptr(el), _ptr(er), plan.N,
+                               plan.E, plan.H, plan.D, float(slope), plan.dt, _ptr(out), _ptr(lse),
+                               _stream(stream)), "gat_attn_fwd")
+    return out, lse
+
+
+def gat_attn_bwd(plan: Plan, Fv, el, er, out, lse, dOut, slope: float = 0.2, stream=None):
+    """(dFv, del, der): the value-path gradient of Fv and the gradients of the
+    two score halves."""
+    for n, t in (("Fv", Fv), ("out", out), ("dOut", dOut)):
+        _need(t, n, plan.dtype)
+    for n, t in (("el", el), ("er", er), ("lse", lse)):
+        _need(t, n, torch.float32)
+    dFv = torch.empty_like(Fv)
+    de_l = torch.empty_like(el)
+    de_r = torch.empty_like(er)
+    _check(_lib().gat_attn_bwd(plan.handle, *plan._graph()[:2], _ptr(Fv), _ptr(el), _ptr(er),
+                               _ptr(out), _ptr(lse), _ptr(dOut), plan.N, plan.E, plan.H, plan.D,
+                               float(slope), plan.dt, _ptr(dFv), _ptr(de_l), _ptr(de_r),
+                               _stream(stream)), "gat_attn_bwd")
+    return dFv, de_l, de_r
+
+
 # ------------------------------------------------------- min / max aggregation
 
 def agg_minmax_fwd(plan: Plan, X, op: str = "max", out=None, arg=None, stream=None):
@@ -515,6 +560,27 @@ class MinMaxAggregation(torch.autograd.Function):
     def backward(ctx, dOut):
         (arg,) = ctx.saved_tensors
         return agg_minmax_bwd(ctx.plan, arg, dOut.contiguous()), None, None
+
+
+class GATEdgeAttention(torch.autograd.Function):
+    """GAT edge stage as an autograd function:
+    ``out = GATEdgeAttention.apply(Fv, el, er, plan, slope)``; with
+    Fv = X @ W and el, er the per-node dots with the attention vector's two
+    halves (ordinary torch ops around it), this is the GAT layer."""
+
+    @staticmethod
+    def forward(ctx, Fv, el, er, plan, slope=0.2):
+        Fv, el, er = Fv.contiguous(), el.contiguous(), er.contiguous()
+        out, lse = gat_attn_fwd(plan, Fv, el, er, slope)
+        ctx.plan, ctx.slope = plan, slope
+        ctx.save_for_backward(Fv, el, er, out, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dOut):
+        Fv, el, er, out, lse = ctx.saved_tensors
+        dFv, de_l, de_r = gat_attn_bwd(ctx.plan, Fv, el, er, out, lse, dOut.contiguous(), ctx.slope)
+        return dFv, de_l, de_r, None, None
 
 
 class GATv2Attention(torch.autograd.Function):

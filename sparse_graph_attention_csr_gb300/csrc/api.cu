@@ -56,6 +56,17 @@ void compute_layout(sga_plan *p) {
         L.total = off;
         return;
     }
+    if (p->layer == SGA_LAYER_GAT) {
+        L.delta = take((size_t)p->N * p->H * 4);
+        L.lse_n = take((size_t)p->N * p->H * 4);
+        L.fwd_ml = take((size_t)p->rows.n_chunks * p->H * 2 * 4);
+        L.fwd_acc = take((size_t)p->rows.n_chunks * HD * 4);
+        L.bwd_rowc = take((size_t)p->rows.n_chunks * p->H * 4 * 4);
+        L.bwd_col = take((size_t)p->cols.n_chunks * HD * 4);
+        L.gat_colc = take((size_t)p->cols.n_chunks * p->H * 4);
+        L.total = off;
+        return;
+    }
     L.delta = take((size_t)p->N * p->H * 4);
     L.lse_n = take((size_t)p->N * p->H * 4);
     L.fwd_ml = take((size_t)p->rows.n_chunks * p->H * 2 * 4);
@@ -184,10 +195,12 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     if (opts) o = *opts;
     if (o.split_threshold < 0 || o.chunk_len < 0 || o.in_features < 0 || o.tile_min_nnz < 0)
         return SGA_EINVAL;
-    if (o.layer != SGA_LAYER_ATTENTION && o.layer != SGA_LAYER_MINMAX) return SGA_EINVAL;
-    if (o.layer == SGA_LAYER_MINMAX && (o.in_features != 0 || o.tile_min_nnz != 0)) return SGA_EINVAL;
+    if (o.layer != SGA_LAYER_ATTENTION && o.layer != SGA_LAYER_MINMAX && o.layer != SGA_LAYER_GAT)
+        return SGA_EINVAL;
+    if (o.layer != SGA_LAYER_ATTENTION && (o.in_features != 0 || o.tile_min_nnz != 0)) return SGA_EINVAL;
     if (o.schedule < SGA_SCHED_STREAM || o.schedule > SGA_SCHED_BILEVEL) return SGA_EINVAL;
     if (o.edge_bias != 0 && o.edge_bias != 1) return SGA_EINVAL;
+    if (o.row_order < 0 || o.row_order > 2) return SGA_EINVAL;
     if (o.edge_bias && (o.layer != SGA_LAYER_ATTENTION || o.in_features != 0 || o.tile_min_nnz != 0))
         return SGA_EUNSUPPORTED;
     if (o.tile_min_nnz > 0 && (!bsr_fwd_supported(dt, D) || N > (1 << 18) || o.tile_min_nnz > 128 * 16))
@@ -204,6 +217,7 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     p->layer = o.layer;
     p->schedule = o.schedule;
     p->edge_bias = o.edge_bias;
+    p->row_order = o.row_order == 2 ? 2 : 1;   // 0 (default) and 1: descending degree
     p->dt = dt;
     p->split_threshold = o.split_threshold > 0 ? o.split_threshold : 256;
     p->chunk_len = o.chunk_len > 0 ? o.chunk_len : 128;
@@ -235,6 +249,7 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
             rp->dt = dt;
             rp->split_threshold = p->split_threshold;
             rp->chunk_len = p->chunk_len;
+            rp->row_order = p->row_order;
             rp->indptr = p->tiles.r_indptr;
             rp->indices = p->tiles.r_indices;
             rp->num_sms = p->num_sms;
@@ -332,6 +347,9 @@ sga_status sga_plan_copy_array(const sga_plan *p, sga_plan_array which, int32_t 
             break;
         case SGA_ARR_R_INDPTR: src = p->tiles.r_indptr; n = p->tiles.min_nnz ? p->N + 1 : 0; break;
         case SGA_ARR_R_INDICES: src = p->tiles.r_indices; n = p->tiles.E_res; break;
+        case SGA_ARR_ROW_ORDER: src = R.order; n = R.order ? p->N : 0; break;
+        case SGA_ARR_T_ROW_ORDER: src = C.order; n = C.order ? p->N : 0; break;
+        case SGA_ARR_T_EID: src = p->t_eid; n = p->t_eid ? p->E : 0; break;
         default: return SGA_EINVAL;
     }
     if (count != n) return SGA_EINVAL;
@@ -667,6 +685,72 @@ sga_status agg_minmax_bwd(const sga_plan *p, const int32_t *arg, const void *dOu
     a.dX = dX;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return cuda_status(dt == SGA_F32 ? agg_bwd_t<float>(a, s) : agg_bwd_t<__nv_bfloat16>(a, s));
+}
+
+static GatArgs gat_args(const sga_plan *p, float slope) {
+    GatArgs a{};
+    a.indptr = p->indptr;
+    a.indices = p->indices;
+    a.t_indptr = p->t_indptr;
+    a.t_dst = p->t_dst;
+    a.N = p->N;
+    a.H = p->H;
+    a.D = p->D;
+    a.slope = slope;
+    a.split_threshold = p->split_threshold;
+    a.rows = p->rows;
+    a.cols = p->cols;
+    a.d_err = p->d_err;
+    if (p->ws) {
+        a.ws_delta = ws_at<float>(p, p->layout.delta);
+        a.ws_lse = ws_at<float>(p, p->layout.lse_n);
+        a.ws_ml = ws_at<float>(p, p->layout.fwd_ml);
+        a.ws_acc = ws_at<float>(p, p->layout.fwd_acc);
+        a.ws_rowc = ws_at<float>(p, p->layout.bwd_rowc);
+        a.ws_col = ws_at<float>(p, p->layout.bwd_col);
+        a.ws_colc = ws_at<float>(p, p->layout.gat_colc);
+    }
+    return a;
+}
+
+sga_status gat_attn_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *indices,
+                        const void *Fv, const float *el, const float *er, int64_t N, int64_t E,
+                        int H, int D, float slope, sga_dtype dt, void *out, float *lse,
+                        void *stream) {
+    if (p && p->layer != SGA_LAYER_GAT) return SGA_EINVAL;
+    sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, 0);
+    if (st != SGA_OK) return st;
+    if (!tensors_ok(N, {Fv, out, lse, el, er})) return SGA_EINVAL;
+    GatArgs a = gat_args(p, slope);
+    a.Fv = Fv;
+    a.el = el;
+    a.er = er;
+    a.out_w = out;
+    a.lse_w = lse;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(dt == SGA_F32 ? gat_fwd_t<float>(a, s) : gat_fwd_t<__nv_bfloat16>(a, s));
+}
+
+sga_status gat_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *indices,
+                        const void *Fv, const float *el, const float *er, const void *out,
+                        const float *lse, const void *dOut, int64_t N, int64_t E, int H, int D,
+                        float slope, sga_dtype dt, void *dFv, float *del, float *der,
+                        void *stream) {
+    if (p && p->layer != SGA_LAYER_GAT) return SGA_EINVAL;
+    sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, 0);
+    if (st != SGA_OK) return st;
+    if (!tensors_ok(N, {Fv, el, er, out, lse, dOut, dFv, del, der})) return SGA_EINVAL;
+    GatArgs a = gat_args(p, slope);
+    a.Fv = Fv;
+    a.el = el;
+    a.er = er;
+    a.lse = lse;
+    a.dOut = dOut;
+    a.dFv = dFv;
+    a.del = del;
+    a.der = der;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return cuda_status(dt == SGA_F32 ? gat_bwd_t<float>(a, s) : gat_bwd_t<__nv_bfloat16>(a, s));
 }
 
 sga_status sga_profile_start(sga_kernel_id which) {

@@ -79,29 +79,31 @@ struct RingDims {
     static_assert(U <= 2 || FIT >= 2, "two steps of several neighbours must fit the ring");
     static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
 };
-template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC, int U2 = 1, int U1 = 2>
+template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC, int U2 = 1, int U1 = 2, int ESC = 0,
+          bool LIST = true>
 using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::U, NROW, NSC, NOWN, NOSC,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
-                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD>;
+                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST>;
 
-// gathered K, V (and the edge's score bias); own Q
-template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4>;
+// gathered K, V (and the edge's score bias); own Q.  LIST = false: no item
+// list (the no-allocation forward, which has no plan)
+template <typename T, int D, int NC, int G, bool BIAS = false, bool LIST = true>
+using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4, BIAS ? 1 : 0, LIST>;
 // gathered K, V (and the edge's score bias); own Q, dOut, lse
 template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4>;
+using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0>;
 // gathered Q, dOut, lse, Delta (over the transposed CSR; and the edge's score
 // bias in transposed order); own K, V
 template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4>;
+using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4, BIAS ? 4 : 0>;
 
 // With BIAS, each edge's score gains a per-head term b[e, h] (fp32, [E, H] in
 // CSR edge order): s_ij = q_i . k_j / sqrt(D) + b_eh.
-template <typename T, int D, int NC, int G, bool BIAS>
+template <typename T, int D, int NC, int G, bool BIAS, bool LIST>
 __global__ void __launch_bounds__(256, 2)
 gt_fwd_kernel(GtArgs a, float scale2) {
     using S = GtShape<T, D, NC, G>;
-    using C = GtFwdStream<T, D, NC, G, BIAS>;
+    using C = GtFwdStream<T, D, NC, G, BIAS, LIST>;
     constexpr int EL = S::EL, LH = S::LH, U = C::U;
     extern __shared__ __align__(16) unsigned char dsmem[];
     const int lane = threadIdx.x & 31, g = lane / G, gl = lane % G;
@@ -110,10 +112,7 @@ gt_fwd_kernel(GtArgs a, float scale2) {
     arr.rows[0] = static_cast<const uint4 *>(a.K);
     arr.rows[1] = static_cast<const uint4 *>(a.V);
     arr.own[0] = static_cast<const uint4 *>(a.Q);
-    if (BIAS) {
-        arr.sc[0] = a.bias;
-        arr.sc_edge = 1u;
-    }
+    if (BIAS) arr.sc[0] = a.bias;
     EdgeStream<C> st;
     st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
             a.split_threshold, a.d_err);
@@ -141,9 +140,11 @@ gt_fwd_kernel(GtArgs a, float scale2) {
                 for (int k = 0; k < NC; ++k) {
                     float kf[EL];
                     unpack<T>(st.row(u, 0, k), kf);
-                    float dot = group_sum<LH>(dot2<EL>(q[k], kf)) * scale2;
-                    if (BIAS) dot += st.scalar(u, 0, (gl + G * k) / LH) * kLog2e;
-                    sc[u][k] = ok[u] ? dot : -INFINITY;
+                    const float dot = group_sum<LH>(dot2<EL>(q[k], kf));
+                    if constexpr (BIAS)
+                        sc[u][k] = ok[u] ? dot * scale2 + st.scalar(u, 0, (gl + G * k) / LH) * kLog2e : -INFINITY;
+                    else
+                        sc[u][k] = ok[u] ? dot * scale2 : -INFINITY;
                 }
             }
             // online softmax with a lazily moved maximum: the accumulator is
@@ -393,10 +394,7 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
     arr.own[0] = static_cast<const uint4 *>(a.Q);
     arr.own[1] = static_cast<const uint4 *>(a.dOut);
     arr.osc[0] = a.lse;
-    if (BIAS) {
-        arr.sc[0] = a.bias;
-        arr.sc_edge = 1u;
-    }
+    if (BIAS) arr.sc[0] = a.bias;
     EdgeStream<C> st;
     st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.rows, a.indptr, a.indices, a.N, a.H, R, LH,
             a.split_threshold, a.d_err);
@@ -438,9 +436,13 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                     }
                     float sdot, dp;
                     const bool hi = head_sums_split<LH>(sd[0], dv[0], sd[1], dv[1], sdot, dp);
-                    float arg = sdot * scale2 - (hi ? lse2[1] : lse2[0]);
-                    if (BIAS) arg += st.scalar(u, 0, (gl + G * (hi ? 1 : 0)) / LH) * kLog2e;
-                    const float p = ok ? exp2f(arg) : 0.f;
+                    float p;
+                    if constexpr (BIAS)
+                        p = ok ? exp2f(sdot * scale2 - (hi ? lse2[1] : lse2[0]) +
+                                       st.scalar(u, 0, (gl + G * (hi ? 1 : 0)) / LH) * kLog2e)
+                               : 0.f;
+                    else
+                        p = ok ? exp2f(sdot * scale2 - (hi ? lse2[1] : lse2[0])) : 0.f;
                     const float pdp = p * dp;
                     const float po = __shfl_xor_sync(SGA_FULL_MASK, p, LH / 2);
                     const float pdpo = __shfl_xor_sync(SGA_FULL_MASK, pdp, LH / 2);
@@ -461,9 +463,12 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                         unpack<T>(st.row(u, 1, k), vf);
                         float sdot = dot2<EL>(q[k], kf), dp = dot2<EL>(go[k], vf);
                         group_sum2<LH>(sdot, dp);
-                        float arg = sdot * scale2 - lse2[k];
-                        if (BIAS) arg += st.scalar(u, 0, (gl + G * k) / LH) * kLog2e;
-                        const float p = ok ? exp2f(arg) : 0.f;
+                        float p;
+                        if constexpr (BIAS)
+                            p = ok ? exp2f(sdot * scale2 - lse2[k] + st.scalar(u, 0, (gl + G * k) / LH) * kLog2e)
+                                   : 0.f;
+                        else
+                            p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
                         const float pdp = p * dp;
                         c[k] += pdp;
                         z[k] += p;
@@ -548,10 +553,7 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
     arr.sc[1] = a.ws_delta;
     arr.own[0] = static_cast<const uint4 *>(a.K);
     arr.own[1] = static_cast<const uint4 *>(a.V);
-    if (BIAS) {
-        arr.sc[2] = a.bias_t;   // the bias in transposed-CSR order
-        arr.sc_edge = 4u;
-    }
+    if (BIAS) arr.sc[2] = a.bias_t;   // the bias in transposed-CSR order
     EdgeStream<C> st;
     st.init(dsmem + (threadIdx.x >> 5) * C::BYTES, arr, a.cols, a.t_indptr, a.t_dst, a.N, a.H, R, LH,
             a.split_threshold, a.d_err);
@@ -584,9 +586,11 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
                     float sdot = dot2<EL>(qf, kj[k]), dp = dot2<EL>(gf, vj[k]);
                     group_sum2<LH>(sdot, dp);
                     const int h = (gl + G * k) / LH;
-                    float arg = sdot * scale2 - st.scalar(u, 0, h) * kLog2e;
-                    if (BIAS) arg += st.scalar(u, 2, h) * kLog2e;
-                    const float p = ok ? exp2f(arg) : 0.f;
+                    float p;
+                    if constexpr (BIAS)
+                        p = ok ? exp2f(sdot * scale2 + (st.scalar(u, 2, h) - st.scalar(u, 0, h)) * kLog2e) : 0.f;
+                    else
+                        p = ok ? exp2f(sdot * scale2 - st.scalar(u, 0, h) * kLog2e) : 0.f;
                     const float ds = p * (dp - st.scalar(u, 1, h));
                     axpy2<EL>(dv[k], p, gf);
                     axpy2<EL>(dk[k], ds, qf);
@@ -773,7 +777,7 @@ template <int LH, int MAXNC, typename F> cudaError_t dispatch_shape(int R, F &&f
 
 template <typename T> constexpr int max_nc() { return sizeof(T) == 4 ? 8 : 4; }
 
-template <typename T, int D, bool BIAS> cudaError_t gt_fwd_db(const GtArgs &a, cudaStream_t s) {
+template <typename T, int D, bool BIAS, bool LIST> cudaError_t gt_fwd_db(const GtArgs &a, cudaStream_t s) {
     constexpr int LH = D * (int)sizeof(T) / 16;
     const int R = a.H * D / Elt<T>::EL;
     const float scale2 = kLog2e / sqrtf((float)D);
@@ -781,8 +785,9 @@ template <typename T, int D, bool BIAS> cudaError_t gt_fwd_db(const GtArgs &a, c
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
         note_launch(SGA_KERN_GT_FWD, s, false);
-        const cudaError_t e = launch_streamed<GtFwdStream<T, D, NC, G, BIAS>, gt_fwd_kernel<T, D, NC, G, BIAS>>(
-            items, s, a, scale2);
+        const cudaError_t e =
+            launch_streamed<GtFwdStream<T, D, NC, G, BIAS, LIST>, gt_fwd_kernel<T, D, NC, G, BIAS, LIST>>(
+                items, s, a, scale2);
         note_launch(SGA_KERN_GT_FWD, s, true);
         return e;
     });
@@ -794,7 +799,8 @@ template <typename T, int D, bool BIAS> cudaError_t gt_fwd_db(const GtArgs &a, c
 }
 
 template <typename T, int D> cudaError_t gt_fwd_d(const GtArgs &a, cudaStream_t s) {
-    return a.bias ? gt_fwd_db<T, D, true>(a, s) : gt_fwd_db<T, D, false>(a, s);
+    if (!a.rows.items) return gt_fwd_db<T, D, false, false>(a, s);   // no plan: no bias either
+    return a.bias ? gt_fwd_db<T, D, true, true>(a, s) : gt_fwd_db<T, D, false, true>(a, s);
 }
 
 // bias_t[te, h] = bias[t_eid[te], h]: the score bias in transposed-CSR order

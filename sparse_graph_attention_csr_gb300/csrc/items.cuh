@@ -13,11 +13,22 @@ struct ItemRange {
     bool partial;
 };
 
-// Work item w of a launch: chunks of split rows first, then every row (rows
-// above the split threshold are skipped; their chunks cover them).
+// Work item w of a launch: the plan's item list (chunks of split rows, then
+// the other rows in walking order), or without one chunks first, then every
+// row by id (rows above the split threshold are skipped; their chunks cover
+// them).
 __device__ __forceinline__ bool decode_item(int64_t item, const Partition &P,
                                             const int32_t *__restrict__ ptr, int64_t N,
                                             int threshold, ItemRange &r) {
+    if (P.items) {   // the plan's item list
+        if (item >= P.n_items) return false;
+        const int4 t = __ldg(P.items + item);
+        r.row = t.x;
+        r.beg = t.y;
+        r.end = t.z;
+        r.partial = item < P.n_chunks;
+        return true;
+    }
     if (item < P.n_chunks) {
         r.row = P.chunk_row[item];
         r.beg = P.chunk_beg[item];
@@ -59,9 +70,24 @@ struct ItemMeta {
     int32_t row, beg, end;   // raw loads; row < 0 past the last item
 };
 
+// LIST: the partition's item list (one load path, no skipped rows);
+// otherwise chunks, then every row by id.
+template <bool LIST>
 __device__ __forceinline__ void meta_issue(int64_t item, const Partition &P,
                                            const int32_t *__restrict__ ptr, int64_t N,
                                            ItemMeta &m) {
+    if constexpr (LIST) {
+        if (item < P.n_items) {
+            const int4 t = __ldg(P.items + item);
+            m.row = t.x;
+            m.beg = t.y;
+            m.end = t.z;
+        } else {
+            m.row = -1;
+            m.beg = m.end = 0;
+        }
+        return;
+    }
     if (item < P.n_chunks) {
         m.row = __ldg(P.chunk_row + item);
         m.beg = __ldg(P.chunk_beg + item);
@@ -79,12 +105,14 @@ __device__ __forceinline__ void meta_issue(int64_t item, const Partition &P,
 
 // True when the item is to be processed here (not past the end, and not a row
 // above the split threshold, whose chunks are separate items).
+template <bool LIST>
 __device__ __forceinline__ bool meta_eval(int64_t item, const ItemMeta &m, const Partition &P,
                                           int threshold, ItemRange &r) {
     r.row = m.row;
     r.beg = m.beg;
     r.end = m.end;
     r.partial = item < P.n_chunks;
+    if constexpr (LIST) return m.row >= 0;
     return m.row >= 0 && (r.partial || m.end - m.beg <= threshold);
 }
 

@@ -223,6 +223,37 @@ __global__ void gather_rows_kernel(const int32_t *__restrict__ rows, const int32
         t_dst[te] = rows[t_eid[te]];
 }
 
+// Sort keys of the walking order, value = row: descending degree
+// (key = maxdeg - degree), or split rows first then ascending id (key = 0 for
+// rows above the threshold, 1 for the others).
+__global__ void order_keys_kernel(const int32_t *__restrict__ ptr, int64_t N, int32_t maxdeg, int threshold,
+                                  bool by_degree, int32_t *__restrict__ key, int32_t *__restrict__ val) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride) {
+        const int32_t deg = ptr[i + 1] - ptr[i];
+        key[i] = by_degree ? maxdeg - deg : (deg > threshold ? 0 : 1);
+        val[i] = (int32_t)i;
+    }
+}
+
+// item list entries of the rows order[0 .. n)
+__global__ void item_fill_kernel(const int32_t *__restrict__ ptr, const int32_t *__restrict__ order, int64_t n,
+                                 int4 *__restrict__ items) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += stride) {
+        const int32_t r = order[x];
+        items[x] = make_int4(r, ptr[r], ptr[r + 1], 0);
+    }
+}
+
+// item list entries of the chunks of split rows
+__global__ void chunk_items_kernel(const int32_t *__restrict__ row, const int32_t *__restrict__ beg,
+                                   const int32_t *__restrict__ end, int64_t n, int4 *__restrict__ items) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += stride)
+        items[x] = make_int4(row[x], beg[x], end[x], 0);
+}
+
 __global__ void count_sources_kernel(const int32_t *__restrict__ indices, int64_t E,
                                      int32_t *__restrict__ counts) {
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -379,6 +410,12 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
     int32_t *ka = tmp.get<int32_t>(E), *kb = tmp.get<int32_t>(E);
     int32_t *va = tmp.get<int32_t>(E), *vb = tmp.get<int32_t>(E);
     int32_t *hist = tmp.get<int32_t>(hist_n);
+    // the item-list sorts need N-long key/value buffers
+    if (N > E) {
+        ka = tmp.get<int32_t>(N); kb = tmp.get<int32_t>(N);
+        va = tmp.get<int32_t>(N); vb = tmp.get<int32_t>(N);
+    }
+    int32_t *hist_o = tmp.get<int32_t>(radix_hist_elems(N));
     SGA_TRY(tmp.err);
     if (E > 0) {
         SGA_TRY(cudaMemcpyAsync(ka, p->indices, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
@@ -425,6 +462,38 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
     st = build_partition(p->t_indptr, N, p->split_threshold, p->chunk_len, p->cols, own, tmp,
                          scan_tmp, s);
     if (st != SGA_OK) { own.release(); return st; }
+    // (4) item lists: the chunks of split rows (chunk order), then the other
+    // rows in walking order -- by descending degree (ties by id: long rows
+    // first, which balances the persistent warps' round-robin share of
+    // work), or by ascending id.  Sorting all rows by descending degree puts
+    // the split rows (degree > threshold) first, so the others are the tail;
+    // for the ascending walk the key is "split" then the id.
+    for (int w = 0; w < 2 && N > 0; ++w) {
+        const int32_t *ptr = w == 0 ? p->indptr : p->t_indptr;
+        Partition &P = w == 0 ? p->rows : p->cols;
+        P.n_items = (int64_t)P.n_chunks + (N - P.n_split);
+        P.items = own.get<int4>(P.n_items);
+        if (p->row_order == 1) P.order = own.get<int32_t>(N);
+        SGA_TRY(own.err);
+        if (P.n_chunks > 0) {
+            chunk_items_kernel<<<grid_for(P.n_chunks, 256, 65535), 256, 0, s>>>(P.chunk_row, P.chunk_beg,
+                                                                                P.chunk_end, P.n_chunks, P.items);
+            SGA_TRY(cudaGetLastError());
+        }
+        int32_t *k1 = ka, *v1 = va, *k2 = kb, *v2 = vb;
+        const int32_t maxdeg = (int32_t)std::min<int64_t>(E, INT32_MAX - 1);
+        order_keys_kernel<<<grid_for(N, 256, 65535), 256, 0, s>>>(ptr, N, maxdeg, p->split_threshold,
+                                                                  p->row_order == 1, k1, v1);
+        SGA_TRY(cudaGetLastError());
+        int bits = 1;
+        if (p->row_order == 1)
+            while (bits < 31 && ((int64_t)1 << bits) <= maxdeg) ++bits;
+        SGA_TRY(radix_sort_pairs(&k1, &v1, &k2, &v2, N, bits, hist_o, scan_tmp, s));
+        if (P.order) SGA_TRY(cudaMemcpyAsync(P.order, v1, 4 * (size_t)N, cudaMemcpyDeviceToDevice, s));
+        item_fill_kernel<<<grid_for(N, 256, 65535), 256, 0, s>>>(ptr, v1 + P.n_split, N - P.n_split,
+                                                                 P.items + P.n_chunks);
+        SGA_TRY(cudaGetLastError());
+    }
     SGA_TRY(cudaStreamSynchronize(s));
     tmp.release();
     p->device_bytes = own.bytes;

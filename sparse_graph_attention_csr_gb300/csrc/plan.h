@@ -20,6 +20,14 @@ struct Partition {
     int32_t *chunk_row = nullptr;   // [n_chunks]
     int32_t *chunk_beg = nullptr;   // [n_chunks] first edge (absolute CSR offset)
     int32_t *chunk_end = nullptr;   // [n_chunks] one past the last edge
+    // The work items of an edge kernel in walking order: every chunk of a split
+    // row (in chunk order), then every row of degree <= the threshold, by
+    // descending degree (ties by id) or by ascending id.  n_items entries;
+    // item x < n_chunks is chunk x.  nullptr: no list (chunks, then all rows
+    // by id, split rows skipped at run time).
+    int64_t n_items = 0;
+    int4 *items = nullptr;          // [n_items] (row, first edge, end edge, 0)
+    int32_t *order = nullptr;       // [N] all rows by descending degree (inspection; descending walks)
 };
 
 // Byte offsets of the regions of the caller's workspace.
@@ -28,6 +36,7 @@ struct WorkspaceLayout {
     size_t lse_n = 0;      // [N, H] f32          lse_i + ln Z_i (backward row normalisation)
     size_t zt = 0;         // [N, H] f32          block-sparse plans: tile part of Z_i
     size_t bias_t = 0;     // [E, H] f32          edge-bias plans: the bias in transposed order
+    size_t gat_colc = 0;   // [t_n_chunks, H] f32 GAT plans: source-pass chunk parts of der
     size_t fwd_ml = 0;     // [n_chunks, H, 2] f32 chunk softmax stats (max, sum), log2 units
     size_t fwd_acc = 0;    // [n_chunks, H*D] f32  chunk unnormalised accumulators
     size_t bwd_row = 0;    // [n_chunks, 4, H*D] f32 chunk partial sums (dQ: A, B; dFL: A, B, da A, B)
@@ -84,6 +93,7 @@ struct sga_plan {
     int32_t *t_dst = nullptr;          // [E]
     int32_t *t_eid = nullptr;          // [E] CSR edge of each transposed entry (edge-bias plans)
     int edge_bias = 0;                 // plan serves gt_attn_bias_fwd/bwd
+    int row_order = 1;                 // 1: rows walked by descending degree, 2: by ascending id
     sga::Partition rows, cols;         // partitions of the CSR and the transposed CSR
     sga::TileSet tiles;                // block-sparse split (tiles.min_nnz > 0)
     sga_plan *residual = nullptr;      // plan over the residual CSR (block-sparse plans)
@@ -209,6 +219,28 @@ cudaError_t launch_bsr_bwd_delta(const BsrBwdArgs &a, cudaStream_t s);
 cudaError_t launch_bsr_bwd_dq(const BsrBwdArgs &a, cudaStream_t s);
 cudaError_t launch_bsr_bwd_dkdv(const BsrBwdArgs &a, cudaStream_t s);
 template <typename T> cudaError_t gatv2_bwd_t(const Gatv2Args &a, cudaStream_t s);
+
+// ---- GAT edge attention (gat.cu) ----
+struct GatArgs {
+    const int32_t *indptr, *indices;
+    const int32_t *t_indptr, *t_dst;
+    const void *Fv, *dOut;          // [N, H, D] projected features, upstream gradient
+    const float *el, *er, *lse;     // [N, H] score halves, forward lse
+    void *out_w, *dFv;              // [N, H, D]
+    float *lse_w, *del, *der;       // [N, H]
+    int64_t N;
+    int H, D;
+    float slope;
+    int split_threshold;
+    Partition rows, cols;
+    float *ws_ml, *ws_acc;          // forward chunk partials (as the GT forward)
+    float *ws_rowc;                 // [n_chunks, H, 4] destination-pass chunk sums C, Z, A, B
+    float *ws_delta, *ws_lse;       // [N, H] Delta and lse + ln Z
+    float *ws_col, *ws_colc;        // [t_n_chunks, H*D], [t_n_chunks, H] source-pass chunk sums
+    int32_t *d_err;
+};
+template <typename T> cudaError_t gat_fwd_t(const GatArgs &a, cudaStream_t s);
+template <typename T> cudaError_t gat_bwd_t(const GatArgs &a, cudaStream_t s);
 
 // ---- min / max aggregation (agg.cu) ----
 struct AggArgs {

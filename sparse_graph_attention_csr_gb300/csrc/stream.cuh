@@ -54,11 +54,18 @@ __device__ __forceinline__ void cp_wait_newer(int n) {
     }
 }
 
-template <int NC_, int G_, int U_, int NROW_, int NSC_, int NOWN_, int NOSC_, int DEPTH_, int QD_>
+template <int NC_, int G_, int U_, int NROW_, int NSC_, int NOWN_, int NOSC_, int DEPTH_, int QD_,
+          int ESC_ = 0, bool LIST_ = true>
 struct StreamCfg {
+    // walk the plan's item list (else: chunks, then all rows by id)
+    static constexpr bool LIST = LIST_;
     static_assert(NSC_ <= 3, "at most three gathered scalar arrays");
     static constexpr int NC = NC_, G = G_, U = U_, NROW = NROW_, NSC = NSC_, NOWN = NOWN_,
                          NOSC = NOSC_, DEPTH = DEPTH_, QD = QD_;
+    // bit s set: gathered scalar array s is indexed by the edge's CSR position
+    // ([E, H]) rather than by its node ([N, H]); fixed at compile time so that
+    // shapes without such arrays pay nothing for them
+    static constexpr uint32_t ESC = ESC_;
     static constexpr int NG = 32 / G, STEP = NG * U;
     static_assert(DEPTH >= 2 && DEPTH <= 8, "ring depth");
     static_assert(QD >= 2, "queue depth");
@@ -96,10 +103,9 @@ struct StreamItem {
 
 struct StreamArrays {
     const uint4 *rows[4];   // gathered node rows, [N][R] sixteen-byte chunks
-    const float *sc[3];     // gathered per-head scalars, [N][H] (or [E][H], see sc_edge)
+    const float *sc[3];     // gathered per-head scalars, [N][H] (or [E][H], see StreamCfg::ESC)
     const uint4 *own[2];    // the item's own rows
     const float *osc[2];    // the item's own scalars
-    uint32_t sc_edge;       // bit s set: sc[s] is indexed by the edge's CSR position, not its node
 };
 
 template <typename C> struct EdgeStream {
@@ -146,11 +152,11 @@ template <typename C> struct EdgeStream {
         g = lane / C::G;
         gl = lane % C::G;
         stride = (int64_t)gridDim.x * (blockDim.x >> 5);
-        n_items = (int64_t)P.n_chunks + N;
+        n_items = C::LIST ? P.n_items : (int64_t)P.n_chunks + N;
         nx_item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-        meta_issue(nx_item, P, ptr, N, m1);
-        meta_issue(nx_item + stride, P, ptr, N, m2);
-        v1 = meta_eval(nx_item, m1, P, threshold, r1);
+        meta_issue<C::LIST>(nx_item, P, ptr, N, m1);
+        meta_issue<C::LIST>(nx_item + stride, P, ptr, N, m2);
+        v1 = meta_eval<C::LIST>(nx_item, m1, P, threshold, r1);
         ids1 = first_ids(ids, r1, v1);
         p_beg = p_deg = p_step = p_nsteps = 0;
         p_ids = p_ids_nx = -1;
@@ -176,8 +182,8 @@ template <typename C> struct EdgeStream {
             // rotate the descriptor pipeline
             nx_item += stride;
             m1 = m2;
-            meta_issue(nx_item + stride, P, ptr, N, m2);
-            v1 = meta_eval(nx_item, m1, P, threshold, r1);
+            meta_issue<C::LIST>(nx_item + stride, P, ptr, N, m2);
+            v1 = meta_eval<C::LIST>(nx_item, m1, P, threshold, r1);
             ids1 = first_ids(ids, r1, v1);
             if (!valid) continue;   // a row above the split threshold: its chunks cover it
             const int32_t deg = r.end - r.beg;
@@ -252,7 +258,7 @@ template <typename C> struct EdgeStream {
             if (gl < H)
 #pragma unroll
                 for (int s = 0; s < C::NSC; ++s) {
-                    const size_t at = ((arr.sc_edge >> s) & 1u) ? (size_t)(p_beg + e) : (size_t)j;
+                    const size_t at = ((C::ESC >> s) & 1u) ? (size_t)(p_beg + e) : (size_t)j;
                     cp4_async(sa + C::OFF_SC + slot * C::SC_SLOT + ((u * C::NSC + s) * 32 + lane) * 4,
                               ok ? arr.sc[s] + at * H + gl : arr.sc[s], ok);
                 }

@@ -213,3 +213,31 @@ def test_device_range_check_flags_corrupted_indices():
     assert plan.device_error() == 1
     assert plan.device_error() == 0   # read clears it
     assert torch.isfinite(out).all()
+
+
+def test_descending_degree_walking_order_is_bitwise_identical():
+    """Walking rows by descending degree changes which warp computes a row,
+    not the row's arithmetic: outputs and gradients are bit-identical to the
+    ascending-id walk; the orders are the stable sort by descending degree."""
+    w = synth.small_workload(4)
+    indptr, indices = synth.make_graph(w)
+    x = synth.gt_inputs(w)
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    Q, K, V, dO = (dev(x[n][0]) for n in ("Q", "K", "V", "dOut"))
+    res = []
+    for ro in (2, 1):   # ascending id, descending degree
+        plan = sga.Plan(ip, ix, w.H, w.D, torch.bfloat16, row_order=ro, split_threshold=64,
+                        chunk_len=32)
+        out, lse = sga.gt_attn_fwd(plan, Q, K, V)
+        res.append((out, lse) + tuple(sga.gt_attn_bwd(plan, Q, K, V, out, lse, dO)))
+        if ro == 1:
+            deg = np.diff(indptr.astype(np.int64))
+            t_indptr, _ = oracle.transpose(indptr, indices)
+            tdeg = np.diff(t_indptr.astype(np.int64))
+            N = len(deg)
+            np.testing.assert_array_equal(plan.array("row_order"), np.lexsort((np.arange(N), -deg)))
+            np.testing.assert_array_equal(plan.array("t_row_order"), np.lexsort((np.arange(N), -tdeg)))
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+    ro, rl = oracle.gt_fwd(indptr, indices, x["Q"][1], x["K"][1], x["V"][1])
+    compare(res[1][0], ro, "bf16", "out")

@@ -803,3 +803,105 @@ def test_gt_bias_special_cases():
     sums = np.zeros((N, H))
     np.add.at(sums, edge_rows(indptr), dB)
     np.testing.assert_allclose(sums, 0.0, atol=1e-12)
+
+
+# --------------------------------------------------- GAT (original attention score)
+
+def dense_gat(X, W, a, mask, slope=0.2, rnd=None):
+    N = X.shape[0]
+    H, _, D = a.shape
+    FL = X @ W
+    if rnd is not None:
+        FL = rnd(FL)
+    FL = FL.reshape(N, H, D)
+    el = (FL * a[:, 0]).sum(-1)                          # [N, H]
+    er = (FL * a[:, 1]).sum(-1)
+    e = torch.nn.functional.leaky_relu(el[:, None, :] + er[None, :, :], slope).permute(2, 0, 1)
+    e = e.masked_fill(~mask[None], float("-inf"))
+    lse = torch.logsumexp(e, -1)
+    p = torch.exp(e - lse[..., None]).nan_to_num(0.0)
+    return torch.einsum("hij,jhd->ihd", p, FL), lse.T
+
+
+def test_gat_hand_example():
+    g = load("gat_hand.json")
+    FL, out, lse = oracle.gat_fwd(np.array(g["indptr"], np.int32), np.array(g["indices"], np.int32),
+                                  np.array(g["X"]), np.array(g["W"]), np.array(g["a"]), 0.2)
+    np.testing.assert_allclose(out, np.array(g["out"]), atol=1e-14)
+    np.testing.assert_allclose(lse, np.array(g["lse"]), atol=1e-14)
+
+
+@pytest.mark.parametrize("store", [None, "bf16"])
+def test_gat_matches_dense_autograd(store):
+    """Forward against the dense masked form; backward against torch autograd
+    of it (for bf16 storage through a straight-through rounding step)."""
+    rng = np.random.default_rng(71)
+    N, F, H, D = 26, 6, 2, 4
+    indptr, indices = rand_graph(rng, N, 0.25)
+    X = rng.standard_normal((N, F)) * 2.0
+    W = rng.standard_normal((F, H * D))
+    a = rng.standard_normal((H, 2, D))
+    dO = rng.standard_normal((N, H, D))
+    FL, out, lse = oracle.gat_fwd(indptr, indices, X, W, a, 0.2, store=store)
+    g = oracle.gat_bwd(indptr, indices, X, W, a, dO, 0.2, store=store)
+    tX, tW, ta = (torch.from_numpy(x).requires_grad_() for x in (X, W, a))
+    rnd = (lambda Y: straight_through(Y, "bf16")) if store == "bf16" else None
+    to, tl = dense_gat(tX, tW, ta, dense_mask(indptr, indices, N), rnd=rnd)
+    np.testing.assert_allclose(out, to.detach().numpy(), atol=1e-12)
+    np.testing.assert_allclose(lse, tl.detach().numpy(), atol=1e-12)
+    (to * torch.from_numpy(dO)).sum().backward()
+    np.testing.assert_allclose(g["dX"], tX.grad.numpy(), atol=1e-10)
+    np.testing.assert_allclose(g["dW"], tW.grad.numpy(), atol=1e-10)
+    np.testing.assert_allclose(g["da"], ta.grad.numpy(), atol=1e-10)
+
+
+def test_gat_closed_forms_and_finite_differences():
+    """a = 0 gives the neighbour mean of FL and lse = ln deg; the backward
+    matches central differences of the forward."""
+    rng = np.random.default_rng(72)
+    N, F, H, D = 14, 4, 2, 3
+    indptr, indices = rand_graph(rng, N, 0.3, dups=True)
+    X = rng.standard_normal((N, F)); W = rng.standard_normal((F, H * D))
+    FL, out, lse = oracle.gat_fwd(indptr, indices, X, W, np.zeros((H, 2, D)))
+    for i in range(N):
+        srcs = indices[indptr[i]:indptr[i + 1]]
+        np.testing.assert_allclose(out[i], FL[srcs].mean(0), atol=1e-12)
+        np.testing.assert_allclose(lse[i], np.log(len(srcs)), atol=1e-12)
+    args = {"X": X, "W": W, "a": rng.standard_normal((H, 2, D))}
+    dO = rng.standard_normal((N, H, D))
+    g = oracle.gat_bwd(indptr, indices, args["X"], args["W"], args["a"], dO)
+    loss = lambda a_: (oracle.gat_fwd(indptr, indices, a_["X"], a_["W"], a_["a"])[1] * dO).sum()
+    eps = 1e-6
+    for name, gname in (("X", "dX"), ("W", "dW"), ("a", "da")):
+        for _ in range(5):
+            idx = tuple(rng.integers(s) for s in args[name].shape)
+            ap = {k: v.copy() for k, v in args.items()}
+            ap[name][idx] += eps
+            am = {k: v.copy() for k, v in args.items()}
+            am[name][idx] -= eps
+            assert (loss(ap) - loss(am)) / (2 * eps) == pytest.approx(g[gname][idx], rel=1e-6, abs=1e-8)
+
+
+def test_gat_edge_stage_composes_to_the_layer():
+    """The edge stage on FL, el = a_l . FL, er = a_r . FL gives the layer's
+    output; its gradients, chained through el, er and FL = X W, give the
+    layer's dX, dW and da."""
+    rng = np.random.default_rng(73)
+    N, F, H, D = 24, 5, 2, 3
+    indptr, indices = rand_graph(rng, N, 0.3, dups=True)
+    X = rng.standard_normal((N, F)); W = rng.standard_normal((F, H * D))
+    a = rng.standard_normal((H, 2, D)); dO = rng.standard_normal((N, H, D))
+    FL, out, lse = oracle.gat_fwd(indptr, indices, X, W, a)
+    el = np.einsum("nhd,hd->nh", FL, a[:, 0])
+    er = np.einsum("nhd,hd->nh", FL, a[:, 1])
+    o2, l2 = oracle.gat_edge_fwd(indptr, indices, FL, el, er)
+    np.testing.assert_allclose(o2, out, atol=1e-12)
+    np.testing.assert_allclose(l2, lse, atol=1e-12)
+    dFv, de_l, de_r = oracle.gat_edge_bwd(indptr, indices, FL, el, er, dO)
+    dFL = dFv + de_l[:, :, None] * a[None, :, 0] + de_r[:, :, None] * a[None, :, 1]
+    g = oracle.gat_bwd(indptr, indices, X, W, a, dO)
+    np.testing.assert_allclose(dFL, g["dFL"], atol=1e-11)
+    np.testing.assert_allclose(dFL.reshape(N, -1) @ W.T, g["dX"], atol=1e-11)
+    np.testing.assert_allclose(X.T @ dFL.reshape(N, -1), g["dW"], atol=1e-11)
+    da = np.stack([np.einsum("nh,nhd->hd", de_l, FL), np.einsum("nh,nhd->hd", de_r, FL)], 1)
+    np.testing.assert_allclose(da, g["da"], atol=1e-11)
