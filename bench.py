@@ -47,7 +47,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 GT_KERNELS = ["gt_fwd", "gt_fwd_merge", "bsr_fwd", "bsr_bwd_delta", "gt_bwd_dq", "gt_bwd_dkdv",
               "gt_bwd_merge", "bsr_bwd_dq", "bsr_bwd_dkdv"]
-AGG_KERNELS = ["agg_fwd", "agg_fwd_merge", "agg_bwd", "agg_bwd_cast"]
+AGG_KERNELS = ["agg_fwd", "agg_fwd_merge", "agg_bwd", "agg_bwd_merge"]
 GATV2_KERNELS = ["gatv2_proj", "gatv2_fwd", "gatv2_fwd_merge", "gatv2_bwd_dst", "gatv2_bwd_src",
                  "gatv2_bwd_merge", "gatv2_bwd_dx", "gatv2_bwd_dw", "gatv2_bwd_reduce"]
 
@@ -194,10 +194,10 @@ def algorithmic_bytes(kernel: str, N: int, E: int, H: int, D: int, F: int, s: in
         return ptr + idx + 2 * row + 4 * N * H + E * HD * s + row + 4 * N * H
     if kernel == "gatv2_bwd_src":
         return ptr + idx + row + E * (2 * HD * s + 8 * H) + row
-    if kernel == "agg_fwd":          # gathered rows; out and the winning source written
-        return ptr + idx + E * HD * s + row + 4 * N * HD
-    if kernel == "agg_bwd":          # arg and dOut read, dX written
-        return 4 * N * HD + row + row
+    if kernel == "agg_fwd":          # gathered rows; out and the win mask written
+        return ptr + idx + E * HD * s + row + E * HD * s // 16
+    if kernel == "agg_bwd":          # transposed CSR and edge map, win mask, each dOut row once, dX
+        return ptr + 2 * idx + E * HD * s // 16 + row + row
     if kernel == "gatv2_proj":
         return N * F * s + F * HD * s + row
     if kernel == "gatv2_bwd_dx":
@@ -357,8 +357,9 @@ class Workload:
             out, lse = sga.gt_attn_fwd(self.plan, d["Q"], d["K"], d["V"])
             return {"out": out, "lse": lse}, (out, lse)
         if w.layer.startswith("agg"):
-            out, arg = sga.agg_minmax_fwd(self.plan, d["X"], w.layer[4:])
-            return {"out": out, "arg": arg}, arg
+            # the layer's outputs: the aggregate and the win mask its backward takes
+            out, _, mask = sga.agg_minmax_fwd(self.plan, d["X"], w.layer[4:], arg=False)
+            return {"out": out, "mask": mask}, mask
         FL, FR, out, lse = sga.gatv2_fwd(self.plan, d["X"], d["W_l"], d["W_r"], d["a"], 0.2)
         return {"out": out, "lse": lse}, (FL, FR, out, lse)
 

@@ -216,24 +216,33 @@ sga_status gatv2_bwd(const sga_plan *plan, const int32_t *indptr, const int32_t 
  * out_i[f] = max (or min) over the sources j of row i of X_j[f], for every
  * element f of the node rows ([N, H, D] tensors read as [N, H*D]).  Needs a
  * plan built with opts->layer = SGA_LAYER_MINMAX (same N, E, H, D, dt).
- * arg[N, H*D] (int32, caller-owned, 16-byte aligned) receives the source node
- * that holds each extreme: the first edge of the row in CSR order among equal
- * values.  An empty row gives out = 0 and arg = -1.  Values must not be NaN.
- * Rows above the split threshold are cut into chunks whose partial extremes
- * are merged in chunk order; out and arg are exact (bit-identical to the
- * definition). */
+ * The winner of an element is the first edge of the row in CSR order among
+ * equal values; an empty row gives out = 0.  Values must not be NaN.  Rows
+ * above the split threshold are cut into chunks whose partial extremes are
+ * merged in chunk order; out is exact (bit-identical to the definition).
+ * Optional outputs (NULL: not written):
+ *   arg[N, H*D] int32 (16-byte aligned): the winning source node (-1 for an
+ *     empty row);
+ *   mask[E, R] bytes, R = H*D*sizeof(dt)/16 (sga_agg_mask_bytes): for CSR
+ *     edge e and 16-byte chunk c of the row, bit x is set when e won
+ *     element 8c + x (bf16) or 4c + x (fp32) of its row; the forward clears
+ *     it first.  The backward takes it. */
 typedef enum { SGA_AGG_MAX = 0, SGA_AGG_MIN = 1 } sga_agg_op;
 
 sga_status agg_minmax_fwd(const sga_plan *plan, const int32_t *indptr, const int32_t *indices,
                           const void *X, int64_t N, int64_t E, int H, int D, sga_dtype dt,
-                          sga_agg_op op, void *out, int32_t *arg, void *stream);
+                          sga_agg_op op, void *out, int32_t *arg, uint8_t *mask, void *stream);
+
+/* Bytes of the forward's win mask for this plan (0 for other plans). */
+size_t sga_agg_mask_bytes(const sga_plan *plan);
 
 /* Backward of the min / max aggregation: dX_j[f] = sum of dOut_i[f] over the
- * rows i whose element f was won by j (arg from the forward).  One fp32
- * atomic add per (i, f) into an fp32 accumulator (dX itself for fp32 layers,
- * the plan's workspace for bf16 layers, then rounded to bf16), so elements
- * that receive several contributions are sums in a run-dependent order. */
-sga_status agg_minmax_bwd(const sga_plan *plan, const int32_t *arg, const void *dOut, int64_t N,
+ * rows i whose element f was won by an edge from j (mask from the forward).
+ * One warp per source (or chunk of a high-degree source) walks its
+ * destinations over the transposed CSR and reads a destination's dOut chunk
+ * only where the mask has a bit; no atomics, sums in a fixed order
+ * (reproducible). */
+sga_status agg_minmax_bwd(const sga_plan *plan, const uint8_t *mask, const void *dOut, int64_t N,
                           int H, int D, sga_dtype dt, void *dX, void *stream);
 
 /* ---- graph reordering ------------------------------------------------------
@@ -392,7 +401,7 @@ typedef enum {
     SGA_KERN_BSR_FWD = 15, SGA_KERN_BSR_BWD_DELTA = 16, SGA_KERN_BSR_BWD_DQ = 17,
     SGA_KERN_BSR_BWD_DKDV = 18,
     SGA_KERN_AGG_FWD = 19, SGA_KERN_AGG_FWD_MERGE = 20, SGA_KERN_AGG_BWD = 21,
-    SGA_KERN_AGG_BWD_CAST = 22,
+    SGA_KERN_AGG_BWD_MERGE = 22,
     SGA_KERN_GAT_FWD = 23, SGA_KERN_GAT_BWD_DST = 24, SGA_KERN_GAT_BWD_SRC = 25,
     SGA_KERN_COUNT = 26
 } sga_kernel_id;

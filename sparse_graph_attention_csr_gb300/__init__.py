@@ -27,7 +27,7 @@ KERNELS = {
     "gatv2_proj": 6, "gatv2_fwd": 7, "gatv2_fwd_merge": 8, "gatv2_bwd_dst": 9,
     "gatv2_bwd_src": 10, "gatv2_bwd_merge": 11, "gatv2_bwd_dx": 12, "gatv2_bwd_dw": 13,
     "gatv2_bwd_reduce": 14, "bsr_fwd": 15, "bsr_bwd_delta": 16, "bsr_bwd_dq": 17,
-    "bsr_bwd_dkdv": 18, "agg_fwd": 19, "agg_fwd_merge": 20, "agg_bwd": 21, "agg_bwd_cast": 22,
+    "bsr_bwd_dkdv": 18, "agg_fwd": 19, "agg_fwd_merge": 20, "agg_bwd": 21, "agg_bwd_merge": 22,
     "gat_fwd": 23, "gat_bwd_dst": 24, "gat_bwd_src": 25,
 }
 
@@ -106,8 +106,9 @@ _SIGNATURES = {
                             _int),
     "sga_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "sga_noalloc_read_device_error": ([_vp, ctypes.POINTER(ctypes.c_int32)], _int),
-    "agg_minmax_fwd": ([_vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _vp, _vp, _vp],
-                       _int),
+    "agg_minmax_fwd": ([_vp, _vp, _vp, _vp, _i64, _i64, _int, _int, _int, _int, _vp, _vp, _vp,
+                        _vp], _int),
+    "sga_agg_mask_bytes": ([_vp], ctypes.c_size_t),
     "agg_minmax_bwd": ([_vp, _vp, _vp, _i64, _int, _int, _int, _vp, _vp], _int),
     "sga_reorder": ([_vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "sga_relabel_csr": ([_vp, _vp, _i64, _i64, _vp, _vp, _vp, _vp], _int),
@@ -500,26 +501,36 @@ def gat_attn_bwd(plan: Plan, Fv, el, er, out, lse, dOut, slope: float = 0.2, str
 
 # ------------------------------------------------------- min / max aggregation
 
-def agg_minmax_fwd(plan: Plan, X, op: str = "max", out=None, arg=None, stream=None):
-    """(out, arg): out [N,H,D] = elementwise max (or min) of the sources' rows,
-    arg [N,H,D] int32 = the winning source (first edge on ties, -1 for an
-    empty row).  ``plan`` must be built with layer=SGA_LAYER_MINMAX."""
+def agg_minmax_fwd(plan: Plan, X, op: str = "max", out=None, arg=True, mask=True, stream=None):
+    """(out, arg, mask): out [N,H,D] = elementwise max (or min) of the sources'
+    rows; arg [N,H,D] int32 = the winning source (first edge on ties, -1 for
+    an empty row); mask [E, R] uint8 = the win mask the backward takes.
+    ``arg``/``mask`` = False skips that output (None in its place), a tensor
+    is filled in place.  ``plan`` must be built with layer=SGA_LAYER_MINMAX."""
     _need(X, "X", plan.dtype)
     out = torch.empty_like(X) if out is None else out
-    arg = torch.empty(X.shape, dtype=torch.int32, device=X.device) if arg is None else arg
+    if arg is True:
+        arg = torch.empty(X.shape, dtype=torch.int32, device=X.device)
+    elif arg is False:
+        arg = None
+    if mask is True:
+        mask = torch.empty(int(_lib().sga_agg_mask_bytes(plan.handle)), dtype=torch.uint8,
+                           device=X.device)
+    elif mask is False:
+        mask = None
     code = {"max": SGA_AGG_MAX, "min": SGA_AGG_MIN}[op]
     _check(_lib().agg_minmax_fwd(plan.handle, *plan._graph()[:2], _ptr(X), plan.N, plan.E, plan.H,
-                                 plan.D, plan.dt, code, _ptr(out), _ptr(arg), _stream(stream)),
-           "agg_minmax_fwd")
-    return out, arg
+                                 plan.D, plan.dt, code, _ptr(out), _ptr(arg), _ptr(mask),
+                                 _stream(stream)), "agg_minmax_fwd")
+    return out, arg, mask
 
 
-def agg_minmax_bwd(plan: Plan, arg, dOut, dX=None, stream=None):
-    """dX [N,H,D]: dOut routed to the winning sources of the forward."""
-    _need(arg, "arg", torch.int32)
+def agg_minmax_bwd(plan: Plan, mask, dOut, dX=None, stream=None):
+    """dX [N,H,D]: dOut gathered into the winning sources of the forward."""
+    _need(mask, "mask", torch.uint8)
     _need(dOut, "dOut", plan.dtype)
     dX = torch.empty_like(dOut) if dX is None else dX
-    _check(_lib().agg_minmax_bwd(plan.handle, _ptr(arg), _ptr(dOut), plan.N, plan.H, plan.D,
+    _check(_lib().agg_minmax_bwd(plan.handle, _ptr(mask), _ptr(dOut), plan.N, plan.H, plan.D,
                                  plan.dt, _ptr(dX), _stream(stream)), "agg_minmax_bwd")
     return dX
 
@@ -551,15 +562,15 @@ class MinMaxAggregation(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, X, plan, op="max"):
-        out, arg = agg_minmax_fwd(plan, X.contiguous(), op)
+        out, _, mask = agg_minmax_fwd(plan, X.contiguous(), op, arg=False)
         ctx.plan = plan
-        ctx.save_for_backward(arg)
+        ctx.save_for_backward(mask)
         return out
 
     @staticmethod
     def backward(ctx, dOut):
-        (arg,) = ctx.saved_tensors
-        return agg_minmax_bwd(ctx.plan, arg, dOut.contiguous()), None, None
+        (mask,) = ctx.saved_tensors
+        return agg_minmax_bwd(ctx.plan, mask, dOut.contiguous()), None, None
 
 
 class GATEdgeAttention(torch.autograd.Function):

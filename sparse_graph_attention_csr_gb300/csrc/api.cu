@@ -50,9 +50,8 @@ void compute_layout(sga_plan *p) {
         return at;
     };
     if (p->layer == SGA_LAYER_MINMAX) {
-        L.agg_val = take((size_t)p->rows.n_chunks * HD * 4);
+        L.agg_val = take((size_t)std::max(p->rows.n_chunks, p->cols.n_chunks) * HD * 4);
         L.agg_pos = take((size_t)p->rows.n_chunks * HD * 4);
-        if (p->dt == SGA_BF16) L.agg_acc = take((size_t)p->N * HD * 4);
         L.total = off;
         return;
     }
@@ -217,6 +216,7 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     p->layer = o.layer;
     p->schedule = o.schedule;
     p->edge_bias = o.edge_bias;
+    p->keep_eid = o.edge_bias || o.layer == SGA_LAYER_MINMAX;   // (the aggregation backward's edge map)
     p->row_order = o.row_order == 2 ? 2 : 1;   // 0 (default) and 1: descending degree
     p->dt = dt;
     p->split_threshold = o.split_threshold > 0 ? o.split_threshold : 256;
@@ -642,45 +642,56 @@ static AggArgs agg_args(const sga_plan *p) {
     AggArgs a{};
     a.indptr = p->indptr;
     a.indices = p->indices;
+    a.t_dst = p->t_dst;
+    a.t_eid = p->t_eid;
     a.N = p->N;
+    a.E = p->E;
     a.HD = p->H * p->D;
     a.split_threshold = p->split_threshold;
     a.num_sms = p->num_sms;
     a.rows = p->rows;
+    a.cols = p->cols;
     a.d_err = p->d_err;
     if (p->ws) {
         a.ws_val = ws_at<float>(p, p->layout.agg_val);
         a.ws_pos = ws_at<int32_t>(p, p->layout.agg_pos);
-        a.ws_acc = ws_at<float>(p, p->layout.agg_acc);
     }
     return a;
 }
 
 sga_status agg_minmax_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *indices,
                           const void *X, int64_t N, int64_t E, int H, int D, sga_dtype dt,
-                          sga_agg_op op, void *out, int32_t *arg, void *stream) {
+                          sga_agg_op op, void *out, int32_t *arg, uint8_t *mask, void *stream) {
     if (p && p->layer != SGA_LAYER_MINMAX) return SGA_EINVAL;
     if (op != SGA_AGG_MAX && op != SGA_AGG_MIN) return SGA_EINVAL;
     sga_status st = check_call(p, indptr, indices, N, E, H, D, dt, 0);
     if (st != SGA_OK) return st;
-    if (!tensors_ok(N, {X, out, arg})) return SGA_EINVAL;
+    if (!tensors_ok(N, {X, out})) return SGA_EINVAL;
+    if (arg && N > 0 && !aligned(arg, 16)) return SGA_EINVAL;
     AggArgs a = agg_args(p);
     a.X = X;
     a.out = out;
     a.arg = arg;
+    a.mask = mask;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool mx = op == SGA_AGG_MAX;
     return cuda_status(dt == SGA_F32 ? agg_fwd_t<float>(a, mx, s) : agg_fwd_t<__nv_bfloat16>(a, mx, s));
 }
 
-sga_status agg_minmax_bwd(const sga_plan *p, const int32_t *arg, const void *dOut, int64_t N,
+size_t sga_agg_mask_bytes(const sga_plan *p) {
+    if (!p || p->layer != SGA_LAYER_MINMAX) return 0;
+    return (size_t)p->E * ((size_t)p->H * p->D * (p->dt == SGA_F32 ? 4 : 2) / 16);
+}
+
+sga_status agg_minmax_bwd(const sga_plan *p, const uint8_t *mask, const void *dOut, int64_t N,
                           int H, int D, sga_dtype dt, void *dX, void *stream) {
     if (!p || p->layer != SGA_LAYER_MINMAX) return SGA_EINVAL;
     if (N != p->N || H != p->H || D != p->D || dt != p->dt) return SGA_EINVAL;
     if (p->layout.total > 0 && (!p->ws || p->ws_bytes < p->layout.total)) return SGA_EWORKSPACE;
-    if (!tensors_ok(N, {arg, dOut, dX})) return SGA_EINVAL;
+    if (!tensors_ok(N, {dOut, dX})) return SGA_EINVAL;
+    if (p->E > 0 && !mask) return SGA_EINVAL;
     AggArgs a = agg_args(p);
-    a.arg = const_cast<int32_t *>(arg);
+    a.mask = const_cast<uint8_t *>(mask);
     a.dOut = dOut;
     a.dX = dX;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -371,7 +371,7 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
     p->d_err = own.get<int32_t>(1);
     p->t_indptr = own.get<int32_t>(N + 1);
     p->t_dst = own.get<int32_t>(E);
-    if (p->edge_bias) p->t_eid = own.get<int32_t>(E);
+    if (p->keep_eid) p->t_eid = own.get<int32_t>(E);
     if (own.err != cudaSuccess) {
         set_cuda_error(own.err);
         own.release();
@@ -421,7 +421,7 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
         SGA_TRY(cudaMemcpyAsync(ka, p->indices, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
         // values: the destination of every edge, or (edge-bias plans) the
         // edge itself, whose destination is looked up after the sort
-        if (p->edge_bias)
+        if (p->keep_eid)
             iota_edges_kernel<<<grid_for(E, 256, 8192), 256, 0, s>>>(va, E);
         else
             edge_rows_kernel<<<grid_for(N * 32, 256, INT32_MAX), 256, 0, s>>>(p->indptr, N, va);
@@ -439,7 +439,7 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
             std::swap(ka, kb);
             std::swap(va, vb);
         }
-        if (p->edge_bias) {
+        if (p->keep_eid) {
             SGA_TRY(cudaMemcpyAsync(p->t_eid, va, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, s));
             edge_rows_kernel<<<grid_for(N * 32, 256, INT32_MAX), 256, 0, s>>>(p->indptr, N, kb);
             gather_rows_kernel<<<grid_for(E, 256, 8192), 256, 0, s>>>(kb, va, E, p->t_dst);

@@ -50,7 +50,7 @@ struct WorkspaceLayout {
     size_t fix = 0;        // int32 count, then [fix_cap] int2 projection elements to round exactly
     size_t agg_val = 0;    // [n_chunks, H*D] f32  min/max aggregation: chunk extremes
     size_t agg_pos = 0;    // [n_chunks, H*D] i32  their edge positions
-    size_t agg_acc = 0;    // [N, H*D] f32         backward accumulator (bf16 layers)
+    size_t agg_col = 0;    // [t_n_chunks, H*D] f32 backward: chunk sums of split sources
     int32_t fix_cap = 0;
     size_t total = 0;
     int32_t da_blocks = 0;
@@ -93,6 +93,7 @@ struct sga_plan {
     int32_t *t_dst = nullptr;          // [E]
     int32_t *t_eid = nullptr;          // [E] CSR edge of each transposed entry (edge-bias plans)
     int edge_bias = 0;                 // plan serves gt_attn_bias_fwd/bwd
+    int keep_eid = 0;                  // plan keeps t_eid (edge-bias and aggregation plans)
     int row_order = 1;                 // 1: rows walked by descending degree, 2: by ascending id
     sga::Partition rows, cols;         // partitions of the CSR and the transposed CSR
     sga::TileSet tiles;                // block-sparse split (tiles.min_nnz > 0)
@@ -247,13 +248,15 @@ struct AggArgs {
     const int32_t *indptr, *indices;
     const void *X, *dOut;   // [N, HD] in the layer dtype
     void *out, *dX;         // likewise
-    int32_t *arg;           // [N, HD] winning source node (-1: empty row)
-    int64_t N;
+    int32_t *arg;           // [N, HD] winning source node (-1: empty row); nullptr: not written
+    uint8_t *mask;          // [E, R] win-mask bytes (R = 16-byte chunks of a row); nullptr: not written
+    const int32_t *t_dst, *t_eid;   // transposed CSR and its CSR edge map
+    int64_t N, E;
     int HD;
     int split_threshold;
     int num_sms;
-    Partition rows;
-    float *ws_val, *ws_acc;
+    Partition rows, cols;
+    float *ws_val;          // forward: chunk extremes [n_chunks, HD]; backward: chunk sums [t_n_chunks, HD]
     int32_t *ws_pos;
     int32_t *d_err;
 };

@@ -27,6 +27,27 @@ def tie_values(rng, N, H, D, dtype, levels=7):
     return t, t.to(torch.float64).numpy()
 
 
+def expected_mask(indptr, indices, arg, dtype):
+    """The win mask the forward must write, from the oracle's winners: the
+    winning edge of (row i, element f) is the first edge of row i whose
+    source is arg[i, f] (equal sources carry equal values, and ties go to the
+    first edge); bit f % EL of byte (edge, f // EL)."""
+    EL = 8 if dtype == "bf16" else 4
+    N = len(indptr) - 1
+    a = arg.reshape(N, -1)
+    HD = a.shape[1]
+    mask = np.zeros((len(indices), HD // EL), np.uint8)
+    for i in range(N):
+        b, e = indptr[i], indptr[i + 1]
+        first = {}
+        for x in range(b, e):
+            first.setdefault(int(indices[x]), x)
+        for f in range(HD):
+            if a[i, f] >= 0:
+                mask[first[int(a[i, f])], f // EL] |= np.uint8(1 << (f % EL))
+    return mask
+
+
 def run_agg(indptr, indices, H, D, dtype, op, seed=0, split=0, chunk=0, backward=True):
     rng = np.random.default_rng(seed)
     N = len(indptr) - 1
@@ -35,14 +56,18 @@ def run_agg(indptr, indices, H, D, dtype, op, seed=0, split=0, chunk=0, backward
     ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
     plan = sga.Plan(ip, ix, H, D, TORCH_DT[dtype], split_threshold=split, chunk_len=chunk,
                     layer=sga.SGA_LAYER_MINMAX)
-    out, arg = sga.agg_minmax_fwd(plan, dev(X), op)
+    out, arg, mask = sga.agg_minmax_fwd(plan, dev(X), op)
     ro, ra = oracle.agg_fwd(indptr, indices, xf, op)
     assert np.array_equal(out.double().cpu().numpy(), ro), "values differ"
     assert np.array_equal(arg.cpu().numpy(), ra), "winning sources differ"
+    if len(indices):
+        assert np.array_equal(mask.cpu().numpy().reshape(len(indices), -1),
+                              expected_mask(indptr, indices, ra, dtype)), "win masks differ"
     if backward:
-        dX = sga.agg_minmax_bwd(plan, arg, dev(dO))
+        dX = sga.agg_minmax_bwd(plan, mask, dev(dO))
         rdx = oracle.agg_bwd(ra, dO.double().numpy())
         compare(dX, rdx, dtype, "dX")
+        assert torch.equal(dX, sga.agg_minmax_bwd(plan, mask, dev(dO))), "backward not reproducible"
     torch.cuda.synchronize()
     assert plan.device_error() == 0
     return plan
@@ -78,11 +103,14 @@ def test_small_workload_recipe():
     x = synth.agg_inputs(w)
     ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
     plan = sga.Plan(ip, ix, w.H, w.D, torch.bfloat16, layer=sga.SGA_LAYER_MINMAX)
-    out, arg = sga.agg_minmax_fwd(plan, dev(x["X"][0]), "min")
+    out, arg, mask = sga.agg_minmax_fwd(plan, dev(x["X"][0]), "min")
     ro, ra = oracle.agg_fwd(indptr, indices, x["X"][1], "min")
     assert np.array_equal(out.double().cpu().numpy(), ro)
     assert np.array_equal(arg.cpu().numpy(), ra)
-    dX = sga.agg_minmax_bwd(plan, arg, dev(x["dOut"][0]))
+    # without the winners output, the values and the mask are the same
+    out2, none, mask2 = sga.agg_minmax_fwd(plan, dev(x["X"][0]), "min", arg=False)
+    assert none is None and torch.equal(out2, out) and torch.equal(mask2, mask)
+    dX = sga.agg_minmax_bwd(plan, mask, dev(x["dOut"][0]))
     compare(dX, oracle.agg_bwd(ra, x["dOut"][1]), "bf16", "dX")
     assert plan.device_error() == 0
 
