@@ -243,11 +243,32 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
 
 
-def source_hash() -> str:
+# the source files each kernel family is compiled from (its own kernels, the
+# edge stream and the plan that orders its work); a traffic figure is kept
+# only while these files are unchanged since the counters were taken
+_COMMON = ["common.cuh", "plan.h", "plan.cu", "items.cuh", "stream.cuh"]
+FAMILY_SOURCES = {
+    "gt": _COMMON + ["gt.cuh", "gt_bf16.cu", "gt_f32.cu"],
+    "gatv2": _COMMON + ["gatv2.cuh", "gatv2_bf16.cu", "gatv2_f32.cu", "gemm.cuh", "tc.cuh",
+                        "tc_proj.cu", "tc_proj.cuh", "tc_dx.cu", "tc_dx.cuh"],
+    "bsr": _COMMON + ["tc.cuh", "bsr.cu", "bsr_fwd.cu", "bsr_bwd.cu"],
+    "agg": _COMMON + ["gt.cuh", "agg.cu"],
+}
+
+
+def kernel_family(kernel: str) -> str:
+    for fam in ("gatv2", "bsr", "agg", "gt"):
+        if kernel.startswith(fam):
+            return fam
+    return ""
+
+
+def source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_graph_attention_csr_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = FAMILY_SOURCES.get(kernel_family(kernel)) or sorted(os.listdir(csrc))
+    for f in sorted(files):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -256,14 +277,14 @@ def source_hash() -> str:
 
 def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, only if it was
-    taken on the current kernel sources."""
+    taken on the current sources of the kernel's family."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
     except Exception:
         return None
     e = t.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
