@@ -98,7 +98,7 @@ typedef enum {
 /* Build a plan: validates the CSR on the device (indptr[0] = 0, monotone,
  * indptr[N] = E, 0 <= indices < N), builds the transposed CSR (sources ->
  * ascending destinations) and the degree partitions of both.
- * Block-sparse plans (opts->tile_min_nnz > 0; bf16, D in {64, 128}, N <= 2^18):
+ * Block-sparse plans (opts->tile_min_nnz > 0; bf16, D in {64, 128}):
  * the "block-sparse graph representation that enables the use of tensor
  * cores" of the IO-aware layers blog post ("Attention-based layers"
  * paragraph).  Destinations are grouped in panels of 128 rows and sources in
@@ -110,8 +110,9 @@ typedef enum {
  * the tensor cores, runs the residual CSR backward with it, then adds the
  * tiles' dQ (row panels) and dK/dV (column panels of 128 sources) from
  * tensor-core products (FlashAttention-2 style).  A
- * mask holds an edge once, so an edge repeated inside a kept tile is refused
- * (SGA_EINVAL); other shapes and dtypes return SGA_EUNSUPPORTED.
+ * mask holds a (destination, source) pair once: the first edge of a pair in a
+ * kept tile sets its bit and any repeat of it (its own softmax term) joins the
+ * residual CSR.  Other shapes and dtypes return SGA_EUNSUPPORTED.
  * indptr/indices: device pointers, read only during this call.
  * The plan owns device memory for the transposed CSR and partitions (freed by
  * sga_plan_destroy).  Synchronises `stream`.  Returns SGA_EINVAL for an

@@ -481,9 +481,12 @@ def gatv2_bwd_bound(indptr, indices, X, Wl, Wr, a, dO, slope=0.2):
 def tile_extract(indptr, indices, N, min_nnz, panel=128, width=16):
     """Block-sparse split of a CSR by its definition: rows in panels of
     ``panel`` destinations, sources in column tiles of ``width``; a
-    (panel, tile) pair with at least ``min_nnz`` edges is kept, with one
-    ``width``-bit mask per panel row (bit b: source width*tile + b present);
-    every other edge stays in a residual CSR (same row order and source order).
+    (panel, tile) pair with at least ``min_nnz`` edges (repeats counted) is
+    kept, with one ``width``-bit mask per panel row (bit b: source width*tile
+    + b present).  A mask holds each (destination, source) pair once: the
+    first edge of the pair in CSR order sets the bit, and a repeat of it
+    (another term of the row's softmax) stays in the residual CSR with every
+    edge of a tile that is not kept (same row order and source order).
 
     Returns dict: tile_ptr [P+1], tile_col [T], tile_bits [T, panel] (uint16),
     r_indptr [N+1], r_indices [E_r]."""
@@ -495,7 +498,12 @@ def tile_extract(indptr, indices, N, min_nnz, panel=128, width=16):
     key = pan * ((N + width - 1) // width) + col
     uniq, counts = np.unique(key, return_counts=True)
     kept_keys = uniq[counts >= min_nnz]
-    kept = np.isin(key, kept_keys)
+    # first occurrence of every (destination, source) pair in CSR order
+    first = np.zeros(len(indices), bool)
+    if len(indices):
+        _, first_at = np.unique(rows * N + indices, return_index=True)
+        first[first_at] = True
+    kept = np.isin(key, kept_keys) & first
     tile_ptr = np.zeros(P + 1, np.int64)
     kp = kept_keys // ((N + width - 1) // width)
     np.add.at(tile_ptr, kp + 1, 1)

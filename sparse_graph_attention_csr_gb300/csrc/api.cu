@@ -72,7 +72,12 @@ void compute_layout(sga_plan *p) {
     L.fwd_acc = take((size_t)p->rows.n_chunks * HD * 4);
     L.bwd_row = take((size_t)p->rows.n_chunks * (p->F > 0 ? 4 : 2) * HD * 4);
     L.bwd_rowc = take((size_t)p->rows.n_chunks * p->H * 2 * 4);
-    if (p->tiles.min_nnz > 0) L.zt = take((size_t)p->N * p->H * 4);
+    if (p->tiles.min_nnz > 0) {
+        L.zt = take((size_t)p->N * p->H * 4);
+        const size_t n_pad = (size_t)((p->N + 127) / 128) * 128;
+        L.bsr_lse_t = take(n_pad * p->H * 4);
+        L.bsr_delta_t = take(n_pad * p->H * 4);
+    }
     if (p->edge_bias) L.bias_t = take((size_t)p->E * p->H * 4);
     L.bwd_col = take((size_t)p->cols.n_chunks * 2 * HD * 4);
     if (p->F > 0) {
@@ -202,7 +207,7 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     if (o.row_order < 0 || o.row_order > 2) return SGA_EINVAL;
     if (o.edge_bias && (o.layer != SGA_LAYER_ATTENTION || o.in_features != 0 || o.tile_min_nnz != 0))
         return SGA_EUNSUPPORTED;
-    if (o.tile_min_nnz > 0 && (!bsr_fwd_supported(dt, D) || N > (1 << 18) || o.tile_min_nnz > 128 * 16))
+    if (o.tile_min_nnz > 0 && (!bsr_fwd_supported(dt, D) || o.tile_min_nnz > 128 * 16))
         return SGA_EUNSUPPORTED;
     if (o.in_features != 0 && (o.in_features % 8 != 0 || o.in_features > 1024))
         return SGA_EUNSUPPORTED;
@@ -425,10 +430,14 @@ sga_status gt_attn_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *
         b.tile_ptr = p->tiles.tile_ptr;
         b.tile_col = p->tiles.tile_col;
         b.tile_bits = p->tiles.tile_bits;
+        b.panel_order = p->tiles.panel_order;
         b.N = N;
         b.H = H;
         b.D = D;
         b.n_panels = p->tiles.n_panels;
+        b.n_tiles = p->tiles.n_tiles;
+        b.n_active = p->tiles.n_active;
+        b.num_sms = p->num_sms;
         b.d_err = p->d_err;
         return cuda_status(launch_bsr_fwd(b, s));
     }
@@ -481,11 +490,21 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
         b.ct_ptr = p->tiles.ct_ptr;
         b.ct_panel = p->tiles.ct_panel;
         b.ct_tile = p->tiles.ct_tile;
+        b.tile_bits_t = p->tiles.tile_bits_t;
+        b.panel_order = p->tiles.panel_order;
+        b.cpanel_order = p->tiles.cpanel_order;
+        b.lse_t = ws_at<float>(p, p->layout.bsr_lse_t);
+        b.delta_t_hm = ws_at<float>(p, p->layout.bsr_delta_t);
         b.N = N;
+        b.N_pad = (N + 127) / 128 * 128;
         b.H = H;
         b.D = D;
         b.n_panels = p->tiles.n_panels;
         b.n_cpanels = p->tiles.n_cpanels;
+        b.n_tiles = p->tiles.n_tiles;
+        b.n_active = p->tiles.n_active;
+        b.n_cactive = p->tiles.n_cactive;
+        b.num_sms = p->num_sms;
         b.d_err = p->d_err;
         cudaError_t e = cudaMemsetAsync(b.delta_t, 0, sizeof(float) * (size_t)N * H, s);
         if (e == cudaSuccess) e = cudaMemsetAsync(b.z_t, 0, sizeof(float) * (size_t)N * H, s);

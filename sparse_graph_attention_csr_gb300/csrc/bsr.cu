@@ -1,16 +1,24 @@
-// Block-sparse split of a destination-sorted CSR for the tensor-core
-// forward: the "block-sparse graph representation that enables the use of
-// tensor cores" of the IO-aware layers blog post ("Attention-based layers"
+// Block-sparse split of a destination-sorted CSR for the tensor-core passes:
+// the "block-sparse graph representation that enables the use of tensor
+// cores" of the IO-aware layers blog post ("Attention-based layers"
 // paragraph), which pays off on locally dense graphs.
 //
 // Rows form panels of 128 destinations, sources form column tiles of 16.  A
 // (panel, tile) pair holding at least min_nnz edges is kept: its column index
-// and one 16-bit source mask per panel row are stored.  All other edges stay
-// in a residual CSR, in their original order.  One CTA per panel counts the
-// edges per column tile in a shared-memory histogram (16-bit counts packed in
-// pairs); kept tiles are listed in column order.  Everything is determined by
-// the graph and min_nnz: the arrays are bit-exact.
+// and one 16-bit source mask per panel row are stored.  A mask holds a
+// (destination, source) pair once, so a repeated edge of a kept tile (the same
+// pair again, later in CSR order) joins the residual: the softmax runs over
+// edges, and the residual pass adds its term.  All other edges stay in a
+// residual CSR, in their original order.
+//
+// The split is found by sorting the edges by (panel, tile, row within the
+// panel, source within the tile), least significant key first, with stable
+// radix passes: runs of equal (panel, tile) are the candidate tiles, and a
+// repeated edge sits right after its first occurrence.  Nothing depends on
+// the number of nodes beyond the int32 index range, and every array is
+// determined by the graph and min_nnz (bit-exact).
 #include <algorithm>
+#include <numeric>
 #include <vector>
 
 #include "common.cuh"
@@ -19,130 +27,169 @@
 namespace sga {
 namespace {
 
-constexpr int kPanel = 128, kWidth = 16, kThreads = 256;
+constexpr int kPanel = 128, kWidth = 16;
 
-__device__ __forceinline__ uint32_t bin_count(const uint32_t *h, int b) {
-    return (h[b >> 1] >> ((b & 1) * 16)) & 0xffffu;
+unsigned grid_of(int64_t n, int64_t cap = 65535) {
+    return (unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, cap));
 }
 
-__device__ void panel_histogram(const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
-                                int64_t N, int p, uint32_t *h, int words) {
-    for (int w = threadIdx.x; w < words; w += blockDim.x) h[w] = 0;
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t r0 = (int64_t)p * kPanel;
-    for (int rr = warp; rr < kPanel && r0 + rr < N; rr += blockDim.x >> 5) {
-        const int32_t b = indptr[r0 + rr], e = indptr[r0 + rr + 1];
-        for (int32_t x = b + lane; x < e; x += 32) {
-            const int bin = indices[x] / kWidth;
-            atomicAdd(&h[bin >> 1], 1u << ((bin & 1) * 16));
+// destination row of every edge (a warp per row)
+__global__ void edge_dst_kernel(const int32_t *__restrict__ indptr, int64_t N, int32_t *__restrict__ rows) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < N; i += nw)
+        for (int32_t e = indptr[i] + lane; e < indptr[i + 1]; e += 32) rows[e] = (int32_t)i;
+}
+
+// least significant sort key: (row within the panel, source within the tile)
+__global__ void key_low_kernel(const int32_t *__restrict__ rows, const int32_t *__restrict__ indices, int64_t E,
+                               int32_t *__restrict__ key, int32_t *__restrict__ val) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < E; e += stride) {
+        key[e] = ((rows[e] & (kPanel - 1)) << 4) | (indices[e] & (kWidth - 1));
+        val[e] = (int32_t)e;
+    }
+}
+
+// next key of the sorted edges: src[edge] >> shift (the tile, then the panel)
+__global__ void key_gather_kernel(const int32_t *__restrict__ src, int shift, const int32_t *__restrict__ val,
+                                  int64_t E, int32_t *__restrict__ key) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < E; k += stride) key[k] = src[val[k]] >> shift;
+}
+
+// run heads (a new (panel, tile) pair) and repeats (the same pair as the
+// previous edge in sorted order) of the sorted edges
+__global__ void run_flags_kernel(const int32_t *__restrict__ rows, const int32_t *__restrict__ indices,
+                                 const int32_t *__restrict__ val, int64_t E, int32_t *__restrict__ head,
+                                 uint8_t *__restrict__ rep) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < E; k += stride) {
+        const int32_t e = val[k], r = rows[e], j = indices[e];
+        int32_t h = 1;
+        uint8_t rp = 0;
+        if (k > 0) {
+            const int32_t e1 = val[k - 1], r1 = rows[e1], j1 = indices[e1];
+            h = (r >> 7) != (r1 >> 7) || (j >> 4) != (j1 >> 4);
+            rp = r == r1 && j == j1;
+        }
+        head[k] = h;
+        rep[k] = rp;
+    }
+}
+
+__global__ void run_start_kernel(const int32_t *__restrict__ head, const int32_t *__restrict__ run_excl, int64_t E,
+                                 int32_t *__restrict__ start) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < E; k += stride)
+        if (head[k]) start[run_excl[k]] = (int32_t)k;
+}
+
+// keep[r] = run r holds at least min_nnz edges (keep[n_runs] = 0)
+__global__ void run_keep_kernel(const int32_t *__restrict__ start, int64_t n_runs, int64_t E, int min_nnz,
+                                int32_t *__restrict__ keep) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r <= n_runs; r += stride) {
+        if (r == n_runs) {
+            keep[r] = 0;
+            continue;
+        }
+        const int64_t end = r + 1 < n_runs ? start[r + 1] : E;
+        keep[r] = end - start[r] >= min_nnz;
+    }
+}
+
+// column and panel of every kept tile
+__global__ void tile_info_kernel(const int32_t *__restrict__ start, const int32_t *__restrict__ keep,
+                                 const int32_t *__restrict__ tix, int64_t n_runs, const int32_t *__restrict__ val,
+                                 const int32_t *__restrict__ rows, const int32_t *__restrict__ indices,
+                                 int32_t *__restrict__ tile_col, int32_t *__restrict__ panel_count) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < n_runs; r += stride)
+        if (keep[r]) {
+            const int32_t e = val[start[r]];
+            tile_col[tix[r]] = indices[e] >> 4;
+            atomicAdd(&panel_count[rows[e] >> 7], 1);
+        }
+}
+
+// mask bits of the kept, first-occurrence edges; residual flag of the others
+__global__ void tile_bits_kernel(const int32_t *__restrict__ head, const int32_t *__restrict__ run_excl,
+                                 const uint8_t *__restrict__ rep, const int32_t *__restrict__ keep,
+                                 const int32_t *__restrict__ tix, const int32_t *__restrict__ val,
+                                 const int32_t *__restrict__ rows, const int32_t *__restrict__ indices, int64_t E,
+                                 uint32_t *__restrict__ bits32, uint8_t *__restrict__ res) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < E; k += stride) {
+        const int32_t run = run_excl[k] + head[k] - 1, e = val[k];
+        if (keep[run] && !rep[k]) {
+            const int32_t r = rows[e], j = indices[e];
+            const int64_t word = ((int64_t)tix[run] * kPanel + (r & (kPanel - 1))) >> 1;
+            atomicOr(&bits32[word], (1u << (j & (kWidth - 1))) << ((r & 1) * 16));
+            res[e] = 0;
+        } else {
+            res[e] = 1;
         }
     }
-    __syncthreads();
 }
 
-// Kept tiles per panel and residual edges per row.
-__global__ void __launch_bounds__(kThreads)
-bsr_count_kernel(const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices, int64_t N,
-                 int n_bins, int min_nnz, int32_t *__restrict__ kept, int32_t *__restrict__ r_count) {
-    extern __shared__ uint32_t h[];
-    __shared__ int32_t red[kThreads / 32];
-    const int p = blockIdx.x, words = (n_bins + 1) / 2;
-    panel_histogram(indptr, indices, N, p, h, words);
-    int c = 0;
-    for (int b = threadIdx.x; b < n_bins; b += blockDim.x) c += bin_count(h, b) >= (uint32_t)min_nnz;
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(SGA_FULL_MASK, c, o);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = c;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int t = 0;
-        for (int w = 0; w < kThreads / 32; ++w) t += red[w];
-        kept[p] = t;
-    }
-    const int64_t r0 = (int64_t)p * kPanel;
-    for (int rr = warp; rr < kPanel && r0 + rr < N; rr += kThreads / 32) {
-        const int32_t b = indptr[r0 + rr], e = indptr[r0 + rr + 1];
+// residual edges per row (a warp per row)
+__global__ void res_count_kernel(const int32_t *__restrict__ indptr, int64_t N, const uint8_t *__restrict__ res,
+                                 int32_t *__restrict__ count) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < N; i += nw) {
         int n = 0;
-        for (int32_t x = b + lane; x < e; x += 32) n += bin_count(h, indices[x] / kWidth) < (uint32_t)min_nnz;
+        for (int32_t e = indptr[i] + lane; e < indptr[i + 1]; e += 32) n += res[e];
         for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(SGA_FULL_MASK, n, o);
-        if (lane == 0) r_count[r0 + rr] = n;
+        if (lane == 0) count[i] = n;
     }
 }
 
-// Tile columns (in column order), tile masks, residual indices (in order).
-__global__ void __launch_bounds__(kThreads)
-bsr_fill_kernel(const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices, int64_t N,
-                int n_bins, int min_nnz, const int32_t *__restrict__ tile_ptr,
-                int32_t *__restrict__ tile_col, uint32_t *__restrict__ tile_bits32,
-                const int32_t *__restrict__ r_indptr, int32_t *__restrict__ r_indices,
-                int32_t *__restrict__ dup) {
-    extern __shared__ uint32_t h[];
-    __shared__ int32_t scan[kThreads];
-    const int p = blockIdx.x, words = (n_bins + 1) / 2, tid = threadIdx.x;
-    panel_histogram(indptr, indices, N, p, h, words);
-    // kept bins of this thread's contiguous range, then a block prefix sum
-    const int per = (n_bins + kThreads - 1) / kThreads;
-    const int b0 = min(n_bins, tid * per), b1 = min(n_bins, b0 + per);
-    int c = 0;
-    for (int b = b0; b < b1; ++b) c += bin_count(h, b) >= (uint32_t)min_nnz;
-    scan[tid] = c;
-    __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int t = 0; t < kThreads; ++t) {
-            const int v = scan[t];
-            scan[t] = run;
-            run += v;
-        }
-    }
-    __syncthreads();
-    // list kept bins; turn the histogram into a map bin -> local tile index (0xffff: not kept)
-    int loc = scan[tid];
-    const int base = tile_ptr[p];
-    uint16_t idx[64];
-    int ni = 0;
-    for (int b = b0; b < b1; ++b) {
-        const bool k = bin_count(h, b) >= (uint32_t)min_nnz;
-        if (k) tile_col[base + loc] = b;
-        if (ni < 64) idx[ni++] = k ? (uint16_t)loc : (uint16_t)0xffff;
-        loc += k;
-    }
-    __syncthreads();
-    uint16_t *map = reinterpret_cast<uint16_t *>(h);
-    for (int b = b0, i = 0; b < b1 && i < 64; ++b, ++i) map[b] = idx[i];
-    __syncthreads();
-    const int warp = tid >> 5, lane = tid & 31;
-    const int64_t r0 = (int64_t)p * kPanel;
-    for (int rr = warp; rr < kPanel && r0 + rr < N; rr += kThreads / 32) {
-        const int32_t b = indptr[r0 + rr], e = indptr[r0 + rr + 1];
-        int32_t out = r_indptr[r0 + rr];
-        for (int32_t x0 = b; x0 < e; x0 += 32) {
+// residual sources of every row, in CSR order (a warp per row)
+__global__ void res_fill_kernel(const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices, int64_t N,
+                                const uint8_t *__restrict__ res, const int32_t *__restrict__ r_indptr,
+                                int32_t *__restrict__ r_indices) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < N; i += nw) {
+        int32_t out = r_indptr[i];
+        const int32_t b = indptr[i], end = indptr[i + 1];
+        for (int32_t x0 = b; x0 < end; x0 += 32) {
             const int32_t x = x0 + lane;
-            const bool in = x < e;
-            const int32_t j = in ? indices[x] : 0;
-            const uint16_t t = in ? map[j / kWidth] : (uint16_t)0xffff;
-            if (in && t != 0xffff) {
-                const int64_t word = ((int64_t)(base + t) * kPanel + rr) >> 1;
-                const uint32_t bit = (1u << (j % kWidth)) << ((rr & 1) * 16);
-                if (atomicOr(&tile_bits32[word], bit) & bit) *dup = 1;   // a repeated edge
-            }
-            const unsigned res = __ballot_sync(SGA_FULL_MASK, in && t == 0xffff);
-            if (in && t == 0xffff) r_indices[out + __popc(res & ((1u << lane) - 1))] = j;
-            out += __popc(res);
+            const bool take = x < end && res[x];
+            const unsigned m = __ballot_sync(SGA_FULL_MASK, take);
+            if (take) r_indices[out + __popc(m & ((1u << lane) - 1))] = indices[x];
+            out += __popc(m);
         }
     }
+}
+
+// transposed masks for the column pass: word (t, half, c) holds in bit i
+// whether row 64 half + i of tile t has source c
+__global__ void tile_bits_t_kernel(const uint16_t *__restrict__ bits, int64_t n_tiles, uint64_t *__restrict__ bt) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n_tiles * 32; x += stride) {
+        const int64_t t = x >> 5;
+        const int hf = (int)(x >> 4) & 1, c = (int)x & 15;
+        const uint16_t *b = bits + t * kPanel + hf * 64;
+        uint64_t w = 0;
+        for (int i = 0; i < 64; ++i) w |= (uint64_t)((b[i] >> c) & 1u) << i;
+        bt[x] = w;
+    }
+}
+
+int bits_for(int64_t max_value) {
+    int b = 1;
+    while (b < 31 && ((int64_t)1 << b) <= max_value) ++b;
+    return b;
 }
 
 }  // namespace
 
 sga_status bsr_build(sga_plan *p, cudaStream_t s) {
     TileSet &T = p->tiles;
-    const int64_t N = p->N;
-    const int n_bins = (int)((N + kWidth - 1) / kWidth);
-    const size_t hist_bytes = (size_t)((n_bins + 1) / 2) * 4;
-    // the histogram and the per-thread bin ranges must fit (bins per thread <= 64)
-    if (hist_bytes > 200 * 1024 || (n_bins + kThreads - 1) / kThreads > 64) return SGA_EUNSUPPORTED;
+    const int64_t N = p->N, E = p->E;
     T.n_panels = (int32_t)((N + kPanel - 1) / kPanel);
     std::vector<void *> tmp;
     auto fail = [&](cudaError_t e) {
@@ -151,7 +198,7 @@ sga_status bsr_build(sga_plan *p, cudaStream_t s) {
         return SGA_ECUDA;
     };
     auto alloc = [&](void **ptr, size_t bytes, bool own) -> cudaError_t {
-        cudaError_t e = cudaMalloc(ptr, std::max<size_t>(bytes, 4));
+        cudaError_t e = cudaMalloc(ptr, std::max<size_t>(bytes, 16));
         if (e == cudaSuccess) {
             if (own) {
                 p->owned.push_back(*ptr);
@@ -162,71 +209,113 @@ sga_status bsr_build(sga_plan *p, cudaStream_t s) {
         }
         return e;
     };
-    int32_t *kept = nullptr, *scan_tmp = nullptr, *dup = nullptr;
-    cudaError_t e;
-    if ((e = alloc((void **)&kept, sizeof(int32_t) * (T.n_panels + 1), false)) != cudaSuccess) return fail(e);
-    if ((e = alloc((void **)&dup, sizeof(int32_t), false)) != cudaSuccess) return fail(e);
-    if ((e = alloc((void **)&T.tile_ptr, sizeof(int32_t) * (T.n_panels + 1), true)) != cudaSuccess) return fail(e);
-    if ((e = alloc((void **)&T.r_indptr, sizeof(int32_t) * (N + 1), true)) != cudaSuccess) return fail(e);
-    if ((e = alloc((void **)&scan_tmp, sizeof(int32_t) * scan_tmp_elems(std::max<int64_t>(N + 1, T.n_panels + 1)),
-                   false)) != cudaSuccess)
-        return fail(e);
-    if (hist_bytes > 48 * 1024) {
-        if ((e = cudaFuncSetAttribute(bsr_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)hist_bytes)) != cudaSuccess)
-            return fail(e);
-        if ((e = cudaFuncSetAttribute(bsr_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)hist_bytes)) != cudaSuccess)
-            return fail(e);
+#define BSR_TRY(x)                                   \
+    do {                                             \
+        const cudaError_t e_ = (x);                  \
+        if (e_ != cudaSuccess) return fail(e_);      \
+    } while (0)
+    const int64_t En = E + 1;   // run arrays hold up to E + 1 entries
+    int32_t *rows, *ka, *va, *kb, *vb, *head, *run_excl, *hist, *scan_tmp, *panel_count;
+    uint8_t *rep, *res;
+    BSR_TRY(alloc((void **)&rows, 4 * (size_t)En, false));
+    BSR_TRY(alloc((void **)&ka, 4 * (size_t)En, false));
+    BSR_TRY(alloc((void **)&va, 4 * (size_t)En, false));
+    BSR_TRY(alloc((void **)&kb, 4 * (size_t)En, false));
+    BSR_TRY(alloc((void **)&vb, 4 * (size_t)En, false));
+    BSR_TRY(alloc((void **)&head, 4 * (size_t)En, false));
+    BSR_TRY(alloc((void **)&run_excl, 4 * (size_t)En, false));
+    BSR_TRY(alloc((void **)&rep, (size_t)En, false));
+    BSR_TRY(alloc((void **)&res, (size_t)En, false));
+    BSR_TRY(alloc((void **)&panel_count, 4 * (size_t)(T.n_panels + 1), false));
+    const int64_t hist_n = radix_hist_elems(En);
+    BSR_TRY(alloc((void **)&hist, 4 * (size_t)hist_n, false));
+    BSR_TRY(alloc((void **)&scan_tmp,
+                  4 * (size_t)scan_tmp_elems(std::max<int64_t>({hist_n, En + 1, N + 1, (int64_t)T.n_panels + 1})),
+                  false));
+    BSR_TRY(alloc((void **)&T.tile_ptr, sizeof(int32_t) * (T.n_panels + 1), true));
+    BSR_TRY(alloc((void **)&T.r_indptr, sizeof(int32_t) * (N + 1), true));
+    BSR_TRY(cudaMemsetAsync(panel_count, 0, 4 * (size_t)(T.n_panels + 1), s));
+    BSR_TRY(cudaMemsetAsync(T.r_indptr, 0, 4 * (size_t)(N + 1), s));
+
+    // sort the edges by (panel, tile, row % 128, source % 16), ties in CSR order
+    int64_t n_runs = 0;
+    if (E > 0) {
+        edge_dst_kernel<<<grid_of(N * 32), 256, 0, s>>>(p->indptr, N, rows);
+        key_low_kernel<<<grid_of(E), 256, 0, s>>>(rows, p->indices, E, ka, va);
+        BSR_TRY(cudaGetLastError());
+        BSR_TRY(radix_sort_pairs(&ka, &va, &kb, &vb, E, 11, hist, scan_tmp, s));
+        key_gather_kernel<<<grid_of(E), 256, 0, s>>>(p->indices, 4, va, E, ka);
+        BSR_TRY(cudaGetLastError());
+        BSR_TRY(radix_sort_pairs(&ka, &va, &kb, &vb, E, bits_for((N - 1) >> 4), hist, scan_tmp, s));
+        key_gather_kernel<<<grid_of(E), 256, 0, s>>>(rows, 7, va, E, ka);
+        BSR_TRY(cudaGetLastError());
+        BSR_TRY(radix_sort_pairs(&ka, &va, &kb, &vb, E, bits_for((N - 1) >> 7), hist, scan_tmp, s));
+        run_flags_kernel<<<grid_of(E), 256, 0, s>>>(rows, p->indices, va, E, head, rep);
+        BSR_TRY(cudaGetLastError());
+        BSR_TRY(exclusive_scan(head, run_excl, E, scan_tmp, s));
+        int32_t last[2];
+        BSR_TRY(cudaMemcpyAsync(&last[0], run_excl + E - 1, 4, cudaMemcpyDeviceToHost, s));
+        BSR_TRY(cudaMemcpyAsync(&last[1], head + E - 1, 4, cudaMemcpyDeviceToHost, s));
+        BSR_TRY(cudaStreamSynchronize(s));
+        n_runs = (int64_t)last[0] + last[1];
     }
-    if ((e = cudaMemsetAsync(kept, 0, sizeof(int32_t) * (T.n_panels + 1), s)) != cudaSuccess) return fail(e);
-    if ((e = cudaMemsetAsync(dup, 0, sizeof(int32_t), s)) != cudaSuccess) return fail(e);
-    if ((e = cudaMemsetAsync(T.r_indptr, 0, sizeof(int32_t) * (N + 1), s)) != cudaSuccess) return fail(e);
-    if (T.n_panels > 0) {
-        bsr_count_kernel<<<T.n_panels, kThreads, hist_bytes, s>>>(p->indptr, p->indices, N, n_bins,
-                                                                  T.min_nnz, kept, T.r_indptr);
-        if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+    // runs -> kept tiles (kb: run starts, vb: keep flags then tile index of each run;
+    // both hold at most E + 1 entries)
+    int32_t *start = kb, *keep = vb, *tix = ka;
+    if (n_runs > 0) {
+        run_start_kernel<<<grid_of(E), 256, 0, s>>>(head, run_excl, E, start);
+        run_keep_kernel<<<grid_of(n_runs + 1), 256, 0, s>>>(start, n_runs, E, T.min_nnz, keep);
+        BSR_TRY(cudaGetLastError());
+        BSR_TRY(exclusive_scan(keep, tix, n_runs + 1, scan_tmp, s));
+        int32_t nt = 0;
+        BSR_TRY(cudaMemcpyAsync(&nt, tix + n_runs, 4, cudaMemcpyDeviceToHost, s));
+        BSR_TRY(cudaStreamSynchronize(s));
+        T.n_tiles = nt;
     }
-    if ((e = exclusive_scan(kept, T.tile_ptr, T.n_panels + 1, scan_tmp, s)) != cudaSuccess) return fail(e);
-    if ((e = exclusive_scan(T.r_indptr, T.r_indptr, N + 1, scan_tmp, s)) != cudaSuccess) return fail(e);
-    int32_t tot[2] = {0, 0};
-    if ((e = cudaMemcpyAsync(&tot[0], T.tile_ptr + T.n_panels, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        return fail(e);
-    if ((e = cudaMemcpyAsync(&tot[1], T.r_indptr + N, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
-        return fail(e);
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(e);
-    T.n_tiles = tot[0];
-    T.E_res = tot[1];
-    if ((e = alloc((void **)&T.tile_col, sizeof(int32_t) * (size_t)T.n_tiles, true)) != cudaSuccess) return fail(e);
-    if ((e = alloc((void **)&T.tile_bits, sizeof(uint16_t) * kPanel * (size_t)T.n_tiles, true)) != cudaSuccess)
-        return fail(e);
-    if ((e = alloc((void **)&T.r_indices, sizeof(int32_t) * (size_t)T.E_res, true)) != cudaSuccess) return fail(e);
-    if (T.n_tiles > 0 &&
-        (e = cudaMemsetAsync(T.tile_bits, 0, sizeof(uint16_t) * kPanel * (size_t)T.n_tiles, s)) != cudaSuccess)
-        return fail(e);
-    if (T.n_panels > 0) {
-        bsr_fill_kernel<<<T.n_panels, kThreads, hist_bytes, s>>>(
-            p->indptr, p->indices, N, n_bins, T.min_nnz, T.tile_ptr, T.tile_col,
-            reinterpret_cast<uint32_t *>(T.tile_bits), T.r_indptr, T.r_indices, dup);
-        if ((e = cudaGetLastError()) != cudaSuccess) return fail(e);
+    // one extra all-zero mask tile (index n_tiles) stands in for missing tiles
+    BSR_TRY(alloc((void **)&T.tile_col, sizeof(int32_t) * (size_t)T.n_tiles, true));
+    BSR_TRY(alloc((void **)&T.tile_bits, sizeof(uint16_t) * kPanel * (size_t)(T.n_tiles + 1), true));
+    BSR_TRY(cudaMemsetAsync(T.tile_bits, 0, sizeof(uint16_t) * kPanel * (size_t)(T.n_tiles + 1), s));
+    BSR_TRY(alloc((void **)&T.tile_bits_t, sizeof(uint64_t) * 32 * (size_t)(T.n_tiles + 1), true));
+    BSR_TRY(cudaMemsetAsync(T.tile_bits_t, 0, sizeof(uint64_t) * 32 * (size_t)(T.n_tiles + 1), s));
+    if (n_runs > 0) {
+        tile_info_kernel<<<grid_of(n_runs), 256, 0, s>>>(start, keep, tix, n_runs, va, rows, p->indices,
+                                                          T.tile_col, panel_count);
+        tile_bits_kernel<<<grid_of(E), 256, 0, s>>>(head, run_excl, rep, keep, tix, va, rows, p->indices, E,
+                                                    reinterpret_cast<uint32_t *>(T.tile_bits), res);
+        BSR_TRY(cudaGetLastError());
     }
-    int32_t repeated = 0;
-    if ((e = cudaMemcpyAsync(&repeated, dup, 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fail(e);
-    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return fail(e);
+    if (T.n_tiles > 0) {
+        tile_bits_t_kernel<<<grid_of((int64_t)T.n_tiles * 32), 256, 0, s>>>(T.tile_bits, T.n_tiles, T.tile_bits_t);
+        BSR_TRY(cudaGetLastError());
+    }
+    BSR_TRY(exclusive_scan(panel_count, T.tile_ptr, T.n_panels + 1, scan_tmp, s));
+    if (E > 0) {
+        res_count_kernel<<<grid_of(N * 32), 256, 0, s>>>(p->indptr, N, res, T.r_indptr);
+        BSR_TRY(cudaGetLastError());
+    }
+    BSR_TRY(exclusive_scan(T.r_indptr, T.r_indptr, N + 1, scan_tmp, s));
+    int32_t e_res = 0;
+    BSR_TRY(cudaMemcpyAsync(&e_res, T.r_indptr + N, 4, cudaMemcpyDeviceToHost, s));
+    BSR_TRY(cudaStreamSynchronize(s));
+    T.E_res = e_res;
+    BSR_TRY(alloc((void **)&T.r_indices, sizeof(int32_t) * (size_t)T.E_res, true));
+    if (T.E_res > 0) {
+        res_fill_kernel<<<grid_of(N * 32), 256, 0, s>>>(p->indptr, p->indices, N, res, T.r_indptr, T.r_indices);
+        BSR_TRY(cudaGetLastError());
+    }
+    BSR_TRY(cudaStreamSynchronize(s));
     for (void *x : tmp) cudaFree(x);
     tmp.clear();
-    // a tile mask holds an edge once: repeated edges inside kept tiles cannot be represented
-    if (repeated) return SGA_EINVAL;
 
     // column view (host, O(tiles)): entries (row panel, column panel of 8 tile
-    // columns) in column-panel order, row panels ascending within each
+    // columns) in column-panel order, row panels ascending within each; and
+    // the order in which the persistent kernels take panels: by descending
+    // work (kept tiles, entries), ties by index, panels without work left out
     std::vector<int32_t> h_ptr(T.n_panels + 1), h_col(T.n_tiles);
-    if ((e = cudaMemcpy(h_ptr.data(), T.tile_ptr, sizeof(int32_t) * (T.n_panels + 1), cudaMemcpyDeviceToHost)) !=
-        cudaSuccess)
-        return fail(e);
-    if (T.n_tiles > 0 &&
-        (e = cudaMemcpy(h_col.data(), T.tile_col, sizeof(int32_t) * T.n_tiles, cudaMemcpyDeviceToHost)) != cudaSuccess)
-        return fail(e);
+    BSR_TRY(cudaMemcpy(h_ptr.data(), T.tile_ptr, sizeof(int32_t) * (T.n_panels + 1), cudaMemcpyDeviceToHost));
+    if (T.n_tiles > 0)
+        BSR_TRY(cudaMemcpy(h_col.data(), T.tile_col, sizeof(int32_t) * T.n_tiles, cudaMemcpyDeviceToHost));
     T.n_cpanels = T.n_panels;   // 128 sources per column panel, N sources
     std::vector<int32_t> c_ptr(T.n_cpanels + 1, 0);
     for (int32_t pn = 0; pn < T.n_panels; ++pn)
@@ -246,21 +335,33 @@ sga_status bsr_build(sga_plan *p, cudaStream_t s) {
             c_tile[(size_t)cur * 8 + h_col[t] % 8] = t;
         }
     }
-    if ((e = alloc((void **)&T.ct_ptr, sizeof(int32_t) * (T.n_cpanels + 1), true)) != cudaSuccess) return fail(e);
-    if ((e = alloc((void **)&T.ct_panel, sizeof(int32_t) * T.n_entries, true)) != cudaSuccess) return fail(e);
-    if ((e = alloc((void **)&T.ct_tile, sizeof(int32_t) * 8 * (size_t)T.n_entries, true)) != cudaSuccess)
-        return fail(e);
-    if ((e = cudaMemcpy(T.ct_ptr, c_ptr.data(), sizeof(int32_t) * (T.n_cpanels + 1), cudaMemcpyHostToDevice)) !=
-        cudaSuccess)
-        return fail(e);
+    auto work_order = [](const std::vector<int32_t> &ptr) {
+        std::vector<int32_t> o;
+        for (int32_t i = 0; i + 1 < (int32_t)ptr.size(); ++i)
+            if (ptr[i + 1] > ptr[i]) o.push_back(i);
+        std::stable_sort(o.begin(), o.end(),
+                         [&](int32_t a, int32_t b) { return ptr[a + 1] - ptr[a] > ptr[b + 1] - ptr[b]; });
+        return o;
+    };
+    const std::vector<int32_t> p_order = work_order(h_ptr), c_order = work_order(c_ptr);
+    T.n_active = (int32_t)p_order.size();
+    T.n_cactive = (int32_t)c_order.size();
+    BSR_TRY(alloc((void **)&T.ct_ptr, sizeof(int32_t) * (T.n_cpanels + 1), true));
+    BSR_TRY(alloc((void **)&T.ct_panel, sizeof(int32_t) * T.n_entries, true));
+    BSR_TRY(alloc((void **)&T.ct_tile, sizeof(int32_t) * 8 * (size_t)T.n_entries, true));
+    BSR_TRY(alloc((void **)&T.panel_order, sizeof(int32_t) * T.n_active, true));
+    BSR_TRY(alloc((void **)&T.cpanel_order, sizeof(int32_t) * T.n_cactive, true));
+    BSR_TRY(cudaMemcpy(T.ct_ptr, c_ptr.data(), sizeof(int32_t) * (T.n_cpanels + 1), cudaMemcpyHostToDevice));
     if (T.n_entries > 0) {
-        if ((e = cudaMemcpy(T.ct_panel, c_panel.data(), sizeof(int32_t) * T.n_entries, cudaMemcpyHostToDevice)) !=
-            cudaSuccess)
-            return fail(e);
-        if ((e = cudaMemcpy(T.ct_tile, c_tile.data(), sizeof(int32_t) * 8 * (size_t)T.n_entries,
-                            cudaMemcpyHostToDevice)) != cudaSuccess)
-            return fail(e);
+        BSR_TRY(cudaMemcpy(T.ct_panel, c_panel.data(), sizeof(int32_t) * T.n_entries, cudaMemcpyHostToDevice));
+        BSR_TRY(cudaMemcpy(T.ct_tile, c_tile.data(), sizeof(int32_t) * 8 * (size_t)T.n_entries,
+                           cudaMemcpyHostToDevice));
     }
+    if (T.n_active > 0)
+        BSR_TRY(cudaMemcpy(T.panel_order, p_order.data(), sizeof(int32_t) * T.n_active, cudaMemcpyHostToDevice));
+    if (T.n_cactive > 0)
+        BSR_TRY(cudaMemcpy(T.cpanel_order, c_order.data(), sizeof(int32_t) * T.n_cactive, cudaMemcpyHostToDevice));
+#undef BSR_TRY
     return SGA_OK;
 }
 

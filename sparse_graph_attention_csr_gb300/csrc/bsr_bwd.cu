@@ -10,64 +10,44 @@
 // dK/dV passes here use): the Delta pass returns the tile parts of
 // sum p dP and of Z.
 //
-// Three passes, each one CTA of 4 warps per (panel, head); all products on
-// the tensor cores with fp32 accumulators in TMEM:
-//   Delta pass (per row panel, groups of four kept tiles = 64 sources):
-//     S = Q K^T, dP = dOut V^T, the row sums of p dP and of p over tile edges;
+// Three passes, each a persistent kernel (one CTA per SM) with the same
+// roles as the forward: warp 0 one lane issues TMA loads into a ring of
+// stages, warp 1 one lane issues the MMAs (fp32 accumulators in TMEM), warps
+// 2-5 (thread = TMEM lane) turn the products into weights and gradients;
+// every handoff is an mbarrier and every wait is bounded.
+//   Delta pass (units: row panel x head, groups of four kept tiles = 64
+//     sources): S = Q K^T, dP = dOut V^T into two TMEM buffers (the next
+//     group's products run while the current one is reduced); the row sums
+//     of p dP and of p over tile edges;
 //   dQ pass (same loop, Delta known): dS to shared memory as a pair of bf16
 //     tiles (hi = bf16(dS), lo = bf16(dS - hi): about 16 significant bits),
-//     dQ += dS_hi K + dS_lo K;
-//   dK/dV pass (per column panel of 128 sources, over the row panels that
-//     keep one of its tiles, 64 rows at a time):
+//     dQ += dS_hi K + dS_lo K in TMEM, issued after the next group's S and dP;
+//   dK/dV pass (units: column panel of 128 sources x head, over the row
+//     panels that keep one of its tiles, 64 rows at a time):
 //     S^T = K Q^T, dP^T = V dOut^T, P^T and the dS^T pair to shared memory,
 //     dV += P^T dOut, dK += dS^T_hi Q + dS^T_lo Q.
 // dS is split because it cancels: a row's dS sum to zero, so a single bf16
 // rounding of every term (2^-9 relative) leaves dQ and dK errors of 2^-9 times
 // the sum of |dS k| terms, which is far larger than the result where scores
 // or dP are large.  P (non-negative) and the node rows stay single bf16.
-// Node rows are staged once, 128-byte swizzled with 64-wide column atoms: the
-// K-major operand over D of the S and dP products, and as they stand the
+// Node rows are staged by TMA, 128-byte swizzled with 64-wide column atoms:
+// the K-major operand over D of the S and dP products, and as they stand the
 // MN-major operand over D of the dQ, dV and dK products (no transposes).
 // The residual CSR passes run in between (their Delta includes the tile part), so
 // each pass here adds its tile part to gradients already stored.  No atomics:
-// every output row is owned by one CTA, and the results are deterministic.
+// every output row is owned by one unit, and the results are deterministic.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "plan.h"
 #include "tc.cuh"
+#include "tc_dx.cuh"
 
 namespace sga {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;
 constexpr int kGroup = 64;   // sources per group of the row passes (four tiles)
-
-// Rows row0 .. row0 + R - 1 of head h of a [N, H, D] bf16 tensor into a
-// swizzled K-major tile of R rows (zero rows past N).
-template <int D>
-__device__ __forceinline__ void load_rows(uint32_t dst, const __nv_bfloat16 *X, int64_t row0, int R,
-                                          int64_t N, int H, int h) {
-    constexpr int DC = D / 8;
-    for (int idx = threadIdx.x; idx < R * DC; idx += kThreads) {
-        const int rr = idx / DC, c = idx % DC;
-        const bool ok = row0 + rr < N;
-        tc::cp16(dst + tc::sw128_offset(rr, c * 8, R), ok ? X + ((row0 + rr) * H + h) * D + c * 8 : X, ok);
-    }
-}
-
-// The 64 source rows of kept tiles t .. t + 3 (rows of missing tiles and
-// sources past N are zero).
-template <int D>
-__device__ __forceinline__ void load_tile_rows(uint32_t dst, const __nv_bfloat16 *X, const int32_t *tile_col,
-                                               int32_t t, int32_t t_end, int64_t N, int H, int h) {
-    constexpr int DC = D / 8;
-    for (int idx = threadIdx.x; idx < kGroup * DC; idx += kThreads) {
-        const int jr = idx / DC, c = idx % DC;
-        const int32_t ti = t + jr / 16;
-        const int64_t j = ti < t_end ? (int64_t)tile_col[ti] * 16 + (jr % 16) : -1;
-        const bool ok = j >= 0 && j < N;
-        tc::cp16(dst + tc::sw128_offset(jr, c * 8, kGroup), ok ? X + (j * H + h) * D + c * 8 : X, ok);
-    }
-}
 
 // Four k-steps over 64 node rows (K = 64): A K-major (one 64-wide atom of the
 // A tile), B the 64 node rows x N columns as an MN-major operand.
@@ -99,408 +79,651 @@ __device__ __forceinline__ void split_bf16x8(const float *x, uint4 &hi, uint4 &l
     lo = pack<__nv_bfloat16>(r);
 }
 
-// Add an fp32 row (from TMEM, times `scale`) to a bf16 row of D values.
+// Add an fp32 row (from TMEM, times `scale`) to a bf16 row of D values: the
+// row's current values are loaded first, all at once (one round trip).
 template <int D>
 __device__ __forceinline__ void add_row_from_tmem(uint32_t taddr, __nv_bfloat16 *dst, float scale, bool has) {
+    uint4 x[D / 8];
+    if (has)
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) x[c] = *reinterpret_cast<const uint4 *>(dst + 8 * c);
+#pragma unroll
     for (int cb = 0; cb < D; cb += 32) {
         uint32_t u[32];
         tc::tmem_ld32(taddr + cb, u);   // warp-collective: every lane takes part
         if (!has) continue;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            float o[8], x[8];
-            unpack<__nv_bfloat16>(*reinterpret_cast<const uint4 *>(dst + cb + 8 * q), x);
+            float o[8], y[8];
+            unpack<__nv_bfloat16>(x[cb / 8 + q], y);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = x[i] + scale * __uint_as_float(u[8 * q + i]);
+            for (int i = 0; i < 8; ++i) o[i] = y[i] + scale * __uint_as_float(u[8 * q + i]);
             *reinterpret_cast<uint4 *>(dst + cb + 8 * q) = pack<__nv_bfloat16>(o);
         }
     }
 }
 
+// L2 prefetch of a bf16 row of D values (read again at the end of the unit).
+template <int D> __device__ __forceinline__ void prefetch_row(const __nv_bfloat16 *row) {
+#pragma unroll
+    for (int b = 0; b < D * 2; b += 128) tc::prefetch_l2(reinterpret_cast<const char *>(row) + b);
+}
+
 // ------------------------------------------------------------ row passes
 
-// The Delta pass keeps one K/V buffer (the next group loads once the S and dP
-// products have consumed it), so that two of its CTAs share an SM; the dQ
-// pass, above half an SM's shared memory either way, keeps two.
-__host__ __device__ constexpr int row_buffers(int mode) { return mode == 0 ? 1 : 2; }
+template <int D, int MODE> struct RowCfg {
+    static constexpr int DA = D / 64;
+    static constexpr uint32_t PB = DA * 128 * 128;       // a 128-row panel tile (Q or dOut)
+    static constexpr uint32_t KB = DA * kGroup * 128;    // K or V rows of a group
+    // panel buffers (two: the next unit's panel loads during this one) and
+    // K/V stages, within the shared memory of one SM
+    static constexpr int NQ = (D == 64 || MODE == 0) ? 2 : 1;
+    static constexpr int NST = D == 64 ? 3 : (MODE == 0 ? 2 : 3);
+    static constexpr uint32_t Q0 = 0;                    // buffer b: Q, then dOut
+    static constexpr uint32_t ST0 = Q0 + NQ * 2 * PB;    // stage s: K, then V
+    static constexpr uint32_t DS0 = ST0 + NST * 2 * KB;  // dQ pass: dS hi, dS lo (128 x 64 bf16 each)
+    static constexpr uint32_t BYTES = DS0 + (MODE == 1 ? 2 * 128 * 128 : 0);
+    static constexpr uint32_t TCOLS = MODE == 1 ? 512 : 256;   // S, dP (x2), dQ
+};
 
-struct RowLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t q, g, k[2], v[2], ds, ds_lo, total;
-    __host__ __device__ RowLayout(int D, int mode) {
-        const uint32_t DA = (uint32_t)D / 64, NB = (uint32_t)row_buffers(mode);
-        q = 0;
-        g = q + DA * 128 * 128;
-        k[0] = g + DA * 128 * 128;
-        k[1] = k[0] + (NB - 1) * DA * kGroup * 128;
-        v[0] = k[1] + DA * kGroup * 128;
-        v[1] = v[0] + (NB - 1) * DA * kGroup * 128;
-        ds = v[1] + DA * kGroup * 128;
-        ds_lo = ds + (mode == 1 ? 128 * 128 : 0);
-        total = ds_lo + (mode == 1 ? 128 * 128 : 0);
-    }
+struct RowParams {
+    CUtensorMap tq, tg, tk, tv;   // [N][H*D] bf16: Q, dOut boxes 64 x 128; K, V boxes 64 x 16
+    BsrBwdArgs a;
 };
 
 // MODE 0: Delta pass (writes delta_t, z_t).  MODE 1: dQ pass (adds to dQ).
 template <int D, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(BsrBwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_constant__ RowParams prm) {
+    using C = RowCfg<D, MODE>;
+    const BsrBwdArgs &a = prm.a;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t mbar_s, mbar_o;
+    __shared__ uint64_t q_full[2], q_empty[2], kv_full[C::NST], kv_empty[C::NST], s_full[2], s_empty[2], ds_full,
+        ds_empty, acc_empty, mma_done;
     __shared__ uint32_t tmem_base;
-    const RowLayout L(D, MODE);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int panel = blockIdx.x, h = blockIdx.y, H = a.H;
-    const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
-    const int ng = (t1 - t0 + 3) / 4;
-    if (ng == 0) return;   // whole CTA: no kept tile
-
-    const int64_t r0 = (int64_t)panel * 128, row = r0 + tid;
-    const bool in = row < a.N;
-    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.Q);
-    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(a.K);
-    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(a.V);
-    const __nv_bfloat16 *G = static_cast<const __nv_bfloat16 *>(a.dOut);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = tc::smem_u32(smem);
+    const int H = a.H;
+    const int64_t n_units = (int64_t)a.n_active * H;
 
-    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
-    if (tid == 0) {
-        tc::mbar_init(&mbar_s, 1);
-        tc::mbar_init(&mbar_o, 1);
-    }
-    load_rows<D>(sbase + L.q, Q, r0, 128, a.N, H, h);
-    load_rows<D>(sbase + L.g, G, r0, 128, a.N, H, h);
-    load_tile_rows<D>(sbase + L.k[0], K, a.tile_col, t0, t1, a.N, H, h);
-    load_tile_rows<D>(sbase + L.v[0], V, a.tile_col, t0, t1, a.N, H, h);
-    tc::cp_commit();
-    // the Delta pass uses the forward's lse and sums C and Z of its tile edges;
-    // the dQ pass uses the normalised lse + ln Z and Delta = C / Z of the row
-    const float lse2 = in ? (MODE == 0 ? a.lse : a.lse_n)[row * H + h] * kLog2e : 0.f;
-    const float dl = (MODE == 1 && in) ? a.delta[row * H + h] : 0.f;
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tS = tmem_base, tP = tmem_base + 64, tQ = tmem_base + 128;
-    const uint32_t tlane = (uint32_t)(warp * 32) << 16;
-    const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_q = tc::idesc_bf16(128, D) | tc::kMajorMnB;
-    const float scale2 = kLog2e * rsqrtf((float)D);
-
-    float dsum = 0.f, zsum = 0.f;
-    bool failed = false;
-    int n_o = 0;   // dQ products issued (uniform over the CTA)
-    constexpr int NB = row_buffers(MODE);
-    for (int g = 0; g < ng; ++g) {
-        const int b = NB == 2 ? (g & 1) : 0;
-        // the previous dS K product reads dS and the other K buffer: it must be done first
-        if (MODE == 1 && g > 0 && !tc::mbar_wait(&mbar_o, (g - 1) & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
-        if (NB == 2 && g + 1 < ng) {
-            load_tile_rows<D>(sbase + L.k[b ^ 1], K, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
-            load_tile_rows<D>(sbase + L.v[b ^ 1], V, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
-            tc::cp_commit();
-            tc::cp_wait<1>();
-        } else {
-            tc::cp_wait<0>();
+    if (warp == 0) tc::tmem_alloc(&tmem_base, C::TCOLS);
+    if (tid == 32) {
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&q_full[i], 1);
+            tc::mbar_init(&q_empty[i], 1);
+            tc::mbar_init(&s_full[i], 1);
+            tc::mbar_init(&s_empty[i], 4);
         }
-        tc::fence_after_sync();
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {   // S = Q K^T, dP = dOut V^T
-            tc::fence_after_sync();
-            mma_over_d(tS, sbase + L.q, sbase + L.k[b], kGroup, D, idesc_s);
-            mma_over_d(tP, sbase + L.g, sbase + L.v[b], kGroup, D, idesc_s);
-            tc::mma_commit(&mbar_s);
+        for (int i = 0; i < C::NST; ++i) {
+            tc::mbar_init(&kv_full[i], 1);
+            tc::mbar_init(&kv_empty[i], 1);
         }
-        if (!tc::mbar_wait(&mbar_s, g & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
-        tc::fence_after_sync();
-        if (NB == 1 && g + 1 < ng) {   // K and V consumed: the next group loads during the softmax
-            load_tile_rows<D>(sbase + L.k[0], K, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
-            load_tile_rows<D>(sbase + L.v[0], V, a.tile_col, t0 + 4 * (g + 1), t1, a.N, H, h);
-            tc::cp_commit();
-        }
-
-        uint32_t bits[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int32_t ti = t0 + 4 * g + q;
-            bits[q] = (ti < t1 && in) ? a.tile_bits[(size_t)ti * 128 + tid] : 0u;
-        }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t us[32], up[32];
-            tc::tmem_ld32(tS + tlane + half * 32, us);
-            tc::tmem_ld32(tP + tlane + half * 32, up);
-            float ds[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int c = half * 32 + i;
-                const bool on = (bits[c >> 4] >> (c & 15)) & 1u;
-                const float p = on ? exp2f(__uint_as_float(us[i]) * scale2 - lse2) : 0.f;
-                const float dp = __uint_as_float(up[i]);
-                if (MODE == 0) {
-                    dsum = fmaf(p, dp, dsum);
-                    zsum += p;
-                }
-                ds[i] = p * (dp - dl);
-            }
-            if (MODE == 1) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t o = tc::sw128_offset(tid, half * 32 + c * 8, 128);
-                    uint4 hi, lo;
-                    split_bf16x8(ds + 8 * c, hi, lo);
-                    *reinterpret_cast<uint4 *>(smem + L.ds + o) = hi;
-                    *reinterpret_cast<uint4 *>(smem + L.ds_lo + o) = lo;
-                }
-            }
-        }
-        tc::fence_before_sync();
-        if (MODE == 1) {
-            tc::fence_proxy_async();
-            __syncthreads();
-            if (tid == 0) {   // dQ += dS_hi K + dS_lo K
-                tc::fence_after_sync();
-                mma_rows64(tQ, sbase + L.ds, sbase + L.k[b], idesc_q, g == 0);
-                mma_rows64(tQ, sbase + L.ds_lo, sbase + L.k[b], idesc_q, false);
-                tc::mma_commit(&mbar_o);
-            }
-            ++n_o;
-        }
-    }
-    tc::cp_wait<0>();
-    if (MODE == 1 && !failed && !tc::mbar_wait(&mbar_o, (ng - 1) & 1, tc::kWaitLimit)) failed = true;
-    failed = __syncthreads_or(failed);
-    if (failed) {
-        if (tid == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
-        if (MODE == 1 && n_o > 0) tc::mbar_wait(&mbar_o, (n_o - 1) & 1, tc::kWaitLimit);
-    } else if (MODE == 0) {
-        if (in) {
-            a.delta_t[row * H + h] = dsum;
-            a.z_t[row * H + h] = zsum;
-        }
-    } else {
-        tc::fence_after_sync();
-        __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dQ) + (row * H + h) * D;
-        add_row_from_tmem<D>(tQ + tlane, dq, rsqrtf((float)D), in);
+        tc::mbar_init(&ds_full, 4);
+        tc::mbar_init(&ds_empty, 1);
+        tc::mbar_init(&acc_empty, 4);
+        tc::mbar_init(&mma_done, 1);
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+    tc::fence_after_sync();
+    // TMEM: S and dP of buffer sb at 128 sb, 128 sb + 64; the dQ accumulator at 256
+    const uint32_t tbase = tmem_base, tQ = tmem_base + 256;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ------------------------------------------------ TMA producer
+            int64_t G = 0, U = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+                const int32_t panel = a.panel_order[u / H];
+                const int h = (int)(u % H);
+                const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
+                const int ng = (t1 - t0 + 3) / 4;
+                const int qb = (int)(U % C::NQ);
+                const int64_t nq = U / C::NQ;
+                if (nq >= 1 && !tc::mbar_wait(&q_empty[qb], (nq - 1) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t qd = sbase + C::Q0 + qb * 2 * C::PB;
+                tc::mbar_expect_tx(&q_full[qb], 2 * C::PB);
+                for (int at = 0; at < C::DA; ++at) {
+                    tc::tma_load_2d(qd + at * 128 * 128, &prm.tq, h * D + at * 64, panel * 128, &q_full[qb]);
+                    tc::tma_load_2d(qd + C::PB + at * 128 * 128, &prm.tg, h * D + at * 64, panel * 128, &q_full[qb]);
+                }
+                for (int g = 0; g < ng; ++g, ++G) {
+                    const int s = (int)(G % C::NST);
+                    const int64_t n = G / C::NST;
+                    if (n >= 1 && !tc::mbar_wait(&kv_empty[s], (n - 1) & 1, tc::kWaitLimit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + C::ST0 + s * 2 * C::KB;
+                    tc::mbar_expect_tx(&kv_full[s], 2 * C::KB);
+                    for (int q = 0; q < 4; ++q) {
+                        const int32_t ti = t0 + 4 * g + q;
+                        const int y = ti < t1 ? a.tile_col[ti] * 16 : (int)a.N;   // past N: zero rows
+                        for (int at = 0; at < C::DA; ++at) {
+                            const uint32_t off = at * kGroup * 128 + q * 16 * 128;
+                            tc::tma_load_2d(st + off, &prm.tk, h * D + at * 64, y, &kv_full[s]);
+                            tc::tma_load_2d(st + C::KB + off, &prm.tv, h * D + at * 64, y, &kv_full[s]);
+                        }
+                    }
+                }
+            }
+            if (!ok) atomicOr(a.d_err, tc::kErrMmaTimeout);
+            // loads that no MMA consumed (only after a timeout) land before the CTA ends
+            for (int64_t i = G - 1; i >= 0 && i >= G - C::NST; --i)
+                tc::mbar_wait(&kv_full[i % C::NST], (i / C::NST) & 1, tc::kWaitLimit);
+            for (int64_t i = U - 1; i >= 0 && i >= U - C::NQ; --i)
+                tc::mbar_wait(&q_full[i % C::NQ], (i / C::NQ) & 1, tc::kWaitLimit);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ------------------------------------------------ MMA issuer
+            const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_q = tc::idesc_bf16(128, D) | tc::kMajorMnB;
+            int64_t G = 0, U = 0;
+            bool ok = true;
+            // dQ += dS_hi K + dS_lo K of group Gp; the first of unit Up
+            // overwrites dQ once the previous unit's epilogue has read it
+            auto issue_dq = [&](int64_t Gp, bool first, int64_t Up) -> bool {
+                if (!tc::mbar_wait(&ds_full, Gp & 1, tc::kWaitLimit)) return false;
+                if (first && Up >= 1 && !tc::mbar_wait(&acc_empty, (Up - 1) & 1, tc::kWaitLimit)) return false;
+                tc::fence_after_sync();
+                const int s = (int)(Gp % C::NST);
+                const uint32_t kr = sbase + C::ST0 + s * 2 * C::KB;
+                mma_rows64(tQ, sbase + C::DS0, kr, idesc_q, first);
+                mma_rows64(tQ, sbase + C::DS0 + 128 * 128, kr, idesc_q, false);
+                tc::mma_commit(&kv_empty[s]);
+                tc::mma_commit(&ds_empty);
+                return true;
+            };
+            int64_t pend = -1, pend_u = 0;
+            bool pend_first = false;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+                const int32_t panel = a.panel_order[u / H];
+                const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
+                const int ng = (t1 - t0 + 3) / 4;
+                const int qb = (int)(U % C::NQ);
+                if (!tc::mbar_wait(&q_full[qb], (U / C::NQ) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t qa = sbase + C::Q0 + qb * 2 * C::PB;
+                for (int g = 0; g < ng; ++g, ++G) {
+                    const int s = (int)(G % C::NST), sb = (int)(G & 1);
+                    if (!tc::mbar_wait(&kv_full[s], (G / C::NST) & 1, tc::kWaitLimit) ||
+                        (G >= 2 && !tc::mbar_wait(&s_empty[sb], ((G >> 1) - 1) & 1, tc::kWaitLimit))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t st = sbase + C::ST0 + s * 2 * C::KB;
+                    mma_over_d(tbase + sb * 128, qa, st, kGroup, D, idesc_s);                   // S = Q K^T
+                    mma_over_d(tbase + sb * 128 + 64, qa + C::PB, st + C::KB, kGroup, D, idesc_s);   // dP = dOut V^T
+                    tc::mma_commit(&s_full[sb]);
+                    if (MODE == 0) tc::mma_commit(&kv_empty[s]);   // the Delta pass is done with K and V
+                    if (g == ng - 1) tc::mma_commit(&q_empty[qb]);
+                    if (MODE == 1) {
+                        if (pend >= 0 && !issue_dq(pend, pend_first, pend_u)) {
+                            ok = false;
+                            break;
+                        }
+                        pend = G;
+                        pend_first = g == 0;
+                        pend_u = U;
+                    }
+                }
+            }
+            if (MODE == 1 && ok && pend >= 0 && !issue_dq(pend, pend_first, pend_u)) ok = false;
+            if (!ok) atomicOr(a.d_err, tc::kErrMmaTimeout);
+            tc::mma_commit(&mma_done);   // every product issued is complete before TMEM is released
+            tc::mbar_wait(&mma_done, 0, tc::kWaitLimit);
+        }
+    } else {   // ---------------------------------------------------- weights and gradients
+        const int quarter = warp & 3, r = quarter * 32 + lane;
+        const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
+        const float scale2 = kLog2e * rsqrtf((float)D);
+        int64_t G = 0, U = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+            const int32_t panel = a.panel_order[u / H];
+            const int h = (int)(u % H);
+            const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
+            const int ng = (t1 - t0 + 3) / 4;
+            const int64_t row = (int64_t)panel * 128 + r;
+            const bool in = row < a.N;
+            // the Delta pass uses the forward's lse and sums C and Z of its tile edges;
+            // the dQ pass uses the normalised lse + ln Z and Delta = C / Z of the row
+            const float lse2 = in ? (MODE == 0 ? a.lse : a.lse_n)[row * H + h] * kLog2e : 0.f;
+            const float dl = (MODE == 1 && in) ? a.delta[row * H + h] : 0.f;
+            if (MODE == 1 && in) prefetch_row<D>(static_cast<const __nv_bfloat16 *>(a.dQ) + (row * H + h) * D);
+            float dsum = 0.f, zsum = 0.f;
+            for (int g = 0; g < ng; ++g, ++G) {
+                const int sb = (int)(G & 1);
+                uint32_t bits[4];   // this row's source masks of the group (zero tile for missing ones)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int32_t ti = t0 + 4 * g + q;
+                    bits[q] = a.tile_bits[(size_t)(ti < t1 ? ti : a.n_tiles) * 128 + r];
+                }
+                if (!tc::warp_wait(&s_full[sb], (G >> 1) & 1, tc::kWaitLimit) ||
+                    (MODE == 1 && G >= 1 && !tc::warp_wait(&ds_empty, (G - 1) & 1, tc::kWaitLimit))) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t us[32], up[32];
+                    tc::tmem_ld32(tbase + sb * 128 + tlane + half * 32, us);
+                    tc::tmem_ld32(tbase + sb * 128 + 64 + tlane + half * 32, up);
+                    float ds[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = half * 32 + i;
+                        const bool on = (bits[c >> 4] >> (c & 15)) & 1u;
+                        const float p = on ? exp2f(__uint_as_float(us[i]) * scale2 - lse2) : 0.f;
+                        const float dp = __uint_as_float(up[i]);
+                        if (MODE == 0) {
+                            dsum = fmaf(p, dp, dsum);
+                            zsum += p;
+                        }
+                        ds[i] = p * (dp - dl);
+                    }
+                    if (MODE == 1) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t o = tc::sw128_offset(r, half * 32 + c * 8, 128);
+                            uint4 hi, lo;
+                            split_bf16x8(ds + 8 * c, hi, lo);
+                            *reinterpret_cast<uint4 *>(smem + C::DS0 + o) = hi;
+                            *reinterpret_cast<uint4 *>(smem + C::DS0 + 128 * 128 + o) = lo;
+                        }
+                    }
+                }
+                tc::fence_before_sync();
+                if (MODE == 1) tc::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&s_empty[sb]);
+                    if (MODE == 1) tc::mbar_arrive(&ds_full);
+                }
+            }
+            if (!ok) break;
+            if (MODE == 0) {
+                if (in) {
+                    a.delta_t[row * H + h] = dsum;
+                    a.z_t[row * H + h] = zsum;
+                }
+            } else {
+                // the unit's last dQ product, then add the tile part to dQ
+                if (!tc::warp_wait(&ds_empty, (G - 1) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dQ) + ((in ? row : 0) * H + h) * D;
+                add_row_from_tmem<D>(tQ + tlane, dq, rsqrtf((float)D), in);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&acc_empty);
+            }
+        }
+        if (!ok && lane == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_dealloc(tmem_base, C::TCOLS);
+    }
 }
 
 // ----------------------------------------------------------- column pass
 
-struct ColLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t kc, vc, qh[2], gh[2], p, ds, ds_lo, bits[2], lse[2], dl[2], total;
-    __host__ __device__ ColLayout(int D) {
-        const uint32_t DA = (uint32_t)D / 64;
-        kc = 0;
-        vc = kc + DA * 128 * 128;
-        qh[0] = vc + DA * 128 * 128;
-        qh[1] = qh[0] + DA * 64 * 128;
-        gh[0] = qh[1] + DA * 64 * 128;
-        gh[1] = gh[0] + DA * 64 * 128;
-        p = gh[1] + DA * 64 * 128;
-        ds = p + 128 * 128;
-        ds_lo = ds + 128 * 128;
-        bits[0] = ds_lo + 128 * 128;  // 8 tiles x 64 rows x 16 bits
-        bits[1] = bits[0] + 1024;
-        lse[0] = bits[1] + 1024;      // 64 fp32
-        lse[1] = lse[0] + 256;
-        dl[0] = lse[1] + 256;
-        dl[1] = dl[0] + 256;
-        total = dl[1] + 256;
-    }
+template <int D> struct ColCfg {
+    static constexpr int DA = D / 64;
+    static constexpr uint32_t CB = DA * 128 * 128;   // K or V of the column panel (128 sources)
+    static constexpr uint32_t HB = DA * 64 * 128;    // Q or dOut of a block (64 destinations)
+    static constexpr int NST = D == 128 ? 3 : 4;
+    static constexpr uint32_t C0 = 0;                // K, then V
+    static constexpr uint32_t ST0 = C0 + 2 * CB;     // stage: Q, dOut, masks (8 tiles x 16 sources x 64 bits), lse, Delta
+    static constexpr uint32_t TX = 2 * HB + 1024 + 256 + 256;   // bytes a stage receives
+    static constexpr uint32_t STB = (TX + 1023) / 1024 * 1024;  // stages 1024-aligned (128-byte swizzle)
+    static constexpr uint32_t PD0 = ST0 + NST * STB; // P^T, dS^T hi, dS^T lo (128 x 64 bf16 each)
+    static constexpr uint32_t BYTES = PD0 + 3 * 128 * 128;
+};
+
+static_assert(ColCfg<64>::STB % 1024 == 0 && ColCfg<128>::STB % 1024 == 0, "stage alignment");
+static_assert(ColCfg<128>::BYTES + 1024 <= 227 * 1024 && ColCfg<64>::BYTES + 1024 <= 227 * 1024, "shared memory");
+static_assert(RowCfg<128, 0>::BYTES + 1024 <= 227 * 1024 && RowCfg<128, 1>::BYTES + 1024 <= 227 * 1024 &&
+                  RowCfg<64, 0>::BYTES + 1024 <= 227 * 1024 && RowCfg<64, 1>::BYTES + 1024 <= 227 * 1024,
+              "shared memory");
+
+struct ColParams {
+    CUtensorMap tk, tv, tq, tg;   // [N][H*D] bf16: K, V boxes 64 x 128; Q, dOut boxes 64 x 64
+    BsrBwdArgs a;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(BsrBwdArgs a) {
-    constexpr uint32_t kCols = D == 128 ? 512 : 256;   // S^T, dP^T (64 each), dV, dK (D each)
+__global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_constant__ ColParams prm) {
+    using C = ColCfg<D>;
+    const BsrBwdArgs &a = prm.a;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t mbar_s, mbar_o;
+    __shared__ uint64_t c_full, c_empty, kv_full[C::NST], kv_empty[C::NST], s_full[2], s_empty[2], pd_full, pd_empty,
+        acc_empty, mma_done;
     __shared__ uint32_t tmem_base;
-    const ColLayout L(D);
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int cp = blockIdx.x, h = blockIdx.y, H = a.H;
-    const int32_t e0 = a.ct_ptr[cp], e1 = a.ct_ptr[cp + 1];
-    const int nu = 2 * (e1 - e0);   // units: (entry, 64-row half)
-    if (nu == 0) return;            // whole CTA: no kept tile in these columns
-
-    const int64_t c0 = (int64_t)cp * 128, src = c0 + tid;
-    const bool in = src < a.N;
-    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.Q);
-    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(a.K);
-    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(a.V);
-    const __nv_bfloat16 *G = static_cast<const __nv_bfloat16 *>(a.dOut);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = tc::smem_u32(smem);
+    const int H = a.H;
+    const int64_t n_units = (int64_t)a.n_cactive * H;
 
-    if (warp == 0) tc::tmem_alloc(&tmem_base, kCols);
-    if (tid == 0) {
-        tc::mbar_init(&mbar_s, 1);
-        tc::mbar_init(&mbar_o, 1);
-    }
-    // rows of one unit: Q and dOut of 64 destinations, their masks, lse, Delta
-    auto load_unit = [&](int u, int b) {
-        const int32_t e = e0 + u / 2;
-        const int hf = u & 1;
-        const int64_t row0 = (int64_t)a.ct_panel[e] * 128 + hf * 64;
-        load_rows<D>(sbase + L.qh[b], Q, row0, 64, a.N, H, h);
-        load_rows<D>(sbase + L.gh[b], G, row0, 64, a.N, H, h);
-        if (tid < 64) {   // 8 tiles x 8 chunks of 8 rows
-            const int t = tid >> 3, ch = tid & 7;
-            const int32_t tile = a.ct_tile[(size_t)e * 8 + t];
-            const bool ok = tile >= 0;
-            tc::cp16(sbase + L.bits[b] + (uint32_t)(t * 64 + ch * 8) * 2,
-                     ok ? a.tile_bits + (size_t)tile * 128 + hf * 64 + ch * 8 : a.tile_bits, ok);
-        } else {
-            const int i = tid - 64;
-            const bool ok = row0 + i < a.N;
-            const size_t off = ok ? (size_t)(row0 + i) * H + h : 0;
-            tc::cp4(sbase + L.lse[b] + i * 4, a.lse_n + off, ok);
-            tc::cp4(sbase + L.dl[b] + i * 4, a.delta + off, ok);
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
+    if (tid == 32) {
+        tc::mbar_init(&c_full, 1);
+        tc::mbar_init(&c_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&s_full[i], 1);
+            tc::mbar_init(&s_empty[i], 4);
         }
-        tc::cp_commit();
-    };
-    load_rows<D>(sbase + L.kc, K, c0, 128, a.N, H, h);
-    load_rows<D>(sbase + L.vc, V, c0, 128, a.N, H, h);
-    load_unit(0, 0);   // the column rows travel in the first group
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tS = tmem_base, tP = tmem_base + 64, tV = tmem_base + 128, tK = tmem_base + 128 + D;
-    const uint32_t tlane = (uint32_t)(warp * 32) << 16;
-    const uint32_t idesc_s = tc::idesc_bf16(128, 64), idesc_d = tc::idesc_bf16(128, D) | tc::kMajorMnB;
-    const float scale2 = kLog2e * rsqrtf((float)D);
-
-    bool failed = false;
-    int n_o = 0;
-    for (int u = 0; u < nu; ++u) {
-        const int b = u & 1;
-        // the previous dV / dK products read P^T, dS^T and the other unit's dOut and Q rows
-        if (u > 0 && !tc::mbar_wait(&mbar_o, (u - 1) & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
-        if (u + 1 < nu) {
-            load_unit(u + 1, b ^ 1);
-            tc::cp_wait<1>();
-        } else {
-            tc::cp_wait<0>();
+        for (int i = 0; i < C::NST; ++i) {
+            tc::mbar_init(&kv_full[i], 1);
+            tc::mbar_init(&kv_empty[i], 1);
         }
-        tc::fence_after_sync();
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {   // S^T = K Q^T, dP^T = V dOut^T
-            tc::fence_after_sync();
-            mma_over_d(tS, sbase + L.kc, sbase + L.qh[b], 64, D, idesc_s);
-            mma_over_d(tP, sbase + L.vc, sbase + L.gh[b], 64, D, idesc_s);
-            tc::mma_commit(&mbar_s);
-        }
-        if (!tc::mbar_wait(&mbar_s, u & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
-        tc::fence_after_sync();
-
-        const uint16_t *bits = reinterpret_cast<const uint16_t *>(smem + L.bits[b]) + (tid >> 4) * 64;
-        const float *lse = reinterpret_cast<const float *>(smem + L.lse[b]);
-        const float *dl = reinterpret_cast<const float *>(smem + L.dl[b]);
-        const int bit = tid & 15;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            uint32_t us[32], up[32];
-            tc::tmem_ld32(tS + tlane + half * 32, us);
-            tc::tmem_ld32(tP + tlane + half * 32, up);
-            float pv[32], ds[32];
-#pragma unroll
-            for (int ii = 0; ii < 32; ++ii) {
-                const int i = half * 32 + ii;
-                const bool on = in && ((bits[i] >> bit) & 1u);
-                const float p = on ? exp2f(__uint_as_float(us[ii]) * scale2 - lse[i] * kLog2e) : 0.f;
-                pv[ii] = p;
-                ds[ii] = p * (__uint_as_float(up[ii]) - dl[i]);
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const uint32_t o = tc::sw128_offset(tid, half * 32 + c * 8, 128);
-                uint4 hi, lo;
-                split_bf16x8(ds + 8 * c, hi, lo);
-                *reinterpret_cast<uint4 *>(smem + L.p + o) = pack<__nv_bfloat16>(pv + 8 * c);
-                *reinterpret_cast<uint4 *>(smem + L.ds + o) = hi;
-                *reinterpret_cast<uint4 *>(smem + L.ds_lo + o) = lo;
-            }
-        }
-        tc::fence_before_sync();
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {   // dV += P^T dOut, dK += dS^T_hi Q + dS^T_lo Q
-            tc::fence_after_sync();
-            mma_rows64(tV, sbase + L.p, sbase + L.gh[b], idesc_d, u == 0);
-            mma_rows64(tK, sbase + L.ds, sbase + L.qh[b], idesc_d, u == 0);
-            mma_rows64(tK, sbase + L.ds_lo, sbase + L.qh[b], idesc_d, false);
-            tc::mma_commit(&mbar_o);
-        }
-        ++n_o;
-    }
-    tc::cp_wait<0>();
-    if (!failed && !tc::mbar_wait(&mbar_o, (nu - 1) & 1, tc::kWaitLimit)) failed = true;
-    failed = __syncthreads_or(failed);
-    if (failed) {
-        if (tid == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
-        if (n_o > 0) tc::mbar_wait(&mbar_o, (n_o - 1) & 1, tc::kWaitLimit);
-    } else {
-        tc::fence_after_sync();
-        const size_t off = ((size_t)src * H + h) * D;
-        add_row_from_tmem<D>(tK + tlane, static_cast<__nv_bfloat16 *>(a.dK) + (in ? off : 0),
-                             rsqrtf((float)D), in);
-        add_row_from_tmem<D>(tV + tlane, static_cast<__nv_bfloat16 *>(a.dV) + (in ? off : 0), 1.f, in);
+        tc::mbar_init(&pd_full, 4);
+        tc::mbar_init(&pd_empty, 1);
+        tc::mbar_init(&acc_empty, 4);
+        tc::mbar_init(&mma_done, 1);
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem_base, kCols);
+    tc::fence_after_sync();
+    // TMEM: S^T and dP^T of buffer sb at 128 sb, 128 sb + 64; dV at 256, dK at 256 + D
+    const uint32_t tbase = tmem_base, tV = tmem_base + 256, tK = tmem_base + 256 + D;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ------------------------------------------------ TMA producer
+            int64_t B = 0, U = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+                const int32_t cp = a.cpanel_order[u / H];
+                const int h = (int)(u % H);
+                const int32_t e0 = a.ct_ptr[cp], e1 = a.ct_ptr[cp + 1];
+                const int nb = 2 * (e1 - e0);   // blocks: (entry, 64-row half)
+                if (U >= 1 && !tc::mbar_wait(&c_empty, (U - 1) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                tc::mbar_expect_tx(&c_full, 2 * C::CB);
+                for (int at = 0; at < C::DA; ++at) {
+                    tc::tma_load_2d(sbase + C::C0 + at * 128 * 128, &prm.tk, h * D + at * 64, cp * 128, &c_full);
+                    tc::tma_load_2d(sbase + C::C0 + C::CB + at * 128 * 128, &prm.tv, h * D + at * 64, cp * 128,
+                                    &c_full);
+                }
+                for (int b = 0; b < nb; ++b, ++B) {
+                    const int s = (int)(B % C::NST);
+                    const int64_t n = B / C::NST;
+                    if (n >= 1 && !tc::mbar_wait(&kv_empty[s], (n - 1) & 1, tc::kWaitLimit)) {
+                        ok = false;
+                        break;
+                    }
+                    const int32_t e = e0 + b / 2;
+                    const int hf = b & 1;
+                    const int row0 = a.ct_panel[e] * 128 + hf * 64;
+                    const uint32_t st = sbase + C::ST0 + s * C::STB;
+                    tc::mbar_expect_tx(&kv_full[s], C::TX);
+                    for (int at = 0; at < C::DA; ++at) {
+                        tc::tma_load_2d(st + at * 64 * 128, &prm.tq, h * D + at * 64, row0, &kv_full[s]);
+                        tc::tma_load_2d(st + C::HB + at * 64 * 128, &prm.tg, h * D + at * 64, row0, &kv_full[s]);
+                    }
+                    for (int t = 0; t < 8; ++t) {   // the 8 tile columns' masks of the 64 rows, transposed
+                        const int32_t tile = a.ct_tile[(size_t)e * 8 + t];
+                        tc::bulk_load(st + 2 * C::HB + t * 128,
+                                      a.tile_bits_t + ((size_t)(tile >= 0 ? tile : a.n_tiles) * 2 + hf) * 16, 128,
+                                      &kv_full[s]);
+                    }
+                    tc::bulk_load(st + 2 * C::HB + 1024, a.lse_t + (size_t)h * a.N_pad + row0, 256, &kv_full[s]);
+                    tc::bulk_load(st + 2 * C::HB + 1280, a.delta_t_hm + (size_t)h * a.N_pad + row0, 256,
+                                  &kv_full[s]);
+                }
+            }
+            if (!ok) atomicOr(a.d_err, tc::kErrMmaTimeout);
+            for (int64_t i = B - 1; i >= 0 && i >= B - C::NST; --i)
+                tc::mbar_wait(&kv_full[i % C::NST], (i / C::NST) & 1, tc::kWaitLimit);
+            if (U >= 1) tc::mbar_wait(&c_full, (U - 1) & 1, tc::kWaitLimit);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ------------------------------------------------ MMA issuer
+            const uint32_t idesc_s = tc::idesc_bf16(128, 64), idesc_d = tc::idesc_bf16(128, D) | tc::kMajorMnB;
+            int64_t B = 0, U = 0;
+            bool ok = true;
+            // dV += P^T dOut, dK += dS^T_hi Q + dS^T_lo Q of block Bp; the first
+            // of unit Up overwrites dK/dV once the previous unit's epilogue has read them
+            auto issue_kv = [&](int64_t Bp, bool first, int64_t Up) -> bool {
+                if (!tc::mbar_wait(&pd_full, Bp & 1, tc::kWaitLimit)) return false;
+                if (first && Up >= 1 && !tc::mbar_wait(&acc_empty, (Up - 1) & 1, tc::kWaitLimit)) return false;
+                tc::fence_after_sync();
+                const int s = (int)(Bp % C::NST);
+                const uint32_t st = sbase + C::ST0 + s * C::STB;
+                mma_rows64(tV, sbase + C::PD0, st + C::HB, idesc_d, first);
+                mma_rows64(tK, sbase + C::PD0 + 128 * 128, st, idesc_d, first);
+                mma_rows64(tK, sbase + C::PD0 + 2 * 128 * 128, st, idesc_d, false);
+                tc::mma_commit(&kv_empty[s]);
+                tc::mma_commit(&pd_empty);
+                return true;
+            };
+            int64_t pend = -1, pend_u = 0;
+            bool pend_first = false;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+                const int32_t cp = a.cpanel_order[u / H];
+                const int nb = 2 * (a.ct_ptr[cp + 1] - a.ct_ptr[cp]);
+                if (!tc::mbar_wait(&c_full, U & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                for (int b = 0; b < nb; ++b, ++B) {
+                    const int s = (int)(B % C::NST), sb = (int)(B & 1);
+                    if (!tc::mbar_wait(&kv_full[s], (B / C::NST) & 1, tc::kWaitLimit) ||
+                        (B >= 2 && !tc::mbar_wait(&s_empty[sb], ((B >> 1) - 1) & 1, tc::kWaitLimit))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t st = sbase + C::ST0 + s * C::STB;
+                    mma_over_d(tbase + sb * 128, sbase + C::C0, st, 64, D, idesc_s);                   // S^T = K Q^T
+                    mma_over_d(tbase + sb * 128 + 64, sbase + C::C0 + C::CB, st + C::HB, 64, D, idesc_s);   // dP^T
+                    tc::mma_commit(&s_full[sb]);
+                    if (b == nb - 1) tc::mma_commit(&c_empty);
+                    if (pend >= 0 && !issue_kv(pend, pend_first, pend_u)) {
+                        ok = false;
+                        break;
+                    }
+                    pend = B;
+                    pend_first = b == 0;
+                    pend_u = U;
+                }
+            }
+            if (ok && pend >= 0 && !issue_kv(pend, pend_first, pend_u)) ok = false;
+            if (!ok) atomicOr(a.d_err, tc::kErrMmaTimeout);
+            tc::mma_commit(&mma_done);
+            tc::mbar_wait(&mma_done, 0, tc::kWaitLimit);
+        }
+    } else {   // ---------------------------------------------------- weights and gradients
+        const int quarter = warp & 3, r = quarter * 32 + lane;   // source of the column panel
+        const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
+        const float scale2 = kLog2e * rsqrtf((float)D);
+        int64_t B = 0, U = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+            const int32_t cp = a.cpanel_order[u / H];
+            const int h = (int)(u % H);
+            const int nb = 2 * (a.ct_ptr[cp + 1] - a.ct_ptr[cp]);
+            const int64_t src = (int64_t)cp * 128 + r;
+            const bool in = src < a.N;
+            if (in) {
+                prefetch_row<D>(static_cast<const __nv_bfloat16 *>(a.dK) + (src * H + h) * D);
+                prefetch_row<D>(static_cast<const __nv_bfloat16 *>(a.dV) + (src * H + h) * D);
+            }
+            for (int b = 0; b < nb; ++b, ++B) {
+                const int s = (int)(B % C::NST), sb = (int)(B & 1);
+                // products, the stage's masks and row terms, and a free P / dS buffer
+                if (!tc::warp_wait(&s_full[sb], (B >> 1) & 1, tc::kWaitLimit) ||
+                    !tc::warp_wait(&kv_full[s], (B / C::NST) & 1, tc::kWaitLimit) ||
+                    (B >= 1 && !tc::warp_wait(&pd_empty, (B - 1) & 1, tc::kWaitLimit))) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const unsigned char *st = smem + C::ST0 + s * C::STB;
+                // this source's 64 row bits of the block (transposed masks: word r)
+                const uint64_t m64 = in ? reinterpret_cast<const uint64_t *>(st + 2 * C::HB)[r] : 0ull;
+                const float4 *lse4 = reinterpret_cast<const float4 *>(st + 2 * C::HB + 1024);
+                const float4 *dl4 = reinterpret_cast<const float4 *>(st + 2 * C::HB + 1280);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t us[32], up[32];
+                    tc::tmem_ld32(tbase + sb * 128 + tlane + half * 32, us);
+                    tc::tmem_ld32(tbase + sb * 128 + 64 + tlane + half * 32, up);
+                    float pv[32], ds[32];
+#pragma unroll
+                    for (int i4 = 0; i4 < 8; ++i4) {
+                        const float4 l4 = lse4[half * 8 + i4], d4 = dl4[half * 8 + i4];
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int ii = i4 * 4 + k, i = half * 32 + ii;
+                            const bool on = (m64 >> i) & 1ull;
+                            const float p = on ? exp2f(__uint_as_float(us[ii]) * scale2 - lv[k] * kLog2e) : 0.f;
+                            pv[ii] = p;
+                            ds[ii] = p * (__uint_as_float(up[ii]) - dv[k]);
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t o = tc::sw128_offset(r, half * 32 + c * 8, 128);
+                        uint4 hi, lo;
+                        split_bf16x8(ds + 8 * c, hi, lo);
+                        *reinterpret_cast<uint4 *>(smem + C::PD0 + o) = pack<__nv_bfloat16>(pv + 8 * c);
+                        *reinterpret_cast<uint4 *>(smem + C::PD0 + 128 * 128 + o) = hi;
+                        *reinterpret_cast<uint4 *>(smem + C::PD0 + 2 * 128 * 128 + o) = lo;
+                    }
+                }
+                tc::fence_before_sync();
+                tc::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&s_empty[sb]);
+                    tc::mbar_arrive(&pd_full);
+                }
+            }
+            if (!ok) break;
+            // the unit's last products, then add the tile parts to dK and dV
+            if (!tc::warp_wait(&pd_empty, (B - 1) & 1, tc::kWaitLimit)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const size_t off = ((size_t)(in ? src : 0) * H + h) * D;
+            add_row_from_tmem<D>(tK + tlane, static_cast<__nv_bfloat16 *>(a.dK) + off, rsqrtf((float)D), in);
+            add_row_from_tmem<D>(tV + tlane, static_cast<__nv_bfloat16 *>(a.dV) + off, 1.f, in);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty);
+        }
+        if (!ok && lane == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// lse + ln Z and Delta in head-major order [H][N_pad] (zero past N), so that
+// a block's 64 consecutive rows are one 256-byte bulk copy
+__global__ void head_major_kernel(const float *__restrict__ lse_n, const float *__restrict__ delta, int64_t N,
+                                  int64_t N_pad, int H, float *__restrict__ lse_t, float *__restrict__ dl_t) {
+    const int64_t n = N_pad * H, stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += stride) {
+        const int h = (int)(x / N_pad);
+        const int64_t i = x % N_pad;
+        lse_t[x] = i < N ? lse_n[i * H + h] : 0.f;
+        dl_t[x] = i < N ? delta[i * H + h] : 0.f;
+    }
 }
 
 // ---------------------------------------------------------------- launch
 
-// At least 100 KB of shared memory per CTA: at most two CTAs (two 256-column
-// TMEM allocations) share an SM; the 512-column dK/dV CTA needs more than
-// half of the SM's shared memory, so it runs alone.
-template <auto Kernel>
-cudaError_t launch(const BsrBwdArgs &a, dim3 grid, size_t bytes, sga_kernel_id id, cudaStream_t s) {
-    const size_t smem = bytes + 1024 > 100 * 1024 ? bytes + 1024 : 100 * 1024;
+template <auto Kernel, typename P>
+cudaError_t launch(const P &prm, int64_t units, int num_sms, size_t bytes, sga_kernel_id id, cudaStream_t s) {
+    const size_t smem = bytes + 1024;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
+    const unsigned grid = (unsigned)(units < num_sms ? units : num_sms);
     note_launch(id, s, false);
-    Kernel<<<grid, kThreads, smem, s>>>(a);
+    Kernel<<<grid, kThreads, smem, s>>>(prm);
     note_launch(id, s, true);
     return cudaGetLastError();
+}
+
+template <int D> cudaError_t row_pass(const BsrBwdArgs &a, int mode, cudaStream_t s) {
+    RowParams prm{};
+    prm.a = a;
+    const int64_t HD = (int64_t)a.H * D;
+    auto bf = [](const void *p) { return static_cast<const __nv_bfloat16 *>(p); };
+    cudaError_t e = bf16_tensor_map(&prm.tq, bf(a.Q), a.N, HD, HD, 64, 128);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tg, bf(a.dOut), a.N, HD, HD, 64, 128);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tk, bf(a.K), a.N, HD, HD, 64, 16);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tv, bf(a.V), a.N, HD, HD, 64, 16);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.n_active * a.H;
+    return mode == 0 ? launch<bsr_bwd_row_kernel<D, 0>>(prm, units, a.num_sms, RowCfg<D, 0>::BYTES,
+                                                         SGA_KERN_BSR_BWD_DELTA, s)
+                     : launch<bsr_bwd_row_kernel<D, 1>>(prm, units, a.num_sms, RowCfg<D, 1>::BYTES,
+                                                        SGA_KERN_BSR_BWD_DQ, s);
+}
+
+template <int D> cudaError_t col_pass(const BsrBwdArgs &a, cudaStream_t s) {
+    ColParams prm{};
+    prm.a = a;
+    const int64_t HD = (int64_t)a.H * D;
+    auto bf = [](const void *p) { return static_cast<const __nv_bfloat16 *>(p); };
+    cudaError_t e = bf16_tensor_map(&prm.tk, bf(a.K), a.N, HD, HD, 64, 128);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tv, bf(a.V), a.N, HD, HD, 64, 128);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tq, bf(a.Q), a.N, HD, HD, 64, 64);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tg, bf(a.dOut), a.N, HD, HD, 64, 64);
+    if (e != cudaSuccess) return e;
+    const int64_t units = (int64_t)a.n_cactive * a.H;
+    return launch<bsr_bwd_col_kernel<D>>(prm, units, a.num_sms, ColCfg<D>::BYTES, SGA_KERN_BSR_BWD_DKDV, s);
 }
 
 }  // namespace
 
 cudaError_t launch_bsr_bwd_delta(const BsrBwdArgs &a, cudaStream_t s) {
-    if (a.n_panels == 0) return cudaSuccess;
-    const dim3 grid((unsigned)a.n_panels, (unsigned)a.H);
-    const size_t bytes = RowLayout(a.D, 0).total;
-    return a.D == 128 ? launch<bsr_bwd_row_kernel<128, 0>>(a, grid, bytes, SGA_KERN_BSR_BWD_DELTA, s)
-                      : launch<bsr_bwd_row_kernel<64, 0>>(a, grid, bytes, SGA_KERN_BSR_BWD_DELTA, s);
+    if (a.n_active == 0) return cudaSuccess;
+    return a.D == 128 ? row_pass<128>(a, 0, s) : row_pass<64>(a, 0, s);
 }
 
 cudaError_t launch_bsr_bwd_dq(const BsrBwdArgs &a, cudaStream_t s) {
-    if (a.n_panels == 0) return cudaSuccess;
-    const dim3 grid((unsigned)a.n_panels, (unsigned)a.H);
-    const size_t bytes = RowLayout(a.D, 1).total;
-    return a.D == 128 ? launch<bsr_bwd_row_kernel<128, 1>>(a, grid, bytes, SGA_KERN_BSR_BWD_DQ, s)
-                      : launch<bsr_bwd_row_kernel<64, 1>>(a, grid, bytes, SGA_KERN_BSR_BWD_DQ, s);
+    if (a.n_active == 0) return cudaSuccess;
+    return a.D == 128 ? row_pass<128>(a, 1, s) : row_pass<64>(a, 1, s);
 }
 
 cudaError_t launch_bsr_bwd_dkdv(const BsrBwdArgs &a, cudaStream_t s) {
-    if (a.n_cpanels == 0) return cudaSuccess;
-    const dim3 grid((unsigned)a.n_cpanels, (unsigned)a.H);
-    const size_t bytes = ColLayout(a.D).total;
-    return a.D == 128 ? launch<bsr_bwd_col_kernel<128>>(a, grid, bytes, SGA_KERN_BSR_BWD_DKDV, s)
-                      : launch<bsr_bwd_col_kernel<64>>(a, grid, bytes, SGA_KERN_BSR_BWD_DKDV, s);
+    if (a.n_cactive == 0) return cudaSuccess;
+    const int64_t n = a.N_pad * a.H;
+    head_major_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 65535), 256, 0, s>>>(
+        a.lse_n, a.delta, a.N, a.N_pad, a.H, a.lse_t, a.delta_t_hm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return a.D == 128 ? col_pass<128>(a, s) : col_pass<64>(a, s);
 }
 
 }  // namespace sga

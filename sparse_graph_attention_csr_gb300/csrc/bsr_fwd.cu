@@ -3,255 +3,389 @@
 // IO-Aware Layers Implementations" (arXiv abstract; blog post,
 // "Attention-based layers" paragraph), which pays off on locally dense graphs.
 //
-// One CTA (4 warps, thread = panel row) per (128-row panel, head).  The
-// panel's kept column tiles are taken four at a time (64 sources).  Per
-// group: S = Q_panel K_group^T (128 x 64, K = D) into TMEM; each thread reads
-// its row of S, masks it with the tile bitmaps, scales it and runs the online
-// softmax with a lazily moved maximum (the accumulator is rescaled only when
-// a row's maximum grows by more than 2^8, so P stays below 2^8); P goes to
-// shared memory in bf16 and O += P V_group (128 x D, K = 64) accumulates in
-// TMEM.  V rows stay in their node-major 128-byte-swizzled layout, which is
-// the MN-major B operand of that product (no transpose).  The next group's K
-// rows load once S has consumed K, its V rows once the previous P V product
-// has consumed the other V buffer; both overlap the softmax.
-//
-// The residual edges (outside kept tiles) were processed beforehand by the
-// CSR forward, whose out/lse sit in the output buffers; each row's tile result
-// (O / l, m + log l) is merged with them by log-sum-exp.
+// Persistent CTAs, one per SM, take work units (128-row panel, head) from the
+// plan's panel order (most kept tiles first), round robin.  A unit's kept
+// column tiles are taken four at a time (64 sources, a "group").  Roles:
+//   warp 0, one lane: TMA loads -- the unit's Q panel (two buffers, so the
+//     next unit's panel loads during this one) and, for every group, its K
+//     and V rows (one 16-row box per tile and 64-wide column atom; missing
+//     tiles read rows past N, which TMA fills with zeros) plus the four tiles'
+//     source masks (a bulk copy each; a missing tile copies the plan's zero
+//     tile), into a ring of stages;
+//   warp 1, one lane: the MMAs -- S = Q K^T (128 x 64, K = D) into one of two
+//     TMEM score buffers, and O += P V (128 x D, K = 64; V rows are the
+//     MN-major B operand as they lie) into the TMEM accumulator, issued in
+//     the order S(g), P V(g-1), so the tensor core computes the next scores
+//     and the previous product while the softmax runs;
+//   warps 2-5 (thread = panel row = TMEM lane): the online softmax with a
+//     lazily moved maximum (O is rescaled in TMEM only when a row's maximum
+//     grows by more than 2^8, so P stays below 2^8), P to shared memory in
+//     bf16, and the epilogue, which merges each row's tile result (O / l,
+//     m + log l) by log-sum-exp with the residual CSR result already stored
+//     in out and lse.
+// Every handoff is an mbarrier (TMA transaction counts, tcgen05.commit, or
+// the arrivals of the four softmax warps); every wait is bounded and a
+// timeout sets the plan's error word and ends the role.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "plan.h"
 #include "tc.cuh"
+#include "tc_dx.cuh"
 
 namespace sga {
 namespace {
 
-constexpr int kBsThreads = 128;
-constexpr int kGroup = 64;           // sources per group (four 16-wide tiles)
-constexpr float kLazy = 8.0f;        // log2 growth that triggers a rescale
+constexpr int kThreads = 192;
+constexpr int kGroup = 64;   // sources per group (four 16-wide tiles)
+constexpr float kLazy = 8.0f;
 
-// One K buffer (reloaded once S has consumed it) and two V buffers (the P V
-// product reads V directly): under 100 KB, so two CTAs share an SM.
-struct BsLayout {   // byte offsets in dynamic shared memory (1024-aligned base)
-    uint32_t q, k, v[2], p, total;
-    __host__ __device__ BsLayout(int D) {
-        const uint32_t DA = (uint32_t)(D + 63) / 64;
-        q = 0;
-        k = q + DA * 128 * 128;
-        v[0] = k + DA * kGroup * 128;
-        v[1] = v[0] + DA * kGroup * 128;
-        p = v[1] + DA * kGroup * 128;
-        total = p + 128 * 128;
-    }
+template <int D> struct FwdCfg {
+    static constexpr int DA = D / 64;                          // 64-wide column atoms of a head row
+    static constexpr uint32_t QB = DA * 128 * 128;             // Q panel (128 rows)
+    static constexpr uint32_t KB = DA * kGroup * 128;          // K (or V) rows of a group
+    static constexpr int NST = D == 128 ? 3 : 4;               // K/V stages
+    static constexpr uint32_t Q0 = 0;                          // two Q buffers
+    static constexpr uint32_t ST0 = Q0 + 2 * QB;               // stage s: K, then V, then masks
+    static constexpr uint32_t STB = 2 * KB + 1024;             //   (masks: 4 tiles x 128 rows x 2 B)
+    static constexpr uint32_t P0 = ST0 + NST * STB;            // two P buffers (128 x 64 bf16)
+    static constexpr uint32_t BYTES = P0 + 2 * 128 * 128;
+    static constexpr uint32_t TX = 2 * KB + 1024;              // transaction bytes of a stage
+};
+
+static_assert(FwdCfg<64>::STB % 1024 == 0 && FwdCfg<128>::STB % 1024 == 0, "stage alignment");
+static_assert(FwdCfg<128>::BYTES + 1024 <= 227 * 1024 && FwdCfg<64>::BYTES + 1024 <= 227 * 1024, "shared memory");
+
+struct FwdParams {
+    CUtensorMap tq, tk, tv;   // [N][H*D] bf16; boxes 64 x 128 (Q), 64 x 16 (K, V); 128-byte swizzle
+    BsrArgs a;
 };
 
 template <int D>
-__global__ void __launch_bounds__(kBsThreads, 1) bsr_fwd_kernel(BsrArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) bsr_fwd_kernel(const __grid_constant__ FwdParams prm) {
+    using C = FwdCfg<D>;
+    const BsrArgs &a = prm.a;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t mbar_s, mbar_o;
+    __shared__ uint64_t q_full[2], q_empty[2], kv_full[C::NST], kv_empty[C::NST], s_full[2], s_empty[2],
+        p_full[2], pv_done[2], o_empty, mma_done;
     __shared__ uint32_t tmem_base;
-    const BsLayout L(D);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int panel = blockIdx.x, h = blockIdx.y, H = a.H;
-    const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
-    const int ng = (t1 - t0 + 3) / 4;
-    if (ng == 0) return;   // whole CTA: no kept tile, the residual result stands
-
-    const int64_t r0 = (int64_t)panel * 128;
-    const int r = tid;                       // panel row of this thread (TMEM lane r)
-    const int64_t row = r0 + r;
-    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.Q);
-    const __nv_bfloat16 *K = static_cast<const __nv_bfloat16 *>(a.K);
-    const __nv_bfloat16 *V = static_cast<const __nv_bfloat16 *>(a.V);
     const uint32_t sbase = tc::smem_u32(smem);
-    constexpr int DC = D / 8;                // 16-byte chunks per head row
+    const int H = a.H;
+    const int64_t n_units = (int64_t)a.n_active * H;
 
     if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
-    if (tid == 0) {
-        tc::mbar_init(&mbar_s, 1);
-        tc::mbar_init(&mbar_o, 1);
-    }
-    // Q panel rows, head h (zero rows past N)
-    for (int idx = tid; idx < 128 * DC; idx += kBsThreads) {
-        const int rr = idx / DC, c = idx % DC;
-        const bool ok = r0 + rr < a.N;
-        tc::cp16(sbase + L.q + tc::sw128_offset(rr, c * 8, 128),
-                 ok ? Q + ((r0 + rr) * H + h) * D + c * 8 : Q, ok);
-    }
-    // rows of group g's kept tiles (zero past N or past the panel's tiles) of
-    // one head of X into the swizzled tile at dst
-    auto load_rows = [&](int g, const __nv_bfloat16 *X, uint32_t dst) {
-        for (int idx = tid; idx < kGroup * DC; idx += kBsThreads) {
-            const int jr = idx / DC, c = idx % DC;
-            const int32_t ti = t0 + 4 * g + jr / 16;
-            const int64_t j = ti < t1 ? (int64_t)a.tile_col[ti] * 16 + (jr % 16) : -1;
-            const bool ok = j >= 0 && j < a.N;
-            tc::cp16(dst + tc::sw128_offset(jr, c * 8, kGroup), ok ? X + ((size_t)j * H + h) * D + c * 8 : X, ok);
+    if (tid == 32) {
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&q_full[i], 1);
+            tc::mbar_init(&q_empty[i], 1);
+            tc::mbar_init(&s_full[i], 1);
+            tc::mbar_init(&s_empty[i], 4);
+            tc::mbar_init(&p_full[i], 4);
+            tc::mbar_init(&pv_done[i], 1);
         }
-        tc::cp_commit();
-    };
-    load_rows(0, K, sbase + L.k);   // Q travels in the same first group
-    load_rows(0, V, sbase + L.v[0]);
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tO = tmem_base, tS = tmem_base + D;
-    const uint32_t tlane = (uint32_t)(warp * 32) << 16;
-    const uint32_t idesc_s = tc::idesc_bf16(128, kGroup), idesc_o = tc::idesc_bf16(128, D) | tc::kMajorMnB;
-    const float scale2 = kLog2e * rsqrtf((float)D);
-
-    float m = -INFINITY, l = 0.f;
-    bool failed = false;
-    int n_o = 0;   // P V products issued (uniform over the CTA)
-    for (int g = 0; g < ng; ++g) {
-        const int b = g & 1;
-        tc::cp_wait<0>();   // this group's K and V rows
-        // the previous P V product must be done before P, O and the other V buffer are touched
-        if (g > 0 && !tc::mbar_wait(&mbar_o, (g - 1) & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
-        tc::fence_after_sync();
-        if (g + 1 < ng) load_rows(g + 1, V, sbase + L.v[b ^ 1]);   // lands during this group
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {   // S = Q K^T
-            tc::fence_after_sync();
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t ao = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
-                const uint32_t bo = (uint32_t)((kk >> 2) * kGroup * 128 + (kk & 3) * 32);
-                tc::mma_bf16_ss(tS, tc::desc_sw128(sbase + L.q + ao), tc::desc_sw128(sbase + L.k + bo),
-                                idesc_s, kk > 0);
-            }
-            tc::mma_commit(&mbar_s);
+        for (int i = 0; i < C::NST; ++i) {
+            tc::mbar_init(&kv_full[i], 1);
+            tc::mbar_init(&kv_empty[i], 1);
         }
-        if (!tc::mbar_wait(&mbar_s, g & 1, tc::kWaitLimit)) failed = true;
-        if (__syncthreads_or(failed)) break;
-        tc::fence_after_sync();
-        // K is consumed: the next group's K rows load during the softmax
-        if (g + 1 < ng) load_rows(g + 1, K, sbase + L.k);
-
-        // masked, scaled scores of row r; lazy online softmax
-        float s[kGroup];
-        {
-            uint32_t u[32];
-            tc::tmem_ld32(tS + tlane, u);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[i] = __uint_as_float(u[i]);
-            tc::tmem_ld32(tS + tlane + 32, u);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[32 + i] = __uint_as_float(u[i]);
-        }
-        float smax = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int32_t ti = t0 + 4 * g + q;
-            const uint32_t bits = (ti < t1 && row < a.N) ? a.tile_bits[(size_t)ti * 128 + r] : 0u;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const float v = ((bits >> c) & 1u) ? s[q * 16 + c] * scale2 : -INFINITY;
-                s[q * 16 + c] = v;
-                smax = fmaxf(smax, v);
-            }
-        }
-        const bool grow = smax > m + kLazy || (m == -INFINITY && smax > -INFINITY);
-        const float m_new = grow ? fmaxf(m, smax) : m;
-        const float alpha = exp2_diff(m, m_new);
-        if (__any_sync(SGA_FULL_MASK, grow && g > 0 && l > 0.f)) {   // rescale O rows of this warp
-            const float f = (grow && l > 0.f) ? alpha : 1.f;
-            for (int cb = 0; cb < D; cb += 32) {
-                uint32_t u[32];
-                tc::tmem_ld32(tO + tlane + cb, u);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * f);
-                tc::tmem_st32(tO + tlane + cb, u);
-            }
-        }
-        if (grow) {
-            l *= alpha;
-            m = m_new;
-        }
-        float pr[kGroup];
-#pragma unroll
-        for (int i = 0; i < kGroup; ++i) {
-            pr[i] = exp2_diff(s[i], m);
-            l += pr[i];
-        }
-        // P row -> shared memory (bf16, K-major swizzled, 64 sources = one atom)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4 *>(smem + L.p + tc::sw128_offset(r, c * 8, 128)) =
-                pack<__nv_bfloat16>(pr + 8 * c);
-        tc::fence_before_sync();
-        tc::fence_proxy_async();
-        __syncthreads();
-        if (tid == 0) {   // O += P V
-            tc::fence_after_sync();
-            // B = V rows as an MN-major operand: D-wide column atoms of 64 rows, 16 rows per k-step
-            for (int kk = 0; kk < kGroup / 16; ++kk)
-                tc::mma_bf16_ss(tO, tc::desc_sw128(sbase + L.p + kk * 32),
-                                tc::desc_sw128_mn(sbase + L.v[b] + kk * 2048, kGroup * 128), idesc_o,
-                                (g > 0 || kk > 0));
-            tc::mma_commit(&mbar_o);
-        }
-        ++n_o;
-    }
-    tc::cp_wait<0>();
-    if (!failed && !tc::mbar_wait(&mbar_o, (ng - 1) & 1, tc::kWaitLimit)) failed = true;
-    failed = __syncthreads_or(failed);
-    if (failed) {
-        if (tid == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
-        // let the last product issued finish (bounded) before TMEM is released
-        if (n_o > 0) tc::mbar_wait(&mbar_o, (n_o - 1) & 1, tc::kWaitLimit);
-    } else {
-        tc::fence_after_sync();
-        // merge the tile result of row r with the residual result already stored
-        const bool has = l > 0.f && row < a.N;
-        __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + (row * H + h) * D;
-        float wt = 0.f, wr = 0.f, lse_new = 0.f;
-        if (has) {
-            const float lt = (m + log2f(l)) * kLn2, lr = a.lse[row * H + h];
-            const float M = fmaxf(lt, lr);
-            wt = __expf(lt - M);
-            wr = lr == -INFINITY ? 0.f : __expf(lr - M);
-            lse_new = M + logf(wt + wr);
-            const float inv = 1.f / (wt + wr);
-            wt *= inv / l;        // weight of the unnormalised tile accumulator
-            wr *= inv;
-        }
-        for (int cb = 0; cb < D; cb += 32) {
-            uint32_t u[32];
-            tc::tmem_ld32(tO + tlane + cb, u);   // warp-collective: every lane takes part
-            if (has) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    float o[8], x[8];
-                    unpack<__nv_bfloat16>(*reinterpret_cast<const uint4 *>(out + cb + 8 * q), x);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = wt * __uint_as_float(u[8 * q + i]) + wr * x[i];
-                    *reinterpret_cast<uint4 *>(out + cb + 8 * q) = pack<__nv_bfloat16>(o);
-                }
-            }
-        }
-        if (has) a.lse[row * H + h] = lse_new;
+        tc::mbar_init(&o_empty, 4);
+        tc::mbar_init(&mma_done, 1);
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+    tc::fence_after_sync();
+    const uint32_t tO = tmem_base, tS0 = tmem_base + D;   // O: D columns; S buffers: 64 columns each
+
+    if (warp == 0) {
+        if (lane == 0) {   // ------------------------------------------------ TMA producer
+            int64_t G = 0, U = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+                const int32_t panel = a.panel_order[u / H];
+                const int h = (int)(u % H);
+                const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
+                const int ng = (t1 - t0 + 3) / 4;
+                const int qb = (int)(U & 1);
+                if (U >= 2 && !tc::mbar_wait(&q_empty[qb], ((U >> 1) - 1) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                tc::mbar_expect_tx(&q_full[qb], C::QB);
+                for (int at = 0; at < C::DA; ++at)
+                    tc::tma_load_2d(sbase + C::Q0 + qb * C::QB + at * 128 * 128, &prm.tq, h * D + at * 64,
+                                    panel * 128, &q_full[qb]);
+                for (int g = 0; g < ng; ++g, ++G) {
+                    const int s = (int)(G % C::NST);
+                    const int64_t n = G / C::NST;
+                    if (n >= 1 && !tc::mbar_wait(&kv_empty[s], (n - 1) & 1, tc::kWaitLimit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t st = sbase + C::ST0 + s * C::STB;
+                    tc::mbar_expect_tx(&kv_full[s], C::TX);
+                    for (int q = 0; q < 4; ++q) {
+                        const int32_t ti = t0 + 4 * g + q;
+                        const int y = ti < t1 ? a.tile_col[ti] * 16 : (int)a.N;   // past N: zero rows
+                        for (int at = 0; at < C::DA; ++at) {
+                            const uint32_t off = at * kGroup * 128 + q * 16 * 128;
+                            tc::tma_load_2d(st + off, &prm.tk, h * D + at * 64, y, &kv_full[s]);
+                            tc::tma_load_2d(st + C::KB + off, &prm.tv, h * D + at * 64, y, &kv_full[s]);
+                        }
+                        tc::bulk_load(st + 2 * C::KB + q * 256,
+                                      a.tile_bits + (size_t)(ti < t1 ? ti : a.n_tiles) * 128, 256, &kv_full[s]);
+                    }
+                }
+            }
+            if (!ok) atomicOr(a.d_err, tc::kErrMmaTimeout);
+            // loads that no MMA consumed (only after a timeout) land before the CTA ends
+            for (int64_t i = G - 1; i >= 0 && i >= G - C::NST; --i)
+                tc::mbar_wait(&kv_full[i % C::NST], (i / C::NST) & 1, tc::kWaitLimit);
+            for (int64_t i = U - 1; i >= 0 && i >= U - 2; --i)
+                tc::mbar_wait(&q_full[i & 1], (i >> 1) & 1, tc::kWaitLimit);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ------------------------------------------------ MMA issuer
+            const uint32_t idesc_s = tc::idesc_bf16(128, kGroup);
+            const uint32_t idesc_o = tc::idesc_bf16(128, D) | tc::kMajorMnB;
+            int64_t G = 0, U = 0;
+            bool ok = true;
+            // O += P(Gp) V(Gp); the first product of unit Up overwrites O, once
+            // the previous unit's epilogue has read it
+            auto issue_pv = [&](int64_t Gp, bool first, int64_t Up) -> bool {
+                const int pb = (int)(Gp & 1), s = (int)(Gp % C::NST);
+                if (!tc::mbar_wait(&p_full[pb], (Gp >> 1) & 1, tc::kWaitLimit)) return false;
+                if (first && Up >= 1 && !tc::mbar_wait(&o_empty, (Up - 1) & 1, tc::kWaitLimit)) return false;
+                tc::fence_after_sync();
+                const uint32_t pa = sbase + C::P0 + pb * 128 * 128;
+                const uint32_t va = sbase + C::ST0 + s * C::STB + C::KB;
+                for (int kk = 0; kk < kGroup / 16; ++kk)
+                    tc::mma_bf16_ss(tO, tc::desc_sw128(pa + kk * 32), tc::desc_sw128_mn(va + kk * 2048, kGroup * 128),
+                                    idesc_o, (!first || kk > 0) ? 1u : 0u);
+                tc::mma_commit(&kv_empty[s]);
+                tc::mma_commit(&pv_done[pb]);
+                return true;
+            };
+            // issue order S(G), P V(G - 1), across unit boundaries too: the
+            // tensor core computes the next scores while the softmax runs
+            int64_t pend = -1, pend_u = 0;
+            bool pend_first = false;
+            for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+                const int32_t panel = a.panel_order[u / H];
+                const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
+                const int ng = (t1 - t0 + 3) / 4;
+                const int qb = (int)(U & 1);
+                if (!tc::mbar_wait(&q_full[qb], (U >> 1) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t qa = sbase + C::Q0 + qb * C::QB;
+                for (int g = 0; g < ng; ++g, ++G) {
+                    const int s = (int)(G % C::NST), sb = (int)(G & 1);
+                    if (!tc::mbar_wait(&kv_full[s], (G / C::NST) & 1, tc::kWaitLimit) ||
+                        (G >= 2 && !tc::mbar_wait(&s_empty[sb], ((G >> 1) - 1) & 1, tc::kWaitLimit))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const uint32_t ka = sbase + C::ST0 + s * C::STB;
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t ao = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
+                        const uint32_t bo = (uint32_t)((kk >> 2) * kGroup * 128 + (kk & 3) * 32);
+                        tc::mma_bf16_ss(tS0 + sb * kGroup, tc::desc_sw128(qa + ao), tc::desc_sw128(ka + bo), idesc_s,
+                                        kk > 0 ? 1u : 0u);
+                    }
+                    tc::mma_commit(&s_full[sb]);
+                    if (g == ng - 1) tc::mma_commit(&q_empty[qb]);
+                    if (pend >= 0 && !issue_pv(pend, pend_first, pend_u)) {
+                        ok = false;
+                        break;
+                    }
+                    pend = G;
+                    pend_first = g == 0;
+                    pend_u = U;
+                }
+            }
+            if (ok && pend >= 0 && !issue_pv(pend, pend_first, pend_u)) ok = false;
+            if (!ok) atomicOr(a.d_err, tc::kErrMmaTimeout);
+            // every product issued is complete before TMEM is released
+            tc::mma_commit(&mma_done);
+            tc::mbar_wait(&mma_done, 0, tc::kWaitLimit);
+        }
+    } else {   // ---------------------------------------------------- softmax + epilogue
+        const int quarter = warp & 3, r = quarter * 32 + lane;   // TMEM lanes 32 * (warp % 4) ..
+        const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
+        const float scale2 = kLog2e * rsqrtf((float)D);
+        int64_t G = 0, U = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
+            const int32_t panel = a.panel_order[u / H];
+            const int h = (int)(u % H);
+            const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
+            const int ng = (t1 - t0 + 3) / 4;
+            const int64_t row = (int64_t)panel * 128 + r;
+            const bool in = row < a.N;
+            // the residual result of this row is read back at the end of the unit
+            __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out) + ((in ? row : 0) * H + h) * D;
+            if (in)
+#pragma unroll
+                for (int b = 0; b < D * 2; b += 128) tc::prefetch_l2(reinterpret_cast<const char *>(out) + b);
+            const float lr = in ? a.lse[row * H + h] : -INFINITY;
+            float m = -INFINITY, l = 0.f;
+            for (int g = 0; g < ng; ++g, ++G) {
+                const int s = (int)(G % C::NST), sb = (int)(G & 1), pb = sb;
+                // scores of this group (the stage's masks landed with its rows)
+                if (!tc::warp_wait(&s_full[sb], (G >> 1) & 1, tc::kWaitLimit) ||
+                    !tc::warp_wait(&kv_full[s], (G / C::NST) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                float sc[kGroup];
+                {
+                    uint32_t v[32];
+                    tc::tmem_ld32(tS0 + sb * kGroup + tlane, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sc[i] = __uint_as_float(v[i]);
+                    tc::tmem_ld32(tS0 + sb * kGroup + 32 + tlane, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) sc[32 + i] = __uint_as_float(v[i]);
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&s_empty[sb]);
+                const uint16_t *mk = reinterpret_cast<const uint16_t *>(smem + C::ST0 + s * C::STB + 2 * C::KB) + r;
+                float smax = -INFINITY;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t bits = mk[q * 128];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float x = ((bits >> c) & 1u) ? sc[q * 16 + c] * scale2 : -INFINITY;
+                        sc[q * 16 + c] = x;
+                        smax = fmaxf(smax, x);
+                    }
+                }
+                const bool grow = smax > m + kLazy || (m == -INFINITY && smax > -INFINITY);
+                const float m_new = grow ? fmaxf(m, smax) : m;
+                const float alpha = exp2_diff(m, m_new);
+                if (__any_sync(SGA_FULL_MASK, grow && l > 0.f)) {
+                    // rescale this warp's O rows once the previous product is in
+                    if (!tc::warp_wait(&pv_done[(G - 1) & 1], ((G - 1) >> 1) & 1, tc::kWaitLimit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                    const float f = (grow && l > 0.f) ? alpha : 1.f;
+                    for (int cb = 0; cb < D; cb += 32) {
+                        uint32_t v[32];
+                        tc::tmem_ld32(tO + tlane + cb, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+                        tc::tmem_st32(tO + tlane + cb, v);
+                    }
+                }
+                if (grow) {
+                    l *= alpha;
+                    m = m_new;
+                }
+                float pr[kGroup];
+#pragma unroll
+                for (int i = 0; i < kGroup; ++i) {
+                    pr[i] = exp2_diff(sc[i], m);
+                    l += pr[i];
+                }
+                // P buffer pb is free once the product of two groups back is done
+                if (G >= 2 && !tc::warp_wait(&pv_done[pb], ((G - 2) >> 1) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char *prow = smem + C::P0 + pb * 128 * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(prow + tc::sw128_offset(r, c * 8, 128)) =
+                        pack<__nv_bfloat16>(pr + 8 * c);
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&p_full[pb]);
+            }
+            if (!ok) break;
+            // epilogue: the unit's last product, then merge with the residual result
+            if (!tc::warp_wait(&pv_done[(G - 1) & 1], ((G - 1) >> 1) & 1, tc::kWaitLimit)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            const bool has = l > 0.f && in;
+            float wt = 0.f, wr = 0.f, lse_new = 0.f;
+            uint4 x[D / 8];
+            if (has) {
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) x[c] = *reinterpret_cast<const uint4 *>(out + 8 * c);
+                const float lt = (m + log2f(l)) * kLn2;
+                const float M = fmaxf(lt, lr);
+                wt = __expf(lt - M);
+                wr = lr == -INFINITY ? 0.f : __expf(lr - M);
+                lse_new = M + logf(wt + wr);
+                const float inv = 1.f / (wt + wr);
+                wt *= inv / l;   // weight of the unnormalised tile accumulator
+                wr *= inv;
+            }
+#pragma unroll
+            for (int cb = 0; cb < D; cb += 32) {
+                uint32_t v[32];
+                tc::tmem_ld32(tO + tlane + cb, v);   // warp-collective: every lane takes part
+                if (has) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float o[8], y[8];
+                        unpack<__nv_bfloat16>(x[cb / 8 + q], y);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) o[i] = wt * __uint_as_float(v[8 * q + i]) + wr * y[i];
+                        *reinterpret_cast<uint4 *>(out + cb + 8 * q) = pack<__nv_bfloat16>(o);
+                    }
+                }
+            }
+            if (has) a.lse[row * H + h] = lse_new;
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&o_empty);
+        }
+        if (!ok && lane == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
+    }
+    // the MMA lane waited for all its products; the producer for its loads
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc::tmem_dealloc(tmem_base, 256);
+    }
 }
 
 template <int D> cudaError_t launch_d(const BsrArgs &a, cudaStream_t s) {
-    const BsLayout L(D);
-    // at least 100 KB: at most two CTAs (2 x 256 TMEM columns) share an SM
-    const size_t smem = L.total + 1024 > 100 * 1024 ? L.total + 1024 : 100 * 1024;
+    using C = FwdCfg<D>;
+    FwdParams prm{};
+    prm.a = a;
+    const __nv_bfloat16 *Q = static_cast<const __nv_bfloat16 *>(a.Q), *K = static_cast<const __nv_bfloat16 *>(a.K),
+                        *V = static_cast<const __nv_bfloat16 *>(a.V);
+    const int64_t HD = (int64_t)a.H * D;
+    cudaError_t e = bf16_tensor_map(&prm.tq, Q, a.N, HD, HD, 64, 128);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tk, K, a.N, HD, HD, 64, 16);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tv, V, a.N, HD, HD, 64, 16);
+    if (e != cudaSuccess) return e;
+    const size_t smem = C::BYTES + 1024;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(bsr_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+        e = cudaFuncSetAttribute(bsr_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    dim3 grid((unsigned)a.n_panels, (unsigned)a.H);
+    const int64_t units = (int64_t)a.n_active * a.H;
+    const unsigned grid = (unsigned)(units < a.num_sms ? units : a.num_sms);
     note_launch(SGA_KERN_BSR_FWD, s, false);
-    bsr_fwd_kernel<D><<<grid, kBsThreads, smem, s>>>(a);
+    bsr_fwd_kernel<D><<<grid, kThreads, smem, s>>>(prm);
     note_launch(SGA_KERN_BSR_FWD, s, true);
     return cudaGetLastError();
 }
@@ -261,7 +395,7 @@ template <int D> cudaError_t launch_d(const BsrArgs &a, cudaStream_t s) {
 bool bsr_fwd_supported(sga_dtype dt, int D) { return dt == SGA_BF16 && (D == 64 || D == 128); }
 
 cudaError_t launch_bsr_fwd(const BsrArgs &a, cudaStream_t s) {
-    if (a.n_panels == 0) return cudaSuccess;
+    if (a.n_active == 0) return cudaSuccess;
     return a.D == 128 ? launch_d<128>(a, s) : launch_d<64>(a, s);
 }
 

@@ -35,6 +35,8 @@ struct WorkspaceLayout {
     size_t delta = 0;      // [N, H] f32          Delta_i = dOut_i . out_i (normalised weights)
     size_t lse_n = 0;      // [N, H] f32          lse_i + ln Z_i (backward row normalisation)
     size_t zt = 0;         // [N, H] f32          block-sparse plans: tile part of Z_i
+    size_t bsr_lse_t = 0;  // [H, N_pad] f32      block-sparse plans: lse + ln Z, head-major
+    size_t bsr_delta_t = 0;// [H, N_pad] f32      and Delta (N_pad: N rounded up to 128)
     size_t bias_t = 0;     // [E, H] f32          edge-bias plans: the bias in transposed order
     size_t gat_colc = 0;   // [t_n_chunks, H] f32 GAT plans: source-pass chunk parts of der
     size_t fwd_ml = 0;     // [n_chunks, H, 2] f32 chunk softmax stats (max, sum), log2 units
@@ -66,7 +68,8 @@ struct TileSet {
     int64_t E_res = 0;
     int32_t *tile_ptr = nullptr;    // [n_panels + 1]
     int32_t *tile_col = nullptr;    // [n_tiles] column tile (sources 16c .. 16c+15)
-    uint16_t *tile_bits = nullptr;  // [n_tiles][128] source masks per panel row
+    uint16_t *tile_bits = nullptr;  // [n_tiles + 1][128] source masks per panel row (the last: all zero)
+    uint64_t *tile_bits_t = nullptr;// [n_tiles + 1][2][16] transposed: bit i of (t, half, c) = row 64 half + i has source c
     int32_t *r_indptr = nullptr;    // [N + 1] residual CSR
     int32_t *r_indices = nullptr;   // [E_res]
     // column view for the dK/dV pass: column panels of 128 sources (8 tile
@@ -76,6 +79,11 @@ struct TileSet {
     int32_t *ct_ptr = nullptr;      // [n_cpanels + 1]
     int32_t *ct_panel = nullptr;    // [n_entries] row panel
     int32_t *ct_tile = nullptr;     // [n_entries][8] tile index per tile column, -1: none
+    // order in which the persistent kernels take panels: by descending kept
+    // tiles (row panels) or entries (column panels), panels without any left out
+    int32_t n_active = 0, n_cactive = 0;
+    int32_t *panel_order = nullptr;   // [n_active]
+    int32_t *cpanel_order = nullptr;  // [n_cactive]
 };
 
 }  // namespace sga
@@ -190,10 +198,12 @@ struct BsrArgs {
     void *out;                  // in: residual forward, out: merged
     float *lse;                 // likewise
     const int32_t *tile_ptr, *tile_col;
-    const uint16_t *tile_bits;
+    const uint16_t *tile_bits;      // [n_tiles + 1][128]: the last tile is all zero
+    const int32_t *panel_order;     // [n_active] row panels with kept tiles, most first
     int64_t N;
     int H, D;
-    int n_panels;
+    int n_panels, n_tiles, n_active;
+    int num_sms;
     int32_t *d_err;
 };
 bool bsr_fwd_supported(sga_dtype dt, int D);
@@ -208,11 +218,16 @@ struct BsrBwdArgs {
     const float *lse_n;             // [N, H] lse + ln Z (read by the dQ and dK/dV passes)
     void *dQ, *dK, *dV;             // in: residual gradients, out: with the tile part added
     const int32_t *tile_ptr, *tile_col;
-    const uint16_t *tile_bits;
+    const uint16_t *tile_bits;      // [n_tiles + 1][128]: the last tile is all zero
+    const uint64_t *tile_bits_t;    // [n_tiles + 1][2][16] the same masks by (half, source)
     const int32_t *ct_ptr, *ct_panel, *ct_tile;
-    int64_t N;
+    const int32_t *panel_order;     // [n_active] row panels with kept tiles, most first
+    const int32_t *cpanel_order;    // [n_cactive] column panels with entries, most first
+    float *lse_t, *delta_t_hm;      // [H][N_pad] head-major copies of lse_n and delta (dK/dV pass)
+    int64_t N, N_pad;               // N_pad: N rounded up to 128
     int H, D;
-    int n_panels, n_cpanels;
+    int n_panels, n_cpanels, n_tiles, n_active, n_cactive;
+    int num_sms;
     int32_t *d_err;
 };
 // Delta pass (delta_t), dQ pass, dK/dV pass (bsr_bwd.cu).

@@ -12,6 +12,8 @@
 // atom and by one atom (R * 128 bytes) every 4 k-steps.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace sga {
@@ -156,7 +158,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *mbar, uint32_t phase, uint32
     return false;
 }
 
+// Every lane of the warp waits; the result is the warp's vote (all lanes saw
+// the phase complete), so that the warp leaves a loop as one after a timeout.
+__device__ __forceinline__ bool warp_wait(uint64_t *mbar, uint32_t phase, uint32_t limit) {
+    const bool ok = mbar_wait(mbar, phase, limit);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");
+}
+
+// Arrive once and add `bytes` to the transaction count of the current phase.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)), "r"(bytes)
+                 : "memory");
+}
+
 // ---- async copies ----------------------------------------------------------
+
+// 2-D tiled TMA load of the box at (x, y) into shared memory, completing on
+// mbar (x * element size must be a multiple of 16 bytes).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(mbar))
+        : "memory");
+}
+
+// Fetch the 128-byte line holding p into L2 (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a
+// multiple of 16), completing on mbar.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(mbar))
+                 : "memory");
+}
 
 __device__ __forceinline__ void cp16(uint32_t dst, const void *src, bool ok) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),

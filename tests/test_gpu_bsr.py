@@ -120,28 +120,114 @@ def test_block_sparse_is_deterministic_and_handles_empty_panels():
         compare(t, ref, "bf16", name)
 
 
-def test_block_sparse_rejects_repeated_edges_in_kept_tiles():
-    # row 0 lists source 3 twice; its tile (panel 0, sources 0..15) is kept
-    N = 64
-    rows = [list(range(16)) + [3]] + [list(range(16))] * (N - 1)
+def test_block_sparse_repeated_edges_join_the_residual():
+    """A mask holds a (destination, source) pair once: in a kept tile the
+    first edge of a pair sets the bit and its repeats go to the residual CSR,
+    where they add their own softmax terms; the layer equals the oracle's,
+    which counts every edge."""
+    N, H, D = 300, 2, 64
+    rng = np.random.default_rng(12)
+    rows = [list(range(16)) + [3] for _ in range(N)]       # tile (panel, sources 0..15) kept everywhere
+    rows[0] = rows[0] + [3, 40, 40]                          # source 3 three times; 40 twice (tile not kept)
+    rows[131] = [5, 5] + rows[131]
+    for i in range(N):
+        rows[i] += list(rng.integers(0, N, 3))
     indptr = np.concatenate([[0], np.cumsum([len(r) for r in rows])]).astype(np.int32)
     indices = np.concatenate(rows).astype(np.int32)
     ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
-    with pytest.raises(sga.SgaError) as ei:
-        sga.Plan(ip, ix, 1, 64, torch.bfloat16, tile_min_nnz=8)
-    assert ei.value.status == sga.SGA_EINVAL
-    # the same graph on the CSR path counts the repeat as its own edge
-    sga.Plan(ip, ix, 1, 64, torch.bfloat16)
-    # a repeat in a tile that is not kept stays in the residual CSR
-    indices2 = indices.copy()
-    indices2[16] = 40   # row 0: source 40 (tile 2, one edge) instead of the repeat
-    rows2 = indices2.tolist()
-    indices3 = np.array(rows2[:16] + [40, 40] + rows2[17:], np.int32)
-    indptr3 = indptr.copy()
-    indptr3[1:] += 1
-    ip3, ix3 = dev(torch.from_numpy(indptr3)), dev(torch.from_numpy(indices3))
-    plan = sga.Plan(ip3, ix3, 1, 64, torch.bfloat16, tile_min_nnz=8)
-    assert plan.info()["E_residual"] == 2
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, tile_min_nnz=8)
+    ref = check_tiles(plan, indptr, indices, N, 8)
+    assert plan.info()["E_residual"] == len(ref["r_indices"]) >= N + 4
+    (q, qf), (k, kf), (v, vf), (do, dof) = inputs(13, N, H, D, 0.5)
+    Q, K, V, dO = (dev(x) for x in (q, k, v, do))
+    out, lse = sga.gt_attn_fwd(plan, Q, K, V)
+    ro, rl = oracle.gt_fwd(indptr, indices, qf, kf, vf)
+    compare(out, ro, "bf16", "out")
+    compare(lse, rl, "bf16", "lse")
+    g = sga.gt_attn_bwd(plan, Q, K, V, out, lse, dO)
+    for t, r_, name in zip(g, oracle.gt_bwd(indptr, indices, qf, kf, vf, dof), ("dQ", "dK", "dV")):
+        compare(t, r_, "bf16", name)
+    assert plan.device_error() == 0
+
+
+def blocky_graph(seed, N, sizes=(16, 48, 96, 200, 384, 520), p_in=0.35, extra=2):
+    """Diagonal blocks of mixed sizes (so that panels keep from one to many
+    tiles, in groups of four with ragged last groups) plus random edges."""
+    rng = np.random.default_rng(seed)
+    dst, src = [], []
+    b0 = 0
+    while b0 < N:
+        b1 = min(N, b0 + int(rng.choice(sizes)))
+        m = rng.random((b1 - b0, b1 - b0)) < p_in
+        d, s_ = np.nonzero(m)
+        dst.append(d + b0)
+        src.append(s_ + b0)
+        b0 = b1
+    dst.append(rng.integers(0, N, extra * N))
+    src.append(rng.integers(0, N, extra * N))
+    return synth.csr_from_edges(N, np.concatenate(dst), np.concatenate(src))
+
+
+@pytest.mark.parametrize("H,D", [(4, 64), (2, 128)])
+def test_block_sparse_many_units_per_cta(H, D):
+    """More (panel, head) units than SMs, with unequal tile counts per panel:
+    every persistent CTA takes several units, so the buffers, TMEM
+    accumulators and barrier phases are handed from unit to unit."""
+    N = 24000
+    indptr, indices = blocky_graph(21, N)
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, tile_min_nnz=12)
+    ref_t = check_tiles(plan, indptr, indices, N, 12)
+    per_panel = np.diff(ref_t["tile_ptr"])
+    assert (per_panel > 0).sum() * H > 2 * 152 and per_panel.max() > 4 * 4 and (per_panel % 4 != 0).any()
+    (q, qf), (k, kf), (v, vf), (do, dof) = inputs(22, N, H, D, 1.5 * D ** -0.5)
+    Q, K, V, dO = (dev(x) for x in (q, k, v, do))
+    out, lse = sga.gt_attn_fwd(plan, Q, K, V)
+    ro, rl = oracle.gt_fwd(indptr, indices, qf, kf, vf)
+    compare(out, ro, "bf16", "out")
+    compare(lse, rl, "bf16", "lse")
+    dQ, dK, dV = sga.gt_attn_bwd(plan, Q, K, V, out, lse, dO)
+    rq, rk, rv = oracle.gt_bwd(indptr, indices, qf, kf, vf, dof)
+    compare(dQ, rq, "bf16", "dQ")
+    compare(dK, rk, "bf16", "dK")
+    compare(dV, rv, "bf16", "dV")
+    again = sga.gt_attn_bwd(plan, Q, K, V, out, lse, dO)
+    assert all(torch.equal(x, y) for x, y in zip((dQ, dK, dV), again))
+    assert plan.device_error() == 0
+
+
+def test_block_sparse_beyond_2_18_nodes():
+    """N above 2^18 (the tile extraction has no per-panel histogram limit);
+    sampled rows and sources against the oracle, tiles bit-exact."""
+    N, H, D = (1 << 18) + 3001, 2, 64
+    rng = np.random.default_rng(31)
+    dst, src = [rng.integers(0, N, 2 * N)], [rng.integers(0, N, 2 * N)]
+    for b0 in list(range(0, 4096, 256)) + [N - 300]:   # dense blocks at both ends
+        b1 = min(N, b0 + 256)
+        m = rng.random((b1 - b0, b1 - b0)) < 0.3
+        d, s_ = np.nonzero(m)
+        dst.append(d + b0)
+        src.append(s_ + b0)
+    indptr, indices = synth.csr_from_edges(N, np.concatenate(dst), np.concatenate(src))
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, tile_min_nnz=16)
+    check_tiles(plan, indptr, indices, N, 16)
+    assert plan.info()["n_tiles"] > 0
+    (q, qf), (k, kf), (v, vf), (do, dof) = inputs(32, N, H, D, D ** -0.5)
+    Q, K, V, dO = (dev(x) for x in (q, k, v, do))
+    out, lse = sga.gt_attn_fwd(plan, Q, K, V)
+    dQ, dK, dV = sga.gt_attn_bwd(plan, Q, K, V, out, lse, dO)
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([rng.integers(0, N, 500), np.arange(0, 600, 7), [N - 300, N - 1]]))
+    ro, rl = oracle.gt_fwd(indptr, indices, qf, kf, vf, rows=rows)
+    r = torch.from_numpy(rows).cuda()
+    compare(out[r], ro, "bf16", "out")
+    compare(lse[r], rl, "bf16", "lse")
+    compare(dQ[r], oracle.gt_bwd_dq_rows(indptr, indices, qf, kf, vf, dof, rows), "bf16", "dQ")
+    rk, rv = oracle.gt_bwd_dkdv_srcs(indptr, indices, qf, kf, vf, dof, rows)
+    compare(dK[r], rk, "bf16", "dK")
+    compare(dV[r], rv, "bf16", "dV")
+    assert plan.device_error() == 0
 
 
 def test_block_sparse_rejects_unsupported_shapes():

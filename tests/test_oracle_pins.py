@@ -491,6 +491,52 @@ def test_tile_extract_by_brute_force():
     assert sum(bin(int(b)).count("1") for b in t["tile_bits"].ravel()) + len(t["r_indices"]) == len(indices)
 
 
+def test_tile_extract_repeated_edges_by_brute_force():
+    """Repeated (destination, source) pairs: counted towards the tile's
+    threshold; in a kept tile the first occurrence in CSR order sets the mask
+    bit and every later one stays in the residual, in CSR order; in a tile
+    that is not kept all of them stay.  Checked by an explicit edge loop."""
+    rng = np.random.default_rng(32)
+    N = 300
+    rows = [list(rng.integers(0, N, rng.integers(0, 5))) for _ in range(N)]
+    for i in range(128, 190):            # a dense block: kept tiles over sources 32..63
+        rows[i] = list(rng.permutation(np.arange(32, 64)))
+    rows[130] = rows[130][:5] + [40, 40] + rows[130][5:] + [40]   # source 40 four times in a kept tile
+    rows[200] = [7, 7, 7, 250]                                    # repeats in a tile that is not kept
+    rows[129] = rows[129] + [33]
+    indptr = np.zeros(N + 1, np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in rows])
+    indices = np.array([j for r in rows for j in r], np.int32)
+    t = oracle.tile_extract(indptr, indices, N, min_nnz=20)
+    counts = {}
+    for i in range(N):
+        for e in range(indptr[i], indptr[i + 1]):
+            k = (i // 128, indices[e] // 16)
+            counts[k] = counts.get(k, 0) + 1
+    kept = sorted(k for k, c in counts.items() if c >= 20)
+    got = [(p, c) for p in range(len(t["tile_ptr"]) - 1)
+           for c in t["tile_col"][t["tile_ptr"][p]:t["tile_ptr"][p + 1]]]
+    assert got == kept and len(kept) > 0
+    bits = np.zeros_like(t["tile_bits"])
+    res_rows = [[] for _ in range(N)]
+    n_rep = 0
+    for i in range(N):
+        seen = set()
+        for e in range(indptr[i], indptr[i + 1]):
+            j = int(indices[e])
+            k = (i // 128, j // 16)
+            if k in kept and j not in seen:
+                bits[kept.index(k), i % 128] |= np.uint16(1 << (j % 16))
+            else:
+                n_rep += k in kept
+                res_rows[i].append(j)
+            seen.add(j)
+    assert n_rep == 4    # row 130: three repeats of 40; row 129: 33 once more
+    np.testing.assert_array_equal(t["tile_bits"], bits)
+    assert [list(t["r_indices"][t["r_indptr"][i]:t["r_indptr"][i + 1]]) for i in range(N)] == res_rows
+    assert sum(bin(int(b)).count("1") for b in t["tile_bits"].ravel()) + len(t["r_indices"]) == len(indices)
+
+
 # ------------------------------------------------------- min / max aggregation
 
 def test_agg_hand_example():
