@@ -430,7 +430,7 @@ sga_status gt_attn_fwd(const sga_plan *p, const int32_t *indptr, const int32_t *
         b.tile_ptr = p->tiles.tile_ptr;
         b.tile_col = p->tiles.tile_col;
         b.tile_bits = p->tiles.tile_bits;
-        b.panel_order = p->tiles.panel_order;
+        b.panel_info = p->tiles.panel_info;
         b.N = N;
         b.H = H;
         b.D = D;
@@ -491,8 +491,8 @@ sga_status gt_attn_bwd(const sga_plan *p, const int32_t *indptr, const int32_t *
         b.ct_panel = p->tiles.ct_panel;
         b.ct_tile = p->tiles.ct_tile;
         b.tile_bits_t = p->tiles.tile_bits_t;
-        b.panel_order = p->tiles.panel_order;
-        b.cpanel_order = p->tiles.cpanel_order;
+        b.panel_info = p->tiles.panel_info;
+        b.cpanel_info = p->tiles.cpanel_info;
         b.lse_t = ws_at<float>(p, p->layout.bsr_lse_t);
         b.delta_t_hm = ws_at<float>(p, p->layout.bsr_delta_t);
         b.N = N;

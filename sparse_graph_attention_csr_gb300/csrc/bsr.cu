@@ -346,11 +346,15 @@ sga_status bsr_build(sga_plan *p, cudaStream_t s) {
     const std::vector<int32_t> p_order = work_order(h_ptr), c_order = work_order(c_ptr);
     T.n_active = (int32_t)p_order.size();
     T.n_cactive = (int32_t)c_order.size();
+    std::vector<int4> p_info(T.n_active), c_info(T.n_cactive);
+    for (int32_t k = 0; k < T.n_active; ++k) p_info[k] = make_int4(p_order[k], h_ptr[p_order[k]], h_ptr[p_order[k] + 1], 0);
+    for (int32_t k = 0; k < T.n_cactive; ++k)
+        c_info[k] = make_int4(c_order[k], c_ptr[c_order[k]], c_ptr[c_order[k] + 1], 0);
     BSR_TRY(alloc((void **)&T.ct_ptr, sizeof(int32_t) * (T.n_cpanels + 1), true));
     BSR_TRY(alloc((void **)&T.ct_panel, sizeof(int32_t) * T.n_entries, true));
     BSR_TRY(alloc((void **)&T.ct_tile, sizeof(int32_t) * 8 * (size_t)T.n_entries, true));
-    BSR_TRY(alloc((void **)&T.panel_order, sizeof(int32_t) * T.n_active, true));
-    BSR_TRY(alloc((void **)&T.cpanel_order, sizeof(int32_t) * T.n_cactive, true));
+    BSR_TRY(alloc((void **)&T.panel_info, sizeof(int4) * T.n_active, true));
+    BSR_TRY(alloc((void **)&T.cpanel_info, sizeof(int4) * T.n_cactive, true));
     BSR_TRY(cudaMemcpy(T.ct_ptr, c_ptr.data(), sizeof(int32_t) * (T.n_cpanels + 1), cudaMemcpyHostToDevice));
     if (T.n_entries > 0) {
         BSR_TRY(cudaMemcpy(T.ct_panel, c_panel.data(), sizeof(int32_t) * T.n_entries, cudaMemcpyHostToDevice));
@@ -358,9 +362,9 @@ sga_status bsr_build(sga_plan *p, cudaStream_t s) {
                            cudaMemcpyHostToDevice));
     }
     if (T.n_active > 0)
-        BSR_TRY(cudaMemcpy(T.panel_order, p_order.data(), sizeof(int32_t) * T.n_active, cudaMemcpyHostToDevice));
+        BSR_TRY(cudaMemcpy(T.panel_info, p_info.data(), sizeof(int4) * T.n_active, cudaMemcpyHostToDevice));
     if (T.n_cactive > 0)
-        BSR_TRY(cudaMemcpy(T.cpanel_order, c_order.data(), sizeof(int32_t) * T.n_cactive, cudaMemcpyHostToDevice));
+        BSR_TRY(cudaMemcpy(T.cpanel_info, c_info.data(), sizeof(int4) * T.n_cactive, cudaMemcpyHostToDevice));
 #undef BSR_TRY
     return SGA_OK;
 }

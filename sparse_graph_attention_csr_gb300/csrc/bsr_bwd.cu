@@ -13,8 +13,9 @@
 // Three passes, each a persistent kernel (one CTA per SM) with the same
 // roles as the forward: warp 0 one lane issues TMA loads into a ring of
 // stages, warp 1 one lane issues the MMAs (fp32 accumulators in TMEM), warps
-// 2-5 (thread = TMEM lane) turn the products into weights and gradients;
-// every handoff is an mbarrier and every wait is bounded.
+// 2-9 (thread = TMEM lane, two warps per lane quarter, each taking half of a
+// group's columns) turn the products into weights and gradients; every
+// handoff is an mbarrier and every wait is bounded.
 //   Delta pass (units: row panel x head, groups of four kept tiles = 64
 //     sources): S = Q K^T, dP = dOut V^T into two TMEM buffers (the next
 //     group's products run while the current one is reduced); the row sums
@@ -46,8 +47,9 @@
 namespace sga {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kGroup = 64;   // sources per group of the row passes (four tiles)
+constexpr int kThreads = 320;   // producer, MMA lane, eight weight warps
+constexpr int kSoft = 8;        // weight warps: arrivals per handoff
+constexpr int kGroup = 64;      // sources per group of the row passes (four tiles)
 
 // Four k-steps over 64 node rows (K = 64): A K-major (one 64-wide atom of the
 // A tile), B the 64 node rows x N columns as an MN-major operand.
@@ -79,8 +81,8 @@ __device__ __forceinline__ void split_bf16x8(const float *x, uint4 &hi, uint4 &l
     lo = pack<__nv_bfloat16>(r);
 }
 
-// Add an fp32 row (from TMEM, times `scale`) to a bf16 row of D values: the
-// row's current values are loaded first, all at once (one round trip).
+// Add an fp32 row (from TMEM, times `scale`) to NCOL bf16 values: the row's
+// current values are loaded first, all at once (one round trip).
 template <int D>
 __device__ __forceinline__ void add_row_from_tmem(uint32_t taddr, __nv_bfloat16 *dst, float scale, bool has) {
     uint4 x[D / 8];
@@ -153,15 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
             tc::mbar_init(&q_full[i], 1);
             tc::mbar_init(&q_empty[i], 1);
             tc::mbar_init(&s_full[i], 1);
-            tc::mbar_init(&s_empty[i], 4);
+            tc::mbar_init(&s_empty[i], kSoft);
         }
         for (int i = 0; i < C::NST; ++i) {
             tc::mbar_init(&kv_full[i], 1);
             tc::mbar_init(&kv_empty[i], 1);
         }
-        tc::mbar_init(&ds_full, 4);
+        tc::mbar_init(&ds_full, kSoft);
         tc::mbar_init(&ds_empty, 1);
-        tc::mbar_init(&acc_empty, 4);
+        tc::mbar_init(&acc_empty, kSoft);
         tc::mbar_init(&mma_done, 1);
     }
     tc::fence_before_sync();
@@ -174,10 +176,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
         if (lane == 0) {   // ------------------------------------------------ TMA producer
             int64_t G = 0, U = 0;
             bool ok = true;
+            int4 nfo = tc::unit_info(a.panel_info, blockIdx.x, n_units, H);
             for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
-                const int32_t panel = a.panel_order[u / H];
+                const int4 cur = nfo;
+                nfo = tc::unit_info(a.panel_info, u + gridDim.x, n_units, H);
+                const int32_t panel = cur.x, t0 = cur.y, t1 = cur.z;
                 const int h = (int)(u % H);
-                const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
                 const int ng = (t1 - t0 + 3) / 4;
                 const int qb = (int)(U % C::NQ);
                 const int64_t nq = U / C::NQ;
@@ -194,6 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
                 for (int g = 0; g < ng; ++g, ++G) {
                     const int s = (int)(G % C::NST);
                     const int64_t n = G / C::NST;
+                    int ys[4];   // first source of each tile (loaded before the wait; past N: zero rows)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int32_t ti = t0 + 4 * g + q;
+                        ys[q] = ti < t1 ? __ldg(a.tile_col + ti) * 16 : (int)a.N;
+                    }
                     if (n >= 1 && !tc::mbar_wait(&kv_empty[s], (n - 1) & 1, tc::kWaitLimit)) {
                         ok = false;
                         break;
@@ -201,8 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
                     const uint32_t st = sbase + C::ST0 + s * 2 * C::KB;
                     tc::mbar_expect_tx(&kv_full[s], 2 * C::KB);
                     for (int q = 0; q < 4; ++q) {
-                        const int32_t ti = t0 + 4 * g + q;
-                        const int y = ti < t1 ? a.tile_col[ti] * 16 : (int)a.N;   // past N: zero rows
+                        const int y = ys[q];
                         for (int at = 0; at < C::DA; ++at) {
                             const uint32_t off = at * kGroup * 128 + q * 16 * 128;
                             tc::tma_load_2d(st + off, &prm.tk, h * D + at * 64, y, &kv_full[s]);
@@ -239,9 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
             };
             int64_t pend = -1, pend_u = 0;
             bool pend_first = false;
+            int4 nfo = tc::unit_info(a.panel_info, blockIdx.x, n_units, H);
             for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
-                const int32_t panel = a.panel_order[u / H];
-                const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
+                const int4 cur = nfo;
+                nfo = tc::unit_info(a.panel_info, u + gridDim.x, n_units, H);
+                const int32_t t0 = cur.y, t1 = cur.z;
                 const int ng = (t1 - t0 + 3) / 4;
                 const int qb = (int)(U % C::NQ);
                 if (!tc::mbar_wait(&q_full[qb], (U / C::NQ) & 1, tc::kWaitLimit)) {
@@ -280,15 +291,18 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
             tc::mbar_wait(&mma_done, 0, tc::kWaitLimit);
         }
     } else {   // ---------------------------------------------------- weights and gradients
-        const int quarter = warp & 3, r = quarter * 32 + lane;
+        const int quarter = warp & 3, hf = (warp - 2) >> 2, r = quarter * 32 + lane;   // half hf: sources 32 hf ..
         const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
         const float scale2 = kLog2e * rsqrtf((float)D);
+        constexpr int DH = D / 2;   // dQ columns this warp adds
         int64_t G = 0, U = 0;
         bool ok = true;
+        int4 nfo = tc::unit_info(a.panel_info, blockIdx.x, n_units, H);
         for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
-            const int32_t panel = a.panel_order[u / H];
+            const int4 cur = nfo;
+            nfo = tc::unit_info(a.panel_info, u + gridDim.x, n_units, H);
+            const int32_t panel = cur.x, t0 = cur.y, t1 = cur.z;
             const int h = (int)(u % H);
-            const int32_t t0 = a.tile_ptr[panel], t1 = a.tile_ptr[panel + 1];
             const int ng = (t1 - t0 + 3) / 4;
             const int64_t row = (int64_t)panel * 128 + r;
             const bool in = row < a.N;
@@ -296,14 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
             // the dQ pass uses the normalised lse + ln Z and Delta = C / Z of the row
             const float lse2 = in ? (MODE == 0 ? a.lse : a.lse_n)[row * H + h] * kLog2e : 0.f;
             const float dl = (MODE == 1 && in) ? a.delta[row * H + h] : 0.f;
-            if (MODE == 1 && in) prefetch_row<D>(static_cast<const __nv_bfloat16 *>(a.dQ) + (row * H + h) * D);
-            float dsum = 0.f, zsum = 0.f;
+            __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dQ) + ((in ? row : 0) * H + h) * D + hf * DH;
+            if (MODE == 1 && in) prefetch_row<DH>(dq);
+            float ps[2] = {0.f, 0.f}, zs[2] = {0.f, 0.f};
             for (int g = 0; g < ng; ++g, ++G) {
                 const int sb = (int)(G & 1);
-                uint32_t bits[4];   // this row's source masks of the group (zero tile for missing ones)
+                uint32_t bits[2];   // this row's source masks of the half's two tiles (zero tile for missing ones)
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int32_t ti = t0 + 4 * g + q;
+                for (int q = 0; q < 2; ++q) {
+                    const int32_t ti = t0 + 4 * g + 2 * hf + q;
                     bits[q] = a.tile_bits[(size_t)(ti < t1 ? ti : a.n_tiles) * 128 + r];
                 }
                 if (!tc::warp_wait(&s_full[sb], (G >> 1) & 1, tc::kWaitLimit) ||
@@ -312,33 +327,29 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
                     break;
                 }
                 tc::fence_after_sync();
+                uint32_t us[32], up[32];
+                tc::tmem_ld32(tbase + sb * 128 + hf * 32 + tlane, us);
+                tc::tmem_ld32(tbase + sb * 128 + 64 + hf * 32 + tlane, up);
+                float ds[32];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t us[32], up[32];
-                    tc::tmem_ld32(tbase + sb * 128 + tlane + half * 32, us);
-                    tc::tmem_ld32(tbase + sb * 128 + 64 + tlane + half * 32, up);
-                    float ds[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int c = half * 32 + i;
-                        const bool on = (bits[c >> 4] >> (c & 15)) & 1u;
-                        const float p = on ? exp2f(__uint_as_float(us[i]) * scale2 - lse2) : 0.f;
-                        const float dp = __uint_as_float(up[i]);
-                        if (MODE == 0) {
-                            dsum = fmaf(p, dp, dsum);
-                            zsum += p;
-                        }
-                        ds[i] = p * (dp - dl);
+                for (int i = 0; i < 32; ++i) {
+                    const bool on = (bits[i >> 4] >> (i & 15)) & 1u;
+                    const float p = on ? tc::ex2(__uint_as_float(us[i]) * scale2 - lse2) : 0.f;
+                    const float dp = __uint_as_float(up[i]);
+                    if (MODE == 0) {
+                        ps[i & 1] = fmaf(p, dp, ps[i & 1]);
+                        zs[i & 1] += p;
                     }
-                    if (MODE == 1) {
+                    ds[i] = p * (dp - dl);
+                }
+                if (MODE == 1) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const uint32_t o = tc::sw128_offset(r, half * 32 + c * 8, 128);
-                            uint4 hi, lo;
-                            split_bf16x8(ds + 8 * c, hi, lo);
-                            *reinterpret_cast<uint4 *>(smem + C::DS0 + o) = hi;
-                            *reinterpret_cast<uint4 *>(smem + C::DS0 + 128 * 128 + o) = lo;
-                        }
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t o = tc::sw128_offset(r, hf * 32 + c * 8, 128);
+                        uint4 hi, lo;
+                        split_bf16x8(ds + 8 * c, hi, lo);
+                        *reinterpret_cast<uint4 *>(smem + C::DS0 + o) = hi;
+                        *reinterpret_cast<uint4 *>(smem + C::DS0 + 128 * 128 + o) = lo;
                     }
                 }
                 tc::fence_before_sync();
@@ -351,19 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
             }
             if (!ok) break;
             if (MODE == 0) {
+                // the two halves' sums of the row added to the zeroed outputs: with two
+                // terms onto zero, either order rounds to the same fl(a + b)
                 if (in) {
-                    a.delta_t[row * H + h] = dsum;
-                    a.z_t[row * H + h] = zsum;
+                    atomicAdd(a.delta_t + row * H + h, ps[0] + ps[1]);
+                    atomicAdd(a.z_t + row * H + h, zs[0] + zs[1]);
                 }
             } else {
-                // the unit's last dQ product, then add the tile part to dQ
+                // the unit's last dQ product, then add this half of the tile part to dQ
                 if (!tc::warp_wait(&ds_empty, (G - 1) & 1, tc::kWaitLimit)) {
                     ok = false;
                     break;
                 }
                 tc::fence_after_sync();
-                __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dQ) + ((in ? row : 0) * H + h) * D;
-                add_row_from_tmem<D>(tQ + tlane, dq, rsqrtf((float)D), in);
+                add_row_from_tmem<DH>(tQ + hf * DH + tlane, dq, rsqrtf((float)D), in);
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&acc_empty);
@@ -426,15 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
         tc::mbar_init(&c_empty, 1);
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&s_full[i], 1);
-            tc::mbar_init(&s_empty[i], 4);
+            tc::mbar_init(&s_empty[i], kSoft);
         }
         for (int i = 0; i < C::NST; ++i) {
             tc::mbar_init(&kv_full[i], 1);
             tc::mbar_init(&kv_empty[i], 1);
         }
-        tc::mbar_init(&pd_full, 4);
+        tc::mbar_init(&pd_full, kSoft);
         tc::mbar_init(&pd_empty, 1);
-        tc::mbar_init(&acc_empty, 4);
+        tc::mbar_init(&acc_empty, kSoft);
         tc::mbar_init(&mma_done, 1);
     }
     tc::fence_before_sync();
@@ -447,10 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
         if (lane == 0) {   // ------------------------------------------------ TMA producer
             int64_t B = 0, U = 0;
             bool ok = true;
+            int4 nfo = tc::unit_info(a.cpanel_info, blockIdx.x, n_units, H);
             for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
-                const int32_t cp = a.cpanel_order[u / H];
+                const int4 cur = nfo;
+                nfo = tc::unit_info(a.cpanel_info, u + gridDim.x, n_units, H);
+                const int32_t cp = cur.x, e0 = cur.y, e1 = cur.z;
                 const int h = (int)(u % H);
-                const int32_t e0 = a.ct_ptr[cp], e1 = a.ct_ptr[cp + 1];
                 const int nb = 2 * (e1 - e0);   // blocks: (entry, 64-row half)
                 if (U >= 1 && !tc::mbar_wait(&c_empty, (U - 1) & 1, tc::kWaitLimit)) {
                     ok = false;
@@ -465,13 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
                 for (int b = 0; b < nb; ++b, ++B) {
                     const int s = (int)(B % C::NST);
                     const int64_t n = B / C::NST;
+                    // the block's row panel and tiles (loaded before the wait)
+                    const int32_t e = e0 + b / 2;
+                    const int hf = b & 1;
+                    const int row0 = __ldg(a.ct_panel + e) * 128 + hf * 64;
+                    const int4 ta = __ldg(reinterpret_cast<const int4 *>(a.ct_tile) + 2 * e);
+                    const int4 tb = __ldg(reinterpret_cast<const int4 *>(a.ct_tile) + 2 * e + 1);
+                    const int32_t tiles[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
                     if (n >= 1 && !tc::mbar_wait(&kv_empty[s], (n - 1) & 1, tc::kWaitLimit)) {
                         ok = false;
                         break;
                     }
-                    const int32_t e = e0 + b / 2;
-                    const int hf = b & 1;
-                    const int row0 = a.ct_panel[e] * 128 + hf * 64;
                     const uint32_t st = sbase + C::ST0 + s * C::STB;
                     tc::mbar_expect_tx(&kv_full[s], C::TX);
                     for (int at = 0; at < C::DA; ++at) {
@@ -479,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
                         tc::tma_load_2d(st + C::HB + at * 64 * 128, &prm.tg, h * D + at * 64, row0, &kv_full[s]);
                     }
                     for (int t = 0; t < 8; ++t) {   // the 8 tile columns' masks of the 64 rows, transposed
-                        const int32_t tile = a.ct_tile[(size_t)e * 8 + t];
+                        const int32_t tile = tiles[t];
                         tc::bulk_load(st + 2 * C::HB + t * 128,
                                       a.tile_bits_t + ((size_t)(tile >= 0 ? tile : a.n_tiles) * 2 + hf) * 16, 128,
                                       &kv_full[s]);
@@ -516,9 +534,11 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
             };
             int64_t pend = -1, pend_u = 0;
             bool pend_first = false;
+            int4 nfo = tc::unit_info(a.cpanel_info, blockIdx.x, n_units, H);
             for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
-                const int32_t cp = a.cpanel_order[u / H];
-                const int nb = 2 * (a.ct_ptr[cp + 1] - a.ct_ptr[cp]);
+                const int4 cur = nfo;
+                nfo = tc::unit_info(a.cpanel_info, u + gridDim.x, n_units, H);
+                const int nb = 2 * (cur.z - cur.y);
                 if (!tc::mbar_wait(&c_full, U & 1, tc::kWaitLimit)) {
                     ok = false;
                     break;
@@ -551,21 +571,24 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
             tc::mbar_wait(&mma_done, 0, tc::kWaitLimit);
         }
     } else {   // ---------------------------------------------------- weights and gradients
-        const int quarter = warp & 3, r = quarter * 32 + lane;   // source of the column panel
+        // thread = source of the column panel (TMEM lane); half hf: destination rows 32 hf ..
+        // of each block, and at the end of the unit dK (hf 0) or dV (hf 1)
+        const int quarter = warp & 3, hf = (warp - 2) >> 2, r = quarter * 32 + lane;
         const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
         const float scale2 = kLog2e * rsqrtf((float)D);
         int64_t B = 0, U = 0;
         bool ok = true;
+        int4 nfo = tc::unit_info(a.cpanel_info, blockIdx.x, n_units, H);
         for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
-            const int32_t cp = a.cpanel_order[u / H];
+            const int4 cur = nfo;
+            nfo = tc::unit_info(a.cpanel_info, u + gridDim.x, n_units, H);
+            const int32_t cp = cur.x;
             const int h = (int)(u % H);
-            const int nb = 2 * (a.ct_ptr[cp + 1] - a.ct_ptr[cp]);
+            const int nb = 2 * (cur.z - cur.y);
             const int64_t src = (int64_t)cp * 128 + r;
             const bool in = src < a.N;
-            if (in) {
-                prefetch_row<D>(static_cast<const __nv_bfloat16 *>(a.dK) + (src * H + h) * D);
-                prefetch_row<D>(static_cast<const __nv_bfloat16 *>(a.dV) + (src * H + h) * D);
-            }
+            __nv_bfloat16 *grad = static_cast<__nv_bfloat16 *>(hf == 0 ? a.dK : a.dV) + ((in ? src : 0) * H + h) * D;
+            if (in) prefetch_row<D>(grad);
             for (int b = 0; b < nb; ++b, ++B) {
                 const int s = (int)(B % C::NST), sb = (int)(B & 1);
                 // products, the stage's masks and row terms, and a free P / dS buffer
@@ -577,38 +600,36 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
                 }
                 tc::fence_after_sync();
                 const unsigned char *st = smem + C::ST0 + s * C::STB;
-                // this source's 64 row bits of the block (transposed masks: word r)
-                const uint64_t m64 = in ? reinterpret_cast<const uint64_t *>(st + 2 * C::HB)[r] : 0ull;
-                const float4 *lse4 = reinterpret_cast<const float4 *>(st + 2 * C::HB + 1024);
-                const float4 *dl4 = reinterpret_cast<const float4 *>(st + 2 * C::HB + 1280);
+                // this source's bits for the half's 32 rows (transposed masks: word r)
+                const uint32_t m32 =
+                    in ? (uint32_t)(reinterpret_cast<const uint64_t *>(st + 2 * C::HB)[r] >> (32 * hf)) : 0u;
+                const float4 *lse4 = reinterpret_cast<const float4 *>(st + 2 * C::HB + 1024) + hf * 8;
+                const float4 *dl4 = reinterpret_cast<const float4 *>(st + 2 * C::HB + 1280) + hf * 8;
+                uint32_t us[32], up[32];
+                tc::tmem_ld32(tbase + sb * 128 + hf * 32 + tlane, us);
+                tc::tmem_ld32(tbase + sb * 128 + 64 + hf * 32 + tlane, up);
+                float pv[32], ds[32];
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t us[32], up[32];
-                    tc::tmem_ld32(tbase + sb * 128 + tlane + half * 32, us);
-                    tc::tmem_ld32(tbase + sb * 128 + 64 + tlane + half * 32, up);
-                    float pv[32], ds[32];
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float4 l4 = lse4[i4], d4 = dl4[i4];
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-                    for (int i4 = 0; i4 < 8; ++i4) {
-                        const float4 l4 = lse4[half * 8 + i4], d4 = dl4[half * 8 + i4];
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int ii = i4 * 4 + k, i = half * 32 + ii;
-                            const bool on = (m64 >> i) & 1ull;
-                            const float p = on ? exp2f(__uint_as_float(us[ii]) * scale2 - lv[k] * kLog2e) : 0.f;
-                            pv[ii] = p;
-                            ds[ii] = p * (__uint_as_float(up[ii]) - dv[k]);
-                        }
+                    for (int k = 0; k < 4; ++k) {
+                        const int ii = i4 * 4 + k;
+                        const bool on = (m32 >> ii) & 1u;
+                        const float p = on ? tc::ex2(__uint_as_float(us[ii]) * scale2 - lv[k] * kLog2e) : 0.f;
+                        pv[ii] = p;
+                        ds[ii] = p * (__uint_as_float(up[ii]) - dv[k]);
                     }
+                }
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const uint32_t o = tc::sw128_offset(r, half * 32 + c * 8, 128);
-                        uint4 hi, lo;
-                        split_bf16x8(ds + 8 * c, hi, lo);
-                        *reinterpret_cast<uint4 *>(smem + C::PD0 + o) = pack<__nv_bfloat16>(pv + 8 * c);
-                        *reinterpret_cast<uint4 *>(smem + C::PD0 + 128 * 128 + o) = hi;
-                        *reinterpret_cast<uint4 *>(smem + C::PD0 + 2 * 128 * 128 + o) = lo;
-                    }
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t o = tc::sw128_offset(r, hf * 32 + c * 8, 128);
+                    uint4 hi, lo;
+                    split_bf16x8(ds + 8 * c, hi, lo);
+                    *reinterpret_cast<uint4 *>(smem + C::PD0 + o) = pack<__nv_bfloat16>(pv + 8 * c);
+                    *reinterpret_cast<uint4 *>(smem + C::PD0 + 128 * 128 + o) = hi;
+                    *reinterpret_cast<uint4 *>(smem + C::PD0 + 2 * 128 * 128 + o) = lo;
                 }
                 tc::fence_before_sync();
                 tc::fence_proxy_async();
@@ -619,15 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
                 }
             }
             if (!ok) break;
-            // the unit's last products, then add the tile parts to dK and dV
+            // the unit's last products, then add the tile part to dK (hf 0) or dV (hf 1)
             if (!tc::warp_wait(&pd_empty, (B - 1) & 1, tc::kWaitLimit)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            const size_t off = ((size_t)(in ? src : 0) * H + h) * D;
-            add_row_from_tmem<D>(tK + tlane, static_cast<__nv_bfloat16 *>(a.dK) + off, rsqrtf((float)D), in);
-            add_row_from_tmem<D>(tV + tlane, static_cast<__nv_bfloat16 *>(a.dV) + off, 1.f, in);
+            add_row_from_tmem<D>((hf == 0 ? tK : tV) + tlane, grad, hf == 0 ? rsqrtf((float)D) : 1.f, in);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty);

@@ -82,8 +82,8 @@ struct TileSet {
     // order in which the persistent kernels take panels: by descending kept
     // tiles (row panels) or entries (column panels), panels without any left out
     int32_t n_active = 0, n_cactive = 0;
-    int32_t *panel_order = nullptr;   // [n_active]
-    int32_t *cpanel_order = nullptr;  // [n_cactive]
+    int4 *panel_info = nullptr;       // [n_active] (row panel, first tile, end tile, 0)
+    int4 *cpanel_info = nullptr;      // [n_cactive] (column panel, first entry, end entry, 0)
 };
 
 }  // namespace sga
@@ -199,7 +199,7 @@ struct BsrArgs {
     float *lse;                 // likewise
     const int32_t *tile_ptr, *tile_col;
     const uint16_t *tile_bits;      // [n_tiles + 1][128]: the last tile is all zero
-    const int32_t *panel_order;     // [n_active] row panels with kept tiles, most first
+    const int4 *panel_info;         // [n_active] (row panel, first tile, end tile, 0), most tiles first
     int64_t N;
     int H, D;
     int n_panels, n_tiles, n_active;
@@ -221,8 +221,8 @@ struct BsrBwdArgs {
     const uint16_t *tile_bits;      // [n_tiles + 1][128]: the last tile is all zero
     const uint64_t *tile_bits_t;    // [n_tiles + 1][2][16] the same masks by (half, source)
     const int32_t *ct_ptr, *ct_panel, *ct_tile;
-    const int32_t *panel_order;     // [n_active] row panels with kept tiles, most first
-    const int32_t *cpanel_order;    // [n_cactive] column panels with entries, most first
+    const int4 *panel_info;         // [n_active] (row panel, first tile, end tile, 0), most tiles first
+    const int4 *cpanel_info;        // [n_cactive] (column panel, first entry, end entry, 0), most first
     float *lse_t, *delta_t_hm;      // [H][N_pad] head-major copies of lse_n and delta (dK/dV pass)
     int64_t N, N_pad;               // N_pad: N rounded up to 128
     int H, D;

@@ -186,10 +186,40 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// 2^x by the MUFU instruction (ex2.approx.ftz: relative error about 2^-22,
+// subnormal results flushed to zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// 2^(a - m), zero for a = -inf (also when m = -inf)
+__device__ __forceinline__ float ex2_diff(float a, float m) { return a == -INFINITY ? 0.0f : ex2(a - m); }
+
+// Work unit u of a persistent block-sparse kernel: units are (panel, head)
+// pairs, panels taken from a list of (panel, first, end, 0) records; past the
+// last unit, zeros.  Loaded one unit ahead by every role.
+__device__ __forceinline__ int4 unit_info(const int4 *info, int64_t u, int64_t n_units, int H) {
+    return u < n_units ? __ldg(info + u / H) : make_int4(0, 0, 0, 0);
+}
+
 // Fetch the 128-byte line holding p into L2 (no register, no wait).
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+
+// 2-D tiled TMA store of the box at (x, y) from shared memory (bulk group of
+// the issuing thread; rows past the tensor are not written).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until this thread's committed bulk stores have read their shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until this thread's committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Untiled bulk copy global -> shared (both addresses 16-byte aligned, bytes a
 // multiple of 16), completing on mbar.
