@@ -105,6 +105,27 @@ __device__ __forceinline__ void add_row_from_tmem(uint32_t taddr, __nv_bfloat16 
     }
 }
 
+// Add an fp32 row (from TMEM, times `scale`) to the NCOL bf16 values of one
+// row of a staged TMA box (128-byte rows, 16-byte chunks swizzled by the row
+// index mod 8); every lane takes part in the TMEM loads.
+template <int NCOL>
+__device__ __forceinline__ void add_box_from_tmem(uint32_t taddr, unsigned char *box_row, int row, float scale) {
+#pragma unroll
+    for (int cb = 0; cb < NCOL; cb += 32) {
+        uint32_t u[32];
+        tc::tmem_ld32(taddr + cb, u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint4 *ptr = reinterpret_cast<uint4 *>(box_row + (((cb / 8 + q) ^ (row & 7)) << 4));
+            float o[8], y[8];
+            unpack<__nv_bfloat16>(*ptr, y);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = y[i] + scale * __uint_as_float(u[8 * q + i]);
+            *ptr = pack<__nv_bfloat16>(o);
+        }
+    }
+}
+
 // L2 prefetch of a bf16 row of D values (read again at the end of the unit).
 template <int D> __device__ __forceinline__ void prefetch_row(const __nv_bfloat16 *row) {
 #pragma unroll
@@ -124,12 +145,17 @@ template <int D, int MODE> struct RowCfg {
     static constexpr uint32_t Q0 = 0;                    // buffer b: Q, then dOut
     static constexpr uint32_t ST0 = Q0 + NQ * 2 * PB;    // stage s: K, then V
     static constexpr uint32_t DS0 = ST0 + NST * 2 * KB;  // dQ pass: dS hi, dS lo (128 x 64 bf16 each)
-    static constexpr uint32_t BYTES = DS0 + (MODE == 1 ? 2 * 128 * 128 : 0);
+    // dQ pass, D = 128: each weight warp stages its 32 rows x 64 dQ columns
+    // (one 128-byte-swizzled TMA box) for a bulk read-modify-write
+    static constexpr bool STAGE = MODE == 1 && D == 128;
+    static constexpr uint32_t O0 = DS0 + (MODE == 1 ? 2 * 128 * 128 : 0);
+    static constexpr uint32_t BYTES = O0 + (STAGE ? 8 * 4096 : 0);
     static constexpr uint32_t TCOLS = MODE == 1 ? 512 : 256;   // S, dP (x2), dQ
 };
 
 struct RowParams {
     CUtensorMap tq, tg, tk, tv;   // [N][H*D] bf16: Q, dOut boxes 64 x 128; K, V boxes 64 x 16
+    CUtensorMap to;               // dQ [N][H*D] bf16, box 64 x 32 (one weight warp's rows and columns)
     BsrBwdArgs a;
 };
 
@@ -142,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t q_full[2], q_empty[2], kv_full[C::NST], kv_empty[C::NST], s_full[2], s_empty[2], ds_full,
-        ds_empty, acc_empty, mma_done;
+        ds_empty, acc_empty, mma_done, st_full[8];
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = tc::smem_u32(smem);
@@ -165,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
         tc::mbar_init(&ds_empty, 1);
         tc::mbar_init(&acc_empty, kSoft);
         tc::mbar_init(&mma_done, 1);
+        for (int i = 0; i < 8; ++i) tc::mbar_init(&st_full[i], 1);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -311,7 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
             const float lse2 = in ? (MODE == 0 ? a.lse : a.lse_n)[row * H + h] * kLog2e : 0.f;
             const float dl = (MODE == 1 && in) ? a.delta[row * H + h] : 0.f;
             __nv_bfloat16 *dq = static_cast<__nv_bfloat16 *>(a.dQ) + ((in ? row : 0) * H + h) * D + hf * DH;
-            if (MODE == 1 && in) prefetch_row<DH>(dq);
+            const uint32_t stg = sbase + C::O0 + (warp - 2) * 4096;   // (STAGE) this warp's box
+            if constexpr (C::STAGE) {
+                if (lane == 0) {
+                    if (U >= 1) tc::bulk_wait_read();   // the previous unit's store has read the box
+                    tc::mbar_expect_tx(&st_full[warp - 2], 4096);
+                    tc::tma_load_2d(stg, &prm.to, h * D + hf * DH, panel * 128 + quarter * 32, &st_full[warp - 2]);
+                }
+            } else if (MODE == 1 && in) {
+                prefetch_row<DH>(dq);
+            }
             float ps[2] = {0.f, 0.f}, zs[2] = {0.f, 0.f};
             for (int g = 0; g < ng; ++g, ++G) {
                 const int sb = (int)(G & 1);
@@ -375,13 +411,37 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_row_kernel(const __grid_c
                     break;
                 }
                 tc::fence_after_sync();
-                add_row_from_tmem<DH>(tQ + hf * DH + tlane, dq, rsqrtf((float)D), in);
+                if constexpr (C::STAGE) {
+                    // the residual dQ values arrived in the staged box (row = lane, 128-byte swizzle)
+                    if (!tc::warp_wait(&st_full[warp - 2], U & 1, tc::kWaitLimit)) {
+                        ok = false;
+                        break;
+                    }
+                    add_box_from_tmem<DH>(tQ + hf * DH + tlane, smem + C::O0 + (warp - 2) * 4096 + lane * 128, lane,
+                                          rsqrtf((float)D));
+                    tc::fence_proxy_async();   // the box's new values, for the TMA store
+                    __syncwarp();
+                    if (lane == 0) {
+                        tc::tma_store_2d(&prm.to, h * D + hf * DH, panel * 128 + quarter * 32, stg);
+                        tc::bulk_commit();
+                    }
+                } else {
+                    add_row_from_tmem<DH>(tQ + hf * DH + tlane, dq, rsqrtf((float)D), in);
+                }
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&acc_empty);
             }
         }
         if (!ok && lane == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
+        if constexpr (C::STAGE) {
+            // a staged box whose load was issued but not consumed (only after a
+            // timeout, in the unit that failed) lands before the CTA ends; every store completes
+            if (lane == 0) {
+                if (!ok) tc::mbar_wait(&st_full[warp - 2], U & 1, tc::kWaitLimit);
+                tc::bulk_wait_all();
+            }
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -397,23 +457,28 @@ template <int D> struct ColCfg {
     static constexpr int DA = D / 64;
     static constexpr uint32_t CB = DA * 128 * 128;   // K or V of the column panel (128 sources)
     static constexpr uint32_t HB = DA * 64 * 128;    // Q or dOut of a block (64 destinations)
-    static constexpr int NST = D == 128 ? 3 : 4;
+    static constexpr int NST = D == 128 ? 2 : 4;
     static constexpr uint32_t C0 = 0;                // K, then V
     static constexpr uint32_t ST0 = C0 + 2 * CB;     // stage: Q, dOut, masks (8 tiles x 16 sources x 64 bits), lse, Delta
     static constexpr uint32_t TX = 2 * HB + 1024 + 256 + 256;   // bytes a stage receives
     static constexpr uint32_t STB = (TX + 1023) / 1024 * 1024;  // stages 1024-aligned (128-byte swizzle)
     static constexpr uint32_t PD0 = ST0 + NST * STB; // P^T, dS^T hi, dS^T lo (128 x 64 bf16 each)
-    static constexpr uint32_t BYTES = PD0 + 3 * 128 * 128;
+    // each weight warp stages 32 rows x 64 columns of its gradient (one
+    // 128-byte-swizzled TMA box) for a bulk read-modify-write, D / 64 boxes in turn
+    static constexpr int NH = D / 64;
+    static constexpr uint32_t O0 = PD0 + 3 * 128 * 128;
+    static constexpr uint32_t BYTES = O0 + 8 * 4096;
 };
 
 static_assert(ColCfg<64>::STB % 1024 == 0 && ColCfg<128>::STB % 1024 == 0, "stage alignment");
 static_assert(ColCfg<128>::BYTES + 1024 <= 227 * 1024 && ColCfg<64>::BYTES + 1024 <= 227 * 1024, "shared memory");
-static_assert(RowCfg<128, 0>::BYTES + 1024 <= 227 * 1024 && RowCfg<128, 1>::BYTES + 1024 <= 227 * 1024 &&
+static_assert(RowCfg<128, 0>::BYTES + 1024 <= 227 * 1024 && RowCfg<128, 1>::BYTES + 1024 + 1024 <= 227 * 1024 &&
                   RowCfg<64, 0>::BYTES + 1024 <= 227 * 1024 && RowCfg<64, 1>::BYTES + 1024 <= 227 * 1024,
               "shared memory");
 
 struct ColParams {
     CUtensorMap tk, tv, tq, tg;   // [N][H*D] bf16: K, V boxes 64 x 128; Q, dOut boxes 64 x 64
+    CUtensorMap tdk, tdv;         // dK, dV [N][H*D] bf16, box 64 x 32 (one weight warp's rows, 64 columns)
     BsrBwdArgs a;
 };
 
@@ -425,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t c_full, c_empty, kv_full[C::NST], kv_empty[C::NST], s_full[2], s_empty[2], pd_full, pd_empty,
-        acc_empty, mma_done;
+        acc_empty, mma_done, st_full[8];
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t sbase = tc::smem_u32(smem);
@@ -448,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
         tc::mbar_init(&pd_empty, 1);
         tc::mbar_init(&acc_empty, kSoft);
         tc::mbar_init(&mma_done, 1);
+        for (int i = 0; i < 8; ++i) tc::mbar_init(&st_full[i], 1);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -576,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
         const int quarter = warp & 3, hf = (warp - 2) >> 2, r = quarter * 32 + lane;
         const uint32_t tlane = (uint32_t)(quarter * 32) << 16;
         const float scale2 = kLog2e * rsqrtf((float)D);
-        int64_t B = 0, U = 0;
+        int64_t B = 0, U = 0, nld = 0;   // nld: staged box loads issued (lane 0 issues them)
         bool ok = true;
         int4 nfo = tc::unit_info(a.cpanel_info, blockIdx.x, n_units, H);
         for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++U) {
@@ -587,8 +653,15 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
             const int nb = 2 * (cur.z - cur.y);
             const int64_t src = (int64_t)cp * 128 + r;
             const bool in = src < a.N;
-            __nv_bfloat16 *grad = static_cast<__nv_bfloat16 *>(hf == 0 ? a.dK : a.dV) + ((in ? src : 0) * H + h) * D;
-            if (in) prefetch_row<D>(grad);
+            // this warp's gradient rows (dK for hf 0, dV for hf 1): the first box loads now
+            const CUtensorMap *tg_map = hf == 0 ? &prm.tdk : &prm.tdv;
+            const uint32_t stg = sbase + C::O0 + (warp - 2) * 4096;
+            if (lane == 0) {
+                if (U >= 1) tc::bulk_wait_read();   // the previous unit's last store has read the box
+                tc::mbar_expect_tx(&st_full[warp - 2], 4096);
+                tc::tma_load_2d(stg, tg_map, h * D, cp * 128 + quarter * 32, &st_full[warp - 2]);
+            }
+            ++nld;
             for (int b = 0; b < nb; ++b, ++B) {
                 const int s = (int)(B % C::NST), sb = (int)(B & 1);
                 // products, the stage's masks and row terms, and a free P / dS buffer
@@ -646,12 +719,39 @@ __global__ void __launch_bounds__(kThreads, 1) bsr_bwd_col_kernel(const __grid_c
                 break;
             }
             tc::fence_after_sync();
-            add_row_from_tmem<D>((hf == 0 ? tK : tV) + tlane, grad, hf == 0 ? rsqrtf((float)D) : 1.f, in);
+            // add the accumulator to the staged boxes, 64 columns at a time (row = lane)
+            for (int c2 = 0; c2 < C::NH; ++c2) {
+                if (c2 > 0 && lane == 0) {   // the box is reloaded once the store has read it
+                    tc::bulk_wait_read();
+                    tc::mbar_expect_tx(&st_full[warp - 2], 4096);
+                    tc::tma_load_2d(stg, tg_map, h * D + c2 * 64, cp * 128 + quarter * 32, &st_full[warp - 2]);
+                }
+                if (c2 > 0) ++nld;
+                if (!tc::warp_wait(&st_full[warp - 2], (U * C::NH + c2) & 1, tc::kWaitLimit)) {
+                    ok = false;
+                    break;
+                }
+                add_box_from_tmem<64>((hf == 0 ? tK : tV) + tlane + c2 * 64,
+                                      smem + C::O0 + (warp - 2) * 4096 + lane * 128, lane,
+                                      hf == 0 ? rsqrtf((float)D) : 1.f);
+                tc::fence_proxy_async();   // the box's new values, for the TMA store
+                __syncwarp();
+                if (lane == 0) {
+                    tc::tma_store_2d(tg_map, h * D + c2 * 64, cp * 128 + quarter * 32, stg);
+                    tc::bulk_commit();
+                }
+            }
+            if (!ok) break;
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty);
         }
         if (!ok && lane == 0) atomicOr(a.d_err, tc::kErrMmaTimeout);
+        if (lane == 0) {
+            // after a timeout the box load last issued lands before the CTA ends; every store completes
+            if (!ok && nld > 0) tc::mbar_wait(&st_full[warp - 2], (nld - 1) & 1, tc::kWaitLimit);
+            tc::bulk_wait_all();
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -701,6 +801,7 @@ template <int D> cudaError_t row_pass(const BsrBwdArgs &a, int mode, cudaStream_
     if (e == cudaSuccess) e = bf16_tensor_map(&prm.tg, bf(a.dOut), a.N, HD, HD, 64, 128);
     if (e == cudaSuccess) e = bf16_tensor_map(&prm.tk, bf(a.K), a.N, HD, HD, 64, 16);
     if (e == cudaSuccess) e = bf16_tensor_map(&prm.tv, bf(a.V), a.N, HD, HD, 64, 16);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.to, bf(a.dQ), a.N, HD, HD, 64, 32);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.n_active * a.H;
     return mode == 0 ? launch<bsr_bwd_row_kernel<D, 0>>(prm, units, a.num_sms, RowCfg<D, 0>::BYTES,
@@ -718,6 +819,8 @@ template <int D> cudaError_t col_pass(const BsrBwdArgs &a, cudaStream_t s) {
     if (e == cudaSuccess) e = bf16_tensor_map(&prm.tv, bf(a.V), a.N, HD, HD, 64, 128);
     if (e == cudaSuccess) e = bf16_tensor_map(&prm.tq, bf(a.Q), a.N, HD, HD, 64, 64);
     if (e == cudaSuccess) e = bf16_tensor_map(&prm.tg, bf(a.dOut), a.N, HD, HD, 64, 64);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tdk, bf(a.dK), a.N, HD, HD, 64, 32);
+    if (e == cudaSuccess) e = bf16_tensor_map(&prm.tdv, bf(a.dV), a.N, HD, HD, 64, 32);
     if (e != cudaSuccess) return e;
     const int64_t units = (int64_t)a.n_cactive * a.H;
     return launch<bsr_bwd_col_kernel<D>>(prm, units, a.num_sms, ColCfg<D>::BYTES, SGA_KERN_BSR_BWD_DKDV, s);
