@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(256, 2) gat_bwd_dst_kernel(GatArgs a) {
                     const float dp = group_sum<LH>(dot2<EL>(go[k], vf));
                     const float zz = el[k] + st.scalar(u, 0, (gl + G * k) / LH);
                     const float lp = zz > 0.f ? 1.f : a.slope;
-                    const float p = ok ? exp2f(lrelu_f(zz, a.slope) * kLog2e - lse2[k]) : 0.f;
+                    const float p = ok ? fast_exp2(lrelu_f(zz, a.slope) * kLog2e - lse2[k]) : 0.f;
                     const float pdp = p * dp;
                     c[k] += pdp;
                     z[k] += p;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(256, 2) gat_bwd_src_kernel(GatArgs a) {
                     const float dp = group_sum<LH>(dot2<EL>(gf, fv[k]));
                     const float zz = st.scalar(u, 2, h) + er[k];
                     const float lp = zz > 0.f ? 1.f : a.slope;
-                    const float p = ok ? exp2f((lrelu_f(zz, a.slope) - st.scalar(u, 0, h)) * kLog2e) : 0.f;
+                    const float p = ok ? fast_exp2((lrelu_f(zz, a.slope) - st.scalar(u, 0, h)) * kLog2e) : 0.f;
                     der[k] = fmaf(p * (dp - st.scalar(u, 1, h)), lp, der[k]);
                     axpy2<EL>(dfv[k], p, gf);
                 }

@@ -285,7 +285,7 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                     lrelu_chunk<EL>(fl[k], f, slope, lz, dz);
                     float e = dot2<EL>(att[k], lz), dp = dot2<EL>(go[k], f);
                     group_sum2<LH>(e, dp);
-                    const float p = ok ? exp2f(e * kLog2e - lse2[k]) : 0.f;
+                    const float p = ok ? fast_exp2(e * kLog2e - lse2[k]) : 0.f;
                     const float pdp = p * dp;
                     c[k] += pdp;
                     z[k] += p;
@@ -470,7 +470,7 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
                     float e = dot2<EL>(att[k], lz), dp = dot2<EL>(gf, frj[k]);
                     group_sum2<LH>(e, dp);
                     const int h = (gl + G * k) / LH;
-                    const float p = ok ? exp2f((e - st.scalar(u, 0, h)) * kLog2e) : 0.f;
+                    const float p = ok ? fast_exp2((e - st.scalar(u, 0, h)) * kLog2e) : 0.f;
                     const float de = p * (dp - st.scalar(u, 1, h));
                     axpy2<EL>(dfr[k], p, gf);
                     if constexpr (kFactorA) {

@@ -438,11 +438,11 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                     const bool hi = head_sums_split<LH>(sd[0], dv[0], sd[1], dv[1], sdot, dp);
                     float p;
                     if constexpr (BIAS)
-                        p = ok ? exp2f(sdot * scale2 - (hi ? lse2[1] : lse2[0]) +
+                        p = ok ? fast_exp2(sdot * scale2 - (hi ? lse2[1] : lse2[0]) +
                                        st.scalar(u, 0, (gl + G * (hi ? 1 : 0)) / LH) * kLog2e)
                                : 0.f;
                     else
-                        p = ok ? exp2f(sdot * scale2 - (hi ? lse2[1] : lse2[0])) : 0.f;
+                        p = ok ? fast_exp2(sdot * scale2 - (hi ? lse2[1] : lse2[0])) : 0.f;
                     const float pdp = p * dp;
                     const float po = __shfl_xor_sync(SGA_FULL_MASK, p, LH / 2);
                     const float pdpo = __shfl_xor_sync(SGA_FULL_MASK, pdp, LH / 2);
@@ -465,10 +465,10 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                         group_sum2<LH>(sdot, dp);
                         float p;
                         if constexpr (BIAS)
-                            p = ok ? exp2f(sdot * scale2 - lse2[k] + st.scalar(u, 0, (gl + G * k) / LH) * kLog2e)
+                            p = ok ? fast_exp2(sdot * scale2 - lse2[k] + st.scalar(u, 0, (gl + G * k) / LH) * kLog2e)
                                    : 0.f;
                         else
-                            p = ok ? exp2f(sdot * scale2 - lse2[k]) : 0.f;
+                            p = ok ? fast_exp2(sdot * scale2 - lse2[k]) : 0.f;
                         const float pdp = p * dp;
                         c[k] += pdp;
                         z[k] += p;
@@ -588,9 +588,9 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
                     const int h = (gl + G * k) / LH;
                     float p;
                     if constexpr (BIAS)
-                        p = ok ? exp2f(sdot * scale2 + (st.scalar(u, 2, h) - st.scalar(u, 0, h)) * kLog2e) : 0.f;
+                        p = ok ? fast_exp2(sdot * scale2 + (st.scalar(u, 2, h) - st.scalar(u, 0, h)) * kLog2e) : 0.f;
                     else
-                        p = ok ? exp2f(sdot * scale2 - st.scalar(u, 0, h) * kLog2e) : 0.f;
+                        p = ok ? fast_exp2(sdot * scale2 - st.scalar(u, 0, h) * kLog2e) : 0.f;
                     const float ds = p * (dp - st.scalar(u, 1, h));
                     axpy2<EL>(dv[k], p, gf);
                     axpy2<EL>(dk[k], ds, qf);

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) gt_fwd_feature_kernel(GtArgs a, float sca
                     unpack<T>(vr[k], vf);
                     const float s = group_sum<LH>(dot2<EL>(q[k], kf)) * scale2;
                     const float mn = fmaxf(m[k], s);
-                    const float alpha = exp2_diff(m[k], mn), p = exp2f(s - mn);
+                    const float alpha = exp2_diff(m[k], mn), p = fast_exp2(s - mn);
                     l[k] = l[k] * alpha + p;
 #pragma unroll
                     for (int x = 0; x < EL; ++x) acc[k][x] = fmaf(p, vf[x], acc[k][x] * alpha);

@@ -186,15 +186,9 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// 2^x by the MUFU instruction (ex2.approx.ftz: relative error about 2^-22,
-// subnormal results flushed to zero; 2^-inf = 0)
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-// 2^(a - m), zero for a = -inf (also when m = -inf)
-__device__ __forceinline__ float ex2_diff(float a, float m) { return a == -INFINITY ? 0.0f : ex2(a - m); }
+// 2^x and 2^(a - m) (zero for a = -inf) by the MUFU instruction (common.cuh)
+__device__ __forceinline__ float ex2(float x) { return fast_exp2(x); }
+__device__ __forceinline__ float ex2_diff(float a, float m) { return exp2_diff(a, m); }
 
 // Work unit u of a persistent block-sparse kernel: units are (panel, head)
 // pairs, panels taken from a list of (panel, first, end, 0) records; past the
