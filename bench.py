@@ -747,6 +747,8 @@ def run_native(args, ws, rank, local):
                    "l2": "flushed before every step (write of 2x L2), outside the timed interval",
                    "parallelism": f"replicas x{ws}",
                    "plan_build_ms": round(wl.plan_ms, 2),
+                   "split_threshold": wl.plan.info()["split_threshold"],
+                   "chunk_len": wl.plan.info()["chunk_len"],
                    "tile_min_nnz": wl.tile_min_nnz,
                    "schedule": ["stream", "feature", "bilevel"][wl.schedule],
                    "reorder": wl.reorder, "reorder_ms": round(wl.reorder_ms, 2),

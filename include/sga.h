@@ -68,8 +68,10 @@ typedef enum {
 
 /* Plan options.  Zero (or a NULL pointer) selects the default of each field. */
 typedef struct {
-    int32_t split_threshold;  /* rows of degree > this are split (default 256) */
-    int32_t chunk_len;        /* edges per chunk of a split row (default 128) */
+    int32_t split_threshold;  /* rows of degree > this are split (default: 256, doubled while
+                                 8x it stays within E / (16 x the SMs), the edges one resident
+                                 warp takes on average, up to 4096) */
+    int32_t chunk_len;        /* edges per chunk of a split row (default: half the threshold) */
     int32_t in_features;      /* GATv2 input width F; 0 for a Graph Transformer plan */
     int32_t tile_min_nnz;     /* > 0: block-sparse tensor-core forward, see below; 0: off */
     int32_t layer;            /* sga_layer (default SGA_LAYER_ATTENTION) */

@@ -224,8 +224,6 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
     p->keep_eid = o.edge_bias || o.layer == SGA_LAYER_MINMAX;   // (the aggregation backward's edge map)
     p->row_order = o.row_order == 2 ? 2 : 1;   // 0 (default) and 1: descending degree
     p->dt = dt;
-    p->split_threshold = o.split_threshold > 0 ? o.split_threshold : 256;
-    p->chunk_len = o.chunk_len > 0 ? o.chunk_len : 128;
     p->indptr = indptr;
     p->indices = indices;
     int dev = 0;
@@ -235,6 +233,15 @@ sga_status sga_plan_create(const int32_t *indptr, const int32_t *indices, int64_
         delete p;
         return cuda_status(ce);
     }
+    // Split only rows that are long against a resident warp's average share
+    // of the edges (16 warps per SM): the persistent warps walk items longest
+    // first, so shorter rows already balance, and every split costs chunk
+    // partials and a merge.
+    int32_t t_default = 256;
+    const int64_t per_warp = E / (16 * (int64_t)std::max(1, p->num_sms));
+    while (t_default < 4096 && (int64_t)t_default * 8 <= per_warp) t_default *= 2;
+    p->split_threshold = o.split_threshold > 0 ? o.split_threshold : t_default;
+    p->chunk_len = o.chunk_len > 0 ? o.chunk_len : std::max(1, p->split_threshold / 2);
     sga_status st = plan_build(p, static_cast<cudaStream_t>(stream));
     if (st != SGA_OK) {
         delete p;
