@@ -435,6 +435,51 @@ class Workload:
                 host_out[k].copy_(v, non_blocking=True)
         main.wait_event(ev_out)
 
+    def e2e_pipelined(self, steps, host_out, flush):
+        """`steps` steps from pinned host inputs to pinned host outputs, the way a
+        training loop overlaps its data movement: step k+1's inputs go up on an
+        upload stream while step k computes (two device input buffers), step k's
+        outputs come down on a download stream while step k+1 computes.  Every
+        step's inputs are copied up and all its outputs copied down inside the
+        timed region, which runs from before the first upload to after the last
+        download.  Returns milliseconds for all steps."""
+        main = torch.cuda.current_stream()
+        up, down = torch.cuda.Stream(self.device), torch.cuda.Stream(self.device)
+        bufs = [{k: torch.empty_like(v) for k, v in self.dev.items()} for _ in range(2)]
+        uploaded, consumed = [None, None], [None, None]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+
+        def upload(b):
+            with torch.cuda.stream(up):
+                if consumed[b] is not None:
+                    up.wait_event(consumed[b])   # the step that read this buffer is done
+                for k in self.in_names:
+                    bufs[b][k].copy_(self.host[k], non_blocking=True)
+                uploaded[b] = up.record_event()
+
+        e0.record(main)
+        up.wait_event(e0)
+        upload(0)
+        for k in range(steps):
+            b = k % 2
+            if k + 1 < steps:
+                upload(1 - b)
+            main.wait_event(uploaded[b])
+            flush.zero_()   # L2 flushed before each step's compute, inside the region
+            outs = self.step(bufs[b])
+            consumed[b] = main.record_event()
+            with torch.cuda.stream(down):
+                down.wait_event(consumed[b])
+                for name, v in outs.items():
+                    host_out[name].copy_(v, non_blocking=True)
+                    v.record_stream(down)   # the allocator keeps v until the copy is done
+        main.wait_stream(down)
+        main.wait_stream(up)
+        e1.record(main)
+        e1.synchronize()
+        return e0.elapsed_time(e1)
+
 
 # --------------------------------------------------------------- CPU oracle leg
 
@@ -717,20 +762,29 @@ def run_native(args, ws, rank, local):
             wl.step_e2e(d_in, host_out, copy_stream)
         torch.cuda.synchronize()
         barrier(ws)
+        # one step at a time: each step's copies and compute in sequence
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e_ms = 0.0
+        e_ser = 0.0
         for _ in range(args.steps):
             flush.zero_()
             e0.record(stream)
             wl.step_e2e(d_in, host_out, copy_stream)
             e1.record(stream)
             e1.synchronize()
-            e_ms += e0.elapsed_time(e1)
-        e_ms = max_over_ranks(e_ms, ws, dev)
+            e_ser += e0.elapsed_time(e1)
+        e_ser = max_over_ranks(e_ser, ws, dev)
+        # K steps as a loader pipelines them (the reported number)
+        wl.e2e_pipelined(2, host_out, flush)
+        torch.cuda.synchronize()
+        barrier(ws)
+        e_ms = max_over_ranks(wl.e2e_pipelined(args.steps, host_out, flush), ws, dev)
         e2e = {"value": ws * wl.units * args.steps / (e_ms / 1e3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / args.steps}
+               "ms_per_step": e_ms / args.steps,
+               "overlap": "step k+1's inputs copied up and step k's outputs copied down while step k+1 "
+                          "computes (two device input buffers); every step's copies inside the timed region",
+               "serial_ms_per_step": e_ser / args.steps}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
