@@ -302,10 +302,17 @@ class Workload:
         if nodes:
             w0 = self.w
             params = {k: int(v * nodes / w0.N) for k, v in w0.params.items() if k == "draws"}
+            if w0.graph == "rmat":   # R-MAT draws node ids from 2^scale: nodes must be a power of two
+                scale = int(nodes).bit_length() - 1
+                if nodes != 1 << scale:
+                    raise SystemExit("--nodes must be a power of two for the R-MAT workload")
+                params["scale"] = scale
             self.w = w0.scaled(N=nodes, name=f"{w0.name}_at_n{nodes}", params=params)
         w = self.w
         self.device = device
         self.indptr, self.indices = synth.make_graph(w)
+        if len(self.indptr) - 1 != w.N:
+            raise SystemExit(f"graph has {len(self.indptr) - 1} nodes, the workload {w.N}")
         self.N, self.E = w.N, int(self.indptr[-1])
         self.units = self.E * w.H
         self.tdt = torch.float32 if w.dtype == "f32" else torch.bfloat16

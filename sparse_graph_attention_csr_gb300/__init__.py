@@ -161,13 +161,32 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _need(t: torch.Tensor, name: str, dtype=None):
-    if not t.is_cuda:
+def _need(t: torch.Tensor, name: str, dtype=None, numel=None, rows=None, plan=None):
+    """Checks a tensor before its pointer reaches the library, which sees
+    pointers only: a CUDA tensor, contiguous, of the expected dtype, element
+    count and leading dimension, on the plan's device."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {tuple(t.shape)}")
+    if rows is not None and (t.dim() == 0 or t.shape[0] != rows):
+        raise ValueError(f"{name} must have {rows} rows, got {tuple(t.shape)}")
+    if plan is not None and t.device != plan.device:
+        raise ValueError(f"{name} is on {t.device}, the plan's graph on {plan.device}")
+
+
+def _node(t, name, plan, dtype=None):
+    """A node tensor [N, H, D] (any contiguous view with N rows and N*H*D elements)."""
+    _need(t, name, plan.dtype if dtype is None else dtype, plan.N * plan.H * plan.D, plan.N, plan)
+
+
+def _head(t, name, plan):
+    """A per-head float32 node tensor [N, H]."""
+    _need(t, name, torch.float32, plan.N * plan.H, plan.N, plan)
 
 
 def launch_count() -> int:
@@ -203,6 +222,7 @@ class Plan:
         self.indptr, self.indices = indptr, indices
         self.N = indptr.numel() - 1
         self.E = indices.numel()
+        self.device = indptr.device
         self.H, self.D, self.F = int(H), int(D), int(F)
         self.dtype = dtype
         self.dt = SGA_F32 if dtype == torch.float32 else SGA_BF16
@@ -276,9 +296,11 @@ class Plan:
 def gt_attn_fwd(plan: Plan, Q, K, V, out=None, lse=None, stream=None):
     """out [N,H,D] (dtype of Q) and lse [N,H] float32."""
     for n, t in (("Q", Q), ("K", K), ("V", V)):
-        _need(t, n, plan.dtype)
+        _node(t, n, plan)
     out = torch.empty_like(Q) if out is None else out
-    lse = torch.empty(Q.shape[:2], dtype=torch.float32, device=Q.device) if lse is None else lse
+    lse = torch.empty((plan.N, plan.H), dtype=torch.float32, device=Q.device) if lse is None else lse
+    _node(out, "out", plan)
+    _head(lse, "lse", plan)
     _check(_lib().gt_attn_fwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V), plan.N,
                               plan.E, plan.H, plan.D, plan.dt, _ptr(out), _ptr(lse),
                               _stream(stream)), "gt_attn_fwd")
@@ -288,11 +310,13 @@ def gt_attn_fwd(plan: Plan, Q, K, V, out=None, lse=None, stream=None):
 def gt_attn_bwd(plan: Plan, Q, K, V, out, lse, dOut, dQ=None, dK=None, dV=None, stream=None):
     """(dQ, dK, dV), each [N,H,D]."""
     for n, t in (("Q", Q), ("K", K), ("V", V), ("out", out), ("dOut", dOut)):
-        _need(t, n, plan.dtype)
-    _need(lse, "lse", torch.float32)
+        _node(t, n, plan)
+    _head(lse, "lse", plan)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
+    for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        _node(t, n, plan)
     _check(_lib().gt_attn_bwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V),
                               _ptr(out), _ptr(lse), _ptr(dOut), plan.N, plan.E, plan.H, plan.D,
                               plan.dt, _ptr(dQ), _ptr(dK), _ptr(dV), _stream(stream)),
@@ -304,12 +328,14 @@ def gt_attn_bias_fwd(plan: Plan, Q, K, V, bias, out=None, lse=None, stream=None)
     """Graph Transformer with a per-edge, per-head score bias [E, H] float32
     (CSR edge order): (out, lse).  The plan needs edge_bias=True."""
     for n, t in (("Q", Q), ("K", K), ("V", V)):
-        _need(t, n, plan.dtype)
-    _need(bias, "bias", torch.float32)
+        _node(t, n, plan)
+    _need(bias, "bias", torch.float32, plan=plan)
     if tuple(bias.shape) != (plan.E, plan.H):
         raise ValueError(f"bias must be [{plan.E}, {plan.H}], got {tuple(bias.shape)}")
     out = torch.empty_like(Q) if out is None else out
-    lse = torch.empty(Q.shape[:2], dtype=torch.float32, device=Q.device) if lse is None else lse
+    lse = torch.empty((plan.N, plan.H), dtype=torch.float32, device=Q.device) if lse is None else lse
+    _node(out, "out", plan)
+    _head(lse, "lse", plan)
     _check(_lib().gt_attn_bias_fwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V),
                                    _ptr(bias), plan.N, plan.E, plan.H, plan.D, plan.dt, _ptr(out),
                                    _ptr(lse), _stream(stream)), "gt_attn_bias_fwd")
@@ -320,13 +346,16 @@ def gt_attn_bias_bwd(plan: Plan, Q, K, V, bias, out, lse, dOut, dQ=None, dK=None
                      dbias=None, stream=None):
     """(dQ, dK, dV, dbias) of the biased layer; dbias [E, H] float32."""
     for n, t in (("Q", Q), ("K", K), ("V", V), ("out", out), ("dOut", dOut)):
-        _need(t, n, plan.dtype)
-    _need(lse, "lse", torch.float32)
-    _need(bias, "bias", torch.float32)
+        _node(t, n, plan)
+    _head(lse, "lse", plan)
+    _need(bias, "bias", torch.float32, plan.E * plan.H, plan.E, plan)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
     dbias = torch.empty_like(bias) if dbias is None else dbias
+    for n, t in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+        _node(t, n, plan)
+    _need(dbias, "dbias", torch.float32, plan.E * plan.H, plan.E, plan)
     _check(_lib().gt_attn_bias_bwd(plan.handle, *plan._graph()[:2], _ptr(Q), _ptr(K), _ptr(V),
                                    _ptr(bias), _ptr(out), _ptr(lse), _ptr(dOut), plan.N, plan.E,
                                    plan.H, plan.D, plan.dt, _ptr(dQ), _ptr(dK), _ptr(dV),
@@ -390,16 +419,25 @@ def noalloc_device_error(stream=None) -> int:
 
 # ----------------------------------------------------------------------- GATv2
 
+def _gatv2_inputs(plan, X, W_l, W_r, a):
+    _need(X, "X", plan.dtype, plan.N * plan.F, plan.N, plan)
+    for n, t in (("W_l", W_l), ("W_r", W_r)):
+        _need(t, n, plan.dtype, plan.F * plan.H * plan.D, plan.F, plan)
+    _need(a, "a", plan.dtype, plan.H * plan.D, None, plan)
+
+
 def gatv2_fwd(plan: Plan, X, W_l, W_r, a, slope: float = 0.2, FL=None, FR=None, out=None,
               lse=None, stream=None):
     """(FL, FR, out, lse): FL = X W_l and FR = X W_r as [N,H,D], out [N,H,D], lse [N,H]."""
-    for n, t in (("X", X), ("W_l", W_l), ("W_r", W_r), ("a", a)):
-        _need(t, n, plan.dtype)
+    _gatv2_inputs(plan, X, W_l, W_r, a)
     shape = (plan.N, plan.H, plan.D)
     FL = torch.empty(shape, dtype=X.dtype, device=X.device) if FL is None else FL
     FR = torch.empty(shape, dtype=X.dtype, device=X.device) if FR is None else FR
     out = torch.empty(shape, dtype=X.dtype, device=X.device) if out is None else out
     lse = torch.empty(shape[:2], dtype=torch.float32, device=X.device) if lse is None else lse
+    for n, t in (("FL", FL), ("FR", FR), ("out", out)):
+        _node(t, n, plan)
+    _head(lse, "lse", plan)
     _check(_lib().gatv2_fwd(plan.handle, *plan._graph()[:2], _ptr(X), _ptr(W_l), _ptr(W_r),
                             _ptr(a), plan.N, plan.E, plan.F, plan.H, plan.D, float(slope), plan.dt,
                             _ptr(FL), _ptr(FR), _ptr(out), _ptr(lse), _stream(stream)),
@@ -410,14 +448,15 @@ def gatv2_fwd(plan: Plan, X, W_l, W_r, a, slope: float = 0.2, FL=None, FR=None, 
 def gatv2_bwd(plan: Plan, X, W_l, W_r, a, FL, FR, out, lse, dOut, slope: float = 0.2,
               dX=None, dW_l=None, dW_r=None, da=None, stream=None):
     """(dX, dW_l, dW_r, da)."""
-    for n, t in (("X", X), ("W_l", W_l), ("W_r", W_r), ("a", a), ("FL", FL), ("FR", FR),
-                 ("out", out), ("dOut", dOut)):
-        _need(t, n, plan.dtype)
-    _need(lse, "lse", torch.float32)
+    _gatv2_inputs(plan, X, W_l, W_r, a)
+    for n, t in (("FL", FL), ("FR", FR), ("out", out), ("dOut", dOut)):
+        _node(t, n, plan)
+    _head(lse, "lse", plan)
     dX = torch.empty_like(X) if dX is None else dX
     dW_l = torch.empty_like(W_l) if dW_l is None else dW_l
     dW_r = torch.empty_like(W_r) if dW_r is None else dW_r
     da = torch.empty_like(a) if da is None else da
+    _gatv2_inputs(plan, dX, dW_l, dW_r, da)
     _check(_lib().gatv2_bwd(plan.handle, *plan._graph()[:2], _ptr(X), _ptr(W_l), _ptr(W_r),
                             _ptr(a), _ptr(FL), _ptr(FR), _ptr(out), _ptr(lse), _ptr(dOut), plan.N,
                             plan.E, plan.F, plan.H, plan.D, float(slope), plan.dt, _ptr(dX),
@@ -445,6 +484,7 @@ def relabel_csr(indptr, indices, perm, stream=None):
     for n, t in (("indptr", indptr), ("indices", indices), ("perm", perm)):
         _need(t, n, torch.int32)
     N = indptr.numel() - 1
+    _need(perm, "perm", torch.int32, N)
     new_ptr = torch.empty_like(indptr)
     new_idx = torch.empty_like(indices)
     _check(_lib().sga_relabel_csr(_ptr(indptr), _ptr(indices), N, indices.numel(), _ptr(perm),
@@ -456,9 +496,10 @@ def permute_rows(x, perm, inverse: bool = False, out=None, stream=None):
     """Rows of a node tensor under perm: out[perm[v]] = x[v] (inverse:
     out[v] = x[perm[v]])."""
     _need(x, "x")
-    _need(perm, "perm", torch.int32)
+    N = x.shape[0] if x.dim() else 0
+    _need(perm, "perm", torch.int32, N)
     out = torch.empty_like(x) if out is None else out
-    N = x.shape[0]
+    _need(out, "out", x.dtype, x.numel(), N)
     row_bytes = x.numel() // max(N, 1) * x.element_size()
     _check(_lib().sga_permute_rows(_ptr(x), N, row_bytes, _ptr(perm), 1 if inverse else 0,
                                    _ptr(out), _stream(stream)), "sga_permute_rows")
@@ -471,11 +512,13 @@ def gat_attn_fwd(plan: Plan, Fv, el, er, slope: float = 0.2, out=None, lse=None,
     """GAT edge attention: (out [N,H,D], lse [N,H]) from the projected features
     Fv [N,H,D] and the score halves el, er [N,H] float32.  The plan must be
     built with layer=SGA_LAYER_GAT."""
-    _need(Fv, "Fv", plan.dtype)
-    _need(el, "el", torch.float32)
-    _need(er, "er", torch.float32)
+    _node(Fv, "Fv", plan)
+    _head(el, "el", plan)
+    _head(er, "er", plan)
     out = torch.empty_like(Fv) if out is None else out
-    lse = torch.empty(Fv.shape[:2], dtype=torch.float32, device=Fv.device) if lse is None else lse
+    lse = torch.empty((plan.N, plan.H), dtype=torch.float32, device=Fv.device) if lse is None else lse
+    _node(out, "out", plan)
+    _head(lse, "lse", plan)
     _check(_lib().gat_attn_fwd(plan.handle, *plan._graph()[:2], _ptr(Fv), _ptr(el), _ptr(er), plan.N,
                                plan.E, plan.H, plan.D, float(slope), plan.dt, _ptr(out), _ptr(lse),
                                _stream(stream)), "gat_attn_fwd")
@@ -486,9 +529,9 @@ def gat_attn_bwd(plan: Plan, Fv, el, er, out, lse, dOut, slope: float = 0.2, str
     """(dFv, del, der): the value-path gradient of Fv and the gradients of the
     two score halves."""
     for n, t in (("Fv", Fv), ("out", out), ("dOut", dOut)):
-        _need(t, n, plan.dtype)
+        _node(t, n, plan)
     for n, t in (("el", el), ("er", er), ("lse", lse)):
-        _need(t, n, torch.float32)
+        _head(t, n, plan)
     dFv = torch.empty_like(Fv)
     de_l = torch.empty_like(el)
     de_r = torch.empty_like(er)
@@ -507,17 +550,22 @@ def agg_minmax_fwd(plan: Plan, X, op: str = "max", out=None, arg=True, mask=True
     an empty row); mask [E, R] uint8 = the win mask the backward takes.
     ``arg``/``mask`` = False skips that output (None in its place), a tensor
     is filled in place.  ``plan`` must be built with layer=SGA_LAYER_MINMAX."""
-    _need(X, "X", plan.dtype)
+    _node(X, "X", plan)
     out = torch.empty_like(X) if out is None else out
+    _node(out, "out", plan)
     if arg is True:
         arg = torch.empty(X.shape, dtype=torch.int32, device=X.device)
     elif arg is False:
         arg = None
+    if arg is not None:
+        _node(arg, "arg", plan, torch.int32)
+    mask_bytes = int(_lib().sga_agg_mask_bytes(plan.handle))
     if mask is True:
-        mask = torch.empty(int(_lib().sga_agg_mask_bytes(plan.handle)), dtype=torch.uint8,
-                           device=X.device)
+        mask = torch.empty(mask_bytes, dtype=torch.uint8, device=X.device)
     elif mask is False:
         mask = None
+    if mask is not None:
+        _need(mask, "mask", torch.uint8, mask_bytes, None, plan)
     code = {"max": SGA_AGG_MAX, "min": SGA_AGG_MIN}[op]
     _check(_lib().agg_minmax_fwd(plan.handle, *plan._graph()[:2], _ptr(X), plan.N, plan.E, plan.H,
                                  plan.D, plan.dt, code, _ptr(out), _ptr(arg), _ptr(mask),
@@ -527,9 +575,10 @@ def agg_minmax_fwd(plan: Plan, X, op: str = "max", out=None, arg=True, mask=True
 
 def agg_minmax_bwd(plan: Plan, mask, dOut, dX=None, stream=None):
     """dX [N,H,D]: dOut gathered into the winning sources of the forward."""
-    _need(mask, "mask", torch.uint8)
-    _need(dOut, "dOut", plan.dtype)
+    _need(mask, "mask", torch.uint8, int(_lib().sga_agg_mask_bytes(plan.handle)), None, plan)
+    _node(dOut, "dOut", plan)
     dX = torch.empty_like(dOut) if dX is None else dX
+    _node(dX, "dX", plan)
     _check(_lib().agg_minmax_bwd(plan.handle, _ptr(mask), _ptr(dOut), plan.N, plan.H, plan.D,
                                  plan.dt, _ptr(dX), _stream(stream)), "agg_minmax_bwd")
     return dX
