@@ -33,6 +33,10 @@ namespace sga {
 __device__ __forceinline__ void cp16_async(uint32_t dst, const void *src, bool ok) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0));
 }
+// The same with the source size given (16 copies, 0 fills zeros and reads nothing).
+__device__ __forceinline__ void cp16_async_sz(uint32_t dst, const void *src, uint32_t sz) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sz));
+}
 __device__ __forceinline__ void cp4_async(uint32_t dst, const void *src, bool ok) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(ok ? 4 : 0));
 }
@@ -120,6 +124,7 @@ template <typename C> struct EdgeStream {
     int32_t *err;
     int64_t stride, n_items;
     int lane, g, gl;
+    uint32_t c_in;           // bit k: this lane's chunk gl + G k of a row exists (< R)
     // producer
     int64_t nx_item;         // next item to consider
     ItemMeta m1, m2;         // descriptors of nx_item and nx_item + stride
@@ -151,6 +156,9 @@ template <typename C> struct EdgeStream {
         lane = threadIdx.x & 31;
         g = lane / C::G;
         gl = lane % C::G;
+        c_in = 0;
+#pragma unroll
+        for (int k = 0; k < C::NC; ++k) c_in |= (gl + C::G * k < R ? 1u : 0u) << k;
         stride = (int64_t)gridDim.x * (blockDim.x >> 5);
         n_items = C::LIST ? P.n_items : (int64_t)P.n_chunks + N;
         nx_item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -241,26 +249,30 @@ template <typename C> struct EdgeStream {
             p_ids = p_ids_nx;
             p_ids_nx = e0 + 32 < p_deg ? load_ids(ids, p_beg + e0 + 32, min(32, p_deg - e0 - 32), N, err) : -1;
         }
+        const uint32_t dst0 = sa + C::OFF_ROW + slot * C::ROW_SLOT + lane * 16;
 #pragma unroll
         for (int u = 0; u < C::U; ++u) {
             const int32_t e = e0 + g + C::NG * u;
             const int32_t j = __shfl_sync(SGA_FULL_MASK, p_ids, e & 31);
             const bool ok = e < p_deg && j >= 0;
+            // a copy that is skipped (src-size 0) still names an address inside the
+            // array: row 0 for a missing neighbour, chunk 0 for a lane past the row
+            const size_t roff = (size_t)(uint32_t)(ok ? j : 0) * R;
 #pragma unroll
-            for (int r = 0; r < C::NROW; ++r)
+            for (int k = 0; k < C::NC; ++k) {
+                const bool cin = (c_in >> k) & 1u;
+                const size_t off = roff + (cin ? gl + C::G * k : 0);
+                const uint32_t sz = (ok && cin) ? 16u : 0u;
 #pragma unroll
-                for (int k = 0; k < C::NC; ++k) {
-                    const int c = gl + C::G * k;
-                    const bool okc = ok && c < R;
-                    cp16_async(sa + C::OFF_ROW + slot * C::ROW_SLOT + (((u * C::NROW + r) * C::NC + k) * 32 + lane) * 16,
-                               okc ? arr.rows[r] + (size_t)j * R + c : arr.rows[r], okc);
-                }
+                for (int r = 0; r < C::NROW; ++r)
+                    cp16_async_sz(dst0 + ((u * C::NROW + r) * C::NC + k) * 32 * 16, arr.rows[r] + off, sz);
+            }
             if (gl < H)
 #pragma unroll
                 for (int s = 0; s < C::NSC; ++s) {
-                    const size_t at = ((C::ESC >> s) & 1u) ? (size_t)(p_beg + e) : (size_t)j;
+                    const size_t at = !ok ? 0 : ((C::ESC >> s) & 1u) ? (size_t)(p_beg + e) : (size_t)j;
                     cp4_async(sa + C::OFF_SC + slot * C::SC_SLOT + ((u * C::NSC + s) * 32 + lane) * 4,
-                              ok ? arr.sc[s] + at * H + gl : arr.sc[s], ok);
+                              arr.sc[s] + at * H + gl, ok);
                 }
             masks[u] = __ballot_sync(SGA_FULL_MASK, ok);
         }
