@@ -779,12 +779,7 @@ __global__ void head_major_kernel(const float *__restrict__ lse_n, const float *
 template <auto Kernel, typename P>
 cudaError_t launch(const P &prm, int64_t units, int num_sms, size_t bytes, sga_kernel_id id, cudaStream_t s) {
     const size_t smem = bytes + 1024;
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if (cudaError_t e = allow_smem<Kernel>(smem); e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(units < num_sms ? units : num_sms);
     note_launch(id, s, false);
     Kernel<<<grid, kThreads, smem, s>>>(prm);

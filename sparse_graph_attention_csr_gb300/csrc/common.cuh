@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/sga.h"
 
 #define SGA_FULL_MASK 0xffffffffu
@@ -174,4 +176,19 @@ constexpr int kErrIndexRange = 1;   // a gathered node id was outside [0, N)
 // ---- host-side launch bookkeeping (defined in api.cu) -----------------------
 namespace sga {
 void note_launch(sga_kernel_id which, cudaStream_t s, bool after);
+
+// Let Kernel launch with `smem` bytes of dynamic shared memory: raises the
+// kernel's limit whenever a launch needs more than any before it (kernels whose
+// size depends on the call's shape would otherwise keep the first call's limit
+// and refuse a larger launch).
+template <auto Kernel> cudaError_t allow_smem(size_t smem) {
+    static std::atomic<size_t> allowed{48 * 1024};
+    if (smem <= allowed.load(std::memory_order_relaxed)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    size_t cur = allowed.load(std::memory_order_relaxed);
+    while (smem > cur && !allowed.compare_exchange_weak(cur, smem, std::memory_order_relaxed)) {
+    }
+    return cudaSuccess;
+}
 }

@@ -366,12 +366,7 @@ cudaError_t tc_dx(const TcDx &p, cudaStream_t s) {
     dp.HD = p.HD;
     dp.err = p.err;
     const size_t smem = dx_smem(p.F, p.HD);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(tc_dx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if (cudaError_t e = allow_smem<tc_dx_kernel>(smem); e != cudaSuccess) return e;
     int dev = 0, sms = 1;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -396,12 +391,7 @@ cudaError_t tc_dw(const TcDw &p, cudaStream_t s) {
     dp.slabs = p.slabs;
     dp.err = p.err;
     const size_t smem = dw_smem(p.F, p.HD);
-    static bool configured = false;
-    if (!configured) {
-        e = cudaFuncSetAttribute(tc_dw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if ((e = allow_smem<tc_dw_kernel>(smem)) != cudaSuccess) return e;
     tc_dw_kernel<<<(unsigned)p.slabs, kDwThreads, smem, s>>>(dp);
     return cudaGetLastError();
 }

@@ -341,12 +341,7 @@ cudaError_t tc_proj(const TcProj &p, cudaStream_t s) {
     pp.nslot = proj_slots(p.K, p.HD);
     pp.err = p.err;
     const size_t smem = proj_smem(p.K, p.HD);
-    static bool configured = false;
-    if (!configured) {
-        e = cudaFuncSetAttribute(tc_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    if ((e = allow_smem<tc_proj_kernel>(smem)) != cudaSuccess) return e;
     int dev = 0, sms = 1;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

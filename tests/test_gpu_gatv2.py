@@ -95,3 +95,49 @@ def test_edge_cases():
     run_gatv2(indptr, indices, 8, 2, 32, "f32", split=2, chunk=1)
     run_gatv2(indptr, indices, 8, 2, 32, "bf16")
     run_gatv2(np.zeros(4, np.int32), np.zeros(0, np.int32), 16, 1, 32, "f32")
+
+
+_GROWING_SHAPES = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, "tests")
+import oracle
+import sparse_graph_attention_csr_gb300 as sga
+from helpers import compare, dev
+from test_gpu_gt import random_csr
+
+rng = np.random.default_rng(11)
+indptr, indices = random_csr(rng, 300, 5)
+ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+# the first call needs the least shared memory of the three, the last the most
+for F, H, D in ((64, 1, 32), (128, 2, 64), (192, 2, 64)):
+    X = rng.standard_normal((len(indptr) - 1, F)).astype(np.float32)
+    W = (rng.standard_normal((F, H * D)) * 0.1).astype(np.float32)
+    a = (rng.standard_normal((H, D)) * 0.1).astype(np.float32)
+    t = [torch.from_numpy(v).to(torch.bfloat16) for v in (X, W, a)]
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, F=F)
+    FL, FR, out, lse = sga.gatv2_fwd(plan, *(dev(v) for v in (t[0], t[1], t[1], t[2])))
+    r = oracle.gatv2_fwd(indptr, indices, *(v.double().numpy() for v in (t[0], t[1], t[1], t[2])),
+                         0.2, store="bf16")
+    compare(out, r[2], "bf16", "out")
+    dO = dev(torch.from_numpy(rng.standard_normal(out.shape).astype(np.float32)).to(torch.bfloat16))
+    g = sga.gatv2_bwd(plan, *(dev(v) for v in (t[0], t[1], t[1], t[2])), FL, FR, out, lse, dO)
+    torch.cuda.synchronize()
+    assert all(bool(torch.isfinite(v.float()).all()) for v in g)
+print("ok")
+"""
+
+
+def test_projection_shapes_growing_within_one_process():
+    """Kernels whose shared memory depends on the call's shape (the bf16
+    projection and its gradient kernels) launch after a smaller call of the
+    same process: a fresh interpreter, so that no earlier test has already
+    raised the limit."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _GROWING_SHAPES], cwd=root, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
