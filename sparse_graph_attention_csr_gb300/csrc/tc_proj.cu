@@ -7,9 +7,10 @@
 //     accumulators ("tfull");
 //   warps 2-17: the epilogue.  Warp w reads TMEM lanes 32 (w mod 4) .. (tile
 //     rows) and every fourth 32-column chunk, checks whether each fp32 value's
-//     bf16 rounding is settled (bound 2 * 2^-24 |x||w| + ulp), stores FL/FR,
+//     bf16 rounding is settled (bound 2 * 2^-24 |x||w| + ulp; two values per
+//     packed instruction), stores FL/FR,
 //     frees the accumulator ("tempty"), then recomputes the flagged elements
-//     exactly from the slot's X rows and the staged weights (half-warp per
+//     exactly from the slot's X rows and the staged weights (four lanes per
 //     element, TwoSum) and frees the slot ("sempty").
 // The weights [W_l | W_r] are transposed into the K-major operand once per
 // CTA.  Every mbarrier wait is bounded; the epilogue warps take their
@@ -53,6 +54,15 @@ __host__ __device__ inline size_t proj_smem(int K, int HD) {
     return 1024 + proj_b_bytes(K, HD) + (size_t)proj_slots(K, HD) * ((K + 63) / 64) * kAtom;
 }
 
+__device__ __forceinline__ void sts16(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+// Both fp32 values rounded to bf16 (round to nearest even), packed low = a.
+__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
+    const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&r);
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *mbar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(mbar)), "r"(bytes)
                  : "memory");
@@ -131,16 +141,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_const
         tc::mbar_init(&done, 1);
         fix_n = 0;
     }
-    // B = [W_l | W_r]^T, K-major swizzled: row n = output column
-#pragma unroll 4
-    for (int idx = tid; idx < K * (NT / 8); idx += kThreads) {
-        const int k = idx / (NT / 8), n0 = (idx % (NT / 8)) * 8;
-        const __nv_bfloat16 *W = n0 < HD ? p.Wl : p.Wr;
-        const uint4 u = ldg16(W + (size_t)k * HD + (n0 % HD));
-        const __nv_bfloat16 *e = reinterpret_cast<const __nv_bfloat16 *>(&u);
+    // B = [W_l | W_r]^T, K-major swizzled: row n = output column.  A thread
+    // moves one 8 x 8 block (W rows 8 kc .., columns n0 ..): eight 16-byte
+    // loads, a transpose in registers, eight 16-byte stores.  k-chunks vary
+    // fastest across the warp, so the eight chunks of one B row land in
+    // distinct bank groups (no conflicts beyond the four wavefronts of 512 B).
+    for (int blk = tid; blk < KC * (NT / 8); blk += kThreads) {
+        const int kc = blk % KC, n0 = (blk / KC) * 8;
+        const __nv_bfloat16 *W = (n0 < HD ? p.Wl : p.Wr) + (size_t)kc * 8 * HD + (n0 % HD);
+        uint4 rw[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            *reinterpret_cast<__nv_bfloat16 *>(smem + tc::sw128_offset(n0 + i, k, NT)) = e[i];
+        for (int q = 0; q < 8; ++q) rw[q] = ldg16(W + (size_t)q * HD);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {   // column n0 + i: element i of each row, rows in pairs
+            const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t a = (&rw[2 * q].x)[i >> 1], b = (&rw[2 * q + 1].x)[i >> 1];
+                w[q] = __byte_perm(a, b, sel);
+            }
+            sts16(sB + tc::sw128_offset(n0 + i, kc * 8, NT), make_uint4(w[0], w[1], w[2], w[3]));
+        }
     }
     __syncthreads();
     for (int n = tid; n < NT; n += kThreads) cnorm[n] = sqrtf(row_sq(sB, n, K, NT));   // column norms of W
@@ -224,26 +246,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_const
             for (int cc = cgroup; cc < NT / 32; cc += kColGroups) {
                 uint32_t v[32];
                 tc::tmem_ld32(tbase + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * NT + cc * 32), v);
-                float o[32], cn[32];
+                // two values a step: their bf16 bits, and whether each one's
+                // rounding is settled (both ends of [f - bound, f + bound] round
+                // to the same bf16)
+                uint32_t packed[16], flags = 0, overflow = 0;   // unsettled; those the list had no room for
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 c4 = reinterpret_cast<const float4 *>(cnorm + cc * 32)[q];
-                    cn[4 * q] = c4.x;
-                    cn[4 * q + 1] = c4.y;
-                    cn[4 * q + 2] = c4.z;
-                    cn[4 * q + 3] = c4.w;
-                }
-                uint32_t flags = 0, overflow = 0;   // unsettled elements; those the list had no room for
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float f = __uint_as_float(v[i]);
-                    const float bound = fmaf(rn, cn[i], fabsf(f) * 1.2e-7f);
-                    o[i] = f;
-                    // both ends of [f - bound, f + bound] rounded at once; unsettled
-                    // when their bf16 bit patterns differ
-                    const __nv_bfloat162 ends = __floats2bfloat162_rn(f - bound, f + bound);
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(&ends);
-                    flags |= (uint32_t)(((w ^ (w >> 16)) & 0xffffu) != 0u) << i;
+                for (int j = 0; j < 16; ++j) {
+                    const float2 f = make_float2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    const float2 cn = *reinterpret_cast<const float2 *>(cnorm + cc * 32 + 2 * j);
+                    const float2 b = ffma2(make_float2(rn, rn), cn,
+                                           fmul2(make_float2(fabsf(f.x), fabsf(f.y)), make_float2(1.2e-7f, 1.2e-7f)));
+                    const float2 lo = fadd2(f, make_float2(-b.x, -b.y)), hi = fadd2(f, b);
+                    packed[j] = bf16x2_bits(f.x, f.y);
+                    const uint32_t d = bf16x2_bits(lo.x, lo.y) ^ bf16x2_bits(hi.x, hi.y);
+                    flags |= ((d & 0xffffu) != 0u ? 1u : 0u) << (2 * j);
+                    flags |= ((d >> 16) != 0u ? 1u : 0u) << (2 * j + 1);
                 }
                 for (uint32_t fl = flags; fl; fl &= fl - 1) {
                     const int i = __ffs(fl) - 1;
@@ -251,7 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_const
                     if (slot < kTpFix) fixl[slot] = make_int2(r, cc * 32 + i);
                     else overflow |= 1u << i;
                 }
-                // (not expected: about 0.5% of a tile's elements are flagged) exact sums by this thread
+                const int c0 = cc * 32;
+                __nv_bfloat16 *dst = c0 < HD ? p.FL + m * HD + c0 : p.FR + m * HD + (c0 - HD);
+                if (m < p.M) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        reinterpret_cast<uint4 *>(dst)[q] =
+                            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                }
+                // (not expected: the list holds about eight times the usual count)
+                // exact sums by this thread, stored over the plain values
                 for (uint32_t ov = overflow; ov; ov &= ov - 1) {
                     const int i = __ffs(ov) - 1, col = cc * 32 + i;
                     float hi = 0.f, lo = 0.f;
@@ -261,29 +287,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_const
                         hi = tt;
                         lo = __fadd_rn(lo, e);
                     }
-#pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        if (q == i) o[q] = __fadd_rn(hi, lo);
-                }
-                if (m < p.M) {
-                    const int c0 = cc * 32;
-                    __nv_bfloat16 *dst = c0 < HD ? p.FL + m * HD + c0 : p.FR + m * HD + (c0 - HD);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) reinterpret_cast<uint4 *>(dst)[q] = pack<__nv_bfloat16>(o + 8 * q);
+                    if (m < p.M) dst[i] = __float2bfloat16_rn(__fadd_rn(hi, lo));
                 }
             }
             tc::fence_before_sync();
             mbar_arrive(&tempty[acc]);   // the accumulator may take the tile after next
             epi_sync();                  // every flagged element is listed (and its plain value stored)
-            // exact recompute: a half-warp per element, lane j takes 16-byte
-            // chunks j, j + 16, ... of the X row and of the W column
-            const int nf = min(fix_n, kTpFix), hl = lane & 15;
-            for (int i0 = ew * 2; i0 < nf; i0 += 2 * kEpiWarps) {
-                const int i = i0 + (lane >> 4);
+            // exact recompute: four lanes per element (eight elements a warp),
+            // lane j of a group takes 16-byte chunks j, j + 4, ... of the X row
+            // and of the W column
+            const int nf = min(fix_n, kTpFix), hl = lane & 3;
+            for (int i0 = ew * 8; i0 < nf; i0 += 8 * kEpiWarps) {
+                const int i = i0 + (lane >> 2);
                 const bool act = i < nf;
                 const int fr = act ? fixl[i].x : 0, fc = act ? fixl[i].y : 0;
                 float hi = 0.f, lo = 0.f;
-                for (int c = hl; c < KC; c += 16) {
+                for (int c = hl; c < KC; c += 4) {
                     float xa[8], xb[8];
                     unpack<__nv_bfloat16>(lds16(xs + tc::sw128_offset(fr, c * 8, 128)), xa);
                     unpack<__nv_bfloat16>(lds16(sB + tc::sw128_offset(fc, c * 8, NT)), xb);
@@ -296,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_proj_kernel(const __grid_const
                     }
                 }
 #pragma unroll
-                for (int o2 = 8; o2 > 0; o2 >>= 1) {
+                for (int o2 = 2; o2 > 0; o2 >>= 1) {
                     const float ho = __shfl_xor_sync(SGA_FULL_MASK, hi, o2);
                     const float lo2 = __shfl_xor_sync(SGA_FULL_MASK, lo, o2);
                     float tt, e;
