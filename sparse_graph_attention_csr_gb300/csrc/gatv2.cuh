@@ -203,9 +203,50 @@ gatv2_fwd_kernel(Gatv2Args a) {
                 }
             }
         }
+        // the last chunk of a split row merges the row
+        if (it.partial && last_chunk(a.rows, it.item)) fwd_merge_row<T, D>(a, __ldg(a.rows.chunk_split + it.item));
         st.finish_item();
     }
     st.drain();
+}
+
+// Finish split row s in one warp (chunk order).  which == 0 (destination
+// rows): C and Z are the sums of the chunk parts, normalised as in the
+// destination pass (Delta = C / Z): dFL = (sum fA - Delta sum fB) / Z, and
+// the row's da contribution (sum gA - Delta sum gB) / Z goes to its own slot;
+// Delta and lse + ln Z are stored for the source pass.  which == 1
+// (sources): dFR is the plain sum of the chunk partials.
+template <typename T, int D>
+__device__ __noinline__ void gatv2_bwd_merge_row(const Gatv2Args &a, int which, int32_t s) {
+    constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
+    const Partition &P = which == 0 ? a.rows : a.cols;
+    const int32_t row = __ldg(P.split_rows + s);
+    const int32_t c0 = __ldg(P.chunk_ptr + s), c1 = __ldg(P.chunk_ptr + s + 1);
+    const int R = a.H * D / EL, HD = a.H * D;
+    for (int c = threadIdx.x & 31; c < R; c += 32) {
+        const int h = c / LH;
+        if (which == 1) {
+            float sum[1][EL], unused[1];
+            warp_sum_chunks<EL, 1, 1>(a.ws_col, 1, HD, nullptr, a.H, h, c0, c1, c, sum, unused);
+            store_dF<T, EL>(a.ws_dfr, row, HD, c, sum[0]);
+        } else {
+            float sum[4][EL], cz[2];
+            warp_sum_chunks<EL, 4, 2>(a.ws_row, 4, HD, a.ws_rowc, a.H, h, c0, c1, c, sum, cz);
+            const RowNorm nrm(cz[0], cz[1]);
+            float v[EL];
+#pragma unroll
+            for (int x = 0; x < EL; ++x) {
+                v[x] = (sum[0][x] - nrm.delta * sum[1][x]) * nrm.inv_z;
+                a.ws_da_split[(size_t)s * HD + c * EL + x] = (sum[2][x] - nrm.delta * sum[3][x]) * nrm.inv_z;
+            }
+            store_dF<T, EL>(a.ws_dfl, row, HD, c, v);
+            if (c % LH == 0) {
+                const size_t rh = (size_t)row * a.H + h;
+                a.ws_delta[rh] = nrm.delta;
+                a.ws_lse[rh] = a.lse[rh] + nrm.lse_shift;
+            }
+        }
+    }
 }
 
 // ---------------------------------------------------- backward: dst pass
@@ -383,6 +424,7 @@ gatv2_bwd_dst_kernel(Gatv2Args a) {
                 }
             }
         }
+        if (it.partial && last_chunk(a.rows, it.item)) gatv2_bwd_merge_row<T, D>(a, 0, __ldg(a.rows.chunk_split + it.item));
         st.finish_item();
     }
     st.drain();
@@ -515,58 +557,10 @@ gatv2_bwd_src_kernel(Gatv2Args a) {
                 }
             }
         }
+        if (it.partial && last_chunk(a.cols, it.item)) gatv2_bwd_merge_row<T, D>(a, 1, __ldg(a.cols.chunk_split + it.item));
         st.finish_item();
     }
     st.drain();
-}
-
-// Finish split rows, one block each.  which == 0 (destination rows): C and
-// Z are the sums of the chunk parts, normalised as in the destination pass
-// (Delta = C / Z): dFL = (sum fA - Delta sum fB) / Z, and the row's da
-// contribution (sum gA - Delta sum gB) / Z goes to its own slot; Delta and
-// lse + ln Z are stored for the source pass.  which == 1 (sources): dFR is
-// the plain sum of the chunk partials.
-template <typename T, int D>
-__global__ void __launch_bounds__(256) gatv2_bwd_merge_kernel(Gatv2Args a, int which) {
-    constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
-    __shared__ float sh[kWarpsPerBlock][4][32 * EL];
-    __shared__ float shc[kWarpsPerBlock][2][32];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t s = blockIdx.x;
-    const Partition &P = which == 0 ? a.rows : a.cols;
-    if (s >= P.n_split) return;
-    const int32_t row = P.split_rows[s];
-    const int32_t c0 = P.chunk_ptr[s], c1 = P.chunk_ptr[s + 1];
-    const int R = a.H * D / EL, HD = a.H * D;
-    for (int cb = 0; cb < R; cb += 32) {
-        const int c = cb + lane;
-        if (which == 1) {
-            float sum[1][EL], unused[2];
-            block_sum_chunks<EL, 1, 2>(a.ws_col, 1, HD, nullptr, a.H, LH, c0, c1, c, c < R,
-                                       reinterpret_cast<float (*)[1][32 * EL]>(sh), shc, sum, unused);
-            if (w == 0 && c < R) store_dF<T, EL>(a.ws_dfr, row, HD, c, sum[0]);
-        } else {
-            float sum[4][EL], cz[2];
-            block_sum_chunks<EL, 4, 2>(a.ws_row, 4, HD, a.ws_rowc, a.H, LH, c0, c1, c, c < R, sh,
-                                       shc, sum, cz);
-            if (w == 0 && c < R) {
-                const RowNorm nrm(cz[0], cz[1]);
-                float v[EL];
-#pragma unroll
-                for (int x = 0; x < EL; ++x) {
-                    v[x] = (sum[0][x] - nrm.delta * sum[1][x]) * nrm.inv_z;
-                    a.ws_da_split[(size_t)s * HD + c * EL + x] = (sum[2][x] - nrm.delta * sum[3][x]) * nrm.inv_z;
-                }
-                store_dF<T, EL>(a.ws_dfl, row, HD, c, v);
-                if (c % LH == 0) {
-                    const size_t rh = (size_t)row * a.H + c / LH;
-                    a.ws_delta[rh] = nrm.delta;
-                    a.ws_lse[rh] = a.lse[rh] + nrm.lse_shift;
-                }
-            }
-        }
-        __syncthreads();
-    }
 }
 
 // ------------------------------------------------------------ dense GEMMs
@@ -799,11 +793,7 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
         note_launch(SGA_KERN_GATV2_FWD, s, true);
         return e2;
     });
-    if (e != cudaSuccess || a.rows.n_split == 0) return e;
-    note_launch(SGA_KERN_GATV2_FWD_MERGE, s, false);
-    gt_fwd_merge_kernel<T, D, Gatv2Args><<<(unsigned)a.rows.n_split, 256, 0, s>>>(b);
-    note_launch(SGA_KERN_GATV2_FWD_MERGE, s, true);
-    return cudaGetLastError();
+    return e;   // (split rows are merged by their last chunk inside the edge kernel)
 }
 
 template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStream_t s) {
@@ -817,24 +807,13 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
                                               4096>(a.da_blocks, s, a);
         note_launch(SGA_KERN_GATV2_BWD_DST, s, true);
         if (e2 != cudaSuccess) return e2;
-        if (a.rows.n_split > 0) {   // Delta of split rows is needed by the source pass
-            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
-            gatv2_bwd_merge_kernel<T, D><<<(unsigned)a.rows.n_split, 256, 0, s>>>(a, 0);
-            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
-            if ((e2 = cudaGetLastError()) != cudaSuccess) return e2;
-        }
+        // (split rows are merged by their last chunk inside each pass; the
+        // destination pass's merges leave Delta for the source pass)
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
         if (items_c == 0) return cudaSuccess;
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, false);
         e2 = launch_streamed<Gatv2SrcStream<T, D, NC, G>, gatv2_bwd_src_kernel<T, D, NC, G>>(items_c, s, a);
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, true);
-        if (e2 != cudaSuccess) return e2;
-        if (a.cols.n_split > 0) {
-            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, false);
-            gatv2_bwd_merge_kernel<T, D><<<(unsigned)a.cols.n_split, 256, 0, s>>>(a, 1);
-            note_launch(SGA_KERN_GATV2_BWD_MERGE, s, true);
-            e2 = cudaGetLastError();
-        }
         return e2;
     });
     if (e != cudaSuccess) return e;

@@ -97,6 +97,102 @@ using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0>;
 template <typename T, int D, int NC, int G, bool BIAS = false>
 using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4, BIAS ? 4 : 0>;
 
+// ---- split rows merged by their last chunk ----------------------------------
+//
+// A chunk of a split row writes its partial and then counts itself in
+// P.arrive[split]; the warp whose arrival completes the row merges all of the
+// row's partials in chunk order (so the result does not depend on which chunk
+// finished last) and sets the count back to 0 for the next launch.  The
+// partials of other SMs are read past L1.  (The split index is looked up from
+// the chunk index here rather than carried by the edge stream, whose state is
+// at the register limit in the Graph Transformer passes.)
+__device__ __forceinline__ bool last_chunk(const Partition &P, int32_t chunk) {
+    __threadfence();   // this warp's partial before its arrival
+    __syncwarp();
+    int32_t last = 0;
+    if ((threadIdx.x & 31) == 0) {
+        const int32_t s = __ldg(P.chunk_split + chunk);
+        const int32_t k = __ldg(P.chunk_ptr + s + 1) - __ldg(P.chunk_ptr + s);
+        last = atomicAdd(P.arrive + s, 1) + 1 == k ? 1 : 0;
+        if (last) P.arrive[s] = 0;   // (every chunk of the row has arrived)
+    }
+    last = __shfl_sync(SGA_FULL_MASK, last, 0);
+    if (last) __threadfence();   // the other chunks' partials after their arrivals
+    return last != 0;
+}
+
+// Forward: fold the chunk partials of split row s with the online rule
+// (m = max, l and acc rescaled by 2^(m_c - m)) in chunk order; one warp,
+// lane-chunks lane, lane + 32, ...; out = acc / l, lse = (m + log2 l) ln 2.
+template <typename T, int D, typename A> __device__ __noinline__ void fwd_merge_row(const A &a, int32_t s) {
+    constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
+    const int32_t row = __ldg(a.rows.split_rows + s);
+    const int32_t c0 = __ldg(a.rows.chunk_ptr + s), c1 = __ldg(a.rows.chunk_ptr + s + 1);
+    const int R = a.H * D / EL, HD = a.H * D;
+    for (int c = threadIdx.x & 31; c < R; c += 32) {
+        const int h = c / LH;
+        float m = -INFINITY, l = 0.f, acc[EL];
+#pragma unroll
+        for (int x = 0; x < EL; ++x) acc[x] = 0.f;
+#pragma unroll 4
+        for (int32_t ch = c0; ch < c1; ++ch) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml + ((size_t)ch * a.H + h) * 2));
+            const float mx = fmaxf(m, ml.x);
+            const float a1 = exp2_diff(m, mx), a2 = exp2_diff(ml.x, mx);
+            const float4 *src = reinterpret_cast<const float4 *>(a.ws_acc + (size_t)ch * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4) {
+                const float4 v = __ldcg(src + x / 4);
+                acc[x] = acc[x] * a1 + v.x * a2;
+                acc[x + 1] = acc[x + 1] * a1 + v.y * a2;
+                acc[x + 2] = acc[x + 2] * a1 + v.z * a2;
+                acc[x + 3] = acc[x + 3] * a1 + v.w * a2;
+            }
+            l = l * a1 + ml.y * a2;
+            m = mx;
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        float o[EL];
+#pragma unroll
+        for (int x = 0; x < EL; ++x) o[x] = acc[x] * inv;
+        reinterpret_cast<uint4 *>(a.out_w)[(size_t)row * R + c] = pack<T>(o);
+        if (c % LH == 0) a.lse_w[(size_t)row * a.H + h] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+}
+
+// Sums over chunks c0 .. c1 - 1 (chunk order) of NCOMP [HD] partial rows
+// (component q of chunk ch at part[(ch * stride_c + q) * HD]) and of NSC
+// per-head scalars (parts_c[(ch * H + h) * NSC + t]), for lane-chunk c.
+template <int EL, int NCOMP, int NSC>
+__device__ __forceinline__ void warp_sum_chunks(const float *part, int stride_c, int HD, const float *parts_c,
+                                                int H, int h, int32_t c0, int32_t c1, int c,
+                                                float (&sum)[NCOMP][EL], float (&csum)[NSC]) {
+#pragma unroll
+    for (int q = 0; q < NCOMP; ++q)
+#pragma unroll
+        for (int x = 0; x < EL; ++x) sum[q][x] = 0.f;
+#pragma unroll
+    for (int t = 0; t < NSC; ++t) csum[t] = 0.f;
+#pragma unroll 2
+    for (int32_t ch = c0; ch < c1; ++ch) {
+#pragma unroll
+        for (int q = 0; q < NCOMP; ++q) {
+            const float4 *src = reinterpret_cast<const float4 *>(part + ((size_t)ch * stride_c + q) * HD + c * EL);
+#pragma unroll
+            for (int x = 0; x < EL; x += 4) {
+                const float4 v = __ldcg(src + x / 4);
+                sum[q][x] += v.x;
+                sum[q][x + 1] += v.y;
+                sum[q][x + 2] += v.z;
+                sum[q][x + 3] += v.w;
+            }
+        }
+        if (parts_c)
+#pragma unroll
+            for (int t = 0; t < NSC; ++t) csum[t] += __ldcg(parts_c + ((size_t)ch * H + h) * NSC + t);
+    }
+}
+
 // With BIAS, each edge's score gains a per-head term b[e, h] (fp32, [E, H] in
 // CSR edge order): s_ij = q_i . k_j / sqrt(D) + b_eh.
 template <typename T, int D, int NC, int G, bool BIAS, bool LIST>

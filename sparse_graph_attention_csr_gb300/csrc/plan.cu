@@ -292,6 +292,7 @@ __global__ void part_fill_kernel(const int32_t *__restrict__ ptr, int64_t N, int
         p.chunk_ptr[s] = c;
         for (int32_t x = b; x < e; x += C, ++c) {
             p.chunk_row[c] = (int32_t)i;
+            p.chunk_split[c] = s;
             p.chunk_beg[c] = x;
             p.chunk_end[c] = min(x + C, e);
         }
@@ -357,7 +358,10 @@ sga_status build_partition(const int32_t *ptr, int64_t N, int T, int C, Partitio
     out.chunk_row = own.get<int32_t>(out.n_chunks);
     out.chunk_beg = own.get<int32_t>(out.n_chunks);
     out.chunk_end = own.get<int32_t>(out.n_chunks);
+    out.chunk_split = own.get<int32_t>(out.n_chunks);
+    out.arrive = own.get<int32_t>(out.n_split);
     SGA_TRY(own.err);
+    if (out.n_split > 0) SGA_TRY(cudaMemsetAsync(out.arrive, 0, sizeof(int32_t) * (size_t)out.n_split, s));
     part_fill_kernel<<<grid_for(N, 256, 65535), 256, 0, s>>>(ptr, N, T, C, flag, nch, out);
     SGA_TRY(cudaGetLastError());
     return SGA_OK;

@@ -20,6 +20,11 @@ struct Partition {
     int32_t *chunk_row = nullptr;   // [n_chunks]
     int32_t *chunk_beg = nullptr;   // [n_chunks] first edge (absolute CSR offset)
     int32_t *chunk_end = nullptr;   // [n_chunks] one past the last edge
+    int32_t *chunk_split = nullptr; // [n_chunks] index of the chunk's split row
+    // [n_split] chunks of each split row finished in the current launch of an
+    // edge kernel that merges split rows itself (the last chunk to finish
+    // merges the row and sets the count back to 0); zero between launches
+    int32_t *arrive = nullptr;
     // The work items of an edge kernel in walking order: every chunk of a split
     // row (in chunk order), then every row of degree <= the threshold, by
     // descending degree (ties by id) or by ascending id.  n_items entries;

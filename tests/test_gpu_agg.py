@@ -121,9 +121,10 @@ def test_autograd_function_and_plan_kind_checks():
     N = len(indptr) - 1
     ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
     plan = sga.Plan(ip, ix, 2, 64, torch.float32, layer=sga.SGA_LAYER_MINMAX)
-    X = torch.randn(N, 2, 64, device="cuda", requires_grad=True)
+    gen = torch.Generator().manual_seed(8)   # seeded: the same draw in every process
+    X = torch.randn(N, 2, 64, generator=gen).cuda().requires_grad_()
     out = sga.MinMaxAggregation.apply(X, plan, "max")
-    g = torch.randn_like(out)
+    g = torch.randn(tuple(out.shape), generator=gen).cuda()
     out.backward(g)
     ro, ra = oracle.agg_fwd(indptr, indices, X.detach().double().cpu().numpy(), "max")
     assert np.array_equal(out.detach().double().cpu().numpy(), ro)

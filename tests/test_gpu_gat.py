@@ -102,11 +102,12 @@ def test_small_workload_recipe_and_autograd():
     plan = sga.Plan(ip, ix, H, D, torch.float32, layer=sga.SGA_LAYER_GAT)
     # features of O(1/sqrt(D)) keep dOut . Fv O(1), as the other fp32 cases keep
     # their scores: with O(1) features the hub sources' fp32 sums sit at 1e-5
-    Fv = (torch.randn(N, H, D, device="cuda") / math.sqrt(D)).requires_grad_()
-    el = torch.randn(N, H, device="cuda", requires_grad=True)
-    er = torch.randn(N, H, device="cuda", requires_grad=True)
+    gen = torch.Generator().manual_seed(7)   # seeded: the same draw in every process
+    Fv = (torch.randn(N, H, D, generator=gen) / math.sqrt(D)).cuda().requires_grad_()
+    el = torch.randn(N, H, generator=gen).cuda().requires_grad_()
+    er = torch.randn(N, H, generator=gen).cuda().requires_grad_()
     out = sga.GATEdgeAttention.apply(Fv, el, er, plan, 0.2)
-    g = torch.randn_like(out)
+    g = torch.randn(tuple(out.shape), generator=gen).cuda()
     out.backward(g)
     h = lambda t: t.detach().double().cpu().numpy()
     rv, rdl, rdr = oracle.gat_edge_bwd(indptr, indices, h(Fv), h(el), h(er), h(g))
