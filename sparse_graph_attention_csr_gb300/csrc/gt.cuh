@@ -80,22 +80,22 @@ struct RingDims {
     static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
 };
 template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC, int U2 = 1, int U1 = 2, int ESC = 0,
-          bool LIST = true>
+          bool LIST = true, bool W32 = false>
 using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::U, NROW, NSC, NOWN, NOSC,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
-                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST>;
+                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST, W32>;
 
 // gathered K, V (and the edge's score bias); own Q.  LIST = false: no item
 // list (the no-allocation forward, which has no plan)
 template <typename T, int D, int NC, int G, bool BIAS = false, bool LIST = true>
-using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4, BIAS ? 1 : 0, LIST>;
+using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4, BIAS ? 1 : 0, LIST, true>;
 // gathered K, V (and the edge's score bias); own Q, dOut, lse
 template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0>;
+using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0, true, true>;
 // gathered Q, dOut, lse, Delta (over the transposed CSR; and the edge's score
 // bias in transposed order); own K, V
 template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4, BIAS ? 4 : 0>;
+using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4, BIAS ? 4 : 0, true, true>;
 
 // ---- split rows merged by their last chunk ----------------------------------
 //

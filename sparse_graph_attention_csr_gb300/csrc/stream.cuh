@@ -59,8 +59,13 @@ __device__ __forceinline__ void cp_wait_newer(int n) {
 }
 
 template <int NC_, int G_, int U_, int NROW_, int NSC_, int NOWN_, int NOSC_, int DEPTH_, int QD_,
-          int ESC_ = 0, bool LIST_ = true>
+          int ESC_ = 0, bool LIST_ = true, bool W32_ = false>
 struct StreamCfg {
+    // W32: the row copies take 32-bit byte offsets from the array bases when
+    // every gathered row array is below 4 GB (checked at run time; 64-bit
+    // offsets otherwise).  Fewer address instructions per copy, but the two
+    // copies of the step enlarge the code; shapes that gain use it.
+    static constexpr bool W32 = W32_;
     // walk the plan's item list (else: chunks, then all rows by id)
     static constexpr bool LIST = LIST_;
     static_assert(NSC_ <= 3, "at most three gathered scalar arrays");
@@ -125,6 +130,7 @@ template <typename C> struct EdgeStream {
     int64_t stride, n_items;
     int lane, g, gl;
     uint32_t c_in;           // bit k: this lane's chunk gl + G k of a row exists (< R)
+    bool off32;              // W32 and every gathered row array below 4 GB: 32-bit byte offsets
     // producer
     int64_t nx_item;         // next item to consider
     ItemMeta m1, m2;         // descriptors of nx_item and nx_item + stride
@@ -159,6 +165,7 @@ template <typename C> struct EdgeStream {
         c_in = 0;
 #pragma unroll
         for (int k = 0; k < C::NC; ++k) c_in |= (gl + C::G * k < R ? 1u : 0u) << k;
+        off32 = C::W32 && (uint64_t)N * (uint64_t)R * 16u <= 0xffffffffull;
         stride = (int64_t)gridDim.x * (blockDim.x >> 5);
         n_items = C::LIST ? P.n_items : (int64_t)P.n_chunks + N;
         nx_item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -241,7 +248,17 @@ template <typename C> struct EdgeStream {
         }
     }
 
+    // (two copies of the step, one per address width, chosen once per step)
     __device__ __forceinline__ void issue_step() {
+        if constexpr (C::W32) {
+            if (off32) {
+                issue_step_w<true>();
+                return;
+            }
+        }
+        issue_step_w<false>();
+    }
+    template <bool O32> __device__ __forceinline__ void issue_step_w() {
         const int slot = p_slot;
         const int32_t e0 = p_step * C::STEP;   // item-local first edge of the step
         uint32_t masks[4] = {0u, 0u, 0u, 0u};
@@ -257,15 +274,29 @@ template <typename C> struct EdgeStream {
             const bool ok = e < p_deg && j >= 0;
             // a copy that is skipped (src-size 0) still names an address inside the
             // array: row 0 for a missing neighbour, chunk 0 for a lane past the row
-            const size_t roff = (size_t)(uint32_t)(ok ? j : 0) * R;
+            if constexpr (O32) {   // byte offsets from the array bases fit 32 bits
+                const uint32_t boff = (uint32_t)(ok ? j : 0) * (uint32_t)(R * 16);
 #pragma unroll
-            for (int k = 0; k < C::NC; ++k) {
-                const bool cin = (c_in >> k) & 1u;
-                const size_t off = roff + (cin ? gl + C::G * k : 0);
-                const uint32_t sz = (ok && cin) ? 16u : 0u;
+                for (int k = 0; k < C::NC; ++k) {
+                    const bool cin = (c_in >> k) & 1u;
+                    const uint32_t koff = boff + (cin ? (uint32_t)(gl + C::G * k) * 16u : 0u);
+                    const uint32_t sz = (ok && cin) ? 16u : 0u;
 #pragma unroll
-                for (int r = 0; r < C::NROW; ++r)
-                    cp16_async_sz(dst0 + ((u * C::NROW + r) * C::NC + k) * 32 * 16, arr.rows[r] + off, sz);
+                    for (int r = 0; r < C::NROW; ++r)
+                        cp16_async_sz(dst0 + ((u * C::NROW + r) * C::NC + k) * 32 * 16,
+                                      reinterpret_cast<const unsigned char *>(arr.rows[r]) + koff, sz);
+                }
+            } else {
+                const size_t roff = (size_t)(uint32_t)(ok ? j : 0) * R;
+#pragma unroll
+                for (int k = 0; k < C::NC; ++k) {
+                    const bool cin = (c_in >> k) & 1u;
+                    const size_t off = roff + (cin ? gl + C::G * k : 0);
+                    const uint32_t sz = (ok && cin) ? 16u : 0u;
+#pragma unroll
+                    for (int r = 0; r < C::NROW; ++r)
+                        cp16_async_sz(dst0 + ((u * C::NROW + r) * C::NC + k) * 32 * 16, arr.rows[r] + off, sz);
+                }
             }
             if (gl < H)
 #pragma unroll
