@@ -80,22 +80,23 @@ struct RingDims {
     static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
 };
 template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC, int U2 = 1, int U1 = 2, int ESC = 0,
-          bool LIST = true, bool W32 = false>
+          bool LIST = true, bool W32 = false, bool DYN = false>
 using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::U, NROW, NSC, NOWN, NOSC,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
-                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST, W32>;
+                          RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST, W32, DYN>;
 
 // gathered K, V (and the edge's score bias); own Q.  LIST = false: no item
 // list (the no-allocation forward, which has no plan)
 template <typename T, int D, int NC, int G, bool BIAS = false, bool LIST = true>
-using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4, BIAS ? 1 : 0, LIST, true>;
+using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4, BIAS ? 1 : 0, LIST, true, LIST>;
 // gathered K, V (and the edge's score bias); own Q, dOut, lse
 template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0, true, true>;
+// (dynamic items on one-chunk rows only: the extra state spills the two-chunk dQ pass)
+using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0, true, true, NC == 1>;
 // gathered Q, dOut, lse, Delta (over the transposed CSR; and the edge's score
 // bias in transposed order); own K, V
 template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4, BIAS ? 4 : 0, true, true>;
+using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4, BIAS ? 4 : 0, true, true, true>;
 
 // ---- split rows merged by their last chunk ----------------------------------
 //
@@ -880,6 +881,8 @@ template <typename T, int D, bool BIAS, bool LIST> cudaError_t gt_fwd_db(const G
     const int64_t items = (int64_t)a.rows.n_chunks + a.N;
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
+        // (planned launches take their items from the partition's counter)
+        if (LIST && cudaMemsetAsync(a.rows.next, 0, sizeof(int32_t), s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GT_FWD, s, false);
         const cudaError_t e =
             launch_streamed<GtFwdStream<T, D, NC, G, BIAS, LIST>, gt_fwd_kernel<T, D, NC, G, BIAS, LIST>>(
@@ -928,6 +931,8 @@ template <typename T, int D, bool BIAS> cudaError_t gt_bwd_db(const GtArgs &a, c
                 if (e0 != cudaSuccess) return e0;
             }
         }
+        if (GtDqStream<T, D, NC, G, BIAS>::DYN && cudaMemsetAsync(a.rows.next, 0, sizeof(int32_t), s) != cudaSuccess)
+            return cudaGetLastError();
         note_launch(SGA_KERN_GT_BWD_DQ, s, false);
         cudaError_t e = launch_streamed<GtDqStream<T, D, NC, G, BIAS>, gt_bwd_dq_kernel<T, D, NC, G, BIAS>>(
             items_r, s, a, scale2, scale);
@@ -939,6 +944,7 @@ template <typename T, int D, bool BIAS> cudaError_t gt_bwd_db(const GtArgs &a, c
             note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
+        if (cudaMemsetAsync(a.cols.next, 0, sizeof(int32_t), s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GT_BWD_DKDV, s, false);
         e = launch_streamed<GtDkdvStream<T, D, NC, G, BIAS>, gt_bwd_dkdv_kernel<T, D, NC, G, BIAS>>(
             items_c, s, a, scale2, scale);

@@ -360,6 +360,7 @@ sga_status build_partition(const int32_t *ptr, int64_t N, int T, int C, Partitio
     out.chunk_end = own.get<int32_t>(out.n_chunks);
     out.chunk_split = own.get<int32_t>(out.n_chunks);
     out.arrive = own.get<int32_t>(out.n_split);
+    out.next = own.get<int32_t>(1);
     SGA_TRY(own.err);
     if (out.n_split > 0) SGA_TRY(cudaMemsetAsync(out.arrive, 0, sizeof(int32_t) * (size_t)out.n_split, s));
     part_fill_kernel<<<grid_for(N, 256, 65535), 256, 0, s>>>(ptr, N, T, C, flag, nch, out);

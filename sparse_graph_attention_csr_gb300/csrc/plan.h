@@ -21,6 +21,7 @@ struct Partition {
     int32_t *chunk_beg = nullptr;   // [n_chunks] first edge (absolute CSR offset)
     int32_t *chunk_end = nullptr;   // [n_chunks] one past the last edge
     int32_t *chunk_split = nullptr; // [n_chunks] index of the chunk's split row
+    int32_t *next = nullptr;        // [1] next item of a launch that takes its items dynamically
     // [n_split] chunks of each split row finished in the current launch of an
     // edge kernel that merges split rows itself (the last chunk to finish
     // merges the row and sets the count back to 0); zero between launches

@@ -59,13 +59,18 @@ __device__ __forceinline__ void cp_wait_newer(int n) {
 }
 
 template <int NC_, int G_, int U_, int NROW_, int NSC_, int NOWN_, int NOSC_, int DEPTH_, int QD_,
-          int ESC_ = 0, bool LIST_ = true, bool W32_ = false>
+          int ESC_ = 0, bool LIST_ = true, bool W32_ = false, bool DYN_ = false>
 struct StreamCfg {
     // W32: the row copies take 32-bit byte offsets from the array bases when
     // every gathered row array is below 4 GB (checked at run time; 64-bit
     // offsets otherwise).  Fewer address instructions per copy, but the two
     // copies of the step enlarge the code; shapes that gain use it.
     static constexpr bool W32 = W32_;
+    // DYN: warps take their items from the partition's counter (P.next, zeroed
+    // before each launch) in list order, instead of the fixed share w, w + S,
+    // ...: the descending-degree list is then consumed largest first by
+    // whichever warp is free, so no warp is left with the last long items.
+    static constexpr bool DYN = DYN_;
     // walk the plan's item list (else: chunks, then all rows by id)
     static constexpr bool LIST = LIST_;
     static_assert(NSC_ <= 3, "at most three gathered scalar arrays");
@@ -133,7 +138,8 @@ template <typename C> struct EdgeStream {
     bool off32;              // W32 and every gathered row array below 4 GB: 32-bit byte offsets
     // producer
     int64_t nx_item;         // next item to consider
-    ItemMeta m1, m2;         // descriptors of nx_item and nx_item + stride
+    int64_t nx2;             // DYN: the item after it (else nx_item + stride)
+    ItemMeta m1, m2;         // descriptors of nx_item and the item after it
     int32_t ids1;            // first id batch of nx_item (when valid)
     bool v1;                 // nx_item is a valid item (its ids1 were issued)
     ItemRange r1;
@@ -168,9 +174,16 @@ template <typename C> struct EdgeStream {
         off32 = C::W32 && (uint64_t)N * (uint64_t)R * 16u <= 0xffffffffull;
         stride = (int64_t)gridDim.x * (blockDim.x >> 5);
         n_items = C::LIST ? P.n_items : (int64_t)P.n_chunks + N;
-        nx_item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-        meta_issue<C::LIST>(nx_item, P, ptr, N, m1);
-        meta_issue<C::LIST>(nx_item + stride, P, ptr, N, m2);
+        if constexpr (C::DYN) {
+            nx_item = fetch_item();
+            nx2 = fetch_item();
+            meta_issue<C::LIST>(nx_item, P, ptr, N, m1);
+            meta_issue<C::LIST>(nx2, P, ptr, N, m2);
+        } else {   // (nx2 is not kept: nx_item + stride)
+            nx_item = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+            meta_issue<C::LIST>(nx_item, P, ptr, N, m1);
+            meta_issue<C::LIST>(nx_item + stride, P, ptr, N, m2);
+        }
         v1 = meta_eval<C::LIST>(nx_item, m1, P, threshold, r1);
         ids1 = first_ids(ids, r1, v1);
         p_beg = p_deg = p_step = p_nsteps = 0;
@@ -182,6 +195,13 @@ template <typename C> struct EdgeStream {
     }
 
     // ---- producer ----------------------------------------------------------
+
+    // The next item of the launch's list (DYN): one atomic of lane 0.
+    __device__ __forceinline__ int64_t fetch_item() {
+        int32_t v = 0;
+        if (lane == 0) v = atomicAdd(P.next, 1);
+        return __shfl_sync(SGA_FULL_MASK, v, 0);
+    }
 
     // Queue the next item to be processed here; false when there is none.
     __device__ __forceinline__ bool advance_item() {
@@ -195,9 +215,15 @@ template <typename C> struct EdgeStream {
             const int64_t cur = nx_item;
             int32_t first = ids1;
             // rotate the descriptor pipeline
-            nx_item += stride;
             m1 = m2;
-            meta_issue<C::LIST>(nx_item + stride, P, ptr, N, m2);
+            if constexpr (C::DYN) {
+                nx_item = nx2;
+                nx2 = fetch_item();
+                meta_issue<C::LIST>(nx2, P, ptr, N, m2);
+            } else {
+                nx_item += stride;
+                meta_issue<C::LIST>(nx_item + stride, P, ptr, N, m2);
+            }
             v1 = meta_eval<C::LIST>(nx_item, m1, P, threshold, r1);
             ids1 = first_ids(ids, r1, v1);
             if (!valid) continue;   // a row above the split threshold: its chunks cover it

@@ -141,3 +141,36 @@ def test_projection_shapes_growing_within_one_process():
     r = subprocess.run([sys.executable, "-c", _GROWING_SHAPES], cwd=root, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+def test_repeated_calls_on_one_plan_are_identical():
+    """The GATv2 passes merge a split row in whichever warp finishes the row's
+    last chunk, counting arrivals in the plan and resetting the count after
+    the merge; a second forward and backward on the same plan (and a third
+    with the rows' chunks in flight together with another plan's) must give
+    bit-identical results, so no count is left over between launches."""
+    rng = np.random.default_rng(31)
+    indptr, indices = random_csr(rng, 600, 6, hubs=[(2, 590), (300, 400), (599, 333)])
+    N, F, H, D = len(indptr) - 1, 64, 2, 64
+    ip, ix = dev(torch.from_numpy(indptr)), dev(torch.from_numpy(indices))
+    plan = sga.Plan(ip, ix, H, D, torch.bfloat16, F=F, split_threshold=64, chunk_len=16)
+    other = sga.Plan(ip, ix, H, D, torch.bfloat16, F=F, split_threshold=64, chunk_len=16)
+    g = torch.Generator().manual_seed(3)
+    X = torch.randn(N, F, generator=g).to(torch.bfloat16).cuda()
+    W = [(torch.randn(F, H * D, generator=g) * 0.1).to(torch.bfloat16).cuda() for _ in range(2)]
+    a = (torch.randn(H, D, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    dO = torch.randn(N, H, D, generator=g).to(torch.bfloat16).cuda()
+
+    def run(p):
+        FL, FR, out, lse = sga.gatv2_fwd(p, X, W[0], W[1], a)
+        grads = sga.gatv2_bwd(p, X, W[0], W[1], a, FL, FR, out, lse, dO)
+        return [t.clone() for t in (out, lse) + tuple(grads)]
+
+    first = run(plan)
+    second = run(plan)
+    run(other)
+    third = run(plan)
+    torch.cuda.synchronize()
+    for x, y, z in zip(first, second, third):
+        assert torch.equal(x, y) and torch.equal(x, z)
+    assert plan.device_error() == 0
