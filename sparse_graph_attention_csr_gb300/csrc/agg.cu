@@ -27,7 +27,7 @@
 namespace sga {
 
 // gathered X rows; no own rows or scalars
-template <int NC, int G> using AggStream = RingCfg<NC, G, 1, 0, 0, 0, 2, 4>;
+template <int NC, int G> using AggStream = RingCfg<NC, G, 1, 0, 0, 0, 2, 4, 0, true, false, true>;
 
 template <bool MAX> __device__ __forceinline__ bool better(float v, float b) {
     return MAX ? v > b : v < b;
@@ -305,6 +305,7 @@ template <typename T, bool MAX> cudaError_t agg_fwd_op(const AggArgs &a, cudaStr
     }
     cudaError_t e = dispatch_shape<1, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
+        if (reset_items<AggStream<NC, G>>(a.rows, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_AGG_FWD, s, false);
         const cudaError_t e = launch_streamed<AggStream<NC, G>, agg_fwd_kernel<T, MAX, NC, G>>(items, s, a);
         note_launch(SGA_KERN_AGG_FWD, s, true);

@@ -52,6 +52,8 @@ __device__ __forceinline__ void store_dF(float *ws, int64_t row, int HD, int c, 
 // gathered FR; own FL
 template <typename T, int D, int NC, int G> using Gatv2FwdStream = RingCfg<NC, G, 1, 0, 1, 0>;
 // gathered FR; own FL, dOut, lse
+// (a fixed share of items: each block's da partial must sum the same rows in
+// every launch for da to be reproducible)
 template <typename T, int D, int NC, int G> using Gatv2DstStream = RingCfg<NC, G, 1, 0, 2, 1>;
 // gathered FL, dOut, lse, Delta (transposed CSR); own FR
 template <typename T, int D, int NC, int G> using Gatv2SrcStream = RingCfg<NC, G, 2, 2, 1, 0>;
@@ -787,6 +789,7 @@ template <typename T, int D> cudaError_t gatv2_fwd_d(const Gatv2Args &a, cudaStr
     const int64_t items = (int64_t)a.rows.n_chunks + a.N;
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
+        if (reset_items<Gatv2FwdStream<T, D, NC, G>>(a.rows, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GATV2_FWD, s, false);
         const cudaError_t e2 =
             launch_streamed<Gatv2FwdStream<T, D, NC, G>, gatv2_fwd_kernel<T, D, NC, G>>(items, s, b);
@@ -801,6 +804,7 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
     const int R = a.H * D / Elt<T>::EL;
     const int HD = a.H * D;
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
+        if (reset_items<Gatv2DstStream<T, D, NC, G>>(a.rows, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GATV2_BWD_DST, s, false);
         // one da partial per block: exactly da_blocks blocks
         cudaError_t e2 = launch_streamed_grid<Gatv2DstStream<T, D, NC, G>, gatv2_bwd_dst_kernel<T, D, NC, G>,
@@ -811,6 +815,7 @@ template <typename T, int D> cudaError_t gatv2_bwd_d(const Gatv2Args &a, cudaStr
         // destination pass's merges leave Delta for the source pass)
         const int64_t items_c = (int64_t)a.cols.n_chunks + a.N;
         if (items_c == 0) return cudaSuccess;
+        if (reset_items<Gatv2SrcStream<T, D, NC, G>>(a.cols, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, false);
         e2 = launch_streamed<Gatv2SrcStream<T, D, NC, G>, gatv2_bwd_src_kernel<T, D, NC, G>>(items_c, s, a);
         note_launch(SGA_KERN_GATV2_BWD_SRC, s, true);

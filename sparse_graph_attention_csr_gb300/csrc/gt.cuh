@@ -815,6 +815,13 @@ template <typename C, int STATIC = 0> constexpr int stream_warps() {
     return fit >= kWarpsPerBlock ? kWarpsPerBlock : (fit > 0 ? fit : 1);
 }
 
+// Zero the partition's item counter before a launch whose stream takes its
+// items dynamically (StreamCfg::DYN).
+template <typename C> cudaError_t reset_items(const Partition &P, cudaStream_t s) {
+    if constexpr (C::DYN) return cudaMemsetAsync(P.next, 0, sizeof(int32_t), s);
+    return cudaSuccess;
+}
+
 // Launch a persistent streamed kernel over `items` work items.
 template <typename C, auto Kernel, typename... Args>
 cudaError_t launch_streamed(int64_t items, cudaStream_t s, Args... args) {
@@ -881,8 +888,7 @@ template <typename T, int D, bool BIAS, bool LIST> cudaError_t gt_fwd_db(const G
     const int64_t items = (int64_t)a.rows.n_chunks + a.N;
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
         if (items == 0) return cudaSuccess;
-        // (planned launches take their items from the partition's counter)
-        if (LIST && cudaMemsetAsync(a.rows.next, 0, sizeof(int32_t), s) != cudaSuccess) return cudaGetLastError();
+        if (reset_items<GtFwdStream<T, D, NC, G, BIAS, LIST>>(a.rows, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GT_FWD, s, false);
         const cudaError_t e =
             launch_streamed<GtFwdStream<T, D, NC, G, BIAS, LIST>, gt_fwd_kernel<T, D, NC, G, BIAS, LIST>>(
@@ -931,8 +937,7 @@ template <typename T, int D, bool BIAS> cudaError_t gt_bwd_db(const GtArgs &a, c
                 if (e0 != cudaSuccess) return e0;
             }
         }
-        if (GtDqStream<T, D, NC, G, BIAS>::DYN && cudaMemsetAsync(a.rows.next, 0, sizeof(int32_t), s) != cudaSuccess)
-            return cudaGetLastError();
+        if (reset_items<GtDqStream<T, D, NC, G, BIAS>>(a.rows, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GT_BWD_DQ, s, false);
         cudaError_t e = launch_streamed<GtDqStream<T, D, NC, G, BIAS>, gt_bwd_dq_kernel<T, D, NC, G, BIAS>>(
             items_r, s, a, scale2, scale);
@@ -944,7 +949,7 @@ template <typename T, int D, bool BIAS> cudaError_t gt_bwd_db(const GtArgs &a, c
             note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        if (cudaMemsetAsync(a.cols.next, 0, sizeof(int32_t), s) != cudaSuccess) return cudaGetLastError();
+        if (reset_items<GtDkdvStream<T, D, NC, G, BIAS>>(a.cols, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GT_BWD_DKDV, s, false);
         e = launch_streamed<GtDkdvStream<T, D, NC, G, BIAS>, gt_bwd_dkdv_kernel<T, D, NC, G, BIAS>>(
             items_c, s, a, scale2, scale);
