@@ -91,8 +91,7 @@ template <typename T, int D, int NC, int G, bool BIAS = false, bool LIST = true>
 using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4, BIAS ? 1 : 0, LIST, true, LIST>;
 // gathered K, V (and the edge's score bias); own Q, dOut, lse
 template <typename T, int D, int NC, int G, bool BIAS = false>
-// (dynamic items on one-chunk rows only: the extra state spills the two-chunk dQ pass)
-using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0, true, true, NC == 1>;
+using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0, true, true, true>;
 // gathered Q, dOut, lse, Delta (over the transposed CSR; and the edge's score
 // bias in transposed order); own K, V
 template <typename T, int D, int NC, int G, bool BIAS = false>

@@ -24,6 +24,8 @@
 // when it has nothing to issue) without breaking the pipeline.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "items.cuh"
 #include "plan.h"
@@ -137,8 +139,9 @@ template <typename C> struct EdgeStream {
     uint32_t c_in;           // bit k: this lane's chunk gl + G k of a row exists (< R)
     bool off32;              // W32 and every gathered row array below 4 GB: 32-bit byte offsets
     // producer
-    int64_t nx_item;         // next item to consider
-    int64_t nx2;             // DYN: the item after it (else nx_item + stride)
+    // next item to consider, and (DYN) the one after it (else nx_item + stride);
+    // 32-bit under DYN, whose items come from a 32-bit counter
+    std::conditional_t<C::DYN, uint32_t, int64_t> nx_item, nx2;
     ItemMeta m1, m2;         // descriptors of nx_item and the item after it
     int32_t ids1;            // first id batch of nx_item (when valid)
     bool v1;                 // nx_item is a valid item (its ids1 were issued)
@@ -197,16 +200,16 @@ template <typename C> struct EdgeStream {
     // ---- producer ----------------------------------------------------------
 
     // The next item of the launch's list (DYN): one atomic of lane 0.
-    __device__ __forceinline__ int64_t fetch_item() {
-        int32_t v = 0;
-        if (lane == 0) v = atomicAdd(P.next, 1);
+    __device__ __forceinline__ uint32_t fetch_item() {
+        uint32_t v = 0;
+        if (lane == 0) v = atomicAdd(reinterpret_cast<unsigned int *>(P.next), 1u);
         return __shfl_sync(SGA_FULL_MASK, v, 0);
     }
 
     // Queue the next item to be processed here; false when there is none.
     __device__ __forceinline__ bool advance_item() {
         for (;;) {
-            if (nx_item >= n_items || m1.row < 0) {
+            if ((int64_t)nx_item >= n_items || m1.row < 0) {
                 p_done = true;
                 return false;
             }
