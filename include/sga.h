@@ -408,9 +408,11 @@ typedef enum {
     SGA_KERN_GAT_FWD = 23, SGA_KERN_GAT_BWD_DST = 24, SGA_KERN_GAT_BWD_SRC = 25,
     SGA_KERN_COUNT = 26
 } sga_kernel_id;
-/* (The GATv2 passes merge their split rows inside the edge kernels -- the
- * last chunk of a row to finish merges it -- so SGA_KERN_GATV2_FWD_MERGE and
- * SGA_KERN_GATV2_BWD_MERGE are no longer launched.) */
+/* (Planned Graph Transformer and GATv2 passes merge their split rows inside
+ * the edge kernels -- the last chunk of a row to finish merges it -- so
+ * SGA_KERN_GT_BWD_MERGE, SGA_KERN_GATV2_FWD_MERGE and SGA_KERN_GATV2_BWD_MERGE
+ * are no longer launched, and SGA_KERN_GT_FWD_MERGE only by
+ * gt_attn_fwd_noalloc.) */
 
 /* Time one kernel kind with CUDA events recorded on the launching stream
  * around each of its launches (at most 4096 launches per window).

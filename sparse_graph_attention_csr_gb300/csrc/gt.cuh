@@ -99,6 +99,11 @@ using GtDkdvStream = RingCfg<NC, G, 2, BIAS ? 3 : 2, 2, 0, 1, 4, BIAS ? 4 : 0, t
 
 // ---- split rows merged by their last chunk ----------------------------------
 //
+// The Graph Transformer passes merge this way on rows of two or more chunks
+// per lane; on one-chunk rows the merge call cost the main loop more than
+// the separate merge kernels cost (workload 4), so those keep the kernels.
+template <int NC> constexpr bool gt_fold() { return NC >= 2; }
+//
 // A chunk of a split row writes its partial and then counts itself in
 // P.arrive[split]; the warp whose arrival completes the row merges all of the
 // row's partials in chunk order (so the result does not depend on which chunk
@@ -313,6 +318,9 @@ gt_fwd_kernel(GtArgs a, float scale2) {
                 }
             }
         }
+        if constexpr (LIST && gt_fold<NC>()) {   // the last chunk of a split row merges the row
+            if (it.partial && last_chunk(a.rows, it.item)) fwd_merge_row<T, D>(a, __ldg(a.rows.chunk_split + it.item));
+        }
         st.finish_item();
     }
     st.drain();
@@ -464,6 +472,43 @@ struct RowNorm {
         lse_shift = z > 0.f ? logf(z) : 0.f;
     }
 };
+
+// Backward: finish split row s in one warp (chunk order).  which == 0: dQ
+// rows (C and Z are the sums of the chunk parts, normalised as in the dQ
+// pass; Delta and lse + ln Z stored for the dK/dV pass).  which == 1: dK, dV
+// of split sources (plain sums).
+template <typename T, int D>
+__device__ __noinline__ void gt_bwd_merge_row(const GtArgs &a, float scale, int which, int32_t s) {
+    constexpr int EL = Elt<T>::EL, LH = D * (int)sizeof(T) / 16;
+    const Partition &P = which == 0 ? a.rows : a.cols;
+    const int32_t row = __ldg(P.split_rows + s);
+    const int32_t c0 = __ldg(P.chunk_ptr + s), c1 = __ldg(P.chunk_ptr + s + 1);
+    const int R = a.H * D / EL, HD = a.H * D;
+    for (int c = threadIdx.x & 31; c < R; c += 32) {
+        const int h = c / LH;
+        float sum[2][EL], cz[2];
+        warp_sum_chunks<EL, 2, 2>(which == 0 ? a.ws_row : a.ws_col, 2, HD, which == 0 ? a.ws_rowc : nullptr,
+                                  a.H, h, c0, c1, c, sum, cz);
+        if (which == 0) {
+            const size_t rh = (size_t)row * a.H + h;
+            const RowNorm nrm(cz[0] + (a.delta_in ? a.delta_in[rh] : 0.f), cz[1] + (a.z_in ? a.z_in[rh] : 0.f));
+            const float sc = scale * nrm.inv_z;
+            float o[EL];
+#pragma unroll
+            for (int x = 0; x < EL; ++x) o[x] = (sum[0][x] - nrm.delta * sum[1][x]) * sc;
+            reinterpret_cast<uint4 *>(a.dQ)[(size_t)row * R + c] = pack<T>(o);
+            if (c % LH == 0) {
+                a.ws_delta[rh] = nrm.delta;
+                a.ws_lse[rh] = a.lse[rh] + nrm.lse_shift;
+            }
+        } else {
+#pragma unroll
+            for (int x = 0; x < EL; ++x) sum[0][x] *= scale;
+            reinterpret_cast<uint4 *>(a.dK)[(size_t)row * R + c] = pack<T>(sum[0]);
+            reinterpret_cast<uint4 *>(a.dV)[(size_t)row * R + c] = pack<T>(sum[1]);
+        }
+    }
+}
 
 // ---------------------------------------------------------- backward: dQ
 
@@ -621,6 +666,10 @@ gt_bwd_dq_kernel(GtArgs a, float scale2, float scale) {
                 }
             }
         }
+        if constexpr (gt_fold<NC>()) {
+            if (it.partial && last_chunk(a.rows, it.item))
+                gt_bwd_merge_row<T, D>(a, scale, 0, __ldg(a.rows.chunk_split + it.item));
+        }
         st.finish_item();
     }
     st.drain();
@@ -729,6 +778,10 @@ gt_bwd_dkdv_kernel(GtArgs a, float scale2, float scale) {
                     reinterpret_cast<uint4 *>(a.dV)[(size_t)it.row * R + c] = pack<T>(dv[k]);
                 }
             }
+        }
+        if constexpr (gt_fold<NC>()) {
+            if (it.partial && last_chunk(a.cols, it.item))
+                gt_bwd_merge_row<T, D>(a, scale, 1, __ldg(a.cols.chunk_split + it.item));
         }
         st.finish_item();
     }
@@ -885,7 +938,9 @@ template <typename T, int D, bool BIAS, bool LIST> cudaError_t gt_fwd_db(const G
     const int R = a.H * D / Elt<T>::EL;
     const float scale2 = kLog2e / sqrtf((float)D);
     const int64_t items = (int64_t)a.rows.n_chunks + a.N;
+    bool folded = false;   // the edge kernel merges the split rows itself
     cudaError_t e = dispatch_shape<LH, max_nc<T>()>(R, [&]<int NC, int G>() -> cudaError_t {
+        folded = LIST && gt_fold<NC>();
         if (items == 0) return cudaSuccess;
         if (reset_items<GtFwdStream<T, D, NC, G, BIAS, LIST>>(a.rows, s) != cudaSuccess) return cudaGetLastError();
         note_launch(SGA_KERN_GT_FWD, s, false);
@@ -895,7 +950,7 @@ template <typename T, int D, bool BIAS, bool LIST> cudaError_t gt_fwd_db(const G
         note_launch(SGA_KERN_GT_FWD, s, true);
         return e;
     });
-    if (e != cudaSuccess || a.rows.n_split == 0) return e;
+    if (e != cudaSuccess || a.rows.n_split == 0 || folded) return e;
     note_launch(SGA_KERN_GT_FWD_MERGE, s, false);
     gt_fwd_merge_kernel<T, D, GtArgs><<<(unsigned)a.rows.n_split, 256, 0, s>>>(a);
     note_launch(SGA_KERN_GT_FWD_MERGE, s, true);
@@ -942,7 +997,7 @@ template <typename T, int D, bool BIAS> cudaError_t gt_bwd_db(const GtArgs &a, c
             items_r, s, a, scale2, scale);
         note_launch(SGA_KERN_GT_BWD_DQ, s, true);
         if (e != cudaSuccess) return e;
-        if (a.rows.n_split > 0) {   // Delta of split rows is needed by the dK/dV pass
+        if (!gt_fold<NC>() && a.rows.n_split > 0) {   // Delta of split rows is needed by the dK/dV pass
             note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
             gt_bwd_merge_kernel<T, D><<<(unsigned)a.rows.n_split, 256, 0, s>>>(a, scale, 0);
             note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
@@ -954,7 +1009,7 @@ template <typename T, int D, bool BIAS> cudaError_t gt_bwd_db(const GtArgs &a, c
             items_c, s, a, scale2, scale);
         note_launch(SGA_KERN_GT_BWD_DKDV, s, true);
         if (e != cudaSuccess) return e;
-        if (a.cols.n_split > 0) {
+        if (!gt_fold<NC>() && a.cols.n_split > 0) {
             note_launch(SGA_KERN_GT_BWD_MERGE, s, false);
             gt_bwd_merge_kernel<T, D><<<(unsigned)a.cols.n_split, 256, 0, s>>>(a, scale, 1);
             note_launch(SGA_KERN_GT_BWD_MERGE, s, true);
