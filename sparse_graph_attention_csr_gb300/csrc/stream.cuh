@@ -300,7 +300,10 @@ template <typename C> struct EdgeStream {
         for (int u = 0; u < C::U; ++u) {
             const int32_t e = e0 + g + C::NG * u;
             const int32_t j = __shfl_sync(SGA_FULL_MASK, p_ids, e & 31);
-            const bool ok = e < p_deg && j >= 0;
+            // (ids past the item's last edge, like out-of-range ids, are -1: a
+            // step never straddles a batch of 32, and a batch's lanes past
+            // the item hold -1)
+            const bool ok = j >= 0;
             // a copy that is skipped (src-size 0) still names an address inside the
             // array: row 0 for a missing neighbour, chunk 0 for a lane past the row
             if constexpr (O32) {   // byte offsets from the array bases fit 32 bits
