@@ -739,7 +739,8 @@ def run_native(args, ws, rank, local):
                 "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": nbytes}
     roof.update({"kernel": dominant, "launches": dom_n, "avg_launch_ms": avg_ms,
                  "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json' if peak_kind == 'measured' else '6.8 TB/s, 1.9 PFLOP/s'})",
-                 "traffic": traffic_for(dominant, w.name)})
+                 # (block-sparse plans keep their own entries: their CSR passes see the residual)
+                 "traffic": traffic_for(dominant, w.name + (f"_tiles{wl.tile_min_nnz}" if wl.tile_min_nnz else ""))})
 
     # block-sparse forward: tensor-core rate of the tile kernel (MMA work
     # issued, masked slots included) over one step
