@@ -129,9 +129,10 @@ size_t sga_plan_workspace_bytes(const sga_plan *plan);
 /* Attach caller-owned device workspace (256-byte aligned, at least
  * sga_plan_workspace_bytes()).  Calls that use the same plan must not overlap
  * on the device: they share this workspace and the plan's own per-launch
- * state (the counter from which the edge kernels take their work items and
- * the arrival counts of split rows merged inside the kernels, both back at
- * zero when a launch ends).  Different plans may run concurrently. */
+ * state (the counter from which the edge kernels take their work items,
+ * zeroed on the stream before each launch, and the arrival counts of split
+ * rows merged inside the kernels, back at zero when a launch ends).
+ * Different plans may run concurrently. */
 sga_status sga_plan_set_workspace(sga_plan *plan, void *d_workspace, size_t bytes);
 
 void sga_plan_destroy(sga_plan *plan);
