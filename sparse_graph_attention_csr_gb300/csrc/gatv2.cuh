@@ -50,7 +50,9 @@ __device__ __forceinline__ void store_dF(float *ws, int64_t row, int HD, int c, 
 // --------------------------------------------------------------- edge fwd
 
 // gathered FR; own FL
-template <typename T, int D, int NC, int G> using Gatv2FwdStream = RingCfg<NC, G, 1, 0, 1, 0>;
+// (items taken dynamically in batches of four; the source pass keeps the
+// fixed share, which measured faster there)
+template <typename T, int D, int NC, int G> using Gatv2FwdStream = RingCfg<NC, G, 1, 0, 1, 0, 1, 2, 0, true, false, 4>;
 // gathered FR; own FL, dOut, lse
 // (a fixed share of items: each block's da partial must sum the same rows in
 // every launch for da to be reproducible)

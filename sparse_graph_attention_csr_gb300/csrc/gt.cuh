@@ -80,7 +80,7 @@ struct RingDims {
     static constexpr int DEPTH = FIT < 2 ? 2 : (FIT > 8 ? 8 : FIT);
 };
 template <int NC, int G, int NROW, int NSC, int NOWN, int NOSC, int U2 = 1, int U1 = 2, int ESC = 0,
-          bool LIST = true, bool W32 = false, bool DYN = false>
+          bool LIST = true, bool W32 = false, int DYN = 0>
 using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::U, NROW, NSC, NOWN, NOSC,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST, W32, DYN>;

@@ -61,7 +61,7 @@ __device__ __forceinline__ void cp_wait_newer(int n) {
 }
 
 template <int NC_, int G_, int U_, int NROW_, int NSC_, int NOWN_, int NOSC_, int DEPTH_, int QD_,
-          int ESC_ = 0, bool LIST_ = true, bool W32_ = false, bool DYN_ = false>
+          int ESC_ = 0, bool LIST_ = true, bool W32_ = false, int DYN_ = 0>
 struct StreamCfg {
     // W32: the row copies take 32-bit byte offsets from the array bases when
     // every gathered row array is below 4 GB (checked at run time; 64-bit
@@ -72,7 +72,10 @@ struct StreamCfg {
     // before each launch) in list order, instead of the fixed share w, w + S,
     // ...: the descending-degree list is then consumed largest first by
     // whichever warp is free, so no warp is left with the last long items.
-    static constexpr bool DYN = DYN_;
+    // DYN_ > 1 takes the items in batches of DYN_ consecutive ones (one atomic
+    // per batch: short rows would otherwise queue on the counter).
+    static constexpr bool DYN = DYN_ > 0;
+    static constexpr int BATCH = DYN_ > 1 ? DYN_ : 1;
     // walk the plan's item list (else: chunks, then all rows by id)
     static constexpr bool LIST = LIST_;
     static_assert(NSC_ <= 3, "at most three gathered scalar arrays");
@@ -142,6 +145,7 @@ template <typename C> struct EdgeStream {
     // next item to consider, and (DYN) the one after it (else nx_item + stride);
     // 32-bit under DYN, whose items come from a 32-bit counter
     std::conditional_t<C::DYN, uint32_t, int64_t> nx_item, nx2;
+    uint32_t b_next, b_left;  // DYN batches: next item of the warp's batch, items left in it
     ItemMeta m1, m2;         // descriptors of nx_item and the item after it
     int32_t ids1;            // first id batch of nx_item (when valid)
     bool v1;                 // nx_item is a valid item (its ids1 were issued)
@@ -178,6 +182,7 @@ template <typename C> struct EdgeStream {
         stride = (int64_t)gridDim.x * (blockDim.x >> 5);
         n_items = C::LIST ? P.n_items : (int64_t)P.n_chunks + N;
         if constexpr (C::DYN) {
+            b_next = b_left = 0;
             nx_item = fetch_item();
             nx2 = fetch_item();
             meta_issue<C::LIST>(nx_item, P, ptr, N, m1);
@@ -199,11 +204,23 @@ template <typename C> struct EdgeStream {
 
     // ---- producer ----------------------------------------------------------
 
-    // The next item of the launch's list (DYN): one atomic of lane 0.
+    // The next item of the launch's list (DYN): one atomic of lane 0 per item
+    // or per batch of C::BATCH items.
     __device__ __forceinline__ uint32_t fetch_item() {
-        uint32_t v = 0;
-        if (lane == 0) v = atomicAdd(reinterpret_cast<unsigned int *>(P.next), 1u);
-        return __shfl_sync(SGA_FULL_MASK, v, 0);
+        if constexpr (C::BATCH == 1) {
+            uint32_t v = 0;
+            if (lane == 0) v = atomicAdd(reinterpret_cast<unsigned int *>(P.next), 1u);
+            return __shfl_sync(SGA_FULL_MASK, v, 0);
+        } else {
+            if (b_left == 0) {
+                uint32_t v = 0;
+                if (lane == 0) v = atomicAdd(reinterpret_cast<unsigned int *>(P.next), (unsigned int)C::BATCH);
+                b_next = __shfl_sync(SGA_FULL_MASK, v, 0);
+                b_left = C::BATCH;
+            }
+            --b_left;
+            return b_next++;
+        }
     }
 
     // Queue the next item to be processed here; false when there is none.
