@@ -412,11 +412,15 @@ typedef enum {
     SGA_KERN_GAT_FWD = 23, SGA_KERN_GAT_BWD_DST = 24, SGA_KERN_GAT_BWD_SRC = 25,
     SGA_KERN_COUNT = 26
 } sga_kernel_id;
-/* (Planned Graph Transformer and GATv2 passes merge their split rows inside
- * the edge kernels -- the last chunk of a row to finish merges it -- so
- * SGA_KERN_GT_BWD_MERGE, SGA_KERN_GATV2_FWD_MERGE and SGA_KERN_GATV2_BWD_MERGE
- * are no longer launched, and SGA_KERN_GT_FWD_MERGE only by
- * gt_attn_fwd_noalloc.) */
+/* (Planned GATv2 passes merge their split rows inside the edge kernels --
+ * the last chunk of a row to finish merges it -- so SGA_KERN_GATV2_FWD_MERGE
+ * and SGA_KERN_GATV2_BWD_MERGE are no longer launched.  Graph Transformer
+ * passes merge inside the edge kernels when a lane holds two or more 16-byte
+ * chunks of a row (H*D above 256 bf16 or 128 fp32 elements) and the rows come
+ * from the plan's item lists; otherwise (one chunk per lane, a forward with
+ * rows walked in id order, the other edge schedules, gt_attn_fwd_noalloc)
+ * split rows are merged by SGA_KERN_GT_FWD_MERGE and SGA_KERN_GT_BWD_MERGE
+ * launches.) */
 
 /* Time one kernel kind with CUDA events recorded on the launching stream
  * around each of its launches (at most 4096 launches per window).
