@@ -85,10 +85,9 @@ using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>:
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST, W32, DYN>;
 
-// Dynamic items of the GT forward and dK/dV passes: batches of four on
-// one-chunk rows (R-MAT forward 3.55 -> 3.44 ms, dK/dV 4.98 -> 4.88); single
-// items on wider rows, where batches lost (SBM forward 2.28 -> 2.84 ms); the
-// dQ pass takes single items (batch state spilled it).
+// Dynamic items of the GT passes: batches of four on one-chunk rows (R-MAT
+// forward 3.55 -> 3.44 ms, dQ 4.25 -> 4.19, dK/dV 4.98 -> 4.88); single items
+// on wider rows, where batches lost (SBM forward 2.28 -> 2.84 ms).
 template <int NC> constexpr int gt_batch() { return NC == 1 ? 4 : 1; }
 
 // gathered K, V (and the edge's score bias); own Q.  LIST = false: no item
@@ -97,7 +96,7 @@ template <typename T, int D, int NC, int G, bool BIAS = false, bool LIST = true>
 using GtFwdStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 1, 0, 2, 4, BIAS ? 1 : 0, LIST, true, LIST ? gt_batch<NC>() : 0>;
 // gathered K, V (and the edge's score bias); own Q, dOut, lse
 template <typename T, int D, int NC, int G, bool BIAS = false>
-using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0, true, true, true>;
+using GtDqStream = RingCfg<NC, G, 2, BIAS ? 1 : 0, 2, 1, 2, 4, BIAS ? 1 : 0, true, true, gt_batch<NC>()>;
 // gathered Q, dOut, lse, Delta (over the transposed CSR; and the edge's score
 // bias in transposed order); own K, V
 template <typename T, int D, int NC, int G, bool BIAS = false>
