@@ -85,10 +85,11 @@ using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>:
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST, W32, DYN>;
 
-// Dynamic items of the GT passes: batches of four on one-chunk rows (R-MAT
-// forward 3.55 -> 3.44 ms, dQ 4.25 -> 4.19, dK/dV 4.98 -> 4.88); single items
-// on wider rows, where batches lost (SBM forward 2.28 -> 2.84 ms).
-template <int NC> constexpr int gt_batch() { return NC == 1 ? 4 : 1; }
+// Dynamic items of the GT passes: batches of eight on one-chunk rows (R-MAT
+// step 12.84 -> 12.50 ms against single items, 12.56 with batches of four);
+// single items on wider rows, where batches lost (SBM forward 2.28 -> 2.84 ms
+// with batches of four).
+template <int NC> constexpr int gt_batch() { return NC == 1 ? 8 : 1; }
 
 // gathered K, V (and the edge's score bias); own Q.  LIST = false: no item
 // list (the no-allocation forward, which has no plan)
