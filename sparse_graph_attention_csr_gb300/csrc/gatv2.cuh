@@ -50,9 +50,12 @@ __device__ __forceinline__ void store_dF(float *ws, int64_t row, int HD, int c, 
 // --------------------------------------------------------------- edge fwd
 
 // gathered FR; own FL
-// (items taken dynamically in batches of four; the source pass keeps the
+// (items taken dynamically in the plan's batches, at most eight: workload of
+// 1.7M edges, batches of four, 0.779 -> 0.773 ms a step; a fixed batch of
+// eight gave the warps that took the first chunks more than their share of
+// the edges, 0.157 -> 0.225 ms for this pass; the source pass keeps the
 // fixed share, which measured faster there)
-template <typename T, int D, int NC, int G> using Gatv2FwdStream = RingCfg<NC, G, 1, 0, 1, 0, 1, 2, 0, true, false, 4>;
+template <typename T, int D, int NC, int G> using Gatv2FwdStream = RingCfg<NC, G, 1, 0, 1, 0, 1, 2, 0, true, false, 8>;
 // gathered FR; own FL, dOut, lse
 // (a fixed share of items: each block's da partial must sum the same rows in
 // every launch for da to be reproducible)

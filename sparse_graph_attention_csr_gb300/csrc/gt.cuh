@@ -85,10 +85,10 @@ using RingCfg = StreamCfg<NC, G, RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>:
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::DEPTH,
                           RingDims<NC, NROW, NSC, NOWN, NOSC, G, U2, U1>::QD, ESC, LIST, W32, DYN>;
 
-// Dynamic items of the GT passes: batches of eight on one-chunk rows (R-MAT
-// step 12.84 -> 12.50 ms against single items, 12.56 with batches of four);
-// single items on wider rows, where batches lost (SBM forward 2.28 -> 2.84 ms
-// with batches of four).
+// Dynamic items of the GT passes: the plan's batch, at most eight, on
+// one-chunk rows (R-MAT step 12.84 -> 12.47 ms against single items); single
+// items on wider rows, where batches lost (SBM forward 2.28 -> 2.84 ms with
+// batches of four).
 template <int NC> constexpr int gt_batch() { return NC == 1 ? 8 : 1; }
 
 // gathered K, V (and the edge's score bias); own Q.  LIST = false: no item

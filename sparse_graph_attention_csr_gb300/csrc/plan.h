@@ -22,6 +22,11 @@ struct Partition {
     int32_t *chunk_end = nullptr;   // [n_chunks] one past the last edge
     int32_t *chunk_split = nullptr; // [n_chunks] index of the chunk's split row
     int32_t *next = nullptr;        // [1] next item of a launch that takes its items dynamically
+    // Items a warp claims with one atomic on `next` in passes that take them
+    // in batches: the largest power of two whose chunks (the longest items,
+    // at the head of the list) stay within a resident warp's average share of
+    // the edges, so no warp starts with more than its share.
+    int32_t batch = 1;
     // [n_split] chunks of each split row finished in the current launch of an
     // edge kernel that merges split rows itself (the last chunk to finish
     // merges the row and sets the count back to 0); zero between launches

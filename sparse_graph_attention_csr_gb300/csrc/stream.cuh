@@ -72,8 +72,9 @@ struct StreamCfg {
     // before each launch) in list order, instead of the fixed share w, w + S,
     // ...: the descending-degree list is then consumed largest first by
     // whichever warp is free, so no warp is left with the last long items.
-    // DYN_ > 1 takes the items in batches of DYN_ consecutive ones (one atomic
-    // per batch: short rows would otherwise queue on the counter).
+    // DYN_ > 1 takes the items in batches of consecutive ones, the plan's
+    // batch (Partition::batch) capped at DYN_: one atomic per batch, as short
+    // rows would otherwise queue on the counter.
     static constexpr bool DYN = DYN_ > 0;
     static constexpr int BATCH = DYN_ > 1 ? DYN_ : 1;
     // walk the plan's item list (else: chunks, then all rows by id)
@@ -205,7 +206,7 @@ template <typename C> struct EdgeStream {
     // ---- producer ----------------------------------------------------------
 
     // The next item of the launch's list (DYN): one atomic of lane 0 per item
-    // or per batch of C::BATCH items.
+    // or per batch of items.
     __device__ __forceinline__ uint32_t fetch_item() {
         if constexpr (C::BATCH == 1) {
             uint32_t v = 0;
@@ -213,10 +214,11 @@ template <typename C> struct EdgeStream {
             return __shfl_sync(SGA_FULL_MASK, v, 0);
         } else {
             if (b_left == 0) {
+                const uint32_t n = min((uint32_t)P.batch, (uint32_t)C::BATCH);
                 uint32_t v = 0;
-                if (lane == 0) v = atomicAdd(reinterpret_cast<unsigned int *>(P.next), (unsigned int)C::BATCH);
+                if (lane == 0) v = atomicAdd(reinterpret_cast<unsigned int *>(P.next), n);
                 b_next = __shfl_sync(SGA_FULL_MASK, v, 0);
-                b_left = C::BATCH;
+                b_left = n;
             }
             --b_left;
             return b_next++;
