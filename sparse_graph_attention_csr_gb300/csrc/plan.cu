@@ -479,7 +479,7 @@ sga_status plan_build(sga_plan *p, cudaStream_t s) {
         P.n_items = (int64_t)P.n_chunks + (N - P.n_split);
         const int64_t per_warp = E / (16 * (int64_t)std::max(1, p->num_sms));   // 16 resident warps per SM
         P.batch = 1;
-        while (P.batch < 64 && (int64_t)P.batch * 2 * std::max(1, p->chunk_len) <= per_warp) P.batch *= 2;
+        while (P.batch < 64 && (int64_t)P.batch * 2 * std::max(1, p->chunk_len) * 4 <= per_warp * 3) P.batch *= 2;
         P.items = own.get<int4>(P.n_items);
         if (p->row_order == 1) P.order = own.get<int32_t>(N);
         SGA_TRY(own.err);

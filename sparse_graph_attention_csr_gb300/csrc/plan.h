@@ -24,8 +24,9 @@ struct Partition {
     int32_t *next = nullptr;        // [1] next item of a launch that takes its items dynamically
     // Items a warp claims with one atomic on `next` in passes that take them
     // in batches: the largest power of two whose chunks (the longest items,
-    // at the head of the list) stay within a resident warp's average share of
-    // the edges, so no warp starts with more than its share.
+    // at the head of the list) stay within three quarters of a resident
+    // warp's average share of the edges, so no warp starts with more than
+    // its share.
     int32_t batch = 1;
     // [n_split] chunks of each split row finished in the current launch of an
     // edge kernel that merges split rows itself (the last chunk to finish
