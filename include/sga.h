@@ -321,12 +321,12 @@ sga_status sga_read_device_error(const sga_plan *plan, void *stream, int32_t *co
  *
  * Behaviour: the call synchronises `stream` once (it copies the split count
  * back to the host to size the launches), then launches the edge kernels
- * asynchronously on it.  Because of that synchronisation it cannot be called
- * while `stream` is being captured into a CUDA graph.  The first call on a
- * device looks up the array's device address for that device (with that
- * device current).  Every call shares the one array and finds the previous
- * call's data in it: calls that can overlap on the GPU (other streams, other
- * host threads) race and must be serialised by the caller.  Allocates
+ * asynchronously on it.  The first call on a device looks up the array's
+ * device address for that device (with that device current); make that
+ * first call before any stream capture.  Every call shares the one array and
+ * finds the previous call's data in it: calls that can overlap on the GPU
+ * (other streams, other host threads) race and must be serialised by the
+ * caller.  Allocates
  * nothing: no cudaMalloc, cudaFree or allocating library routine.
  *
  * Range checks: the CSR is validated before the edge kernels run, so their

@@ -368,7 +368,8 @@ def gt_attn_fwd_noalloc(indptr, indices, Q, K, V, out=None, lse=None, stream=Non
     must not allocate device memory (the library uses a fixed static device
     array instead; see include/sga.h).  Passing ``out`` and ``lse`` keeps this
     call free of allocations on the Python side too.  Synchronises the stream
-    once, so it cannot run inside a CUDA graph capture.  Returns (out, lse).
+    once; the first call on a device looks up the static array's address, so
+    make it before any stream capture.  Returns (out, lse).
 
     Shapes are checked here before the library sees any pointer: N is taken
     from ``indptr`` (N + 1 entries), Q, K, V (and ``out``) must be [N, H, D] of
