@@ -17,6 +17,9 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
 def gt_setup(key):
+    """Forward and backward of a Graph Transformer workload at full size, with
+    the default plan (the one bench.py uses); also returns the plan's split
+    threshold, above which rows and sources take the split-and-merge path."""
     w = synth.WORKLOADS[key]
     indptr, indices = synth.make_graph(w)
     x = synth.gt_inputs(w)
@@ -29,11 +32,11 @@ def gt_setup(key):
     grads = sga.gt_attn_bwd(plan, d["Q"], d["K"], d["V"], out, lse, d["dOut"])
     torch.cuda.synchronize()
     assert plan.device_error() == 0
-    return w, indptr, indices, x, out, lse, grads
+    return w, indptr, indices, x, out, lse, grads, plan.info()["split_threshold"]
 
 
 def test_workload1_gt_forward_fp32_full():
-    w, indptr, indices, x, out, lse, _ = gt_setup(1)
+    w, indptr, indices, x, out, lse, _, _ = gt_setup(1)
     ro, rl = oracle.gt_fwd(indptr, indices, x["Q"][1], x["K"][1], x["V"][1])
     compare(out, ro, "f32", "out")
     compare(lse, rl, "f32", "lse")
@@ -72,7 +75,7 @@ def test_workload2_gatv2_full():
 
 
 def test_workload3_gt_full():
-    w, indptr, indices, x, out, lse, (dQ, dK, dV) = gt_setup(3)
+    w, indptr, indices, x, out, lse, (dQ, dK, dV), _ = gt_setup(3)
     h = {k: v[1] for k, v in x.items()}
     ro, rl = oracle.gt_fwd(indptr, indices, h["Q"], h["K"], h["V"])
     compare(out, ro, "bf16", "out")
@@ -85,14 +88,26 @@ def test_workload3_gt_full():
 
 @pytest.mark.parametrize("key", [4, 5])
 def test_large_workloads_sampled(key):
-    w, indptr, indices, x, out, lse, (dQ, dK, dV) = gt_setup(key)
+    """Sampled rows: 1500 random, the 20 of highest degree and up to 400 more
+    split rows drawn at random (R-MAT has about 1,350 rows above its split
+    threshold, up to 64k edges each).  Sampled sources: 300 random, the 8 of
+    highest degree and up to 12 more split sources; the oracle recomputes
+    the softmax of every destination row of a source, which bounds how many
+    hub sources it can afford."""
+    w, indptr, indices, x, out, lse, (dQ, dK, dV), thr = gt_setup(key)
     h = {k: v[1] for k, v in x.items()}
     rng = np.random.default_rng(key)
     deg = np.diff(indptr.astype(np.int64))
     t_indptr, t_dst = oracle.transpose(indptr, indices)
     tdeg = np.diff(t_indptr.astype(np.int64))
-    rows = np.unique(np.concatenate([rng.integers(0, w.N, 1500), np.argsort(deg)[-8:]]))
-    srcs = np.unique(np.concatenate([rng.integers(0, w.N, 300), np.argsort(tdeg)[-4:]]))
+    split, tsplit = np.flatnonzero(deg > thr), np.flatnonzero(tdeg > thr)
+    rows = np.unique(np.concatenate([rng.integers(0, w.N, 1500), np.argsort(deg)[-20:],
+                                     rng.permutation(split)[:400]]))
+    srcs = np.unique(np.concatenate([rng.integers(0, w.N, 300), np.argsort(tdeg)[-8:],
+                                     rng.permutation(tsplit)[:12]]))
+    if key == 4:
+        # the super-node path is what this workload is for
+        assert np.isin(split, rows).sum() >= min(400, split.size) and split.size > 100
     ro, rl = oracle.gt_fwd(indptr, indices, h["Q"], h["K"], h["V"], rows=rows)
     r = torch.from_numpy(rows).cuda()
     compare(out[r], ro, "bf16", "out")
