@@ -81,8 +81,14 @@ def parse_args(argv=None):
     p.add_argument("--nodes", type=int, default=0,
                    help="profiling case: the workload's recipe at this many nodes "
                         "(SBM, ER and Chung-Lu graphs; draws scale with N)")
+    p.add_argument("--e2e-lanes", type=int, default=1,
+                   help="streams per copy direction in the end-to-end run (each tensor cut into "
+                        "this many row slices, one per stream)")
     p.add_argument("--json-out", default="")
-    return p.parse_args(argv)
+    a = p.parse_args(argv)
+    if a.e2e_lanes < 1:
+        p.error("--e2e-lanes must be at least 1")
+    return a
 
 
 # ------------------------------------------------------------------ distributed
@@ -442,47 +448,74 @@ class Workload:
                 host_out[k].copy_(v, non_blocking=True)
         main.wait_event(ev_out)
 
-    def e2e_pipelined(self, steps, host_out, flush):
+    def e2e_pipelined(self, steps, host_out, flush, lanes=1):
         """`steps` steps from pinned host inputs to pinned host outputs, the way a
-        training loop overlaps its data movement: step k+1's inputs go up on an
-        upload stream while step k computes (two device input buffers), step k's
-        outputs come down on a download stream while step k+1 computes.  Every
-        step's inputs are copied up and all its outputs copied down inside the
-        timed region, which runs from before the first upload to after the last
-        download.  Returns milliseconds for all steps."""
+        training loop overlaps its data movement: step k+1's inputs go up while
+        step k computes (two device input buffers), step k's outputs come down
+        while step k+1 computes.  Every step's inputs are copied up and all its
+        outputs copied down inside the timed region, which runs from before the
+        first upload to after the last download.  Each direction uses `lanes`
+        streams: every tensor is cut into `lanes` row slices, slice i copied on
+        stream i, so that copies can run on several copy engines at once.
+        Returns milliseconds for all steps."""
         main = torch.cuda.current_stream()
-        up, down = torch.cuda.Stream(self.device), torch.cuda.Stream(self.device)
+        ups = [torch.cuda.Stream(self.device) for _ in range(lanes)]
+        downs = [torch.cuda.Stream(self.device) for _ in range(lanes)]
         bufs = [{k: torch.empty_like(v) for k, v in self.dev.items()} for _ in range(2)]
         uploaded, consumed = [None, None], [None, None]
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
 
+        def slices(t):
+            n = t.shape[0] if t.dim() else 1
+            cut = [n * i // lanes for i in range(lanes + 1)]
+            return [(cut[i], cut[i + 1]) for i in range(lanes)]
+
         def upload(b):
-            with torch.cuda.stream(up):
-                if consumed[b] is not None:
-                    up.wait_event(consumed[b])   # the step that read this buffer is done
-                for k in self.in_names:
-                    bufs[b][k].copy_(self.host[k], non_blocking=True)
-                uploaded[b] = up.record_event()
+            done = []
+            for i, st in enumerate(ups):
+                with torch.cuda.stream(st):
+                    if consumed[b] is not None:
+                        st.wait_event(consumed[b])   # the step that read this buffer is done
+                    for k in self.in_names:
+                        dst, src = bufs[b][k], self.host[k]
+                        if dst.dim() == 0:
+                            if i == 0:
+                                dst.copy_(src, non_blocking=True)
+                            continue
+                        lo, hi = slices(dst)[i]
+                        if hi > lo:
+                            dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+                    done.append(st.record_event())
+            uploaded[b] = done
 
         e0.record(main)
-        up.wait_event(e0)
+        for st in ups:
+            st.wait_event(e0)
         upload(0)
         for k in range(steps):
             b = k % 2
             if k + 1 < steps:
                 upload(1 - b)
-            main.wait_event(uploaded[b])
+            for ev in uploaded[b]:
+                main.wait_event(ev)
             flush.zero_()   # L2 flushed before each step's compute, inside the region
             outs = self.step(bufs[b])
             consumed[b] = main.record_event()
-            with torch.cuda.stream(down):
-                down.wait_event(consumed[b])
-                for name, v in outs.items():
-                    host_out[name].copy_(v, non_blocking=True)
-                    v.record_stream(down)   # the allocator keeps v until the copy is done
-        main.wait_stream(down)
-        main.wait_stream(up)
+            for i, st in enumerate(downs):
+                with torch.cuda.stream(st):
+                    st.wait_event(consumed[b])
+                    for name, v in outs.items():
+                        if v.dim() == 0:
+                            if i == 0:
+                                host_out[name].copy_(v, non_blocking=True)
+                        else:
+                            lo, hi = slices(v)[i]
+                            if hi > lo:
+                                host_out[name][lo:hi].copy_(v[lo:hi], non_blocking=True)
+                        v.record_stream(st)   # the allocator keeps v until the copy is done
+        for st in downs + ups:
+            main.wait_stream(st)
         e1.record(main)
         e1.synchronize()
         return e0.elapsed_time(e1)
@@ -783,15 +816,16 @@ def run_native(args, ws, rank, local):
             e_ser += e0.elapsed_time(e1)
         e_ser = max_over_ranks(e_ser, ws, dev)
         # K steps as a loader pipelines them (the reported number)
-        wl.e2e_pipelined(2, host_out, flush)
+        wl.e2e_pipelined(2, host_out, flush, args.e2e_lanes)
         torch.cuda.synchronize()
         barrier(ws)
-        e_ms = max_over_ranks(wl.e2e_pipelined(args.steps, host_out, flush), ws, dev)
+        e_ms = max_over_ranks(wl.e2e_pipelined(args.steps, host_out, flush, args.e2e_lanes), ws, dev)
         e2e = {"value": ws * wl.units * args.steps / (e_ms / 1e3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.steps,
                "overlap": "step k+1's inputs copied up and step k's outputs copied down while step k+1 "
                           "computes (two device input buffers); every step's copies inside the timed region",
+               "copy_lanes": args.e2e_lanes,
                "serial_ms_per_step": e_ser / args.steps}
 
     cpu = None
