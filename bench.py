@@ -281,6 +281,16 @@ def source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def dram_rate(traffic, avg_ms: float, hbm_gbs: float) -> dict:
+    """DRAM rate of a launch: its measured DRAM bytes (ncu, per launch) over its
+    event-timed duration, and that rate as a fraction of the HBM peak.  Empty
+    when no traffic figure is known for the current sources."""
+    if not traffic or not avg_ms or avg_ms <= 0:
+        return {}
+    gbs = traffic / (avg_ms / 1e3) / 1e9
+    return {"dram_gbs": gbs, "dram_frac": gbs / hbm_gbs}
+
+
 def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, only if it was
     taken on the current sources of the kernel's family."""
@@ -774,6 +784,9 @@ def run_native(args, ws, rank, local):
                  "peak_source": f"{peak_kind} ({'MEASURED_PEAKS.json' if peak_kind == 'measured' else '6.8 TB/s, 1.9 PFLOP/s'})",
                  # (block-sparse plans keep their own entries: their CSR passes see the residual)
                  "traffic": traffic_for(dominant, w.name + (f"_tiles{wl.tile_min_nnz}" if wl.tile_min_nnz else ""))})
+    # what DRAM itself delivered during the launch (algorithmic bytes count
+    # every gathered row, also those served from L2)
+    roof.update(dram_rate(roof["traffic"], avg_ms, peaks["hbm_gbs"]))
 
     # block-sparse forward: tensor-core rate of the tile kernel (MMA work
     # issued, masked slots included) over one step
