@@ -273,20 +273,28 @@ typedef enum {
 
 /* perm[N] (device, int32) receives the new id of every node.  Exact and
  * deterministic (bit-identical to the sequential definition).  Allocates its
- * temporary device memory, frees it before returning, synchronises `stream`. */
+ * temporary device memory, frees it before returning, synchronises `stream`.
+ * The CSR is checked on the device first (indptr[0] = 0, non-decreasing,
+ * indptr[N] = E, sources in [0, N)): SGA_EINVAL if it is not valid. */
 sga_status sga_reorder(const int32_t *indptr, const int32_t *indices, int64_t N, int64_t E,
                        sga_order method, int32_t *perm, void *stream);
 
 /* The relabelled graph: new row perm[v] holds the sources of old row v as
  * perm[j], in their original order.  new_indptr[N+1], new_indices[E]: device,
- * caller-owned.  Synchronises `stream`. */
+ * caller-owned.  Synchronises `stream`.  The CSR (as for sga_reorder) and
+ * perm (a permutation of 0..N-1: every entry in range, none repeated) are
+ * checked on the device before anything is written: SGA_EINVAL otherwise. */
 sga_status sga_relabel_csr(const int32_t *indptr, const int32_t *indices, int64_t N, int64_t E,
                            const int32_t *perm, int32_t *new_indptr, int32_t *new_indices,
                            void *stream);
 
 /* Permute the rows of a node tensor (row_bytes a multiple of 16, buffers
  * 16-byte aligned and distinct): dst[perm[v]] = src[v], or with inverse = 1
- * dst[v] = src[perm[v]].  Asynchronous on `stream`. */
+ * dst[v] = src[perm[v]].  Asynchronous on `stream`.  perm should be a
+ * permutation of 0..N-1 (sga_reorder's output is one); it is not checked
+ * here, but a row whose perm entry lies outside [0, N) is skipped (nothing
+ * is read or written for it), and a repeated entry leaves the rows it
+ * targets to whichever copy lands last. */
 sga_status sga_permute_rows(const void *src, int64_t N, int64_t row_bytes, const int32_t *perm,
                             int inverse, void *dst, void *stream);
 

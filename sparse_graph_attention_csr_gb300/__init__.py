@@ -469,9 +469,12 @@ def gatv2_bwd(plan: Plan, X, W_l, W_r, a, FL, FR, out, lse, dOut, slope: float =
 
 def reorder(indptr, indices, method: str = "rcm", stream=None):
     """perm [N] int32 on the device: the new id of every node under the
-    ordering ("rcm": reverse Cuthill-McKee, "degree": descending in-degree)."""
+    ordering ("rcm": reverse Cuthill-McKee, "degree": descending in-degree).
+    The library checks the CSR on the device (SgaError if it is not valid)."""
     _need(indptr, "indptr", torch.int32)
     _need(indices, "indices", torch.int32)
+    if indptr.numel() < 1 or indices.device != indptr.device:
+        raise ValueError("indptr needs N + 1 entries, on the device of indices")
     N = indptr.numel() - 1
     perm = torch.empty(max(N, 1), dtype=torch.int32, device=indptr.device)
     code = {"degree": SGA_ORDER_DEGREE, "rcm": SGA_ORDER_RCM}[method]
@@ -481,9 +484,12 @@ def reorder(indptr, indices, method: str = "rcm", stream=None):
 
 
 def relabel_csr(indptr, indices, perm, stream=None):
-    """(new_indptr, new_indices): row perm[v] = old row v, sources mapped."""
+    """(new_indptr, new_indices): row perm[v] = old row v, sources mapped.  The
+    library checks the CSR and that perm is a permutation (SgaError if not)."""
     for n, t in (("indptr", indptr), ("indices", indices), ("perm", perm)):
         _need(t, n, torch.int32)
+    if indptr.numel() < 1 or not (indices.device == perm.device == indptr.device):
+        raise ValueError("indptr needs N + 1 entries; indptr, indices and perm on one device")
     N = indptr.numel() - 1
     _need(perm, "perm", torch.int32, N)
     new_ptr = torch.empty_like(indptr)
@@ -495,12 +501,15 @@ def relabel_csr(indptr, indices, perm, stream=None):
 
 def permute_rows(x, perm, inverse: bool = False, out=None, stream=None):
     """Rows of a node tensor under perm: out[perm[v]] = x[v] (inverse:
-    out[v] = x[perm[v]])."""
+    out[v] = x[perm[v]]).  perm should be a permutation of 0..N-1; rows whose
+    entry lies outside [0, N) are skipped, not reported."""
     _need(x, "x")
     N = x.shape[0] if x.dim() else 0
     _need(perm, "perm", torch.int32, N)
     out = torch.empty_like(x) if out is None else out
     _need(out, "out", x.dtype, x.numel(), N)
+    if not (perm.device == out.device == x.device):
+        raise ValueError("x, perm and out must be on one device")
     row_bytes = x.numel() // max(N, 1) * x.element_size()
     _check(_lib().sga_permute_rows(_ptr(x), N, row_bytes, _ptr(perm), 1 if inverse else 0,
                                    _ptr(out), _stream(stream)), "sga_permute_rows")

@@ -261,6 +261,7 @@ __global__ void permute_rows_kernel(const uint4 *__restrict__ src, int64_t N, in
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t v = warp; v < N; v += nw) {
         const int64_t p = perm[v];
+        if ((uint64_t)p >= (uint64_t)N) continue;   // not a node id: the row is skipped
         const int64_t from = inverse ? p : v, to = inverse ? v : p;
         for (int64_t c = lane; c < chunks; c += 32) dst[to * chunks + c] = src[from * chunks + c];
     }
@@ -282,6 +283,66 @@ struct Scratch {
         for (void *p : ptrs) cudaFree(p);
     }
 };
+
+// Input checks of the entry points, run before any kernel indexes with the
+// inputs.  Bits: 1 indptr[0] != 0, 2 indptr decreasing somewhere, 4
+// indptr[N] != E, 8 a source id outside [0, N), 16 a perm entry outside
+// [0, N), 32 a perm entry taken twice.
+__global__ void check_csr_kernel(const int32_t *__restrict__ indptr, const int32_t *__restrict__ indices,
+                                 int64_t N, int64_t E, int32_t *bad) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int bits = 0;
+    if (t0 == 0) {
+        if (indptr[0] != 0) bits |= 1;
+        if ((int64_t)indptr[N] != E) bits |= 4;
+    }
+    for (int64_t i = t0; i < N; i += stride)
+        if (indptr[i] > indptr[i + 1]) bits |= 2;
+    for (int64_t e = t0; e < E; e += stride) {
+        const int32_t j = indices[e];
+        if (j < 0 || (int64_t)j >= N) bits |= 8;
+    }
+    if (bits) atomicOr(bad, bits);
+}
+
+__global__ void check_perm_kernel(const int32_t *__restrict__ perm, int64_t N, int32_t *seen, int32_t *bad) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int bits = 0;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < N; v += stride) {
+        const int32_t p = perm[v];
+        if (p < 0 || (int64_t)p >= N)
+            bits |= 16;
+        else if (atomicAdd(seen + p, 1) != 0)
+            bits |= 32;
+    }
+    if (bits) atomicOr(bad, bits);
+}
+
+// Checks the CSR (indptr non-null) and the permutation (perm non-null) on
+// `stream` and synchronises it; *bits receives the OR of the failed checks.
+cudaError_t check_inputs(const int32_t *indptr, const int32_t *indices, int64_t N, int64_t E,
+                         const int32_t *perm, cudaStream_t s, int32_t *bits) {
+    Scratch m;
+    int32_t *bad = m.get<int32_t>(1);
+    int32_t *seen = perm ? m.get<int32_t>(N) : nullptr;
+    if (m.err != cudaSuccess) return m.err;
+    cudaError_t e = cudaMemsetAsync(bad, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess && indptr) {
+        check_csr_kernel<<<grid_n(std::max(N, E), 256, 4096), 256, 0, s>>>(indptr, indices, N, E, bad);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess && perm && N > 0) {
+        e = cudaMemsetAsync(seen, 0, sizeof(int32_t) * (size_t)N, s);
+        if (e == cudaSuccess) {
+            check_perm_kernel<<<grid_n(N, 256, 4096), 256, 0, s>>>(perm, N, seen, bad);
+            e = cudaGetLastError();
+        }
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(bits, bad, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);   // (the scratch is freed on return)
+    return e;
+}
 
 int bits_for(int64_t maxval) {
     int b = 1;
@@ -445,6 +506,10 @@ extern "C" sga_status sga_reorder(const int32_t *indptr, const int32_t *indices,
     if (N < 0 || E < 0 || N >= INT32_MAX || E >= INT32_MAX / 2) return SGA_EINVAL;
     if (method != SGA_ORDER_DEGREE && method != SGA_ORDER_RCM) return SGA_EINVAL;
     if (N == 0) return SGA_OK;
+    int32_t bits = 0;
+    const cudaError_t e = check_inputs(indptr, indices, N, E, nullptr, static_cast<cudaStream_t>(stream), &bits);
+    if (e != cudaSuccess) return to_status(e);
+    if (bits) return SGA_EINVAL;
     return to_status(reorder_impl(indptr, indices, N, E, method, perm, static_cast<cudaStream_t>(stream)));
 }
 
@@ -455,10 +520,14 @@ extern "C" sga_status sga_relabel_csr(const int32_t *indptr, const int32_t *indi
     if (E > 0 && (!indices || !new_indices)) return SGA_EINVAL;
     if (N < 0 || E < 0 || N >= INT32_MAX || E >= INT32_MAX) return SGA_EINVAL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t bits = 0;
+    cudaError_t e = check_inputs(indptr, indices, N, E, perm, s, &bits);
+    if (e != cudaSuccess) return to_status(e);
+    if (bits) return SGA_EINVAL;
     Scratch m;
     int32_t *tmp = m.get<int32_t>(scan_tmp_elems(N + 1));
     if (m.err != cudaSuccess) return to_status(m.err);
-    cudaError_t e = cudaMemsetAsync(new_indptr, 0, sizeof(int32_t) * (N + 1), s);
+    e = cudaMemsetAsync(new_indptr, 0, sizeof(int32_t) * (N + 1), s);
     if (e == cudaSuccess && N > 0) {
         relabel_degree_kernel<<<grid_n(N, 256), 256, 0, s>>>(indptr, perm, N, new_indptr);
         e = cudaGetLastError();

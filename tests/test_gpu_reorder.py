@@ -98,3 +98,55 @@ def test_attention_on_the_relabelled_graph(method, dtype):
     compare(Pi(dK), rk, dtype, "dK")
     compare(Pi(dV), rv, dtype, "dV")
     assert plan.device_error() == 0
+
+
+def test_invalid_graphs_and_permutations_are_rejected():
+    """The reordering calls check their inputs on the device before any kernel
+    indexes with them: an invalid CSR or a perm that is not a permutation
+    returns SGA_EINVAL, and the library stays usable afterwards."""
+    t = lambda x: dev(torch.tensor(x, dtype=torch.int32))
+    good_ptr, good_idx = t([0, 2, 3, 3]), t([1, 0, 2])
+    bad_graphs = [
+        (t([0, 2, 3, 3]), t([1, 0, 3])),    # source id N
+        (t([0, 2, 3, 3]), t([1, -1, 2])),   # negative source id
+        (t([0, 3, 2, 3]), t([1, 0, 2])),    # indptr decreasing
+        (t([1, 2, 3, 3]), t([1, 0, 2])),    # indptr[0] != 0
+    ]
+    for ip, ix in bad_graphs:
+        for method in ("rcm", "degree"):
+            with pytest.raises(sga.SgaError) as ei:
+                sga.reorder(ip, ix, method)
+            assert ei.value.status == sga.SGA_EINVAL
+        with pytest.raises(sga.SgaError) as ei:
+            sga.relabel_csr(ip, ix, t([2, 0, 1]))
+        assert ei.value.status == sga.SGA_EINVAL
+    for perm in ([0, 0, 1], [0, 1, 3], [-1, 0, 1]):
+        with pytest.raises(sga.SgaError) as ei:
+            sga.relabel_csr(good_ptr, good_idx, t(perm))
+        assert ei.value.status == sga.SGA_EINVAL
+    # valid inputs still work after the rejections
+    perm = sga.reorder(good_ptr, good_idx, "rcm")
+    np.testing.assert_array_equal(perm.cpu().numpy(),
+                                  oracle.order_rcm(np.array([0, 2, 3, 3], np.int32),
+                                                   np.array([1, 0, 2], np.int32)))
+    rp, ri = sga.relabel_csr(good_ptr, good_idx, perm)
+    ep, ei2 = oracle.relabel_csr(np.array([0, 2, 3, 3], np.int32), np.array([1, 0, 2], np.int32),
+                                 perm.cpu().numpy())
+    np.testing.assert_array_equal(rp.cpu().numpy(), ep)
+    np.testing.assert_array_equal(ri.cpu().numpy(), ei2)
+
+
+def test_permute_rows_skips_entries_outside_the_node_range():
+    x = dev(torch.arange(4 * 8, dtype=torch.float32).reshape(4, 8))
+    perm = dev(torch.tensor([2, 7, 0, -3], dtype=torch.int32))
+    out = dev(torch.full((4, 8), -1.0))
+    sga.permute_rows(x, perm, out=out)
+    torch.cuda.synchronize()
+    ref = torch.full((4, 8), -1.0)
+    ref[2], ref[0] = x[0].cpu(), x[2].cpu()
+    assert torch.equal(out.cpu(), ref)
+    out.fill_(-1.0)
+    sga.permute_rows(x, perm, inverse=True, out=out)
+    ref = torch.full((4, 8), -1.0)
+    ref[0], ref[2] = x[2].cpu(), x[0].cpu()
+    assert torch.equal(out.cpu(), ref)
