@@ -951,3 +951,17 @@ def test_gat_edge_stage_composes_to_the_layer():
     np.testing.assert_allclose(X.T @ dFL.reshape(N, -1), g["dW"], atol=1e-11)
     da = np.stack([np.einsum("nh,nhd->hd", de_l, FL), np.einsum("nh,nhd->hd", de_r, FL)], 1)
     np.testing.assert_allclose(da, g["da"], atol=1e-11)
+
+
+def test_projection_matmul_matches_numpy():
+    """The oracle's projection product (the X W step of the GATv2 layer) is a
+    plain triple loop; numpy's BLAS product computes the same sum."""
+    rng = np.random.default_rng(21)
+    for n, f, c in ((7, 5, 3), (1, 128, 128), (33, 8, 1)):
+        X, W = rng.standard_normal((n, f)), rng.standard_normal((f, c))
+        np.testing.assert_allclose(oracle.matmul(X, W), X @ W, rtol=1e-12, atol=1e-12)
+    # an identity W returns X; a zero row of X gives a zero row
+    X = rng.standard_normal((4, 6))
+    X[2] = 0.0
+    np.testing.assert_array_equal(oracle.matmul(X, np.eye(6)), X)
+    assert not oracle.matmul(X, rng.standard_normal((6, 3)))[2].any()
