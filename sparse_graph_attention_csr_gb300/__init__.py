@@ -217,8 +217,12 @@ class Plan:
                  tile_min_nnz: int = 0, layer: int = SGA_LAYER_ATTENTION,
                  schedule: int = SGA_SCHED_STREAM, edge_bias: bool = False,
                  row_order: int = 0, stream=None):
+        if dtype not in (torch.float32, torch.bfloat16):
+            raise TypeError(f"the layers compute in torch.float32 or torch.bfloat16, not {dtype}")
         _need(indptr, "indptr", torch.int32)
         _need(indices, "indices", torch.int32)
+        if indices.device != indptr.device:
+            raise ValueError(f"indices on {indices.device}, indptr on {indptr.device}")
         self.indptr, self.indices = indptr, indices
         self.N = indptr.numel() - 1
         self.E = indices.numel()
