@@ -619,6 +619,27 @@ class GTAttention(torch.autograd.Function):
         return dQ, dK, dV, None
 
 
+class GTBiasAttention(torch.autograd.Function):
+    """Graph Transformer edge attention with a per-edge, per-head score bias
+    (e.g. projected edge features), as an autograd function:
+    ``out = GTBiasAttention.apply(Q, K, V, bias, plan)`` with bias [E, H]
+    float32 in CSR edge order; the plan needs edge_bias=True."""
+
+    @staticmethod
+    def forward(ctx, Q, K, V, bias, plan):
+        Q, K, V, bias = Q.contiguous(), K.contiguous(), V.contiguous(), bias.contiguous()
+        out, lse = gt_attn_bias_fwd(plan, Q, K, V, bias)
+        ctx.plan = plan
+        ctx.save_for_backward(Q, K, V, bias, out, lse)
+        return out
+
+    @staticmethod
+    def backward(ctx, dOut):
+        Q, K, V, bias, out, lse = ctx.saved_tensors
+        dQ, dK, dV, dbias = gt_attn_bias_bwd(ctx.plan, Q, K, V, bias, out, lse, dOut.contiguous())
+        return dQ, dK, dV, dbias, None
+
+
 class MinMaxAggregation(torch.autograd.Function):
     """Min / max neighbourhood aggregation:
     ``out = MinMaxAggregation.apply(X, plan, "max")``."""

@@ -117,3 +117,42 @@ def test_gatv2_attention_autograd_routes_gradients(monkeypatch):
     torch.testing.assert_close(out, ref)
     for t, t2 in zip((X, Wl, Wr, a), ins2):
         torch.testing.assert_close(t.grad, t2.grad)
+
+
+def test_gt_bias_attention_autograd_routes_gradients(monkeypatch):
+    torch.manual_seed(2)
+    N, H, D = 5, 2, 4
+    indptr = [0, 2, 3, 5, 6, 7]
+    indices = [0, 1, 1, 2, 3, 4, 0]
+    E = len(indices)
+    rows = torch.repeat_interleave(torch.arange(N), torch.tensor(indptr).diff())
+    cols = torch.tensor(indices)
+
+    def layer(Q, K, V, B):
+        s = torch.full((H, N, N), float("-inf"), dtype=Q.dtype)
+        s[:, rows, cols] = (Q[rows] * K[cols]).sum(-1).T / D ** 0.5 + B.T
+        lse = torch.logsumexp(s, -1)
+        return torch.einsum("hij,jhd->ihd", torch.exp(s - lse[..., None]), V), lse.T.contiguous()
+
+    def fwd(plan, Q, K, V, B):
+        return layer(Q, K, V, B)
+
+    def bwd(plan, Q, K, V, B, out, lse, dOut):
+        with torch.enable_grad():
+            ins = [t.detach().clone().requires_grad_() for t in (Q, K, V, B)]
+            return torch.autograd.grad(layer(*ins)[0], ins, dOut)
+
+    monkeypatch.setattr(sga, "gt_attn_bias_fwd", fwd)
+    monkeypatch.setattr(sga, "gt_attn_bias_bwd", bwd)
+    Q, K, V = (torch.randn(N, H, D, dtype=torch.float64, requires_grad=True) for _ in range(3))
+    B = torch.randn(E, H, dtype=torch.float64, requires_grad=True)
+    dO = torch.randn(N, H, D, dtype=torch.float64)
+    out = sga.GTBiasAttention.apply(Q, K, V, B, _FakePlan())
+    out.backward(dO)
+    ins2 = [t.detach().clone().requires_grad_() for t in (Q, K, V, B)]
+    ref = layer(*ins2)[0]
+    ref.backward(dO)
+    torch.testing.assert_close(out, ref)
+    for t, t2 in zip((Q, K, V, B), ins2):
+        torch.testing.assert_close(t.grad, t2.grad)
+    assert B.grad.abs().sum() > 0
